@@ -1,0 +1,412 @@
+"""Benchmark of the speculative-decoding verify step on one GB300 (or N, one process each).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config 0..4] [--mode sampling|greedy] [--all]
+
+A step is one sampling-mode verify call (row statistics, first-reject scan, residual or bonus
+race: every step of the path) over one batch of the throughput-stress workload (B=256,
+gamma=12, V=152064 bf16; 1.95 GB of logits, larger than L2, so no flush is needed between
+steps).  Rank 0 prints one JSON line:
+
+  value        verified logit rows per second, B*(gamma+1) rows per call, inputs resident
+  e2e          the same through the C ABI with the step's inputs copied from pinned host
+               memory and the outputs read back inside the timed region
+  roofline     the row-statistics kernel (the dominant one): one read of every logit per
+               launch / its CUDA-event duration, against the measured HBM copy bandwidth
+  cpu_baseline the CPU oracle on a bounded sample of the same workload, on 1 host core
+
+``--impl reference`` times the CPU oracle as the reference arm (there is no reference code to
+install: the pages describe the method only).  Under torchrun with N > 1 every rank verifies
+its own batch (global sequence indices offset by rank) with no collective on the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "spec-verify logit rows/s (B*(gamma+1) rows of V) and achieved HBM GB/s vs peak"
+UNIT = "rows/s"
+
+# DRAM traffic of one row-statistics launch on the throughput workload, from the ncu capture
+# summarised in profiles/ (dram__bytes_read.sum + dram__bytes_write.sum), with the hash of
+# the kernel sources it was taken on; reported as null when the sources have changed since.
+NCU_TRAFFIC = {"bytes": None, "sources_sha1": None}
+KERNEL_SOURCES = ["kernels.cuh", "device_common.cuh", "philox.cuh", "specverify.cu"]
+
+
+def kernel_sources_sha1() -> str:
+    h = hashlib.sha1()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "speculative_decoding_verification_31_gb300", "csrc", f),
+                  "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+# -------------------------------------------------------------------------------------------
+# clocks during the timed region
+# -------------------------------------------------------------------------------------------
+
+CLOCK_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index: int, interval_ms: int = 50):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(gpu_index), "-lms", str(interval_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return []
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [l for l in out.splitlines() if l.strip()]
+        return self.lines
+
+    @staticmethod
+    def summarise(lines, t0: float, t1: float):
+        rows = []
+        for l in lines:
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[5:]))
+            except (ValueError, IndexError):
+                continue
+        if not rows:
+            return None
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
+        window = "timed region"
+        if len(inside) < 2:
+            inside = [r for r in rows if r[0] <= t1 + 0.05][-5:] or rows[-5:]
+            window = "nearest samples (timed region shorter than the sampling interval)"
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in inside:
+            for name, v in zip(names, r[3][1:5]):
+                if v.strip().lower() in ("active", "1", "yes"):
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median([r[1] for r in inside])),
+                "sm_max_mhz": float(max(r[2] for r in inside)),
+                "reasons": sorted(reasons), "samples": len(inside), "window": window}
+
+
+# -------------------------------------------------------------------------------------------
+# helpers
+# -------------------------------------------------------------------------------------------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def to_torch(a: np.ndarray, dtype: str):
+    import torch
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
+
+
+def cpu_oracle_rate(w, seed: int, budget_s: float, max_seqs: int):
+    """Time the CPU oracle on whole sequences of workload w until about budget_s seconds."""
+    import oracle
+    orc = oracle.get()
+    done, rows, t_total = 0, 0, 0.0
+    n = 1
+    while done < min(max_seqs, w.B) and t_total < budget_s:
+        k = min(n, w.B - done, max_seqs - done)
+        sl = slice(done, done + k)
+        t0 = time.perf_counter()
+        orc.verify(w.target[sl], w.draft[sl], w.tokens[sl], w.T[sl], w.Td[sl], seed,
+                   b_base=done)
+        t_total += time.perf_counter() - t0
+        done += k
+        rows += k * (w.gamma + 1)
+        per = t_total / done
+        n = max(1, int(min(budget_s - t_total, budget_s) / per)) if per > 0 else 1
+    return rows / t_total, done, t_total
+
+
+# -------------------------------------------------------------------------------------------
+# our arm
+# -------------------------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    import workloads
+    import speculative_decoding_verification_31_gb300 as sv
+
+    ws_, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws_ > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    sv.load_library()
+
+    cfg = args.config
+    w = workloads.config(cfg, greedy=(args.mode == "greedy"))
+    t = to_torch(w.target, w.dtype).to(dev)
+    d = to_torch(w.draft, w.dtype).to(dev)
+    tok = torch.from_numpy(w.tokens).to(dev)
+    Tq = torch.from_numpy(w.T).to(dev)
+    Tdq = torch.from_numpy(w.Td).to(dev)
+    per_seq = cfg == 3
+    out_t = torch.empty((w.B, w.gamma + 1), dtype=torch.int32, device=dev)
+    out_n = torch.empty((w.B,), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    seq_base = rank * w.B
+    greedy = args.mode == "greedy"
+    nkern = 2 if greedy else 3
+
+    def step(events=None, tgt=t, drf=d, tk=tok):
+        if greedy:
+            sv.spec_verify_greedy_ex(tgt, tk, out_t, out_n, prof_events=events)
+        else:
+            kw = dict(T_per_seq=Tq, Td_per_seq=Tdq) if per_seq else {}
+            sv.spec_verify_ex(tgt, drf, tk, float(w.T[0]), float(w.Td[0]), args.seed, out_t,
+                              out_n, seq_index_base=seq_base, prof_events=events, **kw)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    status = sv.spec_verify_check()
+    if status != sv.SPEC_OK:
+        raise RuntimeError(f"device status after warm-up: {sv.spec_verify_strerror(status)}")
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nkern + 1)] for _ in range(K)]
+    for e in evs:  # torch creates the CUDA event on first record: make the handles real
+        for ev in e:
+            ev.record(stream)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.15 if sampler else 0)
+    if ws_ > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    h0 = time.time()
+    start.record(stream)
+    for k in range(K):
+        step(evs[k])
+    end.record(stream)
+    torch.cuda.synchronize()
+    h1 = time.time()
+    if ws_ > 1:
+        torch.distributed.barrier()
+    clocks = None
+    if sampler:
+        clocks = ClockSampler.summarise(sampler.stop(), h0, h1)
+    ms = start.elapsed_time(end)
+    kern_ms = [float(np.mean([e[i].elapsed_time(e[i + 1]) for e in evs])) for i in range(nkern)]
+    if ws_ > 1:
+        mt = torch.tensor([ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(mt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(mt.item())
+    status = sv.spec_verify_check()
+    if status != sv.SPEC_OK:
+        raise RuntimeError(f"device status after timing: {sv.spec_verify_strerror(status)}")
+
+    ms_step = ms / K
+    rows_total = ws_ * w.rows * K
+    value = rows_total / (ms / 1e3)
+
+    # roofline of the dominant kernel (row statistics / row argmax)
+    alg_bytes = w.bytes_greedy() if greedy else w.bytes_sampling()
+    peaks = measured_peaks()
+    achieved = alg_bytes / (kern_ms[0] / 1e3) / 1e9
+    traffic = None
+    if NCU_TRAFFIC["bytes"] and NCU_TRAFFIC["sources_sha1"] == kernel_sources_sha1() and cfg == 4:
+        traffic = NCU_TRAFFIC["bytes"]
+
+    # end to end: inputs from pinned host memory, outputs read back, every step
+    e2e = None
+    if not args.no_e2e:
+        h_t = to_torch(w.target, w.dtype).pin_memory()
+        h_d = to_torch(w.draft, w.dtype).pin_memory()
+        h_tok = torch.from_numpy(w.tokens).pin_memory()
+        h_out_t = torch.empty((w.B, w.gamma + 1), dtype=torch.int32).pin_memory()
+        h_out_n = torch.empty((w.B,), dtype=torch.int32).pin_memory()
+        Ke = max(3, min(K, args.e2e_steps))
+
+        def e2e_step():
+            t.copy_(h_t, non_blocking=True)
+            if not greedy:
+                d.copy_(h_d, non_blocking=True)
+            tok.copy_(h_tok, non_blocking=True)
+            step()
+            h_out_t.copy_(out_t, non_blocking=True)
+            h_out_n.copy_(out_n, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        if ws_ > 1:
+            torch.distributed.barrier()
+        es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        es.record(stream)
+        for _ in range(Ke):
+            e2e_step()
+        ee.record(stream)
+        torch.cuda.synchronize()
+        ems = es.elapsed_time(ee)
+        if ws_ > 1:
+            mt = torch.tensor([ems], device=dev, dtype=torch.float64)
+            torch.distributed.all_reduce(mt, op=torch.distributed.ReduceOp.MAX)
+            ems = float(mt.item())
+        h2d = h_t.numel() * h_t.element_size() + h_tok.numel() * 4
+        if not greedy:
+            h2d += h_d.numel() * h_d.element_size()
+        e2e = {"value": ws_ * w.rows * Ke / (ems / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(h_out_t.numel() * 4 + h_out_n.numel() * 4),
+               "steps": Ke}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, nseq, secs = cpu_oracle_rate(w, args.seed, args.cpu_seconds, max_seqs=w.B)
+        cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{nseq} of {w.B} sequences of the same workload "
+                         f"({nseq * (w.gamma + 1)} rows, {secs:.1f} s, single-threaded C, fp64)"}
+
+    if ws_ > 1:
+        torch.distributed.destroy_process_group()
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded numpy generator; no dataset)",
+        "config": {"workload": workloads.CONFIG_NAMES[cfg], "B": w.B, "gamma": w.gamma,
+                   "V": w.V, "logits": w.dtype, "mode": args.mode,
+                   "rows_per_call": w.rows, "bytes_per_call": alg_bytes,
+                   "l2": "inputs larger than L2 (no flush)" if alg_bytes > 2 * 126e6
+                   else "inputs smaller than L2 (warm-L2 number)",
+                   "parallelism": f"replicas x{ws_} (batch per GPU fixed)"},
+        "achieved_GBps_step": alg_bytes / (ms_step / 1e3) / 1e9,
+        "kernel_ms": {n: v for n, v in zip(
+            ["row_argmax", "scan_greedy"] if greedy else ["row_stats", "scan", "race"], kern_ms)},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "kernel": "row_argmax" if greedy else "row_stats",
+                     "peak_source": f"{peaks['source']} HBM copy bandwidth (MEASURED_PEAKS.json)"},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": nkern * K,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# -------------------------------------------------------------------------------------------
+# reference arm: the CPU oracle
+# -------------------------------------------------------------------------------------------
+
+def run_reference(args):
+    import workloads
+    ws_, rank, local = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    cfg = args.config
+    w = workloads.config(cfg, greedy=(args.mode == "greedy"))
+    orc = oracle.get()
+    # one step = the oracle on a bounded sample of the workload's sequences
+    n_seq = max(1, min(w.B, args.ref_seqs))
+
+    def step(k):
+        lo = (k * n_seq) % w.B
+        sl = slice(lo, min(w.B, lo + n_seq))
+        if args.mode == "greedy":
+            orc.verify_greedy(w.target[sl], w.tokens[sl])
+        else:
+            orc.verify(w.target[sl], w.draft[sl], w.tokens[sl], w.T[sl], w.Td[sl], args.seed,
+                       b_base=lo)
+        return (sl.stop - sl.start) * (w.gamma + 1)
+
+    for k in range(args.warmup):
+        step(k)
+    rows = 0
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        rows += step(k)
+    secs = time.perf_counter() - t0
+    value = rows / secs
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "impl": "reference",
+        "data": "synthetic (seeded numpy generator; no dataset)",
+        "config": {"workload": workloads.CONFIG_NAMES[cfg], "B": w.B, "gamma": w.gamma,
+                   "V": w.V, "logits": w.dtype, "mode": args.mode, "rows_per_call": w.rows,
+                   "parallelism": "single host core"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{n_seq} sequences of {w.B} per step, single-threaded C"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=4, choices=range(5))
+    ap.add_argument("--mode", choices=["sampling", "greedy"], default="sampling")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seqs", type=int, default=1,
+                    help="sequences per reference step (one throughput-workload sequence is\n"
+                         "about 0.04 s of oracle work)")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

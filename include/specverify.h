@@ -1,0 +1,148 @@
+/*
+ * specverify.h -- C ABI of libspecverify, the speculative-decoding verify step on
+ * NVIDIA GB300 (sm_103a).
+ *
+ * One speculative cycle drafts gamma tokens d_0..d_{gamma-1} with a draft distribution q,
+ * runs the target once over gamma + 1 positions to get p, and then verifies: position i is
+ * accepted while a fresh uniform u_i < min(1, p_i(d_i) / q_i(d_i)); at the first rejection j
+ * one token is drawn from norm(max(0, p_j - q_j)) and the rest of the draft is dropped; if
+ * every draft token survives one bonus token is drawn from p_gamma.  Each cycle therefore
+ * emits between 1 and gamma + 1 tokens and the emitted tokens follow p exactly.
+ * ("How speculative decoding makes LLMs go brrr": the pseudocode of one speculative cycle,
+ * module 3 on rejection sampling and losslessness, module 4 on tau in [1, gamma + 1].)
+ * p is the softmax of the target logits at temperature T; q is the softmax of the draft
+ * logits at the draft temperature T_d, which may be sharper than T ("SubSpec: the target
+ * model's own low-bit shadow as the draft model", section 2.2 and section 3.4, Table 5).
+ * The greedy (T = 0) mode accepts a draft token when it equals the target's argmax
+ * (SubSpec's Tables 1-2 run at T = 0).
+ *
+ * Random numbers (both u_i and the draws) come from Philox4x32-10 (Salmon et al., SC'11)
+ * keyed by (lo32(seed), hi32(seed)); b below is the global sequence index
+ * (opts->seq_index_base + local index):
+ *   u_i          counter (0, i, b, 0), word 0 w:          u = (w >> 8) * 2^-24
+ *   draw at row r counter (x >> 2, r, b, 1), word (x & 3) w: E_x = -log1p(-(w + 0.5) * 2^-32)
+ * A draw from weights w(x) is the exponential race argmax_x w(x) / E_x (lowest x on equal
+ * scores), so no prefix sum over the vocabulary decides the token.  The same
+ * (inputs, seed, seq_index_base) always give the same tokens.
+ *
+ * Conventions for every entry point:
+ *   - Every pointer argument is device memory owned by the caller; the library never frees
+ *     it.  Logit base pointers must be 16-byte aligned; V need not be a multiple of 8.
+ *   - Layouts are row-major and contiguous: target [B, gamma+1, V], draft [B, gamma, V],
+ *     draft_tokens [B, gamma] int32, out_tokens [B, gamma+1] int32, out_n_accepted [B].
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy default stream)
+ *     and return once the work is enqueued.  The return value reports argument and launch
+ *     errors only; errors found on the device (a draft token outside [0, V)) are recorded in
+ *     a device status word read by spec_verify_check().
+ *   - B == 0 is an empty batch: nothing is launched and SPEC_OK is returned.
+ *   - gamma == 0 is plain sampling from row 0 (sampling) or its argmax (greedy).
+ *   - Output tokens are padded with -1 after the last emitted token.  out_n_accepted[b] is
+ *     the number j of accepted draft tokens (0..gamma); the cycle emitted j + 1 tokens.
+ *     A sequence holding a draft token outside [0, V) gets n_accepted = -1 and all -1
+ *     tokens, and the status word records SPEC_EBADTOKEN.
+ *   - The plain entry points use a workspace the library allocates per device on first use
+ *     (and grows when a larger problem arrives); calls that use it must not run
+ *     concurrently on one device.  The _ex entry points can take a caller workspace.
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+typedef enum {
+    SPEC_OK = 0,
+    SPEC_EINVAL = 1,     /* bad argument (size, NULL pointer, alignment, temperature) */
+    SPEC_ECUDA = 2,      /* a CUDA runtime call or launch failed */
+    SPEC_EBADTOKEN = 3,  /* (device) a draft token outside [0, V) */
+    SPEC_ETIMEOUT = 4,   /* (device) a bounded wait gave up */
+    SPEC_ENOMEM = 5      /* workspace allocation failed or caller workspace too small */
+} spec_status;
+
+/* Element type of the logits. */
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
+
+/* Options of the _ex entry points.  Zero-initialise (spec_verify_opts_init) and set what is
+ * needed; every pointer may be NULL. */
+typedef struct {
+    int32_t dtype;              /* spec_dtype of both logit tensors */
+    uint32_t seq_index_base;    /* global index of sequence 0 in the random-number counters */
+    const float *T_per_seq;     /* [B] device: target temperature of each sequence (NULL: T) */
+    const float *Td_per_seq;    /* [B] device: draft temperature of each sequence (NULL: T_d) */
+    void *workspace;            /* device scratch of workspace_bytes (NULL: library's own);
+                                   no initial contents are needed.  Calls sharing one
+                                   workspace must not overlap on the device. */
+    size_t workspace_bytes;
+    int32_t *d_status;          /* device int32 status word (NULL: the library's own) */
+    /* Diagnostic outputs (device, NULL = not written), all fp32: */
+    float *out_logp_draft;      /* [B, gamma]   ln p_i(d_i) */
+    float *out_logq_draft;      /* [B, gamma]   ln q_i(d_i) */
+    float *out_logZ_p;          /* [B, gamma+1] ln sum_x exp(L_t[b,i,x] / T_b) */
+    float *out_logZ_q;          /* [B, gamma]   ln sum_x exp(L_d[b,i,x] / Td_b) */
+    float *out_u;               /* [B, gamma]   acceptance uniforms */
+    float *out_race;            /* [B, 2]       winning race score ln(w(y)/E_y), and the
+                                                runner-up score (approximate) */
+    void *prof_events[4];       /* optional cudaEvent_t: recorded before the first kernel and
+                                   after each of the (up to three) kernels of the call */
+} spec_verify_opts;
+
+/* Zero every field and set dtype = SPEC_BF16. */
+void spec_verify_opts_init(spec_verify_opts *opts);
+
+/*
+ * Sampling-mode verify on bf16 logits with scalar temperatures T > 0 and T_d > 0
+ * ("How speculative decoding makes LLMs go brrr", pseudocode and module 3).
+ * target_logits [B, gamma+1, V] bf16, draft_logits [B, gamma, V] bf16,
+ * draft_tokens [B, gamma] int32; writes out_tokens [B, gamma+1] and out_n_accepted [B].
+ * Returns SPEC_EINVAL for B < 0, gamma < 0, V < 1, a non-finite or non-positive
+ * temperature, a NULL pointer (other than draft_logits / draft_tokens when gamma == 0) or a
+ * misaligned logit pointer; SPEC_ECUDA / SPEC_ENOMEM on runtime failures.
+ */
+int spec_verify(const void *target_logits, const void *draft_logits,
+                const int32_t *draft_tokens, int B, int gamma, int V, float T, float T_d,
+                uint64_t seed, int32_t *out_tokens, int32_t *out_n_accepted, void *stream);
+
+/*
+ * Greedy (T = 0) verify on bf16 target logits: g_i = the first argmax of row i of the raw
+ * target logits; draft token i is accepted while d_i == g_i; the cycle emits
+ * d_0..d_{j-1}, g_j.  The draft logits are not needed.
+ * (SubSpec's report runs its main tables at T = 0; the argmax-match rule is the plain
+ * reading of greedy verification.)
+ */
+int spec_verify_greedy(const void *target_logits, const int32_t *draft_tokens, int B, int gamma,
+                       int V, int32_t *out_tokens, int32_t *out_n_accepted, void *stream);
+
+/* Full form of spec_verify: element type, per-sequence temperatures, caller workspace,
+ * status word, global sequence index and diagnostic outputs through `opts` (NULL = the
+ * defaults of spec_verify). */
+int spec_verify_ex(const void *target_logits, const void *draft_logits,
+                   const int32_t *draft_tokens, int B, int gamma, int V, float T, float T_d,
+                   uint64_t seed, int32_t *out_tokens, int32_t *out_n_accepted,
+                   const spec_verify_opts *opts, void *stream);
+
+/* Full form of spec_verify_greedy (uses opts->dtype, workspace, d_status, prof_events). */
+int spec_verify_greedy_ex(const void *target_logits, const int32_t *draft_tokens, int B,
+                          int gamma, int V, int32_t *out_tokens, int32_t *out_n_accepted,
+                          const spec_verify_opts *opts, void *stream);
+
+/* Bytes of caller workspace the _ex entry points need for this problem (either mode).
+ * Returns 0 for invalid sizes. */
+size_t spec_verify_workspace_bytes(int B, int gamma, int V, int dtype);
+
+/* Synchronise `stream`, read the device status word (NULL = the library's own status word
+ * of the current device), reset it to SPEC_OK and return what it held (or SPEC_ECUDA). */
+int spec_verify_check(void *stream, int32_t *d_status);
+
+/* Static English text of a status code. */
+const char *spec_verify_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_H */

@@ -1,0 +1,309 @@
+// specverify.cu -- host side of libspecverify: argument checks, workspace, launches.
+//
+// The C ABI is declared in include/specverify.h; the kernels are in kernels.cuh.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "kernels.cuh"
+#include "specverify.h"
+
+using namespace specverify;
+
+namespace {
+
+constexpr int kMaxGamma = 2048;          // the scan keeps 2*gamma+1 row statistics in shared memory
+constexpr int kPieceBytes = 8192;        // bytes of one row piece (one warp item)
+constexpr int kThreads = 256;
+constexpr int kUnroll = 4;               // 16-byte loads in flight per lane in the streaming pass
+constexpr int kMaxDevices = 64;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int elem_bytes(int dtype) { return dtype == SPEC_F32 ? 4 : 2; }
+
+struct Layout {
+    int piece_len, npieces;
+    size_t stat_off, seq_off, race_off, ticket_off, total;
+};
+
+Layout layout_of(int B, int gamma, int V, int dtype) {
+    Layout L{};
+    L.piece_len = kPieceBytes / elem_bytes(dtype);
+    L.npieces = (V + L.piece_len - 1) / L.piece_len;
+    const size_t R = 2 * static_cast<size_t>(gamma) + 1;
+    size_t off = 0;
+    L.stat_off = off;
+    off = align_up(off + static_cast<size_t>(B) * R * L.npieces * sizeof(float2), 256);
+    L.seq_off = off;
+    off = align_up(off + static_cast<size_t>(B) * sizeof(SeqInfo), 256);
+    L.race_off = off;
+    off = align_up(off + static_cast<size_t>(B) * L.npieces * sizeof(RacePart), 256);
+    L.ticket_off = off;
+    off = align_up(off + static_cast<size_t>(B) * sizeof(int), 256);
+    L.total = off;
+    return L;
+}
+
+struct DeviceState {
+    bool init = false;
+    int sm_count = 0;
+    void* ws = nullptr;
+    size_t ws_bytes = 0;
+    int32_t* status = nullptr;  // library status word (its own allocation)
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+int current_device(int* dev) {
+    if (cudaGetDevice(dev) != cudaSuccess) return SPEC_ECUDA;
+    if (*dev < 0 || *dev >= kMaxDevices) return SPEC_EINVAL;
+    return SPEC_OK;
+}
+
+// Per-device state; allocates the status word on first use.  Caller holds g_mu.
+int device_state(DeviceState** out) {
+    int dev;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    DeviceState& d = g_dev[dev];
+    if (!d.init) {
+        if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return SPEC_ECUDA;
+        if (cudaMalloc(&d.status, sizeof(int32_t)) != cudaSuccess) return SPEC_ENOMEM;
+        if (cudaMemset(d.status, 0, sizeof(int32_t)) != cudaSuccess) return SPEC_ECUDA;
+        d.init = true;
+    }
+    *out = &d;
+    return SPEC_OK;
+}
+
+// Grow the library workspace of this device to `bytes` (zero-filled).  Caller holds g_mu.
+int ensure_workspace(DeviceState& d, size_t bytes) {
+    if (d.ws_bytes >= bytes) return SPEC_OK;
+    if (d.ws) {
+        cudaDeviceSynchronize();
+        cudaFree(d.ws);
+        d.ws = nullptr;
+        d.ws_bytes = 0;
+    }
+    if (cudaMalloc(&d.ws, bytes) != cudaSuccess) return SPEC_ENOMEM;
+    if (cudaMemset(d.ws, 0, bytes) != cudaSuccess) return SPEC_ECUDA;
+    d.ws_bytes = bytes;
+    return SPEC_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool good_temperature(float t) { return std::isfinite(t) && t > 0.0f; }
+
+template <class K>
+int grid_for(K kernel, int sm_count, long long warp_items) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) != cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    const long long want = (warp_items + (kThreads / 32) - 1) / (kThreads / 32);
+    long long g = static_cast<long long>(sm_count) * per_sm;
+    if (want < g) g = want;
+    return static_cast<int>(g < 1 ? 1 : g);
+}
+
+void record(const spec_verify_opts* o, int k, cudaStream_t s) {
+    if (o && o->prof_events[k]) cudaEventRecord(static_cast<cudaEvent_t>(o->prof_events[k]), s);
+}
+
+// Validated common set-up of a call: fills `p` with the workspace pointers.
+int prepare(int B, int gamma, int V, int dtype, const spec_verify_opts* o, VerifyParams& p,
+            DeviceState** dstate) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    int rc = device_state(dstate);
+    if (rc) return rc;
+    const Layout L = layout_of(B, gamma, V, dtype);
+    char* ws;
+    if (o && o->workspace) {
+        if (o->workspace_bytes < L.total) return SPEC_ENOMEM;
+        if (!aligned16(o->workspace)) return SPEC_EINVAL;
+        ws = static_cast<char*>(o->workspace);
+    } else {
+        rc = ensure_workspace(**dstate, L.total);
+        if (rc) return rc;
+        ws = static_cast<char*>((*dstate)->ws);
+    }
+    p.piece_len = L.piece_len;
+    p.npieces = L.npieces;
+    p.stat_parts = reinterpret_cast<float2*>(ws + L.stat_off);
+    p.seq = reinterpret_cast<SeqInfo*>(ws + L.seq_off);
+    p.race_parts = reinterpret_cast<RacePart*>(ws + L.race_off);
+    p.tickets = reinterpret_cast<int*>(ws + L.ticket_off);
+    p.status = (o && o->d_status) ? o->d_status : (*dstate)->status;
+    return SPEC_OK;
+}
+
+int check_common(const void* target, const int32_t* out_tokens, const int32_t* out_n, int B,
+                 int gamma, int V, int dtype) {
+    if (B < 0 || gamma < 0 || gamma > kMaxGamma || V < 1) return SPEC_EINVAL;
+    if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_EINVAL;
+    if (static_cast<long long>(B) * (gamma + 1) * static_cast<long long>(V) >= (1LL << 40))
+        return SPEC_EINVAL;
+    if (B == 0) return SPEC_OK;
+    if (!target || !out_tokens || !out_n) return SPEC_EINVAL;
+    if (!aligned16(target)) return SPEC_EINVAL;
+    return SPEC_OK;
+}
+
+template <class ET>
+int launch_sampling(VerifyParams& p, int sm_count, const spec_verify_opts* o, cudaStream_t s) {
+    const int R = 2 * p.gamma + 1;
+    record(o, 0, s);
+    const long long stat_items = static_cast<long long>(p.B) * R * p.npieces;
+    row_stats_kernel<ET, kUnroll><<<grid_for(row_stats_kernel<ET, kUnroll>, sm_count, stat_items),
+                                    kThreads, 0, s>>>(p);
+    record(o, 1, s);
+    scan_kernel<ET><<<p.B, kThreads, 2 * R * sizeof(float), s>>>(p);
+    record(o, 2, s);
+    const long long race_items = static_cast<long long>(p.B) * p.npieces;
+    race_kernel<ET><<<grid_for(race_kernel<ET>, sm_count, race_items), kThreads, 0, s>>>(p);
+    record(o, 3, s);
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
+}
+
+template <class ET>
+int launch_greedy(VerifyParams& p, int sm_count, const spec_verify_opts* o, cudaStream_t s) {
+    const int R = p.gamma + 1;
+    record(o, 0, s);
+    const long long items = static_cast<long long>(p.B) * R * p.npieces;
+    row_argmax_kernel<ET, kUnroll><<<grid_for(row_argmax_kernel<ET, kUnroll>, sm_count, items),
+                                     kThreads, 0, s>>>(p);
+    record(o, 1, s);
+    scan_greedy_kernel<ET><<<p.B, kThreads, R * sizeof(int), s>>>(p);
+    record(o, 2, s);
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+void spec_verify_opts_init(spec_verify_opts* opts) {
+    if (!opts) return;
+    std::memset(opts, 0, sizeof(*opts));
+    opts->dtype = SPEC_BF16;
+}
+
+size_t spec_verify_workspace_bytes(int B, int gamma, int V, int dtype) {
+    if (B < 0 || gamma < 0 || gamma > kMaxGamma || V < 1) return 0;
+    if (dtype != SPEC_F32 && dtype != SPEC_BF16) return 0;
+    return layout_of(B, gamma, V, dtype).total;
+}
+
+int spec_verify_ex(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
+                   int B, int gamma, int V, float T, float T_d, uint64_t seed, int32_t* out_tokens,
+                   int32_t* out_n_accepted, const spec_verify_opts* opts, void* stream) {
+    const int dtype = opts ? opts->dtype : SPEC_BF16;
+    int rc = check_common(target_logits, out_tokens, out_n_accepted, B, gamma, V, dtype);
+    if (rc || B == 0) return rc;
+    if (gamma > 0 && (!draft_logits || !draft_tokens || !aligned16(draft_logits))) return SPEC_EINVAL;
+    if (!(opts && opts->T_per_seq) && !good_temperature(T)) return SPEC_EINVAL;
+    if (!(opts && opts->Td_per_seq) && !good_temperature(T_d)) return SPEC_EINVAL;
+    VerifyParams p{};
+    p.target = target_logits;
+    p.draft = draft_logits;
+    p.tokens = draft_tokens;
+    p.B = B;
+    p.gamma = gamma;
+    p.V = V;
+    p.T = T;
+    p.Td = T_d;
+    p.T_seq = opts ? opts->T_per_seq : nullptr;
+    p.Td_seq = opts ? opts->Td_per_seq : nullptr;
+    p.key = philox_key(seed);
+    p.seq_base = opts ? opts->seq_index_base : 0u;
+    p.out_tokens = out_tokens;
+    p.out_n = out_n_accepted;
+    if (opts) {
+        p.out_logp = opts->out_logp_draft;
+        p.out_logq = opts->out_logq_draft;
+        p.out_logZp = opts->out_logZ_p;
+        p.out_logZq = opts->out_logZ_q;
+        p.out_u = opts->out_u;
+        p.out_race = opts->out_race;
+    }
+    DeviceState* d = nullptr;
+    rc = prepare(B, gamma, V, dtype, opts, p, &d);
+    if (rc) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return dtype == SPEC_F32 ? launch_sampling<F32Elem>(p, d->sm_count, opts, s)
+                             : launch_sampling<Bf16Elem>(p, d->sm_count, opts, s);
+}
+
+int spec_verify(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
+                int B, int gamma, int V, float T, float T_d, uint64_t seed, int32_t* out_tokens,
+                int32_t* out_n_accepted, void* stream) {
+    return spec_verify_ex(target_logits, draft_logits, draft_tokens, B, gamma, V, T, T_d, seed,
+                          out_tokens, out_n_accepted, nullptr, stream);
+}
+
+int spec_verify_greedy_ex(const void* target_logits, const int32_t* draft_tokens, int B, int gamma,
+                          int V, int32_t* out_tokens, int32_t* out_n_accepted,
+                          const spec_verify_opts* opts, void* stream) {
+    const int dtype = opts ? opts->dtype : SPEC_BF16;
+    int rc = check_common(target_logits, out_tokens, out_n_accepted, B, gamma, V, dtype);
+    if (rc || B == 0) return rc;
+    if (gamma > 0 && !draft_tokens) return SPEC_EINVAL;
+    VerifyParams p{};
+    p.target = target_logits;
+    p.tokens = draft_tokens;
+    p.B = B;
+    p.gamma = gamma;
+    p.V = V;
+    p.out_tokens = out_tokens;
+    p.out_n = out_n_accepted;
+    DeviceState* d = nullptr;
+    rc = prepare(B, gamma, V, dtype, opts, p, &d);
+    if (rc) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return dtype == SPEC_F32 ? launch_greedy<F32Elem>(p, d->sm_count, opts, s)
+                             : launch_greedy<Bf16Elem>(p, d->sm_count, opts, s);
+}
+
+int spec_verify_greedy(const void* target_logits, const int32_t* draft_tokens, int B, int gamma,
+                       int V, int32_t* out_tokens, int32_t* out_n_accepted, void* stream) {
+    return spec_verify_greedy_ex(target_logits, draft_tokens, B, gamma, V, out_tokens,
+                                 out_n_accepted, nullptr, stream);
+}
+
+int spec_verify_check(void* stream, int32_t* d_status) {
+    int32_t* st = d_status;
+    if (!st) {
+        std::lock_guard<std::mutex> lock(g_mu);
+        DeviceState* d = nullptr;
+        int rc = device_state(&d);
+        if (rc) return rc;
+        st = d->status;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t h = 0;
+    if (cudaMemcpyAsync(&h, st, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess) return SPEC_ECUDA;
+    if (cudaMemsetAsync(st, 0, sizeof(int32_t), s) != cudaSuccess) return SPEC_ECUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SPEC_ECUDA;
+    return h;
+}
+
+const char* spec_verify_strerror(int status) {
+    switch (status) {
+        case SPEC_OK: return "success";
+        case SPEC_EINVAL: return "invalid argument";
+        case SPEC_ECUDA: return "CUDA runtime error";
+        case SPEC_EBADTOKEN: return "draft token outside [0, V)";
+        case SPEC_ETIMEOUT: return "bounded device wait timed out";
+        case SPEC_ENOMEM: return "workspace allocation failed or caller workspace too small";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

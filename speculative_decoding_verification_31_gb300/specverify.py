@@ -1,0 +1,257 @@
+"""Python binding of libspecverify (ctypes): argument marshalling only.
+
+Every step of the verify path runs in the CUDA library; this module checks tensor shapes,
+allocates outputs with PyTorch when the caller gives none, and passes raw device pointers
+and the CUDA stream handle through the C ABI declared in ``include/specverify.h``.  There
+is no fallback: if the compiled library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libspecverify.so")
+
+SPEC_OK, SPEC_EINVAL, SPEC_ECUDA, SPEC_EBADTOKEN, SPEC_ETIMEOUT, SPEC_ENOMEM = range(6)
+SPEC_F32, SPEC_BF16 = 0, 1
+
+EXPORTED = ("spec_verify", "spec_verify_greedy", "spec_verify_ex", "spec_verify_greedy_ex",
+            "spec_verify_workspace_bytes", "spec_verify_check", "spec_verify_strerror",
+            "spec_verify_opts_init")
+
+
+class SpecVerifyError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {spec_verify_strerror(code)} (status {code})")
+        self.code = code
+
+
+class SpecVerifyOpts(ctypes.Structure):
+    """Mirror of ``spec_verify_opts``."""
+    _fields_ = [
+        ("dtype", ctypes.c_int32),
+        ("seq_index_base", ctypes.c_uint32),
+        ("T_per_seq", ctypes.c_void_p),
+        ("Td_per_seq", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_size_t),
+        ("d_status", ctypes.c_void_p),
+        ("out_logp_draft", ctypes.c_void_p),
+        ("out_logq_draft", ctypes.c_void_p),
+        ("out_logZ_p", ctypes.c_void_p),
+        ("out_logZ_q", ctypes.c_void_p),
+        ("out_u", ctypes.c_void_p),
+        ("out_race", ctypes.c_void_p),
+        ("prof_events", ctypes.c_void_p * 4),
+    ]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libspecverify.so (built by ``build.build()``); raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libspecverify.so is not built ({path}); run "
+                           "`python -m speculative_decoding_verification_31_gb300.build`")
+    lib = ctypes.CDLL(path)
+    P, I, U64, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64, ctypes.c_float
+    OP = ctypes.POINTER(SpecVerifyOpts)
+    lib.spec_verify.argtypes = [P, P, P, I, I, I, F, F, U64, P, P, P]
+    lib.spec_verify_greedy.argtypes = [P, P, I, I, I, P, P, P]
+    lib.spec_verify_ex.argtypes = [P, P, P, I, I, I, F, F, U64, P, P, OP, P]
+    lib.spec_verify_greedy_ex.argtypes = [P, P, I, I, I, P, P, OP, P]
+    for f in ("spec_verify", "spec_verify_greedy", "spec_verify_ex", "spec_verify_greedy_ex"):
+        getattr(lib, f).restype = ctypes.c_int
+    lib.spec_verify_workspace_bytes.argtypes = [I, I, I, I]
+    lib.spec_verify_workspace_bytes.restype = ctypes.c_size_t
+    lib.spec_verify_check.argtypes = [P, P]
+    lib.spec_verify_check.restype = ctypes.c_int
+    lib.spec_verify_strerror.argtypes = [I]
+    lib.spec_verify_strerror.restype = ctypes.c_char_p
+    lib.spec_verify_opts_init.argtypes = [OP]
+    lib.spec_verify_opts_init.restype = None
+    _lib = lib
+    return lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream, device) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return SPEC_BF16
+    if t.dtype == torch.float32:
+        return SPEC_F32
+    raise TypeError(f"logits must be bfloat16 or float32, got {t.dtype}")
+
+
+def _check_shapes(target, draft, tokens, greedy=False):
+    if target.dim() != 3 or not target.is_cuda or not target.is_contiguous():
+        raise ValueError("target_logits must be a contiguous CUDA tensor [B, gamma+1, V]")
+    B, G1, V = target.shape
+    g = G1 - 1
+    if not greedy and g > 0:
+        if draft is None or tuple(draft.shape) != (B, g, V) or not draft.is_contiguous():
+            raise ValueError(f"draft_logits must be contiguous [B, gamma, V] = {(B, g, V)}")
+        if draft.dtype != target.dtype:
+            raise TypeError("target and draft logits must have the same dtype")
+    if g > 0:
+        if tokens is None or tuple(tokens.shape) != (B, g) or tokens.dtype != torch.int32 \
+                or not tokens.is_contiguous():
+            raise ValueError(f"draft_tokens must be contiguous int32 [B, gamma] = {(B, g)}")
+    return B, g, V
+
+
+def _outputs(target, B, g, out_tokens, out_n):
+    dev = target.device
+    if out_tokens is None:
+        out_tokens = torch.empty((B, g + 1), dtype=torch.int32, device=dev)
+    if out_n is None:
+        out_n = torch.empty((B,), dtype=torch.int32, device=dev)
+    return out_tokens, out_n
+
+
+def spec_verify(target_logits, draft_logits, draft_tokens, T: float, T_d: float, seed: int,
+                out_tokens=None, out_n_accepted=None, stream=None):
+    """Sampling-mode verify on bf16 logits (see ``spec_verify`` in the C header).
+    Returns (out_tokens [B, gamma+1] int32, out_n_accepted [B] int32), both on the device."""
+    B, g, V = _check_shapes(target_logits, draft_logits, draft_tokens)
+    if target_logits.dtype != torch.bfloat16:
+        raise TypeError("spec_verify takes bf16 logits; use spec_verify_ex for float32")
+    out_tokens, out_n_accepted = _outputs(target_logits, B, g, out_tokens, out_n_accepted)
+    rc = load_library().spec_verify(
+        _ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), B, g, V, T, T_d,
+        int(seed) & (2**64 - 1), _ptr(out_tokens), _ptr(out_n_accepted),
+        _stream_handle(stream, target_logits.device))
+    if rc != SPEC_OK:
+        raise SpecVerifyError(rc, "spec_verify")
+    return out_tokens, out_n_accepted
+
+
+def spec_verify_greedy(target_logits, draft_tokens, out_tokens=None, out_n_accepted=None,
+                       stream=None):
+    """Greedy (argmax-match) verify on bf16 target logits."""
+    B, g, V = _check_shapes(target_logits, None, draft_tokens, greedy=True)
+    if target_logits.dtype != torch.bfloat16:
+        raise TypeError("spec_verify_greedy takes bf16 logits; use spec_verify_greedy_ex")
+    out_tokens, out_n_accepted = _outputs(target_logits, B, g, out_tokens, out_n_accepted)
+    rc = load_library().spec_verify_greedy(
+        _ptr(target_logits), _ptr(draft_tokens), B, g, V, _ptr(out_tokens),
+        _ptr(out_n_accepted), _stream_handle(stream, target_logits.device))
+    if rc != SPEC_OK:
+        raise SpecVerifyError(rc, "spec_verify_greedy")
+    return out_tokens, out_n_accepted
+
+
+def _make_opts(dtype, T_per_seq, Td_per_seq, seq_index_base, workspace, d_status, diag,
+               prof_events: Optional[Sequence]):
+    o = SpecVerifyOpts()
+    load_library().spec_verify_opts_init(ctypes.byref(o))
+    o.dtype = dtype
+    o.seq_index_base = int(seq_index_base)
+    o.T_per_seq = T_per_seq.data_ptr() if T_per_seq is not None else None
+    o.Td_per_seq = Td_per_seq.data_ptr() if Td_per_seq is not None else None
+    if workspace is not None:
+        o.workspace = workspace.data_ptr()
+        o.workspace_bytes = workspace.numel() * workspace.element_size()
+    o.d_status = d_status.data_ptr() if d_status is not None else None
+    if diag:
+        o.out_logp_draft = diag["logp"].data_ptr()
+        o.out_logq_draft = diag["logq"].data_ptr()
+        o.out_logZ_p = diag["logZp"].data_ptr()
+        o.out_logZ_q = diag["logZq"].data_ptr()
+        o.out_u = diag["u"].data_ptr()
+        o.out_race = diag["race"].data_ptr()
+    if prof_events:
+        for k, ev in enumerate(prof_events[:4]):
+            if ev is not None and not ev.cuda_event:
+                raise ValueError("torch creates a CUDA event on its first record(); record "
+                                 "each profiling event once before passing it")
+            o.prof_events[k] = ev.cuda_event if ev is not None else None
+    return o
+
+
+def _check_temps(t, B, dev, name):
+    if t is None:
+        return None
+    if tuple(t.shape) != (B,) or t.dtype != torch.float32 or t.device != dev \
+            or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous float32 [B] tensor on {dev}")
+    return t
+
+
+def spec_verify_ex(target_logits, draft_logits, draft_tokens, T: float, T_d: float, seed: int,
+                   out_tokens=None, out_n_accepted=None, *, T_per_seq=None, Td_per_seq=None,
+                   seq_index_base: int = 0, workspace=None, d_status=None,
+                   diagnostics: bool = False, prof_events=None, stream=None):
+    """Full form (see ``spec_verify_ex`` in the C header).  Returns
+    (out_tokens, out_n_accepted, diag) where diag holds the diagnostic outputs when
+    ``diagnostics`` is set (ln p(d_i), ln q(d_i), ln Z_p, ln Z_q, u, race scores)."""
+    B, g, V = _check_shapes(target_logits, draft_logits, draft_tokens)
+    dev = target_logits.device
+    out_tokens, out_n_accepted = _outputs(target_logits, B, g, out_tokens, out_n_accepted)
+    T_per_seq = _check_temps(T_per_seq, B, dev, "T_per_seq")
+    Td_per_seq = _check_temps(Td_per_seq, B, dev, "Td_per_seq")
+    diag = None
+    if diagnostics:
+        f = dict(dtype=torch.float32, device=dev)
+        diag = {"logp": torch.full((B, g), float("nan"), **f),
+                "logq": torch.full((B, g), float("nan"), **f),
+                "logZp": torch.full((B, g + 1), float("nan"), **f),
+                "logZq": torch.full((B, g), float("nan"), **f),
+                "u": torch.full((B, g), float("nan"), **f),
+                "race": torch.full((B, 2), float("nan"), **f)}
+    o = _make_opts(_dtype_code(target_logits), T_per_seq, Td_per_seq, seq_index_base, workspace,
+                   d_status, diag, prof_events)
+    rc = load_library().spec_verify_ex(
+        _ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), B, g, V, float(T),
+        float(T_d), int(seed) & (2**64 - 1), _ptr(out_tokens), _ptr(out_n_accepted),
+        ctypes.byref(o), _stream_handle(stream, dev))
+    if rc != SPEC_OK:
+        raise SpecVerifyError(rc, "spec_verify_ex")
+    return out_tokens, out_n_accepted, diag
+
+
+def spec_verify_greedy_ex(target_logits, draft_tokens, out_tokens=None, out_n_accepted=None, *,
+                          workspace=None, d_status=None, prof_events=None, stream=None):
+    B, g, V = _check_shapes(target_logits, None, draft_tokens, greedy=True)
+    dev = target_logits.device
+    out_tokens, out_n_accepted = _outputs(target_logits, B, g, out_tokens, out_n_accepted)
+    o = _make_opts(_dtype_code(target_logits), None, None, 0, workspace, d_status, None,
+                   prof_events)
+    rc = load_library().spec_verify_greedy_ex(
+        _ptr(target_logits), _ptr(draft_tokens), B, g, V, _ptr(out_tokens), _ptr(out_n_accepted),
+        ctypes.byref(o), _stream_handle(stream, dev))
+    if rc != SPEC_OK:
+        raise SpecVerifyError(rc, "spec_verify_greedy_ex")
+    return out_tokens, out_n_accepted
+
+
+def spec_verify_workspace_bytes(B: int, gamma: int, V: int, dtype: int = SPEC_BF16) -> int:
+    return int(load_library().spec_verify_workspace_bytes(B, gamma, V, dtype))
+
+
+def spec_verify_check(stream=None, d_status=None, device=None) -> int:
+    """Synchronise the stream and return (and clear) the device status word."""
+    return int(load_library().spec_verify_check(_stream_handle(stream, device), _ptr(d_status)))
+
+
+def spec_verify_strerror(code: int) -> str:
+    return load_library().spec_verify_strerror(int(code)).decode()

@@ -1,0 +1,104 @@
+"""Helpers shared by the GPU parity tests: move a workload to the device, run the library
+through its C ABI, run the oracle on the same inputs, and compare under the stated rules.
+
+Parity rules (the method is an exact sampler, so the particular draw is pinned by the
+random-number contract):
+  * greedy mode: tokens and accepted counts bit-exact;
+  * sampling mode: tokens and accepted counts bit-exact, except sequences the oracle flags
+    as near-ties (|u - p/q| < 1e-5 at a tested position, or top-two race scores within
+    1e-6 relative); flagged decisions must stay under 1e-4 of all decisions;
+  * p(d_i) and q(d_i) within 1e-5 relative; u_i bit-exact; ln Z within 1e-6 relative.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import workloads
+
+NEAR_TIE = oracle.FLAG_ACCEPT_NEAR_TIE | oracle.FLAG_RACE_NEAR_TIE | oracle.FLAG_RESIDUAL_EMPTY
+
+# running totals over the session: decisions compared and decisions flagged
+TOTALS = {"decisions": 0, "flagged": 0, "sequences": 0, "mismatch_flagged": 0}
+
+
+def to_device(a: np.ndarray, dtype: str, dev) -> torch.Tensor:
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev)
+
+
+class DeviceWorkload:
+    def __init__(self, w: workloads.Workload, dev="cuda:0"):
+        self.w = w
+        self.dev = torch.device(dev)
+        self.target = to_device(w.target, w.dtype, self.dev)
+        self.draft = to_device(w.draft, w.dtype, self.dev)
+        self.tokens = torch.from_numpy(np.ascontiguousarray(w.tokens)).to(self.dev)
+        self.T = torch.from_numpy(w.T.astype(np.float32)).to(self.dev)
+        self.Td = torch.from_numpy(w.Td.astype(np.float32)).to(self.dev)
+
+
+def run_gpu(sv, dw: DeviceWorkload, seed: int, per_seq_temps: bool = True, seq_index_base=0,
+            diagnostics=True):
+    w = dw.w
+    kw = {}
+    if per_seq_temps:
+        kw = dict(T_per_seq=dw.T, Td_per_seq=dw.Td)
+    out_t, out_n, diag = sv.spec_verify_ex(dw.target, dw.draft, dw.tokens, float(w.T[0]),
+                                           float(w.Td[0]), seed, seq_index_base=seq_index_base,
+                                           diagnostics=diagnostics, **kw)
+    torch.cuda.synchronize()
+    res = {"tokens": out_t.cpu().numpy(), "n": out_n.cpu().numpy()}
+    if diag:
+        res.update({k: v.cpu().numpy() for k, v in diag.items()})
+    return res
+
+
+def compare_sampling(w: workloads.Workload, g: dict, r: "oracle.OracleResult",
+                     check_values: bool = True, idx=None):
+    """Assert parity of GPU results `g` with oracle results `r` (same sequences).
+    `idx` selects GPU rows when the oracle ran on a subset."""
+    if idx is not None:
+        g = {k: v[idx] for k, v in g.items()}
+    B, gamma = w.B if idx is None else len(idx), w.gamma
+    flagged = (r.flags & NEAR_TIE) != 0
+    bad = (r.flags & oracle.FLAG_BAD_TOKEN) != 0
+    decisions = int(np.sum(np.where(bad, 0, np.minimum(r.n_accepted + 1, gamma) + 1)))
+    TOTALS["decisions"] += decisions
+    TOTALS["flagged"] += int(flagged.sum())
+    TOTALS["sequences"] += B
+    for b in range(B):
+        if flagged[b]:
+            TOTALS["mismatch_flagged"] += int(g["n"][b] != r.n_accepted[b] or
+                                               not np.array_equal(g["tokens"][b], r.tokens[b]))
+            # still a valid cycle
+            j = g["n"][b]
+            assert 0 <= j <= gamma
+            assert np.all(g["tokens"][b, j + 1:] == -1) and 0 <= g["tokens"][b, j] < w.V
+            continue
+        assert g["n"][b] == r.n_accepted[b], (b, g["n"][b], r.n_accepted[b], r.flags[b])
+        np.testing.assert_array_equal(g["tokens"][b], r.tokens[b], err_msg=f"sequence {b}")
+    if not check_values or "u" not in g:
+        return
+    ok = ~bad
+    np.testing.assert_array_equal(g["u"].astype(np.float64), r.u)
+    if gamma:
+        for name, ref in (("logp", r.logp), ("logq", r.logq)):
+            got = g[name][ok].astype(np.float64)
+            want = ref[ok]
+            fin = np.isfinite(want)
+            assert np.array_equal(np.isfinite(got), fin), name
+            # p and q within 1e-5 relative  <=>  |ln p_gpu - ln p_oracle| < ~1e-5
+            err = np.abs(np.expm1(got[fin] - want[fin]))
+            assert err.size == 0 or err.max() < 1e-5, (name, float(err.max()))
+        zq = g["logZq"].astype(np.float64)
+        np.testing.assert_allclose(zq, r.logZq, rtol=1e-6, atol=1e-6)
+    zp = g["logZp"].astype(np.float64)
+    np.testing.assert_allclose(zp, r.logZp, rtol=1e-6, atol=1e-6)
+
+
+def compare_greedy(g_tokens, g_n, r_tokens, r_n):
+    np.testing.assert_array_equal(g_n, r_n)
+    np.testing.assert_array_equal(g_tokens, r_tokens)

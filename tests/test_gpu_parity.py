@@ -1,0 +1,261 @@
+"""GPU parity of libspecverify against the CPU oracle (marked gpu).
+
+Every call goes through the C ABI (the ctypes binding).  Sizes span several row pieces
+with ragged tails, unaligned rows (V not a multiple of 8), gamma = 0, fp32 and bf16,
+scalar and per-sequence temperatures; the five named workloads run in the launch
+configuration the benchmark times (full size; the two batched ones compared on sampled
+sequences, which the oracle can compute one by one).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from _parity import TOTALS, DeviceWorkload, compare_greedy, compare_sampling, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sv():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import speculative_decoding_verification_31_gb300 as m
+    m.load_library()
+    return m
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.get()
+
+
+SMALL_SHAPES = [
+    # B, gamma, V, dtype
+    (1, 5, 1024, "f32"),
+    (3, 4, 5003, "bf16"),    # unaligned rows, ragged last piece
+    (2, 7, 9000, "f32"),     # several pieces
+    (4, 0, 777, "bf16"),     # plain sampling
+    (2, 3, 1, "f32"),        # V = 1
+    (5, 2, 7, "bf16"),       # V < one vector
+    (2, 6, 20000, "bf16"),   # several pieces, aligned rows
+    (1, 1, 4100, "f32"),     # piece boundary + 4
+]
+
+
+@pytest.mark.parametrize("B,gamma,V,dtype", SMALL_SHAPES)
+def test_greedy_small(sv, orc, B, gamma, V, dtype):
+    w = workloads.generic(B=B, gamma=gamma, V=V, dtype=dtype, seed=B * 1000 + V, greedy=True)
+    dw = DeviceWorkload(w)
+    # make some drafts disagree so the first mismatch moves
+    tok = w.tokens.copy()
+    if gamma:
+        tok[0, gamma // 2] = (tok[0, gamma // 2] + 1) % V if V > 1 else tok[0, gamma // 2]
+    dtok = torch.from_numpy(tok).cuda()
+    out_t, out_n = sv.spec_verify_greedy_ex(dw.target, dtok)
+    torch.cuda.synchronize()
+    rt, rn, _ = orc.verify_greedy(w.target, tok)
+    compare_greedy(out_t.cpu().numpy(), out_n.cpu().numpy(), rt, rn)
+    assert sv.spec_verify_check() == sv.SPEC_OK
+
+
+def test_greedy_ties_lowest_index(sv, orc):
+    w = workloads.generic(B=2, gamma=3, V=30000, dtype="bf16", seed=3, greedy=True)
+    t = w.target.copy()
+    tf = workloads.as_f32(t, "bf16")
+    for b in range(2):
+        for i in range(4):
+            m = int(np.argmax(tf[b, i]))
+            for off in (9001, 17, 4096 * 3):       # equal maxima after the first
+                t[b, i, (m + off) % w.V] = t[b, i, m]
+            if m > 5:
+                t[b, i, m - 5] = t[b, i, m]        # ... and one before it
+    dt = torch.from_numpy(t.view(np.int16)).view(torch.bfloat16).cuda()
+    out_t, out_n = sv.spec_verify_greedy(dt, torch.from_numpy(w.tokens).cuda())
+    torch.cuda.synchronize()
+    rt, rn, _ = orc.verify_greedy(t, w.tokens)
+    compare_greedy(out_t.cpu().numpy(), out_n.cpu().numpy(), rt, rn)
+
+
+@pytest.mark.parametrize("B,gamma,V,dtype", SMALL_SHAPES)
+@pytest.mark.parametrize("temps", [(1.0, 1.0), (0.6, 0.2), (1.3, 0.8)])
+def test_sampling_small(sv, orc, B, gamma, V, dtype, temps):
+    T, Td = temps
+    w = workloads.generic(B=B, gamma=gamma, V=V, dtype=dtype, seed=B * 7 + V, sigma=0.7, T=T,
+                          Td=Td)
+    dw = DeviceWorkload(w)
+    for seed in range(6):
+        g = run_gpu(sv, dw, seed, per_seq_temps=(seed % 2 == 0))
+        r = orc.verify(w.target, w.draft, w.tokens, w.T, w.Td, seed)
+        compare_sampling(w, g, r)
+    assert sv.spec_verify_check() == sv.SPEC_OK
+
+
+def test_per_sequence_temperatures(sv, orc):
+    w = workloads.config(3, B=6)          # first 6 sequences of the batched workload
+    assert len(np.unique(w.T)) == 6
+    dw = DeviceWorkload(w)
+    for seed in range(3):
+        g = run_gpu(sv, dw, seed, per_seq_temps=True)
+        r = orc.verify(w.target, w.draft, w.tokens, w.T, w.Td, seed)
+        compare_sampling(w, g, r)
+
+
+@pytest.mark.parametrize("cfg", [0, 1, 2])
+def test_named_single_sequence_workloads(sv, orc, cfg):
+    w = workloads.config(cfg)
+    dw = DeviceWorkload(w)
+    nseeds = {0: 200, 1: 12, 2: 6}[cfg]
+    for seed in range(nseeds):
+        g = run_gpu(sv, dw, seed, per_seq_temps=False, diagnostics=(seed < 3))
+        r = orc.verify(w.target, w.draft, w.tokens, w.T, w.Td, seed)
+        compare_sampling(w, g, r, check_values=(seed < 3))
+
+
+def test_named_single_sequence_greedy(sv, orc):
+    w = workloads.config(1, greedy=True)
+    dw = DeviceWorkload(w)
+    out_t, out_n = sv.spec_verify_greedy(dw.target, dw.tokens)
+    torch.cuda.synchronize()
+    rt, rn, _ = orc.verify_greedy(w.target, w.tokens)
+    compare_greedy(out_t.cpu().numpy(), out_n.cpu().numpy(), rt, rn)
+    assert rn[0] == w.gamma or rt[0, rn[0]] != w.tokens[0, rn[0]]
+
+
+def test_batched_serving_workload_full(sv, orc):
+    """B=64, gamma=8, V=128256 with per-sequence temperatures: every sequence checked."""
+    w = workloads.config(3)
+    dw = DeviceWorkload(w)
+    for seed in range(2):
+        g = run_gpu(sv, dw, seed, per_seq_temps=True, diagnostics=(seed == 0))
+        r = orc.verify(w.target, w.draft, w.tokens, w.T, w.Td, seed)
+        compare_sampling(w, g, r, check_values=(seed == 0))
+    wg = workloads.config(3, greedy=True)
+    dg = DeviceWorkload(wg)
+    out_t, out_n = sv.spec_verify_greedy(dg.target, dg.tokens)
+    torch.cuda.synchronize()
+    rt, rn, _ = orc.verify_greedy(wg.target, wg.tokens)
+    compare_greedy(out_t.cpu().numpy(), out_n.cpu().numpy(), rt, rn)
+
+
+def test_throughput_workload_full_size_sampled(sv, orc):
+    """B=256, gamma=12, V=152064 bf16 (1.95 GB): one full-size call in the benchmark's
+    launch configuration, 32 sampled sequences recomputed by the oracle one by one."""
+    w = workloads.config(4)
+    dw = DeviceWorkload(w)
+    rng = np.random.default_rng(0)
+    idx = np.sort(rng.choice(w.B, size=32, replace=False))
+    for seed in (0, 1):
+        g = run_gpu(sv, dw, seed, per_seq_temps=False, diagnostics=True)
+        sub = w.subset(idx)
+        # the oracle takes the global sequence index from b_base: one call per sequence
+        parts = [orc.verify(sub.target[k:k + 1], sub.draft[k:k + 1], sub.tokens[k:k + 1],
+                            sub.T[k:k + 1], sub.Td[k:k + 1], seed, b_base=int(b))
+                 for k, b in enumerate(idx)]
+        r = oracle.OracleResult(**{f: np.concatenate([getattr(p, f) for p in parts])
+                                   for f in oracle.OracleResult.__dataclass_fields__})
+        compare_sampling(sub, g, r, idx=idx)
+        # every sequence emits a valid cycle
+        assert np.all((g["n"] >= 0) & (g["n"] <= w.gamma))
+
+
+def test_seq_index_base_splits_a_batch(sv, orc):
+    """Two half-batch calls with seq_index_base give exactly the one-call result."""
+    w = workloads.generic(B=8, gamma=5, V=6000, dtype="bf16", seed=9, T=0.8, Td=0.4)
+    dw = DeviceWorkload(w)
+    full = run_gpu(sv, dw, 5, per_seq_temps=False, diagnostics=False)
+    halves = []
+    for lo in (0, 4):
+        sub = w.subset(range(lo, lo + 4))
+        halves.append(run_gpu(sv, DeviceWorkload(sub), 5, per_seq_temps=False,
+                              seq_index_base=lo, diagnostics=False))
+    np.testing.assert_array_equal(full["tokens"], np.concatenate([h["tokens"] for h in halves]))
+    np.testing.assert_array_equal(full["n"], np.concatenate([h["n"] for h in halves]))
+
+
+def test_repeatable_and_caller_workspace(sv, orc):
+    w = workloads.generic(B=5, gamma=6, V=33000, dtype="bf16", seed=4, T=1.0, Td=0.3)
+    dw = DeviceWorkload(w)
+    a = run_gpu(sv, dw, 77, per_seq_temps=False, diagnostics=False)
+    nbytes = sv.spec_verify_workspace_bytes(w.B, w.gamma, w.V, sv.SPEC_BF16)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(3):  # tickets must be left at zero by every call
+        t, n, _ = sv.spec_verify_ex(dw.target, dw.draft, dw.tokens, float(w.T[0]),
+                                    float(w.Td[0]), 77, workspace=ws, d_status=status)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(t.cpu().numpy(), a["tokens"])
+        np.testing.assert_array_equal(n.cpu().numpy(), a["n"])
+    assert sv.spec_verify_check(d_status=status) == sv.SPEC_OK
+    small = torch.zeros(nbytes // 2, dtype=torch.uint8, device="cuda")
+    with pytest.raises(sv.SpecVerifyError) as e:
+        sv.spec_verify_ex(dw.target, dw.draft, dw.tokens, 1.0, 1.0, 0, workspace=small)
+    assert e.value.code == sv.SPEC_ENOMEM
+
+
+def test_bad_tokens_are_reported(sv, orc):
+    w = workloads.generic(B=4, gamma=3, V=500, dtype="bf16", seed=6)
+    tok = w.tokens.copy()
+    tok[1, 1] = 500
+    tok[3, 0] = -1
+    dw = DeviceWorkload(w)
+    dtok = torch.from_numpy(tok).cuda()
+    t, n, _ = sv.spec_verify_ex(dw.target, dw.draft, dtok, 1.0, 1.0, 3)
+    assert sv.spec_verify_check() == sv.SPEC_EBADTOKEN
+    assert sv.spec_verify_check() == sv.SPEC_OK  # reading clears it
+    r = orc.verify(w.target, w.draft, tok, w.T, w.Td, 3)
+    np.testing.assert_array_equal(n.cpu().numpy(), r.n_accepted)
+    np.testing.assert_array_equal(t.cpu().numpy(), r.tokens)
+    tg, ng = sv.spec_verify_greedy(dw.target, dtok)
+    assert sv.spec_verify_check() == sv.SPEC_EBADTOKEN
+    assert ng.cpu().numpy()[1] == -1 and ng.cpu().numpy()[3] == -1
+
+
+def test_degenerate_distributions(sv, orc):
+    """-inf draft logits (q = 0 outside the draft token), identical draft and target."""
+    V, g = 3000, 4
+    w = workloads.generic(B=3, gamma=g, V=V, dtype="f32", seed=8, T=0.9, Td=0.9)
+    draft = w.draft.copy()
+    # sequence 0: one-hot q on its draft tokens (draft logits -inf elsewhere)
+    draft[0] = -np.inf
+    for i in range(g):
+        draft[0, i, w.tokens[0, i]] = 0.0
+    # sequence 1: draft identical to target, same temperature -> never rejects
+    draft[1] = w.target[1, :g]
+    tok = w.tokens.copy()
+    tok[1] = np.argmax(w.target[1, :g], axis=-1)
+    w2 = workloads.Workload("degenerate", 3, g, V, "f32", w.target, draft, tok, w.T, w.Td)
+    dw = DeviceWorkload(w2)
+    for seed in range(20):
+        gres = run_gpu(sv, dw, seed, per_seq_temps=False)
+        r = orc.verify(w2.target, w2.draft, w2.tokens, w2.T, w2.Td, seed)
+        compare_sampling(w2, gres, r)
+        assert gres["n"][1] == g
+
+
+def test_empty_batch_and_invalid_arguments(sv):
+    e = torch.empty((0, 4, 100), dtype=torch.bfloat16, device="cuda")
+    d = torch.empty((0, 3, 100), dtype=torch.bfloat16, device="cuda")
+    tok = torch.empty((0, 3), dtype=torch.int32, device="cuda")
+    t, n = sv.spec_verify(e, d, tok, 1.0, 1.0, 0)
+    assert t.shape == (0, 4) and n.shape == (0,)
+    w = workloads.generic(B=2, gamma=3, V=64, dtype="bf16", seed=1)
+    dw = DeviceWorkload(w)
+    for T, Td in ((0.0, 1.0), (1.0, -1.0), (float("nan"), 1.0), (1.0, float("inf"))):
+        with pytest.raises(sv.SpecVerifyError) as ex:
+            sv.spec_verify(dw.target, dw.draft, dw.tokens, T, Td, 0)
+        assert ex.value.code == sv.SPEC_EINVAL
+    # misaligned logit pointer
+    flat = torch.zeros(2 * 4 * 64 + 1, dtype=torch.bfloat16, device="cuda")
+    mis = flat[1:].view(2, 4, 64)
+    with pytest.raises(sv.SpecVerifyError) as ex:
+        sv.spec_verify(mis, dw.draft, dw.tokens, 1.0, 1.0, 0)
+    assert ex.value.code == sv.SPEC_EINVAL
+
+
+def test_zz_near_tie_budget():
+    """Flagged near-tie decisions stay under 1e-4 of all decisions compared in this module."""
+    if TOTALS["decisions"] == 0:
+        pytest.skip("no sampling comparisons ran")
+    assert TOTALS["flagged"] <= max(1, 1e-4 * TOTALS["decisions"]), TOTALS
