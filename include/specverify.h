@@ -61,7 +61,9 @@ typedef enum {
     SPEC_ECUDA = 2,      /* a CUDA runtime call or launch failed */
     SPEC_EBADTOKEN = 3,  /* (device) a draft token outside [0, V) */
     SPEC_ETIMEOUT = 4,   /* (device) a bounded wait gave up */
-    SPEC_ENOMEM = 5      /* workspace allocation failed or caller workspace too small */
+    SPEC_ENOMEM = 5,     /* workspace allocation failed or caller workspace too small */
+    SPEC_ESCRATCH = 6    /* problem needs more scratch than spec_verify_noalloc's static
+                            buffer (SPEC_NOALLOC_SCRATCH_BYTES) holds */
 } spec_status;
 
 /* Element type of the logits. */
@@ -140,6 +142,37 @@ int spec_verify_check(void *stream, int32_t *d_status);
 
 /* Static English text of a status code. */
 const char *spec_verify_strerror(int status);
+
+/*
+ * Allocation-free form of spec_verify_ex.  The pages have no counterpart: this entry point
+ * exists for callers that cannot let a library call cudaMalloc -- an inference server that
+ * reserves nearly all device memory for its own pool up front, or a latency-critical caller
+ * that may not block on the device synchronisation cudaMalloc/cudaFree can imply.  (The
+ * other entry points allocate the library's status word, and the plain ones its workspace,
+ * on first use.)
+ *
+ * The scratch (per-row partial statistics, per-sequence scan results, race partials and
+ * arrival counters, and a status word) lives in one file-scope device array of
+ * SPEC_NOALLOC_SCRATCH_BYTES, which every GPU that loads the library holds until the process
+ * exits.  The caller still passes the inputs and outputs, exactly as for spec_verify_ex;
+ * opts->workspace must be NULL.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress, with that device current); make that first call before any
+ * stream capture.  Calls share the one array and it keeps the last call's contents: calls
+ * that overlap on the GPU (other streams, other threads) race and give wrong results, so
+ * serialise them.  Nothing in the array needs to start at zero: every call writes what it
+ * reads.  Device-side errors go to opts->d_status when given; otherwise to a word inside the
+ * array that this call clears first and that spec_verify_check cannot read (a bad draft
+ * token still shows as n_accepted = -1).  No cudaMalloc, cudaFree or allocating library
+ * routine is called.
+ * Returns SPEC_ESCRATCH, without launching anything, when spec_verify_workspace_bytes() of
+ * the problem exceeds SPEC_NOALLOC_SCRATCH_BYTES - 256; otherwise as spec_verify_ex.
+ */
+#define SPEC_NOALLOC_SCRATCH_BYTES (8u << 20) /* 8 MiB: B=256, gamma=12, V=152064 bf16 needs
+                                                 2.1 MB */
+int spec_verify_noalloc(const void *target_logits, const void *draft_logits,
+                        const int32_t *draft_tokens, int B, int gamma, int V, float T, float T_d,
+                        uint64_t seed, int32_t *out_tokens, int32_t *out_n_accepted,
+                        const spec_verify_opts *opts, void *stream);
 
 #ifdef __cplusplus
 }

@@ -302,8 +302,111 @@ const char* spec_verify_strerror(int status) {
         case SPEC_EBADTOKEN: return "draft token outside [0, V)";
         case SPEC_ETIMEOUT: return "bounded device wait timed out";
         case SPEC_ENOMEM: return "workspace allocation failed or caller workspace too small";
+        case SPEC_ESCRATCH: return "problem needs more scratch than the static no-alloc buffer";
         default: return "unknown status";
     }
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------------------------
+// spec_verify_noalloc: the sampling verify with its scratch in a file-scope device array, for
+// callers that cannot let the library allocate device memory.
+// ------------------------------------------------------------------------------------------
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SPEC_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr size_t kNoallocStatusOff = SPEC_NOALLOC_SCRATCH_BYTES - 256;  // last 256 bytes
+
+struct NoallocDevice {
+    bool ready = false;
+    char* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+    int sm_count = 0;
+};
+
+std::mutex g_noalloc_mu;
+NoallocDevice g_noalloc[kMaxDevices];
+
+// Once per device, with that device current: the array's device address (host code cannot
+// use the symbol itself, which names a host-side stand-in) and the SM count.
+int noalloc_device(NoallocDevice** out) {
+    int dev;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    NoallocDevice& d = g_noalloc[dev];
+    if (!d.ready) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
+            return SPEC_ECUDA;
+        if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return SPEC_ECUDA;
+        d.scratch = static_cast<char*>(ptr);
+        d.ready = true;
+    }
+    *out = &d;
+    return SPEC_OK;
+}
+
+}  // namespace
+
+extern "C" int spec_verify_noalloc(const void* target_logits, const void* draft_logits,
+                                   const int32_t* draft_tokens, int B, int gamma, int V, float T,
+                                   float T_d, uint64_t seed, int32_t* out_tokens,
+                                   int32_t* out_n_accepted, const spec_verify_opts* opts,
+                                   void* stream) {
+    const int dtype = opts ? opts->dtype : SPEC_BF16;
+    int rc = check_common(target_logits, out_tokens, out_n_accepted, B, gamma, V, dtype);
+    if (rc || B == 0) return rc;
+    if (opts && opts->workspace) return SPEC_EINVAL;
+    if (gamma > 0 && (!draft_logits || !draft_tokens || !aligned16(draft_logits))) return SPEC_EINVAL;
+    if (!(opts && opts->T_per_seq) && !good_temperature(T)) return SPEC_EINVAL;
+    if (!(opts && opts->Td_per_seq) && !good_temperature(T_d)) return SPEC_EINVAL;
+    const Layout L = layout_of(B, gamma, V, dtype);
+    if (L.total > kNoallocStatusOff) return SPEC_ESCRATCH;
+    NoallocDevice* nd = nullptr;
+    rc = noalloc_device(&nd);
+    if (rc) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    VerifyParams p{};
+    p.target = target_logits;
+    p.draft = draft_logits;
+    p.tokens = draft_tokens;
+    p.B = B;
+    p.gamma = gamma;
+    p.V = V;
+    p.T = T;
+    p.Td = T_d;
+    p.T_seq = opts ? opts->T_per_seq : nullptr;
+    p.Td_seq = opts ? opts->Td_per_seq : nullptr;
+    p.key = philox_key(seed);
+    p.seq_base = opts ? opts->seq_index_base : 0u;
+    p.out_tokens = out_tokens;
+    p.out_n = out_n_accepted;
+    if (opts) {
+        p.out_logp = opts->out_logp_draft;
+        p.out_logq = opts->out_logq_draft;
+        p.out_logZp = opts->out_logZ_p;
+        p.out_logZq = opts->out_logZ_q;
+        p.out_u = opts->out_u;
+        p.out_race = opts->out_race;
+    }
+    char* ws = nd->scratch;
+    p.piece_len = L.piece_len;
+    p.npieces = L.npieces;
+    p.stat_parts = reinterpret_cast<float2*>(ws + L.stat_off);
+    p.seq = reinterpret_cast<SeqInfo*>(ws + L.seq_off);
+    p.race_parts = reinterpret_cast<RacePart*>(ws + L.race_off);
+    p.tickets = reinterpret_cast<int*>(ws + L.ticket_off);
+    if (opts && opts->d_status) {
+        p.status = opts->d_status;
+    } else {
+        p.status = reinterpret_cast<int32_t*>(ws + kNoallocStatusOff);
+        if (cudaMemsetAsync(p.status, 0, sizeof(int32_t), s) != cudaSuccess) return SPEC_ECUDA;
+    }
+    return dtype == SPEC_F32 ? launch_sampling<F32Elem>(p, nd->sm_count, opts, s)
+                             : launch_sampling<Bf16Elem>(p, nd->sm_count, opts, s);
+}

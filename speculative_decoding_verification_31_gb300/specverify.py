@@ -17,11 +17,13 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libspecverify.so")
 
 SPEC_OK, SPEC_EINVAL, SPEC_ECUDA, SPEC_EBADTOKEN, SPEC_ETIMEOUT, SPEC_ENOMEM = range(6)
+SPEC_ESCRATCH = 6
+SPEC_NOALLOC_SCRATCH_BYTES = 8 << 20
 SPEC_F32, SPEC_BF16 = 0, 1
 
 EXPORTED = ("spec_verify", "spec_verify_greedy", "spec_verify_ex", "spec_verify_greedy_ex",
             "spec_verify_workspace_bytes", "spec_verify_check", "spec_verify_strerror",
-            "spec_verify_opts_init")
+            "spec_verify_opts_init", "spec_verify_noalloc")
 
 
 class SpecVerifyError(RuntimeError):
@@ -68,7 +70,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.spec_verify_greedy.argtypes = [P, P, I, I, I, P, P, P]
     lib.spec_verify_ex.argtypes = [P, P, P, I, I, I, F, F, U64, P, P, OP, P]
     lib.spec_verify_greedy_ex.argtypes = [P, P, I, I, I, P, P, OP, P]
-    for f in ("spec_verify", "spec_verify_greedy", "spec_verify_ex", "spec_verify_greedy_ex"):
+    lib.spec_verify_noalloc.argtypes = [P, P, P, I, I, I, F, F, U64, P, P, OP, P]
+    for f in ("spec_verify", "spec_verify_greedy", "spec_verify_ex", "spec_verify_greedy_ex",
+              "spec_verify_noalloc"):
         getattr(lib, f).restype = ctypes.c_int
     lib.spec_verify_workspace_bytes.argtypes = [I, I, I, I]
     lib.spec_verify_workspace_bytes.restype = ctypes.c_size_t
@@ -241,6 +245,31 @@ def spec_verify_greedy_ex(target_logits, draft_tokens, out_tokens=None, out_n_ac
         ctypes.byref(o), _stream_handle(stream, dev))
     if rc != SPEC_OK:
         raise SpecVerifyError(rc, "spec_verify_greedy_ex")
+    return out_tokens, out_n_accepted
+
+
+def spec_verify_noalloc(target_logits, draft_logits, draft_tokens, T: float, T_d: float,
+                        seed: int, out_tokens, out_n_accepted, *, T_per_seq=None,
+                        Td_per_seq=None, seq_index_base: int = 0, d_status=None, diag=None,
+                        stream=None):
+    """Allocation-free sampling verify (see ``spec_verify_noalloc`` in the C header): the
+    library's scratch is a static device array, so nothing is allocated by the library.  The
+    caller passes every output, including the optional diagnostic tensors in ``diag`` (a dict
+    with the keys of ``spec_verify_ex``'s diagnostics)."""
+    B, g, V = _check_shapes(target_logits, draft_logits, draft_tokens)
+    dev = target_logits.device
+    if out_tokens is None or out_n_accepted is None:
+        raise ValueError("spec_verify_noalloc needs caller-allocated outputs")
+    T_per_seq = _check_temps(T_per_seq, B, dev, "T_per_seq")
+    Td_per_seq = _check_temps(Td_per_seq, B, dev, "Td_per_seq")
+    o = _make_opts(_dtype_code(target_logits), T_per_seq, Td_per_seq, seq_index_base, None,
+                   d_status, diag, None)
+    rc = load_library().spec_verify_noalloc(
+        _ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), B, g, V, float(T),
+        float(T_d), int(seed) & (2**64 - 1), _ptr(out_tokens), _ptr(out_n_accepted),
+        ctypes.byref(o), _stream_handle(stream, dev))
+    if rc != SPEC_OK:
+        raise SpecVerifyError(rc, "spec_verify_noalloc")
     return out_tokens, out_n_accepted
 
 
