@@ -90,8 +90,16 @@ typedef struct {
     float *out_race;            /* [B, 2]       winning race score ln(w(y)/E_y), and the
                                                 runner-up score (approximate) */
     void *prof_events[4];       /* optional cudaEvent_t: recorded before the first kernel and
-                                   after each of the (up to three) kernels of the call */
+                                   after each kernel of the call (the fused sampling path has
+                                   one kernel, the unfused one three, greedy two) */
+    uint32_t debug_flags;       /* SPEC_DEBUG_* bits for tests; 0 in normal use */
 } spec_verify_opts;
+
+/* debug_flags bits (tests only). */
+#define SPEC_DEBUG_UNFUSED 1u    /* sampling: run the three-kernel path instead of the fused one */
+#define SPEC_DEBUG_NEVER_READY 2u /* fused sampling: the race waits on a flag that is never set,
+                                     give up after their bounded wait and report SPEC_ETIMEOUT
+                                     (exercises the timeout path; outputs are then invalid) */
 
 /* Zero every field and set dtype = SPEC_BF16. */
 void spec_verify_opts_init(spec_verify_opts *opts);

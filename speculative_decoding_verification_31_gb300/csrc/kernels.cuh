@@ -26,11 +26,12 @@
 namespace specverify {
 
 // Per-sequence result of the scan, consumed by the race.
-struct SeqInfo {
+struct __align__(16) SeqInfo {
     int j;            // first rejected position (gamma: all accepted), -1: bad draft token
     float mp, l2sp;   // target row raced: scaled max and log2 of the sum
     float mq, l2sq;   // draft row j (residual only)
     float cp, cq;     // log2(e)/T_b, log2(e)/Td_b
+    int pad;
 };
 
 struct RacePart {
@@ -50,6 +51,7 @@ struct VerifyParams {
     const float* T_seq;         // [B] or nullptr
     const float* Td_seq;        // [B] or nullptr
     PhiloxKey key;
+    PhiloxRoundKeys rk;         // round keys of `key`
     uint32_t seq_base;
     // workspace
     float2* stat_parts;         // [B][2*gamma+1][npieces] (m, s) or (value, index) in greedy
@@ -57,6 +59,14 @@ struct VerifyParams {
     RacePart* race_parts;       // [B][npieces]
     int* tickets;               // [B] race arrival counters, zeroed by the scan
     int32_t* status;
+    // fused single-kernel path (zeroed control block, see verify_fused_kernel)
+    float2* row_stat;           // [B][2*gamma+1] merged (scaled max, log2 sum) per row
+    int* row_done;              // [B][2*gamma+1] arrivals of row pieces
+    int* seq_done;              // [B] rows completed
+    int* ready;                 // [B] 1 once the sequence's scan has been published
+    int* race_cursor;           // race items claimed so far (item c: sequence c / P, piece c % P)
+    int* row_cursor;            // row items claimed so far (sequence-major order)
+    uint32_t debug_flags;       // kDebug* test switches
     // outputs
     int32_t* out_tokens;        // [B, gamma+1]
     int32_t* out_n;             // [B]
@@ -67,6 +77,17 @@ struct VerifyParams {
     float* out_u;
     float* out_race;
 };
+
+// (m, s) pairs travel as one naturally aligned 64-bit word.  The fused path pre-fills them
+// with kStatEmpty (two NaN halves, never a real pair) and polls until a pair is written,
+// which needs no memory fence on the writer's side.
+constexpr unsigned long long kStatEmpty = 0xFFFFFFFFFFFFFFFFull;
+
+__device__ __forceinline__ void store_stat(float2* dst, float m, float s) {
+    const unsigned long long v = (static_cast<unsigned long long>(__float_as_uint(s)) << 32) |
+                                 __float_as_uint(m);
+    *reinterpret_cast<unsigned long long*>(dst) = v;
+}
 
 __device__ __forceinline__ float seq_T(const VerifyParams& p, int b) {
     return p.T_seq ? p.T_seq[b] : p.T;
@@ -137,9 +158,32 @@ __device__ __forceinline__ SoftmaxStat stats_piece(const typename ET::storage* r
     return warp_merge_stat(st);
 }
 
+// Row r of sequence b: target row r (r <= gamma, scale log2(e)/T_b) or draft row
+// r - gamma - 1 (scale log2(e)/Td_b).  Writes the piece's partial statistics.
+template <class ET, int U>
+__device__ __forceinline__ void row_stats_item(const VerifyParams& p, int b, int r, int piece,
+                                               int lane) {
+    using S = typename ET::storage;
+    const S* row;
+    float c;
+    if (r <= p.gamma) {
+        row = static_cast<const S*>(p.target) + (static_cast<long long>(b) * (p.gamma + 1) + r) * p.V;
+        c = scale_of(seq_T(p, b));
+    } else {
+        row = static_cast<const S*>(p.draft) +
+              (static_cast<long long>(b) * p.gamma + (r - p.gamma - 1)) * p.V;
+        c = scale_of(seq_Td(p, b));
+    }
+    const int x0 = piece * p.piece_len;
+    const int x1 = min(p.V, x0 + p.piece_len);
+    const SoftmaxStat st = stats_piece<ET, U>(row, x0, x1, c, lane);
+    const int R = 2 * p.gamma + 1;
+    if (lane == 0)  // one aligned 64-bit store: readers see both halves or neither
+        store_stat(p.stat_parts + (static_cast<long long>(b) * R + r) * p.npieces + piece, st.m, st.s);
+}
+
 template <class ET, int U>
 __global__ void __launch_bounds__(256) row_stats_kernel(VerifyParams p) {
-    using S = typename ET::storage;
     const int lane = threadIdx.x & 31;
     const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
     const int R = 2 * p.gamma + 1;
@@ -148,22 +192,7 @@ __global__ void __launch_bounds__(256) row_stats_kernel(VerifyParams p) {
          item < total; item += nwarps) {
         const int piece = static_cast<int>(item % p.npieces);
         const long long br = item / p.npieces;
-        const int r = static_cast<int>(br % R);
-        const int b = static_cast<int>(br / R);
-        const S* row;
-        float c;
-        if (r <= p.gamma) {
-            row = static_cast<const S*>(p.target) + (static_cast<long long>(b) * (p.gamma + 1) + r) * p.V;
-            c = scale_of(seq_T(p, b));
-        } else {
-            row = static_cast<const S*>(p.draft) +
-                  (static_cast<long long>(b) * p.gamma + (r - p.gamma - 1)) * p.V;
-            c = scale_of(seq_Td(p, b));
-        }
-        const int x0 = piece * p.piece_len;
-        const int x1 = min(p.V, x0 + p.piece_len);
-        const SoftmaxStat st = stats_piece<ET, U>(row, x0, x1, c, lane);
-        if (lane == 0) p.stat_parts[item] = make_float2(st.m, st.s);
+        row_stats_item<ET, U>(p, static_cast<int>(br / R), static_cast<int>(br % R), piece, lane);
     }
 }
 
@@ -435,115 +464,471 @@ __device__ __forceinline__ float race_log_weight(float xt, float xd, const SeqIn
     return l2p * kLn2 + logf(-expm1f((l2q - l2p) * kLn2));
 }
 
+// Orderable integer image of a float (for a warp max with redux.sync).
+__device__ __forceinline__ uint32_t float_order(float f) {
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float float_unorder(uint32_t u) {
+    return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
+}
+
+__device__ __forceinline__ float lg2_fast(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Exact fp32 race score ln w(x) - ln E_x of one token (-inf when its weight is zero).  Kept
+// out of line: the filter below calls it for a handful of tokens per row.
+__device__ __noinline__ float race_exact_score(float xt, float xd, SeqInfo si, bool residual,
+                                               uint32_t w) {
+    const float lw = race_log_weight(xt, xd, si, residual);
+    return lw > -INFINITY ? lw - race_log_exponential(w) : -INFINITY;
+}
+
+// A token can win only if its score reaches the best exact score so far.  Its score is at
+// most ln p(x) - ln U_x: the weight max(0, p - q) never exceeds p, and E = -log1p(-U) >= U.
+// With U_x >= w 2^-32 the test  log2(w) <= log2 p(x) + 32 - best/ln2 + margin  is a
+// necessary condition (w = 0 always passes), and costs one FFMA, one I2F and one lg2.approx.
+// The margin (in log2 units) is far above the fp32 error of the exact score.
+constexpr float kRaceBoundMargin2 = 1e-3f;
+
+// Race over tokens [x0, x1) of the raced row; every lane offers its tokens in increasing x.
+// The residual's draft row is read only at candidate tokens.
 template <class ET>
 __device__ __forceinline__ RaceState race_piece(const typename ET::storage* rt,
                                                 const typename ET::storage* rd, int x0, int x1,
-                                                const SeqInfo& si, bool residual, PhiloxKey key,
-                                                uint32_t bg, uint32_t pos, int lane) {
+                                                const SeqInfo& si, bool residual,
+                                                const PhiloxRoundKeys& rk, uint32_t bg,
+                                                uint32_t pos, int lane) {
     RaceState st{-INFINITY, INT_MAX, -INFINITY};
     const RowSpan<ET> sp(rt, x0, x1);
-    // The vector path needs the residual's draft row to share the target row's alignment
-    // and Philox blocks of four tokens to start on a vector boundary.
-    const bool vec_ok =
-        ((x0 + sp.head) & 3) == 0 &&
-        (!residual || ((reinterpret_cast<uintptr_t>(rd + x0) & 15u) ==
-                       (reinterpret_cast<uintptr_t>(rt + x0) & 15u)));
-    auto scalar = [&](int x) {
-        const float xt = ET::load1(rt + x);
-        const float xd = residual ? ET::load1(rd + x) : 0.0f;
-        const float lw = race_log_weight(xt, xd, si, residual);
-        if (lw > -INFINITY) {
-            const uint4 blk = race_block(key, bg, pos, static_cast<uint32_t>(x) >> 2);
-            race_offer(st, lw - race_log_exponential(word_of(blk, static_cast<uint32_t>(x) & 3u)), x);
-        }
+    const RaceRowRng q = race_row_rng(rk, bg, pos);
+    auto word_at = [&](int x) {
+        const uint4 blk = race_block_fast(q, rk, static_cast<uint32_t>(x) >> 2);
+        return word_of(blk, static_cast<uint32_t>(x) & 3u);
     };
-    if (!vec_ok) {
-        for (int x = x0 + lane; x < x1; x += 32) scalar(x);  // (lane order is still increasing)
+    auto offer_exact = [&](float xt, int x, uint32_t w) {
+        const float xd = residual ? ET::load1(rd + x) : 0.0f;
+        const float s = race_exact_score(xt, xd, si, residual, w);
+        if (s > -INFINITY) race_offer(st, s, x);
+    };
+    // Vector path: Philox blocks of four tokens must start on a vector boundary.
+    if (((x0 + sp.head) & 3) != 0) {
+        for (int x = x0 + lane; x < x1; x += 32) offer_exact(ET::load1(rt + x), x, word_at(x));
         return warp_race_merge(st);
     }
-    if (lane < sp.head) scalar(x0 + lane);
+    if (lane < sp.head) offer_exact(ET::load1(sp.base + lane), x0 + lane, word_at(x0 + lane));
     const int xb = x0 + sp.head;
     const uint4* vt = sp.vec();
-    const uint4* vd = residual ? reinterpret_cast<const uint4*>(rd + xb) : nullptr;
-    for (int v = lane; v < sp.nvec; v += 32) {
-        float ft[ET::kVec], fd[ET::kVec];
-        ET::widen(__ldg(vt + v), ft);
-        if (residual) ET::widen(__ldg(vd + v), fd);
-        const int xv = xb + v * ET::kVec;
+    // Seed the threshold: each lane finds its largest target logit (a cheap pass, no random
+    // numbers) and scores that token exactly.  Any token's score is at most the final best,
+    // and a lane's most likely token is usually close to it, so few tokens pass the filter.
+    // Loads are issued kSeedBatch vectors at a time; the second pass finds the piece in L1.
+    constexpr int kSeedBatch = 8;
+    constexpr int kRaceBatch = 2;
+    float seed = -INFINITY;
+    {
+        float vmax = -INFINITY;
+        int xs = -1;
+        for (int v0 = 0; v0 < sp.nvec; v0 += 32 * kSeedBatch) {
+            uint4 raw[kSeedBatch];
 #pragma unroll
-        for (int g = 0; g < ET::kVec / 4; ++g) {
-            float lw[4];
-            bool any = false;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                lw[e] = race_log_weight(ft[4 * g + e], residual ? fd[4 * g + e] : 0.0f, si, residual);
-                any |= lw[e] > -INFINITY;
+            for (int k = 0; k < kSeedBatch; ++k) {
+                const int v = v0 + lane + 32 * k;
+                raw[k] = v < sp.nvec ? __ldg(vt + v)
+                                     : make_uint4(ET::kNegInfWord, ET::kNegInfWord,
+                                                  ET::kNegInfWord, ET::kNegInfWord);
             }
-            if (any) {
-                const uint4 blk = race_block(key, bg, pos, static_cast<uint32_t>(xv + 4 * g) >> 2);
-                const uint32_t w4[4] = {blk.x, blk.y, blk.z, blk.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    if (lw[e] > -INFINITY)
-                        race_offer(st, lw[e] - race_log_exponential(w4[e]), xv + 4 * g + e);
+            for (int k = 0; k < kSeedBatch; ++k) {
+                float ft[ET::kVec];
+                ET::widen(raw[k], ft);
+                float m = ft[0];
+#pragma unroll
+                for (int e = 1; e < ET::kVec; ++e) m = fmaxf(m, ft[e]);
+                if (m > vmax) {
+                    vmax = m;
+#pragma unroll
+                    for (int e = ET::kVec - 1; e >= 0; --e)
+                        if (ft[e] == m) xs = xb + (v0 + lane + 32 * k) * ET::kVec + e;
+                }
             }
         }
+        if (xs >= 0) {
+            const float xd = residual ? ET::load1(rd + xs) : 0.0f;
+            seed = race_exact_score(ET::load1(rt + xs), xd, si, residual, word_at(xs));
+        }
+    }
+    float thr = float_unorder(__reduce_max_sync(0xffffffffu, float_order(fmaxf(seed, st.best))));
+    const float mpl = si.mp + si.l2sp;
+    for (int v0 = 0; v0 < sp.nvec; v0 += 32 * kRaceBatch) {
+        // rhs(x) = log2 p(x) + 32 - thr/ln2 + margin, as one FFMA per token
+        const float C = (thr > -INFINITY) ? 32.0f + kRaceBoundMargin2 - thr * kLog2e - mpl
+                                          : INFINITY;
+        uint4 raw[kRaceBatch];
+#pragma unroll
+        for (int k = 0; k < kRaceBatch; ++k) {
+            const int v = v0 + lane + 32 * k;
+            raw[k] = v < sp.nvec ? __ldg(vt + v) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        uint4 blk[kRaceBatch][ET::kVec / 4];
+#pragma unroll
+        for (int k = 0; k < kRaceBatch; ++k)
+#pragma unroll
+            for (int g = 0; g < ET::kVec / 4; ++g)
+                blk[k][g] = race_block_fast(
+                    q, rk, static_cast<uint32_t>(xb + (v0 + lane + 32 * k) * ET::kVec + 4 * g) >> 2);
+        // candidate bits: token e of vector k passes the bound
+        uint32_t cand = 0;
+#pragma unroll
+        for (int k = 0; k < kRaceBatch; ++k) {
+            const int v = v0 + lane + 32 * k;
+            float ft[ET::kVec];
+            ET::widen(raw[k], ft);
+#pragma unroll
+            for (int g = 0; g < ET::kVec / 4; ++g) {
+                const uint32_t w4[4] = {blk[k][g].x, blk[k][g].y, blk[k][g].z, blk[k][g].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const bool pass = lg2_fast(static_cast<float>(w4[e])) <= fmaf(ft[4 * g + e], si.cp, C);
+                    cand |= (pass && v < sp.nvec) ? (1u << (k * ET::kVec + 4 * g + e)) : 0u;
+                }
+            }
+        }
+        while (cand) {  // rare: score the candidates exactly, in increasing token order
+            const int bit = __ffs(cand) - 1;
+            cand &= cand - 1;
+            const int k = bit / ET::kVec, e = bit % ET::kVec;
+            const int x = xb + (v0 + lane + 32 * k) * ET::kVec + e;
+            offer_exact(ET::load1(rt + x), x, word_at(x));  // recomputed: no indexed registers
+        }
+        thr = fmaxf(thr, float_unorder(__reduce_max_sync(0xffffffffu, float_order(st.best))));
     }
     const int t0 = sp.head + sp.nvec * ET::kVec;
-    if (lane < sp.tail) scalar(x0 + t0 + lane);
+    if (lane < sp.tail) offer_exact(ET::load1(sp.base + t0 + lane), x0 + t0 + lane, word_at(x0 + t0 + lane));
     return warp_race_merge(st);
 }
 
+// One race piece of sequence b (whose scan result is `si`): race the piece, publish the
+// partial winner, and if this is the sequence's last piece merge all pieces and write the
+// token.  Arrivals are counted, never waited for.
 template <class ET>
-__global__ void __launch_bounds__(256) race_kernel(VerifyParams p) {
+__device__ __forceinline__ void race_item(const VerifyParams& p, int b, int piece, const SeqInfo& si,
+                                          int lane) {
     using S = typename ET::storage;
+    if (si.j < 0) return;  // bad draft token: nothing to draw
+    const bool residual = si.j < p.gamma;
+    const S* rt = static_cast<const S*>(p.target) + (static_cast<long long>(b) * (p.gamma + 1) + si.j) * p.V;
+    const S* rd = residual ? static_cast<const S*>(p.draft) + (static_cast<long long>(b) * p.gamma + si.j) * p.V
+                           : nullptr;
+    const uint32_t bg = p.seq_base + static_cast<uint32_t>(b);
+    const int x0 = piece * p.piece_len;
+    const int x1 = min(p.V, x0 + p.piece_len);
+    const RaceState st = race_piece<ET>(rt, rd, x0, x1, si, residual, p.rk, bg,
+                                        static_cast<uint32_t>(si.j), lane);
+    const long long item = static_cast<long long>(b) * p.npieces + piece;
+    if (lane == 0) {
+        p.race_parts[item] = RacePart{st.best, st.idx, st.second, 0};
+        __threadfence();
+    }
+    int ticket = 0;
+    if (lane == 0) ticket = atomicAdd(p.tickets + b, 1);
+    ticket = __shfl_sync(0xffffffffu, ticket, 0);
+    if (ticket != p.npieces - 1) return;
+    // Last piece of this sequence: merge every piece's winner (read through L2).
+    __threadfence();
+    RaceState m{-INFINITY, INT_MAX, -INFINITY};
+    for (int k = lane; k < p.npieces; k += 32) {
+        const RacePart* rp = p.race_parts + static_cast<long long>(b) * p.npieces + k;
+        const float4 raw = __ldcg(reinterpret_cast<const float4*>(rp));
+        m = race_merge(m, RaceState{raw.x, __float_as_int(raw.y), raw.z});
+    }
+    m = warp_race_merge(m);
+    if (m.idx == INT_MAX) {
+        // Every residual weight was zero (p <= q everywhere in fp32): draw from p_j.
+        m = race_piece<ET>(rt, nullptr, 0, p.V, si, false, p.rk, bg, static_cast<uint32_t>(si.j),
+                           lane);
+    }
+    if (lane == 0) {
+        p.out_tokens[static_cast<long long>(b) * (p.gamma + 1) + si.j] = m.idx;
+        if (p.out_race) {
+            p.out_race[2 * b] = m.best;
+            p.out_race[2 * b + 1] = m.second;
+        }
+    }
+}
+
+template <class ET>
+__global__ void __launch_bounds__(256, 4) race_kernel(VerifyParams p) {
     const int lane = threadIdx.x & 31;
     const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
     const long long total = static_cast<long long>(p.B) * p.npieces;
     for (long long item = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
          item < total; item += nwarps) {
         const int b = static_cast<int>(item / p.npieces);
-        const int piece = static_cast<int>(item % p.npieces);
-        const SeqInfo si = p.seq[b];
-        if (si.j < 0) continue;  // bad draft token: nothing to draw
-        const bool residual = si.j < p.gamma;
-        const S* rt = static_cast<const S*>(p.target) + (static_cast<long long>(b) * (p.gamma + 1) + si.j) * p.V;
-        const S* rd = residual ? static_cast<const S*>(p.draft) + (static_cast<long long>(b) * p.gamma + si.j) * p.V
-                               : nullptr;
-        const uint32_t bg = p.seq_base + static_cast<uint32_t>(b);
-        const int x0 = piece * p.piece_len;
-        const int x1 = min(p.V, x0 + p.piece_len);
-        const RaceState st = race_piece<ET>(rt, rd, x0, x1, si, residual, p.key, bg,
-                                            static_cast<uint32_t>(si.j), lane);
-        if (lane == 0) {
-            p.race_parts[item] = RacePart{st.best, st.idx, st.second, 0};
-            __threadfence();
+        race_item<ET>(p, b, static_cast<int>(item % p.npieces), p.seq[b], lane);
+    }
+}
+
+// ----------------------------------------------------------------------------------------
+// verify_fused: the whole sampling verify in one persistent (cooperative) launch, with
+// specialised warps.
+//
+// Streaming warps (the first kStreamWarps of each block) claim row items (b, r, piece) in
+// sequence-major order from row_cursor and never wait: each writes its piece's partial
+// statistics and counts its arrival on the row without a fence (partials are pre-filled
+// with an empty marker that the reader polls for).  The last piece of a row to arrive merges
+// the row; the last row of a sequence to be merged runs the sequence's scan (one warp) and
+// sets ready[b].  Race warps (the rest of each block) claim race items (b, piece) in
+// sequence order from race_cursor, wait (bounded) for ready[b], and race one piece of the
+// raced row while it is still in L2; streaming warps join them when the rows run out.  A
+// warp that waits holds no row item, and every scan is finished by a warp that never waits,
+// so the waits end.  The arrival count of a row item is resolved one item later, so the
+// atomic's round trip overlaps the next item's loads.  Every wait gives up after
+// kWaitLimitNs and records SPEC_ETIMEOUT.
+// ----------------------------------------------------------------------------------------
+
+#ifndef SPECVERIFY_STREAM_WARPS
+#define SPECVERIFY_STREAM_WARPS 7
+#endif
+#ifndef SPECVERIFY_FUSED_MINBLOCKS
+#define SPECVERIFY_FUSED_MINBLOCKS 4
+#endif
+constexpr int kStreamWarps = SPECVERIFY_STREAM_WARPS;  // of the 8 warps of a block (the rest race)
+
+constexpr uint32_t kDebugNeverReady = 1u;         // scans never set ready[b] (tests)
+constexpr unsigned long long kWaitLimitNs = 500000000ull;  // give up a wait after 0.5 s
+
+__device__ __forceinline__ unsigned long long global_time_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ int ld_relaxed(const int* p) {
+    int v;
+    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release(int* p, int v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const void* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Wait (bounded) until a pre-filled (m, s) word has been written; returns it.  On giving up
+// it records SPEC_ETIMEOUT and returns an empty pair.
+__device__ __forceinline__ float2 wait_stat(const VerifyParams& p, const float2* src) {
+    unsigned long long v = ld_relaxed_u64(src);
+    if (v == kStatEmpty) {
+        const unsigned long long t0 = global_time_ns();
+        while ((v = ld_relaxed_u64(src)) == kStatEmpty) {
+            if (global_time_ns() - t0 > kWaitLimitNs) {
+                set_status(p.status, 4 /* SPEC_ETIMEOUT */);
+                return make_float2(-FLT_MAX, 0.0f);
+            }
+            __nanosleep(64);
         }
-        int ticket = 0;
-        if (lane == 0) ticket = atomicAdd(p.tickets + b, 1);
-        ticket = __shfl_sync(0xffffffffu, ticket, 0);
-        if (ticket != p.npieces - 1) continue;
-        // Last piece of this sequence: merge every piece's winner (read through L2).
-        __threadfence();
-        RaceState m{-INFINITY, INT_MAX, -INFINITY};
-        for (int k = lane; k < p.npieces; k += 32) {
-            const RacePart* rp = p.race_parts + static_cast<long long>(b) * p.npieces + k;
-            const float4 raw = __ldcg(reinterpret_cast<const float4*>(rp));
-            m = race_merge(m, RaceState{raw.x, __float_as_int(raw.y), raw.z});
+    }
+    return make_float2(__uint_as_float(static_cast<uint32_t>(v)),
+                       __uint_as_float(static_cast<uint32_t>(v >> 32)));
+}
+
+// One warp: merge a row's partials (after the row's last piece arrived; each partial is
+// waited for, since arrivals are counted without a fence).
+__device__ __forceinline__ void merge_row_warp(const VerifyParams& p, int b, int r, int lane) {
+    const int R = 2 * p.gamma + 1;
+    SoftmaxStat st{-FLT_MAX, 0.0f};
+    const float2* parts = p.stat_parts + (static_cast<long long>(b) * R + r) * p.npieces;
+    for (int k = lane; k < p.npieces; k += 32) {
+        const float2 q = wait_stat(p, parts + k);
+        st = merge_stat(st, SoftmaxStat{q.x, q.y});
+    }
+    st = warp_merge_stat(st);
+    if (lane == 0) {
+        const float l2s = log2f(st.s);
+        store_stat(p.row_stat + static_cast<long long>(b) * R + r, st.m, l2s);
+        const float lz = (st.m + l2s) * kLn2;
+        if (r <= p.gamma) {
+            if (p.out_logZp) p.out_logZp[static_cast<long long>(b) * (p.gamma + 1) + r] = lz;
+        } else if (p.out_logZq) {
+            p.out_logZq[static_cast<long long>(b) * p.gamma + (r - p.gamma - 1)] = lz;
         }
-        m = warp_race_merge(m);
-        if (m.idx == INT_MAX) {
-            // Every residual weight was zero (p <= q everywhere in fp32): draw from p_j.
-            m = race_piece<ET>(rt, nullptr, 0, p.V, si, false, p.key, bg,
-                               static_cast<uint32_t>(si.j), lane);
-        }
-        if (lane == 0) {
-            p.out_tokens[static_cast<long long>(b) * (p.gamma + 1) + si.j] = m.idx;
-            if (p.out_race) {
-                p.out_race[2 * b] = m.best;
-                p.out_race[2 * b + 1] = m.second;
+    }
+}
+
+// One warp: the scan of sequence b (after its rows are merged); publishes the sequence.
+template <class ET>
+__device__ __forceinline__ void scan_sequence_warp(const VerifyParams& p, int b, int lane) {
+    using S = typename ET::storage;
+    const int R = 2 * p.gamma + 1;
+    const float2* rs = p.row_stat + static_cast<long long>(b) * R;
+    const float Tb = seq_T(p, b), Tdb = seq_Td(p, b);
+    const float cp = scale_of(Tb), cq = scale_of(Tdb);
+    const uint32_t bg = p.seq_base + static_cast<uint32_t>(b);
+    int j = p.gamma;
+    bool bad = false;
+    for (int i0 = 0; i0 < p.gamma; i0 += 32) {
+        const int i = i0 + lane;
+        bool reject = false;
+        if (i < p.gamma) {
+            const int d = p.tokens[static_cast<long long>(b) * p.gamma + i];
+            const float u = accept_uniform(p.key, bg, static_cast<uint32_t>(i));
+            const long long k = static_cast<long long>(b) * p.gamma + i;
+            if (p.out_u) p.out_u[k] = u;
+            if (d < 0 || d >= p.V) {
+                bad = true;
+                if (p.out_logp) p.out_logp[k] = NAN;
+                if (p.out_logq) p.out_logq[k] = NAN;
+            } else {
+                const float2 sp = wait_stat(p, rs + i), sq = wait_stat(p, rs + p.gamma + 1 + i);
+                const float xt = ET::load1(static_cast<const S*>(p.target) +
+                                           (static_cast<long long>(b) * (p.gamma + 1) + i) * p.V + d);
+                const float xd = ET::load1(static_cast<const S*>(p.draft) +
+                                           (static_cast<long long>(b) * p.gamma + i) * p.V + d);
+                const float l2p = fmaf(xt, cp, -sp.x) - sp.y;
+                const float l2q = fmaf(xd, cq, -sq.x) - sq.y;
+                if (p.out_logp) p.out_logp[k] = l2p * kLn2;
+                if (p.out_logq) p.out_logq[k] = l2q * kLn2;
+                // accept iff u < min(1, p/q); p(d) = 0 rejects, q(d) = 0 < p(d) accepts
+                reject = !((l2p > -INFINITY) && (u < exp2f(l2p - l2q)));
             }
         }
+        const uint32_t rej = __ballot_sync(0xffffffffu, reject);
+        if (rej && j == p.gamma) j = i0 + __ffs(rej) - 1;
+    }
+    bad = __any_sync(0xffffffffu, bad);
+    if (bad) j = -1;
+    if (lane == 0) {
+        p.out_n[b] = j;
+        SeqInfo si;
+        si.j = j;
+        si.cp = cp;
+        si.cq = cq;
+        const int rr = (j >= 0) ? j : 0;
+        const float2 sp = wait_stat(p, rs + rr);
+        si.mp = sp.x;
+        si.l2sp = sp.y;
+        if (j >= 0 && j < p.gamma) {
+            const float2 sq = wait_stat(p, rs + p.gamma + 1 + j);
+            si.mq = sq.x;
+            si.l2sq = sq.y;
+        } else {
+            si.mq = 0.0f;
+            si.l2sq = 0.0f;
+        }
+        si.pad = 0;
+        p.seq[b] = si;
+        if (j < 0) set_status(p.status, 3 /* SPEC_EBADTOKEN */);
+    }
+    int32_t* out = p.out_tokens + static_cast<long long>(b) * (p.gamma + 1);
+    for (int t = lane; t <= p.gamma; t += 32)
+        out[t] = (j >= 0 && t < j) ? p.tokens[static_cast<long long>(b) * p.gamma + t] : -1;
+    if (lane == 0) {
+        __threadfence();
+        if (!(p.debug_flags & kDebugNeverReady)) st_release(p.ready + b, 1);
+    }
+}
+
+// Race piece `piece` of sequence b (claimed): wait (bounded) for the sequence's scan, then race.
+template <class ET>
+__device__ __forceinline__ void run_claimed_race(const VerifyParams& p, int b, int piece, int lane) {
+    int ok = 0;
+    if (lane == 0) {
+        const unsigned long long t0 = global_time_ns();
+        while (!(ok = ld_acquire(p.ready + b))) {
+            if (global_time_ns() - t0 > kWaitLimitNs) break;
+            __nanosleep(500);
+        }
+        if (!ok) set_status(p.status, 4 /* SPEC_ETIMEOUT */);
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();  // order the other lanes' reads after lane 0's acquire
+    if (!ok) return;
+    SeqInfo si;
+    {
+        const int4 a = __ldcg(reinterpret_cast<const int4*>(p.seq + b));
+        const float4 q = __ldcg(reinterpret_cast<const float4*>(p.seq + b) + 1);
+        si.j = a.x;
+        si.mp = __int_as_float(a.y);
+        si.l2sp = __int_as_float(a.z);
+        si.mq = __int_as_float(a.w);
+        si.l2sq = q.x;
+        si.cp = q.y;
+        si.cq = q.z;
+        si.pad = 0;
+    }
+    race_item<ET>(p, b, piece, si, lane);
+}
+
+// Resolve a row piece's arrival (ticket from the row counter): the last piece merges the row
+// and the last row runs the scan.
+template <class ET>
+__device__ __forceinline__ void resolve_arrival(const VerifyParams& p, int ticket, int b, int r,
+                                                int lane) {
+    const int R = 2 * p.gamma + 1;
+    if (ticket != p.npieces - 1) return;
+    merge_row_warp(p, b, r, lane);
+    int t = 0;
+    if (lane == 0) t = atomicAdd(p.seq_done + b, 1);
+    t = __shfl_sync(0xffffffffu, t, 0);
+    if (t != R - 1) return;
+    scan_sequence_warp<ET>(p, b, lane);
+}
+
+template <class ET, int U>
+__global__ void __launch_bounds__(256, SPECVERIFY_FUSED_MINBLOCKS) verify_fused_kernel(VerifyParams p) {
+    const int lane = threadIdx.x & 31;
+    const int R = 2 * p.gamma + 1;
+    const int P = p.npieces;
+    const int RP = R * P;
+    const long long total_rows = static_cast<long long>(p.B) * RP;
+    if ((threadIdx.x >> 5) < kStreamWarps) {
+        // pending arrival of the previous row item (lane 0 holds the ticket)
+        int pend_ticket = 0, pend_b = -1, pend_r = 0;
+        long long next = 0;
+        if (lane == 0) next = atomicAdd(reinterpret_cast<unsigned long long*>(p.row_cursor), 1ull);
+        next = __shfl_sync(0xffffffffu, next, 0);
+        while (next < total_rows) {
+            const long long g = next;
+            if (lane == 0)  // the next claim, used after this item
+                next = atomicAdd(reinterpret_cast<unsigned long long*>(p.row_cursor), 1ull);
+            const int b = static_cast<int>(g / RP);
+            const int within = static_cast<int>(g % RP);
+            const int r = within / P;
+            row_stats_item<ET, U>(p, b, r, within % P, lane);
+            if (pend_b >= 0)
+                resolve_arrival<ET>(p, __shfl_sync(0xffffffffu, pend_ticket, 0), pend_b, pend_r, lane);
+            if (lane == 0)
+                pend_ticket = atomicAdd(p.row_done + static_cast<long long>(b) * R + r, 1);
+            pend_b = b;
+            pend_r = r;
+            next = __shfl_sync(0xffffffffu, next, 0);
+        }
+        if (pend_b >= 0)
+            resolve_arrival<ET>(p, __shfl_sync(0xffffffffu, pend_ticket, 0), pend_b, pend_r, lane);
+    }
+    // race items, in sequence order
+    const long long total_race = static_cast<long long>(p.B) * P;
+    while (true) {
+        long long c = 0;
+        if (lane == 0) c = atomicAdd(reinterpret_cast<unsigned long long*>(p.race_cursor), 1ull);
+        c = __shfl_sync(0xffffffffu, c, 0);
+        if (c >= total_race) break;
+        run_claimed_race<ET>(p, static_cast<int>(c / P), static_cast<int>(c % P), lane);
     }
 }
 

@@ -42,6 +42,70 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, PhiloxKey key) {
     return c;
 }
 
+// Round keys of one launch: key k_r = key + r * (Weyl increment), r = 0..9.  Passed in the
+// kernel parameters so that every round reads its key as a constant operand.
+struct PhiloxRoundKeys {
+    uint32_t k0[10], k1[10];
+};
+
+__host__ __device__ __forceinline__ PhiloxRoundKeys philox_round_keys(PhiloxKey key) {
+    PhiloxRoundKeys rk;
+    for (int r = 0; r < 10; ++r) {
+        rk.k0[r] = key.k0 + static_cast<uint32_t>(r) * 0x9E3779B9u;
+        rk.k1[r] = key.k1 + static_cast<uint32_t>(r) * 0xBB67AE85u;
+    }
+    return rk;
+}
+
+// One 32x32 -> 64-bit product (a single wide multiply) split into its halves.
+__device__ __forceinline__ void mul_wide(uint32_t a, uint32_t b, uint32_t& hi, uint32_t& lo) {
+    const unsigned long long p = static_cast<unsigned long long>(a) * b;
+    hi = static_cast<uint32_t>(p >> 32);
+    lo = static_cast<uint32_t>(p);
+}
+
+__device__ __forceinline__ void philox_round(uint4& c, uint32_t k0, uint32_t k1) {
+    uint32_t hi0, lo0, hi1, lo1;
+    mul_wide(0xD2511F53u, c.x, hi0, lo0);
+    mul_wide(0xCD9E8D57u, c.z, hi1, lo1);
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+}
+
+// The race counters of one row, (k, r, b, 1), differ only in word 0.  Of the first round's
+// two products, the one of word 2 (= b) is then the same for every k, and so is the second
+// round's product of word 0; both are computed once per row.
+struct RaceRowRng {
+    uint32_t c0_1, c1_1;    // words 0 and 1 after round 1
+    uint32_t hi_2, lo_2;    // 0xD2511F53 * c0_1 (round 2)
+};
+
+__device__ __forceinline__ RaceRowRng race_row_rng(const PhiloxRoundKeys& rk, uint32_t b,
+                                                   uint32_t r) {
+    RaceRowRng q;
+    q.c0_1 = __umulhi(0xCD9E8D57u, b) ^ r ^ rk.k0[0];
+    q.c1_1 = 0xCD9E8D57u * b;
+    q.hi_2 = __umulhi(0xD2511F53u, q.c0_1);
+    q.lo_2 = 0xD2511F53u * q.c0_1;
+    return q;
+}
+
+// Philox4x32-10 of counter (k, r, b, 1): the same four words as race_block(), with the
+// per-row parts of rounds 1 and 2 taken from `q`.
+__device__ __forceinline__ uint4 race_block_fast(const RaceRowRng& q, const PhiloxRoundKeys& rk,
+                                                 uint32_t k) {
+    // round 1
+    uint32_t h, c3;
+    mul_wide(0xD2511F53u, k, h, c3);
+    const uint32_t c2 = h ^ 1u ^ rk.k1[0];
+    // round 2
+    uint32_t h2, l2;
+    mul_wide(0xCD9E8D57u, c2, h2, l2);
+    uint4 c = make_uint4(h2 ^ q.c1_1 ^ rk.k0[1], l2, q.hi_2 ^ c3 ^ rk.k1[1], q.lo_2);
+#pragma unroll
+    for (int round = 2; round < 10; ++round) philox_round(c, rk.k0[round], rk.k1[round]);
+    return c;
+}
+
 // Acceptance uniform u in [0, 1) with 24 random bits.
 __device__ __forceinline__ float accept_uniform(PhiloxKey key, uint32_t b, uint32_t i) {
     const uint4 w = philox4x32_10(make_uint4(0u, i, b, 0u), key);

@@ -16,9 +16,16 @@ using namespace specverify;
 namespace {
 
 constexpr int kMaxGamma = 2048;          // the scan keeps 2*gamma+1 row statistics in shared memory
-constexpr int kPieceBytes = 8192;        // bytes of one row piece (one warp item)
+#ifndef SPECVERIFY_PIECE_BYTES
+#define SPECVERIFY_PIECE_BYTES 16384
+#endif
+constexpr int kPieceBytes = SPECVERIFY_PIECE_BYTES;  // bytes of one row piece (one warp item)
 constexpr int kThreads = 256;
 constexpr int kUnroll = 4;               // 16-byte loads in flight per lane in the streaming pass
+#ifndef SPECVERIFY_FUSED_UNROLL
+#define SPECVERIFY_FUSED_UNROLL 4
+#endif
+constexpr int kFusedUnroll = SPECVERIFY_FUSED_UNROLL;
 constexpr int kMaxDevices = 64;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -27,7 +34,11 @@ int elem_bytes(int dtype) { return dtype == SPEC_F32 ? 4 : 2; }
 
 struct Layout {
     int piece_len, npieces;
-    size_t stat_off, seq_off, race_off, ticket_off, total;
+    size_t stat_off, seq_off, race_off, rowstat_off;
+    size_t ctl_off, ctl_bytes;          // zeroed control block: row_done, seq_done, tickets, ready
+    size_t row_done_off, seq_done_off, ticket_off, ready_off, race_cursor_off,
+        row_cursor_off;
+    size_t total;
 };
 
 Layout layout_of(int B, int gamma, int V, int dtype) {
@@ -42,8 +53,24 @@ Layout layout_of(int B, int gamma, int V, int dtype) {
     off = align_up(off + static_cast<size_t>(B) * sizeof(SeqInfo), 256);
     L.race_off = off;
     off = align_up(off + static_cast<size_t>(B) * L.npieces * sizeof(RacePart), 256);
+    L.rowstat_off = off;
+    off = align_up(off + static_cast<size_t>(B) * R * sizeof(float2), 256);
+    L.ctl_off = off;
+    L.row_done_off = off;
+    off += static_cast<size_t>(B) * R * sizeof(int);
+    L.seq_done_off = off;
+    off += static_cast<size_t>(B) * sizeof(int);
     L.ticket_off = off;
-    off = align_up(off + static_cast<size_t>(B) * sizeof(int), 256);
+    off += static_cast<size_t>(B) * sizeof(int);
+    L.ready_off = off;
+    off += static_cast<size_t>(B) * sizeof(int);
+    off = align_up(off, 8);
+    L.race_cursor_off = off;
+    off += sizeof(unsigned long long);
+    L.row_cursor_off = off;
+    off += sizeof(unsigned long long);
+    L.ctl_bytes = off - L.ctl_off;
+    off = align_up(off, 256);
     L.total = off;
     return L;
 }
@@ -51,6 +78,7 @@ Layout layout_of(int B, int gamma, int V, int dtype) {
 struct DeviceState {
     bool init = false;
     int sm_count = 0;
+    int coop = 0;               // cooperative launch supported
     void* ws = nullptr;
     size_t ws_bytes = 0;
     int32_t* status = nullptr;  // library status word (its own allocation)
@@ -73,6 +101,8 @@ int device_state(DeviceState** out) {
     DeviceState& d = g_dev[dev];
     if (!d.init) {
         if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return SPEC_ECUDA;
+        if (cudaDeviceGetAttribute(&d.coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess)
             return SPEC_ECUDA;
         if (cudaMalloc(&d.status, sizeof(int32_t)) != cudaSuccess) return SPEC_ENOMEM;
         if (cudaMemset(d.status, 0, sizeof(int32_t)) != cudaSuccess) return SPEC_ECUDA;
@@ -117,9 +147,24 @@ void record(const spec_verify_opts* o, int k, cudaStream_t s) {
     if (o && o->prof_events[k]) cudaEventRecord(static_cast<cudaEvent_t>(o->prof_events[k]), s);
 }
 
+void bind_workspace(VerifyParams& p, const Layout& L, char* ws) {
+    p.piece_len = L.piece_len;
+    p.npieces = L.npieces;
+    p.stat_parts = reinterpret_cast<float2*>(ws + L.stat_off);
+    p.seq = reinterpret_cast<SeqInfo*>(ws + L.seq_off);
+    p.race_parts = reinterpret_cast<RacePart*>(ws + L.race_off);
+    p.row_stat = reinterpret_cast<float2*>(ws + L.rowstat_off);
+    p.row_done = reinterpret_cast<int*>(ws + L.row_done_off);
+    p.seq_done = reinterpret_cast<int*>(ws + L.seq_done_off);
+    p.tickets = reinterpret_cast<int*>(ws + L.ticket_off);
+    p.ready = reinterpret_cast<int*>(ws + L.ready_off);
+    p.race_cursor = reinterpret_cast<int*>(ws + L.race_cursor_off);
+    p.row_cursor = reinterpret_cast<int*>(ws + L.row_cursor_off);
+}
+
 // Validated common set-up of a call: fills `p` with the workspace pointers.
 int prepare(int B, int gamma, int V, int dtype, const spec_verify_opts* o, VerifyParams& p,
-            DeviceState** dstate) {
+            DeviceState** dstate, char** ws_out = nullptr) {
     std::lock_guard<std::mutex> lock(g_mu);
     int rc = device_state(dstate);
     if (rc) return rc;
@@ -134,13 +179,9 @@ int prepare(int B, int gamma, int V, int dtype, const spec_verify_opts* o, Verif
         if (rc) return rc;
         ws = static_cast<char*>((*dstate)->ws);
     }
-    p.piece_len = L.piece_len;
-    p.npieces = L.npieces;
-    p.stat_parts = reinterpret_cast<float2*>(ws + L.stat_off);
-    p.seq = reinterpret_cast<SeqInfo*>(ws + L.seq_off);
-    p.race_parts = reinterpret_cast<RacePart*>(ws + L.race_off);
-    p.tickets = reinterpret_cast<int*>(ws + L.ticket_off);
+    bind_workspace(p, L, ws);
     p.status = (o && o->d_status) ? o->d_status : (*dstate)->status;
+    if (ws_out) *ws_out = ws;
     return SPEC_OK;
 }
 
@@ -154,6 +195,34 @@ int check_common(const void* target, const int32_t* out_tokens, const int32_t* o
     if (!target || !out_tokens || !out_n) return SPEC_EINVAL;
     if (!aligned16(target)) return SPEC_EINVAL;
     return SPEC_OK;
+}
+
+// Fused sampling verify: zero the control block, then one cooperative launch with every block
+// resident (the drain phase's waits rely on it).
+template <class ET>
+int launch_fused(VerifyParams& p, int sm_count, const spec_verify_opts* o, cudaStream_t s,
+                 const Layout& L, char* ws) {
+    auto kernel = verify_fused_kernel<ET, kFusedUnroll>;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) != cudaSuccess ||
+        per_sm < 1)
+        return SPEC_ECUDA;
+    const int R = 2 * p.gamma + 1;
+    const long long rows = static_cast<long long>(p.B) * R * p.npieces;
+    long long grid = static_cast<long long>(sm_count) * per_sm;
+    (void)rows;  // every block has race warps: keep the full resident grid
+    if (cudaMemsetAsync(ws + L.ctl_off, 0, L.ctl_bytes, s) != cudaSuccess) return SPEC_ECUDA;
+    // row partials and merged rows start empty (see kStatEmpty)
+    if (cudaMemsetAsync(ws + L.stat_off, 0xFF, L.seq_off - L.stat_off, s) != cudaSuccess ||
+        cudaMemsetAsync(ws + L.rowstat_off, 0xFF, L.ctl_off - L.rowstat_off, s) != cudaSuccess)
+        return SPEC_ECUDA;
+    record(o, 0, s);
+    void* args[] = {&p};
+    if (cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kernel), dim3(static_cast<unsigned>(grid)),
+                                    dim3(kThreads), args, 0, s) != cudaSuccess)
+        return SPEC_ECUDA;
+    record(o, 1, s);
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
 }
 
 template <class ET>
@@ -222,6 +291,7 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, const in
     p.T_seq = opts ? opts->T_per_seq : nullptr;
     p.Td_seq = opts ? opts->Td_per_seq : nullptr;
     p.key = philox_key(seed);
+    p.rk = philox_round_keys(p.key);
     p.seq_base = opts ? opts->seq_index_base : 0u;
     p.out_tokens = out_tokens;
     p.out_n = out_n_accepted;
@@ -233,10 +303,18 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, const in
         p.out_u = opts->out_u;
         p.out_race = opts->out_race;
     }
+    p.debug_flags = (opts && (opts->debug_flags & SPEC_DEBUG_NEVER_READY)) ? kDebugNeverReady : 0u;
     DeviceState* d = nullptr;
-    rc = prepare(B, gamma, V, dtype, opts, p, &d);
+    char* ws = nullptr;
+    rc = prepare(B, gamma, V, dtype, opts, p, &d, &ws);
     if (rc) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool fused = d->coop && !(opts && (opts->debug_flags & SPEC_DEBUG_UNFUSED));
+    if (fused) {
+        const Layout L = layout_of(B, gamma, V, dtype);
+        return dtype == SPEC_F32 ? launch_fused<F32Elem>(p, d->sm_count, opts, s, L, ws)
+                                 : launch_fused<Bf16Elem>(p, d->sm_count, opts, s, L, ws);
+    }
     return dtype == SPEC_F32 ? launch_sampling<F32Elem>(p, d->sm_count, opts, s)
                              : launch_sampling<Bf16Elem>(p, d->sm_count, opts, s);
 }
@@ -324,6 +402,7 @@ struct NoallocDevice {
     bool ready = false;
     char* scratch = nullptr;  // device address of g_noalloc_scratch on this device
     int sm_count = 0;
+    int coop = 0;             // cooperative launch supported
 };
 
 std::mutex g_noalloc_mu;
@@ -342,6 +421,8 @@ int noalloc_device(NoallocDevice** out) {
         if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
             return SPEC_ECUDA;
         if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return SPEC_ECUDA;
+        if (cudaDeviceGetAttribute(&d.coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess)
             return SPEC_ECUDA;
         d.scratch = static_cast<char*>(ptr);
         d.ready = true;
@@ -383,6 +464,7 @@ extern "C" int spec_verify_noalloc(const void* target_logits, const void* draft_
     p.T_seq = opts ? opts->T_per_seq : nullptr;
     p.Td_seq = opts ? opts->Td_per_seq : nullptr;
     p.key = philox_key(seed);
+    p.rk = philox_round_keys(p.key);
     p.seq_base = opts ? opts->seq_index_base : 0u;
     p.out_tokens = out_tokens;
     p.out_n = out_n_accepted;
@@ -395,18 +477,17 @@ extern "C" int spec_verify_noalloc(const void* target_logits, const void* draft_
         p.out_race = opts->out_race;
     }
     char* ws = nd->scratch;
-    p.piece_len = L.piece_len;
-    p.npieces = L.npieces;
-    p.stat_parts = reinterpret_cast<float2*>(ws + L.stat_off);
-    p.seq = reinterpret_cast<SeqInfo*>(ws + L.seq_off);
-    p.race_parts = reinterpret_cast<RacePart*>(ws + L.race_off);
-    p.tickets = reinterpret_cast<int*>(ws + L.ticket_off);
+    bind_workspace(p, L, ws);
+    p.debug_flags = (opts && (opts->debug_flags & SPEC_DEBUG_NEVER_READY)) ? kDebugNeverReady : 0u;
     if (opts && opts->d_status) {
         p.status = opts->d_status;
     } else {
         p.status = reinterpret_cast<int32_t*>(ws + kNoallocStatusOff);
         if (cudaMemsetAsync(p.status, 0, sizeof(int32_t), s) != cudaSuccess) return SPEC_ECUDA;
     }
+    if (nd->coop && !(opts && (opts->debug_flags & SPEC_DEBUG_UNFUSED)))
+        return dtype == SPEC_F32 ? launch_fused<F32Elem>(p, nd->sm_count, opts, s, L, ws)
+                                 : launch_fused<Bf16Elem>(p, nd->sm_count, opts, s, L, ws);
     return dtype == SPEC_F32 ? launch_sampling<F32Elem>(p, nd->sm_count, opts, s)
                              : launch_sampling<Bf16Elem>(p, nd->sm_count, opts, s);
 }

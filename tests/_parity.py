@@ -97,6 +97,11 @@ def compare_sampling(w: workloads.Workload, g: dict, r: "oracle.OracleResult",
         np.testing.assert_allclose(zq, r.logZq, rtol=1e-6, atol=1e-6)
     zp = g["logZp"].astype(np.float64)
     np.testing.assert_allclose(zp, r.logZp, rtol=1e-6, atol=1e-6)
+    # the winning race score ln w(y) - ln E_y (a check of the device Philox and E mapping)
+    sel = ok & ~flagged
+    if sel.any():
+        np.testing.assert_allclose(g["race"][sel, 0].astype(np.float64), r.race[sel, 0],
+                                   rtol=1e-5, atol=2e-5)
 
 
 def compare_greedy(g_tokens, g_n, r_tokens, r_n):

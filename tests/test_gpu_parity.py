@@ -254,6 +254,46 @@ def test_empty_batch_and_invalid_arguments(sv):
     assert ex.value.code == sv.SPEC_EINVAL
 
 
+@pytest.mark.parametrize("B,gamma,V,dtype", [(3, 4, 5003, "bf16"), (2, 7, 9000, "f32"),
+                                              (4, 0, 777, "bf16"), (6, 3, 40000, "bf16")])
+def test_unfused_path_matches_fused_and_oracle(sv, orc, B, gamma, V, dtype):
+    """The three-kernel path (kept for devices without cooperative launch) and the fused
+    single-kernel path give identical outputs, and both match the oracle."""
+    w = workloads.generic(B=B, gamma=gamma, V=V, dtype=dtype, seed=B * 31 + V, sigma=0.9,
+                          T=0.8, Td=0.35)
+    dw = DeviceWorkload(w)
+    for seed in range(3):
+        fused = run_gpu(sv, dw, seed, per_seq_temps=False)
+        t, n, d = sv.spec_verify_ex(dw.target, dw.draft, dw.tokens, float(w.T[0]),
+                                    float(w.Td[0]), seed, diagnostics=True,
+                                    debug_flags=sv.SPEC_DEBUG_UNFUSED)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(t.cpu().numpy(), fused["tokens"])
+        np.testing.assert_array_equal(n.cpu().numpy(), fused["n"])
+        for k in ("logp", "logq", "logZp", "logZq", "u"):
+            np.testing.assert_allclose(d[k].cpu().numpy(), fused[k], rtol=2e-6, atol=2e-6,
+                                       equal_nan=True, err_msg=k)
+        r = orc.verify(w.target, w.draft, w.tokens, w.T, w.Td, seed)
+        compare_sampling(w, fused, r)
+
+
+def test_bounded_wait_times_out_and_context_survives(sv, orc):
+    """The fused kernel's waits are bounded: with the test flag that makes every race wait
+    on a flag nothing sets, the call ends (after about half a second per wait) with
+    SPEC_ETIMEOUT in the status word, and the next normal call is correct."""
+    import time
+    w = workloads.generic(B=2, gamma=3, V=3000, dtype="bf16", seed=77)
+    dw = DeviceWorkload(w)
+    t0 = time.time()
+    sv.spec_verify_ex(dw.target, dw.draft, dw.tokens, 1.0, 1.0, 0,
+                      debug_flags=sv.SPEC_DEBUG_NEVER_READY)
+    assert sv.spec_verify_check() == sv.SPEC_ETIMEOUT
+    assert time.time() - t0 < 30
+    g = run_gpu(sv, dw, 0, per_seq_temps=False)
+    assert sv.spec_verify_check() == sv.SPEC_OK
+    compare_sampling(w, g, orc.verify(w.target, w.draft, w.tokens, w.T, w.Td, 0))
+
+
 def test_zz_near_tie_budget():
     """Flagged near-tie decisions stay under 1e-4 of all decisions compared in this module."""
     if TOTALS["decisions"] == 0:
