@@ -385,6 +385,63 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_table(args):
+    """Every named workload, both sampling paths (fused single kernel, three kernels) and the
+    greedy mode, as a table on stderr.  Workloads smaller than twice L2 are timed twice: on
+    one resident copy (warm L2) and rotating over enough copies to exceed twice L2 (cold)."""
+    import torch
+    import workloads
+    import speculative_decoding_verification_31_gb300 as sv
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    sv.load_library()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    rows_out = []
+    for cfg in range(5):
+        for greedy in ([False, True] if cfg in (1, 3, 4) else [False]):
+            w = workloads.config(cfg, greedy=greedy)
+            nbytes = w.bytes_greedy() if greedy else w.bytes_sampling()
+            copies = 1 if nbytes > 2 * l2 else min(64, -(-2 * l2 // nbytes) + 1)
+            bufs = [(to_torch(w.target, w.dtype).to(dev),
+                     to_torch(w.draft, w.dtype).to(dev)) for _ in range(copies)]
+            tok = torch.from_numpy(w.tokens).to(dev)
+            Tq, Tdq = torch.from_numpy(w.T).to(dev), torch.from_numpy(w.Td).to(dev)
+            out_t = torch.empty((w.B, w.gamma + 1), dtype=torch.int32, device=dev)
+            out_n = torch.empty((w.B,), dtype=torch.int32, device=dev)
+            kw = dict(T_per_seq=Tq, Td_per_seq=Tdq) if cfg == 3 else {}
+            modes = [("greedy", None)] if greedy else [("fused", 0), ("unfused", sv.SPEC_DEBUG_UNFUSED)]
+            for label, dbg in modes:
+                for warm in ([False, True] if copies > 1 else [False]):
+                    def call(k):
+                        t, d = bufs[0 if warm else k % copies]
+                        if greedy:
+                            sv.spec_verify_greedy_ex(t, tok, out_t, out_n)
+                        else:
+                            sv.spec_verify_ex(t, d, tok, float(w.T[0]), float(w.Td[0]), 0, out_t,
+                                              out_n, debug_flags=dbg, **kw)
+                    for k in range(5):
+                        call(k)
+                    torch.cuda.synchronize()
+                    n = max(20, min(2000, int(2e9 / max(nbytes, 1))))
+                    s0 = torch.cuda.Event(enable_timing=True)
+                    s1 = torch.cuda.Event(enable_timing=True)
+                    s0.record()
+                    for k in range(n):
+                        call(k)
+                    s1.record()
+                    torch.cuda.synchronize()
+                    us = s0.elapsed_time(s1) / n * 1e3
+                    st = sv.spec_verify_check()
+                    rows_out.append((cfg, label, "warm" if warm else ("cold" if copies > 1 else "> L2"),
+                                     us, w.rows / us * 1e6, nbytes / us / 1e3, st))
+    print("| workload | path | L2 | us/call | rows/s | GB/s (one read of the logits) | status |",
+          file=sys.stderr)
+    print("|---|---|---|---|---|---|---|", file=sys.stderr)
+    for cfg, label, l2s, us, rps, gbs, st in rows_out:
+        print(f"| {cfg} | {label} | {l2s} | {us:.1f} | {rps:.3e} | {gbs:.0f} | {st} |",
+              file=sys.stderr)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -398,10 +455,15 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--all", action="store_true",
+                    help="print a per-workload table (both sampling paths, greedy) to stderr")
     ap.add_argument("--ref-seqs", type=int, default=1,
                     help="sequences per reference step (one throughput-workload sequence is\n"
                          "about 0.04 s of oracle work)")
     args = ap.parse_args()
+    if args.all:
+        run_table(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

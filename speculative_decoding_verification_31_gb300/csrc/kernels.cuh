@@ -46,7 +46,8 @@ struct VerifyParams {
     const void* draft;          // [B, gamma, V]
     const int32_t* tokens;      // [B, gamma]
     int B, gamma, V;
-    int piece_len, npieces;     // elements per row piece, pieces per row
+    int piece_len, npieces;     // elements per row piece, pieces per row (streaming pass)
+    int rpiece_len, rpieces;    // the same for the race pass (finer: the race is compute-bound)
     float T, Td;                // scalar temperatures
     const float* T_seq;         // [B] or nullptr
     const float* Td_seq;        // [B] or nullptr
@@ -56,7 +57,7 @@ struct VerifyParams {
     // workspace
     float2* stat_parts;         // [B][2*gamma+1][npieces] (m, s) or (value, index) in greedy
     SeqInfo* seq;               // [B]
-    RacePart* race_parts;       // [B][npieces]
+    RacePart* race_parts;       // [B][rpieces]
     int* tickets;               // [B] race arrival counters, zeroed by the scan
     int32_t* status;
     // fused single-kernel path (zeroed control block, see verify_fused_kernel)
@@ -65,7 +66,6 @@ struct VerifyParams {
     int* seq_done;              // [B] rows completed
     int* ready;                 // [B] 1 once the sequence's scan has been published
     int* race_cursor;           // race items claimed so far (item c: sequence c / P, piece c % P)
-    int* row_cursor;            // row items claimed so far (sequence-major order)
     uint32_t debug_flags;       // kDebug* test switches
     // outputs
     int32_t* out_tokens;        // [B, gamma+1]
@@ -624,11 +624,11 @@ __device__ __forceinline__ void race_item(const VerifyParams& p, int b, int piec
     const S* rd = residual ? static_cast<const S*>(p.draft) + (static_cast<long long>(b) * p.gamma + si.j) * p.V
                            : nullptr;
     const uint32_t bg = p.seq_base + static_cast<uint32_t>(b);
-    const int x0 = piece * p.piece_len;
-    const int x1 = min(p.V, x0 + p.piece_len);
+    const int x0 = piece * p.rpiece_len;
+    const int x1 = min(p.V, x0 + p.rpiece_len);
     const RaceState st = race_piece<ET>(rt, rd, x0, x1, si, residual, p.rk, bg,
                                         static_cast<uint32_t>(si.j), lane);
-    const long long item = static_cast<long long>(b) * p.npieces + piece;
+    const long long item = static_cast<long long>(b) * p.rpieces + piece;
     if (lane == 0) {
         p.race_parts[item] = RacePart{st.best, st.idx, st.second, 0};
         __threadfence();
@@ -636,12 +636,12 @@ __device__ __forceinline__ void race_item(const VerifyParams& p, int b, int piec
     int ticket = 0;
     if (lane == 0) ticket = atomicAdd(p.tickets + b, 1);
     ticket = __shfl_sync(0xffffffffu, ticket, 0);
-    if (ticket != p.npieces - 1) return;
+    if (ticket != p.rpieces - 1) return;
     // Last piece of this sequence: merge every piece's winner (read through L2).
     __threadfence();
     RaceState m{-INFINITY, INT_MAX, -INFINITY};
-    for (int k = lane; k < p.npieces; k += 32) {
-        const RacePart* rp = p.race_parts + static_cast<long long>(b) * p.npieces + k;
+    for (int k = lane; k < p.rpieces; k += 32) {
+        const RacePart* rp = p.race_parts + static_cast<long long>(b) * p.rpieces + k;
         const float4 raw = __ldcg(reinterpret_cast<const float4*>(rp));
         m = race_merge(m, RaceState{raw.x, __float_as_int(raw.y), raw.z});
     }
@@ -664,11 +664,182 @@ template <class ET>
 __global__ void __launch_bounds__(256, 4) race_kernel(VerifyParams p) {
     const int lane = threadIdx.x & 31;
     const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
-    const long long total = static_cast<long long>(p.B) * p.npieces;
+    const long long total = static_cast<long long>(p.B) * p.rpieces;
     for (long long item = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
          item < total; item += nwarps) {
-        const int b = static_cast<int>(item / p.npieces);
-        race_item<ET>(p, b, static_cast<int>(item % p.npieces), p.seq[b], lane);
+        const int b = static_cast<int>(item / p.rpieces);
+        race_item<ET>(p, b, static_cast<int>(item % p.rpieces), p.seq[b], lane);
+    }
+}
+
+// ----------------------------------------------------------------------------------------
+// race_block: the race pass with one block per race piece of kRaceBlockTokens tokens.  Each
+// warp holds its kRaceWarpTokens tokens in registers, so the piece is read once; the
+// block's threshold is seeded from every lane's most likely token with a cheap lower bound
+// of its score (no exact evaluation on the critical path).
+// ----------------------------------------------------------------------------------------
+
+constexpr int kRaceWarpTokens = 1024;
+constexpr int kRaceBlockTokens = 8 * kRaceWarpTokens;
+
+// A lower bound of the exact score ln w(x) - ln E_x from fast approximations, or -inf.
+//   ln E <= ln U - ln(1 - U)             (since -log1p(-U) <= U / (1 - U))
+//   ln w = ln p + ln(1 - q/p) >= fast value - margin, unless 1 - q/p is tiny (then -inf)
+__device__ __forceinline__ float race_score_lower_bound(float xt, float xd, const SeqInfo& si,
+                                                       bool residual, uint32_t w) {
+    const float l2p = fmaf(xt, si.cp, -si.mp) - si.l2sp;
+    if (!(l2p > -INFINITY)) return -INFINITY;
+    float l2w = l2p;
+    if (residual) {
+        const float l2q = fmaf(xd, si.cq, -si.mq) - si.l2sq;
+        const float one_minus = 1.0f - ex2_fast(l2q - l2p);
+        if (!(one_minus > 0x1p-10f)) return -INFINITY;
+        l2w += lg2_fast(one_minus);
+    }
+    const float l2U = lg2_fast(static_cast<float>(w) + 0.5f) - 32.0f;
+    const float l2V = lg2_fast(static_cast<float>(~w) + 0.5f) - 32.0f;  // log2(1 - U)
+    return (l2w - (l2U - l2V)) * kLn2 - 1e-3f;
+}
+
+template <class ET>
+__global__ void __launch_bounds__(256, 4) race_block_kernel(VerifyParams p) {
+    using S = typename ET::storage;
+    constexpr int VPL = kRaceWarpTokens / (32 * ET::kVec);  // vectors per lane
+    __shared__ float s_thr[8];
+    __shared__ RaceState s_best[8];
+    __shared__ int s_last;
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    const int b = blockIdx.x / p.rpieces;
+    const int piece = blockIdx.x % p.rpieces;
+    const SeqInfo si = p.seq[b];
+    if (si.j < 0) return;  // bad draft token: nothing to draw
+    const bool residual = si.j < p.gamma;
+    const S* rt = static_cast<const S*>(p.target) + (static_cast<long long>(b) * (p.gamma + 1) + si.j) * p.V;
+    const S* rd = residual ? static_cast<const S*>(p.draft) + (static_cast<long long>(b) * p.gamma + si.j) * p.V
+                           : nullptr;
+    const uint32_t bg = p.seq_base + static_cast<uint32_t>(b);
+    const uint32_t pos = static_cast<uint32_t>(si.j);
+    const RaceRowRng q = race_row_rng(p.rk, bg, pos);
+    const int x0 = piece * kRaceBlockTokens + wib * kRaceWarpTokens;
+    const int x1 = min(p.V, x0 + kRaceWarpTokens);
+    RaceState st{-INFINITY, INT_MAX, -INFINITY};
+    auto word_at = [&](int x) {
+        const uint4 blk = race_block_fast(q, p.rk, static_cast<uint32_t>(x) >> 2);
+        return word_of(blk, static_cast<uint32_t>(x) & 3u);
+    };
+    auto offer_exact = [&](float xt, int x, uint32_t w) {
+        const float xd = residual ? ET::load1(rd + x) : 0.0f;
+        const float sc = race_exact_score(xt, xd, si, residual, w);
+        if (sc > -INFINITY) race_offer(st, sc, x);
+    };
+    // The register path needs a 16-byte aligned chunk start (then every vector is aligned and
+    // starts on a Philox block); otherwise, or for the row's last < 8 tokens, tokens go one by one.
+    const bool vec_ok = x0 < x1 && (reinterpret_cast<uintptr_t>(rt + x0) & 15u) == 0;
+    const int nvec = vec_ok ? (x1 - x0) / ET::kVec : 0;
+    uint4 raw[VPL];
+    float seed = -INFINITY;
+    if (vec_ok) {
+        const uint4* vt = reinterpret_cast<const uint4*>(rt + x0);
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) {
+            const int v = lane + 32 * k;
+            raw[k] = v < nvec ? __ldg(vt + v) : make_uint4(ET::kNegInfWord, ET::kNegInfWord,
+                                                           ET::kNegInfWord, ET::kNegInfWord);
+        }
+        float vmax = -INFINITY;
+        int xs = -1;
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) {
+            float ft[ET::kVec];
+            ET::widen(raw[k], ft);
+#pragma unroll
+            for (int e = 0; e < ET::kVec; ++e)
+                if (ft[e] > vmax) {
+                    vmax = ft[e];
+                    xs = x0 + (lane + 32 * k) * ET::kVec + e;
+                }
+        }
+        if (xs >= 0) {
+            const float xd = residual ? ET::load1(rd + xs) : 0.0f;
+            seed = race_score_lower_bound(vmax, xd, si, residual, word_at(xs));
+        }
+    }
+    seed = float_unorder(__reduce_max_sync(0xffffffffu, float_order(seed)));
+    if (lane == 0) s_thr[wib] = seed;
+    __syncthreads();
+    float thr = s_thr[0];
+#pragma unroll
+    for (int k = 1; k < 8; ++k) thr = fmaxf(thr, s_thr[k]);
+    if (vec_ok) {
+        const float mpl = si.mp + si.l2sp;
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) {
+            const int v = lane + 32 * k;
+            const float C = (thr > -INFINITY) ? 32.0f + kRaceBoundMargin2 - thr * kLog2e - mpl
+                                              : INFINITY;
+            if (v < nvec) {
+                float ft[ET::kVec];
+                ET::widen(raw[k], ft);
+                const int xv = x0 + v * ET::kVec;
+                uint32_t cand = 0;
+                uint4 blk[ET::kVec / 4];
+#pragma unroll
+                for (int g = 0; g < ET::kVec / 4; ++g)
+                    blk[g] = race_block_fast(q, p.rk, static_cast<uint32_t>(xv + 4 * g) >> 2);
+#pragma unroll
+                for (int g = 0; g < ET::kVec / 4; ++g) {
+                    const uint32_t w4[4] = {blk[g].x, blk[g].y, blk[g].z, blk[g].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        cand |= (lg2_fast(static_cast<float>(w4[e])) <= fmaf(ft[4 * g + e], si.cp, C))
+                                    ? (1u << (4 * g + e)) : 0u;
+                }
+                while (cand) {  // rare: exact scores in increasing token order
+                    const int e = __ffs(cand) - 1;
+                    cand &= cand - 1;
+                    offer_exact(ET::load1(rt + xv + e), xv + e, word_at(xv + e));
+                }
+            }
+            thr = fmaxf(thr, float_unorder(__reduce_max_sync(0xffffffffu, float_order(st.best))));
+        }
+        const int t0 = nvec * ET::kVec;  // the row's last < kVec tokens
+        if (lane < (x1 - x0) - t0) offer_exact(ET::load1(rt + x0 + t0 + lane), x0 + t0 + lane,
+                                               word_at(x0 + t0 + lane));
+    } else {
+        for (int x = x0 + lane; x < x1; x += 32) offer_exact(ET::load1(rt + x), x, word_at(x));
+    }
+    st = warp_race_merge(st);
+    if (lane == 0) s_best[wib] = st;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        RaceState m = s_best[0];
+        for (int k = 1; k < 8; ++k) m = race_merge(m, s_best[k]);
+        p.race_parts[static_cast<long long>(b) * p.rpieces + piece] = RacePart{m.best, m.idx, m.second, 0};
+        __threadfence();
+        s_last = (atomicAdd(p.tickets + b, 1) == p.rpieces - 1);
+    }
+    __syncthreads();
+    if (!s_last) return;
+    // last piece of this sequence: warp 0 merges every piece's winner (read through L2)
+    if (wib != 0) return;
+    __threadfence();
+    RaceState m{-INFINITY, INT_MAX, -INFINITY};
+    for (int k = lane; k < p.rpieces; k += 32) {
+        const RacePart* rp = p.race_parts + static_cast<long long>(b) * p.rpieces + k;
+        const float4 r4 = __ldcg(reinterpret_cast<const float4*>(rp));
+        m = race_merge(m, RaceState{r4.x, __float_as_int(r4.y), r4.z});
+    }
+    m = warp_race_merge(m);
+    if (m.idx == INT_MAX) {
+        // Every residual weight was zero (p <= q everywhere in fp32): draw from p_j.
+        m = race_piece<ET>(rt, nullptr, 0, p.V, si, false, p.rk, bg, pos, lane);
+    }
+    if (lane == 0) {
+        p.out_tokens[static_cast<long long>(b) * (p.gamma + 1) + si.j] = m.idx;
+        if (p.out_race) {
+            p.out_race[2 * b] = m.best;
+            p.out_race[2 * b + 1] = m.second;
+        }
     }
 }
 
@@ -676,8 +847,8 @@ __global__ void __launch_bounds__(256, 4) race_kernel(VerifyParams p) {
 // verify_fused: the whole sampling verify in one persistent (cooperative) launch, with
 // specialised warps.
 //
-// Streaming warps (the first kStreamWarps of each block) claim row items (b, r, piece) in
-// sequence-major order from row_cursor and never wait: each writes its piece's partial
+// Streaming warps (the first kStreamWarps of each block) take row items (b, r, piece) in
+// sequence-major order, round-robin, and never wait: each writes its piece's partial
 // statistics and counts its arrival on the row without a fence (partials are pre-filled
 // with an empty marker that the reader polls for).  The last piece of a row to arrive merges
 // the row; the last row of a sequence to be merged runs the sequence's scan (one warp) and
@@ -897,15 +1068,12 @@ __global__ void __launch_bounds__(256, SPECVERIFY_FUSED_MINBLOCKS) verify_fused_
     const int RP = R * P;
     const long long total_rows = static_cast<long long>(p.B) * RP;
     if ((threadIdx.x >> 5) < kStreamWarps) {
+        // streaming warps take row items round-robin (their items all cost the same)
+        const long long sw = static_cast<long long>(blockIdx.x) * kStreamWarps + (threadIdx.x >> 5);
+        const long long nsw = static_cast<long long>(gridDim.x) * kStreamWarps;
         // pending arrival of the previous row item (lane 0 holds the ticket)
         int pend_ticket = 0, pend_b = -1, pend_r = 0;
-        long long next = 0;
-        if (lane == 0) next = atomicAdd(reinterpret_cast<unsigned long long*>(p.row_cursor), 1ull);
-        next = __shfl_sync(0xffffffffu, next, 0);
-        while (next < total_rows) {
-            const long long g = next;
-            if (lane == 0)  // the next claim, used after this item
-                next = atomicAdd(reinterpret_cast<unsigned long long*>(p.row_cursor), 1ull);
+        for (long long g = sw; g < total_rows; g += nsw) {
             const int b = static_cast<int>(g / RP);
             const int within = static_cast<int>(g % RP);
             const int r = within / P;
@@ -916,19 +1084,19 @@ __global__ void __launch_bounds__(256, SPECVERIFY_FUSED_MINBLOCKS) verify_fused_
                 pend_ticket = atomicAdd(p.row_done + static_cast<long long>(b) * R + r, 1);
             pend_b = b;
             pend_r = r;
-            next = __shfl_sync(0xffffffffu, next, 0);
         }
         if (pend_b >= 0)
             resolve_arrival<ET>(p, __shfl_sync(0xffffffffu, pend_ticket, 0), pend_b, pend_r, lane);
     }
     // race items, in sequence order
-    const long long total_race = static_cast<long long>(p.B) * P;
+    const int RPc = p.rpieces;
+    const long long total_race = static_cast<long long>(p.B) * RPc;
     while (true) {
         long long c = 0;
         if (lane == 0) c = atomicAdd(reinterpret_cast<unsigned long long*>(p.race_cursor), 1ull);
         c = __shfl_sync(0xffffffffu, c, 0);
         if (c >= total_race) break;
-        run_claimed_race<ET>(p, static_cast<int>(c / P), static_cast<int>(c % P), lane);
+        run_claimed_race<ET>(p, static_cast<int>(c / RPc), static_cast<int>(c % RPc), lane);
     }
 }
 

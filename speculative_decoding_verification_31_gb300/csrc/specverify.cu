@@ -34,10 +34,10 @@ int elem_bytes(int dtype) { return dtype == SPEC_F32 ? 4 : 2; }
 
 struct Layout {
     int piece_len, npieces;
+    int rpiece_len, rpieces;
     size_t stat_off, seq_off, race_off, rowstat_off;
     size_t ctl_off, ctl_bytes;          // zeroed control block: row_done, seq_done, tickets, ready
-    size_t row_done_off, seq_done_off, ticket_off, ready_off, race_cursor_off,
-        row_cursor_off;
+    size_t row_done_off, seq_done_off, ticket_off, ready_off, race_cursor_off;
     size_t total;
 };
 
@@ -45,6 +45,9 @@ Layout layout_of(int B, int gamma, int V, int dtype) {
     Layout L{};
     L.piece_len = kPieceBytes / elem_bytes(dtype);
     L.npieces = (V + L.piece_len - 1) / L.piece_len;
+    // race pieces: one block of kRaceBlockTokens tokens each
+    L.rpiece_len = kRaceBlockTokens;
+    L.rpieces = (V + kRaceBlockTokens - 1) / kRaceBlockTokens;
     const size_t R = 2 * static_cast<size_t>(gamma) + 1;
     size_t off = 0;
     L.stat_off = off;
@@ -52,7 +55,7 @@ Layout layout_of(int B, int gamma, int V, int dtype) {
     L.seq_off = off;
     off = align_up(off + static_cast<size_t>(B) * sizeof(SeqInfo), 256);
     L.race_off = off;
-    off = align_up(off + static_cast<size_t>(B) * L.npieces * sizeof(RacePart), 256);
+    off = align_up(off + static_cast<size_t>(B) * L.rpieces * sizeof(RacePart), 256);
     L.rowstat_off = off;
     off = align_up(off + static_cast<size_t>(B) * R * sizeof(float2), 256);
     L.ctl_off = off;
@@ -66,8 +69,6 @@ Layout layout_of(int B, int gamma, int V, int dtype) {
     off += static_cast<size_t>(B) * sizeof(int);
     off = align_up(off, 8);
     L.race_cursor_off = off;
-    off += sizeof(unsigned long long);
-    L.row_cursor_off = off;
     off += sizeof(unsigned long long);
     L.ctl_bytes = off - L.ctl_off;
     off = align_up(off, 256);
@@ -150,6 +151,8 @@ void record(const spec_verify_opts* o, int k, cudaStream_t s) {
 void bind_workspace(VerifyParams& p, const Layout& L, char* ws) {
     p.piece_len = L.piece_len;
     p.npieces = L.npieces;
+    p.rpiece_len = L.rpiece_len;
+    p.rpieces = L.rpieces;
     p.stat_parts = reinterpret_cast<float2*>(ws + L.stat_off);
     p.seq = reinterpret_cast<SeqInfo*>(ws + L.seq_off);
     p.race_parts = reinterpret_cast<RacePart*>(ws + L.race_off);
@@ -159,7 +162,6 @@ void bind_workspace(VerifyParams& p, const Layout& L, char* ws) {
     p.tickets = reinterpret_cast<int*>(ws + L.ticket_off);
     p.ready = reinterpret_cast<int*>(ws + L.ready_off);
     p.race_cursor = reinterpret_cast<int*>(ws + L.race_cursor_off);
-    p.row_cursor = reinterpret_cast<int*>(ws + L.row_cursor_off);
 }
 
 // Validated common set-up of a call: fills `p` with the workspace pointers.
@@ -235,8 +237,7 @@ int launch_sampling(VerifyParams& p, int sm_count, const spec_verify_opts* o, cu
     record(o, 1, s);
     scan_kernel<ET><<<p.B, kThreads, 2 * R * sizeof(float), s>>>(p);
     record(o, 2, s);
-    const long long race_items = static_cast<long long>(p.B) * p.npieces;
-    race_kernel<ET><<<grid_for(race_kernel<ET>, sm_count, race_items), kThreads, 0, s>>>(p);
+    race_block_kernel<ET><<<static_cast<unsigned>(static_cast<long long>(p.B) * p.rpieces), kThreads, 0, s>>>(p);
     record(o, 3, s);
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
 }
