@@ -90,16 +90,17 @@ typedef struct {
     float *out_race;            /* [B, 2]       winning race score ln(w(y)/E_y), and the
                                                 runner-up score (approximate) */
     void *prof_events[4];       /* optional cudaEvent_t: recorded before the first kernel and
-                                   after each kernel of the call (the fused sampling path has
-                                   one kernel, the unfused one three, greedy two) */
-    uint32_t debug_flags;       /* SPEC_DEBUG_* bits for tests; 0 in normal use */
+                                   after each kernel of the call (sampling: two kernels, or
+                                   one with SPEC_FLAG_FUSED; greedy: two) */
+    uint32_t flags;             /* SPEC_FLAG_* / SPEC_DEBUG_* bits; 0 in normal use */
 } spec_verify_opts;
 
-/* debug_flags bits (tests only). */
-#define SPEC_DEBUG_UNFUSED 1u    /* sampling: run the three-kernel path instead of the fused one */
-#define SPEC_DEBUG_NEVER_READY 2u /* fused sampling: the race waits on a flag that is never set,
-                                     give up after their bounded wait and report SPEC_ETIMEOUT
-                                     (exercises the timeout path; outputs are then invalid) */
+/* flags bits. */
+#define SPEC_FLAG_FUSED 1u        /* sampling: one persistent cooperative kernel instead of the
+                                     default two kernels (same outputs, bit for bit) */
+#define SPEC_DEBUG_NEVER_READY 2u /* tests only, with SPEC_FLAG_FUSED: the race waits on a flag
+                                     that is never set, give up after their bounded wait and
+                                     report SPEC_ETIMEOUT (outputs are then invalid) */
 
 /* Zero every field and set dtype = SPEC_BF16. */
 void spec_verify_opts_init(spec_verify_opts *opts);

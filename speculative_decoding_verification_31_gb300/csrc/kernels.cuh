@@ -66,6 +66,7 @@ struct VerifyParams {
     int* seq_done;              // [B] rows completed
     int* ready;                 // [B] 1 once the sequence's scan has been published
     int* race_cursor;           // race items claimed so far (item c: sequence c / P, piece c % P)
+    int* row_cursor;            // row items claimed so far (sequence-major order)
     uint32_t debug_flags;       // kDebug* test switches
     // outputs
     int32_t* out_tokens;        // [B, gamma+1]
@@ -182,18 +183,28 @@ __device__ __forceinline__ void row_stats_item(const VerifyParams& p, int b, int
         store_stat(p.stat_parts + (static_cast<long long>(b) * R + r) * p.npieces + piece, st.m, st.s);
 }
 
+// Also empties the race partials and arrival counters the scan-race kernel uses, and lets
+// that kernel (launched as a programmatic dependent) start as soon as blocks retire.
+#ifndef SPECVERIFY_STATS_MINBLOCKS
+#define SPECVERIFY_STATS_MINBLOCKS 3
+#endif
 template <class ET, int U>
-__global__ void __launch_bounds__(256) row_stats_kernel(VerifyParams p) {
+__global__ void __launch_bounds__(256, SPECVERIFY_STATS_MINBLOCKS) row_stats_kernel(VerifyParams p) {
     const int lane = threadIdx.x & 31;
-    const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+    const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
+    const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (long long k = tid; k < static_cast<long long>(p.B) * p.rpieces; k += nthreads)
+        reinterpret_cast<uint4*>(p.race_parts)[k] = make_uint4(0u, 0u, 0u, 0u);
+    for (long long k = tid; k < p.B; k += nthreads) p.tickets[k] = 0;
+    const long long nwarps = nthreads >> 5;
     const int R = 2 * p.gamma + 1;
     const long long total = static_cast<long long>(p.B) * R * p.npieces;
-    for (long long item = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-         item < total; item += nwarps) {
+    for (long long item = tid >> 5; item < total; item += nwarps) {
         const int piece = static_cast<int>(item % p.npieces);
         const long long br = item / p.npieces;
         row_stats_item<ET, U>(p, static_cast<int>(br / R), static_cast<int>(br % R), piece, lane);
     }
+    asm volatile("griddepcontrol.launch_dependents;");
 }
 
 // ----------------------------------------------------------------------------------------
@@ -271,6 +282,15 @@ __global__ void __launch_bounds__(256) row_argmax_kernel(VerifyParams p) {
 // ----------------------------------------------------------------------------------------
 // scan: per sequence, ln Z of each row, p_i(d_i), q_i(d_i), u_i and the first rejection.
 // ----------------------------------------------------------------------------------------
+
+constexpr uint32_t kDebugNeverReady = 1u;         // scans never set ready[b] (tests)
+constexpr unsigned long long kWaitLimitNs = 500000000ull;  // give up a wait after 0.5 s
+
+__device__ __forceinline__ unsigned long long global_time_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
 
 __device__ __forceinline__ void set_status(int32_t* status, int code) {
     atomicCAS(reinterpret_cast<int*>(status), 0, code);
@@ -683,8 +703,10 @@ constexpr int kRaceWarpTokens = 1024;
 constexpr int kRaceBlockTokens = 8 * kRaceWarpTokens;
 
 // A lower bound of the exact score ln w(x) - ln E_x from fast approximations, or -inf.
-//   ln E <= ln U - ln(1 - U)             (since -log1p(-U) <= U / (1 - U))
-//   ln w = ln p + ln(1 - q/p) >= fast value - margin, unless 1 - q/p is tiny (then -inf)
+// E = -log1p(-U) is formed as U (1 + U/2 + U^2/3) below U = 2^-8 (series, relative error
+// below 2^-26) and as -ln(1 - U) from lg2.approx of the exact complement above it (relative
+// error below 2^-15 there); ln w = ln p + ln(1 - q/p) from ex2/lg2.approx, given up (-inf)
+// when 1 - q/p < 2^-10.  The result is reduced by a margin that covers these errors.
 __device__ __forceinline__ float race_score_lower_bound(float xt, float xd, const SeqInfo& si,
                                                        bool residual, uint32_t w) {
     const float l2p = fmaf(xt, si.cp, -si.mp) - si.l2sp;
@@ -696,9 +718,15 @@ __device__ __forceinline__ float race_score_lower_bound(float xt, float xd, cons
         if (!(one_minus > 0x1p-10f)) return -INFINITY;
         l2w += lg2_fast(one_minus);
     }
-    const float l2U = lg2_fast(static_cast<float>(w) + 0.5f) - 32.0f;
-    const float l2V = lg2_fast(static_cast<float>(~w) + 0.5f) - 32.0f;  // log2(1 - U)
-    return (l2w - (l2U - l2V)) * kLn2 - 1e-3f;
+    float E;
+    if (w < 0x01000000u) {
+        const float U = (static_cast<float>(w) + 0.5f) * 0x1p-32f;
+        E = U * fmaf(U, fmaf(U, 1.0f / 3.0f, 0.5f), 1.0f);
+    } else {
+        const float one_minus_U = (static_cast<float>(~w) + 0.5f) * 0x1p-32f;
+        E = -lg2_fast(one_minus_U) * kLn2;
+    }
+    return (l2w - lg2_fast(E)) * kLn2 - 1e-3f;
 }
 
 template <class ET>
@@ -844,11 +872,310 @@ __global__ void __launch_bounds__(256, 4) race_block_kernel(VerifyParams p) {
 }
 
 // ----------------------------------------------------------------------------------------
+// scan_race: one block per race piece (b, piece) of kRaceBlockTokens tokens.  Every block of
+// sequence b repeats the sequence's scan (row merges, gathers, u_i, first rejection j) --
+// cheap next to its piece of the race -- so no separate scan launch sits between the
+// streaming pass and the race; the block of piece 0 writes the sequence's outputs.  The
+// kernel is launched as a programmatic dependent of row_stats: before waiting for it, a
+// block gathers p(d_i), q(d_i) inputs and draws its uniforms.  Race partials are single
+// 64-bit words (score, index + 1) that the streaming pass emptied; the last block of a
+// sequence (by a relaxed arrival count) polls them, so no fence is needed.
+// ----------------------------------------------------------------------------------------
+
+__device__ __forceinline__ unsigned long long pack_race(float best, int idx) {
+    return (static_cast<unsigned long long>(static_cast<uint32_t>(idx) + 1u) << 32) |
+           __float_as_uint(best);
+}
+
+__device__ __forceinline__ unsigned long long ld_relaxed_u64g(const void* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+template <class ET>
+__global__ void __launch_bounds__(256, 4) scan_race_kernel(VerifyParams p) {
+    using S = typename ET::storage;
+    constexpr int VPL = kRaceWarpTokens / (32 * ET::kVec);
+    extern __shared__ float smem[];  // [2R]: scaled max and log2 sum of every row
+    __shared__ int s_j, s_bad, s_last;
+    __shared__ float s_thr[8];
+    __shared__ RaceState s_best[8];
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    const int b = blockIdx.x / p.rpieces;
+    const int piece = blockIdx.x % p.rpieces;
+    const int R = 2 * p.gamma + 1;
+    float* sm_m = smem;
+    float* sm_l = smem + R;
+    const float Tb = seq_T(p, b), Tdb = seq_Td(p, b);
+    const float cp = scale_of(Tb), cq = scale_of(Tdb);
+    const uint32_t bg = p.seq_base + static_cast<uint32_t>(b);
+    const bool writer = (piece == 0);
+    // diagnostics need every row's statistics; otherwise rows are merged only up to the first
+    // rejection, four positions (target and draft rows in parallel) at a time
+    const bool all_rows = writer && (p.out_logZp || p.out_logZq || p.out_logp || p.out_logq);
+    // inputs-only prologue (position i = threadIdx.x): overlaps the streaming pass's tail
+    __shared__ int s_d[256];
+    __shared__ float s_xt[256], s_xd[256], s_u[256];
+    const int i0 = threadIdx.x;
+    if (i0 < p.gamma) {
+        const int d = p.tokens[static_cast<long long>(b) * p.gamma + i0];
+        s_d[i0] = d;
+        s_u[i0] = accept_uniform(p.key, bg, static_cast<uint32_t>(i0));
+        float xt = 0.0f, xd = 0.0f;
+        if (d >= 0 && d < p.V) {
+            xt = ET::load1(static_cast<const S*>(p.target) +
+                           (static_cast<long long>(b) * (p.gamma + 1) + i0) * p.V + d);
+            xd = ET::load1(static_cast<const S*>(p.draft) +
+                           (static_cast<long long>(b) * p.gamma + i0) * p.V + d);
+        }
+        s_xt[i0] = xt;
+        s_xd[i0] = xd;
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (threadIdx.x == 0) {
+        s_j = p.gamma;
+        s_bad = 0;
+    }
+    // any draft token outside [0, V) marks the whole sequence
+    for (int i = threadIdx.x; i < p.gamma; i += blockDim.x) {
+        const int d = (i < 256) ? s_d[i] : p.tokens[static_cast<long long>(b) * p.gamma + i];
+        if (d < 0 || d >= p.V) s_bad = 1;
+    }
+    auto merge_row = [&](int r) {  // one warp: row r's statistics into shared memory
+        SoftmaxStat st{-FLT_MAX, 0.0f};
+        const float2* parts = p.stat_parts + (static_cast<long long>(b) * R + r) * p.npieces;
+        for (int k = lane; k < p.npieces; k += 32) {
+            const float2 qq = parts[k];
+            st = merge_stat(st, SoftmaxStat{qq.x, qq.y});
+        }
+        st = warp_merge_stat(st);
+        if (lane == 0) {
+            const float l2s = log2f(st.s);
+            sm_m[r] = st.m;
+            sm_l[r] = l2s;
+            if (writer) {
+                const float lz = (st.m + l2s) * kLn2;
+                if (r <= p.gamma) {
+                    if (p.out_logZp) p.out_logZp[static_cast<long long>(b) * (p.gamma + 1) + r] = lz;
+                } else if (p.out_logZq) {
+                    p.out_logZq[static_cast<long long>(b) * p.gamma + (r - p.gamma - 1)] = lz;
+                }
+            }
+        }
+    };
+    auto decide = [&](int i) {  // one thread: the accept test at position i
+        int d;
+        float xt, xd, u;
+        if (i < 256) {
+            d = s_d[i]; xt = s_xt[i]; xd = s_xd[i]; u = s_u[i];
+        } else {
+            d = p.tokens[static_cast<long long>(b) * p.gamma + i];
+            u = accept_uniform(p.key, bg, static_cast<uint32_t>(i));
+            xt = ET::load1(static_cast<const S*>(p.target) +
+                           (static_cast<long long>(b) * (p.gamma + 1) + i) * p.V + d);
+            xd = ET::load1(static_cast<const S*>(p.draft) +
+                           (static_cast<long long>(b) * p.gamma + i) * p.V + d);
+        }
+        const long long k = static_cast<long long>(b) * p.gamma + i;
+        if (writer && p.out_u) p.out_u[k] = u;
+        const float l2p = fmaf(xt, cp, -sm_m[i]) - sm_l[i];
+        const float l2q = fmaf(xd, cq, -sm_m[p.gamma + 1 + i]) - sm_l[p.gamma + 1 + i];
+        if (writer && p.out_logp) p.out_logp[k] = l2p * kLn2;
+        if (writer && p.out_logq) p.out_logq[k] = l2q * kLn2;
+        // accept iff u < min(1, p/q); p(d) = 0 rejects, q(d) = 0 < p(d) accepts
+        if (!((l2p > -INFINITY) && (u < exp2f(l2p - l2q)))) atomicMin(&s_j, i);
+    };
+    __syncthreads();
+    if (s_bad) {
+        if (writer) {
+            for (int i = threadIdx.x; i < p.gamma; i += blockDim.x) {
+                const long long k = static_cast<long long>(b) * p.gamma + i;
+                if (p.out_u) p.out_u[k] = accept_uniform(p.key, bg, static_cast<uint32_t>(i));
+                if (p.out_logp) p.out_logp[k] = NAN;
+                if (p.out_logq) p.out_logq[k] = NAN;
+            }
+            for (int r = wib; all_rows && r < R; r += 8) merge_row(r);
+        }
+    } else if (all_rows) {
+        for (int r = wib; r < R; r += 8) merge_row(r);
+        __syncthreads();
+        for (int i = threadIdx.x; i < p.gamma; i += blockDim.x) decide(i);
+    } else {
+        for (int i0b = 0; i0b < p.gamma; i0b += 4) {
+            const int i = i0b + (wib & 3);
+            if (i < p.gamma) merge_row(wib < 4 ? i : p.gamma + 1 + i);
+            __syncthreads();
+            if (threadIdx.x < 4 && i0b + threadIdx.x < p.gamma) decide(i0b + threadIdx.x);
+            __syncthreads();
+            if (s_j < p.gamma) break;
+        }
+        if (s_j == p.gamma && wib == 0) merge_row(p.gamma);  // bonus row
+    }
+    __syncthreads();
+    const int j = s_bad ? -1 : s_j;
+    if (writer) {
+        if (threadIdx.x == 0) {
+            p.out_n[b] = j;
+            if (j < 0) set_status(p.status, 3 /* SPEC_EBADTOKEN */);
+        }
+        int32_t* out = p.out_tokens + static_cast<long long>(b) * (p.gamma + 1);
+        for (int t = threadIdx.x; t <= p.gamma; t += blockDim.x)
+            if (t != j) out[t] = (j >= 0 && t < j) ? p.tokens[static_cast<long long>(b) * p.gamma + t] : -1;
+    }
+    if (j < 0) return;
+    SeqInfo si;
+    si.j = j;
+    si.cp = cp;
+    si.cq = cq;
+    si.mp = sm_m[j];
+    si.l2sp = sm_l[j];
+    const bool residual = j < p.gamma;
+    si.mq = residual ? sm_m[p.gamma + 1 + j] : 0.0f;
+    si.l2sq = residual ? sm_l[p.gamma + 1 + j] : 0.0f;
+    si.pad = 0;
+    const S* rt = static_cast<const S*>(p.target) + (static_cast<long long>(b) * (p.gamma + 1) + j) * p.V;
+    const S* rd = residual ? static_cast<const S*>(p.draft) + (static_cast<long long>(b) * p.gamma + j) * p.V
+                           : nullptr;
+    const uint32_t pos = static_cast<uint32_t>(j);
+    const RaceRowRng q = race_row_rng(p.rk, bg, pos);
+    const int x0 = piece * kRaceBlockTokens + wib * kRaceWarpTokens;
+    const int x1 = min(p.V, x0 + kRaceWarpTokens);
+    RaceState st{-INFINITY, INT_MAX, -INFINITY};
+    auto word_at = [&](int x) {
+        const uint4 blk = race_block_fast(q, p.rk, static_cast<uint32_t>(x) >> 2);
+        return word_of(blk, static_cast<uint32_t>(x) & 3u);
+    };
+    auto offer_exact = [&](float xt, int x, uint32_t w) {
+        const float xd = residual ? ET::load1(rd + x) : 0.0f;
+        const float sc = race_exact_score(xt, xd, si, residual, w);
+        if (sc > -INFINITY) race_offer(st, sc, x);
+    };
+    const bool vec_ok = x0 < x1 && (reinterpret_cast<uintptr_t>(rt + x0) & 15u) == 0;
+    const int nvec = vec_ok ? (x1 - x0) / ET::kVec : 0;
+    uint4 raw[VPL];
+    float seed = -INFINITY;
+    if (vec_ok) {
+        const uint4* vt = reinterpret_cast<const uint4*>(rt + x0);
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) {
+            const int v = lane + 32 * k;
+            raw[k] = v < nvec ? __ldg(vt + v) : make_uint4(ET::kNegInfWord, ET::kNegInfWord,
+                                                           ET::kNegInfWord, ET::kNegInfWord);
+        }
+        float vmax = -INFINITY;
+        int xs = -1;
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) {
+            float ft[ET::kVec];
+            ET::widen(raw[k], ft);
+#pragma unroll
+            for (int e = 0; e < ET::kVec; ++e)
+                if (ft[e] > vmax) {
+                    vmax = ft[e];
+                    xs = x0 + (lane + 32 * k) * ET::kVec + e;
+                }
+        }
+        if (xs >= 0) {
+            const float xd = residual ? ET::load1(rd + xs) : 0.0f;
+            seed = race_score_lower_bound(vmax, xd, si, residual, word_at(xs));
+        }
+    }
+    seed = float_unorder(__reduce_max_sync(0xffffffffu, float_order(seed)));
+    if (lane == 0) s_thr[wib] = seed;
+    __syncthreads();
+    float thr = s_thr[0];
+#pragma unroll
+    for (int k = 1; k < 8; ++k) thr = fmaxf(thr, s_thr[k]);
+    if (vec_ok) {
+        const float mpl = si.mp + si.l2sp;
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) {
+            const int v = lane + 32 * k;
+            const float C = (thr > -INFINITY) ? 32.0f + kRaceBoundMargin2 - thr * kLog2e - mpl
+                                              : INFINITY;
+            if (v < nvec) {
+                float ft[ET::kVec];
+                ET::widen(raw[k], ft);
+                const int xv = x0 + v * ET::kVec;
+                uint32_t cand = 0;
+                uint4 blk[ET::kVec / 4];
+#pragma unroll
+                for (int g = 0; g < ET::kVec / 4; ++g)
+                    blk[g] = race_block_fast(q, p.rk, static_cast<uint32_t>(xv + 4 * g) >> 2);
+#pragma unroll
+                for (int g = 0; g < ET::kVec / 4; ++g) {
+                    const uint32_t w4[4] = {blk[g].x, blk[g].y, blk[g].z, blk[g].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        cand |= (lg2_fast(static_cast<float>(w4[e])) <= fmaf(ft[4 * g + e], si.cp, C))
+                                    ? (1u << (4 * g + e)) : 0u;
+                }
+                while (cand) {  // rare: exact scores in increasing token order
+                    const int e = __ffs(cand) - 1;
+                    cand &= cand - 1;
+                    offer_exact(ET::load1(rt + xv + e), xv + e, word_at(xv + e));
+                }
+            }
+            thr = fmaxf(thr, float_unorder(__reduce_max_sync(0xffffffffu, float_order(st.best))));
+        }
+        const int t0 = nvec * ET::kVec;
+        if (lane < (x1 - x0) - t0) offer_exact(ET::load1(rt + x0 + t0 + lane), x0 + t0 + lane,
+                                               word_at(x0 + t0 + lane));
+    } else {
+        for (int x = x0 + lane; x < x1; x += 32) offer_exact(ET::load1(rt + x), x, word_at(x));
+    }
+    st = warp_race_merge(st);
+    if (lane == 0) s_best[wib] = st;
+    __syncthreads();
+    RacePart* parts = p.race_parts + static_cast<long long>(b) * p.rpieces;
+    if (threadIdx.x == 0) {
+        RaceState m = s_best[0];
+        for (int k = 1; k < 8; ++k) m = race_merge(m, s_best[k]);
+        parts[piece].second = m.second;  // diagnostic only
+        *reinterpret_cast<unsigned long long*>(parts + piece) = pack_race(m.best, m.idx);
+        s_last = (atomicAdd(p.tickets + b, 1) == p.rpieces - 1);
+    }
+    __syncthreads();
+    if (!s_last || wib != 0) return;
+    // last piece of this sequence: merge every piece's winner, waiting (bounded) for each
+    RaceState m{-INFINITY, INT_MAX, -INFINITY};
+    for (int k = lane; k < p.rpieces; k += 32) {
+        unsigned long long v = ld_relaxed_u64g(parts + k);
+        if (v == 0ull) {
+            const unsigned long long t0 = global_time_ns();
+            while ((v = ld_relaxed_u64g(parts + k)) == 0ull) {
+                if (global_time_ns() - t0 > kWaitLimitNs) break;
+                __nanosleep(64);
+            }
+            if (v == 0ull) set_status(p.status, 4 /* SPEC_ETIMEOUT */);
+        }
+        if (v != 0ull) {
+            const float sec = __ldcg(&parts[k].second);
+            m = race_merge(m, RaceState{__uint_as_float(static_cast<uint32_t>(v)),
+                                        static_cast<int>(static_cast<uint32_t>(v >> 32) - 1u), sec});
+        }
+    }
+    m = warp_race_merge(m);
+    if (m.idx == INT_MAX) {
+        // Every residual weight was zero (p <= q everywhere in fp32): draw from p_j.
+        m = race_piece<ET>(rt, nullptr, 0, p.V, si, false, p.rk, bg, pos, lane);
+    }
+    if (lane == 0) {
+        p.out_tokens[static_cast<long long>(b) * (p.gamma + 1) + j] = m.idx;
+        if (p.out_race) {
+            p.out_race[2 * b] = m.best;
+            p.out_race[2 * b + 1] = m.second;
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------------------
 // verify_fused: the whole sampling verify in one persistent (cooperative) launch, with
 // specialised warps.
 //
-// Streaming warps (the first kStreamWarps of each block) take row items (b, r, piece) in
-// sequence-major order, round-robin, and never wait: each writes its piece's partial
+// Streaming warps (the first kStreamWarps of each block) claim row items (b, r, piece) in
+// sequence-major order from row_cursor (one claim ahead) and never wait: each writes its piece's partial
 // statistics and counts its arrival on the row without a fence (partials are pre-filled
 // with an empty marker that the reader polls for).  The last piece of a row to arrive merges
 // the row; the last row of a sequence to be merged runs the sequence's scan (one warp) and
@@ -868,15 +1195,6 @@ __global__ void __launch_bounds__(256, 4) race_block_kernel(VerifyParams p) {
 #define SPECVERIFY_FUSED_MINBLOCKS 4
 #endif
 constexpr int kStreamWarps = SPECVERIFY_STREAM_WARPS;  // of the 8 warps of a block (the rest race)
-
-constexpr uint32_t kDebugNeverReady = 1u;         // scans never set ready[b] (tests)
-constexpr unsigned long long kWaitLimitNs = 500000000ull;  // give up a wait after 0.5 s
-
-__device__ __forceinline__ unsigned long long global_time_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-    return t;
-}
 
 __device__ __forceinline__ int ld_acquire(const int* p) {
     int v;
@@ -1068,12 +1386,15 @@ __global__ void __launch_bounds__(256, SPECVERIFY_FUSED_MINBLOCKS) verify_fused_
     const int RP = R * P;
     const long long total_rows = static_cast<long long>(p.B) * RP;
     if ((threadIdx.x >> 5) < kStreamWarps) {
-        // streaming warps take row items round-robin (their items all cost the same)
-        const long long sw = static_cast<long long>(blockIdx.x) * kStreamWarps + (threadIdx.x >> 5);
-        const long long nsw = static_cast<long long>(gridDim.x) * kStreamWarps;
         // pending arrival of the previous row item (lane 0 holds the ticket)
         int pend_ticket = 0, pend_b = -1, pend_r = 0;
-        for (long long g = sw; g < total_rows; g += nsw) {
+        long long next = 0;
+        if (lane == 0) next = atomicAdd(reinterpret_cast<unsigned long long*>(p.row_cursor), 1ull);
+        next = __shfl_sync(0xffffffffu, next, 0);
+        while (next < total_rows) {
+            const long long g = next;
+            if (lane == 0)  // the next claim, used after this item
+                next = atomicAdd(reinterpret_cast<unsigned long long*>(p.row_cursor), 1ull);
             const int b = static_cast<int>(g / RP);
             const int within = static_cast<int>(g % RP);
             const int r = within / P;
@@ -1084,6 +1405,7 @@ __global__ void __launch_bounds__(256, SPECVERIFY_FUSED_MINBLOCKS) verify_fused_
                 pend_ticket = atomicAdd(p.row_done + static_cast<long long>(b) * R + r, 1);
             pend_b = b;
             pend_r = r;
+            next = __shfl_sync(0xffffffffu, next, 0);
         }
         if (pend_b >= 0)
             resolve_arrival<ET>(p, __shfl_sync(0xffffffffu, pend_ticket, 0), pend_b, pend_r, lane);

@@ -57,11 +57,11 @@ __host__ __device__ __forceinline__ PhiloxRoundKeys philox_round_keys(PhiloxKey 
     return rk;
 }
 
-// One 32x32 -> 64-bit product (a single wide multiply) split into its halves.
+// One 32x32 -> 64-bit product (PTX mul.wide.u32) split into its halves.
 __device__ __forceinline__ void mul_wide(uint32_t a, uint32_t b, uint32_t& hi, uint32_t& lo) {
-    const unsigned long long p = static_cast<unsigned long long>(a) * b;
-    hi = static_cast<uint32_t>(p >> 32);
-    lo = static_cast<uint32_t>(p);
+    asm("{.reg .b64 t; mul.wide.u32 t, %2, %3; mov.b64 {%0, %1}, t;}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(a), "r"(b));
 }
 
 __device__ __forceinline__ void philox_round(uint4& c, uint32_t k0, uint32_t k1) {

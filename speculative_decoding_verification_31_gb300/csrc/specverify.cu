@@ -21,7 +21,10 @@ constexpr int kMaxGamma = 2048;          // the scan keeps 2*gamma+1 row statist
 #endif
 constexpr int kPieceBytes = SPECVERIFY_PIECE_BYTES;  // bytes of one row piece (one warp item)
 constexpr int kThreads = 256;
-constexpr int kUnroll = 4;               // 16-byte loads in flight per lane in the streaming pass
+#ifndef SPECVERIFY_UNROLL
+#define SPECVERIFY_UNROLL 8
+#endif
+constexpr int kUnroll = SPECVERIFY_UNROLL;  // 16-byte loads in flight per lane in the streaming pass
 #ifndef SPECVERIFY_FUSED_UNROLL
 #define SPECVERIFY_FUSED_UNROLL 4
 #endif
@@ -37,7 +40,8 @@ struct Layout {
     int rpiece_len, rpieces;
     size_t stat_off, seq_off, race_off, rowstat_off;
     size_t ctl_off, ctl_bytes;          // zeroed control block: row_done, seq_done, tickets, ready
-    size_t row_done_off, seq_done_off, ticket_off, ready_off, race_cursor_off;
+    size_t row_done_off, seq_done_off, ticket_off, ready_off, race_cursor_off,
+        row_cursor_off;
     size_t total;
 };
 
@@ -69,6 +73,8 @@ Layout layout_of(int B, int gamma, int V, int dtype) {
     off += static_cast<size_t>(B) * sizeof(int);
     off = align_up(off, 8);
     L.race_cursor_off = off;
+    off += sizeof(unsigned long long);
+    L.row_cursor_off = off;
     off += sizeof(unsigned long long);
     L.ctl_bytes = off - L.ctl_off;
     off = align_up(off, 256);
@@ -162,6 +168,7 @@ void bind_workspace(VerifyParams& p, const Layout& L, char* ws) {
     p.tickets = reinterpret_cast<int*>(ws + L.ticket_off);
     p.ready = reinterpret_cast<int*>(ws + L.ready_off);
     p.race_cursor = reinterpret_cast<int*>(ws + L.race_cursor_off);
+    p.row_cursor = reinterpret_cast<int*>(ws + L.row_cursor_off);
 }
 
 // Validated common set-up of a call: fills `p` with the workspace pointers.
@@ -227,6 +234,8 @@ int launch_fused(VerifyParams& p, int sm_count, const spec_verify_opts* o, cudaS
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
 }
 
+// Two-kernel sampling verify: the streaming pass, then the scan-race kernel as its
+// programmatic dependent (its blocks start while the streaming pass drains).
 template <class ET>
 int launch_sampling(VerifyParams& p, int sm_count, const spec_verify_opts* o, cudaStream_t s) {
     const int R = 2 * p.gamma + 1;
@@ -235,10 +244,18 @@ int launch_sampling(VerifyParams& p, int sm_count, const spec_verify_opts* o, cu
     row_stats_kernel<ET, kUnroll><<<grid_for(row_stats_kernel<ET, kUnroll>, sm_count, stat_items),
                                     kThreads, 0, s>>>(p);
     record(o, 1, s);
-    scan_kernel<ET><<<p.B, kThreads, 2 * R * sizeof(float), s>>>(p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(static_cast<long long>(p.B) * p.rpieces));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 2 * R * sizeof(float);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = (o && o->prof_events[1]) ? 0 : 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, scan_race_kernel<ET>, p) != cudaSuccess) return SPEC_ECUDA;
     record(o, 2, s);
-    race_block_kernel<ET><<<static_cast<unsigned>(static_cast<long long>(p.B) * p.rpieces), kThreads, 0, s>>>(p);
-    record(o, 3, s);
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
 }
 
@@ -304,13 +321,13 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, const in
         p.out_u = opts->out_u;
         p.out_race = opts->out_race;
     }
-    p.debug_flags = (opts && (opts->debug_flags & SPEC_DEBUG_NEVER_READY)) ? kDebugNeverReady : 0u;
+    p.debug_flags = (opts && (opts->flags & SPEC_DEBUG_NEVER_READY)) ? kDebugNeverReady : 0u;
     DeviceState* d = nullptr;
     char* ws = nullptr;
     rc = prepare(B, gamma, V, dtype, opts, p, &d, &ws);
     if (rc) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const bool fused = d->coop && !(opts && (opts->debug_flags & SPEC_DEBUG_UNFUSED));
+    const bool fused = d->coop && opts && (opts->flags & SPEC_FLAG_FUSED);
     if (fused) {
         const Layout L = layout_of(B, gamma, V, dtype);
         return dtype == SPEC_F32 ? launch_fused<F32Elem>(p, d->sm_count, opts, s, L, ws)
@@ -479,14 +496,14 @@ extern "C" int spec_verify_noalloc(const void* target_logits, const void* draft_
     }
     char* ws = nd->scratch;
     bind_workspace(p, L, ws);
-    p.debug_flags = (opts && (opts->debug_flags & SPEC_DEBUG_NEVER_READY)) ? kDebugNeverReady : 0u;
+    p.debug_flags = (opts && (opts->flags & SPEC_DEBUG_NEVER_READY)) ? kDebugNeverReady : 0u;
     if (opts && opts->d_status) {
         p.status = opts->d_status;
     } else {
         p.status = reinterpret_cast<int32_t*>(ws + kNoallocStatusOff);
         if (cudaMemsetAsync(p.status, 0, sizeof(int32_t), s) != cudaSuccess) return SPEC_ECUDA;
     }
-    if (nd->coop && !(opts && (opts->debug_flags & SPEC_DEBUG_UNFUSED)))
+    if (nd->coop && opts && (opts->flags & SPEC_FLAG_FUSED))
         return dtype == SPEC_F32 ? launch_fused<F32Elem>(p, nd->sm_count, opts, s, L, ws)
                                  : launch_fused<Bf16Elem>(p, nd->sm_count, opts, s, L, ws);
     return dtype == SPEC_F32 ? launch_sampling<F32Elem>(p, nd->sm_count, opts, s)

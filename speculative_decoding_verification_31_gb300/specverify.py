@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libspecverify.so")
 SPEC_OK, SPEC_EINVAL, SPEC_ECUDA, SPEC_EBADTOKEN, SPEC_ETIMEOUT, SPEC_ENOMEM = range(6)
 SPEC_ESCRATCH = 6
 SPEC_NOALLOC_SCRATCH_BYTES = 8 << 20
-SPEC_DEBUG_UNFUSED, SPEC_DEBUG_NEVER_READY = 1, 2
+SPEC_FLAG_FUSED, SPEC_DEBUG_NEVER_READY = 1, 2
 SPEC_F32, SPEC_BF16 = 0, 1
 
 EXPORTED = ("spec_verify", "spec_verify_greedy", "spec_verify_ex", "spec_verify_greedy_ex",
@@ -50,7 +50,7 @@ class SpecVerifyOpts(ctypes.Structure):
         ("out_u", ctypes.c_void_p),
         ("out_race", ctypes.c_void_p),
         ("prof_events", ctypes.c_void_p * 4),
-        ("debug_flags", ctypes.c_uint32),
+        ("flags", ctypes.c_uint32),
     ]
 
 
@@ -167,11 +167,11 @@ def spec_verify_greedy(target_logits, draft_tokens, out_tokens=None, out_n_accep
 
 
 def _make_opts(dtype, T_per_seq, Td_per_seq, seq_index_base, workspace, d_status, diag,
-               prof_events: Optional[Sequence], debug_flags: int = 0):
+               prof_events: Optional[Sequence], flags: int = 0):
     o = SpecVerifyOpts()
     load_library().spec_verify_opts_init(ctypes.byref(o))
     o.dtype = dtype
-    o.debug_flags = int(debug_flags)
+    o.flags = int(flags)
     o.seq_index_base = int(seq_index_base)
     o.T_per_seq = T_per_seq.data_ptr() if T_per_seq is not None else None
     o.Td_per_seq = Td_per_seq.data_ptr() if Td_per_seq is not None else None
@@ -207,7 +207,7 @@ def _check_temps(t, B, dev, name):
 def spec_verify_ex(target_logits, draft_logits, draft_tokens, T: float, T_d: float, seed: int,
                    out_tokens=None, out_n_accepted=None, *, T_per_seq=None, Td_per_seq=None,
                    seq_index_base: int = 0, workspace=None, d_status=None,
-                   diagnostics: bool = False, prof_events=None, debug_flags: int = 0,
+                   diagnostics: bool = False, prof_events=None, flags: int = 0,
                    stream=None):
     """Full form (see ``spec_verify_ex`` in the C header).  Returns
     (out_tokens, out_n_accepted, diag) where diag holds the diagnostic outputs when
@@ -227,7 +227,7 @@ def spec_verify_ex(target_logits, draft_logits, draft_tokens, T: float, T_d: flo
                 "u": torch.full((B, g), float("nan"), **f),
                 "race": torch.full((B, 2), float("nan"), **f)}
     o = _make_opts(_dtype_code(target_logits), T_per_seq, Td_per_seq, seq_index_base, workspace,
-                   d_status, diag, prof_events, debug_flags)
+                   d_status, diag, prof_events, flags)
     rc = load_library().spec_verify_ex(
         _ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), B, g, V, float(T),
         float(T_d), int(seed) & (2**64 - 1), _ptr(out_tokens), _ptr(out_n_accepted),
@@ -255,7 +255,7 @@ def spec_verify_greedy_ex(target_logits, draft_tokens, out_tokens=None, out_n_ac
 def spec_verify_noalloc(target_logits, draft_logits, draft_tokens, T: float, T_d: float,
                         seed: int, out_tokens, out_n_accepted, *, T_per_seq=None,
                         Td_per_seq=None, seq_index_base: int = 0, d_status=None, diag=None,
-                        stream=None):
+                        flags: int = 0, stream=None):
     """Allocation-free sampling verify (see ``spec_verify_noalloc`` in the C header): the
     library's scratch is a static device array, so nothing is allocated by the library.  The
     caller passes every output, including the optional diagnostic tensors in ``diag`` (a dict
@@ -267,7 +267,7 @@ def spec_verify_noalloc(target_logits, draft_logits, draft_tokens, T: float, T_d
     T_per_seq = _check_temps(T_per_seq, B, dev, "T_per_seq")
     Td_per_seq = _check_temps(Td_per_seq, B, dev, "Td_per_seq")
     o = _make_opts(_dtype_code(target_logits), T_per_seq, Td_per_seq, seq_index_base, None,
-                   d_status, diag, None)
+                   d_status, diag, None, flags)
     rc = load_library().spec_verify_noalloc(
         _ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), B, g, V, float(T),
         float(T_d), int(seed) & (2**64 - 1), _ptr(out_tokens), _ptr(out_n_accepted),

@@ -59,7 +59,7 @@ def test_opts_struct_layout_matches_c(lib, tmp_path):
         "int main(void){printf(\"%zu %zu %zu %zu\\n\", sizeof(spec_verify_opts),"
         " offsetof(spec_verify_opts, workspace_bytes), offsetof(spec_verify_opts, out_race),"
         " offsetof(spec_verify_opts, prof_events)); printf(\"%zu\\n\", offsetof(spec_verify_opts,"
-        " debug_flags)); return 0;}\n")
+        " flags)); return 0;}\n")
     exe = tmp_path / "layout"
     subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
                    check=True)
@@ -69,7 +69,7 @@ def test_opts_struct_layout_matches_c(lib, tmp_path):
     assert SpecVerifyOpts.workspace_bytes.offset == ws
     assert SpecVerifyOpts.out_race.offset == race
     assert SpecVerifyOpts.prof_events.offset == prof
-    assert SpecVerifyOpts.debug_flags.offset == dbg
+    assert SpecVerifyOpts.flags.offset == dbg
 
 
 def test_strerror_and_workspace_size(lib):

@@ -256,24 +256,27 @@ def test_empty_batch_and_invalid_arguments(sv):
 
 @pytest.mark.parametrize("B,gamma,V,dtype", [(3, 4, 5003, "bf16"), (2, 7, 9000, "f32"),
                                               (4, 0, 777, "bf16"), (6, 3, 40000, "bf16")])
-def test_unfused_path_matches_fused_and_oracle(sv, orc, B, gamma, V, dtype):
-    """The three-kernel path (kept for devices without cooperative launch) and the fused
-    single-kernel path give identical outputs, and both match the oracle."""
+def test_fused_path_matches_default_and_oracle(sv, orc, B, gamma, V, dtype):
+    """The fused single-kernel path (SPEC_FLAG_FUSED) and the default two-kernel path give
+    identical outputs, and both match the oracle."""
     w = workloads.generic(B=B, gamma=gamma, V=V, dtype=dtype, seed=B * 31 + V, sigma=0.9,
                           T=0.8, Td=0.35)
     dw = DeviceWorkload(w)
     for seed in range(3):
-        fused = run_gpu(sv, dw, seed, per_seq_temps=False)
+        base = run_gpu(sv, dw, seed, per_seq_temps=False)
         t, n, d = sv.spec_verify_ex(dw.target, dw.draft, dw.tokens, float(w.T[0]),
                                     float(w.Td[0]), seed, diagnostics=True,
-                                    debug_flags=sv.SPEC_DEBUG_UNFUSED)
+                                    flags=sv.SPEC_FLAG_FUSED)
         torch.cuda.synchronize()
-        np.testing.assert_array_equal(t.cpu().numpy(), fused["tokens"])
-        np.testing.assert_array_equal(n.cpu().numpy(), fused["n"])
+        np.testing.assert_array_equal(t.cpu().numpy(), base["tokens"])
+        np.testing.assert_array_equal(n.cpu().numpy(), base["n"])
+        fused = {k: v.cpu().numpy() for k, v in d.items()}
+        fused.update(tokens=t.cpu().numpy(), n=n.cpu().numpy())
         for k in ("logp", "logq", "logZp", "logZq", "u"):
-            np.testing.assert_allclose(d[k].cpu().numpy(), fused[k], rtol=2e-6, atol=2e-6,
+            np.testing.assert_allclose(fused[k], base[k], rtol=2e-6, atol=2e-6,
                                        equal_nan=True, err_msg=k)
         r = orc.verify(w.target, w.draft, w.tokens, w.T, w.Td, seed)
+        compare_sampling(w, base, r)
         compare_sampling(w, fused, r)
 
 
@@ -286,7 +289,7 @@ def test_bounded_wait_times_out_and_context_survives(sv, orc):
     dw = DeviceWorkload(w)
     t0 = time.time()
     sv.spec_verify_ex(dw.target, dw.draft, dw.tokens, 1.0, 1.0, 0,
-                      debug_flags=sv.SPEC_DEBUG_NEVER_READY)
+                      flags=sv.SPEC_FLAG_FUSED | sv.SPEC_DEBUG_NEVER_READY)
     assert sv.spec_verify_check() == sv.SPEC_ETIMEOUT
     assert time.time() - t0 < 30
     g = run_gpu(sv, dw, 0, per_seq_temps=False)
