@@ -48,6 +48,7 @@ struct VerifyParams {
     int B, gamma, V;
     int piece_len, npieces;     // elements per row piece, pieces per row (streaming pass)
     int rpiece_len, rpieces;    // the same for the race pass (finer: the race is compute-bound)
+    int rgroups;                // scan-race blocks per sequence (each races rpieces / rgroups pieces)
     float T, Td;                // scalar temperatures
     const float* T_seq;         // [B] or nullptr
     const float* Td_seq;        // [B] or nullptr
@@ -872,14 +873,16 @@ __global__ void __launch_bounds__(256, 4) race_block_kernel(VerifyParams p) {
 }
 
 // ----------------------------------------------------------------------------------------
-// scan_race: one block per race piece (b, piece) of kRaceBlockTokens tokens.  Every block of
-// sequence b repeats the sequence's scan (row merges, gathers, u_i, first rejection j) --
-// cheap next to its piece of the race -- so no separate scan launch sits between the
-// streaming pass and the race; the block of piece 0 writes the sequence's outputs.  The
+// scan_race: G blocks per sequence b, block g racing pieces g, g + G, ... (kRaceBlockTokens
+// tokens each) of the raced row, loading each next piece while computing the current one
+// and carrying its best score over as the next piece's threshold.  Every block of sequence
+// b repeats the sequence's scan (row merges up to the first rejection, gathers, u_i) --
+// cheap next to its share of the race -- so no separate scan launch sits between the
+// streaming pass and the race; block 0 of the sequence writes the sequence's outputs.  The
 // kernel is launched as a programmatic dependent of row_stats: before waiting for it, a
 // block gathers p(d_i), q(d_i) inputs and draws its uniforms.  Race partials are single
-// 64-bit words (score, index + 1) that the streaming pass emptied; the last block of a
-// sequence (by a relaxed arrival count) polls them, so no fence is needed.
+// 64-bit words (score, index + 1), one per block, that the streaming pass emptied; the last
+// block of a sequence (by a relaxed arrival count) polls them, so no fence is needed.
 // ----------------------------------------------------------------------------------------
 
 __device__ __forceinline__ unsigned long long pack_race(float best, int idx) {
@@ -902,15 +905,16 @@ __global__ void __launch_bounds__(256, 4) scan_race_kernel(VerifyParams p) {
     __shared__ float s_thr[8];
     __shared__ RaceState s_best[8];
     const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
-    const int b = blockIdx.x / p.rpieces;
-    const int piece = blockIdx.x % p.rpieces;
+    const int G = p.rgroups;  // blocks per sequence
+    const int b = blockIdx.x / G;
+    const int g = blockIdx.x % G;
     const int R = 2 * p.gamma + 1;
     float* sm_m = smem;
     float* sm_l = smem + R;
     const float Tb = seq_T(p, b), Tdb = seq_Td(p, b);
     const float cp = scale_of(Tb), cq = scale_of(Tdb);
     const uint32_t bg = p.seq_base + static_cast<uint32_t>(b);
-    const bool writer = (piece == 0);
+    const bool writer = (g == 0);
     // diagnostics need every row's statistics; otherwise rows are merged only up to the first
     // rejection, four positions (target and draft rows in parallel) at a time
     const bool all_rows = writer && (p.out_logZp || p.out_logZq || p.out_logp || p.out_logq);
@@ -1039,8 +1043,6 @@ __global__ void __launch_bounds__(256, 4) scan_race_kernel(VerifyParams p) {
                            : nullptr;
     const uint32_t pos = static_cast<uint32_t>(j);
     const RaceRowRng q = race_row_rng(p.rk, bg, pos);
-    const int x0 = piece * kRaceBlockTokens + wib * kRaceWarpTokens;
-    const int x1 = min(p.V, x0 + kRaceWarpTokens);
     RaceState st{-INFINITY, INT_MAX, -INFINITY};
     auto word_at = [&](int x) {
         const uint4 blk = race_block_fast(q, p.rk, static_cast<uint32_t>(x) >> 2);
@@ -1051,79 +1053,114 @@ __global__ void __launch_bounds__(256, 4) scan_race_kernel(VerifyParams p) {
         const float sc = race_exact_score(xt, xd, si, residual, w);
         if (sc > -INFINITY) race_offer(st, sc, x);
     };
-    const bool vec_ok = x0 < x1 && (reinterpret_cast<uintptr_t>(rt + x0) & 15u) == 0;
-    const int nvec = vec_ok ? (x1 - x0) / ET::kVec : 0;
-    uint4 raw[VPL];
-    float seed = -INFINITY;
-    if (vec_ok) {
-        const uint4* vt = reinterpret_cast<const uint4*>(rt + x0);
+    // This block races pieces g, g + G, ... of the row (warp w: tokens [w, w+1) x 1024 of a
+    // piece).  Vectors of the next piece are loaded before the current one is computed.
+    auto load_piece = [&](int pc, uint4 (&dst)[VPL]) {
+        const int x0 = pc * kRaceBlockTokens + wib * kRaceWarpTokens;
+        const int x1 = min(p.V, x0 + kRaceWarpTokens);
+        const bool ok = x0 < x1 && (reinterpret_cast<uintptr_t>(rt + x0) & 15u) == 0;
+        const int nv = ok ? (x1 - x0) / ET::kVec : 0;
+        const uint4* vt = reinterpret_cast<const uint4*>(rt + (ok ? x0 : 0));
 #pragma unroll
         for (int k = 0; k < VPL; ++k) {
             const int v = lane + 32 * k;
-            raw[k] = v < nvec ? __ldg(vt + v) : make_uint4(ET::kNegInfWord, ET::kNegInfWord,
-                                                           ET::kNegInfWord, ET::kNegInfWord);
+            dst[k] = v < nv ? __ldg(vt + v) : make_uint4(ET::kNegInfWord, ET::kNegInfWord,
+                                                         ET::kNegInfWord, ET::kNegInfWord);
         }
-        float vmax = -INFINITY;
-        int xs = -1;
+    };
+    uint4 raw[VPL], raw_next[VPL];
+    load_piece(g, raw);
+    float thr = -INFINITY;
+    bool first = true;
+    for (int pc = g; pc < p.rpieces; pc += G) {
+        const int x0 = pc * kRaceBlockTokens + wib * kRaceWarpTokens;
+        const int x1 = min(p.V, x0 + kRaceWarpTokens);
+        const bool vec_ok = x0 < x1 && (reinterpret_cast<uintptr_t>(rt + x0) & 15u) == 0;
+        const int nvec = vec_ok ? (x1 - x0) / ET::kVec : 0;
+        if (pc + G < p.rpieces) load_piece(pc + G, raw_next);
+        if (first) {
+            // seed: each lane's largest logit, scored by a fast lower bound
+            float seed = -INFINITY;
+            if (vec_ok) {
+                float vmax = -INFINITY;
+                int xs = -1;
 #pragma unroll
-        for (int k = 0; k < VPL; ++k) {
-            float ft[ET::kVec];
-            ET::widen(raw[k], ft);
+                for (int k = 0; k < VPL; ++k) {
+                    float ft[ET::kVec];
+                    ET::widen(raw[k], ft);
+                    float m = ft[0];
 #pragma unroll
-            for (int e = 0; e < ET::kVec; ++e)
-                if (ft[e] > vmax) {
-                    vmax = ft[e];
-                    xs = x0 + (lane + 32 * k) * ET::kVec + e;
+                    for (int e = 1; e < ET::kVec; ++e) m = fmaxf(m, ft[e]);
+                    if (m > vmax) {
+                        vmax = m;
+#pragma unroll
+                        for (int e = ET::kVec - 1; e >= 0; --e)
+                            if (ft[e] == m) xs = x0 + (lane + 32 * k) * ET::kVec + e;
+                    }
                 }
-        }
-        if (xs >= 0) {
-            const float xd = residual ? ET::load1(rd + xs) : 0.0f;
-            seed = race_score_lower_bound(vmax, xd, si, residual, word_at(xs));
-        }
-    }
-    seed = float_unorder(__reduce_max_sync(0xffffffffu, float_order(seed)));
-    if (lane == 0) s_thr[wib] = seed;
-    __syncthreads();
-    float thr = s_thr[0];
-#pragma unroll
-    for (int k = 1; k < 8; ++k) thr = fmaxf(thr, s_thr[k]);
-    if (vec_ok) {
-        const float mpl = si.mp + si.l2sp;
-#pragma unroll
-        for (int k = 0; k < VPL; ++k) {
-            const int v = lane + 32 * k;
-            const float C = (thr > -INFINITY) ? 32.0f + kRaceBoundMargin2 - thr * kLog2e - mpl
-                                              : INFINITY;
-            if (v < nvec) {
-                float ft[ET::kVec];
-                ET::widen(raw[k], ft);
-                const int xv = x0 + v * ET::kVec;
-                uint32_t cand = 0;
-                uint4 blk[ET::kVec / 4];
-#pragma unroll
-                for (int g = 0; g < ET::kVec / 4; ++g)
-                    blk[g] = race_block_fast(q, p.rk, static_cast<uint32_t>(xv + 4 * g) >> 2);
-#pragma unroll
-                for (int g = 0; g < ET::kVec / 4; ++g) {
-                    const uint32_t w4[4] = {blk[g].x, blk[g].y, blk[g].z, blk[g].w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        cand |= (lg2_fast(static_cast<float>(w4[e])) <= fmaf(ft[4 * g + e], si.cp, C))
-                                    ? (1u << (4 * g + e)) : 0u;
-                }
-                while (cand) {  // rare: exact scores in increasing token order
-                    const int e = __ffs(cand) - 1;
-                    cand &= cand - 1;
-                    offer_exact(ET::load1(rt + xv + e), xv + e, word_at(xv + e));
+                if (xs >= 0) {
+                    const float xd = residual ? ET::load1(rd + xs) : 0.0f;
+                    seed = race_score_lower_bound(vmax, xd, si, residual, word_at(xs));
                 }
             }
-            thr = fmaxf(thr, float_unorder(__reduce_max_sync(0xffffffffu, float_order(st.best))));
+            seed = float_unorder(__reduce_max_sync(0xffffffffu, float_order(seed)));
+            if (lane == 0) s_thr[wib] = seed;
+            __syncthreads();
+            thr = s_thr[0];
+#pragma unroll
+            for (int k = 1; k < 8; ++k) thr = fmaxf(thr, s_thr[k]);
+            first = false;
         }
-        const int t0 = nvec * ET::kVec;
-        if (lane < (x1 - x0) - t0) offer_exact(ET::load1(rt + x0 + t0 + lane), x0 + t0 + lane,
-                                               word_at(x0 + t0 + lane));
-    } else {
-        for (int x = x0 + lane; x < x1; x += 32) offer_exact(ET::load1(rt + x), x, word_at(x));
+        if (vec_ok) {
+            const float mpl = si.mp + si.l2sp;
+#pragma unroll
+            for (int k = 0; k < VPL; ++k) {
+                const int v = lane + 32 * k;
+                const float C = (thr > -INFINITY) ? 32.0f + kRaceBoundMargin2 - thr * kLog2e - mpl
+                                                  : INFINITY;
+                if (v < nvec) {
+                    float ft[ET::kVec];
+                    ET::widen(raw[k], ft);
+                    const int xv = x0 + v * ET::kVec;
+                    uint32_t cand = 0;
+                    uint4 blk[ET::kVec / 4];
+#pragma unroll
+                    for (int gg = 0; gg < ET::kVec / 4; ++gg)
+                        blk[gg] = race_block_fast(q, p.rk, static_cast<uint32_t>(xv + 4 * gg) >> 2);
+#pragma unroll
+                    for (int gg = 0; gg < ET::kVec / 4; ++gg) {
+                        const uint32_t w4[4] = {blk[gg].x, blk[gg].y, blk[gg].z, blk[gg].w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            cand |= (lg2_fast(static_cast<float>(w4[e])) <= fmaf(ft[4 * gg + e], si.cp, C))
+                                        ? (1u << (4 * gg + e)) : 0u;
+                    }
+                    while (cand) {  // rare: exact scores in increasing token order
+                        const int e = __ffs(cand) - 1;
+                        cand &= cand - 1;
+                        offer_exact(ET::load1(rt + xv + e), xv + e, word_at(xv + e));
+                    }
+                }
+                thr = fmaxf(thr, float_unorder(__reduce_max_sync(0xffffffffu, float_order(st.best))));
+            }
+            const int t0 = nvec * ET::kVec;
+            if (lane < (x1 - x0) - t0) offer_exact(ET::load1(rt + x0 + t0 + lane), x0 + t0 + lane,
+                                                   word_at(x0 + t0 + lane));
+        } else {
+            for (int x = x0 + lane; x < x1; x += 32) offer_exact(ET::load1(rt + x), x, word_at(x));
+        }
+        if (pc + G < p.rpieces) {
+            // the block's best so far bounds the sequence's best from below: carry it over
+            if (lane == 0) s_thr[wib] = thr;
+            __syncthreads();
+            float t = s_thr[0];
+#pragma unroll
+            for (int k = 1; k < 8; ++k) t = fmaxf(t, s_thr[k]);
+            thr = fmaxf(thr, t);
+            __syncthreads();
+#pragma unroll
+            for (int k = 0; k < VPL; ++k) raw[k] = raw_next[k];
+        }
     }
     st = warp_race_merge(st);
     if (lane == 0) s_best[wib] = st;
@@ -1132,15 +1169,15 @@ __global__ void __launch_bounds__(256, 4) scan_race_kernel(VerifyParams p) {
     if (threadIdx.x == 0) {
         RaceState m = s_best[0];
         for (int k = 1; k < 8; ++k) m = race_merge(m, s_best[k]);
-        parts[piece].second = m.second;  // diagnostic only
-        *reinterpret_cast<unsigned long long*>(parts + piece) = pack_race(m.best, m.idx);
-        s_last = (atomicAdd(p.tickets + b, 1) == p.rpieces - 1);
+        parts[g].second = m.second;  // diagnostic only
+        *reinterpret_cast<unsigned long long*>(parts + g) = pack_race(m.best, m.idx);
+        s_last = (atomicAdd(p.tickets + b, 1) == G - 1);
     }
     __syncthreads();
     if (!s_last || wib != 0) return;
-    // last piece of this sequence: merge every piece's winner, waiting (bounded) for each
+    // last block of this sequence: merge every block's winner, waiting (bounded) for each
     RaceState m{-INFINITY, INT_MAX, -INFINITY};
-    for (int k = lane; k < p.rpieces; k += 32) {
+    for (int k = lane; k < G; k += 32) {
         unsigned long long v = ld_relaxed_u64g(parts + k);
         if (v == 0ull) {
             const unsigned long long t0 = global_time_ns();
@@ -1175,7 +1212,7 @@ __global__ void __launch_bounds__(256, 4) scan_race_kernel(VerifyParams p) {
 // specialised warps.
 //
 // Streaming warps (the first kStreamWarps of each block) claim row items (b, r, piece) in
-// sequence-major order from row_cursor (one claim ahead) and never wait: each writes its piece's partial
+// sequence-major order from row_cursor, kClaimChunk at a time, and never wait: each writes its piece's partial
 // statistics and counts its arrival on the row without a fence (partials are pre-filled
 // with an empty marker that the reader polls for).  The last piece of a row to arrive merges
 // the row; the last row of a sequence to be merged runs the sequence's scan (one warp) and
@@ -1195,6 +1232,10 @@ __global__ void __launch_bounds__(256, 4) scan_race_kernel(VerifyParams p) {
 #define SPECVERIFY_FUSED_MINBLOCKS 4
 #endif
 constexpr int kStreamWarps = SPECVERIFY_STREAM_WARPS;  // of the 8 warps of a block (the rest race)
+#ifndef SPECVERIFY_CLAIM_CHUNK
+#define SPECVERIFY_CLAIM_CHUNK 1
+#endif
+constexpr int kClaimChunk = SPECVERIFY_CLAIM_CHUNK;     // row items per claim of the cursor
 
 __device__ __forceinline__ int ld_acquire(const int* p) {
     int v;
@@ -1388,13 +1429,17 @@ __global__ void __launch_bounds__(256, SPECVERIFY_FUSED_MINBLOCKS) verify_fused_
     if ((threadIdx.x >> 5) < kStreamWarps) {
         // pending arrival of the previous row item (lane 0 holds the ticket)
         int pend_ticket = 0, pend_b = -1, pend_r = 0;
-        long long next = 0;
-        if (lane == 0) next = atomicAdd(reinterpret_cast<unsigned long long*>(p.row_cursor), 1ull);
-        next = __shfl_sync(0xffffffffu, next, 0);
-        while (next < total_rows) {
-            const long long g = next;
-            if (lane == 0)  // the next claim, used after this item
-                next = atomicAdd(reinterpret_cast<unsigned long long*>(p.row_cursor), 1ull);
+        // row items are claimed kClaimChunk at a time (one atomic per chunk on the shared
+        // cursor); the next chunk is claimed while the current one streams
+        unsigned long long* cursor = reinterpret_cast<unsigned long long*>(p.row_cursor);
+        long long chunk = 0, next_chunk = 0;
+        if (lane == 0) chunk = atomicAdd(cursor, static_cast<unsigned long long>(kClaimChunk));
+        chunk = __shfl_sync(0xffffffffu, chunk, 0);
+        int in_chunk = 0;
+        while (chunk + in_chunk < total_rows) {
+            const long long g = chunk + in_chunk;
+            if (in_chunk == 0 && lane == 0)  // the next claim, used after this chunk
+                next_chunk = atomicAdd(cursor, static_cast<unsigned long long>(kClaimChunk));
             const int b = static_cast<int>(g / RP);
             const int within = static_cast<int>(g % RP);
             const int r = within / P;
@@ -1405,7 +1450,10 @@ __global__ void __launch_bounds__(256, SPECVERIFY_FUSED_MINBLOCKS) verify_fused_
                 pend_ticket = atomicAdd(p.row_done + static_cast<long long>(b) * R + r, 1);
             pend_b = b;
             pend_r = r;
-            next = __shfl_sync(0xffffffffu, next, 0);
+            if (++in_chunk == kClaimChunk) {
+                chunk = __shfl_sync(0xffffffffu, next_chunk, 0);
+                in_chunk = 0;
+            }
         }
         if (pend_b >= 0)
             resolve_arrival<ET>(p, __shfl_sync(0xffffffffu, pend_ticket, 0), pend_b, pend_r, lane);

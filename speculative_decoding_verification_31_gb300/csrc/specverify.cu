@@ -20,6 +20,8 @@ constexpr int kMaxGamma = 2048;          // the scan keeps 2*gamma+1 row statist
 #define SPECVERIFY_PIECE_BYTES 16384
 #endif
 constexpr int kPieceBytes = SPECVERIFY_PIECE_BYTES;  // bytes of one row piece (one warp item)
+constexpr int kMinPieceBytes = 8192;                 // range the streaming pass picks from
+constexpr int kMaxPieceBytes = 32768;
 constexpr int kThreads = 256;
 #ifndef SPECVERIFY_UNROLL
 #define SPECVERIFY_UNROLL 8
@@ -45,17 +47,44 @@ struct Layout {
     size_t total;
 };
 
-Layout layout_of(int B, int gamma, int V, int dtype) {
+// Pieces per row for the streaming pass: between kMinPieceBytes and kMaxPieceBytes of logits,
+// chosen so that the row items fill whole rounds of the grid's `stream_warps` warps (the
+// last, partly idle round costs a whole item's time).  stream_warps = 0 takes the default
+// piece size (for sizing the workspace, which is allocated for the most pieces).
+void choose_pieces(int B, int gamma, int V, int dtype, long long stream_warps, int* len, int* np) {
+    const int es = elem_bytes(dtype);
+    const long long rows = static_cast<long long>(B) * (2 * gamma + 1);
+    int best_len = kPieceBytes / es;
+    if (stream_warps > 0) {
+        double best_eff = -1.0;
+        for (int bytes = kMaxPieceBytes; bytes >= kMinPieceBytes; bytes -= 1024) {
+            const int l = bytes / es;
+            const long long pcs = (V + l - 1) / l;
+            const long long items = rows * pcs;
+            const long long rounds = (items + stream_warps - 1) / stream_warps;
+            const double eff = static_cast<double>(items) / (rounds * stream_warps);
+            if (eff > best_eff + 0.02) {  // prefer bigger pieces unless clearly better filled
+                best_eff = eff;
+                best_len = l;
+            }
+        }
+    }
+    *len = best_len;
+    *np = (V + best_len - 1) / best_len;
+}
+
+Layout layout_of(int B, int gamma, int V, int dtype, long long stream_warps = 0) {
     Layout L{};
-    L.piece_len = kPieceBytes / elem_bytes(dtype);
-    L.npieces = (V + L.piece_len - 1) / L.piece_len;
+    choose_pieces(B, gamma, V, dtype, stream_warps, &L.piece_len, &L.npieces);
+    // the workspace always holds the most pieces any choice can give
+    const int max_np = (V + kMinPieceBytes / elem_bytes(dtype) - 1) / (kMinPieceBytes / elem_bytes(dtype));
     // race pieces: one block of kRaceBlockTokens tokens each
     L.rpiece_len = kRaceBlockTokens;
     L.rpieces = (V + kRaceBlockTokens - 1) / kRaceBlockTokens;
     const size_t R = 2 * static_cast<size_t>(gamma) + 1;
     size_t off = 0;
     L.stat_off = off;
-    off = align_up(off + static_cast<size_t>(B) * R * L.npieces * sizeof(float2), 256);
+    off = align_up(off + static_cast<size_t>(B) * R * max_np * sizeof(float2), 256);
     L.seq_off = off;
     off = align_up(off + static_cast<size_t>(B) * sizeof(SeqInfo), 256);
     L.race_off = off;
@@ -86,6 +115,7 @@ struct DeviceState {
     bool init = false;
     int sm_count = 0;
     int coop = 0;               // cooperative launch supported
+    long long stream_warps[2] = {0, 0};  // warps of a full streaming grid, per dtype
     void* ws = nullptr;
     size_t ws_bytes = 0;
     int32_t* status = nullptr;  // library status word (its own allocation)
@@ -150,6 +180,16 @@ int grid_for(K kernel, int sm_count, long long warp_items) {
     return static_cast<int>(g < 1 ? 1 : g);
 }
 
+// Warps of the streaming kernel's full grid (the grid_for cap).
+long long stream_warps_of(int sm_count, int dtype) {
+    int per_sm = 0;
+    cudaError_t e = dtype == SPEC_F32
+        ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, row_stats_kernel<F32Elem, kUnroll>, kThreads, 0)
+        : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, row_stats_kernel<Bf16Elem, kUnroll>, kThreads, 0);
+    if (e != cudaSuccess || per_sm < 1) per_sm = 1;
+    return static_cast<long long>(sm_count) * per_sm * (kThreads / 32);
+}
+
 void record(const spec_verify_opts* o, int k, cudaStream_t s) {
     if (o && o->prof_events[k]) cudaEventRecord(static_cast<cudaEvent_t>(o->prof_events[k]), s);
 }
@@ -177,7 +217,9 @@ int prepare(int B, int gamma, int V, int dtype, const spec_verify_opts* o, Verif
     std::lock_guard<std::mutex> lock(g_mu);
     int rc = device_state(dstate);
     if (rc) return rc;
-    const Layout L = layout_of(B, gamma, V, dtype);
+    long long& sw = (*dstate)->stream_warps[dtype == SPEC_F32 ? 0 : 1];
+    if (sw == 0) sw = stream_warps_of((*dstate)->sm_count, dtype);
+    const Layout L = layout_of(B, gamma, V, dtype, sw);
     char* ws;
     if (o && o->workspace) {
         if (o->workspace_bytes < L.total) return SPEC_ENOMEM;
@@ -244,8 +286,21 @@ int launch_sampling(VerifyParams& p, int sm_count, const spec_verify_opts* o, cu
     row_stats_kernel<ET, kUnroll><<<grid_for(row_stats_kernel<ET, kUnroll>, sm_count, stat_items),
                                     kThreads, 0, s>>>(p);
     record(o, 1, s);
+    // blocks per sequence: about one resident wave of scan-race blocks in total
+    {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, scan_race_kernel<ET>, kThreads,
+                                                          2 * R * sizeof(float)) != cudaSuccess ||
+            per_sm < 1)
+            per_sm = 1;
+        const long long wave = static_cast<long long>(sm_count) * per_sm;
+        long long G = wave / p.B;  // rounded down: no partial second wave
+        if (G > p.rpieces) G = p.rpieces;
+        if (G < 1) G = 1;
+        p.rgroups = static_cast<int>(G);
+    }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(static_cast<long long>(p.B) * p.rpieces));
+    cfg.gridDim = dim3(static_cast<unsigned>(static_cast<long long>(p.B) * p.rgroups));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = 2 * R * sizeof(float);
     cfg.stream = s;
@@ -329,7 +384,7 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, const in
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool fused = d->coop && opts && (opts->flags & SPEC_FLAG_FUSED);
     if (fused) {
-        const Layout L = layout_of(B, gamma, V, dtype);
+        const Layout L = layout_of(B, gamma, V, dtype, d->stream_warps[dtype == SPEC_F32 ? 0 : 1]);
         return dtype == SPEC_F32 ? launch_fused<F32Elem>(p, d->sm_count, opts, s, L, ws)
                                  : launch_fused<Bf16Elem>(p, d->sm_count, opts, s, L, ws);
     }
@@ -421,6 +476,7 @@ struct NoallocDevice {
     char* scratch = nullptr;  // device address of g_noalloc_scratch on this device
     int sm_count = 0;
     int coop = 0;             // cooperative launch supported
+    long long stream_warps[2] = {0, 0};
 };
 
 std::mutex g_noalloc_mu;
@@ -443,6 +499,8 @@ int noalloc_device(NoallocDevice** out) {
         if (cudaDeviceGetAttribute(&d.coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess)
             return SPEC_ECUDA;
         d.scratch = static_cast<char*>(ptr);
+        d.stream_warps[0] = stream_warps_of(d.sm_count, SPEC_F32);
+        d.stream_warps[1] = stream_warps_of(d.sm_count, SPEC_BF16);
         d.ready = true;
     }
     *out = &d;
@@ -463,11 +521,11 @@ extern "C" int spec_verify_noalloc(const void* target_logits, const void* draft_
     if (gamma > 0 && (!draft_logits || !draft_tokens || !aligned16(draft_logits))) return SPEC_EINVAL;
     if (!(opts && opts->T_per_seq) && !good_temperature(T)) return SPEC_EINVAL;
     if (!(opts && opts->Td_per_seq) && !good_temperature(T_d)) return SPEC_EINVAL;
-    const Layout L = layout_of(B, gamma, V, dtype);
-    if (L.total > kNoallocStatusOff) return SPEC_ESCRATCH;
+    if (layout_of(B, gamma, V, dtype).total > kNoallocStatusOff) return SPEC_ESCRATCH;
     NoallocDevice* nd = nullptr;
     rc = noalloc_device(&nd);
     if (rc) return rc;
+    const Layout L = layout_of(B, gamma, V, dtype, nd->stream_warps[dtype == SPEC_F32 ? 0 : 1]);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     VerifyParams p{};
