@@ -168,6 +168,28 @@ def cpu_oracle_rate(w, seed: int, budget_s: float, max_seqs: int):
 # our arm
 # -------------------------------------------------------------------------------------------
 
+def early_exit_rows_read(n: np.ndarray, gamma: int) -> tuple[int, int]:
+    """Logit rows the early-exit path streams for accepted counts n (waves of positions
+    [0,1), [1,2), [2,4), ... each reading target and draft rows, the bonus row with the
+    wave that ends at gamma), and the rows the race then reads again."""
+    waves, lo, hi = [], 0, min(1, gamma)
+    while True:
+        waves.append((lo, hi))
+        if hi == gamma:
+            break
+        lo, hi = hi, min(2 * hi, gamma)
+    streamed = raced = 0
+    for j in n.tolist():
+        if j < 0:
+            continue
+        for lo, hi in waves:
+            streamed += 2 * (hi - lo) + (1 if hi == gamma else 0)
+            if j < hi or hi == gamma:
+                break
+        raced += 2 if j < gamma else 1
+    return streamed, raced
+
+
 def run_ours(args):
     import torch
     import workloads
@@ -264,6 +286,40 @@ def run_ours(args):
     if NCU_TRAFFIC["bytes"] and NCU_TRAFFIC["sources_sha1"] == kernel_sources_sha1() and cfg == 4:
         traffic = NCU_TRAFFIC["bytes"]
 
+    # the early-exit path (SPEC_FLAG_EARLY_EXIT) on the same inputs, with the bytes it reads
+    early = None
+    if not greedy:
+        def estep():
+            kw = dict(T_per_seq=Tq, Td_per_seq=Tdq) if per_seq else {}
+            sv.spec_verify_ex(t, d, tok, float(w.T[0]), float(w.Td[0]), args.seed, out_t,
+                              out_n, seq_index_base=seq_base, flags=sv.SPEC_FLAG_EARLY_EXIT, **kw)
+        for _ in range(max(3, args.warmup)):
+            estep()
+        torch.cuda.synchronize()
+        Kx = min(K, 1000)
+        es0, es1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        es0.record(stream)
+        for _ in range(Kx):
+            estep()
+        es1.record(stream)
+        torch.cuda.synchronize()
+        ems_x = es0.elapsed_time(es1) / Kx
+        if ws_ > 1:
+            mt = torch.tensor([ems_x], device=dev, dtype=torch.float64)
+            torch.distributed.all_reduce(mt, op=torch.distributed.ReduceOp.MAX)
+            ems_x = float(mt.item())
+        streamed, raced = early_exit_rows_read(out_n.cpu().numpy(), w.gamma)
+        es_ = 2 if w.dtype == "bf16" else 4
+        early = {"value": ws_ * w.rows / (ems_x / 1e3), "unit": UNIT, "ms_per_step": ems_x,
+                 "steps": Kx, "rows_streamed_per_call": streamed, "rows_raced_per_call": raced,
+                 "logit_bytes_read_per_call": (streamed + raced) * w.V * es_,
+                 "GBps_of_bytes_read": (streamed + raced) * w.V * es_ / (ems_x / 1e3) / 1e9,
+                 "note": "same outputs as the full read; reads only rows up to each "
+                         "sequence's first rejection (counted from this call's outputs)"}
+        status = sv.spec_verify_check()
+        if status != sv.SPEC_OK:
+            raise RuntimeError(f"device status after early exit: {sv.spec_verify_strerror(status)}")
+
     # end to end: inputs from pinned host memory, outputs read back, every step
     e2e = None
     if not args.no_e2e:
@@ -338,6 +394,7 @@ def run_ours(args):
                      "peak_source": f"{peaks['source']} HBM copy bandwidth (MEASURED_PEAKS.json)"},
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "early_exit": early,
         "gpu_launches": nkern * K,
         "clocks": clocks,
     }
@@ -417,7 +474,8 @@ def run_table(args):
             out_t = torch.empty((w.B, w.gamma + 1), dtype=torch.int32, device=dev)
             out_n = torch.empty((w.B,), dtype=torch.int32, device=dev)
             kw = dict(T_per_seq=Tq, Td_per_seq=Tdq) if cfg == 3 else {}
-            modes = [("greedy", None)] if greedy else [("two-kernel", 0), ("fused", sv.SPEC_FLAG_FUSED)]
+            modes = [("greedy", None)] if greedy else [("two-kernel", 0), ("fused", sv.SPEC_FLAG_FUSED),
+                                                        ("early-exit", sv.SPEC_FLAG_EARLY_EXIT)]
             for label, dbg in modes:
                 for warm in ([False, True] if copies > 1 else [False]):
                     def call(k):

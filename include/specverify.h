@@ -91,7 +91,9 @@ typedef struct {
                                                 runner-up score (approximate) */
     void *prof_events[4];       /* optional cudaEvent_t: recorded before the first kernel and
                                    after each kernel of the call (sampling: two kernels, or
-                                   one with SPEC_FLAG_FUSED; greedy: two) */
+                                   one with SPEC_FLAG_FUSED; greedy: two; with
+                                   SPEC_FLAG_EARLY_EXIT: [1] after the last wave, [2] after
+                                   the race) */
     uint32_t flags;             /* SPEC_FLAG_* / SPEC_DEBUG_* bits; 0 in normal use */
 } spec_verify_opts;
 
@@ -101,6 +103,14 @@ typedef struct {
 #define SPEC_DEBUG_NEVER_READY 2u /* tests only, with SPEC_FLAG_FUSED: the race waits on a flag
                                      that is never set, give up after their bounded wait and
                                      report SPEC_ETIMEOUT (outputs are then invalid) */
+#define SPEC_FLAG_EARLY_EXIT 4u   /* sampling, spec_verify_ex only: read rows in waves of
+                                     positions [0,1), [1,2), [2,4), [4,8), ... and stop reading a
+                                     sequence's rows after its first rejection (the rows the
+                                     method discards).  Same outputs under the same rules as
+                                     the full read; fewer bytes when drafts are rejected early,
+                                     more launches (two per wave, plus one).  Ignored (the full
+                                     read runs) when any diagnostic output is requested, since
+                                     those cover every row. */
 
 /* Zero every field and set dtype = SPEC_BF16. */
 void spec_verify_opts_init(spec_verify_opts *opts);

@@ -69,6 +69,13 @@ struct VerifyParams {
     int* race_cursor;           // race items claimed so far (item c: sequence c / P, piece c % P)
     int* row_cursor;            // row items claimed so far (sequence-major order)
     uint32_t debug_flags;       // kDebug* test switches
+    // early-exit path: the current wave covers draft positions [wave_lo, wave_hi) of the
+    // sequences in alive[wave_parity] (all sequences in wave 0), and also row gamma
+    // (the bonus row) when wave_hi == gamma
+    int* alive[2];
+    int* alive_count[2];
+    int wave_lo, wave_hi, wave_parity;
+    long long wave_warps;       // warps of the wave_stats grid (fixes the wave's piece length)
     // outputs
     int32_t* out_tokens;        // [B, gamma+1]
     int32_t* out_n;             // [B]
@@ -79,6 +86,37 @@ struct VerifyParams {
     float* out_u;
     float* out_race;
 };
+
+// Row pieces of the streaming passes: between kMinPieceBytes and kMaxPieceBytes of logits.
+#ifndef SPECVERIFY_PIECE_BYTES
+#define SPECVERIFY_PIECE_BYTES 16384
+#endif
+constexpr int kPieceBytes = SPECVERIFY_PIECE_BYTES;  // default (no grid given)
+constexpr int kMinPieceBytes = 8192;
+constexpr int kMaxPieceBytes = 32768;
+
+// Elements per piece for `rows` rows of V elements of es bytes streamed by `warps` warps:
+// the largest piece whose items fill the grid's rounds clearly better than any larger one
+// (the last, partly idle round costs a whole item's time).  warps = 0: the default size.
+// Single-precision arithmetic only (every thread of a wave's kernels evaluates it, and
+// double precision is slow on this GPU); host and device get the same answer.
+__host__ __device__ inline int pick_piece_len(long long rows, int V, int es, long long warps) {
+    int best_len = kPieceBytes / es;
+    if (warps > 0) {
+        const float fw = static_cast<float>(warps);
+        float best_eff = -1.0f;
+        for (int bytes = kMaxPieceBytes; bytes >= kMinPieceBytes; bytes -= 1024) {
+            const int l = bytes / es;
+            const float items = static_cast<float>(rows) * static_cast<float>((V + l - 1) / l);
+            const float eff = items / (ceilf(items / fw) * fw);
+            if (eff > best_eff + 0.02f) {  // prefer bigger pieces unless clearly better filled
+                best_eff = eff;
+                best_len = l;
+            }
+        }
+    }
+    return best_len;
+}
 
 // (m, s) pairs travel as one naturally aligned 64-bit word.  The fused path pre-fills them
 // with kStatEmpty (two NaN halves, never a real pair) and polls until a pair is written,
@@ -896,148 +934,19 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64g(const void* p) {
     return v;
 }
 
+// The race of sequence b (scan result si, j = si.j >= 0) by block g of its G blocks: race
+// pieces g, g + G, ... of the raced row, publish the block's winner, and if this is the
+// sequence's last block merge the blocks' winners and write the token.
 template <class ET>
-__global__ void __launch_bounds__(256, 4) scan_race_kernel(VerifyParams p) {
+__device__ __forceinline__ void race_sequence_block(const VerifyParams& p, int b, int g, int G,
+                                                   const SeqInfo& si, float* s_thr,
+                                                   RaceState* s_best, int& s_last) {
     using S = typename ET::storage;
     constexpr int VPL = kRaceWarpTokens / (32 * ET::kVec);
-    extern __shared__ float smem[];  // [2R]: scaled max and log2 sum of every row
-    __shared__ int s_j, s_bad, s_last;
-    __shared__ float s_thr[8];
-    __shared__ RaceState s_best[8];
     const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
-    const int G = p.rgroups;  // blocks per sequence
-    const int b = blockIdx.x / G;
-    const int g = blockIdx.x % G;
-    const int R = 2 * p.gamma + 1;
-    float* sm_m = smem;
-    float* sm_l = smem + R;
-    const float Tb = seq_T(p, b), Tdb = seq_Td(p, b);
-    const float cp = scale_of(Tb), cq = scale_of(Tdb);
-    const uint32_t bg = p.seq_base + static_cast<uint32_t>(b);
-    const bool writer = (g == 0);
-    // diagnostics need every row's statistics; otherwise rows are merged only up to the first
-    // rejection, four positions (target and draft rows in parallel) at a time
-    const bool all_rows = writer && (p.out_logZp || p.out_logZq || p.out_logp || p.out_logq);
-    // inputs-only prologue (position i = threadIdx.x): overlaps the streaming pass's tail
-    __shared__ int s_d[256];
-    __shared__ float s_xt[256], s_xd[256], s_u[256];
-    const int i0 = threadIdx.x;
-    if (i0 < p.gamma) {
-        const int d = p.tokens[static_cast<long long>(b) * p.gamma + i0];
-        s_d[i0] = d;
-        s_u[i0] = accept_uniform(p.key, bg, static_cast<uint32_t>(i0));
-        float xt = 0.0f, xd = 0.0f;
-        if (d >= 0 && d < p.V) {
-            xt = ET::load1(static_cast<const S*>(p.target) +
-                           (static_cast<long long>(b) * (p.gamma + 1) + i0) * p.V + d);
-            xd = ET::load1(static_cast<const S*>(p.draft) +
-                           (static_cast<long long>(b) * p.gamma + i0) * p.V + d);
-        }
-        s_xt[i0] = xt;
-        s_xd[i0] = xd;
-    }
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (threadIdx.x == 0) {
-        s_j = p.gamma;
-        s_bad = 0;
-    }
-    // any draft token outside [0, V) marks the whole sequence
-    for (int i = threadIdx.x; i < p.gamma; i += blockDim.x) {
-        const int d = (i < 256) ? s_d[i] : p.tokens[static_cast<long long>(b) * p.gamma + i];
-        if (d < 0 || d >= p.V) s_bad = 1;
-    }
-    auto merge_row = [&](int r) {  // one warp: row r's statistics into shared memory
-        SoftmaxStat st{-FLT_MAX, 0.0f};
-        const float2* parts = p.stat_parts + (static_cast<long long>(b) * R + r) * p.npieces;
-        for (int k = lane; k < p.npieces; k += 32) {
-            const float2 qq = parts[k];
-            st = merge_stat(st, SoftmaxStat{qq.x, qq.y});
-        }
-        st = warp_merge_stat(st);
-        if (lane == 0) {
-            const float l2s = log2f(st.s);
-            sm_m[r] = st.m;
-            sm_l[r] = l2s;
-            if (writer) {
-                const float lz = (st.m + l2s) * kLn2;
-                if (r <= p.gamma) {
-                    if (p.out_logZp) p.out_logZp[static_cast<long long>(b) * (p.gamma + 1) + r] = lz;
-                } else if (p.out_logZq) {
-                    p.out_logZq[static_cast<long long>(b) * p.gamma + (r - p.gamma - 1)] = lz;
-                }
-            }
-        }
-    };
-    auto decide = [&](int i) {  // one thread: the accept test at position i
-        int d;
-        float xt, xd, u;
-        if (i < 256) {
-            d = s_d[i]; xt = s_xt[i]; xd = s_xd[i]; u = s_u[i];
-        } else {
-            d = p.tokens[static_cast<long long>(b) * p.gamma + i];
-            u = accept_uniform(p.key, bg, static_cast<uint32_t>(i));
-            xt = ET::load1(static_cast<const S*>(p.target) +
-                           (static_cast<long long>(b) * (p.gamma + 1) + i) * p.V + d);
-            xd = ET::load1(static_cast<const S*>(p.draft) +
-                           (static_cast<long long>(b) * p.gamma + i) * p.V + d);
-        }
-        const long long k = static_cast<long long>(b) * p.gamma + i;
-        if (writer && p.out_u) p.out_u[k] = u;
-        const float l2p = fmaf(xt, cp, -sm_m[i]) - sm_l[i];
-        const float l2q = fmaf(xd, cq, -sm_m[p.gamma + 1 + i]) - sm_l[p.gamma + 1 + i];
-        if (writer && p.out_logp) p.out_logp[k] = l2p * kLn2;
-        if (writer && p.out_logq) p.out_logq[k] = l2q * kLn2;
-        // accept iff u < min(1, p/q); p(d) = 0 rejects, q(d) = 0 < p(d) accepts
-        if (!((l2p > -INFINITY) && (u < exp2f(l2p - l2q)))) atomicMin(&s_j, i);
-    };
-    __syncthreads();
-    if (s_bad) {
-        if (writer) {
-            for (int i = threadIdx.x; i < p.gamma; i += blockDim.x) {
-                const long long k = static_cast<long long>(b) * p.gamma + i;
-                if (p.out_u) p.out_u[k] = accept_uniform(p.key, bg, static_cast<uint32_t>(i));
-                if (p.out_logp) p.out_logp[k] = NAN;
-                if (p.out_logq) p.out_logq[k] = NAN;
-            }
-            for (int r = wib; all_rows && r < R; r += 8) merge_row(r);
-        }
-    } else if (all_rows) {
-        for (int r = wib; r < R; r += 8) merge_row(r);
-        __syncthreads();
-        for (int i = threadIdx.x; i < p.gamma; i += blockDim.x) decide(i);
-    } else {
-        for (int i0b = 0; i0b < p.gamma; i0b += 4) {
-            const int i = i0b + (wib & 3);
-            if (i < p.gamma) merge_row(wib < 4 ? i : p.gamma + 1 + i);
-            __syncthreads();
-            if (threadIdx.x < 4 && i0b + threadIdx.x < p.gamma) decide(i0b + threadIdx.x);
-            __syncthreads();
-            if (s_j < p.gamma) break;
-        }
-        if (s_j == p.gamma && wib == 0) merge_row(p.gamma);  // bonus row
-    }
-    __syncthreads();
-    const int j = s_bad ? -1 : s_j;
-    if (writer) {
-        if (threadIdx.x == 0) {
-            p.out_n[b] = j;
-            if (j < 0) set_status(p.status, 3 /* SPEC_EBADTOKEN */);
-        }
-        int32_t* out = p.out_tokens + static_cast<long long>(b) * (p.gamma + 1);
-        for (int t = threadIdx.x; t <= p.gamma; t += blockDim.x)
-            if (t != j) out[t] = (j >= 0 && t < j) ? p.tokens[static_cast<long long>(b) * p.gamma + t] : -1;
-    }
-    if (j < 0) return;
-    SeqInfo si;
-    si.j = j;
-    si.cp = cp;
-    si.cq = cq;
-    si.mp = sm_m[j];
-    si.l2sp = sm_l[j];
+    const int j = si.j;
     const bool residual = j < p.gamma;
-    si.mq = residual ? sm_m[p.gamma + 1 + j] : 0.0f;
-    si.l2sq = residual ? sm_l[p.gamma + 1 + j] : 0.0f;
-    si.pad = 0;
+    const uint32_t bg = p.seq_base + static_cast<uint32_t>(b);
     const S* rt = static_cast<const S*>(p.target) + (static_cast<long long>(b) * (p.gamma + 1) + j) * p.V;
     const S* rd = residual ? static_cast<const S*>(p.draft) + (static_cast<long long>(b) * p.gamma + j) * p.V
                            : nullptr;
@@ -1205,6 +1114,358 @@ __global__ void __launch_bounds__(256, 4) scan_race_kernel(VerifyParams p) {
             p.out_race[2 * b + 1] = m.second;
         }
     }
+}
+
+template <class ET>
+__global__ void __launch_bounds__(256, 4) scan_race_kernel(VerifyParams p) {
+    using S = typename ET::storage;
+    constexpr int VPL = kRaceWarpTokens / (32 * ET::kVec);
+    extern __shared__ float smem[];  // [2R]: scaled max and log2 sum of every row
+    __shared__ int s_j, s_bad, s_last;
+    __shared__ float s_thr[8];
+    __shared__ RaceState s_best[8];
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    const int G = p.rgroups;  // blocks per sequence
+    const int b = blockIdx.x / G;
+    const int g = blockIdx.x % G;
+    const int R = 2 * p.gamma + 1;
+    float* sm_m = smem;
+    float* sm_l = smem + R;
+    const float Tb = seq_T(p, b), Tdb = seq_Td(p, b);
+    const float cp = scale_of(Tb), cq = scale_of(Tdb);
+    const uint32_t bg = p.seq_base + static_cast<uint32_t>(b);
+    const bool writer = (g == 0);
+    // diagnostics need every row's statistics; otherwise rows are merged only up to the first
+    // rejection, four positions (target and draft rows in parallel) at a time
+    const bool all_rows = writer && (p.out_logZp || p.out_logZq || p.out_logp || p.out_logq);
+    // inputs-only prologue (position i = threadIdx.x): overlaps the streaming pass's tail
+    __shared__ int s_d[256];
+    __shared__ float s_xt[256], s_xd[256], s_u[256];
+    const int i0 = threadIdx.x;
+    if (i0 < p.gamma) {
+        const int d = p.tokens[static_cast<long long>(b) * p.gamma + i0];
+        s_d[i0] = d;
+        s_u[i0] = accept_uniform(p.key, bg, static_cast<uint32_t>(i0));
+        float xt = 0.0f, xd = 0.0f;
+        if (d >= 0 && d < p.V) {
+            xt = ET::load1(static_cast<const S*>(p.target) +
+                           (static_cast<long long>(b) * (p.gamma + 1) + i0) * p.V + d);
+            xd = ET::load1(static_cast<const S*>(p.draft) +
+                           (static_cast<long long>(b) * p.gamma + i0) * p.V + d);
+        }
+        s_xt[i0] = xt;
+        s_xd[i0] = xd;
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (threadIdx.x == 0) {
+        s_j = p.gamma;
+        s_bad = 0;
+    }
+    // any draft token outside [0, V) marks the whole sequence
+    for (int i = threadIdx.x; i < p.gamma; i += blockDim.x) {
+        const int d = (i < 256) ? s_d[i] : p.tokens[static_cast<long long>(b) * p.gamma + i];
+        if (d < 0 || d >= p.V) s_bad = 1;
+    }
+    auto merge_row = [&](int r) {  // one warp: row r's statistics into shared memory
+        SoftmaxStat st{-FLT_MAX, 0.0f};
+        const float2* parts = p.stat_parts + (static_cast<long long>(b) * R + r) * p.npieces;
+        for (int k = lane; k < p.npieces; k += 32) {
+            const float2 qq = parts[k];
+            st = merge_stat(st, SoftmaxStat{qq.x, qq.y});
+        }
+        st = warp_merge_stat(st);
+        if (lane == 0) {
+            const float l2s = log2f(st.s);
+            sm_m[r] = st.m;
+            sm_l[r] = l2s;
+            if (writer) {
+                const float lz = (st.m + l2s) * kLn2;
+                if (r <= p.gamma) {
+                    if (p.out_logZp) p.out_logZp[static_cast<long long>(b) * (p.gamma + 1) + r] = lz;
+                } else if (p.out_logZq) {
+                    p.out_logZq[static_cast<long long>(b) * p.gamma + (r - p.gamma - 1)] = lz;
+                }
+            }
+        }
+    };
+    auto decide = [&](int i) {  // one thread: the accept test at position i
+        int d;
+        float xt, xd, u;
+        if (i < 256) {
+            d = s_d[i]; xt = s_xt[i]; xd = s_xd[i]; u = s_u[i];
+        } else {
+            d = p.tokens[static_cast<long long>(b) * p.gamma + i];
+            u = accept_uniform(p.key, bg, static_cast<uint32_t>(i));
+            xt = ET::load1(static_cast<const S*>(p.target) +
+                           (static_cast<long long>(b) * (p.gamma + 1) + i) * p.V + d);
+            xd = ET::load1(static_cast<const S*>(p.draft) +
+                           (static_cast<long long>(b) * p.gamma + i) * p.V + d);
+        }
+        const long long k = static_cast<long long>(b) * p.gamma + i;
+        if (writer && p.out_u) p.out_u[k] = u;
+        const float l2p = fmaf(xt, cp, -sm_m[i]) - sm_l[i];
+        const float l2q = fmaf(xd, cq, -sm_m[p.gamma + 1 + i]) - sm_l[p.gamma + 1 + i];
+        if (writer && p.out_logp) p.out_logp[k] = l2p * kLn2;
+        if (writer && p.out_logq) p.out_logq[k] = l2q * kLn2;
+        // accept iff u < min(1, p/q); p(d) = 0 rejects, q(d) = 0 < p(d) accepts
+        if (!((l2p > -INFINITY) && (u < exp2f(l2p - l2q)))) atomicMin(&s_j, i);
+    };
+    __syncthreads();
+    if (s_bad) {
+        if (writer) {
+            for (int i = threadIdx.x; i < p.gamma; i += blockDim.x) {
+                const long long k = static_cast<long long>(b) * p.gamma + i;
+                if (p.out_u) p.out_u[k] = accept_uniform(p.key, bg, static_cast<uint32_t>(i));
+                if (p.out_logp) p.out_logp[k] = NAN;
+                if (p.out_logq) p.out_logq[k] = NAN;
+            }
+            for (int r = wib; all_rows && r < R; r += 8) merge_row(r);
+        }
+    } else if (all_rows) {
+        for (int r = wib; r < R; r += 8) merge_row(r);
+        __syncthreads();
+        for (int i = threadIdx.x; i < p.gamma; i += blockDim.x) decide(i);
+    } else {
+        for (int i0b = 0; i0b < p.gamma; i0b += 4) {
+            const int i = i0b + (wib & 3);
+            if (i < p.gamma) merge_row(wib < 4 ? i : p.gamma + 1 + i);
+            __syncthreads();
+            if (threadIdx.x < 4 && i0b + threadIdx.x < p.gamma) decide(i0b + threadIdx.x);
+            __syncthreads();
+            if (s_j < p.gamma) break;
+        }
+        if (s_j == p.gamma && wib == 0) merge_row(p.gamma);  // bonus row
+    }
+    __syncthreads();
+    const int j = s_bad ? -1 : s_j;
+    if (writer) {
+        if (threadIdx.x == 0) {
+            p.out_n[b] = j;
+            if (j < 0) set_status(p.status, 3 /* SPEC_EBADTOKEN */);
+        }
+        int32_t* out = p.out_tokens + static_cast<long long>(b) * (p.gamma + 1);
+        for (int t = threadIdx.x; t <= p.gamma; t += blockDim.x)
+            if (t != j) out[t] = (j >= 0 && t < j) ? p.tokens[static_cast<long long>(b) * p.gamma + t] : -1;
+    }
+    if (j < 0) return;
+    SeqInfo si;
+    si.j = j;
+    si.cp = cp;
+    si.cq = cq;
+    si.mp = sm_m[j];
+    si.l2sp = sm_l[j];
+    const bool residual = j < p.gamma;
+    si.mq = residual ? sm_m[p.gamma + 1 + j] : 0.0f;
+    si.l2sq = residual ? sm_l[p.gamma + 1 + j] : 0.0f;
+    si.pad = 0;
+    race_sequence_block<ET>(p, b, g, G, si, s_thr, s_best, s_last);
+}
+
+// ----------------------------------------------------------------------------------------
+// Early-exit sampling verify.  Draft positions are taken in waves [lo, hi) of 1, 1, 2, 4,
+// 8, ... positions, and the bonus row gamma joins the wave that ends at gamma.  A sequence
+// leaves after the wave that decides it (its first rejection, or every position accepted),
+// so no row after its first rejection is read: the method discards that part of the draft
+// ("How speculative decoding makes LLMs go brrr": pseudocode, rejection step).  Each wave is
+// two kernels:
+//   wave_stats   partial statistics of the wave's rows of every sequence still undecided;
+//   wave_decide  one block per undecided sequence: merge the rows, test positions lo, lo+1,
+//                ... in order, and either finish the sequence's scan (outputs and the
+//                SeqInfo of the row to race) or append it to the next wave's list;
+// and race_final races the chosen row of every decided sequence at the end.  Decisions use
+// the same per-row arithmetic as the full-read path (only the row piece boundaries may
+// differ, which moves ln Z by rounding alone).
+//
+// The undecided list of wave w is alive[w & 1] with count alive_count[w & 1] (wave 0 takes
+// every sequence and reads no list); wave_stats of wave w empties alive_count[(w + 1) & 1]
+// for wave_decide to append to.  Every kernel of the chain waits for its predecessor
+// (griddepcontrol.wait) before touching the workspace, so each one's completion implies that
+// of all earlier ones.
+// ----------------------------------------------------------------------------------------
+
+// Rows of a wave: target rows lo..hi-1, draft rows lo..hi-1, and target row gamma if hi == gamma.
+__host__ __device__ inline int wave_rows(int gamma, int lo, int hi) {
+    return 2 * (hi - lo) + (hi == gamma ? 1 : 0);
+}
+
+// Row index (target rows 0..gamma, draft row i at gamma + 1 + i) of the k-th row of a wave.
+__device__ __forceinline__ int wave_row(int gamma, int lo, int hi, int k) {
+    const int n = hi - lo;
+    return k < n ? lo + k : (k < 2 * n ? gamma + 1 + lo + (k - n) : gamma);
+}
+
+__device__ __forceinline__ int wave_count(const VerifyParams& p) {
+    return p.wave_lo == 0 ? p.B : *static_cast<volatile int*>(p.alive_count[p.wave_parity]);
+}
+
+template <class ET>
+__device__ __forceinline__ int wave_piece_len(const VerifyParams& p, int count) {
+    return pick_piece_len(static_cast<long long>(count) * wave_rows(p.gamma, p.wave_lo, p.wave_hi),
+                          p.V, static_cast<int>(sizeof(typename ET::storage)), p.wave_warps);
+}
+
+template <class ET, int U>
+__global__ void __launch_bounds__(256, SPECVERIFY_STATS_MINBLOCKS) wave_stats_kernel(VerifyParams p) {
+    using S = typename ET::storage;
+    const int lane = threadIdx.x & 31;
+    const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
+    const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const bool first = p.wave_lo == 0;
+    if (first) {  // the race's partials and arrival counters start empty
+        for (long long k = tid; k < static_cast<long long>(p.B) * p.rpieces; k += nthreads)
+            reinterpret_cast<uint4*>(p.race_parts)[k] = make_uint4(0u, 0u, 0u, 0u);
+        for (long long k = tid; k < p.B; k += nthreads) p.tickets[k] = 0;
+    }
+    if (tid == 0) *p.alive_count[p.wave_parity ^ 1] = 0;
+    const int count = wave_count(p);
+    const int* list = p.alive[p.wave_parity];
+    const int Rw = wave_rows(p.gamma, p.wave_lo, p.wave_hi);
+    const int len = wave_piece_len<ET>(p, count);
+    const int np = (p.V + len - 1) / len;
+    const int R = 2 * p.gamma + 1;
+    const long long nwarps = nthreads >> 5;
+    const long long total = static_cast<long long>(count) * Rw * np;
+    for (long long item = tid >> 5; item < total; item += nwarps) {
+        const int piece = static_cast<int>(item % np);
+        const long long ak = item / np;
+        const int a = static_cast<int>(ak / Rw);
+        const int r = wave_row(p.gamma, p.wave_lo, p.wave_hi, static_cast<int>(ak % Rw));
+        const int b = first ? a : list[a];
+        const S* row;
+        float c;
+        if (r <= p.gamma) {
+            row = static_cast<const S*>(p.target) + (static_cast<long long>(b) * (p.gamma + 1) + r) * p.V;
+            c = scale_of(seq_T(p, b));
+        } else {
+            row = static_cast<const S*>(p.draft) +
+                  (static_cast<long long>(b) * p.gamma + (r - p.gamma - 1)) * p.V;
+            c = scale_of(seq_Td(p, b));
+        }
+        const int x0 = piece * len;
+        const SoftmaxStat st = stats_piece<ET, U>(row, x0, min(p.V, x0 + len), c, lane);
+        if (lane == 0)
+            store_stat(p.stat_parts + (static_cast<long long>(b) * R + r) * np + piece, st.m, st.s);
+    }
+    asm volatile("griddepcontrol.launch_dependents;");
+}
+
+template <class ET>
+__global__ void __launch_bounds__(256) wave_decide_kernel(VerifyParams p) {
+    using S = typename ET::storage;
+    __shared__ float s_m[8], s_l[8];  // batch of four positions: target rows 0-3, draft rows 4-7
+    __shared__ int s_j, s_bad;
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    asm volatile("griddepcontrol.launch_dependents;");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const bool first = p.wave_lo == 0;
+    const int count = wave_count(p);
+    const int len = wave_piece_len<ET>(p, count);
+    const int np = (p.V + len - 1) / len;
+    const int R = 2 * p.gamma + 1;
+    const int nxt = p.wave_parity ^ 1;
+    for (int a = blockIdx.x; a < count; a += gridDim.x) {
+        const int b = first ? a : p.alive[p.wave_parity][a];
+        const float cp = scale_of(seq_T(p, b)), cq = scale_of(seq_Td(p, b));
+        const uint32_t bg = p.seq_base + static_cast<uint32_t>(b);
+        const int32_t* tok = p.tokens + static_cast<long long>(b) * p.gamma;
+        if (threadIdx.x == 0) {
+            s_j = p.gamma;
+            s_bad = 0;
+        }
+        __syncthreads();
+        if (first) {  // any draft token outside [0, V) marks the whole sequence
+            for (int i = threadIdx.x; i < p.gamma; i += blockDim.x)
+                if (tok[i] < 0 || tok[i] >= p.V) s_bad = 1;
+            __syncthreads();
+        }
+        int32_t* out = p.out_tokens + static_cast<long long>(b) * (p.gamma + 1);
+        if (s_bad) {
+            for (int t = threadIdx.x; t <= p.gamma; t += blockDim.x) out[t] = -1;
+            if (threadIdx.x == 0) {
+                p.out_n[b] = -1;
+                p.seq[b].j = -1;
+                set_status(p.status, 3 /* SPEC_EBADTOKEN */);
+            }
+            __syncthreads();
+            continue;
+        }
+        auto merge_row = [&](int r, int slot) {  // one warp: row r's statistics into slot
+            SoftmaxStat st{-FLT_MAX, 0.0f};
+            const float2* parts = p.stat_parts + (static_cast<long long>(b) * R + r) * np;
+            for (int k = lane; k < np; k += 32) {
+                const float2 qq = parts[k];
+                st = merge_stat(st, SoftmaxStat{qq.x, qq.y});
+            }
+            st = warp_merge_stat(st);
+            if (lane == 0) {
+                s_m[slot] = st.m;
+                s_l[slot] = log2f(st.s);
+            }
+        };
+        int i0b = p.wave_lo;
+        for (; i0b < p.wave_hi; i0b += 4) {
+            const int i = i0b + (wib & 3);
+            if (i < p.wave_hi) merge_row(wib < 4 ? i : p.gamma + 1 + i, wib);
+            __syncthreads();
+            if (threadIdx.x < 4 && i0b + threadIdx.x < p.wave_hi) {
+                const int ii = i0b + threadIdx.x;
+                const int d = tok[ii];
+                const float u = accept_uniform(p.key, bg, static_cast<uint32_t>(ii));
+                const float xt = ET::load1(static_cast<const S*>(p.target) +
+                                           (static_cast<long long>(b) * (p.gamma + 1) + ii) * p.V + d);
+                const float xd = ET::load1(static_cast<const S*>(p.draft) +
+                                           (static_cast<long long>(b) * p.gamma + ii) * p.V + d);
+                const float l2p = fmaf(xt, cp, -s_m[threadIdx.x]) - s_l[threadIdx.x];
+                const float l2q = fmaf(xd, cq, -s_m[4 + threadIdx.x]) - s_l[4 + threadIdx.x];
+                // accept iff u < min(1, p/q); p(d) = 0 rejects, q(d) = 0 < p(d) accepts
+                if (!((l2p > -INFINITY) && (u < exp2f(l2p - l2q)))) atomicMin(&s_j, ii);
+            }
+            __syncthreads();
+            if (s_j < p.gamma) break;
+        }
+        const int j = s_j;
+        const bool rejected = j < p.gamma;
+        if (!rejected && p.wave_hi < p.gamma) {  // undecided: on to the next wave
+            if (threadIdx.x == 0) p.alive[nxt][atomicAdd(p.alive_count[nxt], 1)] = b;
+            __syncthreads();
+            continue;
+        }
+        if (!rejected && wib == 0) merge_row(p.gamma, 0);  // every position accepted: bonus row
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            SeqInfo si;
+            si.j = j;
+            si.cp = cp;
+            si.cq = cq;
+            const int slot = rejected ? j - i0b : 0;
+            si.mp = s_m[slot];
+            si.l2sp = s_l[slot];
+            si.mq = rejected ? s_m[4 + slot] : 0.0f;
+            si.l2sq = rejected ? s_l[4 + slot] : 0.0f;
+            si.pad = 0;
+            p.seq[b] = si;
+            p.out_n[b] = j;
+        }
+        for (int t = threadIdx.x; t <= p.gamma; t += blockDim.x)
+            if (t != j) out[t] = t < j ? tok[t] : -1;
+        __syncthreads();
+    }
+}
+
+// G = rgroups blocks per sequence race the row each decided sequence needs.
+template <class ET>
+__global__ void __launch_bounds__(256, 4) race_final_kernel(VerifyParams p) {
+    __shared__ float s_thr[8];
+    __shared__ RaceState s_best[8];
+    __shared__ int s_last;
+    const int G = p.rgroups;
+    const int b = blockIdx.x / G;
+    const int g = blockIdx.x % G;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const SeqInfo si = p.seq[b];
+    if (si.j < 0) return;
+    race_sequence_block<ET>(p, b, g, G, si, s_thr, s_best, s_last);
 }
 
 // ----------------------------------------------------------------------------------------

@@ -16,12 +16,6 @@ using namespace specverify;
 namespace {
 
 constexpr int kMaxGamma = 2048;          // the scan keeps 2*gamma+1 row statistics in shared memory
-#ifndef SPECVERIFY_PIECE_BYTES
-#define SPECVERIFY_PIECE_BYTES 16384
-#endif
-constexpr int kPieceBytes = SPECVERIFY_PIECE_BYTES;  // bytes of one row piece (one warp item)
-constexpr int kMinPieceBytes = 8192;                 // range the streaming pass picks from
-constexpr int kMaxPieceBytes = 32768;
 constexpr int kThreads = 256;
 #ifndef SPECVERIFY_UNROLL
 #define SPECVERIFY_UNROLL 8
@@ -44,33 +38,16 @@ struct Layout {
     size_t ctl_off, ctl_bytes;          // zeroed control block: row_done, seq_done, tickets, ready
     size_t row_done_off, seq_done_off, ticket_off, ready_off, race_cursor_off,
         row_cursor_off;
+    size_t alive_off;
     size_t total;
 };
 
-// Pieces per row for the streaming pass: between kMinPieceBytes and kMaxPieceBytes of logits,
-// chosen so that the row items fill whole rounds of the grid's `stream_warps` warps (the
-// last, partly idle round costs a whole item's time).  stream_warps = 0 takes the default
-// piece size (for sizing the workspace, which is allocated for the most pieces).
+// Pieces per row for the streaming pass (see pick_piece_len); stream_warps = 0 takes the
+// default piece size (for sizing the workspace, which is allocated for the most pieces).
 void choose_pieces(int B, int gamma, int V, int dtype, long long stream_warps, int* len, int* np) {
-    const int es = elem_bytes(dtype);
     const long long rows = static_cast<long long>(B) * (2 * gamma + 1);
-    int best_len = kPieceBytes / es;
-    if (stream_warps > 0) {
-        double best_eff = -1.0;
-        for (int bytes = kMaxPieceBytes; bytes >= kMinPieceBytes; bytes -= 1024) {
-            const int l = bytes / es;
-            const long long pcs = (V + l - 1) / l;
-            const long long items = rows * pcs;
-            const long long rounds = (items + stream_warps - 1) / stream_warps;
-            const double eff = static_cast<double>(items) / (rounds * stream_warps);
-            if (eff > best_eff + 0.02) {  // prefer bigger pieces unless clearly better filled
-                best_eff = eff;
-                best_len = l;
-            }
-        }
-    }
-    *len = best_len;
-    *np = (V + best_len - 1) / best_len;
+    *len = pick_piece_len(rows, V, elem_bytes(dtype), stream_warps);
+    *np = (V + *len - 1) / *len;
 }
 
 Layout layout_of(int B, int gamma, int V, int dtype, long long stream_warps = 0) {
@@ -107,6 +84,8 @@ Layout layout_of(int B, int gamma, int V, int dtype, long long stream_warps = 0)
     off += sizeof(unsigned long long);
     L.ctl_bytes = off - L.ctl_off;
     off = align_up(off, 256);
+    L.alive_off = off;  // early exit: two lists of B sequences and their counts
+    off = align_up(off + 2 * static_cast<size_t>(B) * sizeof(int) + 2 * sizeof(int), 256);
     L.total = off;
     return L;
 }
@@ -209,6 +188,11 @@ void bind_workspace(VerifyParams& p, const Layout& L, char* ws) {
     p.ready = reinterpret_cast<int*>(ws + L.ready_off);
     p.race_cursor = reinterpret_cast<int*>(ws + L.race_cursor_off);
     p.row_cursor = reinterpret_cast<int*>(ws + L.row_cursor_off);
+    int* alive = reinterpret_cast<int*>(ws + L.alive_off);
+    p.alive[0] = alive;
+    p.alive[1] = alive + p.B;
+    p.alive_count[0] = alive + 2 * p.B;
+    p.alive_count[1] = alive + 2 * p.B + 1;
 }
 
 // Validated common set-up of a call: fills `p` with the workspace pointers.
@@ -314,6 +298,62 @@ int launch_sampling(VerifyParams& p, int sm_count, const spec_verify_opts* o, cu
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
 }
 
+template <class K>
+cudaError_t launch_pdl(K kernel, int grid, size_t smem, cudaStream_t s, bool pdl, const VerifyParams& p) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
+// Early-exit sampling verify: waves of positions [lo, hi) = [0,1), [1,2), [2,4), [4,8), ...
+// up to gamma, each a wave_stats and a wave_decide launch, then race_final; every launch
+// after the first is a programmatic dependent of the one before.
+template <class ET>
+int launch_early_exit(VerifyParams& p, int sm_count, const spec_verify_opts* o, cudaStream_t s) {
+    auto stats = wave_stats_kernel<ET, kUnroll>;
+    auto decide = wave_decide_kernel<ET>;
+    auto race = race_final_kernel<ET>;
+    const int es = static_cast<int>(sizeof(typename ET::storage));
+    const int max_np = (p.V + kMinPieceBytes / es - 1) / (kMinPieceBytes / es);
+    record(o, 0, s);
+    int lo = 0, hi = p.gamma > 0 ? 1 : 0, w = 0;
+    for (;;) {
+        p.wave_lo = lo;
+        p.wave_hi = hi;
+        p.wave_parity = w & 1;
+        const long long items = static_cast<long long>(p.B) * wave_rows(p.gamma, lo, hi) * max_np;
+        const int grid = grid_for(stats, sm_count, items);
+        p.wave_warps = static_cast<long long>(grid) * (kThreads / 32);
+        if (launch_pdl(stats, grid, 0, s, w > 0, p) != cudaSuccess) return SPEC_ECUDA;
+        if (launch_pdl(decide, p.B, 0, s, true, p) != cudaSuccess) return SPEC_ECUDA;
+        if (hi == p.gamma) break;
+        lo = hi;
+        hi = hi * 2 < p.gamma ? hi * 2 : p.gamma;
+        ++w;
+    }
+    record(o, 1, s);
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, race, kThreads, 0) != cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    long long G = static_cast<long long>(sm_count) * per_sm / p.B;
+    if (G > p.rpieces) G = p.rpieces;
+    if (G < 1) G = 1;
+    p.rgroups = static_cast<int>(G);
+    if (launch_pdl(race, static_cast<int>(p.B * G), 0, s, !(o && o->prof_events[1]), p) != cudaSuccess)
+        return SPEC_ECUDA;
+    record(o, 2, s);
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
+}
+
 template <class ET>
 int launch_greedy(VerifyParams& p, int sm_count, const spec_verify_opts* o, cudaStream_t s) {
     const int R = p.gamma + 1;
@@ -382,6 +422,11 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, const in
     rc = prepare(B, gamma, V, dtype, opts, p, &d, &ws);
     if (rc) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool diagnostics = p.out_logp || p.out_logq || p.out_logZp || p.out_logZq || p.out_u ||
+                             p.out_race;
+    if (opts && (opts->flags & SPEC_FLAG_EARLY_EXIT) && !diagnostics)
+        return dtype == SPEC_F32 ? launch_early_exit<F32Elem>(p, d->sm_count, opts, s)
+                                 : launch_early_exit<Bf16Elem>(p, d->sm_count, opts, s);
     const bool fused = d->coop && opts && (opts->flags & SPEC_FLAG_FUSED);
     if (fused) {
         const Layout L = layout_of(B, gamma, V, dtype, d->stream_warps[dtype == SPEC_F32 ? 0 : 1]);

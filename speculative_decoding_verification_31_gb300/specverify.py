@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libspecverify.so")
 SPEC_OK, SPEC_EINVAL, SPEC_ECUDA, SPEC_EBADTOKEN, SPEC_ETIMEOUT, SPEC_ENOMEM = range(6)
 SPEC_ESCRATCH = 6
 SPEC_NOALLOC_SCRATCH_BYTES = 8 << 20
-SPEC_FLAG_FUSED, SPEC_DEBUG_NEVER_READY = 1, 2
+SPEC_FLAG_FUSED, SPEC_DEBUG_NEVER_READY, SPEC_FLAG_EARLY_EXIT = 1, 2, 4
 SPEC_F32, SPEC_BF16 = 0, 1
 
 EXPORTED = ("spec_verify", "spec_verify_greedy", "spec_verify_ex", "spec_verify_greedy_ex",

@@ -41,14 +41,14 @@ class DeviceWorkload:
 
 
 def run_gpu(sv, dw: DeviceWorkload, seed: int, per_seq_temps: bool = True, seq_index_base=0,
-            diagnostics=True):
+            diagnostics=True, flags=0):
     w = dw.w
     kw = {}
     if per_seq_temps:
         kw = dict(T_per_seq=dw.T, Td_per_seq=dw.Td)
     out_t, out_n, diag = sv.spec_verify_ex(dw.target, dw.draft, dw.tokens, float(w.T[0]),
                                            float(w.Td[0]), seed, seq_index_base=seq_index_base,
-                                           diagnostics=diagnostics, **kw)
+                                           diagnostics=diagnostics, flags=flags, **kw)
     torch.cuda.synchronize()
     res = {"tokens": out_t.cpu().numpy(), "n": out_n.cpu().numpy()}
     if diag:
@@ -102,6 +102,26 @@ def compare_sampling(w: workloads.Workload, g: dict, r: "oracle.OracleResult",
     if sel.any():
         np.testing.assert_allclose(g["race"][sel, 0].astype(np.float64), r.race[sel, 0],
                                    rtol=1e-5, atol=2e-5)
+
+
+def gpu_near_ties(g: dict, gamma: int) -> np.ndarray:
+    """Sequences whose decisions are near-ties by the GPU's own diagnostics (the same rules
+    as the oracle's flags, applied to a full-read call's outputs): used where the oracle
+    does not run on every sequence."""
+    B = len(g["n"])
+    flagged = np.zeros(B, dtype=bool)
+    for b in range(B):
+        j = int(g["n"][b])
+        if j < 0:
+            continue
+        for i in range(min(j + 1, gamma)):
+            a = np.exp(min(0.0, float(g["logp"][b, i]) - float(g["logq"][b, i])))
+            if abs(float(g["u"][b, i]) - a) < 1e-5:
+                flagged[b] = True
+        best, second = float(g["race"][b, 0]), float(g["race"][b, 1])
+        if np.isfinite(second) and abs(best - second) <= 1e-6 * max(1.0, abs(best)):
+            flagged[b] = True
+    return flagged
 
 
 def compare_greedy(g_tokens, g_n, r_tokens, r_n):
