@@ -740,6 +740,13 @@ __global__ void __launch_bounds__(256, 4) race_kernel(VerifyParams p) {
 
 constexpr int kRaceWarpTokens = 1024;
 constexpr int kRaceBlockTokens = 8 * kRaceWarpTokens;
+#ifndef SPECVERIFY_RACE_CHAINS
+#define SPECVERIFY_RACE_CHAINS 8
+#endif
+constexpr int kRaceChains = SPECVERIFY_RACE_CHAINS;  // Philox blocks in flight per lane in the race
+#ifndef SPECVERIFY_RACE_MINBLOCKS
+#define SPECVERIFY_RACE_MINBLOCKS 2
+#endif
 
 // A lower bound of the exact score ln w(x) - ln E_x from fast approximations, or -inf.
 // E = -log1p(-U) is formed as U (1 + U/2 + U^2/3) below U = 2^-8 (series, relative error
@@ -913,7 +920,7 @@ __global__ void __launch_bounds__(256, 4) race_block_kernel(VerifyParams p) {
 // ----------------------------------------------------------------------------------------
 // scan_race: G blocks per sequence b, block g racing pieces g, g + G, ... (kRaceBlockTokens
 // tokens each) of the raced row, loading each next piece while computing the current one
-// and carrying its best score over as the next piece's threshold.  Every block of sequence
+// and sharing the warps' best scores as the next piece's threshold.  Every block of sequence
 // b repeats the sequence's scan (row merges up to the first rejection, gathers, u_i) --
 // cheap next to its share of the race -- so no separate scan launch sits between the
 // streaming pass and the race; block 0 of the sequence writes the sequence's outputs.  The
@@ -934,11 +941,13 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64g(const void* p) {
     return v;
 }
 
-// The race of sequence b (scan result si, j = si.j >= 0) by block g of its G blocks: race
-// pieces g, g + G, ... of the raced row, publish the block's winner, and if this is the
-// sequence's last block merge the blocks' winners and write the token.
+// The race of sequence b (scan result si, j = si.j >= 0) by one of the `nslots` blocks that
+// share it: race pieces pc_begin, pc_begin + pc_step, ... (< pc_end) of the raced row,
+// publish the block's winner in partial slot `slot`, and if this is the sequence's last
+// block to finish, merge the blocks' winners and write the token.
 template <class ET>
-__device__ __forceinline__ void race_sequence_block(const VerifyParams& p, int b, int g, int G,
+__device__ __forceinline__ void race_sequence_block(const VerifyParams& p, int b, int pc_begin,
+                                                   int pc_end, int pc_step, int slot, int nslots,
                                                    const SeqInfo& si, float* s_thr,
                                                    RaceState* s_best, int& s_last) {
     using S = typename ET::storage;
@@ -978,15 +987,15 @@ __device__ __forceinline__ void race_sequence_block(const VerifyParams& p, int b
         }
     };
     uint4 raw[VPL], raw_next[VPL];
-    load_piece(g, raw);
+    load_piece(pc_begin, raw);
     float thr = -INFINITY;
     bool first = true;
-    for (int pc = g; pc < p.rpieces; pc += G) {
+    for (int pc = pc_begin; pc < pc_end; pc += pc_step) {
         const int x0 = pc * kRaceBlockTokens + wib * kRaceWarpTokens;
         const int x1 = min(p.V, x0 + kRaceWarpTokens);
         const bool vec_ok = x0 < x1 && (reinterpret_cast<uintptr_t>(rt + x0) & 15u) == 0;
         const int nvec = vec_ok ? (x1 - x0) / ET::kVec : 0;
-        if (pc + G < p.rpieces) load_piece(pc + G, raw_next);
+        if (pc + pc_step < pc_end) load_piece(pc + pc_step, raw_next);
         if (first) {
             // seed: each lane's largest logit, scored by a fast lower bound
             float seed = -INFINITY;
@@ -1022,23 +1031,34 @@ __device__ __forceinline__ void race_sequence_block(const VerifyParams& p, int b
         }
         if (vec_ok) {
             const float mpl = si.mp + si.l2sp;
+            // Philox blocks are computed kRaceChains at a time (independent dependency chains,
+            // so the rounds of one hide the latency of another), then tested
+            constexpr int BPV = ET::kVec / 4;  // Philox blocks per 16-byte vector
+            constexpr int VG = kRaceChains / BPV;
+            static_assert(VPL % VG == 0, "race vectors per lane must fill whole groups");
 #pragma unroll
-            for (int k = 0; k < VPL; ++k) {
-                const int v = lane + 32 * k;
+            for (int k0 = 0; k0 < VPL; k0 += VG) {
                 const float C = (thr > -INFINITY) ? 32.0f + kRaceBoundMargin2 - thr * kLog2e - mpl
                                                   : INFINITY;
-                if (v < nvec) {
+                uint4 blk[VG * BPV];
+#pragma unroll
+                for (int kk = 0; kk < VG; ++kk)
+#pragma unroll
+                    for (int gg = 0; gg < BPV; ++gg)
+                        blk[kk * BPV + gg] = race_block_fast(
+                            q, p.rk, static_cast<uint32_t>(x0 + (lane + 32 * (k0 + kk)) * ET::kVec + 4 * gg) >> 2);
+#pragma unroll
+                for (int kk = 0; kk < VG; ++kk) {
+                    const int v = lane + 32 * (k0 + kk);
+                    if (v >= nvec) continue;
                     float ft[ET::kVec];
-                    ET::widen(raw[k], ft);
+                    ET::widen(raw[k0 + kk], ft);
                     const int xv = x0 + v * ET::kVec;
                     uint32_t cand = 0;
-                    uint4 blk[ET::kVec / 4];
 #pragma unroll
-                    for (int gg = 0; gg < ET::kVec / 4; ++gg)
-                        blk[gg] = race_block_fast(q, p.rk, static_cast<uint32_t>(xv + 4 * gg) >> 2);
-#pragma unroll
-                    for (int gg = 0; gg < ET::kVec / 4; ++gg) {
-                        const uint32_t w4[4] = {blk[gg].x, blk[gg].y, blk[gg].z, blk[gg].w};
+                    for (int gg = 0; gg < BPV; ++gg) {
+                        const uint4 bk = blk[kk * BPV + gg];
+                        const uint32_t w4[4] = {bk.x, bk.y, bk.z, bk.w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
                             cand |= (lg2_fast(static_cast<float>(w4[e])) <= fmaf(ft[4 * gg + e], si.cp, C))
@@ -1058,15 +1078,14 @@ __device__ __forceinline__ void race_sequence_block(const VerifyParams& p, int b
         } else {
             for (int x = x0 + lane; x < x1; x += 32) offer_exact(ET::load1(rt + x), x, word_at(x));
         }
-        if (pc + G < p.rpieces) {
-            // the block's best so far bounds the sequence's best from below: carry it over
-            if (lane == 0) s_thr[wib] = thr;
-            __syncthreads();
-            float t = s_thr[0];
-#pragma unroll
-            for (int k = 1; k < 8; ++k) t = fmaxf(t, s_thr[k]);
-            thr = fmaxf(thr, t);
-            __syncthreads();
+        if (pc + pc_step < pc_end) {
+            // every warp's best so far bounds the sequence's best from below: share them
+            // through shared memory without a barrier (whatever value a slot holds, old or
+            // new, is such a bound)
+            volatile float* vt = s_thr;
+            if (lane == 0) vt[wib] = thr;
+            const float t = lane < 8 ? vt[lane] : -INFINITY;
+            thr = fmaxf(thr, float_unorder(__reduce_max_sync(0xffffffffu, float_order(t))));
 #pragma unroll
             for (int k = 0; k < VPL; ++k) raw[k] = raw_next[k];
         }
@@ -1078,15 +1097,15 @@ __device__ __forceinline__ void race_sequence_block(const VerifyParams& p, int b
     if (threadIdx.x == 0) {
         RaceState m = s_best[0];
         for (int k = 1; k < 8; ++k) m = race_merge(m, s_best[k]);
-        parts[g].second = m.second;  // diagnostic only
-        *reinterpret_cast<unsigned long long*>(parts + g) = pack_race(m.best, m.idx);
-        s_last = (atomicAdd(p.tickets + b, 1) == G - 1);
+        parts[slot].second = m.second;  // diagnostic only
+        *reinterpret_cast<unsigned long long*>(parts + slot) = pack_race(m.best, m.idx);
+        s_last = (atomicAdd(p.tickets + b, 1) == nslots - 1);
     }
     __syncthreads();
     if (!s_last || wib != 0) return;
     // last block of this sequence: merge every block's winner, waiting (bounded) for each
     RaceState m{-INFINITY, INT_MAX, -INFINITY};
-    for (int k = lane; k < G; k += 32) {
+    for (int k = lane; k < nslots; k += 32) {
         unsigned long long v = ld_relaxed_u64g(parts + k);
         if (v == 0ull) {
             const unsigned long long t0 = global_time_ns();
@@ -1117,7 +1136,7 @@ __device__ __forceinline__ void race_sequence_block(const VerifyParams& p, int b
 }
 
 template <class ET>
-__global__ void __launch_bounds__(256, 4) scan_race_kernel(VerifyParams p) {
+__global__ void __launch_bounds__(256, SPECVERIFY_RACE_MINBLOCKS) scan_race_kernel(VerifyParams p) {
     using S = typename ET::storage;
     constexpr int VPL = kRaceWarpTokens / (32 * ET::kVec);
     extern __shared__ float smem[];  // [2R]: scaled max and log2 sum of every row
@@ -1258,7 +1277,7 @@ __global__ void __launch_bounds__(256, 4) scan_race_kernel(VerifyParams p) {
     si.mq = residual ? sm_m[p.gamma + 1 + j] : 0.0f;
     si.l2sq = residual ? sm_l[p.gamma + 1 + j] : 0.0f;
     si.pad = 0;
-    race_sequence_block<ET>(p, b, g, G, si, s_thr, s_best, s_last);
+    race_sequence_block<ET>(p, b, g, p.rpieces, G, g, G, si, s_thr, s_best, s_last);
 }
 
 // ----------------------------------------------------------------------------------------
@@ -1455,7 +1474,7 @@ __global__ void __launch_bounds__(256) wave_decide_kernel(VerifyParams p) {
 
 // G = rgroups blocks per sequence race the row each decided sequence needs.
 template <class ET>
-__global__ void __launch_bounds__(256, 4) race_final_kernel(VerifyParams p) {
+__global__ void __launch_bounds__(256, SPECVERIFY_RACE_MINBLOCKS) race_final_kernel(VerifyParams p) {
     __shared__ float s_thr[8];
     __shared__ RaceState s_best[8];
     __shared__ int s_last;
@@ -1465,7 +1484,7 @@ __global__ void __launch_bounds__(256, 4) race_final_kernel(VerifyParams p) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const SeqInfo si = p.seq[b];
     if (si.j < 0) return;
-    race_sequence_block<ET>(p, b, g, G, si, s_thr, s_best, s_last);
+    race_sequence_block<ET>(p, b, g, p.rpieces, G, g, G, si, s_thr, s_best, s_last);
 }
 
 // ----------------------------------------------------------------------------------------
