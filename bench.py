@@ -169,23 +169,14 @@ def cpu_oracle_rate(w, seed: int, budget_s: float, max_seqs: int):
 # -------------------------------------------------------------------------------------------
 
 def early_exit_rows_read(n: np.ndarray, gamma: int) -> tuple[int, int]:
-    """Logit rows the early-exit path streams for accepted counts n (waves of positions
-    [0,1), [1,2), [2,4), ... each reading target and draft rows, the bonus row with the
-    wave that ends at gamma), and the rows the race then reads again."""
-    waves, lo, hi = [], 0, min(1, gamma)
-    while True:
-        waves.append((lo, hi))
-        if hi == gamma:
-            break
-        lo, hi = hi, min(2 * hi, gamma)
+    """Logit rows the early-exit path streams for accepted counts n (target and draft rows of
+    every position up to the first rejection, plus the bonus row when all are accepted), and
+    the rows the race then reads again."""
     streamed = raced = 0
     for j in n.tolist():
         if j < 0:
             continue
-        for lo, hi in waves:
-            streamed += 2 * (hi - lo) + (1 if hi == gamma else 0)
-            if j < hi or hi == gamma:
-                break
+        streamed += 2 * (j + 1) if j < gamma else 2 * gamma + 1
         raced += 2 if j < gamma else 1
     return streamed, raced
 

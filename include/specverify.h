@@ -91,9 +91,8 @@ typedef struct {
                                                 runner-up score (approximate) */
     void *prof_events[4];       /* optional cudaEvent_t: recorded before the first kernel and
                                    after each kernel of the call (sampling: two kernels, or
-                                   one with SPEC_FLAG_FUSED; greedy: two; with
-                                   SPEC_FLAG_EARLY_EXIT: [1] after the last wave, [2] after
-                                   the race) */
+                                   one with SPEC_FLAG_FUSED or SPEC_FLAG_EARLY_EXIT;
+                                   greedy: two) */
     uint32_t flags;             /* SPEC_FLAG_* / SPEC_DEBUG_* bits; 0 in normal use */
 } spec_verify_opts;
 
@@ -103,14 +102,15 @@ typedef struct {
 #define SPEC_DEBUG_NEVER_READY 2u /* tests only, with SPEC_FLAG_FUSED: the race waits on a flag
                                      that is never set, give up after their bounded wait and
                                      report SPEC_ETIMEOUT (outputs are then invalid) */
-#define SPEC_FLAG_EARLY_EXIT 4u   /* sampling, spec_verify_ex only: read rows in waves of
-                                     positions [0,1), [1,2), [2,4), [4,8), ... and stop reading a
-                                     sequence's rows after its first rejection (the rows the
-                                     method discards).  Same outputs under the same rules as
-                                     the full read; fewer bytes when drafts are rejected early,
-                                     more launches (two per wave, plus one).  Ignored (the full
-                                     read runs) when any diagnostic output is requested, since
-                                     those cover every row. */
+#define SPEC_FLAG_EARLY_EXIT 4u   /* sampling, spec_verify_ex only: read each sequence's rows one
+                                     position at a time and stop after its first rejection (the
+                                     rows the method discards); one persistent cooperative
+                                     kernel schedules the rows, decisions and races.  Same
+                                     outputs under the same rules as the full read; fewer bytes
+                                     when drafts are rejected early.  Ignored (the full read
+                                     runs) when any diagnostic output is requested, since those
+                                     cover every row, or when the device has no cooperative
+                                     launch. */
 
 /* Zero every field and set dtype = SPEC_BF16. */
 void spec_verify_opts_init(spec_verify_opts *opts);

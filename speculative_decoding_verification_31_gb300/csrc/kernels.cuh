@@ -69,13 +69,24 @@ struct VerifyParams {
     int* race_cursor;           // race items claimed so far (item c: sequence c / P, piece c % P)
     int* row_cursor;            // row items claimed so far (sequence-major order)
     uint32_t debug_flags;       // kDebug* test switches
-    // early-exit path: the current wave covers draft positions [wave_lo, wave_hi) of the
-    // sequences in alive[wave_parity] (all sequences in wave 0), and also row gamma
-    // (the bonus row) when wave_hi == gamma
-    int* alive[2];
-    int* alive_count[2];
-    int wave_lo, wave_hi, wave_parity;
-    long long wave_warps;       // warps of the wave_stats grid (fixes the wave's piece length)
+    // early-exit path (verify_early_kernel): task queue and its counters
+    int* task;                  // [task_cap] appended task descriptors (pre-filled kTaskEmpty)
+    int task_cap;
+    int n_init;                 // implicit initial tasks (position 0 rows, or bonus rows)
+    int* task_tail;             // slots of `task` reserved so far
+    unsigned long long* unit_cursor;  // units claimed so far
+    int* row_arrivals;          // [B][R] pieces of each row finished
+    int* pos_done;              // [B][gamma+1] completion events of each position
+    int* enq_pos;               // [B] last position whose rows are queued, minus early_L0
+    int early_L0;               // positions 0..early_L0 of every sequence are queued at the start
+    int early_fill;             // positions in flight that keep the row warps busy
+    int* race_done;             // [B] race units finished
+    int* seq_decided;           // sequences whose first rejection (or bonus) is known
+    int* seq_finished;          // sequences finished (token written)
+    int* race_task;             // [B] race queue: sequence indices (pre-filled kTaskEmpty)
+    int* race_tail;             // slots of race_task reserved so far
+    unsigned long long* race_unit_cursor;  // race units claimed so far
+    unsigned long long* early_race;  // [B][npieces] packed (score, index + 1) race winners
     // outputs
     int32_t* out_tokens;        // [B, gamma+1]
     int32_t* out_n;             // [B]
@@ -87,20 +98,24 @@ struct VerifyParams {
     float* out_race;
 };
 
-// Row pieces of the streaming passes: between kMinPieceBytes and kMaxPieceBytes of logits.
+// Row pieces of the streaming passes: between kMinPieceBytes and kMaxPieceBytes of logits
+// (the early-exit path: kEarlyPieceBytes).
 #ifndef SPECVERIFY_PIECE_BYTES
 #define SPECVERIFY_PIECE_BYTES 16384
 #endif
 constexpr int kPieceBytes = SPECVERIFY_PIECE_BYTES;  // default (no grid given)
 constexpr int kMinPieceBytes = 8192;
 constexpr int kMaxPieceBytes = 32768;
+#ifndef SPECVERIFY_EARLY_PIECE_BYTES
+#define SPECVERIFY_EARLY_PIECE_BYTES 8192
+#endif
+constexpr int kEarlyPieceBytes = SPECVERIFY_EARLY_PIECE_BYTES;
+static_assert(kEarlyPieceBytes >= kMinPieceBytes, "the workspace holds rows of kMinPieceBytes pieces");
 
 // Elements per piece for `rows` rows of V elements of es bytes streamed by `warps` warps:
 // the largest piece whose items fill the grid's rounds clearly better than any larger one
 // (the last, partly idle round costs a whole item's time).  warps = 0: the default size.
-// Single-precision arithmetic only (every thread of a wave's kernels evaluates it, and
-// double precision is slow on this GPU); host and device get the same answer.
-__host__ __device__ inline int pick_piece_len(long long rows, int V, int es, long long warps) {
+inline int pick_piece_len(long long rows, int V, int es, long long warps) {
     int best_len = kPieceBytes / es;
     if (warps > 0) {
         const float fw = static_cast<float>(warps);
@@ -1281,213 +1296,6 @@ __global__ void __launch_bounds__(256, SPECVERIFY_RACE_MINBLOCKS) scan_race_kern
 }
 
 // ----------------------------------------------------------------------------------------
-// Early-exit sampling verify.  Draft positions are taken in waves [lo, hi) of 1, 1, 2, 4,
-// 8, ... positions, and the bonus row gamma joins the wave that ends at gamma.  A sequence
-// leaves after the wave that decides it (its first rejection, or every position accepted),
-// so no row after its first rejection is read: the method discards that part of the draft
-// ("How speculative decoding makes LLMs go brrr": pseudocode, rejection step).  Each wave is
-// two kernels:
-//   wave_stats   partial statistics of the wave's rows of every sequence still undecided;
-//   wave_decide  one block per undecided sequence: merge the rows, test positions lo, lo+1,
-//                ... in order, and either finish the sequence's scan (outputs and the
-//                SeqInfo of the row to race) or append it to the next wave's list;
-// and race_final races the chosen row of every decided sequence at the end.  Decisions use
-// the same per-row arithmetic as the full-read path (only the row piece boundaries may
-// differ, which moves ln Z by rounding alone).
-//
-// The undecided list of wave w is alive[w & 1] with count alive_count[w & 1] (wave 0 takes
-// every sequence and reads no list); wave_stats of wave w empties alive_count[(w + 1) & 1]
-// for wave_decide to append to.  Every kernel of the chain waits for its predecessor
-// (griddepcontrol.wait) before touching the workspace, so each one's completion implies that
-// of all earlier ones.
-// ----------------------------------------------------------------------------------------
-
-// Rows of a wave: target rows lo..hi-1, draft rows lo..hi-1, and target row gamma if hi == gamma.
-__host__ __device__ inline int wave_rows(int gamma, int lo, int hi) {
-    return 2 * (hi - lo) + (hi == gamma ? 1 : 0);
-}
-
-// Row index (target rows 0..gamma, draft row i at gamma + 1 + i) of the k-th row of a wave.
-__device__ __forceinline__ int wave_row(int gamma, int lo, int hi, int k) {
-    const int n = hi - lo;
-    return k < n ? lo + k : (k < 2 * n ? gamma + 1 + lo + (k - n) : gamma);
-}
-
-__device__ __forceinline__ int wave_count(const VerifyParams& p) {
-    return p.wave_lo == 0 ? p.B : *static_cast<volatile int*>(p.alive_count[p.wave_parity]);
-}
-
-template <class ET>
-__device__ __forceinline__ int wave_piece_len(const VerifyParams& p, int count) {
-    return pick_piece_len(static_cast<long long>(count) * wave_rows(p.gamma, p.wave_lo, p.wave_hi),
-                          p.V, static_cast<int>(sizeof(typename ET::storage)), p.wave_warps);
-}
-
-template <class ET, int U>
-__global__ void __launch_bounds__(256, SPECVERIFY_STATS_MINBLOCKS) wave_stats_kernel(VerifyParams p) {
-    using S = typename ET::storage;
-    const int lane = threadIdx.x & 31;
-    const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
-    const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    const bool first = p.wave_lo == 0;
-    if (first) {  // the race's partials and arrival counters start empty
-        for (long long k = tid; k < static_cast<long long>(p.B) * p.rpieces; k += nthreads)
-            reinterpret_cast<uint4*>(p.race_parts)[k] = make_uint4(0u, 0u, 0u, 0u);
-        for (long long k = tid; k < p.B; k += nthreads) p.tickets[k] = 0;
-    }
-    if (tid == 0) *p.alive_count[p.wave_parity ^ 1] = 0;
-    const int count = wave_count(p);
-    const int* list = p.alive[p.wave_parity];
-    const int Rw = wave_rows(p.gamma, p.wave_lo, p.wave_hi);
-    const int len = wave_piece_len<ET>(p, count);
-    const int np = (p.V + len - 1) / len;
-    const int R = 2 * p.gamma + 1;
-    const long long nwarps = nthreads >> 5;
-    const long long total = static_cast<long long>(count) * Rw * np;
-    for (long long item = tid >> 5; item < total; item += nwarps) {
-        const int piece = static_cast<int>(item % np);
-        const long long ak = item / np;
-        const int a = static_cast<int>(ak / Rw);
-        const int r = wave_row(p.gamma, p.wave_lo, p.wave_hi, static_cast<int>(ak % Rw));
-        const int b = first ? a : list[a];
-        const S* row;
-        float c;
-        if (r <= p.gamma) {
-            row = static_cast<const S*>(p.target) + (static_cast<long long>(b) * (p.gamma + 1) + r) * p.V;
-            c = scale_of(seq_T(p, b));
-        } else {
-            row = static_cast<const S*>(p.draft) +
-                  (static_cast<long long>(b) * p.gamma + (r - p.gamma - 1)) * p.V;
-            c = scale_of(seq_Td(p, b));
-        }
-        const int x0 = piece * len;
-        const SoftmaxStat st = stats_piece<ET, U>(row, x0, min(p.V, x0 + len), c, lane);
-        if (lane == 0)
-            store_stat(p.stat_parts + (static_cast<long long>(b) * R + r) * np + piece, st.m, st.s);
-    }
-    asm volatile("griddepcontrol.launch_dependents;");
-}
-
-template <class ET>
-__global__ void __launch_bounds__(256) wave_decide_kernel(VerifyParams p) {
-    using S = typename ET::storage;
-    __shared__ float s_m[8], s_l[8];  // batch of four positions: target rows 0-3, draft rows 4-7
-    __shared__ int s_j, s_bad;
-    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
-    asm volatile("griddepcontrol.launch_dependents;");
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    const bool first = p.wave_lo == 0;
-    const int count = wave_count(p);
-    const int len = wave_piece_len<ET>(p, count);
-    const int np = (p.V + len - 1) / len;
-    const int R = 2 * p.gamma + 1;
-    const int nxt = p.wave_parity ^ 1;
-    for (int a = blockIdx.x; a < count; a += gridDim.x) {
-        const int b = first ? a : p.alive[p.wave_parity][a];
-        const float cp = scale_of(seq_T(p, b)), cq = scale_of(seq_Td(p, b));
-        const uint32_t bg = p.seq_base + static_cast<uint32_t>(b);
-        const int32_t* tok = p.tokens + static_cast<long long>(b) * p.gamma;
-        if (threadIdx.x == 0) {
-            s_j = p.gamma;
-            s_bad = 0;
-        }
-        __syncthreads();
-        if (first) {  // any draft token outside [0, V) marks the whole sequence
-            for (int i = threadIdx.x; i < p.gamma; i += blockDim.x)
-                if (tok[i] < 0 || tok[i] >= p.V) s_bad = 1;
-            __syncthreads();
-        }
-        int32_t* out = p.out_tokens + static_cast<long long>(b) * (p.gamma + 1);
-        if (s_bad) {
-            for (int t = threadIdx.x; t <= p.gamma; t += blockDim.x) out[t] = -1;
-            if (threadIdx.x == 0) {
-                p.out_n[b] = -1;
-                p.seq[b].j = -1;
-                set_status(p.status, 3 /* SPEC_EBADTOKEN */);
-            }
-            __syncthreads();
-            continue;
-        }
-        auto merge_row = [&](int r, int slot) {  // one warp: row r's statistics into slot
-            SoftmaxStat st{-FLT_MAX, 0.0f};
-            const float2* parts = p.stat_parts + (static_cast<long long>(b) * R + r) * np;
-            for (int k = lane; k < np; k += 32) {
-                const float2 qq = parts[k];
-                st = merge_stat(st, SoftmaxStat{qq.x, qq.y});
-            }
-            st = warp_merge_stat(st);
-            if (lane == 0) {
-                s_m[slot] = st.m;
-                s_l[slot] = log2f(st.s);
-            }
-        };
-        int i0b = p.wave_lo;
-        for (; i0b < p.wave_hi; i0b += 4) {
-            const int i = i0b + (wib & 3);
-            if (i < p.wave_hi) merge_row(wib < 4 ? i : p.gamma + 1 + i, wib);
-            __syncthreads();
-            if (threadIdx.x < 4 && i0b + threadIdx.x < p.wave_hi) {
-                const int ii = i0b + threadIdx.x;
-                const int d = tok[ii];
-                const float u = accept_uniform(p.key, bg, static_cast<uint32_t>(ii));
-                const float xt = ET::load1(static_cast<const S*>(p.target) +
-                                           (static_cast<long long>(b) * (p.gamma + 1) + ii) * p.V + d);
-                const float xd = ET::load1(static_cast<const S*>(p.draft) +
-                                           (static_cast<long long>(b) * p.gamma + ii) * p.V + d);
-                const float l2p = fmaf(xt, cp, -s_m[threadIdx.x]) - s_l[threadIdx.x];
-                const float l2q = fmaf(xd, cq, -s_m[4 + threadIdx.x]) - s_l[4 + threadIdx.x];
-                // accept iff u < min(1, p/q); p(d) = 0 rejects, q(d) = 0 < p(d) accepts
-                if (!((l2p > -INFINITY) && (u < exp2f(l2p - l2q)))) atomicMin(&s_j, ii);
-            }
-            __syncthreads();
-            if (s_j < p.gamma) break;
-        }
-        const int j = s_j;
-        const bool rejected = j < p.gamma;
-        if (!rejected && p.wave_hi < p.gamma) {  // undecided: on to the next wave
-            if (threadIdx.x == 0) p.alive[nxt][atomicAdd(p.alive_count[nxt], 1)] = b;
-            __syncthreads();
-            continue;
-        }
-        if (!rejected && wib == 0) merge_row(p.gamma, 0);  // every position accepted: bonus row
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            SeqInfo si;
-            si.j = j;
-            si.cp = cp;
-            si.cq = cq;
-            const int slot = rejected ? j - i0b : 0;
-            si.mp = s_m[slot];
-            si.l2sp = s_l[slot];
-            si.mq = rejected ? s_m[4 + slot] : 0.0f;
-            si.l2sq = rejected ? s_l[4 + slot] : 0.0f;
-            si.pad = 0;
-            p.seq[b] = si;
-            p.out_n[b] = j;
-        }
-        for (int t = threadIdx.x; t <= p.gamma; t += blockDim.x)
-            if (t != j) out[t] = t < j ? tok[t] : -1;
-        __syncthreads();
-    }
-}
-
-// G = rgroups blocks per sequence race the row each decided sequence needs.
-template <class ET>
-__global__ void __launch_bounds__(256, SPECVERIFY_RACE_MINBLOCKS) race_final_kernel(VerifyParams p) {
-    __shared__ float s_thr[8];
-    __shared__ RaceState s_best[8];
-    __shared__ int s_last;
-    const int G = p.rgroups;
-    const int b = blockIdx.x / G;
-    const int g = blockIdx.x % G;
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    const SeqInfo si = p.seq[b];
-    if (si.j < 0) return;
-    race_sequence_block<ET>(p, b, g, p.rpieces, G, g, G, si, s_thr, s_best, s_last);
-}
-
-// ----------------------------------------------------------------------------------------
 // verify_fused: the whole sampling verify in one persistent (cooperative) launch, with
 // specialised warps.
 //
@@ -1747,6 +1555,373 @@ __global__ void __launch_bounds__(256, SPECVERIFY_FUSED_MINBLOCKS) verify_fused_
         c = __shfl_sync(0xffffffffu, c, 0);
         if (c >= total_race) break;
         run_claimed_race<ET>(p, static_cast<int>(c / RPc), static_cast<int>(c % RPc), lane);
+    }
+}
+
+// ----------------------------------------------------------------------------------------
+// verify_early: the early-exit sampling verify as one persistent (cooperative) launch that
+// schedules its own work.  A sequence's rows are read one position at a time, and only up
+// to its first rejection: the method discards the rest of the draft ("How speculative
+// decoding makes LLMs go brrr": pseudocode, rejection step), so those rows never decide
+// anything.
+//
+// Work comes from two queues of tasks, each task split into npieces units of piece_len
+// logits:
+//   row queue    (b, r): partial softmax statistics of row r of sequence b, one piece per
+//                unit.  The first tasks (target and draft rows of position 0 of every
+//                sequence, or the bonus rows when gamma = 0) are implicit; the rest are
+//                appended as positions are accepted;
+//   race queue   b: the exponential race over the raced row of b, one piece per unit,
+//                appended when b is decided.
+// Row warps (the first 8 - kEarlyRaceWarps of each block) claim row units in queue order
+// from one counter; race warps claim race units from another, and row warps join them once
+// every sequence is decided.  Keeping the races out of the row queue keeps the chain of a
+// long-accepted draft (merge, decide, next position) from queueing behind race work.  The
+// last unit of a row to finish merges the row; the second row of a position to be merged
+// decides the position: on acceptance it appends the next position's two rows (or the bonus
+// row after position gamma-1), on rejection -- or when the bonus row is merged -- it writes
+// the sequence's outputs and appends its race.  The last race unit of a sequence merges the
+// units' winners and writes the token.
+//
+// No unit ever waits on another claimed unit: a warp waits only for a queue slot that is
+// not written yet, or for partial results whose writers have already counted their arrival
+// (partials are pre-filled with empty markers and polled, so no fence is needed).  Each
+// undecided sequence always has one task in the row queue, so a row slot a warp waits for
+// is either written soon by the warp that reserved it, or lies past every queued row task,
+// whose units are then all claimed by warps that do not wait; race warps hold no row work.
+// Every wait gives up after kWaitLimitNs and records SPEC_ETIMEOUT.
+// ----------------------------------------------------------------------------------------
+
+constexpr int kTaskEmpty = -1;  // queue slot not written yet (the slots are pre-filled)
+
+__device__ __forceinline__ void st_relaxed(int* p, int v) {
+    asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Rows of position i: its target and draft rows, or the bonus row (target row gamma).
+__device__ __forceinline__ int early_rows_of(const VerifyParams& p, int i) {
+    return i < p.gamma ? 2 : 1;
+}
+
+// Events that complete position i: each of its rows merged and, after position 0, the
+// acceptance of position i - 1.  Whoever brings the count to this decides the position.
+__device__ __forceinline__ int early_events_of(const VerifyParams& p, int i) {
+    return early_rows_of(p, i) + (i > 0 ? 1 : 0);
+}
+
+// Rows of positions 0..L (target row k, draft row k, ...; the bonus row last if L = gamma).
+__device__ __forceinline__ int early_rows_upto(const VerifyParams& p, int L) {
+    return L < p.gamma ? 2 * (L + 1) : 2 * p.gamma + 1;
+}
+
+// Row task descriptor b * R + r of initial slot q: positions 0..early_L0 of every sequence.
+__device__ __forceinline__ int early_initial_task(const VerifyParams& p, int q) {
+    const int R = 2 * p.gamma + 1;
+    const int per = early_rows_upto(p, p.early_L0);
+    const int b = q / per, m = q % per;
+    const int k = m >> 1;
+    return b * R + ((m & 1) ? p.gamma + 1 + k : k);
+}
+
+// Lane 0 waits (bounded) for queue slot `slot`; returns its value, or kTaskEmpty once
+// *done reaches B (the slot will never be written) or the wait gave up.  Polls back off
+// from 64 ns to 1 us, and look at *done (one word every waiting warp reads) every fourth
+// time only.
+__device__ __forceinline__ int early_wait_slot(const VerifyParams& p, const int* slot,
+                                               const int* done) {
+    int d = ld_acquire(slot);
+    if (d != kTaskEmpty) return d;
+    const unsigned long long t0 = global_time_ns();
+    unsigned sleep_ns = 64;
+    for (unsigned it = 0;; ++it) {
+        if ((it & 3) == 3 && ld_relaxed(done) >= p.B) return kTaskEmpty;
+        if (global_time_ns() - t0 > kWaitLimitNs) {
+            set_status(p.status, 4 /* SPEC_ETIMEOUT */);
+            return kTaskEmpty;
+        }
+        __nanosleep(sleep_ns);
+        if (sleep_ns < 1024) sleep_ns *= 2;
+        if ((d = ld_acquire(slot)) != kTaskEmpty) return d;
+    }
+}
+
+// Lane 0: queue the rows of every position of sequence b up to `hi` not queued yet.
+__device__ __forceinline__ void early_enqueue_upto(const VerifyParams& p, int b, int hi) {
+    const int R = 2 * p.gamma + 1;
+    const int old = atomicMax(p.enq_pos + b, hi - p.early_L0) + p.early_L0;
+    if (hi <= old) return;
+    const int n = early_rows_upto(p, hi) - early_rows_upto(p, old);
+    int q = atomicAdd(p.task_tail, n);
+    for (int k = old + 1; k <= hi; ++k) {
+        st_relaxed(p.task + q++, b * R + k);
+        if (k < p.gamma) st_relaxed(p.task + q++, b * R + p.gamma + 1 + k);
+    }
+}
+
+// Warp: a finished sequence with a bad draft token (no race).
+__device__ __forceinline__ void early_finish_bad(const VerifyParams& p, int b, int lane) {
+    int32_t* out = p.out_tokens + static_cast<long long>(b) * (p.gamma + 1);
+    for (int t = lane; t <= p.gamma; t += 32) out[t] = -1;
+    if (lane == 0) {
+        p.out_n[b] = -1;
+        set_status(p.status, 3 /* SPEC_EBADTOKEN */);
+        atomicAdd(p.seq_finished, 1);
+        atomicAdd(p.seq_decided, 1);
+    }
+}
+
+// Warp: sequence b is decided at j (first rejection, or gamma): outputs, then its race.
+__device__ __forceinline__ void early_finish(const VerifyParams& p, int b, int j, float mp,
+                                             float l2sp, float mq, float l2sq, int lane) {
+    int32_t* out = p.out_tokens + static_cast<long long>(b) * (p.gamma + 1);
+    const int32_t* tok = p.tokens + static_cast<long long>(b) * p.gamma;
+    for (int t = lane; t <= p.gamma; t += 32)
+        if (t != j) out[t] = t < j ? tok[t] : -1;
+    if (lane == 0) {
+        SeqInfo si;
+        si.j = j;
+        si.mp = mp;
+        si.l2sp = l2sp;
+        si.mq = mq;
+        si.l2sq = l2sq;
+        si.cp = scale_of(seq_T(p, b));
+        si.cq = scale_of(seq_Td(p, b));
+        si.pad = 0;
+        p.seq[b] = si;
+        p.out_n[b] = j;
+        // the race reads seq[b] after acquiring this slot
+        st_release(p.race_task + atomicAdd(p.race_tail, 1), b);
+        atomicAdd(p.seq_decided, 1);
+    }
+}
+
+#ifndef SPECVERIFY_EARLY_GROWTH
+#define SPECVERIFY_EARLY_GROWTH 0
+#endif
+constexpr int kEarlyGrowth = SPECVERIFY_EARLY_GROWTH;  // queue (i+1)*g/4 extra positions ahead
+
+// Warp: position i of sequence b is complete (its rows merged, the previous position
+// accepted) -- decide it, and go on through the following positions while they are complete
+// too.  On acceptance later positions are queued ahead of their decisions: a number that
+// grows with the accepted prefix (so a long accepted draft needs few decide-and-queue round
+// trips), and more when too few sequences are left undecided to keep the row warps busy.
+// Rows read past a rejection are wasted; the growth bounds them by the rows the sequence
+// needed.
+template <class ET>
+__device__ __forceinline__ void early_decide_from(const VerifyParams& p, int b, int i, int lane) {
+    using S = typename ET::storage;
+    const int R = 2 * p.gamma + 1;
+    const int32_t* tok = p.tokens + static_cast<long long>(b) * p.gamma;
+    const float2* rs = p.row_stat + static_cast<long long>(b) * R;
+    if (i == 0) {  // any draft token outside [0, V) marks the whole sequence
+        bool bad = false;
+        for (int t = lane; t < p.gamma; t += 32) bad |= (tok[t] < 0 || tok[t] >= p.V);
+        if (__any_sync(0xffffffffu, bad)) {
+            early_finish_bad(p, b, lane);
+            return;
+        }
+    }
+    for (;;) {
+        float2 sp = make_float2(0.0f, 0.0f), sq = make_float2(0.0f, 0.0f);
+        int accept = 0;
+        if (lane == 0) {
+            sp = wait_stat(p, rs + i);
+            if (i < p.gamma) {
+                sq = wait_stat(p, rs + p.gamma + 1 + i);
+                const int d = tok[i];
+                const uint32_t bg = p.seq_base + static_cast<uint32_t>(b);
+                const float u = accept_uniform(p.key, bg, static_cast<uint32_t>(i));
+                const float xt = ET::load1(static_cast<const S*>(p.target) +
+                                           (static_cast<long long>(b) * (p.gamma + 1) + i) * p.V + d);
+                const float xd = ET::load1(static_cast<const S*>(p.draft) +
+                                           (static_cast<long long>(b) * p.gamma + i) * p.V + d);
+                const float l2p = fmaf(xt, scale_of(seq_T(p, b)), -sp.x) - sp.y;
+                const float l2q = fmaf(xd, scale_of(seq_Td(p, b)), -sq.x) - sq.y;
+                // accept iff u < min(1, p/q); p(d) = 0 rejects, q(d) = 0 < p(d) accepts
+                accept = (l2p > -INFINITY) && (u < exp2f(l2p - l2q));
+            }
+        }
+        accept = __shfl_sync(0xffffffffu, accept, 0);
+        if (!accept) {  // rejected at i, or i = gamma: the bonus row
+            sp.x = __shfl_sync(0xffffffffu, sp.x, 0);
+            sp.y = __shfl_sync(0xffffffffu, sp.y, 0);
+            sq.x = __shfl_sync(0xffffffffu, sq.x, 0);
+            sq.y = __shfl_sync(0xffffffffu, sq.y, 0);
+            early_finish(p, b, i, sp.x, sp.y, i < p.gamma ? sq.x : 0.0f, i < p.gamma ? sq.y : 0.0f, lane);
+            return;
+        }
+        int t = 0;
+        if (lane == 0) {
+            const int undecided = max(1, p.B - ld_relaxed(p.seq_decided));
+            const int fill = (p.early_fill + undecided - 1) / undecided;
+            const int grow = ((i + 1) * kEarlyGrowth) >> 2;
+            early_enqueue_upto(p, b, min(p.gamma, i + max(1, max(fill, 1 + grow))));
+            t = atomicAdd(p.pos_done + static_cast<long long>(b) * (p.gamma + 1) + i + 1, 1);
+        }
+        t = __shfl_sync(0xffffffffu, t, 0);
+        ++i;
+        if (t != early_events_of(p, i) - 1) return;  // the last row of position i decides it
+    }
+}
+
+// Warp: the last piece of row r of sequence b arrived -- merge the row; if that completes
+// its position, decide.
+template <class ET>
+__device__ __forceinline__ void early_row_done(const VerifyParams& p, int b, int r, int lane) {
+    const int R = 2 * p.gamma + 1;
+    SoftmaxStat st{-FLT_MAX, 0.0f};
+    const float2* parts = p.stat_parts + (static_cast<long long>(b) * R + r) * p.npieces;
+    for (int k = lane; k < p.npieces; k += 32) {
+        const float2 q = wait_stat(p, parts + k);
+        st = merge_stat(st, SoftmaxStat{q.x, q.y});
+    }
+    st = warp_merge_stat(st);
+    const int i = r <= p.gamma ? r : r - p.gamma - 1;
+    int t = 0;
+    if (lane == 0) {
+        store_stat(p.row_stat + static_cast<long long>(b) * R + r, st.m, log2f(st.s));
+        t = atomicAdd(p.pos_done + static_cast<long long>(b) * (p.gamma + 1) + i, 1);
+    }
+    t = __shfl_sync(0xffffffffu, t, 0);
+    if (t == early_events_of(p, i) - 1) early_decide_from<ET>(p, b, i, lane);
+}
+
+// Warp: one race unit (piece `piece` of the raced row of sequence b).
+template <class ET>
+__device__ __forceinline__ void early_race_unit(const VerifyParams& p, int b, int piece, int lane) {
+    using S = typename ET::storage;
+    SeqInfo si;
+    {
+        const int4 a = __ldcg(reinterpret_cast<const int4*>(p.seq + b));
+        const float4 q = __ldcg(reinterpret_cast<const float4*>(p.seq + b) + 1);
+        si.j = a.x;
+        si.mp = __int_as_float(a.y);
+        si.l2sp = __int_as_float(a.z);
+        si.mq = __int_as_float(a.w);
+        si.l2sq = q.x;
+        si.cp = q.y;
+        si.cq = q.z;
+        si.pad = 0;
+    }
+    const int j = si.j;
+    const bool residual = j < p.gamma;
+    const S* rt = static_cast<const S*>(p.target) + (static_cast<long long>(b) * (p.gamma + 1) + j) * p.V;
+    const S* rd = residual ? static_cast<const S*>(p.draft) + (static_cast<long long>(b) * p.gamma + j) * p.V
+                           : nullptr;
+    const uint32_t bg = p.seq_base + static_cast<uint32_t>(b);
+    const int x0 = piece * p.piece_len;
+    const int x1 = min(p.V, x0 + p.piece_len);
+    const RaceState st = race_piece<ET>(rt, rd, x0, x1, si, residual, p.rk, bg,
+                                        static_cast<uint32_t>(j), lane);
+    unsigned long long* parts = p.early_race + static_cast<long long>(b) * p.npieces;
+    int t = 0;
+    if (lane == 0) {
+        parts[piece] = pack_race(st.best, st.idx);  // never zero: the index field is idx + 1
+        t = atomicAdd(p.race_done + b, 1);
+    }
+    t = __shfl_sync(0xffffffffu, t, 0);
+    if (t != p.npieces - 1) return;
+    // the sequence's last race unit: merge every unit's winner, waiting (bounded) for each
+    RaceState m{-INFINITY, INT_MAX, -INFINITY};
+    for (int k = lane; k < p.npieces; k += 32) {
+        unsigned long long v = ld_relaxed_u64(parts + k);
+        if (v == 0ull) {
+            const unsigned long long t0 = global_time_ns();
+            while ((v = ld_relaxed_u64(parts + k)) == 0ull) {
+                if (global_time_ns() - t0 > kWaitLimitNs) break;
+                __nanosleep(64);
+            }
+            if (v == 0ull) set_status(p.status, 4 /* SPEC_ETIMEOUT */);
+        }
+        if (v != 0ull)
+            m = race_merge(m, RaceState{__uint_as_float(static_cast<uint32_t>(v)),
+                                        static_cast<int>(static_cast<uint32_t>(v >> 32) - 1u),
+                                        -INFINITY});
+    }
+    m = warp_race_merge(m);
+    if (m.idx == INT_MAX) {
+        // Every residual weight was zero (p <= q everywhere in fp32): draw from p_j.
+        m = race_piece<ET>(rt, nullptr, 0, p.V, si, false, p.rk, bg, static_cast<uint32_t>(j), lane);
+    }
+    if (lane == 0) {
+        p.out_tokens[static_cast<long long>(b) * (p.gamma + 1) + j] = m.idx;
+        atomicAdd(p.seq_finished, 1);
+    }
+}
+
+#ifndef SPECVERIFY_EARLY_MINBLOCKS
+#define SPECVERIFY_EARLY_MINBLOCKS 2
+#endif
+#ifndef SPECVERIFY_EARLY_UNROLL
+#define SPECVERIFY_EARLY_UNROLL 8
+#endif
+constexpr int kEarlyUnroll = SPECVERIFY_EARLY_UNROLL;
+
+#ifndef SPECVERIFY_EARLY_RACE_WARPS
+#define SPECVERIFY_EARLY_RACE_WARPS 2
+#endif
+constexpr int kEarlyRaceWarps = SPECVERIFY_EARLY_RACE_WARPS;  // of the 8 warps of a block
+
+template <class ET, int U>
+__global__ void __launch_bounds__(256, SPECVERIFY_EARLY_MINBLOCKS) verify_early_kernel(VerifyParams p) {
+    using S = typename ET::storage;
+    const int lane = threadIdx.x & 31;
+    const int R = 2 * p.gamma + 1;
+    const int np = p.npieces;
+    if ((threadIdx.x >> 5) < 8 - kEarlyRaceWarps) {
+        // row units, until every sequence is decided
+        const long long units_cap = static_cast<long long>(p.n_init + p.task_cap) * np;
+        for (;;) {
+            long long c = 0;
+            if (lane == 0) c = static_cast<long long>(atomicAdd(p.unit_cursor, 1ull));
+            c = __shfl_sync(0xffffffffu, c, 0);
+            if (c >= units_cap) break;
+            const int q = static_cast<int>(c / np);
+            const int piece = static_cast<int>(c % np);
+            int d;
+            if (q < p.n_init) {
+                d = early_initial_task(p, q);
+            } else {
+                d = 0;
+                if (lane == 0) d = early_wait_slot(p, p.task + (q - p.n_init), p.seq_decided);
+                d = __shfl_sync(0xffffffffu, d, 0);
+                if (d == kTaskEmpty) break;
+            }
+            const int b = d / R, r = d % R;
+            const S* row;
+            float cs;
+            if (r <= p.gamma) {
+                row = static_cast<const S*>(p.target) + (static_cast<long long>(b) * (p.gamma + 1) + r) * p.V;
+                cs = scale_of(seq_T(p, b));
+            } else {
+                row = static_cast<const S*>(p.draft) +
+                      (static_cast<long long>(b) * p.gamma + (r - p.gamma - 1)) * p.V;
+                cs = scale_of(seq_Td(p, b));
+            }
+            const int x0 = piece * p.piece_len;
+            const SoftmaxStat st = stats_piece<ET, U>(row, x0, min(p.V, x0 + p.piece_len), cs, lane);
+            int t = 0;
+            if (lane == 0) {
+                store_stat(p.stat_parts + static_cast<long long>(d) * np + piece, st.m, st.s);
+                t = atomicAdd(p.row_arrivals + d, 1);
+            }
+            t = __shfl_sync(0xffffffffu, t, 0);
+            if (t == np - 1) early_row_done<ET>(p, b, r, lane);
+        }
+    }
+    // race units, until every sequence is finished
+    const long long race_cap = static_cast<long long>(p.B) * np;
+    for (;;) {
+        long long c = 0;
+        if (lane == 0) c = static_cast<long long>(atomicAdd(p.race_unit_cursor, 1ull));
+        c = __shfl_sync(0xffffffffu, c, 0);
+        if (c >= race_cap) break;
+        int b = 0;
+        if (lane == 0) b = early_wait_slot(p, p.race_task + c / np, p.seq_finished);
+        b = __shfl_sync(0xffffffffu, b, 0);
+        __syncwarp();  // the other lanes' reads of seq[b] follow lane 0's acquire
+        if (b == kTaskEmpty) break;
+        early_race_unit<ET>(p, b, static_cast<int>(c % np), lane);
     }
 }
 

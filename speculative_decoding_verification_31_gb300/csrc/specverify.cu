@@ -3,6 +3,7 @@
 // The C ABI is declared in include/specverify.h; the kernels are in kernels.cuh.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -38,7 +39,10 @@ struct Layout {
     size_t ctl_off, ctl_bytes;          // zeroed control block: row_done, seq_done, tickets, ready
     size_t row_done_off, seq_done_off, ticket_off, ready_off, race_cursor_off,
         row_cursor_off;
-    size_t alive_off;
+    int e_n_init, e_task_cap;           // early-exit path (verify_early_kernel)
+    size_t e_rowstat_off, e_task_off, e_stat_off, e_zero_off, e_cursor_off, e_tail_off,
+        e_finished_off, e_rowarr_off, e_pos_off, e_racedone_off, e_race_off, e_racetask_off,
+        e_racecursor_off, e_racetail_off, e_decided_off, e_enq_off;
     size_t total;
 };
 
@@ -84,8 +88,45 @@ Layout layout_of(int B, int gamma, int V, int dtype, long long stream_warps = 0)
     off += sizeof(unsigned long long);
     L.ctl_bytes = off - L.ctl_off;
     off = align_up(off, 256);
-    L.alive_off = off;  // early exit: two lists of B sequences and their counts
-    off = align_up(off + 2 * static_cast<size_t>(B) * sizeof(int) + 2 * sizeof(int), 256);
+    // early-exit region: a block filled with 0xFF before each call (merged rows, task queue,
+    // then the row partials, last so that only the pieces in use need filling), then a
+    // zeroed block (counters, then the race winners)
+    L.e_n_init = gamma > 0 ? 2 * B : B;     // the fewest initial row tasks (launch_early may
+    L.e_task_cap = B * (2 * gamma + 1) - L.e_n_init;  // queue more): the queue's capacity
+    L.e_rowstat_off = off;
+    off += static_cast<size_t>(B) * R * sizeof(float2);
+    L.e_task_off = off;
+    off += static_cast<size_t>(L.e_task_cap) * sizeof(int);
+    L.e_racetask_off = off;
+    off = align_up(off + static_cast<size_t>(B) * sizeof(int), 8);
+    L.e_stat_off = off;
+    off = align_up(off + static_cast<size_t>(B) * R * max_np * sizeof(float2), 256);
+    L.e_zero_off = off;
+    // each counter on its own 128-byte line: waiting warps poll two of them, and claims and
+    // appends update the others
+    L.e_cursor_off = off;
+    off += 128;
+    L.e_tail_off = off;
+    off += 128;
+    L.e_finished_off = off;
+    off += 128;
+    L.e_racecursor_off = off;
+    off += 128;
+    L.e_racetail_off = off;
+    off += 128;
+    L.e_decided_off = off;
+    off += 128;
+    L.e_rowarr_off = off;
+    off += static_cast<size_t>(B) * R * sizeof(int);
+    L.e_pos_off = off;
+    off += static_cast<size_t>(B) * (gamma + 1) * sizeof(int);
+    L.e_enq_off = off;
+    off += static_cast<size_t>(B) * sizeof(int);
+    L.e_racedone_off = off;
+    off += static_cast<size_t>(B) * sizeof(int);
+    off = align_up(off, 8);
+    L.e_race_off = off;
+    off = align_up(off + static_cast<size_t>(B) * max_np * sizeof(unsigned long long), 256);
     L.total = off;
     return L;
 }
@@ -188,11 +229,6 @@ void bind_workspace(VerifyParams& p, const Layout& L, char* ws) {
     p.ready = reinterpret_cast<int*>(ws + L.ready_off);
     p.race_cursor = reinterpret_cast<int*>(ws + L.race_cursor_off);
     p.row_cursor = reinterpret_cast<int*>(ws + L.row_cursor_off);
-    int* alive = reinterpret_cast<int*>(ws + L.alive_off);
-    p.alive[0] = alive;
-    p.alive[1] = alive + p.B;
-    p.alive_count[0] = alive + 2 * p.B;
-    p.alive_count[1] = alive + 2 * p.B + 1;
 }
 
 // Validated common set-up of a call: fills `p` with the workspace pointers.
@@ -260,6 +296,23 @@ int launch_fused(VerifyParams& p, int sm_count, const spec_verify_opts* o, cudaS
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
 }
 
+// Launch with programmatic stream serialization when `pdl`: the kernel may start before the
+// previous one on the stream ends, and waits for it with griddepcontrol.wait.
+template <class K>
+cudaError_t launch_pdl(K kernel, int grid, size_t smem, cudaStream_t s, bool pdl, const VerifyParams& p) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
 // Two-kernel sampling verify: the streaming pass, then the scan-race kernel as its
 // programmatic dependent (its blocks start while the streaming pass drains).
 template <class ET>
@@ -283,74 +336,69 @@ int launch_sampling(VerifyParams& p, int sm_count, const spec_verify_opts* o, cu
         if (G < 1) G = 1;
         p.rgroups = static_cast<int>(G);
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(static_cast<long long>(p.B) * p.rgroups));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = 2 * R * sizeof(float);
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = (o && o->prof_events[1]) ? 0 : 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, scan_race_kernel<ET>, p) != cudaSuccess) return SPEC_ECUDA;
+    // (no PDL when an event is recorded between the kernels, so that each one is timed alone)
+    if (launch_pdl(scan_race_kernel<ET>, static_cast<int>(static_cast<long long>(p.B) * p.rgroups),
+                   2 * R * sizeof(float), s, !(o && o->prof_events[1]), p) != cudaSuccess)
+        return SPEC_ECUDA;
     record(o, 2, s);
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
 }
 
-template <class K>
-cudaError_t launch_pdl(K kernel, int grid, size_t smem, cudaStream_t s, bool pdl, const VerifyParams& p) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, p);
-}
-
-// Early-exit sampling verify: waves of positions [lo, hi) = [0,1), [1,2), [2,4), [4,8), ...
-// up to gamma, each a wave_stats and a wave_decide launch, then race_final; every launch
-// after the first is a programmatic dependent of the one before.
+// Early-exit sampling verify: fill the queue and the row partials with empty markers, zero
+// the counters, then one cooperative launch (every block resident; the warps wait only for
+// work that warps which never wait will publish).
 template <class ET>
-int launch_early_exit(VerifyParams& p, int sm_count, const spec_verify_opts* o, cudaStream_t s) {
-    auto stats = wave_stats_kernel<ET, kUnroll>;
-    auto decide = wave_decide_kernel<ET>;
-    auto race = race_final_kernel<ET>;
-    const int es = static_cast<int>(sizeof(typename ET::storage));
-    const int max_np = (p.V + kMinPieceBytes / es - 1) / (kMinPieceBytes / es);
-    record(o, 0, s);
-    int lo = 0, hi = p.gamma > 0 ? 1 : 0, w = 0;
-    for (;;) {
-        p.wave_lo = lo;
-        p.wave_hi = hi;
-        p.wave_parity = w & 1;
-        const long long items = static_cast<long long>(p.B) * wave_rows(p.gamma, lo, hi) * max_np;
-        const int grid = grid_for(stats, sm_count, items);
-        p.wave_warps = static_cast<long long>(grid) * (kThreads / 32);
-        if (launch_pdl(stats, grid, 0, s, w > 0, p) != cudaSuccess) return SPEC_ECUDA;
-        if (launch_pdl(decide, p.B, 0, s, true, p) != cudaSuccess) return SPEC_ECUDA;
-        if (hi == p.gamma) break;
-        lo = hi;
-        hi = hi * 2 < p.gamma ? hi * 2 : p.gamma;
-        ++w;
-    }
-    record(o, 1, s);
+int launch_early(VerifyParams& p, int sm_count, const spec_verify_opts* o, cudaStream_t s,
+                 const Layout& L, char* ws) {
+    auto kernel = verify_early_kernel<ET, kEarlyUnroll>;
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, race, kThreads, 0) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) != cudaSuccess ||
         per_sm < 1)
-        per_sm = 1;
-    long long G = static_cast<long long>(sm_count) * per_sm / p.B;
-    if (G > p.rpieces) G = p.rpieces;
-    if (G < 1) G = 1;
-    p.rgroups = static_cast<int>(G);
-    if (launch_pdl(race, static_cast<int>(p.B * G), 0, s, !(o && o->prof_events[1]), p) != cudaSuccess)
         return SPEC_ECUDA;
-    record(o, 2, s);
+    const int R = 2 * p.gamma + 1;
+    p.piece_len = kEarlyPieceBytes / static_cast<int>(sizeof(typename ET::storage));
+    p.npieces = (p.V + p.piece_len - 1) / p.piece_len;
+    p.stat_parts = reinterpret_cast<float2*>(ws + L.e_stat_off);
+    p.row_stat = reinterpret_cast<float2*>(ws + L.e_rowstat_off);
+    p.task = reinterpret_cast<int*>(ws + L.e_task_off);
+    p.pos_done = reinterpret_cast<int*>(ws + L.e_pos_off);
+    p.enq_pos = reinterpret_cast<int*>(ws + L.e_enq_off);
+    // positions in flight that keep the row warps busy, and the positions every sequence
+    // starts with (more than position 0 only when there are too few sequences for that)
+    const long long row_warps = static_cast<long long>(sm_count) * per_sm * (8 - kEarlyRaceWarps);
+    p.early_fill = static_cast<int>(std::max(1LL, row_warps / (2LL * p.npieces)));
+    p.early_L0 = std::min(p.gamma, std::max(0, (p.early_fill + p.B - 1) / p.B - 1));
+    const int per_seq = p.early_L0 < p.gamma ? 2 * (p.early_L0 + 1) : 2 * p.gamma + 1;
+    p.n_init = p.B * per_seq;
+    p.task_cap = p.B * R - p.n_init;
+    p.unit_cursor = reinterpret_cast<unsigned long long*>(ws + L.e_cursor_off);
+    p.task_tail = reinterpret_cast<int*>(ws + L.e_tail_off);
+    p.seq_finished = reinterpret_cast<int*>(ws + L.e_finished_off);
+    p.seq_decided = reinterpret_cast<int*>(ws + L.e_decided_off);
+    p.race_task = reinterpret_cast<int*>(ws + L.e_racetask_off);
+    p.race_tail = reinterpret_cast<int*>(ws + L.e_racetail_off);
+    p.race_unit_cursor = reinterpret_cast<unsigned long long*>(ws + L.e_racecursor_off);
+    p.row_arrivals = reinterpret_cast<int*>(ws + L.e_rowarr_off);
+    p.race_done = reinterpret_cast<int*>(ws + L.e_racedone_off);
+    p.early_race = reinterpret_cast<unsigned long long*>(ws + L.e_race_off);
+    const size_t rows = static_cast<size_t>(p.B) * R;
+    // no more warps than the units queued at the start
+    long long grid = static_cast<long long>(sm_count) * per_sm;
+    const long long want = (static_cast<long long>(p.n_init) * p.npieces + (kThreads / 32) - 1) /
+                           (kThreads / 32);
+    if (want < grid) grid = want;
+    if (cudaMemsetAsync(ws + L.e_rowstat_off, 0xFF,
+                        (L.e_stat_off - L.e_rowstat_off) + rows * p.npieces * sizeof(float2), s) != cudaSuccess ||
+        cudaMemsetAsync(ws + L.e_zero_off, 0,
+                        (L.e_race_off - L.e_zero_off) +
+                            static_cast<size_t>(p.B) * p.npieces * sizeof(unsigned long long), s) != cudaSuccess)
+        return SPEC_ECUDA;
+    record(o, 0, s);
+    void* args[] = {&p};
+    if (cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kernel), dim3(static_cast<unsigned>(grid)),
+                                    dim3(kThreads), args, 0, s) != cudaSuccess)
+        return SPEC_ECUDA;
+    record(o, 1, s);
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
 }
 
@@ -424,12 +472,12 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, const in
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool diagnostics = p.out_logp || p.out_logq || p.out_logZp || p.out_logZq || p.out_u ||
                              p.out_race;
-    if (opts && (opts->flags & SPEC_FLAG_EARLY_EXIT) && !diagnostics)
-        return dtype == SPEC_F32 ? launch_early_exit<F32Elem>(p, d->sm_count, opts, s)
-                                 : launch_early_exit<Bf16Elem>(p, d->sm_count, opts, s);
+    const Layout L = layout_of(B, gamma, V, dtype, d->stream_warps[dtype == SPEC_F32 ? 0 : 1]);
+    if (d->coop && opts && (opts->flags & SPEC_FLAG_EARLY_EXIT) && !diagnostics)
+        return dtype == SPEC_F32 ? launch_early<F32Elem>(p, d->sm_count, opts, s, L, ws)
+                                 : launch_early<Bf16Elem>(p, d->sm_count, opts, s, L, ws);
     const bool fused = d->coop && opts && (opts->flags & SPEC_FLAG_FUSED);
     if (fused) {
-        const Layout L = layout_of(B, gamma, V, dtype, d->stream_warps[dtype == SPEC_F32 ? 0 : 1]);
         return dtype == SPEC_F32 ? launch_fused<F32Elem>(p, d->sm_count, opts, s, L, ws)
                                  : launch_fused<Bf16Elem>(p, d->sm_count, opts, s, L, ws);
     }

@@ -1,13 +1,13 @@
 """GPU parity of the early-exit sampling path (SPEC_FLAG_EARLY_EXIT) against the oracle and
 the full-read path (marked gpu).
 
-The early-exit path reads rows in waves of positions [0,1), [1,2), [2,4), [4,8), ... and
-stops reading a sequence after its first rejection.  Its outputs follow the same rules as
-the full read: tokens and counts equal the oracle's except at flagged near-ties.  The cases
-cross every wave boundary (gamma = 0..13 and 48), run draft noise from small (long
-accepted prefixes, late waves) to large (early rejections), and include bad tokens in a
-late position, degenerate distributions, per-sequence temperatures, split batches,
-repeated calls on one caller workspace, and the two batched workloads at full size.
+The early-exit path reads a sequence's rows one position at a time and stops after its first
+rejection.  Its outputs follow the same rules as the full read: tokens and counts equal the
+oracle's except at flagged near-ties.  The cases run gamma = 0..13 and 48, draft noise from
+small (long accepted prefixes, the bonus row) to large (early rejections), and include bad
+tokens in a late position, degenerate distributions, per-sequence temperatures, split
+batches, repeated calls on one caller workspace, and the two batched workloads at full
+size.
 """
 import numpy as np
 import pytest
@@ -73,9 +73,9 @@ def test_early_exit_small(sv, orc, B, gamma, V, dtype, sigma):
     assert sv.spec_verify_check() == sv.SPEC_OK
 
 
-def test_early_exit_reaches_every_wave(sv, orc):
-    """Draft = target at the same temperature accepts every position: every wave runs and
-    the bonus row decides; one sequence per wave boundary rejects by a planted token."""
+def test_early_exit_reaches_every_position(sv, orc):
+    """Draft = target at the same temperature accepts every position, so the bonus row
+    decides; the other sequences reject at planted positions (p(d) = 0) from 0 to 12."""
     B, gamma, V = 6, 13, 4000
     w = workloads.generic(B=B, gamma=gamma, V=V, dtype="bf16", seed=5, T=1.0, Td=1.0)
     draft = w.target[:, :gamma].copy()
@@ -86,7 +86,7 @@ def test_early_exit_reaches_every_wave(sv, orc):
     for b, i in enumerate([None, 0, 1, 3, 7, 12]):
         if i is not None:
             target[b, i, tok[b, i]] = ninf
-    w2 = workloads.Workload("every-wave", B, gamma, V, "bf16", target, draft, tok, w.T, w.Td)
+    w2 = workloads.Workload("every-position", B, gamma, V, "bf16", target, draft, tok, w.T, w.Td)
     dw = DeviceWorkload(w2)
     for seed in range(3):
         g = early(sv, dw, seed, per_seq_temps=False)
@@ -115,7 +115,7 @@ def test_early_exit_per_sequence_temperatures_and_split(sv, orc):
 def test_early_exit_bad_token_in_a_late_position(sv, orc):
     w = workloads.generic(B=4, gamma=12, V=900, dtype="bf16", seed=6, sigma=0.05)
     tok = w.tokens.copy()
-    tok[1, 11] = 900    # checked in the first wave although its position is never reached
+    tok[1, 11] = 900    # checked at position 0 although position 11 is never reached
     tok[2, 0] = -1
     dw = DeviceWorkload(w)
     dtok = torch.from_numpy(tok).cuda()
