@@ -74,6 +74,23 @@ class Oracle:
         lib.oracle_row_overlap.argtypes = [ctypes.c_int, _P, _P, ctypes.c_int, ctypes.c_int,
                                            _P, _P, _P]
         lib.oracle_row_overlap.restype = None
+        lib.oracle_position_stats.argtypes = [ctypes.c_int, _P, _P, ctypes.c_int, ctypes.c_int,
+                                              ctypes.c_int, _P, _P, _P, _P, _P]
+        lib.oracle_position_stats.restype = None
+        lib.oracle_row_kl.argtypes = [ctypes.c_int, _P, _P, ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_double, ctypes.c_double, _P]
+        lib.oracle_row_kl.restype = None
+        lib.oracle_row_entropies.argtypes = [ctypes.c_int, _P, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_double, _P]
+        lib.oracle_row_entropies.restype = None
+        lib.oracle_entropy_centres_update.argtypes = [ctypes.c_int, ctypes.c_int, _P, _P,
+                                                      ctypes.c_double, _P]
+        lib.oracle_entropy_centres_update.restype = None
+        lib.oracle_soft_accept.argtypes = [ctypes.c_double, ctypes.c_double, ctypes.c_double]
+        lib.oracle_soft_accept.restype = ctypes.c_double
+        lib.oracle_adaptive_k.argtypes = [ctypes.c_int, ctypes.c_int, _P, _P, _P, ctypes.c_int,
+                                          ctypes.c_double, ctypes.c_double, _P, _P]
+        lib.oracle_adaptive_k.restype = ctypes.c_int
         lib.oracle_verify.argtypes = [ctypes.c_int, _P, _P, _P, ctypes.c_int, ctypes.c_int,
                                       ctypes.c_int, _P, _P, ctypes.c_uint64, ctypes.c_uint32,
                                       _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]
@@ -136,6 +153,68 @@ class Oracle:
         self.lib.oracle_row_overlap(dtype, a.ctypes.data, d.ctypes.data, R, V, t.ctypes.data,
                                     td.ctypes.data, out.ctypes.data)
         return out
+
+    # -- per-position statistics and the adaptive draft length ([SPARSESPEC] section 3.3)
+    def position_stats(self, target, draft, T, Td):
+        """(H(p_i) [B, g+1], H(q_i) [B, g], KL(p_i || q_i) [B, g]) in nats, fp64."""
+        dtype, t = _logits(target)
+        dtype2, d = _logits(draft)
+        assert dtype == dtype2
+        B, G1, V = t.shape
+        g = G1 - 1
+        assert d.shape == (B, g, V)
+        Tb = np.ascontiguousarray(np.broadcast_to(np.asarray(T, np.float64), (B,)))
+        Tdb = np.ascontiguousarray(np.broadcast_to(np.asarray(Td, np.float64), (B,)))
+        hp, hq, kl = np.zeros((B, g + 1)), np.zeros((B, g)), np.zeros((B, g))
+        self.lib.oracle_position_stats(dtype, t.ctypes.data, d.ctypes.data, B, g, V,
+                                       Tb.ctypes.data, Tdb.ctypes.data, hp.ctypes.data,
+                                       hq.ctypes.data, kl.ctypes.data)
+        return hp, hq, kl
+
+    def row_entropies(self, rows, temp: float) -> np.ndarray:
+        dtype, a = _logits(rows)
+        R, V = a.shape
+        out = np.zeros(R)
+        self.lib.oracle_row_entropies(dtype, a.ctypes.data, R, V, float(temp), out.ctypes.data)
+        return out
+
+    def row_kl(self, target_rows, draft_rows, T: float, Td: float) -> np.ndarray:
+        dtype, a = _logits(target_rows)
+        dtype2, d = _logits(draft_rows)
+        assert dtype == dtype2 and a.shape == d.shape
+        R, V = a.shape
+        out = np.zeros(R)
+        self.lib.oracle_row_kl(dtype, a.ctypes.data, d.ctypes.data, R, V, float(T), float(Td),
+                               out.ctypes.data)
+        return out
+
+    def entropy_centres_update(self, Hq, n_accepted, beta: float, centres) -> np.ndarray:
+        """New class centres [B, 2] (accepted, rejected) after one verify."""
+        h = np.ascontiguousarray(Hq, dtype=np.float64)
+        B, g = h.shape
+        n = np.ascontiguousarray(n_accepted, dtype=np.int32).reshape(B)
+        c = np.array(centres, dtype=np.float64, copy=True).reshape(B, 2)
+        self.lib.oracle_entropy_centres_update(B, g, h.ctypes.data, n.ctypes.data,
+                                               float(beta), c.ctypes.data)
+        return c
+
+    def soft_accept(self, H: float, c_acc: float, c_rej: float) -> float:
+        return self.lib.oracle_soft_accept(float(H), float(c_acc), float(c_rej))
+
+    def adaptive_k(self, H, centres, candidates, Cd: float, Cv: float):
+        """(k* [B] int32, best efficiency [B]) from the next K draft entropies H [B, K]."""
+        h = np.ascontiguousarray(H, dtype=np.float64)
+        B, K = h.shape
+        c = np.ascontiguousarray(centres, dtype=np.float64).reshape(B, 2)
+        cand = np.ascontiguousarray(candidates, dtype=np.int32)
+        k = np.zeros(B, np.int32)
+        eff = np.zeros(B)
+        rc = self.lib.oracle_adaptive_k(B, K, h.ctypes.data, c.ctypes.data, cand.ctypes.data,
+                                        len(cand), float(Cd), float(Cv), k.ctypes.data,
+                                        eff.ctypes.data)
+        if rc != 0:
+            raise ValueError("oracle_adaptive_k: candidates must lie in 1..K")
+        return k, eff
 
     # -- the verify step ---------------------------------------------------------------
     def verify(self, target, draft, tokens, T, Td, seed: int, b_base: int = 0) -> "OracleResult":

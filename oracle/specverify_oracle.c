@@ -425,3 +425,166 @@ int oracle_verify_greedy(int dtype, const void *target, const int32_t *tokens, i
     free(g);
     return 0;
 }
+
+/* ------------------------------------------------------------------------------------ */
+/* Per-position draft statistics and the adaptive draft length.                          */
+/*                                                                                       */
+/* [SPARSESPEC] "投机解码的第二本账" (SparseSpec-L), section 3.3: every draft token        */
+/* records the entropy H_i of its distribution; after verification the entropies of     */
+/* accepted and of rejected tokens feed two class centres kept as exponential moving    */
+/* averages; a new draft token is classified softly by its distances to the two centres, */
+/* giving an acceptance probability p_i; the draft length is the k of a candidate set    */
+/* that maximises (1 + sum_{m=1..k} prod_{i=1..m} p_i) / (k C_d + C_v).                  */
+/* [SUBSPEC] "SubSpec: the target model's own low-bit shadow as the draft model" quotes   */
+/* the draft-target KL divergence as its alignment measure; KL(p_i || q_i) per position   */
+/* is reported beside the entropies.                                                     */
+/*                                                                                       */
+/* Readings where the page is silent (each also listed in the design notes):            */
+/*   - H_i is the entropy of the draft distribution q_i = softmax(L_d / T_d), the one    */
+/*     the draft token was drawn from, in nats;                                          */
+/*   - after a verify with first rejection j, positions i < j update the accepted centre */
+/*     and position j (if j < gamma) the rejected centre, in position order; positions   */
+/*     after j were never tested and leave the centres alone; c <- (1 - beta) c +       */
+/*     beta H_i with beta given by the caller;                                           */
+/*   - soft classification: p = d_rej / (d_acc + d_rej) with d = |H - centre| (1/2 when  */
+/*     both distances are 0);                                                            */
+/*   - the candidate set, C_d and C_v are the caller's; equal efficiencies keep the      */
+/*     earlier candidate.                                                                */
+/* ------------------------------------------------------------------------------------ */
+
+/* Entropy of softmax(L / temp) of one row, in nats: -sum_x p(x) log p(x) (0 log 0 = 0). */
+static double row_entropy(int dtype, const void *base, int64_t off, int V, double temp) {
+    const double lz = row_log_normaliser(dtype, base, off, V, temp);
+    double h = 0.0;
+    for (int x = 0; x < V; ++x) {
+        const double l = widen(dtype, base, off + x) / temp - lz;
+        const double p = exp(l);
+#if ORACLE_MUTATION == 9 /* planted: the entropy sums p log p with the wrong sign */
+        if (p > 0.0) h += p * l;
+#else
+        if (p > 0.0) h -= p * l;
+#endif
+    }
+    return h;
+}
+
+/* KL(p || q) of one position: sum_x p(x) (log p(x) - log q(x)); terms with p(x) = 0 are 0,
+ * and q(x) = 0 < p(x) makes it +inf. */
+static double row_kl(int dtype, const void *target, const void *draft, int64_t off, int V,
+                     double T, double Td) {
+    const double zp = row_log_normaliser(dtype, target, off, V, T);
+    const double zq = row_log_normaliser(dtype, draft, off, V, Td);
+    double kl = 0.0;
+    for (int x = 0; x < V; ++x) {
+        const double lp = widen(dtype, target, off + x) / T - zp;
+        const double p = exp(lp);
+        if (p == 0.0) continue;
+        const double lq = widen(dtype, draft, off + x) / Td - zq;
+        kl += p * (lp - lq);
+    }
+    return kl;
+}
+
+/* H(p_i) for i <= gamma, H(q_i) and KL(p_i || q_i) for i < gamma, every sequence (NULL
+ * outputs are skipped).  T, Td: per sequence. */
+void oracle_position_stats(int dtype, const void *target, const void *draft, int B, int gamma,
+                           int V, const double *T, const double *Td, double *out_Hp,
+                           double *out_Hq, double *out_KL) {
+    for (int b = 0; b < B; ++b) {
+        for (int i = 0; i <= gamma; ++i) {
+            const int64_t toff = ((int64_t)b * (gamma + 1) + i) * V;
+            if (out_Hp) out_Hp[(int64_t)b * (gamma + 1) + i] = row_entropy(dtype, target, toff, V, T[b]);
+            if (i == gamma) continue;
+            const int64_t doff = ((int64_t)b * gamma + i) * V;
+            if (out_Hq) out_Hq[(int64_t)b * gamma + i] = row_entropy(dtype, draft, doff, V, Td[b]);
+            if (out_KL) {
+                /* target row i and draft row i have different offsets: KL over the pair */
+                const double zp = row_log_normaliser(dtype, target, toff, V, T[b]);
+                const double zq = row_log_normaliser(dtype, draft, doff, V, Td[b]);
+                double kl = 0.0;
+                for (int x = 0; x < V; ++x) {
+                    const double lp = widen(dtype, target, toff + x) / T[b] - zp;
+                    const double p = exp(lp);
+                    if (p == 0.0) continue;
+                    kl += p * (lp - (widen(dtype, draft, doff + x) / Td[b] - zq));
+                }
+                out_KL[(int64_t)b * gamma + i] = kl;
+            }
+        }
+    }
+}
+
+/* Rows laid out alike (row r of `target` and of `draft`): KL per row (for the pins). */
+void oracle_row_kl(int dtype, const void *target, const void *draft, int rows, int V,
+                   double T, double Td, double *out) {
+    for (int r = 0; r < rows; ++r) out[r] = row_kl(dtype, target, draft, (int64_t)r * V, V, T, Td);
+}
+
+/* Entropy of each of `rows` contiguous rows at temperature temp. */
+void oracle_row_entropies(int dtype, const void *base, int rows, int V, double temp, double *out) {
+    for (int r = 0; r < rows; ++r) out[r] = row_entropy(dtype, base, (int64_t)r * V, V, temp);
+}
+
+/* Class centres after a verify: centres[b] = {accepted, rejected}, Hq[b][i] the draft
+ * entropies, n[b] the accepted count (gamma: all accepted; -1: bad draft, no update). */
+void oracle_entropy_centres_update(int B, int gamma, const double *Hq, const int32_t *n,
+                                   double beta, double *centres) {
+    for (int b = 0; b < B; ++b) {
+        const int j = n[b];
+        if (j < 0) continue;
+        for (int i = 0; i <= j && i < gamma; ++i) {
+#if ORACLE_MUTATION == 6 /* planted: the accepted and rejected centres swapped */
+            double *c = centres + 2 * (int64_t)b + (i < j ? 1 : 0);
+#else
+            double *c = centres + 2 * (int64_t)b + (i < j ? 0 : 1);
+#endif
+            *c = (1.0 - beta) * *c + beta * Hq[(int64_t)b * gamma + i];
+        }
+    }
+}
+
+/* Acceptance probability of a draft token of entropy H. */
+double oracle_soft_accept(double H, double c_acc, double c_rej) {
+    const double da = fabs(H - c_acc), dr = fabs(H - c_rej);
+    if (da + dr == 0.0) return 0.5;
+#if ORACLE_MUTATION == 7 /* planted: soft classification inverted */
+    return da / (da + dr);
+#else
+    return dr / (da + dr);
+#endif
+}
+
+/* k* per sequence from the entropies H[b][0..K-1] of its next K draft tokens: candidates
+ * cand[0..n_cand-1] (each in 1..K); out_eff[b] = the best efficiency (NULL: skipped). */
+int oracle_adaptive_k(int B, int K, const double *H, const double *centres,
+                      const int32_t *cand, int n_cand, double Cd, double Cv, int32_t *out_k,
+                      double *out_eff) {
+    for (int c = 0; c < n_cand; ++c)
+        if (cand[c] < 1 || cand[c] > K) return -1;
+    for (int b = 0; b < B; ++b) {
+        int best_k = -1;
+        double best = -INFINITY;
+        for (int c = 0; c < n_cand; ++c) {
+            const int k = cand[c];
+            double prod = 1.0, expect = 0.0;
+            for (int m = 0; m < k; ++m) {
+#if ORACLE_MUTATION == 8 /* planted: expected yield sums p_i instead of prefix products */
+                prod = oracle_soft_accept(H[(int64_t)b * K + m], centres[2 * (int64_t)b],
+                                          centres[2 * (int64_t)b + 1]);
+#else
+                prod *= oracle_soft_accept(H[(int64_t)b * K + m], centres[2 * (int64_t)b],
+                                           centres[2 * (int64_t)b + 1]);
+#endif
+                expect += prod;
+            }
+            const double eff = (1.0 + expect) / ((double)k * Cd + Cv);
+            if (eff > best) {
+                best = eff;
+                best_k = k;
+            }
+        }
+        out_k[b] = best_k;
+        if (out_eff) out_eff[b] = best;
+    }
+    return 0;
+}
