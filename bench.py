@@ -311,6 +311,32 @@ def run_ours(args):
         if status != sv.SPEC_OK:
             raise RuntimeError(f"device status after early exit: {sv.spec_verify_strerror(status)}")
 
+    # the same call also producing the per-position entropies and KL divergences
+    stats = None
+    if not greedy:
+        stats_out = {"Hp": torch.empty((w.B, w.gamma + 1), dtype=torch.float32, device=dev),
+                     "Hq": torch.empty((w.B, w.gamma), dtype=torch.float32, device=dev),
+                     "KL": torch.empty((w.B, w.gamma), dtype=torch.float32, device=dev)}
+
+        def sstep():
+            kw = dict(T_per_seq=Tq, Td_per_seq=Tdq) if per_seq else {}
+            sv.spec_verify_ex(t, d, tok, float(w.T[0]), float(w.Td[0]), args.seed, out_t,
+                              out_n, seq_index_base=seq_base, position_stats=stats_out, **kw)
+        for _ in range(3):
+            sstep()
+        torch.cuda.synchronize()
+        Ks = min(K, 300)
+        ss0, ss1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ss0.record(stream)
+        for _ in range(Ks):
+            sstep()
+        ss1.record(stream)
+        torch.cuda.synchronize()
+        sms = ss0.elapsed_time(ss1) / Ks
+        stats = {"value": ws_ * w.rows / (sms / 1e3), "unit": UNIT, "ms_per_step": sms,
+                 "steps": Ks, "GBps_one_read": alg_bytes / (sms / 1e3) / 1e9,
+                 "note": "same call with H(p_i), H(q_i), KL(p_i||q_i) for every position"}
+
     # end to end: inputs from pinned host memory, outputs read back, every step
     e2e = None
     if not args.no_e2e:
@@ -386,6 +412,7 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "early_exit": early,
+        "with_position_stats": stats,
         "gpu_launches": nkern * K,
         "clocks": clocks,
     }
@@ -465,14 +492,21 @@ def run_table(args):
             out_t = torch.empty((w.B, w.gamma + 1), dtype=torch.int32, device=dev)
             out_n = torch.empty((w.B,), dtype=torch.int32, device=dev)
             kw = dict(T_per_seq=Tq, Td_per_seq=Tdq) if cfg == 3 else {}
+            stats_out = {"Hp": torch.empty((w.B, w.gamma + 1), dtype=torch.float32, device=dev),
+                         "Hq": torch.empty((w.B, w.gamma), dtype=torch.float32, device=dev),
+                         "KL": torch.empty((w.B, w.gamma), dtype=torch.float32, device=dev)}
             modes = [("greedy", None)] if greedy else [("two-kernel", 0), ("fused", sv.SPEC_FLAG_FUSED),
-                                                        ("early-exit", sv.SPEC_FLAG_EARLY_EXIT)]
+                                                        ("early-exit", sv.SPEC_FLAG_EARLY_EXIT),
+                                                        ("with H, KL", "stats")]
             for label, dbg in modes:
                 for warm in ([False, True] if copies > 1 else [False]):
                     def call(k):
                         t, d = bufs[0 if warm else k % copies]
                         if greedy:
                             sv.spec_verify_greedy_ex(t, tok, out_t, out_n)
+                        elif dbg == "stats":
+                            sv.spec_verify_ex(t, d, tok, float(w.T[0]), float(w.Td[0]), 0, out_t,
+                                              out_n, position_stats=stats_out, **kw)
                         else:
                             sv.spec_verify_ex(t, d, tok, float(w.T[0]), float(w.Td[0]), 0, out_t,
                                               out_n, flags=dbg, **kw)

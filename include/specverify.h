@@ -90,10 +90,27 @@ typedef struct {
     float *out_race;            /* [B, 2]       winning race score ln(w(y)/E_y), and the
                                                 runner-up score (approximate) */
     void *prof_events[4];       /* optional cudaEvent_t: recorded before the first kernel and
-                                   after each kernel of the call (sampling: two kernels, or
-                                   one with SPEC_FLAG_FUSED or SPEC_FLAG_EARLY_EXIT;
-                                   greedy: two) */
+                                   after each kernel of the call (sampling: two kernels, three
+                                   with per-position statistics, one with SPEC_FLAG_FUSED or
+                                   SPEC_FLAG_EARLY_EXIT; greedy: two) */
     uint32_t flags;             /* SPEC_FLAG_* / SPEC_DEBUG_* bits; 0 in normal use */
+    /* Per-position statistics ("投机解码的第二本账" (SparseSpec-L), section 3.3: every draft
+     * token's entropy feeds two class centres, accepted and rejected, kept as moving
+     * averages; "SubSpec: the target model's own low-bit shadow as the draft model" quotes
+     * the draft-target KL divergence).  Device, NULL = not computed; all in nats.  Asking
+     * for any of them reads every logit in one pass paired by position (target row i with
+     * draft row i) and runs the full read whatever the flags say. */
+    float *out_H_p;             /* [B, gamma+1] entropy of p_i = softmax(L_t[b,i] / T_b) */
+    float *out_H_q;             /* [B, gamma]   entropy of q_i = softmax(L_d[b,i] / Td_b) */
+    float *out_KL;              /* [B, gamma]   KL(p_i || q_i) (+inf where q = 0 < p) */
+    double *ctrl_centres;       /* [B, 2] device (accepted, rejected) class centres of draft
+                                   entropies, updated in place after the verify: positions
+                                   before the first rejection j move the accepted centre,
+                                   position j (if j < gamma) the rejected one, in position
+                                   order, c <- (1 - beta) c + beta H(q_i); positions after j
+                                   and sequences with a bad draft token leave them alone */
+    double ctrl_beta;           /* the moving averages' rate, 0 < beta <= 1 (else SPEC_EINVAL
+                                   when ctrl_centres is set) */
 } spec_verify_opts;
 
 /* flags bits. */
@@ -183,15 +200,43 @@ const char *spec_verify_strerror(int status);
  * array that this call clears first and that spec_verify_check cannot read (a bad draft
  * token still shows as n_accepted = -1).  No cudaMalloc, cudaFree or allocating library
  * routine is called.
+ * SPEC_FLAG_EARLY_EXIT and the per-position statistics (out_H_p, out_H_q, out_KL,
+ * ctrl_centres) are ignored here.
  * Returns SPEC_ESCRATCH, without launching anything, when spec_verify_workspace_bytes() of
  * the problem exceeds SPEC_NOALLOC_SCRATCH_BYTES - 256; otherwise as spec_verify_ex.
  */
 #define SPEC_NOALLOC_SCRATCH_BYTES (8u << 20) /* 8 MiB: B=256, gamma=12, V=152064 bf16 needs
-                                                 2.1 MB */
+                                                 4.3 MB */
 int spec_verify_noalloc(const void *target_logits, const void *draft_logits,
                         const int32_t *draft_tokens, int B, int gamma, int V, float T, float T_d,
                         uint64_t seed, int32_t *out_tokens, int32_t *out_n_accepted,
                         const spec_verify_opts *opts, void *stream);
+
+/*
+ * Entropy of softmax(L / T) of each of `rows` contiguous rows of V logits (dtype
+ * spec_dtype), in nats, into out_H [rows] (device) -- e.g. the next draft tokens' entropies
+ * for spec_adaptive_k.  Uses the library's own workspace.  SPEC_EINVAL for bad sizes, a
+ * non-positive or non-finite T, NULL or misaligned pointers.
+ */
+int spec_row_entropy(const void *logits, int rows, int V, float T, int dtype, float *out_H,
+                     void *stream);
+
+/*
+ * Adaptive draft length ("投机解码的第二本账" (SparseSpec-L), section 3.3).  For each of B
+ * sequences, the acceptance probability of its next draft tokens i = 1..K comes from their
+ * entropies H_next [B, K] (device, fp32) and the sequence's class centres [B, 2] (device,
+ * fp64: accepted, rejected): p_i = d_rej / (d_acc + d_rej) with d = |H_i - centre| (1/2 when
+ * both distances are 0).  The chosen length is the candidate k maximising
+ *     (1 + sum_{m=1..k} prod_{i=1..m} p_i) / (k C_d + C_v),
+ * the earlier candidate on equal values; candidates (host array, 1..64 values, each in
+ * 1..K) are the caller's, as are the draft and verify costs C_d and C_v.  Writes out_k [B]
+ * (device int32) and, if not NULL, the best value into out_eff [B] (device fp64).  Computed
+ * in fp64, each operation rounded on its own, in the order of the formula.  SPEC_EINVAL for
+ * bad sizes, candidates outside 1..K, non-finite costs or a non-positive k C_d + C_v.
+ */
+int spec_adaptive_k(const float *H_next, int B, int K, const double *centres,
+                    const int32_t *candidates, int n_cand, double C_d, double C_v,
+                    int32_t *out_k, double *out_eff, void *stream);
 
 #ifdef __cplusplus
 }

@@ -96,6 +96,13 @@ struct VerifyParams {
     float* out_logZq;
     float* out_u;
     float* out_race;
+    // per-position statistics (pair_stats / position_stats)
+    float2* ext_parts;          // [B][2*gamma+1][npieces] entropy and cross terms per piece
+    float* out_Hp;              // [B, gamma+1] entropy of p_i (nats), or nullptr
+    float* out_Hq;              // [B, gamma]   entropy of q_i (nats), or nullptr
+    float* out_KL;              // [B, gamma]   KL(p_i || q_i) (nats), or nullptr
+    double* ctrl_centres;       // [B, 2] entropy class centres updated in place, or nullptr
+    double ctrl_beta;
 };
 
 // Row pieces of the streaming passes: between kMinPieceBytes and kMaxPieceBytes of logits
@@ -259,6 +266,310 @@ __global__ void __launch_bounds__(256, SPECVERIFY_STATS_MINBLOCKS) row_stats_ker
         row_stats_item<ET, U>(p, static_cast<int>(br / R), static_cast<int>(br % R), piece, lane);
     }
     asm volatile("griddepcontrol.launch_dependents;");
+}
+
+// ----------------------------------------------------------------------------------------
+// Per-position entropies and KL divergence, and the entropy class centres
+// ("投机解码的第二本账" (SparseSpec-L), section 3.3: every draft token's entropy H_i; class
+// centres of the entropies of accepted and rejected tokens kept as moving averages.  KL is
+// the draft-target divergence quoted by "SubSpec: the target model's own low-bit shadow as
+// the draft model").
+//
+// pair_stats replaces row_stats when these are asked for: one item is a piece of target
+// row i together with the same piece of draft row i (target row gamma alone), so the same
+// bytes are read once.  Besides each row's (max m, sum s) partial -- written exactly as
+// row_stats writes it, so the scan and race read it unchanged -- a lane keeps, in base 2
+// with t = x c - m,
+//     A = sum 2^t t            (entropy: H = ln 2 (log2 s - A / s))
+//     C = sum 2^tp tq          (p-weighted draft log-weights, relative to the draft max)
+// so that KL(p || q) = ln 2 (A_p / s_p - log2 s_p - C / s_p + log2 s_q).  A change of a max
+// from m to m' (delta = m - m') rescales A to 2^delta (A + s delta), and C to
+// 2^delta_p (C + s_p delta_q).  A term whose weight 2^t is 0 contributes nothing (no 0 * inf).
+// ----------------------------------------------------------------------------------------
+
+struct PairStat {
+    float mp, sp, ap, c;  // target row: max, sum, entropy term, cross term
+    float mq, sq, aq;     // draft row
+};
+
+__device__ __forceinline__ void pair_rescale(float& m, float& s, float& a, float mn) {
+    const float d = m - mn;  // <= 0
+    const float f = ex2_fast(d);
+    a = f * fmaf(s, d, a);
+    s *= f;
+    m = mn;
+}
+
+__device__ __forceinline__ PairStat pair_merge(PairStat x, PairStat y) {
+    PairStat r;
+    const float Mp = fmaxf(x.mp, y.mp), Mq = fmaxf(x.mq, y.mq);
+    const float dxp = x.mp - Mp, dyp = y.mp - Mp, dxq = x.mq - Mq, dyq = y.mq - Mq;
+    const float fxp = ex2_fast(dxp), fyp = ex2_fast(dyp), fxq = ex2_fast(dxq), fyq = ex2_fast(dyq);
+    r.mp = Mp;
+    r.mq = Mq;
+    r.sp = x.sp * fxp + y.sp * fyp;
+    r.ap = fxp * fmaf(x.sp, dxp, x.ap) + fyp * fmaf(y.sp, dyp, y.ap);
+    r.c = fxp * fmaf(x.sp, dxq, x.c) + fyp * fmaf(y.sp, dyq, y.c);
+    r.sq = x.sq * fxq + y.sq * fyq;
+    r.aq = fxq * fmaf(x.sq, dxq, x.aq) + fyq * fmaf(y.sq, dyq, y.aq);
+    return r;
+}
+
+__device__ __forceinline__ PairStat warp_pair_merge(PairStat v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        PairStat o;
+        o.mp = __shfl_xor_sync(0xffffffffu, v.mp, off);
+        o.sp = __shfl_xor_sync(0xffffffffu, v.sp, off);
+        o.ap = __shfl_xor_sync(0xffffffffu, v.ap, off);
+        o.c = __shfl_xor_sync(0xffffffffu, v.c, off);
+        o.mq = __shfl_xor_sync(0xffffffffu, v.mq, off);
+        o.sq = __shfl_xor_sync(0xffffffffu, v.sq, off);
+        o.aq = __shfl_xor_sync(0xffffffffu, v.aq, off);
+        v = pair_merge(v, o);
+    }
+    return v;
+}
+
+// Exponents below this are clamped in the extra terms: a weight 2^t is then 0 and 0 times
+// the clamp is 0, with no branch; a draft exponent at the clamp under a positive target
+// weight (q(x) = 0 < p(x)) drives C below kKlInfinite, which position_stats reports as an
+// infinite KL.  Exponents of real logits are far above both (|t| < 2^16 for |x c| < 2^15).
+constexpr float kTermClamp = -1e30f;
+constexpr float kKlInfinite = -1e20f;
+
+// One element pair (target logit xp, draft logit xq; has_q: the position has a draft row).
+__device__ __forceinline__ void pair_push(PairStat& st, float xp, float xq, float cp, float cq,
+                                          bool has_q) {
+    const float tp = fmaxf(fmaf(xp, cp, -st.mp), kTermClamp), ep = ex2_fast(tp);
+    st.sp += ep;
+    st.ap = fmaf(ep, tp, st.ap);
+    if (has_q) {
+        const float tq = fmaxf(fmaf(xq, cq, -st.mq), kTermClamp), eq = ex2_fast(tq);
+        st.sq += eq;
+        st.aq = fmaf(eq, tq, st.aq);
+        st.c = fmaf(ep, tq, st.c);
+    }
+}
+
+// Partial statistics of elements [x0, x1) of target row i and (has_q) draft row i, whose
+// starts have the same alignment (both rows are V elements apart from their tensor's base,
+// and both bases are 16-byte aligned).
+template <class ET, int U>
+__device__ __forceinline__ PairStat pair_piece(const typename ET::storage* rp,
+                                               const typename ET::storage* rq, bool has_q,
+                                               int x0, int x1, float cp, float cq, int lane) {
+    PairStat st{-FLT_MAX, 0.0f, 0.0f, 0.0f, -FLT_MAX, 0.0f, 0.0f};
+    const RowSpan<ET> sp(rp, x0, x1);
+    const RowSpan<ET> sq(has_q ? rq : rp, x0, x1);
+    const bool same = sp.head == sq.head;  // equal alignment: vectors pair up
+    // raise the maxima to (mp, mq): C is shifted with the draft max, then rescaled with the
+    // target weights
+    auto raise = [&](float mp, float mq) {
+        st.c = fmaf(st.sp, st.mq - mq, st.c);
+        pair_rescale(st.mq, st.sq, st.aq, mq);
+        const float d = st.mp - mp, f = ex2_fast(d);
+        st.ap = f * fmaf(st.sp, d, st.ap);
+        st.c *= f;
+        st.sp *= f;
+        st.mp = mp;
+    };
+    auto push_scalar = [&](int x) {
+        const float xp = ET::load1(rp + x);
+        const float xq = has_q ? ET::load1(rq + x) : -INFINITY;
+        raise(fmaxf(st.mp, fmaxf(xp * cp, -FLT_MAX)), fmaxf(st.mq, fmaxf(xq * cq, -FLT_MAX)));
+        pair_push(st, xp, xq, cp, cq, has_q);
+    };
+    if (!same) {  // unaligned pair (only when a caller's draft base breaks the rule): scalar
+        for (int x = x0 + lane; x < x1; x += 32) push_scalar(x);
+        return warp_pair_merge(st);
+    }
+    if (lane < sp.head) push_scalar(x0 + lane);
+    const uint4* vp = sp.vec();
+    const uint4* vq = sq.vec();
+    for (int v0 = 0; v0 < sp.nvec; v0 += 32 * U) {
+        uint4 rawp[U], rawq[U];
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const int v = v0 + lane + 32 * k;
+            const uint4 ninf = make_uint4(ET::kNegInfWord, ET::kNegInfWord, ET::kNegInfWord, ET::kNegInfWord);
+            rawp[k] = v < sp.nvec ? ld_stream16(vp + v) : ninf;
+            rawq[k] = (has_q && v < sp.nvec) ? ld_stream16(vq + v) : ninf;
+        }
+        float bp = -INFINITY, bq = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            float f[ET::kVec], g[ET::kVec];
+            ET::widen(rawp[k], f);
+            ET::widen(rawq[k], g);
+#pragma unroll
+            for (int e = 0; e < ET::kVec; ++e) {
+                bp = fmaxf(bp, f[e]);
+                bq = fmaxf(bq, g[e]);
+            }
+        }
+        raise(fmaxf(st.mp, fmaxf(bp * cp, -FLT_MAX)), fmaxf(st.mq, fmaxf(bq * cq, -FLT_MAX)));
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            float f[ET::kVec], g[ET::kVec];
+            ET::widen(rawp[k], f);
+            ET::widen(rawq[k], g);
+#pragma unroll
+            for (int e = 0; e < ET::kVec; ++e) pair_push(st, f[e], g[e], cp, cq, has_q);
+        }
+    }
+    const int t0 = sp.head + sp.nvec * ET::kVec;
+    if (lane < sp.tail) push_scalar(x0 + t0 + lane);
+    return warp_pair_merge(st);
+}
+
+// pair_stats: row_stats with the extra terms (see above).  Item (b, i, piece), i <= gamma.
+#ifndef SPECVERIFY_PAIR_MINBLOCKS
+#define SPECVERIFY_PAIR_MINBLOCKS 3
+#endif
+template <class ET, int U>
+__global__ void __launch_bounds__(256, SPECVERIFY_PAIR_MINBLOCKS) pair_stats_kernel(VerifyParams p) {
+    using S = typename ET::storage;
+    const int lane = threadIdx.x & 31;
+    const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
+    const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (long long k = tid; k < static_cast<long long>(p.B) * p.rpieces; k += nthreads)
+        reinterpret_cast<uint4*>(p.race_parts)[k] = make_uint4(0u, 0u, 0u, 0u);
+    for (long long k = tid; k < p.B; k += nthreads) p.tickets[k] = 0;
+    const long long nwarps = nthreads >> 5;
+    const int R = 2 * p.gamma + 1;
+    const long long total = static_cast<long long>(p.B) * (p.gamma + 1) * p.npieces;
+    for (long long item = tid >> 5; item < total; item += nwarps) {
+        const int piece = static_cast<int>(item % p.npieces);
+        const long long bi = item / p.npieces;
+        const int b = static_cast<int>(bi / (p.gamma + 1)), i = static_cast<int>(bi % (p.gamma + 1));
+        const bool has_q = i < p.gamma;
+        const S* rp = static_cast<const S*>(p.target) + (static_cast<long long>(b) * (p.gamma + 1) + i) * p.V;
+        const S* rq = has_q ? static_cast<const S*>(p.draft) + (static_cast<long long>(b) * p.gamma + i) * p.V
+                            : rp;
+        const int x0 = piece * p.piece_len;
+        const PairStat st = pair_piece<ET, U>(rp, rq, has_q, x0, min(p.V, x0 + p.piece_len),
+                                              scale_of(seq_T(p, b)), scale_of(seq_Td(p, b)), lane);
+        if (lane == 0) {
+            const long long kp = (static_cast<long long>(b) * R + i) * p.npieces + piece;
+            store_stat(p.stat_parts + kp, st.mp, st.sp);
+            p.ext_parts[kp] = make_float2(st.ap, st.c);
+            if (has_q) {
+                const long long kq = (static_cast<long long>(b) * R + p.gamma + 1 + i) * p.npieces + piece;
+                store_stat(p.stat_parts + kq, st.mq, st.sq);
+                p.ext_parts[kq] = make_float2(st.aq, 0.0f);
+            }
+        }
+    }
+    asm volatile("griddepcontrol.launch_dependents;");
+}
+
+// position_stats: one block per sequence merges the pieces of every position into H(p_i),
+// H(q_i) and KL(p_i || q_i); then, given class centres, moves them with this verify's
+// outcome (positions before the first rejection j update the accepted centre, position j
+// the rejected one, in position order; c <- (1 - beta) c + beta H(q_i), in fp64 with every
+// operation rounded on its own).  Runs after the scan, whose accepted counts it reads.
+__global__ void __launch_bounds__(256) position_stats_kernel(VerifyParams p) {
+    extern __shared__ float s_hq[];  // [gamma]
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    const int b = blockIdx.x;
+    const int R = 2 * p.gamma + 1;
+    for (int i = wib; i <= p.gamma; i += 8) {
+        const bool has_q = i < p.gamma;
+        PairStat acc{-FLT_MAX, 0.0f, 0.0f, 0.0f, -FLT_MAX, 0.0f, 0.0f};
+        const long long base_p = (static_cast<long long>(b) * R + i) * p.npieces;
+        const long long base_q = (static_cast<long long>(b) * R + p.gamma + 1 + i) * p.npieces;
+        for (int k = lane; k < p.npieces; k += 32) {
+            const float2 sp = p.stat_parts[base_p + k], ep = p.ext_parts[base_p + k];
+            PairStat x{sp.x, sp.y, ep.x, ep.y, -FLT_MAX, 0.0f, 0.0f};
+            if (has_q) {
+                const float2 sq = p.stat_parts[base_q + k], eq = p.ext_parts[base_q + k];
+                x.mq = sq.x;
+                x.sq = sq.y;
+                x.aq = eq.x;
+            }
+            acc = pair_merge(acc, x);
+        }
+        acc = warp_pair_merge(acc);
+        if (lane == 0) {
+            const float l2p = log2f(acc.sp), l2q = log2f(acc.sq);
+            const float hp = kLn2 * (l2p - acc.ap / acc.sp);
+            if (p.out_Hp) p.out_Hp[static_cast<long long>(b) * (p.gamma + 1) + i] = hp;
+            if (has_q) {
+                const float hq = kLn2 * (l2q - acc.aq / acc.sq);
+                const float cs = acc.c / acc.sp;
+                const float kl = cs < kKlInfinite ? INFINITY
+                                                  : kLn2 * (acc.ap / acc.sp - cs - l2p + l2q);
+                if (p.out_Hq) p.out_Hq[static_cast<long long>(b) * p.gamma + i] = hq;
+                if (p.out_KL) p.out_KL[static_cast<long long>(b) * p.gamma + i] = kl;
+                s_hq[i] = hq;
+            }
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && p.ctrl_centres) {
+        const int j = p.out_n[b];
+        if (j >= 0) {
+            const double beta = p.ctrl_beta, keep = __dsub_rn(1.0, beta);
+            for (int i = 0; i <= j && i < p.gamma; ++i) {
+                double* c = p.ctrl_centres + 2 * static_cast<long long>(b) + (i < j ? 0 : 1);
+                *c = __dadd_rn(__dmul_rn(keep, *c), __dmul_rn(beta, static_cast<double>(s_hq[i])));
+            }
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------------------
+// Adaptive draft length ("投机解码的第二本账" (SparseSpec-L), section 3.3): each next draft
+// token's acceptance probability p_i comes from its entropy's distances to the two class
+// centres, p = d_rej / (d_acc + d_rej) (1/2 when both are 0), and the draft length is the
+// candidate k maximising (1 + sum_{m=1..k} prod_{i<=m} p_i) / (k C_d + C_v), the earlier
+// candidate on equal values.  One thread per sequence, fp64 with every operation rounded on
+// its own, in the order of that definition.
+// ----------------------------------------------------------------------------------------
+
+constexpr int kMaxCandidates = 64;
+
+struct AdaptiveKParams {
+    const float* H;          // [B, K] next draft tokens' entropies
+    const double* centres;   // [B, 2] (accepted, rejected)
+    int B, K, n_cand;
+    int cand[kMaxCandidates];
+    double Cd, Cv;
+    int32_t* out_k;          // [B]
+    double* out_eff;         // [B] or nullptr
+};
+
+__device__ __forceinline__ double soft_accept(double H, double ca, double cr) {
+    const double da = fabs(__dsub_rn(H, ca)), dr = fabs(__dsub_rn(H, cr));
+    const double s = __dadd_rn(da, dr);
+    return s == 0.0 ? 0.5 : __ddiv_rn(dr, s);
+}
+
+__global__ void adaptive_k_kernel(AdaptiveKParams a) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= a.B) return;
+    const double ca = a.centres[2 * static_cast<long long>(b)];
+    const double cr = a.centres[2 * static_cast<long long>(b) + 1];
+    const float* h = a.H + static_cast<long long>(b) * a.K;
+    int best_k = -1;
+    double best = -INFINITY;
+    for (int c = 0; c < a.n_cand; ++c) {
+        const int k = a.cand[c];
+        double prod = 1.0, expect = 0.0;
+        for (int m = 0; m < k; ++m) {
+            prod = __dmul_rn(prod, soft_accept(static_cast<double>(h[m]), ca, cr));
+            expect = __dadd_rn(expect, prod);
+        }
+        const double eff = __ddiv_rn(__dadd_rn(1.0, expect),
+                                     __dadd_rn(__dmul_rn(static_cast<double>(k), a.Cd), a.Cv));
+        if (eff > best) {
+            best = eff;
+            best_k = k;
+        }
+    }
+    a.out_k[b] = best_k;
+    if (a.out_eff) a.out_eff[b] = best;
 }
 
 // ----------------------------------------------------------------------------------------

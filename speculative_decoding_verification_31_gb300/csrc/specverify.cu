@@ -35,7 +35,7 @@ int elem_bytes(int dtype) { return dtype == SPEC_F32 ? 4 : 2; }
 struct Layout {
     int piece_len, npieces;
     int rpiece_len, rpieces;
-    size_t stat_off, seq_off, race_off, rowstat_off;
+    size_t stat_off, ext_off, seq_off, race_off, rowstat_off;
     size_t ctl_off, ctl_bytes;          // zeroed control block: row_done, seq_done, tickets, ready
     size_t row_done_off, seq_done_off, ticket_off, ready_off, race_cursor_off,
         row_cursor_off;
@@ -65,6 +65,8 @@ Layout layout_of(int B, int gamma, int V, int dtype, long long stream_warps = 0)
     const size_t R = 2 * static_cast<size_t>(gamma) + 1;
     size_t off = 0;
     L.stat_off = off;
+    off = align_up(off + static_cast<size_t>(B) * R * max_np * sizeof(float2), 256);
+    L.ext_off = off;  // per-position statistics: entropy and cross terms per row piece
     off = align_up(off + static_cast<size_t>(B) * R * max_np * sizeof(float2), 256);
     L.seq_off = off;
     off = align_up(off + static_cast<size_t>(B) * sizeof(SeqInfo), 256);
@@ -220,6 +222,7 @@ void bind_workspace(VerifyParams& p, const Layout& L, char* ws) {
     p.rpiece_len = L.rpiece_len;
     p.rpieces = L.rpieces;
     p.stat_parts = reinterpret_cast<float2*>(ws + L.stat_off);
+    p.ext_parts = reinterpret_cast<float2*>(ws + L.ext_off);
     p.seq = reinterpret_cast<SeqInfo*>(ws + L.seq_off);
     p.race_parts = reinterpret_cast<RacePart*>(ws + L.race_off);
     p.row_stat = reinterpret_cast<float2*>(ws + L.rowstat_off);
@@ -315,13 +318,30 @@ cudaError_t launch_pdl(K kernel, int grid, size_t smem, cudaStream_t s, bool pdl
 
 // Two-kernel sampling verify: the streaming pass, then the scan-race kernel as its
 // programmatic dependent (its blocks start while the streaming pass drains).
+#ifndef SPECVERIFY_PAIR_UNROLL
+#define SPECVERIFY_PAIR_UNROLL 3
+#endif
+constexpr int kPairUnroll = SPECVERIFY_PAIR_UNROLL;  // 16-byte loads per row in flight per lane
+
+// Whether a call asks for the per-position statistics (entropies, KL, class centres).
+bool wants_position_stats(const VerifyParams& p) {
+    return p.out_Hp || p.out_Hq || p.out_KL || p.ctrl_centres;
+}
+
 template <class ET>
 int launch_sampling(VerifyParams& p, int sm_count, const spec_verify_opts* o, cudaStream_t s) {
     const int R = 2 * p.gamma + 1;
+    const bool extra = wants_position_stats(p);
     record(o, 0, s);
-    const long long stat_items = static_cast<long long>(p.B) * R * p.npieces;
-    row_stats_kernel<ET, kUnroll><<<grid_for(row_stats_kernel<ET, kUnroll>, sm_count, stat_items),
-                                    kThreads, 0, s>>>(p);
+    if (extra) {  // the same read of every logit, paired by position, with the extra terms
+        const long long items = static_cast<long long>(p.B) * (p.gamma + 1) * p.npieces;
+        pair_stats_kernel<ET, kPairUnroll><<<grid_for(pair_stats_kernel<ET, kPairUnroll>, sm_count, items),
+                                             kThreads, 0, s>>>(p);
+    } else {
+        const long long stat_items = static_cast<long long>(p.B) * R * p.npieces;
+        row_stats_kernel<ET, kUnroll><<<grid_for(row_stats_kernel<ET, kUnroll>, sm_count, stat_items),
+                                        kThreads, 0, s>>>(p);
+    }
     record(o, 1, s);
     // blocks per sequence: about one resident wave of scan-race blocks in total
     {
@@ -341,6 +361,10 @@ int launch_sampling(VerifyParams& p, int sm_count, const spec_verify_opts* o, cu
                    2 * R * sizeof(float), s, !(o && o->prof_events[1]), p) != cudaSuccess)
         return SPEC_ECUDA;
     record(o, 2, s);
+    if (extra) {
+        position_stats_kernel<<<p.B, kThreads, static_cast<size_t>(p.gamma) * sizeof(float), s>>>(p);
+        record(o, 3, s);
+    }
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
 }
 
@@ -463,6 +487,12 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, const in
         p.out_logZq = opts->out_logZ_q;
         p.out_u = opts->out_u;
         p.out_race = opts->out_race;
+        p.out_Hp = opts->out_H_p;
+        p.out_Hq = opts->out_H_q;
+        p.out_KL = opts->out_KL;
+        p.ctrl_centres = opts->ctrl_centres;
+        p.ctrl_beta = opts->ctrl_beta;
+        if (p.ctrl_centres && !(p.ctrl_beta > 0.0 && p.ctrl_beta <= 1.0)) return SPEC_EINVAL;
     }
     p.debug_flags = (opts && (opts->flags & SPEC_DEBUG_NEVER_READY)) ? kDebugNeverReady : 0u;
     DeviceState* d = nullptr;
@@ -471,12 +501,12 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, const in
     if (rc) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool diagnostics = p.out_logp || p.out_logq || p.out_logZp || p.out_logZq || p.out_u ||
-                             p.out_race;
+                             p.out_race || wants_position_stats(p);
     const Layout L = layout_of(B, gamma, V, dtype, d->stream_warps[dtype == SPEC_F32 ? 0 : 1]);
     if (d->coop && opts && (opts->flags & SPEC_FLAG_EARLY_EXIT) && !diagnostics)
         return dtype == SPEC_F32 ? launch_early<F32Elem>(p, d->sm_count, opts, s, L, ws)
                                  : launch_early<Bf16Elem>(p, d->sm_count, opts, s, L, ws);
-    const bool fused = d->coop && opts && (opts->flags & SPEC_FLAG_FUSED);
+    const bool fused = d->coop && opts && (opts->flags & SPEC_FLAG_FUSED) && !wants_position_stats(p);
     if (fused) {
         return dtype == SPEC_F32 ? launch_fused<F32Elem>(p, d->sm_count, opts, s, L, ws)
                                  : launch_fused<Bf16Elem>(p, d->sm_count, opts, s, L, ws);
@@ -536,6 +566,61 @@ int spec_verify_check(void* stream, int32_t* d_status) {
     if (cudaMemsetAsync(st, 0, sizeof(int32_t), s) != cudaSuccess) return SPEC_ECUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return SPEC_ECUDA;
     return h;
+}
+
+int spec_adaptive_k(const float* H_next, int B, int K, const double* centres,
+                    const int32_t* candidates, int n_cand, double C_d, double C_v,
+                    int32_t* out_k, double* out_eff, void* stream) {
+    if (B < 0 || K < 1 || n_cand < 1 || n_cand > kMaxCandidates || !candidates) return SPEC_EINVAL;
+    if (!std::isfinite(C_d) || !std::isfinite(C_v)) return SPEC_EINVAL;
+    AdaptiveKParams a{};
+    for (int c = 0; c < n_cand; ++c) {
+        if (candidates[c] < 1 || candidates[c] > K) return SPEC_EINVAL;
+        if (!(static_cast<double>(candidates[c]) * C_d + C_v > 0.0)) return SPEC_EINVAL;
+        a.cand[c] = candidates[c];
+    }
+    if (B == 0) return SPEC_OK;
+    if (!H_next || !centres || !out_k) return SPEC_EINVAL;
+    a.H = H_next;
+    a.centres = centres;
+    a.B = B;
+    a.K = K;
+    a.n_cand = n_cand;
+    a.Cd = C_d;
+    a.Cv = C_v;
+    a.out_k = out_k;
+    a.out_eff = out_eff;
+    adaptive_k_kernel<<<(B + 127) / 128, 128, 0, static_cast<cudaStream_t>(stream)>>>(a);
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
+}
+
+int spec_row_entropy(const void* logits, int rows, int V, float T, int dtype, float* out_H,
+                     void* stream) {
+    int rc = check_common(logits, reinterpret_cast<const int32_t*>(out_H),
+                          reinterpret_cast<const int32_t*>(out_H), rows, 0, V, dtype);
+    if (rc || rows == 0) return rc;
+    if (!good_temperature(T)) return SPEC_EINVAL;
+    VerifyParams p{};
+    p.target = logits;
+    p.B = rows;
+    p.gamma = 0;
+    p.V = V;
+    p.T = T;
+    p.Td = T;
+    p.out_Hp = out_H;
+    DeviceState* d = nullptr;
+    rc = prepare(rows, 0, V, dtype, nullptr, p, &d);
+    if (rc) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const long long items = static_cast<long long>(rows) * p.npieces;
+    if (dtype == SPEC_F32)
+        pair_stats_kernel<F32Elem, kPairUnroll><<<grid_for(pair_stats_kernel<F32Elem, kPairUnroll>, d->sm_count, items),
+                                                  kThreads, 0, s>>>(p);
+    else
+        pair_stats_kernel<Bf16Elem, kPairUnroll><<<grid_for(pair_stats_kernel<Bf16Elem, kPairUnroll>, d->sm_count, items),
+                                                   kThreads, 0, s>>>(p);
+    position_stats_kernel<<<rows, kThreads, 0, s>>>(p);
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
 }
 
 const char* spec_verify_strerror(int status) {

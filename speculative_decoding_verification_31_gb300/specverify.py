@@ -24,7 +24,8 @@ SPEC_F32, SPEC_BF16 = 0, 1
 
 EXPORTED = ("spec_verify", "spec_verify_greedy", "spec_verify_ex", "spec_verify_greedy_ex",
             "spec_verify_workspace_bytes", "spec_verify_check", "spec_verify_strerror",
-            "spec_verify_opts_init", "spec_verify_noalloc")
+            "spec_verify_opts_init", "spec_verify_noalloc", "spec_row_entropy",
+            "spec_adaptive_k")
 
 
 class SpecVerifyError(RuntimeError):
@@ -51,6 +52,11 @@ class SpecVerifyOpts(ctypes.Structure):
         ("out_race", ctypes.c_void_p),
         ("prof_events", ctypes.c_void_p * 4),
         ("flags", ctypes.c_uint32),
+        ("out_H_p", ctypes.c_void_p),
+        ("out_H_q", ctypes.c_void_p),
+        ("out_KL", ctypes.c_void_p),
+        ("ctrl_centres", ctypes.c_void_p),
+        ("ctrl_beta", ctypes.c_double),
     ]
 
 
@@ -84,6 +90,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.spec_verify_strerror.restype = ctypes.c_char_p
     lib.spec_verify_opts_init.argtypes = [OP]
     lib.spec_verify_opts_init.restype = None
+    lib.spec_row_entropy.argtypes = [P, I, I, F, I, P, P]
+    lib.spec_row_entropy.restype = ctypes.c_int
+    D = ctypes.c_double
+    lib.spec_adaptive_k.argtypes = [P, I, I, P, P, I, D, D, P, P, P]
+    lib.spec_adaptive_k.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -207,11 +218,15 @@ def _check_temps(t, B, dev, name):
 def spec_verify_ex(target_logits, draft_logits, draft_tokens, T: float, T_d: float, seed: int,
                    out_tokens=None, out_n_accepted=None, *, T_per_seq=None, Td_per_seq=None,
                    seq_index_base: int = 0, workspace=None, d_status=None,
-                   diagnostics: bool = False, prof_events=None, flags: int = 0,
+                   diagnostics: bool = False, position_stats=False,
+                   ctrl_centres=None, ctrl_beta: float = 0.0, prof_events=None, flags: int = 0,
                    stream=None):
     """Full form (see ``spec_verify_ex`` in the C header).  Returns
     (out_tokens, out_n_accepted, diag) where diag holds the diagnostic outputs when
-    ``diagnostics`` is set (ln p(d_i), ln q(d_i), ln Z_p, ln Z_q, u, race scores)."""
+    ``diagnostics`` is set (ln p(d_i), ln q(d_i), ln Z_p, ln Z_q, u, race scores) and the
+    per-position statistics when ``position_stats`` is set (H_p, H_q, KL; a dict of those
+    three float32 tensors is written in place of new ones).  ``ctrl_centres``
+    (float64 [B, 2] on the device) is updated in place with rate ``ctrl_beta``."""
     B, g, V = _check_shapes(target_logits, draft_logits, draft_tokens)
     dev = target_logits.device
     out_tokens, out_n_accepted = _outputs(target_logits, B, g, out_tokens, out_n_accepted)
@@ -228,6 +243,26 @@ def spec_verify_ex(target_logits, draft_logits, draft_tokens, T: float, T_d: flo
                 "race": torch.full((B, 2), float("nan"), **f)}
     o = _make_opts(_dtype_code(target_logits), T_per_seq, Td_per_seq, seq_index_base, workspace,
                    d_status, diag, prof_events, flags)
+    if position_stats:
+        diag = dict(diag or {})
+        if isinstance(position_stats, dict):  # caller-allocated outputs
+            for k, shape in (("Hp", (B, g + 1)), ("Hq", (B, g)), ("KL", (B, g))):
+                t = position_stats[k]
+                if tuple(t.shape) != shape or t.dtype != torch.float32 or not t.is_contiguous():
+                    raise ValueError(f"position_stats[{k!r}] must be contiguous float32 {shape}")
+                diag[k] = t
+        else:
+            f = dict(dtype=torch.float32, device=dev)
+            diag.update(Hp=torch.full((B, g + 1), float("nan"), **f),
+                        Hq=torch.full((B, g), float("nan"), **f),
+                        KL=torch.full((B, g), float("nan"), **f))
+        o.out_H_p, o.out_H_q, o.out_KL = (diag[k].data_ptr() for k in ("Hp", "Hq", "KL"))
+    if ctrl_centres is not None:
+        if tuple(ctrl_centres.shape) != (B, 2) or ctrl_centres.dtype != torch.float64 \
+                or ctrl_centres.device != dev or not ctrl_centres.is_contiguous():
+            raise ValueError(f"ctrl_centres must be a contiguous float64 [B, 2] tensor on {dev}")
+        o.ctrl_centres = ctrl_centres.data_ptr()
+        o.ctrl_beta = float(ctrl_beta)
     rc = load_library().spec_verify_ex(
         _ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), B, g, V, float(T),
         float(T_d), int(seed) & (2**64 - 1), _ptr(out_tokens), _ptr(out_n_accepted),
@@ -275,6 +310,45 @@ def spec_verify_noalloc(target_logits, draft_logits, draft_tokens, T: float, T_d
     if rc != SPEC_OK:
         raise SpecVerifyError(rc, "spec_verify_noalloc")
     return out_tokens, out_n_accepted
+
+
+def spec_row_entropy(logits, T: float, out_H=None, stream=None):
+    """Entropy (nats) of softmax(row / T) of every row of a contiguous [rows, V] bf16 or
+    float32 CUDA tensor (see ``spec_row_entropy`` in the C header)."""
+    if logits.dim() != 2 or not logits.is_cuda or not logits.is_contiguous():
+        raise ValueError("logits must be a contiguous CUDA tensor [rows, V]")
+    rows, V = logits.shape
+    if out_H is None:
+        out_H = torch.empty((rows,), dtype=torch.float32, device=logits.device)
+    rc = load_library().spec_row_entropy(_ptr(logits), rows, V, float(T), _dtype_code(logits),
+                                         _ptr(out_H), _stream_handle(stream, logits.device))
+    if rc != SPEC_OK:
+        raise SpecVerifyError(rc, "spec_row_entropy")
+    return out_H
+
+
+def spec_adaptive_k(H_next, centres, candidates: Sequence[int], C_d: float, C_v: float,
+                    out_k=None, out_eff=None, stream=None):
+    """Adaptive draft length per sequence (see ``spec_adaptive_k`` in the C header):
+    H_next float32 [B, K] and centres float64 [B, 2] on the device; returns (k [B] int32,
+    best efficiency [B] float64)."""
+    if H_next.dim() != 2 or H_next.dtype != torch.float32 or not H_next.is_contiguous():
+        raise ValueError("H_next must be a contiguous float32 [B, K] tensor")
+    B, K = H_next.shape
+    dev = H_next.device
+    if tuple(centres.shape) != (B, 2) or centres.dtype != torch.float64 or not centres.is_contiguous():
+        raise ValueError("centres must be a contiguous float64 [B, 2] tensor")
+    cand = (ctypes.c_int32 * len(candidates))(*[int(c) for c in candidates])
+    if out_k is None:
+        out_k = torch.empty((B,), dtype=torch.int32, device=dev)
+    if out_eff is None:
+        out_eff = torch.empty((B,), dtype=torch.float64, device=dev)
+    rc = load_library().spec_adaptive_k(_ptr(H_next), B, K, _ptr(centres), cand, len(candidates),
+                                        float(C_d), float(C_v), _ptr(out_k), _ptr(out_eff),
+                                        _stream_handle(stream, dev))
+    if rc != SPEC_OK:
+        raise SpecVerifyError(rc, "spec_adaptive_k")
+    return out_k, out_eff
 
 
 def spec_verify_workspace_bytes(B: int, gamma: int, V: int, dtype: int = SPEC_BF16) -> int:

@@ -16,7 +16,7 @@ HEADER = os.path.join(ROOT, "include", "specverify.h")
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(spec_verify\w*)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(spec_\w+)\s*\(", text)))
 
 
 @pytest.fixture(scope="module")
@@ -33,7 +33,7 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for f in ("spec_verify", "spec_verify_greedy", "spec_verify_ex", "spec_verify_greedy_ex",
               "spec_verify_workspace_bytes", "spec_verify_check", "spec_verify_strerror",
-              "spec_verify_opts_init"):
+              "spec_verify_opts_init", "spec_verify_noalloc", "spec_row_entropy", "spec_adaptive_k"):
         assert f in names
 
 
@@ -47,7 +47,7 @@ def test_every_declared_symbol_is_exported(lib):
     if nm:
         out = subprocess.run([nm, "-D", "--defined-only", sv.specverify.LIB_PATH],
                              capture_output=True, text=True, check=True).stdout
-        exported = set(re.findall(r"\bT (spec_verify\w*)", out))
+        exported = set(re.findall(r"\bT (spec_\w+)", out))
         assert set(names) <= exported
 
 
@@ -58,18 +58,21 @@ def test_opts_struct_layout_matches_c(lib, tmp_path):
         '#include <stdio.h>\n#include <stddef.h>\n#include "specverify.h"\n'
         "int main(void){printf(\"%zu %zu %zu %zu\\n\", sizeof(spec_verify_opts),"
         " offsetof(spec_verify_opts, workspace_bytes), offsetof(spec_verify_opts, out_race),"
-        " offsetof(spec_verify_opts, prof_events)); printf(\"%zu\\n\", offsetof(spec_verify_opts,"
-        " flags)); return 0;}\n")
+        " offsetof(spec_verify_opts, prof_events)); printf(\"%zu %zu %zu\\n\", offsetof(spec_verify_opts,"
+        " flags), offsetof(spec_verify_opts, out_H_p), offsetof(spec_verify_opts, ctrl_beta));"
+        " return 0;}\n")
     exe = tmp_path / "layout"
     subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
                    check=True)
-    size, ws, race, prof, dbg = map(int, subprocess.run([str(exe)], capture_output=True,
-                                                        text=True, check=True).stdout.split())
+    size, ws, race, prof, dbg, hp, beta = map(int, subprocess.run(
+        [str(exe)], capture_output=True, text=True, check=True).stdout.split())
     assert ctypes.sizeof(SpecVerifyOpts) == size
     assert SpecVerifyOpts.workspace_bytes.offset == ws
     assert SpecVerifyOpts.out_race.offset == race
     assert SpecVerifyOpts.prof_events.offset == prof
     assert SpecVerifyOpts.flags.offset == dbg
+    assert SpecVerifyOpts.out_H_p.offset == hp
+    assert SpecVerifyOpts.ctrl_beta.offset == beta
 
 
 def test_strerror_and_workspace_size(lib):
