@@ -91,6 +91,10 @@ class Oracle:
         lib.oracle_adaptive_k.argtypes = [ctypes.c_int, ctypes.c_int, _P, _P, _P, ctypes.c_int,
                                           ctypes.c_double, ctypes.c_double, _P, _P]
         lib.oracle_adaptive_k.restype = ctypes.c_int
+        lib.oracle_verify_tree.argtypes = [ctypes.c_int, _P, _P, _P, _P, ctypes.c_int,
+                                           ctypes.c_int, ctypes.c_int, _P, _P, ctypes.c_uint64,
+                                           ctypes.c_uint32, _P, _P, _P, _P]
+        lib.oracle_verify_tree.restype = ctypes.c_int
         lib.oracle_verify.argtypes = [ctypes.c_int, _P, _P, _P, ctypes.c_int, ctypes.c_int,
                                       ctypes.c_int, _P, _P, ctypes.c_uint64, ctypes.c_uint32,
                                       _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]
@@ -242,6 +246,34 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle_verify rejected its arguments")
         return r
+
+    def verify_tree(self, target, draft, tokens, parent, T, Td, seed: int, b_base: int = 0):
+        """Token-tree verify.  target [B, N, V], draft [B, M, V] (M internal nodes), tokens
+        [B, N], parent [N].  Returns (tokens [B, D+1], nodes [B, D], n [B], flags [B])."""
+        dtype, t = _logits(target)
+        dtype2, d = _logits(draft)
+        assert dtype == dtype2
+        B, N, V = t.shape
+        par = np.ascontiguousarray(parent, dtype=np.int32)
+        assert par.shape == (N,)
+        depth = np.zeros(N, np.int64)
+        for n in range(1, N):
+            depth[n] = depth[par[n]] + 1
+        D = int(depth.max()) if N > 1 else 0
+        tok = np.ascontiguousarray(tokens, dtype=np.int32).reshape(B, N)
+        Tb = np.ascontiguousarray(np.broadcast_to(np.asarray(T, np.float64), (B,)))
+        Tdb = np.ascontiguousarray(np.broadcast_to(np.asarray(Td, np.float64), (B,)))
+        out_t = np.zeros((B, D + 1), np.int32)
+        out_nodes = np.zeros((B, max(D, 1)), np.int32)
+        out_n = np.zeros(B, np.int32)
+        flags = np.zeros(B, np.int32)
+        rc = self.lib.oracle_verify_tree(dtype, t.ctypes.data, d.ctypes.data, tok.ctypes.data,
+                                         par.ctypes.data, B, N, V, Tb.ctypes.data, Tdb.ctypes.data,
+                                         seed, b_base, out_t.ctypes.data, out_nodes.ctypes.data,
+                                         out_n.ctypes.data, flags.ctypes.data)
+        if rc != 0:
+            raise ValueError("oracle_verify_tree rejected its arguments")
+        return out_t, out_nodes[:, :D], out_n, flags
 
     def verify_greedy(self, target, tokens):
         dtype, t = _logits(target)

@@ -588,3 +588,171 @@ int oracle_adaptive_k(int B, int K, const double *H, const double *centres,
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------------------ */
+/* Static token-tree verification.                                                       */
+/*                                                                                       */
+/* [SUBSPEC] "SubSpec: Speculate Deep and Accurate" (papernotes), on SpecInfer: the draft */
+/* is a token tree whose candidate paths one target forward verifies in parallel; SubSpec */
+/* keeps a static tree, deep and narrow (k = 6, depth 48).  The pages do not give the     */
+/* multi-branch acceptance rule.  Reading taken (SpecInfer's multi-draft speculative      */
+/* sampling, which is lossless when the children of a node are independent draws from    */
+/* that node's draft distribution q_u):                                                  */
+/*   at node u, with target distribution p_u, try its children v (in node order) with    */
+/*   the running residual p' = max(0, p_u - c q_u) / N (c = 0, N = 1 at first):          */
+/*   accept child v, token x, iff u_v < min(1, p'(x) / q_u(x)); on acceptance move to v; */
+/*   on rejection set c <- c + N, N <- sum_x max(0, p_u(x) - c q_u(x)) (the next         */
+/*   residual, norm(max(0, p' - q_u)) written in closed form) and try the next child.    */
+/*   If every child is rejected, draw from p' (the race over max(0, p_u - c q_u)); at a   */
+/*   node without children (an accepted leaf, or a root with none), draw the bonus token  */
+/*   from p_u.  A chain-shaped tree is exactly the chain verify above.                  */
+/* Random numbers: child v's uniform is counter (0, v - 1, b, 0) word 0 (a chain's node  */
+/* v is its draft position v - 1); the race at node u uses counters (x >> 2, u, b, 1).    */
+/* ------------------------------------------------------------------------------------ */
+
+/* Race over max(0, p - c q) (c > 0), or over p (c == 0). */
+static race_result run_race_scaled(int dtype, const void *target, int64_t t_off, double T,
+                                   double logZp, const void *draft, int64_t d_off, double Td,
+                                   double logZq, double c, int V, uint64_t seed, uint32_t bg,
+                                   uint32_t pos) {
+    race_result r = {-1, -INFINITY, -INFINITY};
+    const double logc = c > 0.0 ? log(c) : 0.0;
+    for (int x = 0; x < V; ++x) {
+        const double lp = widen(dtype, target, t_off + x) / T - logZp;
+        double lw;
+        if (c > 0.0) {
+            const double lq = widen(dtype, draft, d_off + x) / Td - logZq + logc; /* log(c q) */
+            if (!(lp > lq)) continue;
+            lw = (lq == -INFINITY) ? lp : lp + log(-expm1(lq - lp));
+        } else {
+            if (lp == -INFINITY) continue;
+            lw = lp;
+        }
+        race_offer(&r, x, lw - log(oracle_race_exponential(seed, bg, pos, (uint32_t)x)));
+    }
+    return r;
+}
+
+/*
+ * target [B, N, V]: p at every node (node 0 the root); draft [B, M, V]: q at every internal
+ * node (draft row m = the node's rank among the nodes with children); tokens [B, N]: the
+ * token of node n >= 1 (column 0 unused); parent [N]: parent[0] = -1, 0 <= parent[n] < n.
+ * Outputs (NULL = skip): out_tokens [B, D+1] (accepted path tokens then the drawn token,
+ * -1 padded; D = the tree's depth), out_nodes [B, D] (accepted nodes, -1 padded), out_n [B]
+ * (accepted count, -1 = bad token), out_flags [B].  Returns 0, or -1 on bad arguments.
+ */
+int oracle_verify_tree(int dtype, const void *target, const void *draft, const int32_t *tokens,
+                       const int32_t *parent, int B, int N, int V, const double *T,
+                       const double *Td, uint64_t seed, uint32_t b_base, int32_t *out_tokens,
+                       int32_t *out_nodes, int32_t *out_n, int32_t *out_flags) {
+    if (B < 0 || N < 1 || V < 1 || (dtype != ORACLE_F32 && dtype != ORACLE_BF16)) return -1;
+    if (parent[0] != -1) return -1;
+    for (int n = 1; n < N; ++n)
+        if (parent[n] < 0 || parent[n] >= n) return -1;
+    int *depth = (int *)calloc((size_t)N, sizeof(int));
+    int *nchild = (int *)calloc((size_t)N, sizeof(int));
+    int *drow = (int *)malloc(sizeof(int) * (size_t)N);
+    if (!depth || !nchild || !drow) { free(depth); free(nchild); free(drow); return -1; }
+    int D = 0, M = 0;
+    for (int n = 1; n < N; ++n) {
+        depth[n] = depth[parent[n]] + 1;
+        if (depth[n] > D) D = depth[n];
+        nchild[parent[n]]++;
+    }
+    for (int n = 0; n < N; ++n) drow[n] = nchild[n] > 0 ? M++ : -1;
+    for (int b = 0; b < B; ++b) {
+        const uint32_t bg = b_base + (uint32_t)b;
+        const double Tb = T[b], Tdb = Td[b];
+        int32_t flags = 0;
+        int32_t *tok = out_tokens ? out_tokens + (int64_t)b * (D + 1) : NULL;
+        int32_t *nodes = out_nodes ? out_nodes + (int64_t)b * D : NULL;
+        if (tok) for (int i = 0; i <= D; ++i) tok[i] = -1;
+        if (nodes) for (int i = 0; i < D; ++i) nodes[i] = -1;
+        int bad = 0;
+        for (int n = 1; n < N; ++n) {
+            const int32_t d = tokens[(int64_t)b * N + n];
+            if (d < 0 || d >= V) bad = 1;
+        }
+        if (bad) {
+            if (out_n) out_n[b] = -1;
+            if (out_flags) out_flags[b] = ORACLE_FLAG_BAD_TOKEN;
+            continue;
+        }
+        int u = 0, k = 0;
+        race_result rr;
+        for (;;) {
+            const int64_t t_off = ((int64_t)b * N + u) * V;
+            const double lzp = row_log_normaliser(dtype, target, t_off, V, Tb);
+            if (nchild[u] == 0) { /* bonus token from p_u */
+                rr = run_race_scaled(dtype, target, t_off, Tb, lzp, NULL, 0, 1.0, 0.0, 0.0, V,
+                                     seed, bg, (uint32_t)u);
+                break;
+            }
+            const int64_t d_off = ((int64_t)b * M + drow[u]) * V;
+            const double lzq = row_log_normaliser(dtype, draft, d_off, V, Tdb);
+            double c = 0.0, Nc = 1.0;
+            int accepted = -1;
+            for (int v = u + 1; v < N; ++v) {
+                if (parent[v] != u) continue;
+                const int32_t x = tokens[(int64_t)b * N + v];
+                const double lp = widen(dtype, target, t_off + x) / Tb - lzp;
+                const double lq = widen(dtype, draft, d_off + x) / Tdb - lzq;
+                /* p'(x) = max(0, p(x) - c q(x)) / N, in the log domain */
+                double lpp;
+                if (c == 0.0) lpp = lp;
+                else {
+                    const double lcq = lq + log(c);
+#if ORACLE_MUTATION == 11 /* planted: the running residual is not renormalised */
+                    lpp = (lp > lcq) ? ((lcq == -INFINITY) ? lp : lp + log(-expm1(lcq - lp)))
+                                     : -INFINITY;
+#else
+                    lpp = (lp > lcq) ? ((lcq == -INFINITY) ? lp : lp + log(-expm1(lcq - lp))) - log(Nc)
+                                     : -INFINITY;
+#endif
+                }
+                double a;
+                if (lpp == -INFINITY) a = 0.0;
+                else if (lq == -INFINITY) a = INFINITY;
+                else a = exp(lpp - lq);
+                const double uv = oracle_accept_uniform(seed, bg, (uint32_t)(v - 1));
+                if (fabs(uv - a) < 1e-5) flags |= ORACLE_FLAG_ACCEPT_NEAR_TIE;
+                if ((float)uv < (float)a) { accepted = v; break; }
+#if ORACLE_MUTATION == 10 /* planted: the residual coefficient stops at 1 */
+                c = 1.0;
+#else
+                c += Nc;
+#endif
+                double s = 0.0;
+                for (int y = 0; y < V; ++y) {
+                    const double p = exp(widen(dtype, target, t_off + y) / Tb - lzp);
+                    const double q = exp(widen(dtype, draft, d_off + y) / Tdb - lzq);
+                    if (p > c * q) s += p - c * q;
+                }
+                Nc = s;
+            }
+            if (accepted >= 0) {
+                if (tok) tok[k] = tokens[(int64_t)b * N + accepted];
+                if (nodes) nodes[k] = accepted;
+                ++k;
+                u = accepted;
+                continue;
+            }
+            rr = run_race_scaled(dtype, target, t_off, Tb, lzp, draft, d_off, Tdb, lzq, c, V,
+                                 seed, bg, (uint32_t)u);
+            if (rr.winner < 0) { /* every residual weight was 0: fall back to p_u */
+                flags |= ORACLE_FLAG_RESIDUAL_EMPTY;
+                rr = run_race_scaled(dtype, target, t_off, Tb, lzp, NULL, 0, 1.0, 0.0, 0.0, V,
+                                     seed, bg, (uint32_t)u);
+            }
+            break;
+        }
+        if (rr.second > -INFINITY && rr.best - rr.second < 1e-6) flags |= ORACLE_FLAG_RACE_NEAR_TIE;
+        if (tok) tok[k] = rr.winner;
+        if (out_n) out_n[b] = k;
+        if (out_flags) out_flags[b] = flags;
+    }
+    free(depth);
+    free(nchild);
+    free(drow);
+    return 0;
+}
