@@ -213,6 +213,40 @@ int spec_verify_noalloc(const void *target_logits, const void *draft_logits,
                         const spec_verify_opts *opts, void *stream);
 
 /*
+ * Static token-tree verify ("SubSpec: Speculate Deep and Accurate" (papernotes): a draft
+ * token tree whose candidate paths one target forward verifies; SubSpec's tree is static,
+ * deep and narrow).  The pages give no multi-branch rule; the one implemented is
+ * multi-draft rejection sampling, lossless when the children of a node are independent
+ * draws from that node's draft distribution: at node u its children are tried in node
+ * order against the running residual p' = max(0, p_u - c q_u) / N (c = 0, N = 1 first;
+ * after a rejection c <- c + N, N <- sum_x max(0, p_u(x) - c q_u(x))): child v with token x
+ * is accepted iff u_v < min(1, p'(x) / q_u(x)), and the walk moves to v.  When every child
+ * is rejected the token is drawn from p' (an exponential race); at a node without children
+ * the bonus token is drawn from p_u.  A chain-shaped tree (parent[n] = n - 1) gives exactly
+ * spec_verify_ex's tokens.
+ * Random numbers: child v's uniform is counter (0, v - 1, b, 0) word 0; the race at node u
+ * uses counters (x >> 2, u, b, 1) (b = seq_index_base + sequence).
+ *   target_logits [B, N, V]: p at every node n (node 0 the root: the distribution after the
+ *                 prefix; node n: after the path to n);
+ *   draft_logits  [B, M, V]: q at every internal node (a node with children), row m = the
+ *                 node's rank among internal nodes in node order (NULL when M = 0);
+ *   draft_tokens  [B, N] int32: the token of node n >= 1 (column 0 unused);
+ *   parent        [N] HOST int32: parent[0] = -1, 0 <= parent[n] < n; N <= 512;
+ *   out_tokens    [B, D+1] int32 (D = the tree's depth): the accepted path's tokens, then
+ *                 the drawn token, -1 padded; out_nodes [B, D] (device, NULL: skipped): the
+ *                 accepted nodes, -1 padded; out_n_accepted [B]: accepted count (-1: a
+ *                 draft token outside [0, V), which also sets SPEC_EBADTOKEN).
+ * opts: dtype, per-sequence temperatures, seq_index_base, workspace, d_status and
+ * prof_events (before the first kernel and after each of the three) are honoured; the
+ * diagnostic and per-position outputs and the flags are not.  SPEC_EINVAL for a bad tree or
+ * sizes, NULL or misaligned pointers, bad temperatures.
+ */
+int spec_verify_tree(const void *target_logits, const void *draft_logits,
+                     const int32_t *draft_tokens, const int32_t *parent, int B, int N, int V,
+                     float T, float T_d, uint64_t seed, int32_t *out_tokens, int32_t *out_nodes,
+                     int32_t *out_n_accepted, const spec_verify_opts *opts, void *stream);
+
+/*
  * Entropy of softmax(L / T) of each of `rows` contiguous rows of V logits (dtype
  * spec_dtype), in nats, into out_H [rows] (device) -- e.g. the next draft tokens' entropies
  * for spec_adaptive_k.  Uses the library's own workspace.  SPEC_EINVAL for bad sizes, a

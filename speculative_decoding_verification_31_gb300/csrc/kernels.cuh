@@ -103,6 +103,9 @@ struct VerifyParams {
     float* out_KL;              // [B, gamma]   KL(p_i || q_i) (nats), or nullptr
     double* ctrl_centres;       // [B, 2] entropy class centres updated in place, or nullptr
     double ctrl_beta;
+    // token-tree verify
+    int32_t* out_nodes;         // [B, depth] accepted nodes, or nullptr
+    struct TreeRace* tree_race; // [B] the node each sequence races
 };
 
 // Row pieces of the streaming passes: between kMinPieceBytes and kMaxPieceBytes of logits
@@ -1267,25 +1270,23 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64g(const void* p) {
     return v;
 }
 
-// The race of sequence b (scan result si, j = si.j >= 0) by one of the `nslots` blocks that
-// share it: race pieces pc_begin, pc_begin + pc_step, ... (< pc_end) of the raced row,
-// publish the block's winner in partial slot `slot`, and if this is the sequence's last
-// block to finish, merge the blocks' winners and write the token.
+// The race of sequence b by one of the `nslots` blocks that share it, over target row rt
+// (and, for a residual, draft row rd; statistics in si) with random-number row `pos`: race
+// pieces pc_begin, pc_begin + pc_step, ... (< pc_end), publish the block's winner in
+// partial slot `slot`, and if this is the sequence's last block to finish, merge the
+// blocks' winners and write the token to *out.
 template <class ET>
-__device__ __forceinline__ void race_sequence_block(const VerifyParams& p, int b, int pc_begin,
-                                                   int pc_end, int pc_step, int slot, int nslots,
-                                                   const SeqInfo& si, float* s_thr,
-                                                   RaceState* s_best, int& s_last) {
+__device__ __forceinline__ void race_rows_block(const VerifyParams& p, int b,
+                                               const typename ET::storage* rt,
+                                               const typename ET::storage* rd, bool residual,
+                                               uint32_t pos, int32_t* out, int pc_begin,
+                                               int pc_end, int pc_step, int slot, int nslots,
+                                               const SeqInfo& si, float* s_thr,
+                                               RaceState* s_best, int& s_last) {
     using S = typename ET::storage;
     constexpr int VPL = kRaceWarpTokens / (32 * ET::kVec);
     const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
-    const int j = si.j;
-    const bool residual = j < p.gamma;
     const uint32_t bg = p.seq_base + static_cast<uint32_t>(b);
-    const S* rt = static_cast<const S*>(p.target) + (static_cast<long long>(b) * (p.gamma + 1) + j) * p.V;
-    const S* rd = residual ? static_cast<const S*>(p.draft) + (static_cast<long long>(b) * p.gamma + j) * p.V
-                           : nullptr;
-    const uint32_t pos = static_cast<uint32_t>(j);
     const RaceRowRng q = race_row_rng(p.rk, bg, pos);
     RaceState st{-INFINITY, INT_MAX, -INFINITY};
     auto word_at = [&](int x) {
@@ -1453,12 +1454,29 @@ __device__ __forceinline__ void race_sequence_block(const VerifyParams& p, int b
         m = race_piece<ET>(rt, nullptr, 0, p.V, si, false, p.rk, bg, pos, lane);
     }
     if (lane == 0) {
-        p.out_tokens[static_cast<long long>(b) * (p.gamma + 1) + j] = m.idx;
+        *out = m.idx;
         if (p.out_race) {
             p.out_race[2 * b] = m.best;
             p.out_race[2 * b + 1] = m.second;
         }
     }
+}
+
+// The chain's race: row j = si.j (the residual of position j < gamma, or the bonus row).
+template <class ET>
+__device__ __forceinline__ void race_sequence_block(const VerifyParams& p, int b, int pc_begin,
+                                                   int pc_end, int pc_step, int slot, int nslots,
+                                                   const SeqInfo& si, float* s_thr,
+                                                   RaceState* s_best, int& s_last) {
+    using S = typename ET::storage;
+    const int j = si.j;
+    const bool residual = j < p.gamma;
+    const S* rt = static_cast<const S*>(p.target) + (static_cast<long long>(b) * (p.gamma + 1) + j) * p.V;
+    const S* rd = residual ? static_cast<const S*>(p.draft) + (static_cast<long long>(b) * p.gamma + j) * p.V
+                           : nullptr;
+    race_rows_block<ET>(p, b, rt, rd, residual, static_cast<uint32_t>(j),
+                        p.out_tokens + static_cast<long long>(b) * (p.gamma + 1) + j, pc_begin,
+                        pc_end, pc_step, slot, nslots, si, s_thr, s_best, s_last);
 }
 
 template <class ET>
@@ -1604,6 +1622,243 @@ __global__ void __launch_bounds__(256, SPECVERIFY_RACE_MINBLOCKS) scan_race_kern
     si.l2sq = residual ? sm_l[p.gamma + 1 + j] : 0.0f;
     si.pad = 0;
     race_sequence_block<ET>(p, b, g, p.rpieces, G, g, G, si, s_thr, s_best, s_last);
+}
+
+// ----------------------------------------------------------------------------------------
+// Static token-tree verification ("SubSpec: Speculate Deep and Accurate" (papernotes): the
+// draft is a token tree whose candidate paths one target forward verifies; SubSpec keeps a
+// static, deep and narrow tree).  The pages give no multi-branch rule; the one taken is
+// multi-draft rejection sampling, lossless when the children of a node are independent
+// draws from the node's draft distribution q_u: at node u try its children in node order
+// against the running residual p' = max(0, p_u - c q_u) / N (c = 0, N = 1 at first):
+// accept child v (token x) iff u_v < min(1, p'(x) / q_u(x)) and move to v; on a rejection
+// set c <- c + N and N <- sum_x max(0, p_u(x) - c q_u(x)).  When every child is rejected the
+// token is drawn from p' -- the race over max(0, p_u - c q_u), which is the chain's residual
+// race with log2 c added to the draft row's log-normaliser -- and at a node without
+// children the bonus token is drawn from p_u.  A chain-shaped tree is the chain verify.
+//
+// tree_stats   row statistics of the target row of every node and the draft row of every
+//              internal node (the streaming pass of the chain, another row mapping);
+// tree_walk    one block per sequence walks the tree from the root, merging the rows of
+//              the nodes it visits; each rejection costs one block-wide pass over the node's
+//              two rows for the next N;
+// tree_race    the race of each sequence's last node, G blocks per sequence.
+// ----------------------------------------------------------------------------------------
+
+constexpr int kMaxTreeNodes = 512;
+
+struct TreeShape {
+    int N, M, D;                          // nodes, internal nodes (draft rows), depth
+    int16_t drow[kMaxTreeNodes];          // draft row of node u (its rank among internal nodes), -1: leaf
+    int16_t first_child[kMaxTreeNodes];   // -1: none
+    int16_t next_sibling[kMaxTreeNodes];  // next child of the same parent in node order, -1: last
+};
+
+struct TreeRace {
+    int node, k, residual, drow;  // node raced (-1: none), output slot, residual?, its draft row
+};
+
+template <class ET, int U>
+__global__ void __launch_bounds__(256, SPECVERIFY_STATS_MINBLOCKS) tree_stats_kernel(VerifyParams p, int N, int M) {
+    using S = typename ET::storage;
+    const int lane = threadIdx.x & 31;
+    const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
+    const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (long long k = tid; k < static_cast<long long>(p.B) * p.rpieces; k += nthreads)
+        reinterpret_cast<uint4*>(p.race_parts)[k] = make_uint4(0u, 0u, 0u, 0u);
+    for (long long k = tid; k < p.B; k += nthreads) p.tickets[k] = 0;
+    const long long nwarps = nthreads >> 5;
+    const int R = N + M;
+    const long long total = static_cast<long long>(p.B) * R * p.npieces;
+    for (long long item = tid >> 5; item < total; item += nwarps) {
+        const int piece = static_cast<int>(item % p.npieces);
+        const long long br = item / p.npieces;
+        const int b = static_cast<int>(br / R), r = static_cast<int>(br % R);
+        const S* row;
+        float c;
+        if (r < N) {
+            row = static_cast<const S*>(p.target) + (static_cast<long long>(b) * N + r) * p.V;
+            c = scale_of(seq_T(p, b));
+        } else {
+            row = static_cast<const S*>(p.draft) + (static_cast<long long>(b) * M + (r - N)) * p.V;
+            c = scale_of(seq_Td(p, b));
+        }
+        const int x0 = piece * p.piece_len;
+        const SoftmaxStat st = stats_piece<ET, U>(row, x0, min(p.V, x0 + p.piece_len), c, lane);
+        if (lane == 0) store_stat(p.stat_parts + br * p.npieces + piece, st.m, st.s);
+    }
+    asm volatile("griddepcontrol.launch_dependents;");
+}
+
+// Block: sum over the row of max(0, p(x) - c q(x)), p(x) = 2^(xt cp - mp - l2sp) and
+// q(x) = 2^(xd cq - mq - l2sq) (fp32; c > 0).
+template <class ET>
+__device__ float residual_mass_block(const typename ET::storage* rt, const typename ET::storage* rd,
+                                     int V, float cp, float mp, float l2sp, float cq, float mq,
+                                     float l2sq, float c, float* s_red) {
+    const float l2c = log2f(c);
+    float acc = 0.0f;
+    auto term = [&](float xt, float xd) {
+        const float p = exp2f(fmaf(xt, cp, -mp) - l2sp);
+        const float cq_ = exp2f(fmaf(xd, cq, -mq) - l2sq + l2c);
+        return p > cq_ ? p - cq_ : 0.0f;
+    };
+    const RowSpan<ET> st(rt, 0, V), sd(rd, 0, V);
+    if (st.head == sd.head) {
+        if (static_cast<int>(threadIdx.x) < st.head)
+            acc += term(ET::load1(rt + threadIdx.x), ET::load1(rd + threadIdx.x));
+        const uint4* vt = st.vec();
+        const uint4* vd = sd.vec();
+        for (int v = threadIdx.x; v < st.nvec; v += blockDim.x) {
+            float ft[ET::kVec], fd[ET::kVec];
+            ET::widen(__ldg(vt + v), ft);
+            ET::widen(__ldg(vd + v), fd);
+#pragma unroll
+            for (int e = 0; e < ET::kVec; ++e) acc += term(ft[e], fd[e]);
+        }
+        const int t0 = st.head + st.nvec * ET::kVec;
+        if (static_cast<int>(threadIdx.x) < st.tail)
+            acc += term(ET::load1(rt + t0 + threadIdx.x), ET::load1(rd + t0 + threadIdx.x));
+    } else {
+        for (int x = threadIdx.x; x < V; x += blockDim.x) acc += term(ET::load1(rt + x), ET::load1(rd + x));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = acc;
+    __syncthreads();
+    float total = 0.0f;
+    for (int k = 0; k < static_cast<int>(blockDim.x >> 5); ++k) total += s_red[k];
+    return total;
+}
+
+template <class ET>
+__global__ void __launch_bounds__(256) tree_walk_kernel(VerifyParams p, TreeShape t) {
+    using S = typename ET::storage;
+    __shared__ float s_m[2], s_l[2], s_red[8];
+    __shared__ int s_bad, s_acc;
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    const int b = blockIdx.x;
+    const int N = t.N, M = t.M, R = N + M;
+    const float cp = scale_of(seq_T(p, b)), cq = scale_of(seq_Td(p, b));
+    const uint32_t bg = p.seq_base + static_cast<uint32_t>(b);
+    const int32_t* tok = p.tokens + static_cast<long long>(b) * N;
+    int32_t* out = p.out_tokens + static_cast<long long>(b) * (t.D + 1);
+    int32_t* nodes = p.out_nodes ? p.out_nodes + static_cast<long long>(b) * t.D : nullptr;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (threadIdx.x == 0) s_bad = 0;
+    for (int i = threadIdx.x; i <= t.D; i += blockDim.x) out[i] = -1;
+    for (int i = threadIdx.x; nodes && i < t.D; i += blockDim.x) nodes[i] = -1;
+    __syncthreads();
+    for (int n = 1 + threadIdx.x; n < N; n += blockDim.x)
+        if (tok[n] < 0 || tok[n] >= p.V) s_bad = 1;
+    __syncthreads();
+    if (s_bad) {
+        if (threadIdx.x == 0) {
+            p.out_n[b] = -1;
+            p.tree_race[b] = TreeRace{-1, 0, 0, -1};
+            set_status(p.status, 3 /* SPEC_EBADTOKEN */);
+        }
+        return;
+    }
+    auto merge_row = [&](int r, int slot) {  // one warp
+        SoftmaxStat st{-FLT_MAX, 0.0f};
+        const float2* parts = p.stat_parts + (static_cast<long long>(b) * R + r) * p.npieces;
+        for (int k = lane; k < p.npieces; k += 32) {
+            const float2 q = parts[k];
+            st = merge_stat(st, SoftmaxStat{q.x, q.y});
+        }
+        st = warp_merge_stat(st);
+        if (lane == 0) {
+            s_m[slot] = st.m;
+            s_l[slot] = log2f(st.s);
+        }
+    };
+    int u = 0, k = 0;
+    for (;;) {
+        const int dr = t.drow[u];
+        if (wib == 0) merge_row(u, 0);
+        if (wib == 1 && dr >= 0) merge_row(N + dr, 1);
+        __syncthreads();
+        const float mp = s_m[0], l2sp = s_l[0];
+        if (dr < 0) {  // no children: the bonus token from p_u
+            if (threadIdx.x == 0) {
+                SeqInfo si{u, mp, l2sp, 0.0f, 0.0f, cp, cq, 0};
+                p.seq[b] = si;
+                p.tree_race[b] = TreeRace{u, k, 0, -1};
+                p.out_n[b] = k;
+            }
+            return;
+        }
+        const float mq = s_m[1], l2sq = s_l[1];
+        const S* rt = static_cast<const S*>(p.target) + (static_cast<long long>(b) * N + u) * p.V;
+        const S* rd = static_cast<const S*>(p.draft) + (static_cast<long long>(b) * M + dr) * p.V;
+        float c = 0.0f, mass = 1.0f;
+        int accepted = -1;
+        for (int v = t.first_child[u]; v >= 0; v = t.next_sibling[v]) {
+            if (threadIdx.x == 0) {
+                const int x = tok[v];
+                const float l2p = fmaf(ET::load1(rt + x), cp, -mp) - l2sp;
+                const float l2q = fmaf(ET::load1(rd + x), cq, -mq) - l2sq;
+                float l2pp = l2p;  // log2 of the running residual p'(x)
+                if (c > 0.0f) {
+                    const float l2cq = l2q + log2f(c);
+                    l2pp = (l2p > l2cq) ? l2p + log1pf(-exp2f(l2cq - l2p)) * kLog2e - log2f(mass)
+                                        : -INFINITY;
+                }
+                const float uv = accept_uniform(p.key, bg, static_cast<uint32_t>(v - 1));
+                // accept iff u < min(1, p'(x)/q(x)); p'(x) = 0 rejects, q(x) = 0 < p'(x) accepts
+                s_acc = (l2pp > -INFINITY) && (uv < exp2f(l2pp - l2q));
+            }
+            __syncthreads();
+            const int acc = s_acc;
+            __syncthreads();
+            if (acc) {
+                accepted = v;
+                break;
+            }
+            c += mass;
+            mass = residual_mass_block<ET>(rt, rd, p.V, cp, mp, l2sp, cq, mq, l2sq, c, s_red);
+        }
+        if (accepted >= 0) {
+            if (threadIdx.x == 0) {
+                out[k] = tok[accepted];
+                if (nodes) nodes[k] = accepted;
+            }
+            ++k;
+            u = accepted;
+            __syncthreads();
+            continue;
+        }
+        // every child rejected: the race over max(0, p_u - c q_u)
+        if (threadIdx.x == 0) {
+            SeqInfo si{u, mp, l2sp, mq, l2sq - log2f(c), cp, cq, 0};
+            p.seq[b] = si;
+            p.tree_race[b] = TreeRace{u, k, 1, dr};
+            p.out_n[b] = k;
+        }
+        return;
+    }
+}
+
+template <class ET>
+__global__ void __launch_bounds__(256, SPECVERIFY_RACE_MINBLOCKS) tree_race_kernel(VerifyParams p, int N, int M, int D) {
+    using S = typename ET::storage;
+    __shared__ float s_thr[8];
+    __shared__ RaceState s_best[8];
+    __shared__ int s_last;
+    const int G = p.rgroups;
+    const int b = blockIdx.x / G, g = blockIdx.x % G;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const TreeRace tr = p.tree_race[b];
+    if (tr.node < 0) return;
+    const SeqInfo si = p.seq[b];
+    const S* rt = static_cast<const S*>(p.target) + (static_cast<long long>(b) * N + tr.node) * p.V;
+    const S* rd = tr.residual ? static_cast<const S*>(p.draft) + (static_cast<long long>(b) * M + tr.drow) * p.V
+                              : nullptr;
+    race_rows_block<ET>(p, b, rt, rd, tr.residual != 0, static_cast<uint32_t>(tr.node),
+                        p.out_tokens + static_cast<long long>(b) * (D + 1) + tr.k, g, p.rpieces,
+                        G, g, G, si, s_thr, s_best, s_last);
 }
 
 // ----------------------------------------------------------------------------------------

@@ -426,6 +426,55 @@ int launch_early(VerifyParams& p, int sm_count, const spec_verify_opts* o, cudaS
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
 }
 
+// Token-tree verify: the streaming pass, the walk (one block per sequence, a programmatic
+// dependent), then the race (G blocks per sequence, another dependent).
+template <class ET>
+int launch_tree(VerifyParams& p, const TreeShape& t, int sm_count, const spec_verify_opts* o,
+                cudaStream_t s) {
+    const bool pdl = !(o && o->prof_events[1]);
+    record(o, 0, s);
+    const long long items = static_cast<long long>(p.B) * (t.N + t.M) * p.npieces;
+    auto stats = tree_stats_kernel<ET, kUnroll>;
+    stats<<<grid_for(stats, sm_count, items), kThreads, 0, s>>>(p, t.N, t.M);
+    record(o, 1, s);
+    {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(p.B));
+        cfg.blockDim = dim3(kThreads);
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, tree_walk_kernel<ET>, p, t) != cudaSuccess) return SPEC_ECUDA;
+    }
+    record(o, 2, s);
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tree_race_kernel<ET>, kThreads, 0) != cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    long long G = static_cast<long long>(sm_count) * per_sm / p.B;
+    if (G > p.rpieces) G = p.rpieces;
+    if (G < 1) G = 1;
+    p.rgroups = static_cast<int>(G);
+    {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(p.B * G));
+        cfg.blockDim = dim3(kThreads);
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, tree_race_kernel<ET>, p, t.N, t.M, t.D) != cudaSuccess)
+            return SPEC_ECUDA;
+    }
+    record(o, 3, s);
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
+}
+
 template <class ET>
 int launch_greedy(VerifyParams& p, int sm_count, const spec_verify_opts* o, cudaStream_t s) {
     const int R = p.gamma + 1;
@@ -566,6 +615,71 @@ int spec_verify_check(void* stream, int32_t* d_status) {
     if (cudaMemsetAsync(st, 0, sizeof(int32_t), s) != cudaSuccess) return SPEC_ECUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return SPEC_ECUDA;
     return h;
+}
+
+int spec_verify_tree(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
+                     const int32_t* parent, int B, int N, int V, float T, float T_d, uint64_t seed,
+                     int32_t* out_tokens, int32_t* out_nodes, int32_t* out_n_accepted,
+                     const spec_verify_opts* opts, void* stream) {
+    const int dtype = opts ? opts->dtype : SPEC_BF16;
+    if (N < 1 || N > kMaxTreeNodes || !parent) return SPEC_EINVAL;
+    if (parent[0] != -1) return SPEC_EINVAL;
+    TreeShape t{};
+    t.N = N;
+    int depth[kMaxTreeNodes] = {0};
+    int nchild[kMaxTreeNodes] = {0};
+    int last_child[kMaxTreeNodes];
+    for (int n = 0; n < N; ++n) {
+        t.first_child[n] = -1;
+        t.next_sibling[n] = -1;
+        last_child[n] = -1;
+    }
+    for (int n = 1; n < N; ++n) {
+        const int u = parent[n];
+        if (u < 0 || u >= n) return SPEC_EINVAL;
+        depth[n] = depth[u] + 1;
+        t.D = std::max(t.D, depth[n]);
+        if (last_child[u] < 0) t.first_child[u] = static_cast<int16_t>(n);
+        else t.next_sibling[last_child[u]] = static_cast<int16_t>(n);
+        last_child[u] = n;
+        ++nchild[u];
+    }
+    for (int n = 0; n < N; ++n) t.drow[n] = static_cast<int16_t>(nchild[n] > 0 ? t.M++ : -1);
+    const int R = N + t.M;
+    const int gamma_eq = R / 2;  // the workspace holds 2 * gamma_eq + 1 >= R rows per sequence
+    int rc = check_common(target_logits, out_tokens, out_n_accepted, B, gamma_eq, V, dtype);
+    if (rc || B == 0) return rc;
+    if (static_cast<long long>(B) * N * static_cast<long long>(V) >= (1LL << 40)) return SPEC_EINVAL;
+    if (t.M > 0 && (!draft_logits || !aligned16(draft_logits))) return SPEC_EINVAL;
+    if (N > 1 && !draft_tokens) return SPEC_EINVAL;
+    if (!(opts && opts->T_per_seq) && !good_temperature(T)) return SPEC_EINVAL;
+    if (!(opts && opts->Td_per_seq) && !good_temperature(T_d)) return SPEC_EINVAL;
+    VerifyParams p{};
+    p.target = target_logits;
+    p.draft = draft_logits;
+    p.tokens = draft_tokens;
+    p.B = B;
+    p.gamma = gamma_eq;
+    p.V = V;
+    p.T = T;
+    p.Td = T_d;
+    p.T_seq = opts ? opts->T_per_seq : nullptr;
+    p.Td_seq = opts ? opts->Td_per_seq : nullptr;
+    p.key = philox_key(seed);
+    p.rk = philox_round_keys(p.key);
+    p.seq_base = opts ? opts->seq_index_base : 0u;
+    p.out_tokens = out_tokens;
+    p.out_n = out_n_accepted;
+    p.out_nodes = out_nodes;
+    DeviceState* d = nullptr;
+    rc = prepare(B, gamma_eq, V, dtype, opts, p, &d);
+    if (rc) return rc;
+    // the per-sequence race records live in the fused path's merged-row area (B * R float2
+    // >= B TreeRace), which the tree path does not otherwise use
+    p.tree_race = reinterpret_cast<TreeRace*>(p.row_stat);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return dtype == SPEC_F32 ? launch_tree<F32Elem>(p, t, d->sm_count, opts, s)
+                             : launch_tree<Bf16Elem>(p, t, d->sm_count, opts, s);
 }
 
 int spec_adaptive_k(const float* H_next, int B, int K, const double* centres,

@@ -252,3 +252,108 @@ def generic(B: int, gamma: int, V: int, dtype: str = "bf16", seed: int = 0, scal
     }
     return make_workload(f"generic-{B}x{gamma}x{V}-{dtype}-{kind}", B, gamma, V, dtype, seed,
                          fns[kind], sigma, T, Td=Td, greedy=greedy)
+
+
+# ---------------------------------------------------------------------------------------
+# token trees
+# ---------------------------------------------------------------------------------------
+
+@dataclass
+class TreeWorkload:
+    """A static draft token tree per sequence.  parent[n] < n (parent[0] = -1); target row
+    n is p at node n; draft row m is q at the m-th internal node (in node order); node n's
+    token (n >= 1) is drawn from q at its parent; siblings are independent draws."""
+    name: str
+    B: int
+    V: int
+    dtype: str
+    parent: np.ndarray         # [N] int32
+    target: np.ndarray         # [B, N, V]
+    draft: np.ndarray          # [B, M, V]
+    tokens: np.ndarray         # [B, N] int32 (column 0 unused: 0)
+    T: np.ndarray              # [B] float32
+    Td: np.ndarray             # [B] float32
+    info: dict = field(default_factory=dict)
+
+    @property
+    def N(self) -> int:
+        return len(self.parent)
+
+    @property
+    def internal(self) -> np.ndarray:
+        has = np.zeros(self.N, bool)
+        has[self.parent[1:]] = True
+        return np.nonzero(has)[0]
+
+    @property
+    def depth(self) -> int:
+        d = np.zeros(self.N, np.int64)
+        for n in range(1, self.N):
+            d[n] = d[self.parent[n]] + 1
+        return int(d.max()) if self.N > 1 else 0
+
+    def rows(self) -> int:
+        """Logit rows per call: every node's target row and every internal node's draft row."""
+        return self.B * (self.N + len(self.internal))
+
+    def bytes(self) -> int:
+        return (2 if self.dtype == "bf16" else 4) * self.V * self.rows()
+
+    def subset(self, idx: Sequence[int]) -> "TreeWorkload":
+        idx = np.asarray(idx)
+        return TreeWorkload(self.name, len(idx), self.V, self.dtype, self.parent, self.target[idx],
+                            self.draft[idx], self.tokens[idx], self.T[idx], self.Td[idx], self.info)
+
+
+def deep_narrow_tree(depth: int, k: int) -> np.ndarray:
+    """SubSpec-style static tree, deep and narrow: a main path of `depth` draft levels whose
+    nodes each have k children, the first continuing the path and the others leaves."""
+    parent = [-1]
+    main = 0
+    for _ in range(depth):
+        first = len(parent)
+        parent.extend([main] * k)
+        main = first
+    return np.asarray(parent, np.int32)
+
+
+def random_tree(rng: np.random.Generator, N: int, max_children: int = 4) -> np.ndarray:
+    """A random tree of N nodes in node order (each node's parent is an earlier node with
+    fewer than max_children children)."""
+    parent = [-1]
+    nchild = [0]
+    for n in range(1, N):
+        cand = [u for u in range(n) if nchild[u] < max_children]
+        u = int(rng.choice(cand))
+        parent.append(u)
+        nchild[u] += 1
+        nchild.append(0)
+    return np.asarray(parent, np.int32)
+
+
+def tree(parent, B: int, V: int, dtype: str = "bf16", seed: int = 0, scale: float = 5.0,
+         sigma: float = 1.0, T: float = 0.6, Td: float = 0.2, name: str = "tree") -> TreeWorkload:
+    """Per sequence: Zipf-shaped target rows (one per node), draft rows = target + N(0, sigma^2)
+    at internal nodes, children drawn from q at their parent (independently)."""
+    parent = np.asarray(parent, np.int32)
+    N = len(parent)
+    has = np.zeros(N, bool)
+    has[parent[1:]] = True
+    internal = np.nonzero(has)[0]
+    drow = -np.ones(N, np.int64)
+    drow[internal] = np.arange(len(internal))
+    rngs = [np.random.default_rng(s) for s in np.random.SeedSequence(seed).spawn(B)]
+    tgt, drf, tok = [], [], np.zeros((B, N), np.int32)
+    for b, rng in enumerate(rngs):
+        t32 = zipf_shaped_rows(rng, N, V, scale)
+        d32 = t32[internal] + rng.standard_normal((len(internal), V), dtype=np.float32) * np.float32(sigma)
+        t_enc, d_enc = _encode(t32, dtype), _encode(d32, dtype)
+        d_used = as_f32(d_enc, dtype)
+        for n in range(1, N):
+            tok[b, n] = draw_drafts(rng, d_used[drow[parent[n]]][None, :], Td)[0]
+        tgt.append(t_enc)
+        drf.append(d_enc)
+    shape_d = (B, len(internal), V)
+    draft = np.stack(drf) if len(internal) else np.zeros(shape_d, tgt[0].dtype)
+    return TreeWorkload(name, B, V, dtype, parent, np.stack(tgt), draft, tok,
+                        np.full(B, T, np.float32), np.full(B, Td, np.float32))
