@@ -525,6 +525,40 @@ def run_table(args):
                     st = sv.spec_verify_check()
                     rows_out.append((cfg, label, "warm" if warm else ("cold" if copies > 1 else "> L2"),
                                      us, w.rows / us * 1e6, nbytes / us / 1e3, st))
+    # static token trees (SubSpec's shape: depth 48, six children per main-path node)
+    for B in (1, 8):
+        tw = workloads.tree(workloads.deep_narrow_tree(48, 6), B=B, V=152064, dtype="bf16",
+                            seed=1005, scale=5.0, sigma=workloads.DEEP_CHAIN_SIGMA, T=0.6, Td=0.2,
+                            name=f"tree depth 48 x 6, B={B}")
+        nbytes = tw.bytes()
+        copies = 1 if nbytes > 2 * l2 else min(64, -(-2 * l2 // nbytes) + 1)
+        bufs = [(to_torch(tw.target, tw.dtype).to(dev), to_torch(tw.draft, tw.dtype).to(dev))
+                for _ in range(copies)]
+        ttok = torch.from_numpy(tw.tokens).to(dev)
+        tree = sv.Tree(tw.parent)
+        t_out = torch.empty((B, tree.D + 1), dtype=torch.int32, device=dev)
+        t_nodes = torch.empty((B, tree.D), dtype=torch.int32, device=dev)
+        t_n = torch.empty((B,), dtype=torch.int32, device=dev)
+        for warm in ([False, True] if copies > 1 else [False]):
+            def tcall(k):
+                t, d = bufs[0 if warm else k % copies]
+                return sv.spec_verify_tree(t, d, ttok, tree, 0.6, 0.2, 0, out_tokens=t_out,
+                                           out_nodes=t_nodes, out_n_accepted=t_n)
+            for k in range(5):
+                tcall(k)
+            torch.cuda.synchronize()
+            n = 200
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0.record()
+            for k in range(n):
+                _, _, nacc = tcall(k)
+            s1.record()
+            torch.cuda.synchronize()
+            us = s0.elapsed_time(s1) / n * 1e3
+            emitted = float(nacc.float().mean().item()) + 1.0
+            rows_out.append((tw.name, f"tree (emits {emitted:.1f} tokens/seq)",
+                             "warm" if warm else ("cold" if copies > 1 else "> L2"), us,
+                             tw.rows() / us * 1e6, nbytes / us / 1e3, sv.spec_verify_check()))
     print("| workload | path | L2 | us/call | rows/s | GB/s (one read of the logits) | status |",
           file=sys.stderr)
     print("|---|---|---|---|---|---|---|", file=sys.stderr)

@@ -20,6 +20,8 @@
 #include <climits>
 #include <cstdint>
 
+#include <cooperative_groups.h>
+
 #include "device_common.cuh"
 #include "philox.cuh"
 
@@ -1690,26 +1692,36 @@ __global__ void __launch_bounds__(256, SPECVERIFY_STATS_MINBLOCKS) tree_stats_ke
     asm volatile("griddepcontrol.launch_dependents;");
 }
 
-// Block: sum over the row of max(0, p(x) - c q(x)), p(x) = 2^(xt cp - mp - l2sp) and
-// q(x) = 2^(xd cq - mq - l2sq) (fp32; c > 0).
+constexpr int kTreeCluster = 8;  // CTAs per sequence in tree_walk (a portable cluster size)
+
+// Cluster: sum over the row of max(0, p(x) - c q(x)), p(x) = 2^(xt cp - mp - l2sp) and
+// q(x) = 2^(xd cq - mq - l2sq) (fp32; c > 0).  CTA r of the cluster sums elements
+// r, r + kTreeCluster, ... (in 16-byte vectors when the two rows are aligned alike), the
+// CTAs publish their sums in shared memory, and after a cluster barrier every CTA adds the
+// kTreeCluster sums in rank order -- so every CTA gets the same value.
 template <class ET>
-__device__ float residual_mass_block(const typename ET::storage* rt, const typename ET::storage* rd,
-                                     int V, float cp, float mp, float l2sp, float cq, float mq,
-                                     float l2sq, float c, float* s_red) {
+__device__ float residual_mass_cluster(const typename ET::storage* rt, const typename ET::storage* rd,
+                                       int V, float cp, float mp, float l2sp, float cq, float mq,
+                                       float l2sq, float c, float* s_red, float* s_part) {
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = static_cast<int>(cluster.block_rank());
     const float l2c = log2f(c);
+    const float op = -mp - l2sp, oq = -mq - l2sq + l2c;
     float acc = 0.0f;
     auto term = [&](float xt, float xd) {
-        const float p = exp2f(fmaf(xt, cp, -mp) - l2sp);
-        const float cq_ = exp2f(fmaf(xd, cq, -mq) - l2sq + l2c);
-        return p > cq_ ? p - cq_ : 0.0f;
+        const float p = ex2_fast(fmaf(xt, cp, op));
+        const float cq_ = ex2_fast(fmaf(xd, cq, oq));
+        return fmaxf(p - cq_, 0.0f);
     };
     const RowSpan<ET> st(rt, 0, V), sd(rd, 0, V);
+    const int stride = blockDim.x * kTreeCluster;
+    const int t = rank * blockDim.x + threadIdx.x;
     if (st.head == sd.head) {
-        if (static_cast<int>(threadIdx.x) < st.head)
-            acc += term(ET::load1(rt + threadIdx.x), ET::load1(rd + threadIdx.x));
+        if (t < st.head) acc += term(ET::load1(rt + t), ET::load1(rd + t));
         const uint4* vt = st.vec();
         const uint4* vd = sd.vec();
-        for (int v = threadIdx.x; v < st.nvec; v += blockDim.x) {
+        for (int v = t; v < st.nvec; v += stride) {
             float ft[ET::kVec], fd[ET::kVec];
             ET::widen(__ldg(vt + v), ft);
             ET::widen(__ldg(vd + v), fd);
@@ -1717,28 +1729,40 @@ __device__ float residual_mass_block(const typename ET::storage* rt, const typen
             for (int e = 0; e < ET::kVec; ++e) acc += term(ft[e], fd[e]);
         }
         const int t0 = st.head + st.nvec * ET::kVec;
-        if (static_cast<int>(threadIdx.x) < st.tail)
-            acc += term(ET::load1(rt + t0 + threadIdx.x), ET::load1(rd + t0 + threadIdx.x));
+        if (t < st.tail) acc += term(ET::load1(rt + t0 + t), ET::load1(rd + t0 + t));
     } else {
-        for (int x = threadIdx.x; x < V; x += blockDim.x) acc += term(ET::load1(rt + x), ET::load1(rd + x));
+        for (int x = t; x < V; x += stride) acc += term(ET::load1(rt + x), ET::load1(rd + x));
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     __syncthreads();
     if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = acc;
     __syncthreads();
+    if (threadIdx.x == 0) {
+        float sum = 0.0f;
+        for (int k = 0; k < static_cast<int>(blockDim.x >> 5); ++k) sum += s_red[k];
+        *s_part = sum;
+    }
+    cluster.sync();  // every CTA's sum is published
     float total = 0.0f;
-    for (int k = 0; k < static_cast<int>(blockDim.x >> 5); ++k) total += s_red[k];
+    for (int r = 0; r < kTreeCluster; ++r) total += *cluster.map_shared_rank(s_part, r);
+    cluster.sync();  // nobody overwrites a sum before every CTA has read it
     return total;
 }
 
+// One cluster of kTreeCluster CTAs per sequence: every CTA walks the tree with the same
+// values (so they take the same decisions), and they share each residual pass; CTA 0
+// writes the results.
 template <class ET>
-__global__ void __launch_bounds__(256) tree_walk_kernel(VerifyParams p, TreeShape t) {
+__global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(256)
+tree_walk_kernel(VerifyParams p, TreeShape t) {
     using S = typename ET::storage;
-    __shared__ float s_m[2], s_l[2], s_red[8];
+    namespace cg = cooperative_groups;
+    __shared__ float s_m[2], s_l[2], s_red[8], s_part;
     __shared__ int s_bad, s_acc;
     const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
-    const int b = blockIdx.x;
+    const int b = blockIdx.x / kTreeCluster;
+    const bool leader = cg::this_cluster().block_rank() == 0;
     const int N = t.N, M = t.M, R = N + M;
     const float cp = scale_of(seq_T(p, b)), cq = scale_of(seq_Td(p, b));
     const uint32_t bg = p.seq_base + static_cast<uint32_t>(b);
@@ -1747,14 +1771,16 @@ __global__ void __launch_bounds__(256) tree_walk_kernel(VerifyParams p, TreeShap
     int32_t* nodes = p.out_nodes ? p.out_nodes + static_cast<long long>(b) * t.D : nullptr;
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (threadIdx.x == 0) s_bad = 0;
-    for (int i = threadIdx.x; i <= t.D; i += blockDim.x) out[i] = -1;
-    for (int i = threadIdx.x; nodes && i < t.D; i += blockDim.x) nodes[i] = -1;
+    if (leader) {
+        for (int i = threadIdx.x; i <= t.D; i += blockDim.x) out[i] = -1;
+        for (int i = threadIdx.x; nodes && i < t.D; i += blockDim.x) nodes[i] = -1;
+    }
     __syncthreads();
     for (int n = 1 + threadIdx.x; n < N; n += blockDim.x)
         if (tok[n] < 0 || tok[n] >= p.V) s_bad = 1;
     __syncthreads();
     if (s_bad) {
-        if (threadIdx.x == 0) {
+        if (leader && threadIdx.x == 0) {
             p.out_n[b] = -1;
             p.tree_race[b] = TreeRace{-1, 0, 0, -1};
             set_status(p.status, 3 /* SPEC_EBADTOKEN */);
@@ -1782,7 +1808,7 @@ __global__ void __launch_bounds__(256) tree_walk_kernel(VerifyParams p, TreeShap
         __syncthreads();
         const float mp = s_m[0], l2sp = s_l[0];
         if (dr < 0) {  // no children: the bonus token from p_u
-            if (threadIdx.x == 0) {
+            if (leader && threadIdx.x == 0) {
                 SeqInfo si{u, mp, l2sp, 0.0f, 0.0f, cp, cq, 0};
                 p.seq[b] = si;
                 p.tree_race[b] = TreeRace{u, k, 0, -1};
@@ -1818,10 +1844,10 @@ __global__ void __launch_bounds__(256) tree_walk_kernel(VerifyParams p, TreeShap
                 break;
             }
             c += mass;
-            mass = residual_mass_block<ET>(rt, rd, p.V, cp, mp, l2sp, cq, mq, l2sq, c, s_red);
+            mass = residual_mass_cluster<ET>(rt, rd, p.V, cp, mp, l2sp, cq, mq, l2sq, c, s_red, &s_part);
         }
         if (accepted >= 0) {
-            if (threadIdx.x == 0) {
+            if (leader && threadIdx.x == 0) {
                 out[k] = tok[accepted];
                 if (nodes) nodes[k] = accepted;
             }
@@ -1831,7 +1857,7 @@ __global__ void __launch_bounds__(256) tree_walk_kernel(VerifyParams p, TreeShap
             continue;
         }
         // every child rejected: the race over max(0, p_u - c q_u)
-        if (threadIdx.x == 0) {
+        if (leader && threadIdx.x == 0) {
             SeqInfo si{u, mp, l2sp, mq, l2sq - log2f(c), cp, cq, 0};
             p.seq[b] = si;
             p.tree_race[b] = TreeRace{u, k, 1, dr};

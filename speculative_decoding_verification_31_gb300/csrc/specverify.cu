@@ -426,7 +426,7 @@ int launch_early(VerifyParams& p, int sm_count, const spec_verify_opts* o, cudaS
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
 }
 
-// Token-tree verify: the streaming pass, the walk (one block per sequence, a programmatic
+// Token-tree verify: the streaming pass, the walk (one cluster per sequence, a programmatic
 // dependent), then the race (G blocks per sequence, another dependent).
 template <class ET>
 int launch_tree(VerifyParams& p, const TreeShape& t, int sm_count, const spec_verify_opts* o,
@@ -439,7 +439,7 @@ int launch_tree(VerifyParams& p, const TreeShape& t, int sm_count, const spec_ve
     record(o, 1, s);
     {
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(static_cast<unsigned>(p.B));
+        cfg.gridDim = dim3(static_cast<unsigned>(p.B) * kTreeCluster);  // one cluster per sequence
         cfg.blockDim = dim3(kThreads);
         cfg.stream = s;
         cudaLaunchAttribute attr[1];

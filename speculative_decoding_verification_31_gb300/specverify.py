@@ -314,51 +314,64 @@ def spec_verify_noalloc(target_logits, draft_logits, draft_tokens, T: float, T_d
     return out_tokens, out_n_accepted
 
 
-def tree_depth(parent: Sequence[int]) -> int:
-    depth = [0] * len(parent)
-    for n in range(1, len(parent)):
-        depth[n] = depth[parent[n]] + 1
-    return max(depth) if depth else 0
+class Tree:
+    """A static token tree prepared once for spec_verify_tree: the parent array as the C
+    call takes it, and its node, internal-node and depth counts."""
+
+    def __init__(self, parent: Sequence[int]):
+        par = [int(x) for x in parent]
+        self.N = len(par)
+        self.valid = self.N >= 1 and par[0] == -1 and all(0 <= par[n] < n for n in range(1, self.N))
+        self.M = len({par[v] for v in range(1, self.N)}) if self.valid else 0
+        depth = [0] * self.N
+        if self.valid:
+            for n in range(1, self.N):
+                depth[n] = depth[par[n]] + 1
+        self.D = max(depth) if depth else 0
+        self.c_parent = (ctypes.c_int32 * self.N)(*par)
 
 
-def spec_verify_tree(target_logits, draft_logits, draft_tokens, parent: Sequence[int], T: float,
-                     T_d: float, seed: int, *, T_per_seq=None, Td_per_seq=None,
-                     seq_index_base: int = 0, workspace=None, d_status=None, prof_events=None,
-                     stream=None):
+def spec_verify_tree(target_logits, draft_logits, draft_tokens, tree, T: float, T_d: float,
+                     seed: int, *, out_tokens=None, out_nodes=None, out_n_accepted=None,
+                     T_per_seq=None, Td_per_seq=None, seq_index_base: int = 0, workspace=None,
+                     d_status=None, prof_events=None, stream=None):
     """Token-tree verify (see ``spec_verify_tree`` in the C header).  target [B, N, V],
-    draft [B, M, V] (M internal nodes), draft_tokens int32 [B, N], parent: N host ints.
-    Returns (out_tokens [B, D+1], out_nodes [B, D], out_n_accepted [B]) on the device."""
+    draft [B, M, V] (M internal nodes), draft_tokens int32 [B, N]; ``tree``: a Tree or the
+    N parent indices.  Returns (out_tokens [B, D+1], out_nodes [B, D], out_n_accepted [B])
+    on the device (new tensors unless given).  An invalid tree is passed through: the
+    library answers SPEC_EINVAL."""
+    if not isinstance(tree, Tree):
+        tree = Tree(tree)
     if target_logits.dim() != 3 or not target_logits.is_cuda or not target_logits.is_contiguous():
         raise ValueError("target_logits must be a contiguous CUDA tensor [B, N, V]")
     B, N, V = target_logits.shape
-    par = (ctypes.c_int32 * len(parent))(*[int(x) for x in parent])
-    if len(parent) != N:
-        raise ValueError(f"parent must have N = {N} entries")
-    # (an invalid tree is passed through: the library answers SPEC_EINVAL)
-    valid = N >= 1 and int(parent[0]) == -1 and all(0 <= int(parent[n]) < n for n in range(1, N))
-    M = len({int(parent[v]) for v in range(1, N)}) if valid else 0
+    if tree.N != N:
+        raise ValueError(f"the tree must have N = {N} nodes")
+    M, D = tree.M, tree.D
     if M and (draft_logits is None or tuple(draft_logits.shape) != (B, M, V)
               or draft_logits.dtype != target_logits.dtype or not draft_logits.is_contiguous()):
         raise ValueError(f"draft_logits must be contiguous [B, M, V] = {(B, M, V)}")
     if tuple(draft_tokens.shape) != (B, N) or draft_tokens.dtype != torch.int32:
         raise ValueError(f"draft_tokens must be int32 [B, N] = {(B, N)}")
     dev = target_logits.device
-    D = tree_depth([int(x) for x in parent]) if valid else 0
-    out_t = torch.empty((B, D + 1), dtype=torch.int32, device=dev)
-    out_nodes = torch.empty((B, max(D, 1)), dtype=torch.int32, device=dev)
-    out_n = torch.empty((B,), dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, D + 1), dtype=torch.int32, device=dev)
+    if out_nodes is None:
+        out_nodes = torch.empty((B, max(D, 1)), dtype=torch.int32, device=dev)
+    if out_n_accepted is None:
+        out_n_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
     T_per_seq = _check_temps(T_per_seq, B, dev, "T_per_seq")
     Td_per_seq = _check_temps(Td_per_seq, B, dev, "Td_per_seq")
     o = _make_opts(_dtype_code(target_logits), T_per_seq, Td_per_seq, seq_index_base, workspace,
                    d_status, None, prof_events)
     rc = load_library().spec_verify_tree(
-        _ptr(target_logits), _ptr(draft_logits) if (M or not valid) else None, _ptr(draft_tokens),
-        par, B, N, V,
-        float(T), float(T_d), int(seed) & (2**64 - 1), _ptr(out_t), _ptr(out_nodes), _ptr(out_n),
-        ctypes.byref(o), _stream_handle(stream, dev))
+        _ptr(target_logits), _ptr(draft_logits) if (M or not tree.valid) else None,
+        _ptr(draft_tokens), tree.c_parent, B, N, V, float(T), float(T_d), int(seed) & (2**64 - 1),
+        _ptr(out_tokens), _ptr(out_nodes), _ptr(out_n_accepted), ctypes.byref(o),
+        _stream_handle(stream, dev))
     if rc != SPEC_OK:
         raise SpecVerifyError(rc, "spec_verify_tree")
-    return out_t, out_nodes[:, :D], out_n
+    return out_tokens, out_nodes[:, :D], out_n_accepted
 
 
 def spec_row_entropy(logits, T: float, out_H=None, stream=None):
