@@ -337,17 +337,41 @@ def run_ours(args):
                  "steps": Ks, "GBps_one_read": alg_bytes / (sms / 1e3) / 1e9,
                  "note": "same call with H(p_i), H(q_i), KL(p_i||q_i) for every position"}
 
-    # end to end: inputs from pinned host memory, outputs read back, every step
-    e2e = None
+    # End to end through the C ABI with HOST buffers (spec_verify_host): logits, draft tokens
+    # and temperatures in pinned host memory, outputs written to pinned host memory; the
+    # kernels read over the host link only the rows they need (early exit).  Beside it, for
+    # context, the copy path: copy every input to the device, full-read verify, copy back.
+    e2e = e2e_copy = None
     if not args.no_e2e:
         h_t = to_torch(w.target, w.dtype).pin_memory()
         h_d = to_torch(w.draft, w.dtype).pin_memory()
         h_tok = torch.from_numpy(w.tokens).pin_memory()
+        h_T = torch.from_numpy(w.T).pin_memory()
+        h_Td = torch.from_numpy(w.Td).pin_memory()
         h_out_t = torch.empty((w.B, w.gamma + 1), dtype=torch.int32).pin_memory()
         h_out_n = torch.empty((w.B,), dtype=torch.int32).pin_memory()
         Ke = max(3, min(K, args.e2e_steps))
 
-        def e2e_step():
+        def timed(fn, k):
+            for _ in range(2):
+                fn()
+            torch.cuda.synchronize()
+            if ws_ > 1:
+                torch.distributed.barrier()
+            es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            es.record(stream)
+            for _ in range(k):
+                fn()
+            ee.record(stream)
+            torch.cuda.synchronize()
+            ems = es.elapsed_time(ee)
+            if ws_ > 1:
+                mt = torch.tensor([ems], device=dev, dtype=torch.float64)
+                torch.distributed.all_reduce(mt, op=torch.distributed.ReduceOp.MAX)
+                ems = float(mt.item())
+            return ems
+
+        def copy_step():
             t.copy_(h_t, non_blocking=True)
             if not greedy:
                 d.copy_(h_d, non_blocking=True)
@@ -356,29 +380,33 @@ def run_ours(args):
             h_out_t.copy_(out_t, non_blocking=True)
             h_out_n.copy_(out_n, non_blocking=True)
 
-        for _ in range(2):
-            e2e_step()
-        torch.cuda.synchronize()
-        if ws_ > 1:
-            torch.distributed.barrier()
-        es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        es.record(stream)
-        for _ in range(Ke):
-            e2e_step()
-        ee.record(stream)
-        torch.cuda.synchronize()
-        ems = es.elapsed_time(ee)
-        if ws_ > 1:
-            mt = torch.tensor([ems], device=dev, dtype=torch.float64)
-            torch.distributed.all_reduce(mt, op=torch.distributed.ReduceOp.MAX)
-            ems = float(mt.item())
+        ems = timed(copy_step, Ke)
         h2d = h_t.numel() * h_t.element_size() + h_tok.numel() * 4
         if not greedy:
             h2d += h_d.numel() * h_d.element_size()
-        e2e = {"value": ws_ * w.rows * Ke / (ems / 1e3), "unit": UNIT,
-               "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(h_out_t.numel() * 4 + h_out_n.numel() * 4),
-               "steps": Ke}
+        e2e_copy = {"value": ws_ * w.rows * Ke / (ems / 1e3), "unit": UNIT,
+                    "h2d_bytes_per_step": int(h2d),
+                    "d2h_bytes_per_step": int(h_out_t.numel() * 4 + h_out_n.numel() * 4),
+                    "steps": Ke, "path": "copy inputs to the device, full-read verify, copy back"}
+        if greedy:
+            e2e = e2e_copy
+        else:
+            def host_step():
+                kw = dict(T_per_seq=h_T, Td_per_seq=h_Td) if per_seq else {}
+                sv.spec_verify_host(h_t, h_d, h_tok, float(w.T[0]), float(w.Td[0]), args.seed,
+                                    h_out_t, h_out_n, seq_index_base=seq_base, **kw)
+
+            Kh = max(3, min(K, 4 * args.e2e_steps))
+            ems = timed(host_step, Kh)
+            streamed, raced = early_exit_rows_read(h_out_n.numpy(), w.gamma)
+            es_ = 2 if w.dtype == "bf16" else 4
+            e2e = {"value": ws_ * w.rows * Kh / (ems / 1e3), "unit": UNIT,
+                   "h2d_bytes_per_step": int((streamed + raced) * w.V * es_ + h_tok.numel() * 4),
+                   "d2h_bytes_per_step": int(h_out_t.numel() * 4 + h_out_n.numel() * 4),
+                   "steps": Kh,
+                   "path": "spec_verify_host: pinned host buffers read and written in place over "
+                           "the host link (no staging copy); early exit reads the rows up to each "
+                           "sequence's first rejection (h2d bytes counted from the outputs)"}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -411,6 +439,7 @@ def run_ours(args):
                      "peak_source": f"{peaks['source']} HBM copy bandwidth (MEASURED_PEAKS.json)"},
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "e2e_copy": e2e_copy,
         "early_exit": early,
         "with_position_stats": stats,
         "gpu_launches": nkern * K,

@@ -129,6 +129,9 @@ typedef struct {
                                      cover every row, or when the device has no cooperative
                                      launch. */
 
+#define SPEC_FLAG_FULL_READ 8u    /* spec_verify_host only: read every row (the default there
+                                     is SPEC_FLAG_EARLY_EXIT) */
+
 /* Zero every field and set dtype = SPEC_BF16. */
 void spec_verify_opts_init(spec_verify_opts *opts);
 
@@ -211,6 +214,22 @@ int spec_verify_noalloc(const void *target_logits, const void *draft_logits,
                         const int32_t *draft_tokens, int B, int gamma, int V, float T, float T_d,
                         uint64_t seed, int32_t *out_tokens, int32_t *out_n_accepted,
                         const spec_verify_opts *opts, void *stream);
+
+/*
+ * Sampling verify on buffers in host memory.  Every pointer (logits, draft tokens,
+ * outputs, and the per-sequence temperatures of opts) may be device memory or pinned host
+ * memory mapped into the device address space (cudaHostAlloc, cudaHostRegister -- on this
+ * GPU's coherent host link the kernels read and write it in place); pageable host memory
+ * is refused with SPEC_EINVAL.  Reading logits over the host link is the bottleneck, so
+ * this entry point verifies with SPEC_FLAG_EARLY_EXIT (only the rows up to each sequence's
+ * first rejection cross the link) unless opts->flags has SPEC_FLAG_FULL_READ or a
+ * diagnostic output is requested.  Outputs land in host memory when the stream's work
+ * completes: synchronise the stream before reading them.  Otherwise as spec_verify_ex.
+ */
+int spec_verify_host(const void *target_logits, const void *draft_logits,
+                     const int32_t *draft_tokens, int B, int gamma, int V, float T, float T_d,
+                     uint64_t seed, int32_t *out_tokens, int32_t *out_n_accepted,
+                     const spec_verify_opts *opts, void *stream);
 
 /*
  * Static token-tree verify ("SubSpec: Speculate Deep and Accurate" (papernotes): a draft

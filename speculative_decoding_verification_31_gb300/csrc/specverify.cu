@@ -617,6 +617,55 @@ int spec_verify_check(void* stream, int32_t* d_status) {
     return h;
 }
 
+}  // extern "C"
+
+namespace {
+
+// The device address of a buffer the GPU can reach: device memory as it is, mapped pinned
+// host memory (cudaHostAlloc / cudaHostRegister) through its device alias.  Anything else
+// (pageable host memory) is refused.
+template <class P>
+int device_alias(P* ptr, P** out) {
+    *out = ptr;
+    if (!ptr) return SPEC_OK;
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+        cudaGetLastError();  // clear the sticky-free error of an unknown pointer
+        return SPEC_EINVAL;
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return SPEC_OK;
+    if (a.type == cudaMemoryTypeHost && a.devicePointer) {
+        *out = static_cast<P*>(a.devicePointer);
+        return SPEC_OK;
+    }
+    return SPEC_EINVAL;
+}
+
+}  // namespace
+
+extern "C" {
+
+int spec_verify_host(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
+                     int B, int gamma, int V, float T, float T_d, uint64_t seed, int32_t* out_tokens,
+                     int32_t* out_n_accepted, const spec_verify_opts* opts, void* stream) {
+    if (B == 0) return check_common(target_logits, out_tokens, out_n_accepted, B, gamma, V,
+                                    opts ? opts->dtype : SPEC_BF16);
+    const void *t = nullptr, *d = nullptr;
+    const int32_t* tok = nullptr;
+    int32_t *ot = nullptr, *on = nullptr;
+    if (device_alias(target_logits, &t) || device_alias(draft_logits, &d) ||
+        device_alias(draft_tokens, &tok) || device_alias(out_tokens, &ot) ||
+        device_alias(out_n_accepted, &on))
+        return SPEC_EINVAL;
+    spec_verify_opts o;
+    if (opts) o = *opts;
+    else spec_verify_opts_init(&o);
+    if (device_alias(o.T_per_seq, &o.T_per_seq) || device_alias(o.Td_per_seq, &o.Td_per_seq))
+        return SPEC_EINVAL;
+    if (!(o.flags & SPEC_FLAG_FULL_READ)) o.flags |= SPEC_FLAG_EARLY_EXIT;
+    return spec_verify_ex(t, d, tok, B, gamma, V, T, T_d, seed, ot, on, &o, stream);
+}
+
 int spec_verify_tree(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
                      const int32_t* parent, int B, int N, int V, float T, float T_d, uint64_t seed,
                      int32_t* out_tokens, int32_t* out_nodes, int32_t* out_n_accepted,

@@ -19,13 +19,13 @@ LIB_PATH = os.path.join(_HERE, "libspecverify.so")
 SPEC_OK, SPEC_EINVAL, SPEC_ECUDA, SPEC_EBADTOKEN, SPEC_ETIMEOUT, SPEC_ENOMEM = range(6)
 SPEC_ESCRATCH = 6
 SPEC_NOALLOC_SCRATCH_BYTES = 8 << 20
-SPEC_FLAG_FUSED, SPEC_DEBUG_NEVER_READY, SPEC_FLAG_EARLY_EXIT = 1, 2, 4
+SPEC_FLAG_FUSED, SPEC_DEBUG_NEVER_READY, SPEC_FLAG_EARLY_EXIT, SPEC_FLAG_FULL_READ = 1, 2, 4, 8
 SPEC_F32, SPEC_BF16 = 0, 1
 
 EXPORTED = ("spec_verify", "spec_verify_greedy", "spec_verify_ex", "spec_verify_greedy_ex",
             "spec_verify_workspace_bytes", "spec_verify_check", "spec_verify_strerror",
             "spec_verify_opts_init", "spec_verify_noalloc", "spec_row_entropy",
-            "spec_adaptive_k", "spec_verify_tree")
+            "spec_adaptive_k", "spec_verify_tree", "spec_verify_host")
 
 
 class SpecVerifyError(RuntimeError):
@@ -90,6 +90,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.spec_verify_strerror.restype = ctypes.c_char_p
     lib.spec_verify_opts_init.argtypes = [OP]
     lib.spec_verify_opts_init.restype = None
+    lib.spec_verify_host.argtypes = [P, P, P, I, I, I, F, F, U64, P, P, OP, P]
+    lib.spec_verify_host.restype = ctypes.c_int
     lib.spec_verify_tree.argtypes = [P, P, P, P, I, I, I, F, F, U64, P, P, P, OP, P]
     lib.spec_verify_tree.restype = ctypes.c_int
     lib.spec_row_entropy.argtypes = [P, I, I, F, I, P, P]
@@ -311,6 +313,36 @@ def spec_verify_noalloc(target_logits, draft_logits, draft_tokens, T: float, T_d
         ctypes.byref(o), _stream_handle(stream, dev))
     if rc != SPEC_OK:
         raise SpecVerifyError(rc, "spec_verify_noalloc")
+    return out_tokens, out_n_accepted
+
+
+def spec_verify_host(target_logits, draft_logits, draft_tokens, T: float, T_d: float, seed: int,
+                     out_tokens, out_n_accepted, *, T_per_seq=None, Td_per_seq=None,
+                     seq_index_base: int = 0, full_read: bool = False, stream=None):
+    """Sampling verify on pinned host tensors (see ``spec_verify_host`` in the C header): the
+    kernels read the logits and write the outputs in place over the host link.  Every
+    tensor is a contiguous pinned CPU tensor (or a CUDA tensor); the outputs are valid once
+    the stream has finished."""
+    for name, t in (("target_logits", target_logits), ("draft_logits", draft_logits),
+                    ("draft_tokens", draft_tokens), ("out_tokens", out_tokens),
+                    ("out_n_accepted", out_n_accepted)):
+        if t is not None and t.numel() and not t.is_cuda and not t.is_pinned():
+            raise ValueError(f"{name} must be pinned host memory or a CUDA tensor")
+        if t is not None and not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    B, G1, V = target_logits.shape
+    g = G1 - 1
+    dev = torch.device("cuda", torch.cuda.current_device())
+    o = _make_opts(_dtype_code(target_logits), T_per_seq, Td_per_seq, seq_index_base, None,
+                   None, None, None, SPEC_FLAG_FULL_READ if full_read else 0)
+    if g == 0:  # nothing to read: no draft rows or tokens
+        draft_logits = draft_tokens = None
+    rc = load_library().spec_verify_host(
+        _ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), B, g, V, float(T),
+        float(T_d), int(seed) & (2**64 - 1), _ptr(out_tokens), _ptr(out_n_accepted),
+        ctypes.byref(o), _stream_handle(stream, dev))
+    if rc != SPEC_OK:
+        raise SpecVerifyError(rc, "spec_verify_host")
     return out_tokens, out_n_accepted
 
 
