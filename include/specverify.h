@@ -266,6 +266,27 @@ int spec_verify_tree(const void *target_logits, const void *draft_logits,
                      int32_t *out_n_accepted, const spec_verify_opts *opts, void *stream);
 
 /*
+ * The LM head on the tensor cores (tcgen05): logits L = H W^T with hidden states H
+ * [rows, d] and head weights W [V, d], both bf16 row-major in device memory (16-byte
+ * aligned), d a multiple of 64, accumulated in fp32.  spec_lmhead_logits writes L
+ * [rows, V] fp32.  spec_lmhead_row_stats never writes L: its epilogue folds each tile into
+ * the row's online softmax statistics at temperature T_row[row] (device [rows]) and keeps
+ * the logit at token_row[row] (device [rows], -1: none; NULL when out_logp_token is NULL),
+ * then writes out_logZ [rows] = ln sum_x exp(L[row, x] / T) and out_logp_token [rows] =
+ * L[row, token] / T - ln Z (NaN without a token); either output may be NULL, not both.
+ * These are the row statistics of the verify step ("How speculative decoding makes LLMs go
+ * brrr", module 2: p_i = softmax of the target's logits at position i) computed from the
+ * model's last hidden states, so the B (gamma+1) x V logits are never written and read
+ * back.  spec_lmhead_row_stats uses the library's own workspace.  SPEC_EINVAL for bad sizes,
+ * NULL or misaligned pointers; SPEC_ECUDA if the tensor-map encoder is unavailable.
+ */
+int spec_lmhead_logits(const void *hidden, const void *weight, int rows, int V, int d,
+                       float *out_logits, void *stream);
+int spec_lmhead_row_stats(const void *hidden, const void *weight, int rows, int V, int d,
+                          const float *T_row, const int32_t *token_row, float *out_logZ,
+                          float *out_logp_token, void *stream);
+
+/*
  * Entropy of softmax(L / T) of each of `rows` contiguous rows of V logits (dtype
  * spec_dtype), in nats, into out_H [rows] (device) -- e.g. the next draft tokens' entropies
  * for spec_adaptive_k.  Uses the library's own workspace.  SPEC_EINVAL for bad sizes, a

@@ -1,0 +1,378 @@
+// lmhead.cuh -- the LM head on the tensor cores (sm_103a tcgen05), with the verify step's
+// row statistics as its epilogue.
+//
+// Logits are L = H W^T: hidden states H [rows, d] and head weights W [V, d], both bf16 and
+// row-major (so both operands are K-major), accumulated in fp32.  A CTA owns one tile of
+// 128 rows and a contiguous run of 256-wide vocabulary tiles; per tile it streams K in
+// 64-element slices:
+//   warp 0     one elected thread issues TMA loads (cp.async.bulk.tensor, 128-byte swizzle)
+//              of the A and B slices into a 4-stage shared-memory ring;
+//   warp 1     allocates 512 TMEM columns (two 128 x 256 fp32 accumulators) and one
+//              elected thread issues tcgen05.mma (M = 128, N = 256, K = 16; bf16 x bf16 ->
+//              fp32), committing each stage back to the producer and each finished tile
+//              to the epilogue;
+//   warps 2-5  the epilogue: each reads its 32 TMEM lanes (one row per thread) with
+//              tcgen05.ld and either writes the logits (spec_lmhead_logits) or folds them
+//              into the row's online softmax statistics -- max and sum of 2^(x c - m) in
+//              base 2, c = log2(e) / T of the row -- and keeps the logit at the row's draft
+//              token; the logits never reach HBM.
+// The two accumulators let the tensor cores run the next tile while the epilogue drains the
+// last.  Every mbarrier wait is bounded (kWaitLimitNs): on a timeout the kernel records
+// SPEC_ETIMEOUT, stops issuing, waits (bounded) for its loads in flight and frees its TMEM.
+// This is a dense contraction (2 rows * V * d flops per row), the one place of the verify
+// pipeline where tensor cores apply.
+#pragma once
+
+#include <cuda.h>
+#include <cstdint>
+
+namespace specverify {
+
+constexpr int kGemmBM = 128;      // rows per tile (TMEM lanes)
+constexpr int kGemmBN = 256;      // vocabulary entries per tile (TMEM columns per accumulator)
+constexpr int kGemmBK = 64;       // K per stage: one 128-byte swizzle row of bf16
+constexpr int kGemmStages = 4;
+constexpr int kGemmThreads = 192; // 6 warps
+constexpr uint32_t kGemmStageA = kGemmBM * kGemmBK * 2;  // 16 KB
+constexpr uint32_t kGemmStageB = kGemmBN * kGemmBK * 2;  // 32 KB
+constexpr uint32_t kGemmTmemCols = 512;
+// dynamic shared memory: 1024-byte alignment slack, the ring, then the barriers
+constexpr uint32_t kGemmSmem = 1024 + kGemmStages * (kGemmStageA + kGemmStageB) + 256;
+
+// Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
+// (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22,
+// M >> 4 at bits 24-28.
+constexpr uint32_t kGemmIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                                (static_cast<uint32_t>(kGemmBN >> 3) << 17) |
+                                (static_cast<uint32_t>(kGemmBM >> 4) << 24);
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Shared-memory matrix descriptor of a K-major tile stored as TMA writes it with the
+// 128-byte swizzle: rows of 128 bytes, 8-row (1024-byte) swizzle atoms.  Start address
+// >> 4 in bits 0-13, leading-byte offset (unused by this layout) 1 in bits 16-29, stride
+// byte offset 1024 >> 4 in bits 32-45, descriptor version 1 in bits 46-47, layout
+// SWIZZLE_128B = 2 in bits 61-63.  The stage buffers are 1024-byte aligned.
+__device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
+    return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1) << 16) |
+           (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+           (static_cast<uint64_t>(2) << 61);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase of the given parity to complete; false after kWaitLimitNs or
+// once *abort is set by another thread of the CTA.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+    if (mbar_test(bar, parity)) return true;
+    const unsigned long long t0 = global_time_ns();
+    while (!mbar_test(bar, parity)) {
+        if (*abort) return false;
+        if (global_time_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(const CUtensorMap* map, uint64_t* bar, void* dst, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(kGemmIdesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_addr(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane (the warp's 32-lane slice).
+__device__ __forceinline__ void tmem_load32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32"
+        " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15,"
+        " %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+          "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+          "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+struct LmHeadParams {
+    int rows, V, d;               // L = H W^T: H [rows, d], W [V, d]
+    int tiles_per_cta;            // vocabulary tiles of one CTA (its chunk)
+    int nchunks;                  // chunks per row: ceil(V / (kGemmBN * tiles_per_cta))
+    float* logits;                // [rows, V] fp32 output (spec_lmhead_logits), or nullptr
+    // statistics epilogue
+    const float* T_row;           // [rows] temperature of each row
+    const int32_t* token_row;     // [rows] token whose logit to keep (-1: none), or nullptr
+    float2* stat_parts;           // [rows][nchunks] (scaled max, sum) in base 2
+    float* token_logit;           // [rows] logit at token_row (raw, before 1/T)
+    int32_t* status;
+};
+
+// kLogits: write the logits; otherwise the statistics epilogue.
+template <bool kLogits>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+lmhead_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w,
+              LmHeadParams p) {
+    extern __shared__ uint8_t gemm_smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(gemm_smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    uint8_t* stage_a = base;
+    uint8_t* stage_b = base + kGemmStages * kGemmStageA;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(stage_b + kGemmStages * kGemmStageB);
+    uint64_t* full = bars;                     // [stages] TMA -> MMA
+    uint64_t* empty = bars + kGemmStages;      // [stages] MMA -> TMA
+    uint64_t* tfull = bars + 2 * kGemmStages;  // [2] MMA -> epilogue
+    uint64_t* tempty = tfull + 2;              // [2] epilogue -> MMA
+    uint64_t* tdrain = tempty + 2;             // every MMA of this CTA is done
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tdrain + 1);
+    volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m_tile = blockIdx.y;
+    const int chunk = blockIdx.x;
+    const int n_tiles_total = (p.V + kGemmBN - 1) / kGemmBN;
+    const int t_begin = chunk * p.tiles_per_cta;
+    const int t_end = min(n_tiles_total, t_begin + p.tiles_per_cta);
+    const int ntiles = max(0, t_end - t_begin);
+    const int kb_count = p.d / kGemmBK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kGemmStages; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull + a, 1);
+            mbar_init(tempty + a, 4);  // one arrival per epilogue warp
+        }
+        mbar_init(tdrain, 1);
+        *abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {  // TMEM: two 256-column accumulators
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_addr(tmem_slot)),
+                     "r"(kGemmTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tmem_fence_before();
+    __syncthreads();
+    tmem_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ---- TMA producer ----
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            for (int t = 0; t < ntiles && !*abort; ++t) {
+                const int n0 = (t_begin + t) * kGemmBN;
+                for (int kb = 0; kb < kb_count; ++kb) {
+                    if (!mbar_wait(empty + stage, phase ^ 1u, abort)) {
+                        *abort = 1;
+                        break;
+                    }
+                    mbar_expect_tx(full + stage, kGemmStageA + kGemmStageB);
+                    tma_load_2d(&map_h, full + stage, stage_a + stage * kGemmStageA, kb * kGemmBK,
+                                m_tile * kGemmBM);
+                    tma_load_2d(&map_w, full + stage, stage_b + stage * kGemmStageB, kb * kGemmBK, n0);
+                    ++issued;
+                    if (++stage == kGemmStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (*abort) {
+                // let the loads in flight land before the CTA's shared memory goes away
+                const int pending = min(issued, kGemmStages);
+                for (int k = 0; k < pending; ++k) {
+                    if (--stage < 0) {
+                        stage = kGemmStages - 1;
+                        phase ^= 1u;
+                    }
+                    volatile int never = 0;
+                    mbar_wait(full + stage, phase, &never);
+                }
+                set_status(p.status, 4 /* SPEC_ETIMEOUT */);
+            }
+        }
+    } else if (warp == 1) {
+        // ---- MMA issuer ----
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int t = 0; t < ntiles && !*abort; ++t) {
+                const int acc = t & 1;
+                const uint32_t acc_phase = (t >> 1) & 1u;
+                if (!mbar_wait(tempty + acc, acc_phase ^ 1u, abort)) {
+                    *abort = 1;
+                    break;
+                }
+                tmem_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kGemmBN);
+                for (int kb = 0; kb < kb_count; ++kb) {
+                    if (!mbar_wait(full + stage, phase, abort)) {
+                        *abort = 1;
+                        break;
+                    }
+                    tmem_fence_after();
+                    const uint64_t adesc = sw128_kmajor_desc(smem_addr(stage_a + stage * kGemmStageA));
+                    const uint64_t bdesc = sw128_kmajor_desc(smem_addr(stage_b + stage * kGemmStageB));
+#pragma unroll
+                    for (int kk = 0; kk < kGemmBK / 16; ++kk)  // +32 bytes of K per step
+                        umma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, (kb | kk) != 0);
+                    umma_commit(empty + stage);  // the stage is free once these MMAs are done
+                    if (++stage == kGemmStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (*abort) break;
+                umma_commit(tfull + acc);  // the tile's accumulator is complete
+            }
+            // whatever happened, no MMA may still write TMEM when it is freed
+            umma_commit(tdrain);
+            volatile int never = 0;
+            if (!mbar_wait(tdrain, 0, &never)) set_status(p.status, 4 /* SPEC_ETIMEOUT */);
+        }
+    } else {
+        // ---- epilogue: warps 2..5, TMEM lane slice (warp % 4) * 32 ----
+        const int slice = warp & 3;
+        const int row = m_tile * kGemmBM + slice * 32 + lane;
+        const bool row_ok = row < p.rows;
+        float c = 1.0f;
+        int tok = -1;
+        if (!kLogits && row_ok) {
+            c = kLog2e / p.T_row[row];
+            if (p.token_row) tok = p.token_row[row];
+        }
+        float m = -FLT_MAX, s = 0.0f, xtok = 0.0f;
+        for (int t = 0; t < ntiles; ++t) {
+            const int acc = t & 1;
+            const uint32_t acc_phase = (t >> 1) & 1u;
+            // lane 0 waits (bounded) and the warp follows it, so that the warp stays converged
+            // for the .sync.aligned TMEM loads; then every lane observes the completed phase
+            int ok = 0;
+            if (lane == 0) ok = mbar_wait(tfull + acc, acc_phase, abort);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) *abort = 1;
+                break;
+            }
+            volatile int never = 0;
+            mbar_wait(tfull + acc, acc_phase, &never);  // completed: returns at once
+            __syncwarp();
+            tmem_fence_after();
+            const int n0 = (t_begin + t) * kGemmBN;
+#pragma unroll 1
+            for (int c32 = 0; c32 < kGemmBN / 32; ++c32) {
+                float v[32];
+                tmem_load32(tmem_base + (static_cast<uint32_t>(slice * 32) << 16) +
+                                static_cast<uint32_t>(acc * kGemmBN + c32 * 32),
+                            v);
+                const int col0 = n0 + c32 * 32;
+                if (kLogits) {
+                    if (row_ok) {
+                        float* dst = p.logits + static_cast<long long>(row) * p.V + col0;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (col0 + i < p.V) dst[i] = v[i];
+                    }
+                } else {
+                    float bmax = -INFINITY;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (col0 + i < p.V) bmax = fmaxf(bmax, v[i]);
+                    const float mn = fmaxf(m, fmaxf(bmax * c, -FLT_MAX));
+                    float part = 0.0f;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (col0 + i < p.V) part += ex2_fast(fmaf(v[i], c, -mn));
+                    s = s * ex2_fast(m - mn) + part;
+                    m = mn;
+                    if (tok >= col0 && tok < col0 + 32) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (tok == col0 + i) xtok = v[i];
+                    }
+                }
+            }
+            tmem_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty + acc);
+        }
+        if (!kLogits && row_ok && !*abort) {
+            store_stat(p.stat_parts + static_cast<long long>(row) * p.nchunks + chunk, m, s);
+            if (tok >= t_begin * kGemmBN && tok < t_end * kGemmBN && tok < p.V && p.token_logit)
+                p.token_logit[row] = xtok;
+        }
+        if (*abort && lane == 0) set_status(p.status, 4 /* SPEC_ETIMEOUT */);
+    }
+    tmem_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(kGemmTmemCols)
+                     : "memory");
+    }
+}
+
+}  // namespace specverify

@@ -1,6 +1,8 @@
 // specverify.cu -- host side of libspecverify: argument checks, workspace, launches.
 //
 // The C ABI is declared in include/specverify.h; the kernels are in kernels.cuh.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -10,6 +12,7 @@
 #include <mutex>
 
 #include "kernels.cuh"
+#include "lmhead.cuh"
 #include "specverify.h"
 
 using namespace specverify;
@@ -729,6 +732,172 @@ int spec_verify_tree(const void* target_logits, const void* draft_logits, const 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return dtype == SPEC_F32 ? launch_tree<F32Elem>(p, t, d->sm_count, opts, s)
                              : launch_tree<Bf16Elem>(p, t, d->sm_count, opts, s);
+}
+
+}  // extern "C"
+
+namespace {
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link-time libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// 2-D bf16 tensor map of a row-major [rows, cols] matrix, box of box_rows x 64 elements
+// (128 bytes: one 128-byte swizzle row).
+int bf16_tensor_map(CUtensorMap* map, const void* base, int rows, int cols, int box_rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return SPEC_ECUDA;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kGemmBK), static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                           box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? SPEC_OK : SPEC_EINVAL;
+}
+
+int lmhead_check(const void* H, const void* W, int rows, int V, int d) {
+    if (rows < 0 || V < 1 || d < kGemmBK || d % kGemmBK != 0) return SPEC_EINVAL;
+    if (static_cast<long long>(rows) * V >= (1LL << 40)) return SPEC_EINVAL;
+    if (rows == 0) return SPEC_OK;
+    if (!H || !W || !aligned16(H) || !aligned16(W)) return SPEC_EINVAL;
+    return SPEC_OK;
+}
+
+// Grid of the LM-head kernel: one row tile per grid row, the vocabulary tiles split into
+// chunks so that the CTAs fill the GPU about once (one CTA per SM: it holds 512 TMEM
+// columns and 193 KB of shared memory).
+void lmhead_grid(int rows, int V, int sm_count, LmHeadParams& lp, dim3& grid) {
+    const int m_tiles = (rows + kGemmBM - 1) / kGemmBM;
+    const int n_tiles = (V + kGemmBN - 1) / kGemmBN;
+    long long want = sm_count / m_tiles;  // chunks per row tile
+    if (want < 1) want = 1;
+    if (want > n_tiles) want = n_tiles;
+    lp.tiles_per_cta = static_cast<int>((n_tiles + want - 1) / want);
+    lp.nchunks = (n_tiles + lp.tiles_per_cta - 1) / lp.tiles_per_cta;
+    grid = dim3(static_cast<unsigned>(lp.nchunks), static_cast<unsigned>(m_tiles));
+}
+
+template <bool kLogits>
+int launch_lmhead(const void* H, const void* W, LmHeadParams& lp, int sm_count, cudaStream_t s) {
+    CUtensorMap mh, mw;
+    int rc = bf16_tensor_map(&mh, H, lp.rows, lp.d, kGemmBM);
+    if (rc) return rc;
+    rc = bf16_tensor_map(&mw, W, lp.V, lp.d, kGemmBN);
+    if (rc) return rc;
+    dim3 grid;
+    lmhead_grid(lp.rows, lp.V, sm_count, lp, grid);
+    auto kernel = lmhead_kernel<kLogits>;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem) != cudaSuccess)
+        return SPEC_ECUDA;
+    kernel<<<grid, kGemmThreads, kGemmSmem, s>>>(mh, mw, lp);
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int spec_lmhead_logits(const void* hidden, const void* weight, int rows, int V, int d,
+                       float* out_logits, void* stream) {
+    int rc = lmhead_check(hidden, weight, rows, V, d);
+    if (rc || rows == 0) return rc;
+    if (!out_logits) return SPEC_EINVAL;
+    DeviceState* dev = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        rc = device_state(&dev);
+        if (rc) return rc;
+    }
+    LmHeadParams lp{};
+    lp.rows = rows;
+    lp.V = V;
+    lp.d = d;
+    lp.logits = out_logits;
+    lp.status = dev->status;
+    return launch_lmhead<true>(hidden, weight, lp, dev->sm_count, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"
+
+namespace {
+
+// Merge each row's chunk partials: ln Z = (m + log2 s) ln 2 and, when a token is given,
+// ln p(token) = x_token / T - ln Z.  One warp per row.
+__global__ void __launch_bounds__(256) lmhead_merge_kernel(LmHeadParams p, float* out_logZ,
+                                                           float* out_logp_token) {
+    const int lane = threadIdx.x & 31;
+    const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (row >= p.rows) return;
+    SoftmaxStat st{-FLT_MAX, 0.0f};
+    for (int k = lane; k < p.nchunks; k += 32) {
+        const float2 q = p.stat_parts[static_cast<long long>(row) * p.nchunks + k];
+        st = merge_stat(st, SoftmaxStat{q.x, q.y});
+    }
+    st = warp_merge_stat(st);
+    if (lane == 0) {
+        const float lz = (st.m + log2f(st.s)) * kLn2;
+        if (out_logZ) out_logZ[row] = lz;
+        if (out_logp_token) {
+            const int tok = p.token_row ? p.token_row[row] : -1;
+            out_logp_token[row] = (tok >= 0 && tok < p.V) ? p.token_logit[row] / p.T_row[row] - lz : NAN;
+        }
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+int spec_lmhead_row_stats(const void* hidden, const void* weight, int rows, int V, int d,
+                          const float* T_row, const int32_t* token_row, float* out_logZ,
+                          float* out_logp_token, void* stream) {
+    int rc = lmhead_check(hidden, weight, rows, V, d);
+    if (rc || rows == 0) return rc;
+    if (!T_row || (!out_logZ && !out_logp_token)) return SPEC_EINVAL;
+    if (out_logp_token && !token_row) return SPEC_EINVAL;
+    DeviceState* dev = nullptr;
+    char* ws = nullptr;
+    LmHeadParams lp{};
+    lp.rows = rows;
+    lp.V = V;
+    lp.d = d;
+    dim3 grid;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        rc = device_state(&dev);
+        if (rc) return rc;
+        lmhead_grid(rows, V, dev->sm_count, lp, grid);
+        // workspace: [rows][nchunks] partials, then [rows] token logits
+        const size_t need = align_up(static_cast<size_t>(rows) * lp.nchunks * sizeof(float2), 256) +
+                            align_up(static_cast<size_t>(rows) * sizeof(float), 256);
+        rc = ensure_workspace(*dev, need);
+        if (rc) return rc;
+        ws = static_cast<char*>(dev->ws);
+    }
+    lp.T_row = T_row;
+    lp.token_row = token_row;
+    lp.stat_parts = reinterpret_cast<float2*>(ws);
+    lp.token_logit = reinterpret_cast<float*>(
+        ws + align_up(static_cast<size_t>(rows) * lp.nchunks * sizeof(float2), 256));
+    lp.status = dev->status;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    rc = launch_lmhead<false>(hidden, weight, lp, dev->sm_count, s);
+    if (rc) return rc;
+    lmhead_merge_kernel<<<(rows * 32 + 255) / 256, 256, 0, s>>>(lp, out_logZ, out_logp_token);
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
 }
 
 int spec_adaptive_k(const float* H_next, int B, int K, const double* centres,

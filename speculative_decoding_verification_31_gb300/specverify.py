@@ -25,7 +25,8 @@ SPEC_F32, SPEC_BF16 = 0, 1
 EXPORTED = ("spec_verify", "spec_verify_greedy", "spec_verify_ex", "spec_verify_greedy_ex",
             "spec_verify_workspace_bytes", "spec_verify_check", "spec_verify_strerror",
             "spec_verify_opts_init", "spec_verify_noalloc", "spec_row_entropy",
-            "spec_adaptive_k", "spec_verify_tree", "spec_verify_host")
+            "spec_adaptive_k", "spec_verify_tree", "spec_verify_host", "spec_lmhead_logits",
+            "spec_lmhead_row_stats")
 
 
 class SpecVerifyError(RuntimeError):
@@ -90,6 +91,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.spec_verify_strerror.restype = ctypes.c_char_p
     lib.spec_verify_opts_init.argtypes = [OP]
     lib.spec_verify_opts_init.restype = None
+    lib.spec_lmhead_logits.argtypes = [P, P, I, I, I, P, P]
+    lib.spec_lmhead_logits.restype = ctypes.c_int
+    lib.spec_lmhead_row_stats.argtypes = [P, P, I, I, I, P, P, P, P, P]
+    lib.spec_lmhead_row_stats.restype = ctypes.c_int
     lib.spec_verify_host.argtypes = [P, P, P, I, I, I, F, F, U64, P, P, OP, P]
     lib.spec_verify_host.restype = ctypes.c_int
     lib.spec_verify_tree.argtypes = [P, P, P, P, I, I, I, F, F, U64, P, P, P, OP, P]
@@ -344,6 +349,42 @@ def spec_verify_host(target_logits, draft_logits, draft_tokens, T: float, T_d: f
     if rc != SPEC_OK:
         raise SpecVerifyError(rc, "spec_verify_host")
     return out_tokens, out_n_accepted
+
+
+def _check_lmhead(hidden, weight):
+    for name, t in (("hidden", hidden), ("weight", weight)):
+        if t.dim() != 2 or t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 CUDA matrix")
+    if hidden.shape[1] != weight.shape[1]:
+        raise ValueError("hidden [rows, d] and weight [V, d] must share d")
+    return hidden.shape[0], weight.shape[0], hidden.shape[1]
+
+
+def spec_lmhead_logits(hidden, weight, out_logits=None, stream=None):
+    """Logits hidden @ weight^T (fp32) on the tensor cores."""
+    rows, V, d = _check_lmhead(hidden, weight)
+    if out_logits is None:
+        out_logits = torch.empty((rows, V), dtype=torch.float32, device=hidden.device)
+    rc = load_library().spec_lmhead_logits(_ptr(hidden), _ptr(weight), rows, V, d, _ptr(out_logits),
+                                           _stream_handle(stream, hidden.device))
+    if rc != SPEC_OK:
+        raise SpecVerifyError(rc, "spec_lmhead_logits")
+    return out_logits
+
+
+def spec_lmhead_row_stats(hidden, weight, T_row, token_row=None, stream=None):
+    """(ln Z [rows], ln p(token) [rows] or None) of softmax(hidden @ weight^T / T_row)
+    without writing the logits."""
+    rows, V, d = _check_lmhead(hidden, weight)
+    dev = hidden.device
+    logz = torch.empty((rows,), dtype=torch.float32, device=dev)
+    logp = torch.empty((rows,), dtype=torch.float32, device=dev) if token_row is not None else None
+    rc = load_library().spec_lmhead_row_stats(_ptr(hidden), _ptr(weight), rows, V, d, _ptr(T_row),
+                                              _ptr(token_row), _ptr(logz), _ptr(logp),
+                                              _stream_handle(stream, dev))
+    if rc != SPEC_OK:
+        raise SpecVerifyError(rc, "spec_lmhead_row_stats")
+    return logz, logp
 
 
 class Tree:
