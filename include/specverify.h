@@ -287,6 +287,24 @@ int spec_lmhead_row_stats(const void *hidden, const void *weight, int rows, int 
                           float *out_logp_token, void *stream);
 
 /*
+ * The sampling verify step from the models' last hidden states: h_target [B, gamma+1, d]
+ * with the target LM head w_target [V, d], and h_draft [B, gamma, d] with the draft LM head
+ * w_draft [V, d] (may be w_target), all bf16 row-major device memory, d a multiple of 64.
+ * The target and draft row statistics come from spec_lmhead_row_stats' kernel (the B (2
+ * gamma + 1) x V logits are never written); only the raced row of each sequence (target
+ * row j, and draft row j for a residual) is computed as logits, on the tensor cores, and
+ * raced.  Outputs, decisions and random numbers are those of spec_verify_ex run on the
+ * logits H W^T.  opts: per-sequence temperatures, seq_index_base, d_status and prof_events
+ * (before the first kernel, after the statistics, after the raced rows' logits, after the
+ * race) are honoured; the library's own workspace is used (about 8 B V bytes for the raced
+ * rows' fp32 logits).  SPEC_EINVAL for bad sizes, NULL or misaligned pointers.
+ */
+int spec_verify_lmhead(const void *h_target, const void *w_target, const void *h_draft,
+                       const void *w_draft, const int32_t *draft_tokens, int B, int gamma, int V,
+                       int d, float T, float T_d, uint64_t seed, int32_t *out_tokens,
+                       int32_t *out_n_accepted, const spec_verify_opts *opts, void *stream);
+
+/*
  * Entropy of softmax(L / T) of each of `rows` contiguous rows of V logits (dtype
  * spec_dtype), in nats, into out_H [rows] (device) -- e.g. the next draft tokens' entropies
  * for spec_adaptive_k.  Uses the library's own workspace.  SPEC_EINVAL for bad sizes, a

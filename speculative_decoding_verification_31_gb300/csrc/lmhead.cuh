@@ -375,4 +375,133 @@ lmhead_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__
     }
 }
 
+// ----------------------------------------------------------------------------------------
+// The verify step from hidden states (spec_verify_lmhead): the statistics kernel above runs
+// on the target rows (T) and the draft rows (T_d) with each row's draft token, then
+//   lmhead_scan   one warp per sequence: the accept test of every position from ln p(d_i),
+//                 ln q(d_i) and u_i (the same rule and random numbers as the logits path),
+//                 the sequence's outputs, and the hidden states of the row it races
+//                 (target row j, and draft row j for a residual) gathered for the GEMM;
+//   the tensor-core GEMM writes the logits of just those rows (2 B rows), and
+//   lmhead_race   races them (the logits path's race, rows from that small buffer).
+// ----------------------------------------------------------------------------------------
+
+struct LmVerifyParams {
+    int B, gamma, V, d;
+    const uint16_t* h_target;    // [B, gamma+1, d] bf16 bits
+    const uint16_t* h_draft;     // [B, gamma, d]
+    const int32_t* tokens;       // [B, gamma]
+    const float* logZ_t;         // [B, gamma+1] nats
+    const float* logp_t;         // [B, gamma+1] ln p_i(d_i) (NaN at row gamma)
+    const float* logZ_d;         // [B, gamma]
+    const float* logq_d;         // [B, gamma]
+    uint16_t* h_race_t;          // [B, d] gathered target hidden state of the raced row
+    uint16_t* h_race_d;          // [B, d] gathered draft hidden state (residual) or zeros
+    SeqInfo* seq;                // [B]
+    float T, Td;
+    const float* T_seq;
+    const float* Td_seq;
+    PhiloxKey key;
+    uint32_t seq_base;
+    int32_t* out_tokens;         // [B, gamma+1]
+    int32_t* out_n;              // [B]
+    int32_t* status;
+};
+
+__global__ void __launch_bounds__(256) lmhead_scan_kernel(LmVerifyParams q) {
+    const int lane = threadIdx.x & 31;
+    const int b = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (b >= q.B) return;
+    const float Tb = q.T_seq ? q.T_seq[b] : q.T, Tdb = q.Td_seq ? q.Td_seq[b] : q.Td;
+    const uint32_t bg = q.seq_base + static_cast<uint32_t>(b);
+    const int32_t* tok = q.tokens + static_cast<long long>(b) * q.gamma;
+    bool bad = false;
+    int j = q.gamma;
+    for (int i0 = 0; i0 < q.gamma; i0 += 32) {
+        const int i = i0 + lane;
+        bool reject = false;
+        if (i < q.gamma) {
+            const int d = tok[i];
+            if (d < 0 || d >= q.V) {
+                bad = true;
+            } else {
+                const float u = accept_uniform(q.key, bg, static_cast<uint32_t>(i));
+                const float lp = q.logp_t[static_cast<long long>(b) * (q.gamma + 1) + i];
+                const float lq = q.logq_d[static_cast<long long>(b) * q.gamma + i];
+                // accept iff u < min(1, p/q); p(d) = 0 rejects, q(d) = 0 < p(d) accepts
+                reject = !((lp > -INFINITY) && (u < expf(lp - lq)));
+            }
+        }
+        const uint32_t rej = __ballot_sync(0xffffffffu, reject);
+        if (rej && j == q.gamma) j = i0 + __ffs(rej) - 1;
+    }
+    if (__any_sync(0xffffffffu, bad)) j = -1;
+    int32_t* out = q.out_tokens + static_cast<long long>(b) * (q.gamma + 1);
+    for (int t = lane; t <= q.gamma; t += 32)
+        if (t != j || j < 0) out[t] = (j >= 0 && t < j) ? tok[t] : -1;
+    // gather the raced rows' hidden states (zeros for a bonus draw's draft row)
+    const int rj = j < 0 ? 0 : j;
+    const uint4* st = reinterpret_cast<const uint4*>(q.h_target + (static_cast<long long>(b) * (q.gamma + 1) + rj) * q.d);
+    uint4* dt = reinterpret_cast<uint4*>(q.h_race_t + static_cast<long long>(b) * q.d);
+    uint4* dd = reinterpret_cast<uint4*>(q.h_race_d + static_cast<long long>(b) * q.d);
+    const bool residual = j >= 0 && j < q.gamma;
+    const uint4* sd = residual ? reinterpret_cast<const uint4*>(q.h_draft + (static_cast<long long>(b) * q.gamma + j) * q.d)
+                               : nullptr;
+    for (int k = lane; k < q.d / 8; k += 32) {
+        dt[k] = st[k];
+        dd[k] = residual ? sd[k] : make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (lane == 0) {
+        q.out_n[b] = j;
+        SeqInfo si;
+        si.j = j;
+        si.cp = kLog2e / Tb;
+        si.cq = kLog2e / Tdb;
+        // log2 p(x) = x cp - mp - l2sp with mp = log2 Z (the row statistics as one number)
+        si.mp = j >= 0 ? q.logZ_t[static_cast<long long>(b) * (q.gamma + 1) + j] * kLog2e : 0.0f;
+        si.l2sp = 0.0f;
+        si.mq = residual ? q.logZ_d[static_cast<long long>(b) * q.gamma + j] * kLog2e : 0.0f;
+        si.l2sq = 0.0f;
+        si.pad = 0;
+        q.seq[b] = si;
+        if (j < 0) set_status(q.status, 3 /* SPEC_EBADTOKEN */);
+    }
+}
+
+// Per-row temperature and draft token of the target rows (b, i <= gamma; no token at
+// i = gamma) and the draft rows (b, i < gamma).
+__global__ void lmhead_rows_kernel(LmVerifyParams q, float* T_t, int32_t* tok_t, float* T_d, int32_t* tok_d) {
+    const long long k = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const long long rows_t = static_cast<long long>(q.B) * (q.gamma + 1);
+    if (k < rows_t) {
+        const int b = static_cast<int>(k / (q.gamma + 1)), i = static_cast<int>(k % (q.gamma + 1));
+        T_t[k] = q.T_seq ? q.T_seq[b] : q.T;
+        tok_t[k] = i < q.gamma ? q.tokens[static_cast<long long>(b) * q.gamma + i] : -1;
+    }
+    if (k < static_cast<long long>(q.B) * q.gamma) {
+        const int b = static_cast<int>(k / q.gamma);
+        T_d[k] = q.Td_seq ? q.Td_seq[b] : q.Td;
+        tok_d[k] = q.tokens[k];
+    }
+}
+
+// G blocks per sequence race its raced row (fp32 logits in rows b of lt / ld).
+__global__ void __launch_bounds__(256, SPECVERIFY_RACE_MINBLOCKS) lmhead_race_kernel(VerifyParams p,
+                                                                                    const float* lt,
+                                                                                    const float* ld) {
+    __shared__ float s_thr[8];
+    __shared__ RaceState s_best[8];
+    __shared__ int s_last;
+    const int G = p.rgroups;
+    const int b = blockIdx.x / G, g = blockIdx.x % G;
+    const SeqInfo si = p.seq[b];
+    if (si.j < 0) return;
+    const bool residual = si.j < p.gamma;
+    race_rows_block<F32Elem>(p, b, lt + static_cast<long long>(b) * p.V,
+                             residual ? ld + static_cast<long long>(b) * p.V : nullptr, residual,
+                             static_cast<uint32_t>(si.j),
+                             p.out_tokens + static_cast<long long>(b) * (p.gamma + 1) + si.j, g,
+                             p.rpieces, G, g, G, si, s_thr, s_best, s_last);
+}
+
 }  // namespace specverify

@@ -900,6 +900,168 @@ int spec_lmhead_row_stats(const void* hidden, const void* weight, int rows, int 
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
 }
 
+int spec_verify_lmhead(const void* h_target, const void* w_target, const void* h_draft,
+                       const void* w_draft, const int32_t* draft_tokens, int B, int gamma, int V,
+                       int d, float T, float T_d, uint64_t seed, int32_t* out_tokens,
+                       int32_t* out_n_accepted, const spec_verify_opts* opts, void* stream) {
+    if (B < 0 || gamma < 0 || gamma > kMaxGamma) return SPEC_EINVAL;
+    int rc = lmhead_check(h_target, w_target, B * (gamma + 1), V, d);
+    if (rc) return rc;
+    if (B == 0) return SPEC_OK;
+    if (!out_tokens || !out_n_accepted) return SPEC_EINVAL;
+    if (gamma > 0) {
+        rc = lmhead_check(h_draft, w_draft, B * gamma, V, d);
+        if (rc) return rc;
+        if (!draft_tokens) return SPEC_EINVAL;
+    }
+    if (!(opts && opts->T_per_seq) && !good_temperature(T)) return SPEC_EINVAL;
+    if (!(opts && opts->Td_per_seq) && !good_temperature(T_d)) return SPEC_EINVAL;
+    const int rows_t = B * (gamma + 1), rows_d = B * gamma;
+    DeviceState* dev = nullptr;
+    LmHeadParams pt{}, pd{};
+    pt.rows = rows_t;
+    pd.rows = rows_d;
+    pt.V = pd.V = V;
+    pt.d = pd.d = d;
+    dim3 grid_t, grid_d;
+    const int rpieces = (V + kRaceBlockTokens - 1) / kRaceBlockTokens;
+    // workspace carve-up
+    size_t off = 0;
+    auto take = [&](size_t bytes) { const size_t o = off; off = align_up(off + bytes, 256); return o; };
+    char* ws = nullptr;
+    size_t o_Tt, o_tokt, o_partt, o_xt, o_Zt, o_pt, o_Td, o_tokd, o_partd, o_xd, o_Zd, o_qd, o_ht, o_hd,
+        o_lt, o_ld, o_seq, o_race, o_tick;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        rc = device_state(&dev);
+        if (rc) return rc;
+        lmhead_grid(rows_t, V, dev->sm_count, pt, grid_t);
+        if (rows_d) lmhead_grid(rows_d, V, dev->sm_count, pd, grid_d);
+        o_Tt = take(rows_t * sizeof(float));
+        o_tokt = take(rows_t * sizeof(int32_t));
+        o_partt = take(static_cast<size_t>(rows_t) * pt.nchunks * sizeof(float2));
+        o_xt = take(rows_t * sizeof(float));
+        o_Zt = take(rows_t * sizeof(float));
+        o_pt = take(rows_t * sizeof(float));
+        o_Td = take(rows_d * sizeof(float) + 4);
+        o_tokd = take(rows_d * sizeof(int32_t) + 4);
+        o_partd = take(static_cast<size_t>(rows_d) * pd.nchunks * sizeof(float2) + 8);
+        o_xd = take(rows_d * sizeof(float) + 4);
+        o_Zd = take(rows_d * sizeof(float) + 4);
+        o_qd = take(rows_d * sizeof(float) + 4);
+        o_ht = take(static_cast<size_t>(B) * d * 2);
+        o_hd = take(static_cast<size_t>(B) * d * 2);
+        o_lt = take(static_cast<size_t>(B) * V * sizeof(float));
+        o_ld = take(static_cast<size_t>(B) * V * sizeof(float));
+        o_seq = take(static_cast<size_t>(B) * sizeof(SeqInfo));
+        o_race = take(static_cast<size_t>(B) * rpieces * sizeof(RacePart));
+        o_tick = take(static_cast<size_t>(B) * sizeof(int));
+        rc = ensure_workspace(*dev, off);
+        if (rc) return rc;
+        ws = static_cast<char*>(dev->ws);
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    LmVerifyParams q{};
+    q.B = B;
+    q.gamma = gamma;
+    q.V = V;
+    q.d = d;
+    q.h_target = static_cast<const uint16_t*>(h_target);
+    q.h_draft = static_cast<const uint16_t*>(h_draft);
+    q.tokens = draft_tokens;
+    q.logZ_t = reinterpret_cast<float*>(ws + o_Zt);
+    q.logp_t = reinterpret_cast<float*>(ws + o_pt);
+    q.logZ_d = reinterpret_cast<float*>(ws + o_Zd);
+    q.logq_d = reinterpret_cast<float*>(ws + o_qd);
+    q.h_race_t = reinterpret_cast<uint16_t*>(ws + o_ht);
+    q.h_race_d = reinterpret_cast<uint16_t*>(ws + o_hd);
+    q.seq = reinterpret_cast<SeqInfo*>(ws + o_seq);
+    q.T = T;
+    q.Td = T_d;
+    q.T_seq = opts ? opts->T_per_seq : nullptr;
+    q.Td_seq = opts ? opts->Td_per_seq : nullptr;
+    q.key = philox_key(seed);
+    q.seq_base = opts ? opts->seq_index_base : 0u;
+    q.out_tokens = out_tokens;
+    q.out_n = out_n_accepted;
+    q.status = (opts && opts->d_status) ? opts->d_status : dev->status;
+    record(opts, 0, s);
+    {
+        const long long n = rows_t;
+        lmhead_rows_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(
+            q, reinterpret_cast<float*>(ws + o_Tt), reinterpret_cast<int32_t*>(ws + o_tokt),
+            reinterpret_cast<float*>(ws + o_Td), reinterpret_cast<int32_t*>(ws + o_tokd));
+    }
+    if (cudaMemsetAsync(ws + o_race, 0, static_cast<size_t>(B) * rpieces * sizeof(RacePart), s) != cudaSuccess ||
+        cudaMemsetAsync(ws + o_tick, 0, static_cast<size_t>(B) * sizeof(int), s) != cudaSuccess)
+        return SPEC_ECUDA;
+    // row statistics of the target rows (T_b) and the draft rows (Td_b), with the draft tokens
+    pt.T_row = reinterpret_cast<float*>(ws + o_Tt);
+    pt.token_row = reinterpret_cast<int32_t*>(ws + o_tokt);
+    pt.stat_parts = reinterpret_cast<float2*>(ws + o_partt);
+    pt.token_logit = reinterpret_cast<float*>(ws + o_xt);
+    pt.status = q.status;
+    rc = launch_lmhead<false>(h_target, w_target, pt, dev->sm_count, s);
+    if (rc) return rc;
+    lmhead_merge_kernel<<<(rows_t * 32 + 255) / 256, 256, 0, s>>>(pt, reinterpret_cast<float*>(ws + o_Zt),
+                                                                 reinterpret_cast<float*>(ws + o_pt));
+    if (rows_d) {
+        pd.T_row = reinterpret_cast<float*>(ws + o_Td);
+        pd.token_row = reinterpret_cast<int32_t*>(ws + o_tokd);
+        pd.stat_parts = reinterpret_cast<float2*>(ws + o_partd);
+        pd.token_logit = reinterpret_cast<float*>(ws + o_xd);
+        pd.status = q.status;
+        rc = launch_lmhead<false>(h_draft, w_draft, pd, dev->sm_count, s);
+        if (rc) return rc;
+        lmhead_merge_kernel<<<(rows_d * 32 + 255) / 256, 256, 0, s>>>(pd, reinterpret_cast<float*>(ws + o_Zd),
+                                                                     reinterpret_cast<float*>(ws + o_qd));
+    }
+    record(opts, 1, s);
+    lmhead_scan_kernel<<<(B * 32 + 255) / 256, 256, 0, s>>>(q);
+    // logits of the raced rows only
+    LmHeadParams rt{}, rd{};
+    rt.rows = rd.rows = B;
+    rt.V = rd.V = V;
+    rt.d = rd.d = d;
+    rt.logits = reinterpret_cast<float*>(ws + o_lt);
+    rd.logits = reinterpret_cast<float*>(ws + o_ld);
+    rt.status = rd.status = q.status;
+    rc = launch_lmhead<true>(q.h_race_t, w_target, rt, dev->sm_count, s);
+    if (rc) return rc;
+    if (gamma > 0) {
+        rc = launch_lmhead<true>(q.h_race_d, w_draft, rd, dev->sm_count, s);
+        if (rc) return rc;
+    }
+    record(opts, 2, s);
+    VerifyParams p{};
+    p.B = B;
+    p.gamma = gamma;
+    p.V = V;
+    p.key = q.key;
+    p.rk = philox_round_keys(q.key);
+    p.seq_base = q.seq_base;
+    p.seq = q.seq;
+    p.rpiece_len = kRaceBlockTokens;
+    p.rpieces = rpieces;
+    p.race_parts = reinterpret_cast<RacePart*>(ws + o_race);
+    p.tickets = reinterpret_cast<int*>(ws + o_tick);
+    p.status = q.status;
+    p.out_tokens = out_tokens;
+    p.out_n = out_n_accepted;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, lmhead_race_kernel, kThreads, 0) != cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    long long G = static_cast<long long>(dev->sm_count) * per_sm / B;
+    if (G > rpieces) G = rpieces;
+    if (G < 1) G = 1;
+    p.rgroups = static_cast<int>(G);
+    lmhead_race_kernel<<<static_cast<unsigned>(B * G), kThreads, 0, s>>>(
+        p, reinterpret_cast<float*>(ws + o_lt), reinterpret_cast<float*>(ws + o_ld));
+    record(opts, 3, s);
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
+}
+
 int spec_adaptive_k(const float* H_next, int B, int K, const double* centres,
                     const int32_t* candidates, int n_cand, double C_d, double C_v,
                     int32_t* out_k, double* out_eff, void* stream) {

@@ -26,7 +26,7 @@ EXPORTED = ("spec_verify", "spec_verify_greedy", "spec_verify_ex", "spec_verify_
             "spec_verify_workspace_bytes", "spec_verify_check", "spec_verify_strerror",
             "spec_verify_opts_init", "spec_verify_noalloc", "spec_row_entropy",
             "spec_adaptive_k", "spec_verify_tree", "spec_verify_host", "spec_lmhead_logits",
-            "spec_lmhead_row_stats")
+            "spec_lmhead_row_stats", "spec_verify_lmhead")
 
 
 class SpecVerifyError(RuntimeError):
@@ -91,6 +91,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.spec_verify_strerror.restype = ctypes.c_char_p
     lib.spec_verify_opts_init.argtypes = [OP]
     lib.spec_verify_opts_init.restype = None
+    lib.spec_verify_lmhead.argtypes = [P, P, P, P, P, I, I, I, I, F, F, U64, P, P, OP, P]
+    lib.spec_verify_lmhead.restype = ctypes.c_int
     lib.spec_lmhead_logits.argtypes = [P, P, I, I, I, P, P]
     lib.spec_lmhead_logits.restype = ctypes.c_int
     lib.spec_lmhead_row_stats.argtypes = [P, P, I, I, I, P, P, P, P, P]
@@ -385,6 +387,36 @@ def spec_lmhead_row_stats(hidden, weight, T_row, token_row=None, stream=None):
     if rc != SPEC_OK:
         raise SpecVerifyError(rc, "spec_lmhead_row_stats")
     return logz, logp
+
+
+def spec_verify_lmhead(h_target, w_target, h_draft, w_draft, draft_tokens, T: float, T_d: float,
+                       seed: int, out_tokens=None, out_n_accepted=None, *, T_per_seq=None,
+                       Td_per_seq=None, seq_index_base: int = 0, prof_events=None, stream=None):
+    """Sampling verify from hidden states (see ``spec_verify_lmhead`` in the C header):
+    h_target bf16 [B, gamma+1, d], w_target [V, d], h_draft [B, gamma, d], w_draft [V, d]."""
+    if h_target.dim() != 3 or h_target.dtype != torch.bfloat16 or not h_target.is_contiguous():
+        raise ValueError("h_target must be a contiguous bf16 tensor [B, gamma+1, d]")
+    B, G1, d = h_target.shape
+    g = G1 - 1
+    V = w_target.shape[0]
+    for name, t, shape in (("w_target", w_target, (V, d)), ("h_draft", h_draft, (B, g, d)),
+                           ("w_draft", w_draft, (V, d))):
+        if g == 0 and name != "w_target":
+            continue
+        if tuple(t.shape) != shape or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 tensor {shape}")
+    dev = h_target.device
+    out_tokens, out_n_accepted = _outputs(h_target, B, g, out_tokens, out_n_accepted)
+    T_per_seq = _check_temps(T_per_seq, B, dev, "T_per_seq")
+    Td_per_seq = _check_temps(Td_per_seq, B, dev, "Td_per_seq")
+    o = _make_opts(SPEC_BF16, T_per_seq, Td_per_seq, seq_index_base, None, None, None, prof_events)
+    rc = load_library().spec_verify_lmhead(
+        _ptr(h_target), _ptr(w_target), _ptr(h_draft) if g else None, _ptr(w_draft) if g else None,
+        _ptr(draft_tokens) if g else None, B, g, V, d, float(T), float(T_d), int(seed) & (2**64 - 1),
+        _ptr(out_tokens), _ptr(out_n_accepted), ctypes.byref(o), _stream_handle(stream, dev))
+    if rc != SPEC_OK:
+        raise SpecVerifyError(rc, "spec_verify_lmhead")
+    return out_tokens, out_n_accepted
 
 
 class Tree:

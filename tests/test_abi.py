@@ -35,7 +35,7 @@ def test_header_declares_the_boundary():
               "spec_verify_workspace_bytes", "spec_verify_check", "spec_verify_strerror",
               "spec_verify_opts_init", "spec_verify_noalloc", "spec_row_entropy", "spec_adaptive_k",
               "spec_verify_tree", "spec_verify_host", "spec_lmhead_logits",
-              "spec_lmhead_row_stats"):
+              "spec_lmhead_row_stats", "spec_verify_lmhead"):
         assert f in names
 
 

@@ -84,3 +84,48 @@ def test_lmhead_argument_checks(sv):
     with pytest.raises(sv.SpecVerifyError) as e:
         sv.spec_lmhead_logits(h, w)
     assert e.value.code == sv.SPEC_EINVAL
+
+
+def lmhead_workload(B, gamma, V, d, seed, sigma=0.3, scale=1.0):
+    """Hidden states and heads for a verify from hidden states: draft states are the
+    target's plus noise, the draft head the target's plus noise; draft tokens drawn from
+    the draft logits (computed here in fp64 from the bf16 inputs) at T_d."""
+    rng = np.random.default_rng(seed)
+    ht32 = (rng.standard_normal((B, gamma + 1, d)) * scale).astype(np.float32)
+    wt32 = (rng.standard_normal((V, d)) / np.sqrt(d) * 6).astype(np.float32)
+    hd32 = (ht32[:, :gamma] + rng.standard_normal((B, gamma, d)) * sigma).astype(np.float32)
+    wd32 = (wt32 + rng.standard_normal((V, d)) / np.sqrt(d) * sigma).astype(np.float32)
+    ht, wt, hd, wd = (workloads.to_bf16_bits(a) for a in (ht32, wt32, hd32, wd32))
+    return ht, wt, hd, wd
+
+
+@pytest.mark.parametrize("B,gamma,V,d,T,Td", [(4, 3, 4096, 128, 1.0, 0.5), (8, 5, 10000, 256, 0.8, 0.4),
+                                               (3, 0, 2048, 64, 1.0, 1.0), (64, 8, 32000, 256, 1.0, 0.5)])
+def test_verify_from_hidden_states_matches_oracle(sv, B, gamma, V, d, T, Td):
+    """The fused verify equals the oracle run on the logits the tensor cores compute (the
+    same GEMM: spec_lmhead_logits) under the usual parity rules, and the logits path on
+    those logits."""
+    from _parity import compare_sampling
+    ht, wt, hd, wd = lmhead_workload(B, gamma, V, d, seed=B * 100 + V)
+    dev = torch.device("cuda")
+    Ht, Wt, Hd, Wd = (to_dev(a) for a in (ht, wt, hd, wd))
+    lt = sv.spec_lmhead_logits(Ht.reshape(B * (gamma + 1), d), Wt).reshape(B, gamma + 1, V)
+    ld = (sv.spec_lmhead_logits(Hd.reshape(B * gamma, d), Wd).reshape(B, gamma, V) if gamma
+          else torch.empty((B, 0, V), dtype=torch.float32, device=dev))
+    torch.cuda.synchronize()
+    lt_np, ld_np = lt.cpu().numpy(), ld.cpu().numpy()
+    rng = np.random.default_rng(7)
+    tok = np.zeros((B, gamma), np.int32)
+    for b in range(B):
+        if gamma:
+            tok[b] = workloads.draw_drafts(rng, ld_np[b], Td)
+    dtok = torch.from_numpy(tok).to(dev)
+    w = workloads.Workload("lmhead", B, gamma, V, "f32", lt_np, ld_np, tok,
+                           np.full(B, T, np.float32), np.full(B, Td, np.float32))
+    orc = oracle.get()
+    for seed in range(3):
+        t, n = sv.spec_verify_lmhead(Ht, Wt, Hd if gamma else None, Wd if gamma else None, dtok, T, Td, seed)
+        torch.cuda.synchronize()
+        assert sv.spec_verify_check() == sv.SPEC_OK
+        g = {"tokens": t.cpu().numpy(), "n": n.cpu().numpy()}
+        compare_sampling(w, g, orc.verify(lt_np, ld_np, tok, w.T, w.Td, seed))
