@@ -497,6 +497,49 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_lmhead(sv, dev, B, gamma, V, d, steps=10):
+    """Time the verify from hidden states (spec_verify_lmhead) and the unfused pipeline on
+    seeded random bf16 hidden states and heads."""
+    import torch
+    g = torch.Generator(device=dev).manual_seed(0)
+    ht = torch.randn((B, gamma + 1, d), generator=g, device=dev).to(torch.bfloat16)
+    hd = (ht[:, :gamma].float() + 0.3 * torch.randn((B, gamma, d), generator=g, device=dev)).to(torch.bfloat16)
+    wt = (torch.randn((V, d), generator=g, device=dev) * (6.0 / d ** 0.5)).to(torch.bfloat16)
+    wd = (wt.float() + torch.randn((V, d), generator=g, device=dev) * (0.3 / d ** 0.5)).to(torch.bfloat16)
+    tok = torch.randint(0, V, (B, gamma), generator=g, device=dev, dtype=torch.int32)
+    out_t = torch.empty((B, gamma + 1), dtype=torch.int32, device=dev)
+    out_n = torch.empty((B,), dtype=torch.int32, device=dev)
+
+    def fused():
+        sv.spec_verify_lmhead(ht, wt, hd, wd, tok, 1.0, 0.2, 0, out_t, out_n)
+
+    def unfused():
+        lt = torch.matmul(ht.reshape(-1, d), wt.t()).reshape(B, gamma + 1, V)
+        ld = torch.matmul(hd.reshape(-1, d), wd.t()).reshape(B, gamma, V)
+        sv.spec_verify_ex(lt, ld, tok, 1.0, 0.2, 0, out_t, out_n)
+
+    def timeit(fn):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record()
+        for _ in range(steps):
+            fn()
+        s1.record()
+        torch.cuda.synchronize()
+        return s0.elapsed_time(s1) / steps
+
+    fms = timeit(fused)
+    status = sv.spec_verify_check()
+    ums = timeit(unfused)
+    rows = B * (gamma + 1)
+    flops = 2.0 * B * (2 * gamma + 1) * V * d
+    return {"fused_ms": fms, "unfused_ms": ums, "rows_per_s": rows / (fms / 1e3),
+            "unfused_rows_per_s": rows / (ums / 1e3), "tflops": flops / (fms / 1e3) / 1e12,
+            "status": status}
+
+
 def run_table(args):
     """Every named workload, both sampling paths (fused single kernel, three kernels) and the
     greedy mode, as a table on stderr.  Workloads smaller than twice L2 are timed twice: on
@@ -588,6 +631,15 @@ def run_table(args):
             rows_out.append((tw.name, f"tree (emits {emitted:.1f} tokens/seq)",
                              "warm" if warm else ("cold" if copies > 1 else "> L2"), us,
                              tw.rows() / us * 1e6, nbytes / us / 1e3, sv.spec_verify_check()))
+    # the verify from hidden states (fused LM head, tensor cores) at the throughput shape,
+    # against the unfused pipeline: the library GEMM (torch.matmul: cuBLAS) writing bf16
+    # logits, then the logits verify reading them
+    lm = run_lmhead(sv, dev, B=256, gamma=12, V=152064, d=4096)
+    print("| verify from hidden states, B=256 gamma=12 V=152064 d=4096 | fused LM head "
+          f"(tensor cores) | - | {lm['fused_ms'] * 1e3:.0f} | {lm['rows_per_s']:.3e} | "
+          f"GEMM {lm['tflops']:.0f} TFLOP/s | {lm['status']} |", file=sys.stderr)
+    print("| same | cuBLAS bf16 logits + logits verify | - | "
+          f"{lm['unfused_ms'] * 1e3:.0f} | {lm['unfused_rows_per_s']:.3e} | - | 0 |", file=sys.stderr)
     print("| workload | path | L2 | us/call | rows/s | GB/s (one read of the logits) | status |",
           file=sys.stderr)
     print("|---|---|---|---|---|---|---|", file=sys.stderr)
@@ -609,12 +661,24 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--lmhead", action="store_true",
+                    help="time the verify from hidden states (fused LM head) only, to stderr")
+    ap.add_argument("--lm-steps", type=int, default=10)
     ap.add_argument("--all", action="store_true",
                     help="print a per-workload table (both sampling paths, greedy) to stderr")
     ap.add_argument("--ref-seqs", type=int, default=1,
                     help="sequences per reference step (one throughput-workload sequence is\n"
                          "about 0.04 s of oracle work)")
     args = ap.parse_args()
+    if args.lmhead:
+        import torch
+        import speculative_decoding_verification_31_gb300 as sv
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        sv.load_library()
+        print(json.dumps(run_lmhead(sv, dev, B=256, gamma=12, V=152064, d=4096,
+                                    steps=args.lm_steps)), file=sys.stderr)
+        return
     if args.all:
         run_table(args)
         return

@@ -148,23 +148,39 @@ __device__ __forceinline__ void tmem_load32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-struct LmHeadParams {
-    int rows, V, d;               // L = H W^T: H [rows, d], W [V, d]
-    int tiles_per_cta;            // vocabulary tiles of one CTA (its chunk)
-    int nchunks;                  // chunks per row: ceil(V / (kGemmBN * tiles_per_cta))
-    float* logits;                // [rows, V] fp32 output (spec_lmhead_logits), or nullptr
-    // statistics epilogue
-    const float* T_row;           // [rows] temperature of each row
+// One product of a launch: rows of H against W, with its epilogue outputs.
+struct LmHeadPart {
+    int rows;                     // rows of H (0: the part is absent)
+    float* logits;                // [rows, V] fp32 output (logits epilogue), or nullptr
+    const float* T_row;           // [rows] temperature of each row (statistics epilogue)
     const int32_t* token_row;     // [rows] token whose logit to keep (-1: none), or nullptr
     float2* stat_parts;           // [rows][nchunks] (scaled max, sum) in base 2
     float* token_logit;           // [rows] logit at token_row (raw, before 1/T)
+};
+
+// A launch computes up to two products with the same V and d (the target rows against the
+// target head and the draft rows against the draft head): grid rows [0, m_tiles0) are
+// part 0's row tiles, the rest part 1's, so both share one wave of CTAs.
+struct LmHeadParams {
+    int V, d;
+    int tiles_per_cta;            // vocabulary tiles of one CTA (its chunk)
+    int nchunks;                  // chunks per row: ceil(V / (kGemmBN * tiles_per_cta))
+    int m_tiles0;                 // row tiles of part 0
+    LmHeadPart part[2];
     int32_t* status;
+    // single-part views used by the merge kernel
+    int rows;
+    const float* T_row;
+    const int32_t* token_row;
+    float2* stat_parts;
+    float* token_logit;
 };
 
 // kLogits: write the logits; otherwise the statistics epilogue.
 template <bool kLogits>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-lmhead_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w,
+lmhead_kernel(const __grid_constant__ CUtensorMap map_h0, const __grid_constant__ CUtensorMap map_w0,
+              const __grid_constant__ CUtensorMap map_h1, const __grid_constant__ CUtensorMap map_w1,
               LmHeadParams p) {
     extern __shared__ uint8_t gemm_smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(gemm_smem_raw) + 1023) &
@@ -181,7 +197,11 @@ lmhead_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__
     volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m_tile = blockIdx.y;
+    const bool second = static_cast<int>(blockIdx.y) >= p.m_tiles0;
+    const LmHeadPart& part = p.part[second ? 1 : 0];
+    const CUtensorMap* map_h = second ? &map_h1 : &map_h0;
+    const CUtensorMap* map_w = second ? &map_w1 : &map_w0;
+    const int m_tile = second ? static_cast<int>(blockIdx.y) - p.m_tiles0 : static_cast<int>(blockIdx.y);
     const int chunk = blockIdx.x;
     const int n_tiles_total = (p.V + kGemmBN - 1) / kGemmBN;
     const int t_begin = chunk * p.tiles_per_cta;
@@ -228,9 +248,9 @@ lmhead_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__
                         break;
                     }
                     mbar_expect_tx(full + stage, kGemmStageA + kGemmStageB);
-                    tma_load_2d(&map_h, full + stage, stage_a + stage * kGemmStageA, kb * kGemmBK,
+                    tma_load_2d(map_h, full + stage, stage_a + stage * kGemmStageA, kb * kGemmBK,
                                 m_tile * kGemmBM);
-                    tma_load_2d(&map_w, full + stage, stage_b + stage * kGemmStageB, kb * kGemmBK, n0);
+                    tma_load_2d(map_w, full + stage, stage_b + stage * kGemmStageB, kb * kGemmBK, n0);
                     ++issued;
                     if (++stage == kGemmStages) {
                         stage = 0;
@@ -295,12 +315,12 @@ lmhead_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__
         // ---- epilogue: warps 2..5, TMEM lane slice (warp % 4) * 32 ----
         const int slice = warp & 3;
         const int row = m_tile * kGemmBM + slice * 32 + lane;
-        const bool row_ok = row < p.rows;
+        const bool row_ok = row < part.rows;
         float c = 1.0f;
         int tok = -1;
         if (!kLogits && row_ok) {
-            c = kLog2e / p.T_row[row];
-            if (p.token_row) tok = p.token_row[row];
+            c = kLog2e / part.T_row[row];
+            if (part.token_row) tok = part.token_row[row];
         }
         float m = -FLT_MAX, s = 0.0f, xtok = 0.0f;
         for (int t = 0; t < ntiles; ++t) {
@@ -329,10 +349,16 @@ lmhead_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__
                 const int col0 = n0 + c32 * 32;
                 if (kLogits) {
                     if (row_ok) {
-                        float* dst = p.logits + static_cast<long long>(row) * p.V + col0;
+                        float* dst = part.logits + static_cast<long long>(row) * p.V + col0;
+                        if (col0 + 32 <= p.V && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (col0 + i < p.V) dst[i] = v[i];
+                            for (int i = 0; i < 32; i += 4)
+                                *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                if (col0 + i < p.V) dst[i] = v[i];
+                        }
                     }
                 } else {
                     float bmax = -INFINITY;
@@ -358,9 +384,9 @@ lmhead_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__
             if (lane == 0) mbar_arrive(tempty + acc);
         }
         if (!kLogits && row_ok && !*abort) {
-            store_stat(p.stat_parts + static_cast<long long>(row) * p.nchunks + chunk, m, s);
-            if (tok >= t_begin * kGemmBN && tok < t_end * kGemmBN && tok < p.V && p.token_logit)
-                p.token_logit[row] = xtok;
+            store_stat(part.stat_parts + static_cast<long long>(row) * p.nchunks + chunk, m, s);
+            if (tok >= t_begin * kGemmBN && tok < t_end * kGemmBN && tok < p.V && part.token_logit)
+                part.token_logit[row] = xtok;
         }
         if (*abort && lane == 0) set_status(p.status, 4 /* SPEC_ETIMEOUT */);
     }

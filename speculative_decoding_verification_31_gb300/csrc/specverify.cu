@@ -776,34 +776,58 @@ int lmhead_check(const void* H, const void* W, int rows, int V, int d) {
     return SPEC_OK;
 }
 
-// Grid of the LM-head kernel: one row tile per grid row, the vocabulary tiles split into
-// chunks so that the CTAs fill the GPU about once (one CTA per SM: it holds 512 TMEM
-// columns and 193 KB of shared memory).
-void lmhead_grid(int rows, int V, int sm_count, LmHeadParams& lp, dim3& grid) {
-    const int m_tiles = (rows + kGemmBM - 1) / kGemmBM;
+// Grid of the LM-head kernel: one grid row per row tile (of both parts), the vocabulary
+// tiles split into chunks so that the CTAs fill the GPU about once (one CTA per SM: each
+// holds 512 TMEM columns and 193 KB of shared memory).  The CTAs of one chunk sweep the same
+// head tiles in step, so each head is read from HBM about once.
+void lmhead_grid(int rows0, int rows1, int V, int sm_count, LmHeadParams& lp, dim3& grid) {
+    const int m0 = (rows0 + kGemmBM - 1) / kGemmBM, m1 = (rows1 + kGemmBM - 1) / kGemmBM;
     const int n_tiles = (V + kGemmBN - 1) / kGemmBN;
-    long long want = sm_count / m_tiles;  // chunks per row tile
+    long long want = sm_count / std::max(1, m0 + m1);  // chunks per row tile
     if (want < 1) want = 1;
     if (want > n_tiles) want = n_tiles;
     lp.tiles_per_cta = static_cast<int>((n_tiles + want - 1) / want);
     lp.nchunks = (n_tiles + lp.tiles_per_cta - 1) / lp.tiles_per_cta;
-    grid = dim3(static_cast<unsigned>(lp.nchunks), static_cast<unsigned>(m_tiles));
+    lp.m_tiles0 = m0;
+    grid = dim3(static_cast<unsigned>(lp.nchunks), static_cast<unsigned>(m0 + m1));
 }
 
+// Launch part 0 = (H0, W0) and, if lp.part[1].rows > 0, part 1 = (H1, W1) in one grid.
 template <bool kLogits>
-int launch_lmhead(const void* H, const void* W, LmHeadParams& lp, int sm_count, cudaStream_t s) {
-    CUtensorMap mh, mw;
-    int rc = bf16_tensor_map(&mh, H, lp.rows, lp.d, kGemmBM);
+int launch_lmhead(const void* H0, const void* W0, const void* H1, const void* W1, LmHeadParams& lp,
+                  int sm_count, cudaStream_t s) {
+    CUtensorMap mh0, mw0, mh1, mw1;
+    int rc = bf16_tensor_map(&mh0, H0, lp.part[0].rows, lp.d, kGemmBM);
     if (rc) return rc;
-    rc = bf16_tensor_map(&mw, W, lp.V, lp.d, kGemmBN);
+    rc = bf16_tensor_map(&mw0, W0, lp.V, lp.d, kGemmBN);
     if (rc) return rc;
+    if (lp.part[1].rows > 0) {
+        rc = bf16_tensor_map(&mh1, H1, lp.part[1].rows, lp.d, kGemmBM);
+        if (rc) return rc;
+        rc = bf16_tensor_map(&mw1, W1, lp.V, lp.d, kGemmBN);
+        if (rc) return rc;
+    } else {
+        mh1 = mh0;
+        mw1 = mw0;
+    }
     dim3 grid;
-    lmhead_grid(lp.rows, lp.V, sm_count, lp, grid);
+    lmhead_grid(lp.part[0].rows, lp.part[1].rows, lp.V, sm_count, lp, grid);
     auto kernel = lmhead_kernel<kLogits>;
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem) != cudaSuccess)
         return SPEC_ECUDA;
-    kernel<<<grid, kGemmThreads, kGemmSmem, s>>>(mh, mw, lp);
+    kernel<<<grid, kGemmThreads, kGemmSmem, s>>>(mh0, mw0, mh1, mw1, lp);
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
+}
+
+// The merge kernel's view of one part.
+LmHeadParams part_view(const LmHeadParams& lp, int k) {
+    LmHeadParams v = lp;
+    v.rows = lp.part[k].rows;
+    v.T_row = lp.part[k].T_row;
+    v.token_row = lp.part[k].token_row;
+    v.stat_parts = lp.part[k].stat_parts;
+    v.token_logit = lp.part[k].token_logit;
+    return v;
 }
 
 }  // namespace
@@ -822,12 +846,13 @@ int spec_lmhead_logits(const void* hidden, const void* weight, int rows, int V, 
         if (rc) return rc;
     }
     LmHeadParams lp{};
-    lp.rows = rows;
     lp.V = V;
     lp.d = d;
-    lp.logits = out_logits;
+    lp.part[0].rows = rows;
+    lp.part[0].logits = out_logits;
     lp.status = dev->status;
-    return launch_lmhead<true>(hidden, weight, lp, dev->sm_count, static_cast<cudaStream_t>(stream));
+    return launch_lmhead<true>(hidden, weight, nullptr, nullptr, lp, dev->sm_count,
+                               static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"
@@ -871,15 +896,15 @@ int spec_lmhead_row_stats(const void* hidden, const void* weight, int rows, int 
     DeviceState* dev = nullptr;
     char* ws = nullptr;
     LmHeadParams lp{};
-    lp.rows = rows;
     lp.V = V;
     lp.d = d;
+    lp.part[0].rows = rows;
     dim3 grid;
     {
         std::lock_guard<std::mutex> lock(g_mu);
         rc = device_state(&dev);
         if (rc) return rc;
-        lmhead_grid(rows, V, dev->sm_count, lp, grid);
+        lmhead_grid(rows, 0, V, dev->sm_count, lp, grid);
         // workspace: [rows][nchunks] partials, then [rows] token logits
         const size_t need = align_up(static_cast<size_t>(rows) * lp.nchunks * sizeof(float2), 256) +
                             align_up(static_cast<size_t>(rows) * sizeof(float), 256);
@@ -887,16 +912,16 @@ int spec_lmhead_row_stats(const void* hidden, const void* weight, int rows, int 
         if (rc) return rc;
         ws = static_cast<char*>(dev->ws);
     }
-    lp.T_row = T_row;
-    lp.token_row = token_row;
-    lp.stat_parts = reinterpret_cast<float2*>(ws);
-    lp.token_logit = reinterpret_cast<float*>(
+    lp.part[0].T_row = T_row;
+    lp.part[0].token_row = token_row;
+    lp.part[0].stat_parts = reinterpret_cast<float2*>(ws);
+    lp.part[0].token_logit = reinterpret_cast<float*>(
         ws + align_up(static_cast<size_t>(rows) * lp.nchunks * sizeof(float2), 256));
     lp.status = dev->status;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    rc = launch_lmhead<false>(hidden, weight, lp, dev->sm_count, s);
+    rc = launch_lmhead<false>(hidden, weight, nullptr, nullptr, lp, dev->sm_count, s);
     if (rc) return rc;
-    lmhead_merge_kernel<<<(rows * 32 + 255) / 256, 256, 0, s>>>(lp, out_logZ, out_logp_token);
+    lmhead_merge_kernel<<<(rows * 32 + 255) / 256, 256, 0, s>>>(part_view(lp, 0), out_logZ, out_logp_token);
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
 }
 
@@ -918,12 +943,12 @@ int spec_verify_lmhead(const void* h_target, const void* w_target, const void* h
     if (!(opts && opts->Td_per_seq) && !good_temperature(T_d)) return SPEC_EINVAL;
     const int rows_t = B * (gamma + 1), rows_d = B * gamma;
     DeviceState* dev = nullptr;
-    LmHeadParams pt{}, pd{};
-    pt.rows = rows_t;
-    pd.rows = rows_d;
-    pt.V = pd.V = V;
-    pt.d = pd.d = d;
-    dim3 grid_t, grid_d;
+    LmHeadParams ps{};  // statistics: part 0 the target rows, part 1 the draft rows
+    ps.V = V;
+    ps.d = d;
+    ps.part[0].rows = rows_t;
+    ps.part[1].rows = rows_d;
+    dim3 grid_s;
     const int rpieces = (V + kRaceBlockTokens - 1) / kRaceBlockTokens;
     // workspace carve-up
     size_t off = 0;
@@ -935,24 +960,23 @@ int spec_verify_lmhead(const void* h_target, const void* w_target, const void* h
         std::lock_guard<std::mutex> lock(g_mu);
         rc = device_state(&dev);
         if (rc) return rc;
-        lmhead_grid(rows_t, V, dev->sm_count, pt, grid_t);
-        if (rows_d) lmhead_grid(rows_d, V, dev->sm_count, pd, grid_d);
+        lmhead_grid(rows_t, rows_d, V, dev->sm_count, ps, grid_s);
         o_Tt = take(rows_t * sizeof(float));
         o_tokt = take(rows_t * sizeof(int32_t));
-        o_partt = take(static_cast<size_t>(rows_t) * pt.nchunks * sizeof(float2));
+        o_partt = take(static_cast<size_t>(rows_t) * ps.nchunks * sizeof(float2));
         o_xt = take(rows_t * sizeof(float));
         o_Zt = take(rows_t * sizeof(float));
         o_pt = take(rows_t * sizeof(float));
         o_Td = take(rows_d * sizeof(float) + 4);
         o_tokd = take(rows_d * sizeof(int32_t) + 4);
-        o_partd = take(static_cast<size_t>(rows_d) * pd.nchunks * sizeof(float2) + 8);
+        o_partd = take(static_cast<size_t>(rows_d) * ps.nchunks * sizeof(float2) + 8);
         o_xd = take(rows_d * sizeof(float) + 4);
         o_Zd = take(rows_d * sizeof(float) + 4);
         o_qd = take(rows_d * sizeof(float) + 4);
         o_ht = take(static_cast<size_t>(B) * d * 2);
         o_hd = take(static_cast<size_t>(B) * d * 2);
         o_lt = take(static_cast<size_t>(B) * V * sizeof(float));
-        o_ld = take(static_cast<size_t>(B) * V * sizeof(float));
+        o_ld = take(static_cast<size_t>(B) * V * sizeof(float));  // (unused when gamma = 0)
         o_seq = take(static_cast<size_t>(B) * sizeof(SeqInfo));
         o_race = take(static_cast<size_t>(B) * rpieces * sizeof(RacePart));
         o_tick = take(static_cast<size_t>(B) * sizeof(int));
@@ -995,43 +1019,37 @@ int spec_verify_lmhead(const void* h_target, const void* w_target, const void* h
     if (cudaMemsetAsync(ws + o_race, 0, static_cast<size_t>(B) * rpieces * sizeof(RacePart), s) != cudaSuccess ||
         cudaMemsetAsync(ws + o_tick, 0, static_cast<size_t>(B) * sizeof(int), s) != cudaSuccess)
         return SPEC_ECUDA;
-    // row statistics of the target rows (T_b) and the draft rows (Td_b), with the draft tokens
-    pt.T_row = reinterpret_cast<float*>(ws + o_Tt);
-    pt.token_row = reinterpret_cast<int32_t*>(ws + o_tokt);
-    pt.stat_parts = reinterpret_cast<float2*>(ws + o_partt);
-    pt.token_logit = reinterpret_cast<float*>(ws + o_xt);
-    pt.status = q.status;
-    rc = launch_lmhead<false>(h_target, w_target, pt, dev->sm_count, s);
+    // row statistics of the target rows (T_b) and the draft rows (Td_b), with the draft
+    // tokens, in one launch
+    ps.part[0].T_row = reinterpret_cast<float*>(ws + o_Tt);
+    ps.part[0].token_row = reinterpret_cast<int32_t*>(ws + o_tokt);
+    ps.part[0].stat_parts = reinterpret_cast<float2*>(ws + o_partt);
+    ps.part[0].token_logit = reinterpret_cast<float*>(ws + o_xt);
+    ps.part[1].T_row = reinterpret_cast<float*>(ws + o_Td);
+    ps.part[1].token_row = reinterpret_cast<int32_t*>(ws + o_tokd);
+    ps.part[1].stat_parts = reinterpret_cast<float2*>(ws + o_partd);
+    ps.part[1].token_logit = reinterpret_cast<float*>(ws + o_xd);
+    ps.status = q.status;
+    rc = launch_lmhead<false>(h_target, w_target, h_draft, w_draft, ps, dev->sm_count, s);
     if (rc) return rc;
-    lmhead_merge_kernel<<<(rows_t * 32 + 255) / 256, 256, 0, s>>>(pt, reinterpret_cast<float*>(ws + o_Zt),
+    lmhead_merge_kernel<<<(rows_t * 32 + 255) / 256, 256, 0, s>>>(part_view(ps, 0), reinterpret_cast<float*>(ws + o_Zt),
                                                                  reinterpret_cast<float*>(ws + o_pt));
-    if (rows_d) {
-        pd.T_row = reinterpret_cast<float*>(ws + o_Td);
-        pd.token_row = reinterpret_cast<int32_t*>(ws + o_tokd);
-        pd.stat_parts = reinterpret_cast<float2*>(ws + o_partd);
-        pd.token_logit = reinterpret_cast<float*>(ws + o_xd);
-        pd.status = q.status;
-        rc = launch_lmhead<false>(h_draft, w_draft, pd, dev->sm_count, s);
-        if (rc) return rc;
-        lmhead_merge_kernel<<<(rows_d * 32 + 255) / 256, 256, 0, s>>>(pd, reinterpret_cast<float*>(ws + o_Zd),
+    if (rows_d)
+        lmhead_merge_kernel<<<(rows_d * 32 + 255) / 256, 256, 0, s>>>(part_view(ps, 1), reinterpret_cast<float*>(ws + o_Zd),
                                                                      reinterpret_cast<float*>(ws + o_qd));
-    }
     record(opts, 1, s);
     lmhead_scan_kernel<<<(B * 32 + 255) / 256, 256, 0, s>>>(q);
-    // logits of the raced rows only
-    LmHeadParams rt{}, rd{};
-    rt.rows = rd.rows = B;
-    rt.V = rd.V = V;
-    rt.d = rd.d = d;
-    rt.logits = reinterpret_cast<float*>(ws + o_lt);
-    rd.logits = reinterpret_cast<float*>(ws + o_ld);
-    rt.status = rd.status = q.status;
-    rc = launch_lmhead<true>(q.h_race_t, w_target, rt, dev->sm_count, s);
+    // logits of the raced rows only (target row j; draft row j of the residuals), one launch
+    LmHeadParams pr{};
+    pr.V = V;
+    pr.d = d;
+    pr.part[0].rows = B;
+    pr.part[0].logits = reinterpret_cast<float*>(ws + o_lt);
+    pr.part[1].rows = gamma > 0 ? B : 0;
+    pr.part[1].logits = reinterpret_cast<float*>(ws + o_ld);
+    pr.status = q.status;
+    rc = launch_lmhead<true>(q.h_race_t, w_target, q.h_race_d, w_draft, pr, dev->sm_count, s);
     if (rc) return rc;
-    if (gamma > 0) {
-        rc = launch_lmhead<true>(q.h_race_d, w_draft, rd, dev->sm_count, s);
-        if (rc) return rc;
-    }
     record(opts, 2, s);
     VerifyParams p{};
     p.B = B;
