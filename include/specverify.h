@@ -114,8 +114,10 @@ typedef struct {
 } spec_verify_opts;
 
 /* flags bits. */
-#define SPEC_FLAG_FUSED 1u        /* sampling: one persistent cooperative kernel instead of the
-                                     default two kernels (same outputs, bit for bit) */
+#define SPEC_FLAG_FUSED 1u        /* sampling: one persistent cooperative kernel (after a small
+                                     kernel that zeroes its control words) instead of the
+                                     default two kernels; same outputs, bit for bit, but
+                                     slower on GB300 at every size measured */
 #define SPEC_DEBUG_NEVER_READY 2u /* tests only, with SPEC_FLAG_FUSED: the race waits on a flag
                                      that is never set, give up after their bounded wait and
                                      report SPEC_ETIMEOUT (outputs are then invalid) */
@@ -209,7 +211,7 @@ const char *spec_verify_strerror(int status);
  * the problem exceeds SPEC_NOALLOC_SCRATCH_BYTES - 256; otherwise as spec_verify_ex.
  */
 #define SPEC_NOALLOC_SCRATCH_BYTES (8u << 20) /* 8 MiB: B=256, gamma=12, V=152064 bf16 needs
-                                                 4.3 MB */
+                                                 6.6 MB */
 int spec_verify_noalloc(const void *target_logits, const void *draft_logits,
                         const int32_t *draft_tokens, int B, int gamma, int V, float T, float T_d,
                         uint64_t seed, int32_t *out_tokens, int32_t *out_n_accepted,

@@ -89,9 +89,12 @@ struct SoftmaxStat {
     float m, s;
 };
 
+// Symmetric in a and b, with every rounding explicit (no contraction into an FMA, whose
+// choice of product could differ between call sites): every lane of a butterfly ends with the
+// same bits, and so does every kernel that merges the same partials in the same order.
 __device__ __forceinline__ SoftmaxStat merge_stat(SoftmaxStat a, SoftmaxStat b) {
     const float M = fmaxf(a.m, b.m);
-    return SoftmaxStat{M, a.s * ex2_fast(a.m - M) + b.s * ex2_fast(b.m - M)};
+    return SoftmaxStat{M, __fadd_rn(__fmul_rn(a.s, ex2_fast(a.m - M)), __fmul_rn(b.s, ex2_fast(b.m - M)))};
 }
 
 __device__ __forceinline__ SoftmaxStat warp_merge_stat(SoftmaxStat v) {

@@ -1,19 +1,23 @@
 // kernels.cuh -- the verify step's CUDA kernels (sm_103a).
 //
-// Sampling mode runs three kernels on the caller's stream:
+// Sampling mode, default schedule: two kernels on the caller's stream.
 //   row_stats   one pass over every target and draft logit: per (row, piece) partial
 //               softmax statistics of p at T and q at T_d (max and sum of exponentials);
-//   scan        one block per sequence: merge the partials into ln Z per row, gather
+//   scan_race   G blocks per sequence: merge the partials into ln Z per row, gather
 //               p_i(d_i) and q_i(d_i), draw u_i and find the first rejection j
-//               ("How speculative decoding makes LLMs go brrr": pseudocode and module 3);
-//   race        one pass over the one row each sequence still needs -- target and draft row
-//               j for the residual max(0, p_j - q_j), or target row gamma for the bonus
-//               token -- as an exponential race; the last warp to finish a sequence merges
-//               the pieces and writes the token.
+//               ("How speculative decoding makes LLMs go brrr": pseudocode and module 3),
+//               then race the one row each sequence still needs -- target and draft row j
+//               for the residual max(0, p_j - q_j), or target row gamma for the bonus token
+//               -- as an exponential race; the last block of a sequence merges the winners
+//               and writes the token.
+// Other schedules of the same computation: the flow kernel (flow.cuh: one persistent launch
+// whose races overlap the streaming of later sequences), the early-exit kernel (below: reads
+// rows only up to each sequence's first rejection), pair_stats (the streaming pass with
+// per-position entropies and KL), and the token-tree kernels.
 // Greedy mode runs row_argmax (first argmax per (row, piece)) and scan_greedy.
 //
-// Work is split into warp-sized items (one row piece each) taken round-robin by every warp
-// of a grid sized to the GPU, so that no item ever waits for another.
+// Streaming work is split into warp-sized items (one row piece each) taken round-robin by
+// every warp of a grid sized to the GPU, so that no item ever waits for another.
 #pragma once
 
 #include <cfloat>
@@ -43,6 +47,19 @@ struct RacePart {
     int pad;
 };
 
+// The flow path's workspace region (verify_flow_kernel): every word means "nothing yet" when
+// zero, and the region is zeroed before each call.
+struct FlowRegion {
+    unsigned long long* cursors;  // [0]: row items claimed, [16]: race units claimed (own lines)
+    int* items;                   // [B] row items of sequence b streamed
+    int* ready;                   // [B] 1 once sequence b's scan is published
+    int* tickets;                 // [B] race units of sequence b finished
+    unsigned long long* race;     // [B][units] packed unit winners (score bits | index + 1)
+    float* second;                // [B][units] runner-up scores of the units (diagnostic)
+    SeqInfo* seq;                 // [B] published scans
+    int units;                    // race units per sequence
+};
+
 struct VerifyParams {
     const void* target;         // [B, gamma+1, V]
     const void* draft;          // [B, gamma, V]
@@ -63,13 +80,8 @@ struct VerifyParams {
     RacePart* race_parts;       // [B][rpieces]
     int* tickets;               // [B] race arrival counters, zeroed by the scan
     int32_t* status;
-    // fused single-kernel path (zeroed control block, see verify_fused_kernel)
-    float2* row_stat;           // [B][2*gamma+1] merged (scaled max, log2 sum) per row
-    int* row_done;              // [B][2*gamma+1] arrivals of row pieces
-    int* seq_done;              // [B] rows completed
-    int* ready;                 // [B] 1 once the sequence's scan has been published
-    int* race_cursor;           // race items claimed so far (item c: sequence c / P, piece c % P)
-    int* row_cursor;            // row items claimed so far (sequence-major order)
+    float2* row_stat;           // [B][2*gamma+1] merged (scaled max, log2 sum) per row (early exit)
+    FlowRegion flow;            // the flow path's region (verify_flow_kernel)
     uint32_t debug_flags;       // kDebug* test switches
     // early-exit path (verify_early_kernel): task queue and its counters
     int* task;                  // [task_cap] appended task descriptors (pre-filled kTaskEmpty)
@@ -145,9 +157,10 @@ inline int pick_piece_len(long long rows, int V, int es, long long warps) {
     return best_len;
 }
 
-// (m, s) pairs travel as one naturally aligned 64-bit word.  The fused path pre-fills them
-// with kStatEmpty (two NaN halves, never a real pair) and polls until a pair is written,
-// which needs no memory fence on the writer's side.
+// (m, s) pairs travel as one naturally aligned 64-bit word, so a reader that polls the word
+// sees both halves or neither and the writer needs no memory fence.  The early-exit path
+// pre-fills them with kStatEmpty (two NaN halves); the flow path with zero (a real pair has
+// s >= 1, or m = -FLT_MAX when every logit of the piece is -inf).
 constexpr unsigned long long kStatEmpty = 0xFFFFFFFFFFFFFFFFull;
 
 __device__ __forceinline__ void store_stat(float2* dst, float m, float s) {
@@ -172,53 +185,60 @@ __device__ __forceinline__ float scale_of(float T) { return kLog2e / T; }
 
 __device__ __forceinline__ void stat_push1(SoftmaxStat& st, float x, float c) {
     const float mn = fmaxf(st.m, fmaxf(x * c, -FLT_MAX));
-    st.s = st.s * ex2_fast(st.m - mn) + ex2_fast(fmaf(x, c, -mn));
+    st.s = fmaf(st.s, ex2_fast(st.m - mn), ex2_fast(fmaf(x, c, -mn)));
     st.m = mn;
 }
 
-template <class ET, int U>
+// Partial statistics of row[x0, x1) by one warp: 16-byte vectors L per lane in flight, taken
+// U at a time (one running-max update per U vectors per lane).  The arithmetic depends on U
+// only: any L (a multiple of U) gives the same bits; an all-padding batch changes nothing.
+template <class ET, int U, int L = U>
 __device__ __forceinline__ SoftmaxStat stats_piece(const typename ET::storage* row, int x0, int x1,
                                                    float c, int lane) {
+    static_assert(L % U == 0, "loads in flight must be whole batches");
     SoftmaxStat st{-FLT_MAX, 0.0f};
     const RowSpan<ET> sp(row, x0, x1);
     if (lane < sp.head) stat_push1(st, ET::load1(sp.base + lane), c);
     const uint4* vp = sp.vec();
-    for (int v0 = 0; v0 < sp.nvec; v0 += 32 * U) {
-        uint4 raw[U];
+    for (int v0 = 0; v0 < sp.nvec; v0 += 32 * L) {
+        uint4 raw[L];
 #pragma unroll
-        for (int k = 0; k < U; ++k) {
+        for (int k = 0; k < L; ++k) {
             const int v = v0 + lane + 32 * k;
             raw[k] = v < sp.nvec ? ld_stream16(vp + v)
                                  : make_uint4(ET::kNegInfWord, ET::kNegInfWord, ET::kNegInfWord,
                                               ET::kNegInfWord);
         }
-        float f[U][ET::kVec];
 #pragma unroll
-        for (int k = 0; k < U; ++k) ET::widen(raw[k], f[k]);
-        float bmax = f[0][0];
+        for (int h = 0; h < L / U; ++h) {
+            float f[U][ET::kVec];
 #pragma unroll
-        for (int k = 0; k < U; ++k)
+            for (int k = 0; k < U; ++k) ET::widen(raw[h * U + k], f[k]);
+            float bmax = f[0][0];
 #pragma unroll
-            for (int e = 0; e < ET::kVec; ++e) bmax = fmaxf(bmax, f[k][e]);
-        const float mn = fmaxf(st.m, fmaxf(bmax * c, -FLT_MAX));
-        float part[U];
+            for (int k = 0; k < U; ++k)
 #pragma unroll
-        for (int k = 0; k < U; ++k) {
-            float t[ET::kVec];
+                for (int e = 0; e < ET::kVec; ++e) bmax = fmaxf(bmax, f[k][e]);
+            const float mn = fmaxf(st.m, fmaxf(bmax * c, -FLT_MAX));
+            float part[U];
 #pragma unroll
-            for (int e = 0; e < ET::kVec; ++e) t[e] = ex2_fast(fmaf(f[k][e], c, -mn));
+            for (int k = 0; k < U; ++k) {
+                float t[ET::kVec];
 #pragma unroll
-            for (int w = ET::kVec / 2; w > 0; w >>= 1)
+                for (int e = 0; e < ET::kVec; ++e) t[e] = ex2_fast(fmaf(f[k][e], c, -mn));
 #pragma unroll
-                for (int e = 0; e < w; ++e) t[e] += t[e + w];
-            part[k] = t[0];
+                for (int w = ET::kVec / 2; w > 0; w >>= 1)
+#pragma unroll
+                    for (int e = 0; e < w; ++e) t[e] += t[e + w];
+                part[k] = t[0];
+            }
+#pragma unroll
+            for (int w = U / 2; w > 0; w >>= 1)
+#pragma unroll
+                for (int k = 0; k < w; ++k) part[k] += part[k + w];
+            st.s = fmaf(st.s, ex2_fast(st.m - mn), part[0]);
+            st.m = mn;
         }
-#pragma unroll
-        for (int w = U / 2; w > 0; w >>= 1)
-#pragma unroll
-            for (int k = 0; k < w; ++k) part[k] += part[k + w];
-        st.s = st.s * ex2_fast(st.m - mn) + part[0];
-        st.m = mn;
     }
     const int t0 = sp.head + sp.nvec * ET::kVec;
     if (lane < sp.tail) stat_push1(st, ET::load1(sp.base + t0 + lane), c);
@@ -227,7 +247,7 @@ __device__ __forceinline__ SoftmaxStat stats_piece(const typename ET::storage* r
 
 // Row r of sequence b: target row r (r <= gamma, scale log2(e)/T_b) or draft row
 // r - gamma - 1 (scale log2(e)/Td_b).  Writes the piece's partial statistics.
-template <class ET, int U>
+template <class ET, int U, int L = U>
 __device__ __forceinline__ void row_stats_item(const VerifyParams& p, int b, int r, int piece,
                                                int lane) {
     using S = typename ET::storage;
@@ -243,7 +263,7 @@ __device__ __forceinline__ void row_stats_item(const VerifyParams& p, int b, int
     }
     const int x0 = piece * p.piece_len;
     const int x1 = min(p.V, x0 + p.piece_len);
-    const SoftmaxStat st = stats_piece<ET, U>(row, x0, x1, c, lane);
+    const SoftmaxStat st = stats_piece<ET, U, L>(row, x0, x1, c, lane);
     const int R = 2 * p.gamma + 1;
     if (lane == 0)  // one aligned 64-bit store: readers see both halves or neither
         store_stat(p.stat_parts + (static_cast<long long>(b) * R + r) * p.npieces + piece, st.m, st.s);
@@ -650,10 +670,11 @@ __global__ void __launch_bounds__(256) row_argmax_kernel(VerifyParams p) {
 }
 
 // ----------------------------------------------------------------------------------------
-// scan: per sequence, ln Z of each row, p_i(d_i), q_i(d_i), u_i and the first rejection.
+// Bounded waits and the status word; scan_greedy: per sequence, the first position whose
+// draft token is not the target row's argmax.
 // ----------------------------------------------------------------------------------------
 
-constexpr uint32_t kDebugNeverReady = 1u;         // scans never set ready[b] (tests)
+constexpr uint32_t kDebugNeverReady = 1u;         // published scans never set their flag (tests)
 constexpr unsigned long long kWaitLimitNs = 500000000ull;  // give up a wait after 0.5 s
 
 __device__ __forceinline__ unsigned long long global_time_ns() {
@@ -664,94 +685,6 @@ __device__ __forceinline__ unsigned long long global_time_ns() {
 
 __device__ __forceinline__ void set_status(int32_t* status, int code) {
     atomicCAS(reinterpret_cast<int*>(status), 0, code);
-}
-
-template <class ET>
-__global__ void __launch_bounds__(256) scan_kernel(VerifyParams p) {
-    using S = typename ET::storage;
-    extern __shared__ float smem[];
-    const int R = 2 * p.gamma + 1;
-    float* sm_m = smem;        // [R] scaled max
-    float* sm_l = smem + R;    // [R] log2 of the sum
-    __shared__ int s_j, s_bad;
-    const int b = blockIdx.x;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    if (threadIdx.x == 0) {
-        s_j = p.gamma;
-        s_bad = 0;
-    }
-    const float Tb = seq_T(p, b), Tdb = seq_Td(p, b);
-    const float cp = scale_of(Tb), cq = scale_of(Tdb);
-    for (int r = warp; r < R; r += nw) {
-        SoftmaxStat st{-FLT_MAX, 0.0f};
-        const float2* parts = p.stat_parts + (static_cast<long long>(b) * R + r) * p.npieces;
-        for (int k = lane; k < p.npieces; k += 32) {
-            const float2 q = parts[k];
-            st = merge_stat(st, SoftmaxStat{q.x, q.y});
-        }
-        st = warp_merge_stat(st);
-        if (lane == 0) {
-            const float l2s = log2f(st.s);
-            sm_m[r] = st.m;
-            sm_l[r] = l2s;
-            const float lz = (st.m + l2s) * kLn2;
-            if (r <= p.gamma) {
-                if (p.out_logZp) p.out_logZp[static_cast<long long>(b) * (p.gamma + 1) + r] = lz;
-            } else if (p.out_logZq) {
-                p.out_logZq[static_cast<long long>(b) * p.gamma + (r - p.gamma - 1)] = lz;
-            }
-        }
-    }
-    __syncthreads();
-    const uint32_t bg = p.seq_base + static_cast<uint32_t>(b);
-    for (int i = threadIdx.x; i < p.gamma; i += blockDim.x) {
-        const int d = p.tokens[static_cast<long long>(b) * p.gamma + i];
-        const float u = accept_uniform(p.key, bg, static_cast<uint32_t>(i));
-        const long long k = static_cast<long long>(b) * p.gamma + i;
-        if (p.out_u) p.out_u[k] = u;
-        if (d < 0 || d >= p.V) {
-            s_bad = 1;
-            if (p.out_logp) p.out_logp[k] = NAN;
-            if (p.out_logq) p.out_logq[k] = NAN;
-            continue;
-        }
-        const float xt = ET::load1(static_cast<const S*>(p.target) +
-                                   (static_cast<long long>(b) * (p.gamma + 1) + i) * p.V + d);
-        const float xd = ET::load1(static_cast<const S*>(p.draft) +
-                                   (static_cast<long long>(b) * p.gamma + i) * p.V + d);
-        const float l2p = fmaf(xt, cp, -sm_m[i]) - sm_l[i];
-        const float l2q = fmaf(xd, cq, -sm_m[p.gamma + 1 + i]) - sm_l[p.gamma + 1 + i];
-        if (p.out_logp) p.out_logp[k] = l2p * kLn2;
-        if (p.out_logq) p.out_logq[k] = l2q * kLn2;
-        // accept iff u < min(1, p/q); p(d) = 0 rejects, q(d) = 0 < p(d) accepts
-        const bool accept = (l2p > -INFINITY) && (u < exp2f(l2p - l2q));
-        if (!accept) atomicMin(&s_j, i);
-    }
-    __syncthreads();
-    const int j = s_bad ? -1 : s_j;
-    if (threadIdx.x == 0) {
-        p.out_n[b] = j;
-        SeqInfo si;
-        si.j = j;
-        si.cp = cp;
-        si.cq = cq;
-        const int rr = (j >= 0) ? j : 0;
-        si.mp = sm_m[rr];
-        si.l2sp = sm_l[rr];
-        if (j >= 0 && j < p.gamma) {
-            si.mq = sm_m[p.gamma + 1 + j];
-            si.l2sq = sm_l[p.gamma + 1 + j];
-        } else {
-            si.mq = 0.0f;
-            si.l2sq = 0.0f;
-        }
-        p.seq[b] = si;
-        p.tickets[b] = 0;  // the race's per-sequence arrival counter starts from zero
-        if (j < 0) set_status(p.status, 3 /* SPEC_EBADTOKEN */);
-    }
-    int32_t* out = p.out_tokens + static_cast<long long>(b) * (p.gamma + 1);
-    for (int t = threadIdx.x; t <= p.gamma; t += blockDim.x)
-        out[t] = (j >= 0 && t < j) ? p.tokens[static_cast<long long>(b) * p.gamma + t] : -1;
 }
 
 template <class ET>
@@ -1001,72 +934,10 @@ __device__ __forceinline__ RaceState race_piece(const typename ET::storage* rt,
     return warp_race_merge(st);
 }
 
-// One race piece of sequence b (whose scan result is `si`): race the piece, publish the
-// partial winner, and if this is the sequence's last piece merge all pieces and write the
-// token.  Arrivals are counted, never waited for.
-template <class ET>
-__device__ __forceinline__ void race_item(const VerifyParams& p, int b, int piece, const SeqInfo& si,
-                                          int lane) {
-    using S = typename ET::storage;
-    if (si.j < 0) return;  // bad draft token: nothing to draw
-    const bool residual = si.j < p.gamma;
-    const S* rt = static_cast<const S*>(p.target) + (static_cast<long long>(b) * (p.gamma + 1) + si.j) * p.V;
-    const S* rd = residual ? static_cast<const S*>(p.draft) + (static_cast<long long>(b) * p.gamma + si.j) * p.V
-                           : nullptr;
-    const uint32_t bg = p.seq_base + static_cast<uint32_t>(b);
-    const int x0 = piece * p.rpiece_len;
-    const int x1 = min(p.V, x0 + p.rpiece_len);
-    const RaceState st = race_piece<ET>(rt, rd, x0, x1, si, residual, p.rk, bg,
-                                        static_cast<uint32_t>(si.j), lane);
-    const long long item = static_cast<long long>(b) * p.rpieces + piece;
-    if (lane == 0) {
-        p.race_parts[item] = RacePart{st.best, st.idx, st.second, 0};
-        __threadfence();
-    }
-    int ticket = 0;
-    if (lane == 0) ticket = atomicAdd(p.tickets + b, 1);
-    ticket = __shfl_sync(0xffffffffu, ticket, 0);
-    if (ticket != p.rpieces - 1) return;
-    // Last piece of this sequence: merge every piece's winner (read through L2).
-    __threadfence();
-    RaceState m{-INFINITY, INT_MAX, -INFINITY};
-    for (int k = lane; k < p.rpieces; k += 32) {
-        const RacePart* rp = p.race_parts + static_cast<long long>(b) * p.rpieces + k;
-        const float4 raw = __ldcg(reinterpret_cast<const float4*>(rp));
-        m = race_merge(m, RaceState{raw.x, __float_as_int(raw.y), raw.z});
-    }
-    m = warp_race_merge(m);
-    if (m.idx == INT_MAX) {
-        // Every residual weight was zero (p <= q everywhere in fp32): draw from p_j.
-        m = race_piece<ET>(rt, nullptr, 0, p.V, si, false, p.rk, bg, static_cast<uint32_t>(si.j),
-                           lane);
-    }
-    if (lane == 0) {
-        p.out_tokens[static_cast<long long>(b) * (p.gamma + 1) + si.j] = m.idx;
-        if (p.out_race) {
-            p.out_race[2 * b] = m.best;
-            p.out_race[2 * b + 1] = m.second;
-        }
-    }
-}
-
-template <class ET>
-__global__ void __launch_bounds__(256, 4) race_kernel(VerifyParams p) {
-    const int lane = threadIdx.x & 31;
-    const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
-    const long long total = static_cast<long long>(p.B) * p.rpieces;
-    for (long long item = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-         item < total; item += nwarps) {
-        const int b = static_cast<int>(item / p.rpieces);
-        race_item<ET>(p, b, static_cast<int>(item % p.rpieces), p.seq[b], lane);
-    }
-}
-
 // ----------------------------------------------------------------------------------------
-// race_block: the race pass with one block per race piece of kRaceBlockTokens tokens.  Each
-// warp holds its kRaceWarpTokens tokens in registers, so the piece is read once; the
-// block's threshold is seeded from every lane's most likely token with a cheap lower bound
-// of its score (no exact evaluation on the critical path).
+// Race geometry: a warp scores kRaceWarpTokens tokens per step from registers (so each is
+// read once), a block kRaceBlockTokens; thresholds are seeded from every lane's most likely
+// token with a cheap lower bound of its score (no exact evaluation on the critical path).
 // ----------------------------------------------------------------------------------------
 
 constexpr int kRaceWarpTokens = 1024;
@@ -1104,148 +975,6 @@ __device__ __forceinline__ float race_score_lower_bound(float xt, float xd, cons
         E = -lg2_fast(one_minus_U) * kLn2;
     }
     return (l2w - lg2_fast(E)) * kLn2 - 1e-3f;
-}
-
-template <class ET>
-__global__ void __launch_bounds__(256, 4) race_block_kernel(VerifyParams p) {
-    using S = typename ET::storage;
-    constexpr int VPL = kRaceWarpTokens / (32 * ET::kVec);  // vectors per lane
-    __shared__ float s_thr[8];
-    __shared__ RaceState s_best[8];
-    __shared__ int s_last;
-    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
-    const int b = blockIdx.x / p.rpieces;
-    const int piece = blockIdx.x % p.rpieces;
-    const SeqInfo si = p.seq[b];
-    if (si.j < 0) return;  // bad draft token: nothing to draw
-    const bool residual = si.j < p.gamma;
-    const S* rt = static_cast<const S*>(p.target) + (static_cast<long long>(b) * (p.gamma + 1) + si.j) * p.V;
-    const S* rd = residual ? static_cast<const S*>(p.draft) + (static_cast<long long>(b) * p.gamma + si.j) * p.V
-                           : nullptr;
-    const uint32_t bg = p.seq_base + static_cast<uint32_t>(b);
-    const uint32_t pos = static_cast<uint32_t>(si.j);
-    const RaceRowRng q = race_row_rng(p.rk, bg, pos);
-    const int x0 = piece * kRaceBlockTokens + wib * kRaceWarpTokens;
-    const int x1 = min(p.V, x0 + kRaceWarpTokens);
-    RaceState st{-INFINITY, INT_MAX, -INFINITY};
-    auto word_at = [&](int x) {
-        const uint4 blk = race_block_fast(q, p.rk, static_cast<uint32_t>(x) >> 2);
-        return word_of(blk, static_cast<uint32_t>(x) & 3u);
-    };
-    auto offer_exact = [&](float xt, int x, uint32_t w) {
-        const float xd = residual ? ET::load1(rd + x) : 0.0f;
-        const float sc = race_exact_score(xt, xd, si, residual, w);
-        if (sc > -INFINITY) race_offer(st, sc, x);
-    };
-    // The register path needs a 16-byte aligned chunk start (then every vector is aligned and
-    // starts on a Philox block); otherwise, or for the row's last < 8 tokens, tokens go one by one.
-    const bool vec_ok = x0 < x1 && (reinterpret_cast<uintptr_t>(rt + x0) & 15u) == 0;
-    const int nvec = vec_ok ? (x1 - x0) / ET::kVec : 0;
-    uint4 raw[VPL];
-    float seed = -INFINITY;
-    if (vec_ok) {
-        const uint4* vt = reinterpret_cast<const uint4*>(rt + x0);
-#pragma unroll
-        for (int k = 0; k < VPL; ++k) {
-            const int v = lane + 32 * k;
-            raw[k] = v < nvec ? __ldg(vt + v) : make_uint4(ET::kNegInfWord, ET::kNegInfWord,
-                                                           ET::kNegInfWord, ET::kNegInfWord);
-        }
-        float vmax = -INFINITY;
-        int xs = -1;
-#pragma unroll
-        for (int k = 0; k < VPL; ++k) {
-            float ft[ET::kVec];
-            ET::widen(raw[k], ft);
-#pragma unroll
-            for (int e = 0; e < ET::kVec; ++e)
-                if (ft[e] > vmax) {
-                    vmax = ft[e];
-                    xs = x0 + (lane + 32 * k) * ET::kVec + e;
-                }
-        }
-        if (xs >= 0) {
-            const float xd = residual ? ET::load1(rd + xs) : 0.0f;
-            seed = race_score_lower_bound(vmax, xd, si, residual, word_at(xs));
-        }
-    }
-    seed = float_unorder(__reduce_max_sync(0xffffffffu, float_order(seed)));
-    if (lane == 0) s_thr[wib] = seed;
-    __syncthreads();
-    float thr = s_thr[0];
-#pragma unroll
-    for (int k = 1; k < 8; ++k) thr = fmaxf(thr, s_thr[k]);
-    if (vec_ok) {
-        const float mpl = si.mp + si.l2sp;
-#pragma unroll
-        for (int k = 0; k < VPL; ++k) {
-            const int v = lane + 32 * k;
-            const float C = (thr > -INFINITY) ? 32.0f + kRaceBoundMargin2 - thr * kLog2e - mpl
-                                              : INFINITY;
-            if (v < nvec) {
-                float ft[ET::kVec];
-                ET::widen(raw[k], ft);
-                const int xv = x0 + v * ET::kVec;
-                uint32_t cand = 0;
-                uint4 blk[ET::kVec / 4];
-#pragma unroll
-                for (int g = 0; g < ET::kVec / 4; ++g)
-                    blk[g] = race_block_fast(q, p.rk, static_cast<uint32_t>(xv + 4 * g) >> 2);
-#pragma unroll
-                for (int g = 0; g < ET::kVec / 4; ++g) {
-                    const uint32_t w4[4] = {blk[g].x, blk[g].y, blk[g].z, blk[g].w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        cand |= (lg2_fast(static_cast<float>(w4[e])) <= fmaf(ft[4 * g + e], si.cp, C))
-                                    ? (1u << (4 * g + e)) : 0u;
-                }
-                while (cand) {  // rare: exact scores in increasing token order
-                    const int e = __ffs(cand) - 1;
-                    cand &= cand - 1;
-                    offer_exact(ET::load1(rt + xv + e), xv + e, word_at(xv + e));
-                }
-            }
-            thr = fmaxf(thr, float_unorder(__reduce_max_sync(0xffffffffu, float_order(st.best))));
-        }
-        const int t0 = nvec * ET::kVec;  // the row's last < kVec tokens
-        if (lane < (x1 - x0) - t0) offer_exact(ET::load1(rt + x0 + t0 + lane), x0 + t0 + lane,
-                                               word_at(x0 + t0 + lane));
-    } else {
-        for (int x = x0 + lane; x < x1; x += 32) offer_exact(ET::load1(rt + x), x, word_at(x));
-    }
-    st = warp_race_merge(st);
-    if (lane == 0) s_best[wib] = st;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        RaceState m = s_best[0];
-        for (int k = 1; k < 8; ++k) m = race_merge(m, s_best[k]);
-        p.race_parts[static_cast<long long>(b) * p.rpieces + piece] = RacePart{m.best, m.idx, m.second, 0};
-        __threadfence();
-        s_last = (atomicAdd(p.tickets + b, 1) == p.rpieces - 1);
-    }
-    __syncthreads();
-    if (!s_last) return;
-    // last piece of this sequence: warp 0 merges every piece's winner (read through L2)
-    if (wib != 0) return;
-    __threadfence();
-    RaceState m{-INFINITY, INT_MAX, -INFINITY};
-    for (int k = lane; k < p.rpieces; k += 32) {
-        const RacePart* rp = p.race_parts + static_cast<long long>(b) * p.rpieces + k;
-        const float4 r4 = __ldcg(reinterpret_cast<const float4*>(rp));
-        m = race_merge(m, RaceState{r4.x, __float_as_int(r4.y), r4.z});
-    }
-    m = warp_race_merge(m);
-    if (m.idx == INT_MAX) {
-        // Every residual weight was zero (p <= q everywhere in fp32): draw from p_j.
-        m = race_piece<ET>(rt, nullptr, 0, p.V, si, false, p.rk, bg, pos, lane);
-    }
-    if (lane == 0) {
-        p.out_tokens[static_cast<long long>(b) * (p.gamma + 1) + si.j] = m.idx;
-        if (p.out_race) {
-            p.out_race[2 * b] = m.best;
-            p.out_race[2 * b + 1] = m.second;
-        }
-    }
 }
 
 // ----------------------------------------------------------------------------------------
@@ -1481,65 +1210,147 @@ __device__ __forceinline__ void race_sequence_block(const VerifyParams& p, int b
                         pc_end, pc_step, slot, nslots, si, s_thr, s_best, s_last);
 }
 
+// Poll a packed word until it is nonzero; after kWaitLimitNs give up, record SPEC_ETIMEOUT
+// and return 0.
+__device__ __forceinline__ unsigned long long poll_nonzero_u64(const VerifyParams& p,
+                                                               const unsigned long long* w) {
+    unsigned long long v = ld_relaxed_u64g(w);
+    if (v != 0ull) return v;
+    const unsigned long long t0 = global_time_ns();
+    unsigned ns = 32;
+    while ((v = ld_relaxed_u64g(w)) == 0ull) {
+        if (global_time_ns() - t0 > kWaitLimitNs) {
+            set_status(p.status, 4 /* SPEC_ETIMEOUT */);
+            return 0ull;
+        }
+        __nanosleep(ns);
+        if (ns < 256) ns <<= 1;
+    }
+    return v;
+}
+
+// The merged statistics of one row from its P partials (packed (m, s) words), by one thread
+// in a fixed order: eight partials at a time merged as a balanced tree (pairs, pairs of
+// pairs, root), the eight-partial results folded in piece order.  Every schedule merges rows
+// this way, so they all get the same bits.  kPoll: partials are polled until written (the
+// flow path, where they carry no fence); otherwise they are complete (a kernel boundary).
+template <bool kPoll>
+__device__ __forceinline__ SoftmaxStat fold_row_stats(const VerifyParams& p,
+                                                      const unsigned long long* parts, int P) {
+    SoftmaxStat acc{-FLT_MAX, 0.0f};
+    for (int k0 = 0; k0 < P; k0 += 8) {
+        unsigned long long v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            v[q] = (k0 + q < P) ? (kPoll ? ld_relaxed_u64g(parts + k0 + q) : __ldcg(parts + k0 + q)) : 0ull;
+        SoftmaxStat t[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            if (kPoll && k0 + q < P && v[q] == 0ull) v[q] = poll_nonzero_u64(p, parts + k0 + q);
+            t[q] = (k0 + q < P) ? SoftmaxStat{__uint_as_float(static_cast<uint32_t>(v[q])),
+                                              __uint_as_float(static_cast<uint32_t>(v[q] >> 32))}
+                                : SoftmaxStat{-FLT_MAX, 0.0f};
+        }
+        t[0] = merge_stat(t[0], t[1]);
+        t[2] = merge_stat(t[2], t[3]);
+        t[4] = merge_stat(t[4], t[5]);
+        t[6] = merge_stat(t[6], t[7]);
+        t[0] = merge_stat(t[0], t[2]);
+        t[4] = merge_stat(t[4], t[6]);
+        acc = merge_stat(acc, merge_stat(t[0], t[4]));
+    }
+    return acc;
+}
+
 template <class ET>
 __global__ void __launch_bounds__(256, SPECVERIFY_RACE_MINBLOCKS) scan_race_kernel(VerifyParams p) {
     using S = typename ET::storage;
-    constexpr int VPL = kRaceWarpTokens / (32 * ET::kVec);
     extern __shared__ float smem[];  // [2R]: scaled max and log2 sum of every row
     __shared__ int s_j, s_bad, s_last;
     __shared__ float s_thr[8];
     __shared__ RaceState s_best[8];
-    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
-    const int G = p.rgroups;  // blocks per sequence
-    const int b = blockIdx.x / G;
-    const int g = blockIdx.x % G;
+    __shared__ int s_d[256];
+    __shared__ float s_xt[256], s_xd[256], s_u[256];
     const int R = 2 * p.gamma + 1;
     float* sm_m = smem;
     float* sm_l = smem + R;
-    const float Tb = seq_T(p, b), Tdb = seq_Td(p, b);
-    const float cp = scale_of(Tb), cq = scale_of(Tdb);
-    const uint32_t bg = p.seq_base + static_cast<uint32_t>(b);
-    const bool writer = (g == 0);
-    // diagnostics need every row's statistics; otherwise rows are merged only up to the first
-    // rejection, four positions (target and draft rows in parallel) at a time
-    const bool all_rows = writer && (p.out_logZp || p.out_logZq || p.out_logp || p.out_logq);
-    // inputs-only prologue (position i = threadIdx.x): overlaps the streaming pass's tail
-    __shared__ int s_d[256];
-    __shared__ float s_xt[256], s_xd[256], s_u[256];
-    const int i0 = threadIdx.x;
-    if (i0 < p.gamma) {
-        const int d = p.tokens[static_cast<long long>(b) * p.gamma + i0];
-        s_d[i0] = d;
-        s_u[i0] = accept_uniform(p.key, bg, static_cast<uint32_t>(i0));
-        float xt = 0.0f, xd = 0.0f;
-        if (d >= 0 && d < p.V) {
-            xt = ET::load1(static_cast<const S*>(p.target) +
-                           (static_cast<long long>(b) * (p.gamma + 1) + i0) * p.V + d);
-            xd = ET::load1(static_cast<const S*>(p.draft) +
-                           (static_cast<long long>(b) * p.gamma + i0) * p.V + d);
+    // this block's race pieces: [k T / n, (k + 1) T / n) of the T = B * rpieces pieces in
+    // sequence-major order (the same count, within one, for every block); a block whose range
+    // crosses a sequence boundary scans and races both sequences
+    const long long T = static_cast<long long>(p.B) * p.rpieces;
+    const long long nblk = gridDim.x;
+    const long long q0 = static_cast<long long>(blockIdx.x) * T / nblk;
+    const long long q1 = (static_cast<long long>(blockIdx.x) + 1) * T / nblk;
+    auto block_of = [&](long long x) { return ((x + 1) * nblk - 1) / T; };  // block racing piece x
+    bool first = true;
+    for (long long q = q0; q < q1;) {
+        const int b = static_cast<int>(q / p.rpieces);
+        const int pc0 = static_cast<int>(q % p.rpieces);
+        const int pc1 = static_cast<int>(min(static_cast<long long>(p.rpieces), pc0 + (q1 - q)));
+        q += pc1 - pc0;
+        const long long k_lo = block_of(static_cast<long long>(b) * p.rpieces);
+        const long long k_hi = block_of(static_cast<long long>(b + 1) * p.rpieces - 1);
+        const int slot = static_cast<int>(blockIdx.x - k_lo), nslots = static_cast<int>(k_hi - k_lo + 1);
+        const bool writer = (slot == 0);  // writes the sequence's outputs
+        const float cp = scale_of(seq_T(p, b)), cq = scale_of(seq_Td(p, b));
+        const uint32_t bg = p.seq_base + static_cast<uint32_t>(b);
+        // inputs-only prologue (position i = threadIdx.x): the first sequence's overlaps the
+        // streaming pass's tail
+        const int i0 = threadIdx.x;
+        if (i0 < p.gamma) {
+            const int d = p.tokens[static_cast<long long>(b) * p.gamma + i0];
+            s_d[i0] = d;
+            s_u[i0] = accept_uniform(p.key, bg, static_cast<uint32_t>(i0));
+            float xt = 0.0f, xd = 0.0f;
+            if (d >= 0 && d < p.V) {
+                xt = ET::load1(static_cast<const S*>(p.target) +
+                               (static_cast<long long>(b) * (p.gamma + 1) + i0) * p.V + d);
+                xd = ET::load1(static_cast<const S*>(p.draft) +
+                               (static_cast<long long>(b) * p.gamma + i0) * p.V + d);
+            }
+            s_xt[i0] = xt;
+            s_xd[i0] = xd;
         }
-        s_xt[i0] = xt;
-        s_xd[i0] = xd;
-    }
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (threadIdx.x == 0) {
-        s_j = p.gamma;
-        s_bad = 0;
-    }
-    // any draft token outside [0, V) marks the whole sequence
-    for (int i = threadIdx.x; i < p.gamma; i += blockDim.x) {
-        const int d = (i < 256) ? s_d[i] : p.tokens[static_cast<long long>(b) * p.gamma + i];
-        if (d < 0 || d >= p.V) s_bad = 1;
-    }
-    auto merge_row = [&](int r) {  // one warp: row r's statistics into shared memory
-        SoftmaxStat st{-FLT_MAX, 0.0f};
-        const float2* parts = p.stat_parts + (static_cast<long long>(b) * R + r) * p.npieces;
-        for (int k = lane; k < p.npieces; k += 32) {
-            const float2 qq = parts[k];
-            st = merge_stat(st, SoftmaxStat{qq.x, qq.y});
+        if (threadIdx.x == 0) {
+            s_j = p.gamma;
+            s_bad = 0;
         }
-        st = warp_merge_stat(st);
-        if (lane == 0) {
+        if (first) asm volatile("griddepcontrol.wait;" ::: "memory");
+        first = false;
+        __syncthreads();  // s_j and s_bad are set before any thread reports a bad token
+        // any draft token outside [0, V) marks the whole sequence
+        for (int i = threadIdx.x; i < p.gamma; i += blockDim.x) {
+            const int d = (i < 256) ? s_d[i] : p.tokens[static_cast<long long>(b) * p.gamma + i];
+            if (d < 0 || d >= p.V) s_bad = 1;
+        }
+        auto decide = [&](int i) {  // one thread: the accept test at position i
+            int d;
+            float xt, xd, u;
+            if (i < 256) {
+                d = s_d[i]; xt = s_xt[i]; xd = s_xd[i]; u = s_u[i];
+            } else {
+                d = p.tokens[static_cast<long long>(b) * p.gamma + i];
+                u = accept_uniform(p.key, bg, static_cast<uint32_t>(i));
+                xt = ET::load1(static_cast<const S*>(p.target) +
+                               (static_cast<long long>(b) * (p.gamma + 1) + i) * p.V + d);
+                xd = ET::load1(static_cast<const S*>(p.draft) +
+                               (static_cast<long long>(b) * p.gamma + i) * p.V + d);
+            }
+            const long long k = static_cast<long long>(b) * p.gamma + i;
+            if (writer && p.out_u) p.out_u[k] = u;
+            const float l2p = fmaf(xt, cp, -sm_m[i]) - sm_l[i];
+            const float l2q = fmaf(xd, cq, -sm_m[p.gamma + 1 + i]) - sm_l[p.gamma + 1 + i];
+            if (writer && p.out_logp) p.out_logp[k] = l2p * kLn2;
+            if (writer && p.out_logq) p.out_logq[k] = l2q * kLn2;
+            // accept iff u < min(1, p/q); p(d) = 0 rejects, q(d) = 0 < p(d) accepts
+            if (!((l2p > -INFINITY) && (u < exp2f(l2p - l2q)))) atomicMin(&s_j, i);
+        };
+        // every row's statistics, one thread per row (fold_row_stats: the order every schedule
+        // uses); rows past the first rejection decide nothing but cost one L2 read per partial
+        const unsigned long long* parts =
+            reinterpret_cast<const unsigned long long*>(p.stat_parts) + static_cast<long long>(b) * R * p.npieces;
+        for (int r = threadIdx.x; r < R; r += blockDim.x) {
+            const SoftmaxStat st = fold_row_stats<false>(p, parts + static_cast<long long>(r) * p.npieces, p.npieces);
             const float l2s = log2f(st.s);
             sm_m[r] = st.m;
             sm_l[r] = l2s;
@@ -1552,78 +1363,45 @@ __global__ void __launch_bounds__(256, SPECVERIFY_RACE_MINBLOCKS) scan_race_kern
                 }
             }
         }
-    };
-    auto decide = [&](int i) {  // one thread: the accept test at position i
-        int d;
-        float xt, xd, u;
-        if (i < 256) {
-            d = s_d[i]; xt = s_xt[i]; xd = s_xd[i]; u = s_u[i];
-        } else {
-            d = p.tokens[static_cast<long long>(b) * p.gamma + i];
-            u = accept_uniform(p.key, bg, static_cast<uint32_t>(i));
-            xt = ET::load1(static_cast<const S*>(p.target) +
-                           (static_cast<long long>(b) * (p.gamma + 1) + i) * p.V + d);
-            xd = ET::load1(static_cast<const S*>(p.draft) +
-                           (static_cast<long long>(b) * p.gamma + i) * p.V + d);
-        }
-        const long long k = static_cast<long long>(b) * p.gamma + i;
-        if (writer && p.out_u) p.out_u[k] = u;
-        const float l2p = fmaf(xt, cp, -sm_m[i]) - sm_l[i];
-        const float l2q = fmaf(xd, cq, -sm_m[p.gamma + 1 + i]) - sm_l[p.gamma + 1 + i];
-        if (writer && p.out_logp) p.out_logp[k] = l2p * kLn2;
-        if (writer && p.out_logq) p.out_logq[k] = l2q * kLn2;
-        // accept iff u < min(1, p/q); p(d) = 0 rejects, q(d) = 0 < p(d) accepts
-        if (!((l2p > -INFINITY) && (u < exp2f(l2p - l2q)))) atomicMin(&s_j, i);
-    };
-    __syncthreads();
-    if (s_bad) {
-        if (writer) {
-            for (int i = threadIdx.x; i < p.gamma; i += blockDim.x) {
-                const long long k = static_cast<long long>(b) * p.gamma + i;
-                if (p.out_u) p.out_u[k] = accept_uniform(p.key, bg, static_cast<uint32_t>(i));
-                if (p.out_logp) p.out_logp[k] = NAN;
-                if (p.out_logq) p.out_logq[k] = NAN;
-            }
-            for (int r = wib; all_rows && r < R; r += 8) merge_row(r);
-        }
-    } else if (all_rows) {
-        for (int r = wib; r < R; r += 8) merge_row(r);
         __syncthreads();
-        for (int i = threadIdx.x; i < p.gamma; i += blockDim.x) decide(i);
-    } else {
-        for (int i0b = 0; i0b < p.gamma; i0b += 4) {
-            const int i = i0b + (wib & 3);
-            if (i < p.gamma) merge_row(wib < 4 ? i : p.gamma + 1 + i);
-            __syncthreads();
-            if (threadIdx.x < 4 && i0b + threadIdx.x < p.gamma) decide(i0b + threadIdx.x);
-            __syncthreads();
-            if (s_j < p.gamma) break;
+        if (s_bad) {
+            if (writer) {
+                for (int i = threadIdx.x; i < p.gamma; i += blockDim.x) {
+                    const long long k = static_cast<long long>(b) * p.gamma + i;
+                    if (p.out_u) p.out_u[k] = accept_uniform(p.key, bg, static_cast<uint32_t>(i));
+                    if (p.out_logp) p.out_logp[k] = NAN;
+                    if (p.out_logq) p.out_logq[k] = NAN;
+                }
+            }
+        } else {
+            for (int i = threadIdx.x; i < p.gamma; i += blockDim.x) decide(i);
         }
-        if (s_j == p.gamma && wib == 0) merge_row(p.gamma);  // bonus row
-    }
-    __syncthreads();
-    const int j = s_bad ? -1 : s_j;
-    if (writer) {
-        if (threadIdx.x == 0) {
-            p.out_n[b] = j;
-            if (j < 0) set_status(p.status, 3 /* SPEC_EBADTOKEN */);
+        __syncthreads();
+        const int j = s_bad ? -1 : s_j;
+        if (writer) {
+            if (threadIdx.x == 0) {
+                p.out_n[b] = j;
+                if (j < 0) set_status(p.status, 3 /* SPEC_EBADTOKEN */);
+            }
+            int32_t* out = p.out_tokens + static_cast<long long>(b) * (p.gamma + 1);
+            for (int t = threadIdx.x; t <= p.gamma; t += blockDim.x)
+                if (t != j) out[t] = (j >= 0 && t < j) ? p.tokens[static_cast<long long>(b) * p.gamma + t] : -1;
         }
-        int32_t* out = p.out_tokens + static_cast<long long>(b) * (p.gamma + 1);
-        for (int t = threadIdx.x; t <= p.gamma; t += blockDim.x)
-            if (t != j) out[t] = (j >= 0 && t < j) ? p.tokens[static_cast<long long>(b) * p.gamma + t] : -1;
+        if (j >= 0) {
+            SeqInfo si;
+            si.j = j;
+            si.cp = cp;
+            si.cq = cq;
+            si.mp = sm_m[j];
+            si.l2sp = sm_l[j];
+            const bool residual = j < p.gamma;
+            si.mq = residual ? sm_m[p.gamma + 1 + j] : 0.0f;
+            si.l2sq = residual ? sm_l[p.gamma + 1 + j] : 0.0f;
+            si.pad = 0;
+            race_sequence_block<ET>(p, b, pc0, pc1, 1, slot, nslots, si, s_thr, s_best, s_last);
+        }
+        __syncthreads();  // before the next sequence reuses shared memory
     }
-    if (j < 0) return;
-    SeqInfo si;
-    si.j = j;
-    si.cp = cp;
-    si.cq = cq;
-    si.mp = sm_m[j];
-    si.l2sp = sm_l[j];
-    const bool residual = j < p.gamma;
-    si.mq = residual ? sm_m[p.gamma + 1 + j] : 0.0f;
-    si.l2sq = residual ? sm_l[p.gamma + 1 + j] : 0.0f;
-    si.pad = 0;
-    race_sequence_block<ET>(p, b, g, p.rpieces, G, g, G, si, s_thr, s_best, s_last);
 }
 
 // ----------------------------------------------------------------------------------------
@@ -1887,36 +1665,6 @@ __global__ void __launch_bounds__(256, SPECVERIFY_RACE_MINBLOCKS) tree_race_kern
                         G, g, G, si, s_thr, s_best, s_last);
 }
 
-// ----------------------------------------------------------------------------------------
-// verify_fused: the whole sampling verify in one persistent (cooperative) launch, with
-// specialised warps.
-//
-// Streaming warps (the first kStreamWarps of each block) claim row items (b, r, piece) in
-// sequence-major order from row_cursor, kClaimChunk at a time, and never wait: each writes its piece's partial
-// statistics and counts its arrival on the row without a fence (partials are pre-filled
-// with an empty marker that the reader polls for).  The last piece of a row to arrive merges
-// the row; the last row of a sequence to be merged runs the sequence's scan (one warp) and
-// sets ready[b].  Race warps (the rest of each block) claim race items (b, piece) in
-// sequence order from race_cursor, wait (bounded) for ready[b], and race one piece of the
-// raced row while it is still in L2; streaming warps join them when the rows run out.  A
-// warp that waits holds no row item, and every scan is finished by a warp that never waits,
-// so the waits end.  The arrival count of a row item is resolved one item later, so the
-// atomic's round trip overlaps the next item's loads.  Every wait gives up after
-// kWaitLimitNs and records SPEC_ETIMEOUT.
-// ----------------------------------------------------------------------------------------
-
-#ifndef SPECVERIFY_STREAM_WARPS
-#define SPECVERIFY_STREAM_WARPS 7
-#endif
-#ifndef SPECVERIFY_FUSED_MINBLOCKS
-#define SPECVERIFY_FUSED_MINBLOCKS 4
-#endif
-constexpr int kStreamWarps = SPECVERIFY_STREAM_WARPS;  // of the 8 warps of a block (the rest race)
-#ifndef SPECVERIFY_CLAIM_CHUNK
-#define SPECVERIFY_CLAIM_CHUNK 1
-#endif
-constexpr int kClaimChunk = SPECVERIFY_CLAIM_CHUNK;     // row items per claim of the cursor
-
 __device__ __forceinline__ int ld_acquire(const int* p) {
     int v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -1955,199 +1703,6 @@ __device__ __forceinline__ float2 wait_stat(const VerifyParams& p, const float2*
     }
     return make_float2(__uint_as_float(static_cast<uint32_t>(v)),
                        __uint_as_float(static_cast<uint32_t>(v >> 32)));
-}
-
-// One warp: merge a row's partials (after the row's last piece arrived; each partial is
-// waited for, since arrivals are counted without a fence).
-__device__ __forceinline__ void merge_row_warp(const VerifyParams& p, int b, int r, int lane) {
-    const int R = 2 * p.gamma + 1;
-    SoftmaxStat st{-FLT_MAX, 0.0f};
-    const float2* parts = p.stat_parts + (static_cast<long long>(b) * R + r) * p.npieces;
-    for (int k = lane; k < p.npieces; k += 32) {
-        const float2 q = wait_stat(p, parts + k);
-        st = merge_stat(st, SoftmaxStat{q.x, q.y});
-    }
-    st = warp_merge_stat(st);
-    if (lane == 0) {
-        const float l2s = log2f(st.s);
-        store_stat(p.row_stat + static_cast<long long>(b) * R + r, st.m, l2s);
-        const float lz = (st.m + l2s) * kLn2;
-        if (r <= p.gamma) {
-            if (p.out_logZp) p.out_logZp[static_cast<long long>(b) * (p.gamma + 1) + r] = lz;
-        } else if (p.out_logZq) {
-            p.out_logZq[static_cast<long long>(b) * p.gamma + (r - p.gamma - 1)] = lz;
-        }
-    }
-}
-
-// One warp: the scan of sequence b (after its rows are merged); publishes the sequence.
-template <class ET>
-__device__ __forceinline__ void scan_sequence_warp(const VerifyParams& p, int b, int lane) {
-    using S = typename ET::storage;
-    const int R = 2 * p.gamma + 1;
-    const float2* rs = p.row_stat + static_cast<long long>(b) * R;
-    const float Tb = seq_T(p, b), Tdb = seq_Td(p, b);
-    const float cp = scale_of(Tb), cq = scale_of(Tdb);
-    const uint32_t bg = p.seq_base + static_cast<uint32_t>(b);
-    int j = p.gamma;
-    bool bad = false;
-    for (int i0 = 0; i0 < p.gamma; i0 += 32) {
-        const int i = i0 + lane;
-        bool reject = false;
-        if (i < p.gamma) {
-            const int d = p.tokens[static_cast<long long>(b) * p.gamma + i];
-            const float u = accept_uniform(p.key, bg, static_cast<uint32_t>(i));
-            const long long k = static_cast<long long>(b) * p.gamma + i;
-            if (p.out_u) p.out_u[k] = u;
-            if (d < 0 || d >= p.V) {
-                bad = true;
-                if (p.out_logp) p.out_logp[k] = NAN;
-                if (p.out_logq) p.out_logq[k] = NAN;
-            } else {
-                const float2 sp = wait_stat(p, rs + i), sq = wait_stat(p, rs + p.gamma + 1 + i);
-                const float xt = ET::load1(static_cast<const S*>(p.target) +
-                                           (static_cast<long long>(b) * (p.gamma + 1) + i) * p.V + d);
-                const float xd = ET::load1(static_cast<const S*>(p.draft) +
-                                           (static_cast<long long>(b) * p.gamma + i) * p.V + d);
-                const float l2p = fmaf(xt, cp, -sp.x) - sp.y;
-                const float l2q = fmaf(xd, cq, -sq.x) - sq.y;
-                if (p.out_logp) p.out_logp[k] = l2p * kLn2;
-                if (p.out_logq) p.out_logq[k] = l2q * kLn2;
-                // accept iff u < min(1, p/q); p(d) = 0 rejects, q(d) = 0 < p(d) accepts
-                reject = !((l2p > -INFINITY) && (u < exp2f(l2p - l2q)));
-            }
-        }
-        const uint32_t rej = __ballot_sync(0xffffffffu, reject);
-        if (rej && j == p.gamma) j = i0 + __ffs(rej) - 1;
-    }
-    bad = __any_sync(0xffffffffu, bad);
-    if (bad) j = -1;
-    if (lane == 0) {
-        p.out_n[b] = j;
-        SeqInfo si;
-        si.j = j;
-        si.cp = cp;
-        si.cq = cq;
-        const int rr = (j >= 0) ? j : 0;
-        const float2 sp = wait_stat(p, rs + rr);
-        si.mp = sp.x;
-        si.l2sp = sp.y;
-        if (j >= 0 && j < p.gamma) {
-            const float2 sq = wait_stat(p, rs + p.gamma + 1 + j);
-            si.mq = sq.x;
-            si.l2sq = sq.y;
-        } else {
-            si.mq = 0.0f;
-            si.l2sq = 0.0f;
-        }
-        si.pad = 0;
-        p.seq[b] = si;
-        if (j < 0) set_status(p.status, 3 /* SPEC_EBADTOKEN */);
-    }
-    int32_t* out = p.out_tokens + static_cast<long long>(b) * (p.gamma + 1);
-    for (int t = lane; t <= p.gamma; t += 32)
-        out[t] = (j >= 0 && t < j) ? p.tokens[static_cast<long long>(b) * p.gamma + t] : -1;
-    if (lane == 0) {
-        __threadfence();
-        if (!(p.debug_flags & kDebugNeverReady)) st_release(p.ready + b, 1);
-    }
-}
-
-// Race piece `piece` of sequence b (claimed): wait (bounded) for the sequence's scan, then race.
-template <class ET>
-__device__ __forceinline__ void run_claimed_race(const VerifyParams& p, int b, int piece, int lane) {
-    int ok = 0;
-    if (lane == 0) {
-        const unsigned long long t0 = global_time_ns();
-        while (!(ok = ld_acquire(p.ready + b))) {
-            if (global_time_ns() - t0 > kWaitLimitNs) break;
-            __nanosleep(500);
-        }
-        if (!ok) set_status(p.status, 4 /* SPEC_ETIMEOUT */);
-    }
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    __syncwarp();  // order the other lanes' reads after lane 0's acquire
-    if (!ok) return;
-    SeqInfo si;
-    {
-        const int4 a = __ldcg(reinterpret_cast<const int4*>(p.seq + b));
-        const float4 q = __ldcg(reinterpret_cast<const float4*>(p.seq + b) + 1);
-        si.j = a.x;
-        si.mp = __int_as_float(a.y);
-        si.l2sp = __int_as_float(a.z);
-        si.mq = __int_as_float(a.w);
-        si.l2sq = q.x;
-        si.cp = q.y;
-        si.cq = q.z;
-        si.pad = 0;
-    }
-    race_item<ET>(p, b, piece, si, lane);
-}
-
-// Resolve a row piece's arrival (ticket from the row counter): the last piece merges the row
-// and the last row runs the scan.
-template <class ET>
-__device__ __forceinline__ void resolve_arrival(const VerifyParams& p, int ticket, int b, int r,
-                                                int lane) {
-    const int R = 2 * p.gamma + 1;
-    if (ticket != p.npieces - 1) return;
-    merge_row_warp(p, b, r, lane);
-    int t = 0;
-    if (lane == 0) t = atomicAdd(p.seq_done + b, 1);
-    t = __shfl_sync(0xffffffffu, t, 0);
-    if (t != R - 1) return;
-    scan_sequence_warp<ET>(p, b, lane);
-}
-
-template <class ET, int U>
-__global__ void __launch_bounds__(256, SPECVERIFY_FUSED_MINBLOCKS) verify_fused_kernel(VerifyParams p) {
-    const int lane = threadIdx.x & 31;
-    const int R = 2 * p.gamma + 1;
-    const int P = p.npieces;
-    const int RP = R * P;
-    const long long total_rows = static_cast<long long>(p.B) * RP;
-    if ((threadIdx.x >> 5) < kStreamWarps) {
-        // pending arrival of the previous row item (lane 0 holds the ticket)
-        int pend_ticket = 0, pend_b = -1, pend_r = 0;
-        // row items are claimed kClaimChunk at a time (one atomic per chunk on the shared
-        // cursor); the next chunk is claimed while the current one streams
-        unsigned long long* cursor = reinterpret_cast<unsigned long long*>(p.row_cursor);
-        long long chunk = 0, next_chunk = 0;
-        if (lane == 0) chunk = atomicAdd(cursor, static_cast<unsigned long long>(kClaimChunk));
-        chunk = __shfl_sync(0xffffffffu, chunk, 0);
-        int in_chunk = 0;
-        while (chunk + in_chunk < total_rows) {
-            const long long g = chunk + in_chunk;
-            if (in_chunk == 0 && lane == 0)  // the next claim, used after this chunk
-                next_chunk = atomicAdd(cursor, static_cast<unsigned long long>(kClaimChunk));
-            const int b = static_cast<int>(g / RP);
-            const int within = static_cast<int>(g % RP);
-            const int r = within / P;
-            row_stats_item<ET, U>(p, b, r, within % P, lane);
-            if (pend_b >= 0)
-                resolve_arrival<ET>(p, __shfl_sync(0xffffffffu, pend_ticket, 0), pend_b, pend_r, lane);
-            if (lane == 0)
-                pend_ticket = atomicAdd(p.row_done + static_cast<long long>(b) * R + r, 1);
-            pend_b = b;
-            pend_r = r;
-            if (++in_chunk == kClaimChunk) {
-                chunk = __shfl_sync(0xffffffffu, next_chunk, 0);
-                in_chunk = 0;
-            }
-        }
-        if (pend_b >= 0)
-            resolve_arrival<ET>(p, __shfl_sync(0xffffffffu, pend_ticket, 0), pend_b, pend_r, lane);
-    }
-    // race items, in sequence order
-    const int RPc = p.rpieces;
-    const long long total_race = static_cast<long long>(p.B) * RPc;
-    while (true) {
-        long long c = 0;
-        if (lane == 0) c = atomicAdd(reinterpret_cast<unsigned long long*>(p.race_cursor), 1ull);
-        c = __shfl_sync(0xffffffffu, c, 0);
-        if (c >= total_race) break;
-        run_claimed_race<ET>(p, static_cast<int>(c / RPc), static_cast<int>(c % RPc), lane);
-    }
 }
 
 // ----------------------------------------------------------------------------------------

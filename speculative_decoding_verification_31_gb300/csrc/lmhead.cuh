@@ -370,7 +370,7 @@ lmhead_kernel(const __grid_constant__ CUtensorMap map_h0, const __grid_constant_
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         if (col0 + i < p.V) part += ex2_fast(fmaf(v[i], c, -mn));
-                    s = s * ex2_fast(m - mn) + part;
+                    s = fmaf(s, ex2_fast(m - mn), part);
                     m = mn;
                     if (tok >= col0 && tok < col0 + 32) {
 #pragma unroll

@@ -12,6 +12,7 @@
 #include <mutex>
 
 #include "kernels.cuh"
+#include "flow.cuh"
 #include "lmhead.cuh"
 #include "specverify.h"
 
@@ -25,10 +26,6 @@ constexpr int kThreads = 256;
 #define SPECVERIFY_UNROLL 8
 #endif
 constexpr int kUnroll = SPECVERIFY_UNROLL;  // 16-byte loads in flight per lane in the streaming pass
-#ifndef SPECVERIFY_FUSED_UNROLL
-#define SPECVERIFY_FUSED_UNROLL 4
-#endif
-constexpr int kFusedUnroll = SPECVERIFY_FUSED_UNROLL;
 constexpr int kMaxDevices = 64;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -38,10 +35,11 @@ int elem_bytes(int dtype) { return dtype == SPEC_F32 ? 4 : 2; }
 struct Layout {
     int piece_len, npieces;
     int rpiece_len, rpieces;
-    size_t stat_off, ext_off, seq_off, race_off, rowstat_off;
-    size_t ctl_off, ctl_bytes;          // zeroed control block: row_done, seq_done, tickets, ready
-    size_t row_done_off, seq_done_off, ticket_off, ready_off, race_cursor_off,
-        row_cursor_off;
+    size_t stat_off, ext_off, seq_off, race_off, ticket_off;
+    size_t flow_off, flow_bytes;        // flow path (verify_flow_kernel), zeroed before each call
+    size_t f_cursor_off, f_items_off, f_ready_off, f_tickets_off, f_race_off, f_second_off,
+        f_seq_off, f_stat_off;
+    int f_units;                        // flow race units per sequence
     int e_n_init, e_task_cap;           // early-exit path (verify_early_kernel)
     size_t e_rowstat_off, e_task_off, e_stat_off, e_zero_off, e_cursor_off, e_tail_off,
         e_finished_off, e_rowarr_off, e_pos_off, e_racedone_off, e_race_off, e_racetask_off,
@@ -70,28 +68,33 @@ Layout layout_of(int B, int gamma, int V, int dtype, long long stream_warps = 0)
     L.stat_off = off;
     off = align_up(off + static_cast<size_t>(B) * R * max_np * sizeof(float2), 256);
     L.ext_off = off;  // per-position statistics: entropy and cross terms per row piece
-    off = align_up(off + static_cast<size_t>(B) * R * max_np * sizeof(float2), 256);
+    L.f_stat_off = off;  // the flow path's row partials (that path computes no such terms)
+    off = align_up(off + static_cast<size_t>(B) * R * max_np * sizeof(float2) + 16, 256);
     L.seq_off = off;
     off = align_up(off + static_cast<size_t>(B) * sizeof(SeqInfo), 256);
     L.race_off = off;
     off = align_up(off + static_cast<size_t>(B) * L.rpieces * sizeof(RacePart), 256);
-    L.rowstat_off = off;
-    off = align_up(off + static_cast<size_t>(B) * R * sizeof(float2), 256);
-    L.ctl_off = off;
-    L.row_done_off = off;
-    off += static_cast<size_t>(B) * R * sizeof(int);
-    L.seq_done_off = off;
-    off += static_cast<size_t>(B) * sizeof(int);
     L.ticket_off = off;
+    off = align_up(off + static_cast<size_t>(B) * sizeof(int), 256);
+    // flow control region: the two cursors on their own 128-byte lines, then per-sequence
+    // counts, flags and tickets, the units' packed winners and runner-up scores, the scans
+    L.flow_off = off;
+    L.f_cursor_off = off;
+    off += 2 * 128;
+    L.f_items_off = off;
     off += static_cast<size_t>(B) * sizeof(int);
-    L.ready_off = off;
+    L.f_ready_off = off;
     off += static_cast<size_t>(B) * sizeof(int);
-    off = align_up(off, 8);
-    L.race_cursor_off = off;
-    off += sizeof(unsigned long long);
-    L.row_cursor_off = off;
-    off += sizeof(unsigned long long);
-    L.ctl_bytes = off - L.ctl_off;
+    L.f_tickets_off = off;
+    off = align_up(off + static_cast<size_t>(B) * sizeof(int), 16);
+    L.f_units = (V + kFlowUnitTokens - 1) / kFlowUnitTokens;
+    L.f_race_off = off;
+    off += static_cast<size_t>(B) * L.f_units * sizeof(unsigned long long);
+    L.f_second_off = off;
+    off = align_up(off + static_cast<size_t>(B) * L.f_units * sizeof(float), 16);
+    L.f_seq_off = off;
+    off = align_up(off + static_cast<size_t>(B) * sizeof(SeqInfo), 256);
+    L.flow_bytes = off - L.flow_off;
     off = align_up(off, 256);
     // early-exit region: a block filled with 0xFF before each call (merged rows, task queue,
     // then the row partials, last so that only the pieces in use need filling), then a
@@ -228,13 +231,15 @@ void bind_workspace(VerifyParams& p, const Layout& L, char* ws) {
     p.ext_parts = reinterpret_cast<float2*>(ws + L.ext_off);
     p.seq = reinterpret_cast<SeqInfo*>(ws + L.seq_off);
     p.race_parts = reinterpret_cast<RacePart*>(ws + L.race_off);
-    p.row_stat = reinterpret_cast<float2*>(ws + L.rowstat_off);
-    p.row_done = reinterpret_cast<int*>(ws + L.row_done_off);
-    p.seq_done = reinterpret_cast<int*>(ws + L.seq_done_off);
     p.tickets = reinterpret_cast<int*>(ws + L.ticket_off);
-    p.ready = reinterpret_cast<int*>(ws + L.ready_off);
-    p.race_cursor = reinterpret_cast<int*>(ws + L.race_cursor_off);
-    p.row_cursor = reinterpret_cast<int*>(ws + L.row_cursor_off);
+    p.flow.cursors = reinterpret_cast<unsigned long long*>(ws + L.f_cursor_off);
+    p.flow.items = reinterpret_cast<int*>(ws + L.f_items_off);
+    p.flow.ready = reinterpret_cast<int*>(ws + L.f_ready_off);
+    p.flow.tickets = reinterpret_cast<int*>(ws + L.f_tickets_off);
+    p.flow.race = reinterpret_cast<unsigned long long*>(ws + L.f_race_off);
+    p.flow.second = reinterpret_cast<float*>(ws + L.f_second_off);
+    p.flow.seq = reinterpret_cast<SeqInfo*>(ws + L.f_seq_off);
+    p.flow.units = L.f_units;
 }
 
 // Validated common set-up of a call: fills `p` with the workspace pointers.
@@ -274,30 +279,43 @@ int check_common(const void* target, const int32_t* out_tokens, const int32_t* o
     return SPEC_OK;
 }
 
-// Fused sampling verify: zero the control block, then one cooperative launch with every block
-// resident (the drain phase's waits rely on it).
+// Flow sampling verify (SPEC_FLAG_FUSED): flow_prep zeroes the flow region, then the flow
+// kernel runs as one cooperative launch (every block resident: its waits rely on it), started
+// as the prep kernel's programmatic dependent where the device accepts both attributes.
 template <class ET>
-int launch_fused(VerifyParams& p, int sm_count, const spec_verify_opts* o, cudaStream_t s,
-                 const Layout& L, char* ws) {
-    auto kernel = verify_fused_kernel<ET, kFusedUnroll>;
+int launch_flow(VerifyParams& p, int sm_count, const spec_verify_opts* o, cudaStream_t s,
+                const Layout& L, char* ws) {
+    auto kernel = verify_flow_kernel<ET, kUnroll>;
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) != cudaSuccess ||
         per_sm < 1)
         return SPEC_ECUDA;
-    const int R = 2 * p.gamma + 1;
-    const long long rows = static_cast<long long>(p.B) * R * p.npieces;
-    long long grid = static_cast<long long>(sm_count) * per_sm;
-    (void)rows;  // every block has race warps: keep the full resident grid
-    if (cudaMemsetAsync(ws + L.ctl_off, 0, L.ctl_bytes, s) != cudaSuccess) return SPEC_ECUDA;
-    // row partials and merged rows start empty (see kStatEmpty)
-    if (cudaMemsetAsync(ws + L.stat_off, 0xFF, L.seq_off - L.stat_off, s) != cudaSuccess ||
-        cudaMemsetAsync(ws + L.rowstat_off, 0xFF, L.ctl_off - L.rowstat_off, s) != cudaSuccess)
-        return SPEC_ECUDA;
+    p.stat_parts = reinterpret_cast<float2*>(ws + L.f_stat_off);
+    // both zeroed ranges are whole 16-byte words inside their regions (256-byte aligned ends)
+    const long long n_ctl = static_cast<long long>(L.flow_bytes / 16);
+    const long long n_stat = static_cast<long long>(
+        (static_cast<size_t>(p.B) * (2 * p.gamma + 1) * p.npieces * sizeof(unsigned long long) + 15) / 16);
+    long long prep_grid = (n_ctl + n_stat + kThreads - 1) / kThreads;
+    if (prep_grid > 2LL * sm_count) prep_grid = 2LL * sm_count;
     record(o, 0, s);
-    void* args[] = {&p};
-    if (cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kernel), dim3(static_cast<unsigned>(grid)),
-                                    dim3(kThreads), args, 0, s) != cudaSuccess)
-        return SPEC_ECUDA;
+    flow_prep_kernel<<<static_cast<unsigned>(prep_grid < 1 ? 1 : prep_grid), kThreads, 0, s>>>(
+        reinterpret_cast<uint4*>(ws + L.flow_off), n_ctl, reinterpret_cast<uint4*>(ws + L.f_stat_off), n_stat);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(sm_count * per_sm));
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    if (cudaLaunchKernelEx(&cfg, kernel, p) != cudaSuccess) {
+        (void)cudaGetLastError();  // not accepted together: a plain cooperative launch
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, kernel, p) != cudaSuccess) return SPEC_ECUDA;
+    }
     record(o, 1, s);
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
 }
@@ -346,7 +364,9 @@ int launch_sampling(VerifyParams& p, int sm_count, const spec_verify_opts* o, cu
                                         kThreads, 0, s>>>(p);
     }
     record(o, 1, s);
-    // blocks per sequence: about one resident wave of scan-race blocks in total
+    // scan-race grid: one resident wave of blocks sharing the B * rpieces race pieces evenly
+    // (one block per sequence when the sequences alone fill the wave)
+    long long grid;
     {
         int per_sm = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, scan_race_kernel<ET>, kThreads,
@@ -354,14 +374,12 @@ int launch_sampling(VerifyParams& p, int sm_count, const spec_verify_opts* o, cu
             per_sm < 1)
             per_sm = 1;
         const long long wave = static_cast<long long>(sm_count) * per_sm;
-        long long G = wave / p.B;  // rounded down: no partial second wave
-        if (G > p.rpieces) G = p.rpieces;
-        if (G < 1) G = 1;
-        p.rgroups = static_cast<int>(G);
+        const long long pieces = static_cast<long long>(p.B) * p.rpieces;
+        grid = p.B >= wave ? p.B : (pieces < wave ? pieces : wave);
     }
     // (no PDL when an event is recorded between the kernels, so that each one is timed alone)
-    if (launch_pdl(scan_race_kernel<ET>, static_cast<int>(static_cast<long long>(p.B) * p.rgroups),
-                   2 * R * sizeof(float), s, !(o && o->prof_events[1]), p) != cudaSuccess)
+    if (launch_pdl(scan_race_kernel<ET>, static_cast<int>(grid), 2 * R * sizeof(float), s,
+                   !(o && o->prof_events[1]), p) != cudaSuccess)
         return SPEC_ECUDA;
     record(o, 2, s);
     if (extra) {
@@ -560,8 +578,8 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, const in
                                  : launch_early<Bf16Elem>(p, d->sm_count, opts, s, L, ws);
     const bool fused = d->coop && opts && (opts->flags & SPEC_FLAG_FUSED) && !wants_position_stats(p);
     if (fused) {
-        return dtype == SPEC_F32 ? launch_fused<F32Elem>(p, d->sm_count, opts, s, L, ws)
-                                 : launch_fused<Bf16Elem>(p, d->sm_count, opts, s, L, ws);
+        return dtype == SPEC_F32 ? launch_flow<F32Elem>(p, d->sm_count, opts, s, L, ws)
+                                 : launch_flow<Bf16Elem>(p, d->sm_count, opts, s, L, ws);
     }
     return dtype == SPEC_F32 ? launch_sampling<F32Elem>(p, d->sm_count, opts, s)
                              : launch_sampling<Bf16Elem>(p, d->sm_count, opts, s);
@@ -726,9 +744,10 @@ int spec_verify_tree(const void* target_logits, const void* draft_logits, const 
     DeviceState* d = nullptr;
     rc = prepare(B, gamma_eq, V, dtype, opts, p, &d);
     if (rc) return rc;
-    // the per-sequence race records live in the fused path's merged-row area (B * R float2
-    // >= B TreeRace), which the tree path does not otherwise use
-    p.tree_race = reinterpret_cast<TreeRace*>(p.row_stat);
+    // the per-sequence race records live in the flow path's scan area (B SeqInfo of 32 bytes
+    // >= B TreeRace of 16), which the tree path does not otherwise use
+    static_assert(sizeof(TreeRace) <= sizeof(SeqInfo), "the scan area holds the race records");
+    p.tree_race = reinterpret_cast<TreeRace*>(p.flow.seq);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return dtype == SPEC_F32 ? launch_tree<F32Elem>(p, t, d->sm_count, opts, s)
                              : launch_tree<Bf16Elem>(p, t, d->sm_count, opts, s);
@@ -1252,8 +1271,8 @@ extern "C" int spec_verify_noalloc(const void* target_logits, const void* draft_
         if (cudaMemsetAsync(p.status, 0, sizeof(int32_t), s) != cudaSuccess) return SPEC_ECUDA;
     }
     if (nd->coop && opts && (opts->flags & SPEC_FLAG_FUSED))
-        return dtype == SPEC_F32 ? launch_fused<F32Elem>(p, nd->sm_count, opts, s, L, ws)
-                                 : launch_fused<Bf16Elem>(p, nd->sm_count, opts, s, L, ws);
+        return dtype == SPEC_F32 ? launch_flow<F32Elem>(p, nd->sm_count, opts, s, L, ws)
+                                 : launch_flow<Bf16Elem>(p, nd->sm_count, opts, s, L, ws);
     return dtype == SPEC_F32 ? launch_sampling<F32Elem>(p, nd->sm_count, opts, s)
                              : launch_sampling<Bf16Elem>(p, nd->sm_count, opts, s);
 }
