@@ -332,6 +332,50 @@ int spec_adaptive_k(const float *H_next, int B, int K, const double *centres,
                     const int32_t *candidates, int n_cand, double C_d, double C_v,
                     int32_t *out_k, double *out_eff, void *stream);
 
+/*
+ * Vocabulary-parallel sampling verify ("How speculative decoding makes LLMs go brrr":
+ * pseudocode and module 3, with the logits split by vocabulary column over W ranks, as a
+ * tensor-parallel LM head leaves them).  Rank w holds target_shard [B, gamma+1, V_w] and
+ * draft_shard [B, gamma, V_w]: columns [x_w, x_w + V_w) of every row, x_w a multiple of 8.
+ * One verify is, on every rank, in this order on one stream:
+ *   1. spec_vp_partials   -> stats [B, 2 gamma + 1, 2] (fp32 scaled max and sum of each row's
+ *                            columns, base 2) and gathered [B, gamma, 2] (the target and draft
+ *                            logits at each draft token the rank holds, -inf where it does not);
+ *   2. the caller all-gathers stats into stats_all [W, B, 2 gamma + 1, 2] (rank order) and
+ *      max-reduces gathered over the ranks;
+ *   3. spec_vp_decide     -> out_tokens (accepted prefix, -1 padding; the drawn token's slot
+ *                            is written in step 6), out_n_accepted, and state;
+ *   4. spec_vp_race       -> keys [B, 2] int64: the rank's race winners (the residual race,
+ *                            and the race over p_j where the rank's residual weights are all
+ *                            zero), each as a key whose signed maximum is the winner;
+ *   5. the caller max-reduces keys over the ranks;
+ *   6. spec_vp_finish     -> the drawn token into out_tokens[b, j].
+ * Random numbers are keyed by the global token index, so the result is the one-GPU verify's,
+ * except that the two merge orders may round a near-tie (|u - p/q| or the top two race
+ * scores within the tolerances of spec_verify) the other way.  All pointers are device
+ * memory owned by the caller; state holds spec_vp_state_bytes(B) bytes (opaque), written by
+ * step 3 and read by steps 4 and 6.  opts (may be NULL) supplies dtype, T_per_seq,
+ * Td_per_seq, seq_index_base and d_status as in spec_verify_ex; step 1 uses the library
+ * workspace (or opts->workspace, of spec_verify_workspace_bytes(B, gamma, V_w, dtype)).
+ * Draft tokens outside [0, V) are reported by step 3 as in spec_verify (n_accepted = -1,
+ * SPEC_EBADTOKEN in the status word).  SPEC_EINVAL for bad sizes, NULL or misaligned
+ * pointers, an x_offset that is not a multiple of 8, bad temperatures.
+ */
+size_t spec_vp_state_bytes(int B);
+int spec_vp_partials(const void *target_shard, const void *draft_shard, const int32_t *draft_tokens,
+                     int B, int gamma, int V_shard, int x_offset, float T, float T_d,
+                     float *out_stats, float *out_gathered, const spec_verify_opts *opts,
+                     void *stream);
+int spec_vp_decide(const float *stats_all, int world, const float *gathered,
+                   const int32_t *draft_tokens, int B, int gamma, int V, float T, float T_d,
+                   uint64_t seed, int32_t *out_tokens, int32_t *out_n_accepted, void *state,
+                   const spec_verify_opts *opts, void *stream);
+int spec_vp_race(const void *target_shard, const void *draft_shard, int B, int gamma, int V_shard,
+                 int x_offset, uint64_t seed, const void *state, int64_t *out_keys,
+                 const spec_verify_opts *opts, void *stream);
+int spec_vp_finish(const int64_t *keys, const void *state, int B, int gamma, int32_t *out_tokens,
+                   void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -11,3 +11,6 @@ from .specverify import (  # noqa: F401
     spec_verify_workspace_bytes, spec_row_entropy, spec_adaptive_k, spec_verify_tree, Tree,
     spec_verify_host, SPEC_FLAG_FULL_READ, spec_lmhead_logits, spec_lmhead_row_stats,
     spec_verify_lmhead)
+from .vocab_parallel import (  # noqa: F401
+    LibraryBackend, VocabShard, spec_vp_decide, spec_vp_finish, spec_vp_partials, spec_vp_race,
+    verify_vocab_parallel, vocab_range)

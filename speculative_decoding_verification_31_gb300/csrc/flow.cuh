@@ -74,24 +74,26 @@ __device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned l
 // from each lane's largest logit (a fast lower bound of its score) and raised to the warp's
 // best exact score after every group, and a token is scored exactly only if it passes the
 // bound test (see kRaceBoundMargin2).  Each lane offers its tokens in increasing x, so the
-// result is the same winner, bit for bit, as any other split of the row.
+// result is the same winner, bit for bit, as any other split of the row.  rt and rd hold
+// tokens xoff, xoff + 1, ... of the row (a vocabulary shard; xoff a multiple of 8): random
+// numbers and the winner's index are those of token x + xoff.
 template <class ET>
 __device__ __forceinline__ RaceState race_warp_span(const VerifyParams& p,
                                                    const typename ET::storage* rt,
                                                    const typename ET::storage* rd, bool residual,
                                                    uint32_t bg, uint32_t pos, int xa, int xb,
-                                                   const SeqInfo& si, int lane) {
+                                                   const SeqInfo& si, int lane, int xoff = 0) {
     constexpr int VPL = kRaceWarpTokens / (32 * ET::kVec);
     const RaceRowRng q = race_row_rng(p.rk, bg, pos);
     RaceState st{-INFINITY, INT_MAX, -INFINITY};
     auto word_at = [&](int x) {
-        const uint4 blk = race_block_fast(q, p.rk, static_cast<uint32_t>(x) >> 2);
-        return word_of(blk, static_cast<uint32_t>(x) & 3u);
+        const uint4 blk = race_block_fast(q, p.rk, static_cast<uint32_t>(x + xoff) >> 2);
+        return word_of(blk, static_cast<uint32_t>(x + xoff) & 3u);
     };
     auto offer_exact = [&](float xt, int x, uint32_t w) {
         const float xd = residual ? ET::load1(rd + x) : 0.0f;
         const float sc = race_exact_score(xt, xd, si, residual, w);
-        if (sc > -INFINITY) race_offer(st, sc, x);
+        if (sc > -INFINITY) race_offer(st, sc, x + xoff);
     };
     auto load_chunk = [&](int x0, uint4 (&dst)[VPL]) {
         const int x1 = min(xb, x0 + kRaceWarpTokens);
@@ -158,7 +160,7 @@ __device__ __forceinline__ RaceState race_warp_span(const VerifyParams& p,
                     for (int gg = 0; gg < BPV; ++gg)
                         blk[kk * BPV + gg] = race_block_fast(
                             q, p.rk,
-                            static_cast<uint32_t>(x0 + (lane + 32 * (k0 + kk)) * ET::kVec + 4 * gg) >> 2);
+                            static_cast<uint32_t>(xoff + x0 + (lane + 32 * (k0 + kk)) * ET::kVec + 4 * gg) >> 2);
 #pragma unroll
                 for (int kk = 0; kk < VG; ++kk) {
                     const int v = lane + 32 * (k0 + kk);

@@ -13,6 +13,7 @@
 
 #include "kernels.cuh"
 #include "flow.cuh"
+#include "vocab.cuh"
 #include "lmhead.cuh"
 #include "specverify.h"
 
@@ -1165,6 +1166,158 @@ const char* spec_verify_strerror(int status) {
         case SPEC_ESCRATCH: return "problem needs more scratch than the static no-alloc buffer";
         default: return "unknown status";
     }
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------------------------------------
+// Vocabulary-parallel verify (vocab.cuh): each rank's steps around two small collectives that
+// the caller runs (an all-gather of the row statistics and the gathered logits' max, then a
+// max of the race keys).
+// ------------------------------------------------------------------------------------------
+
+namespace {
+
+// The parameters shared by the vocabulary-parallel steps; V is the shard's width (or, for
+// vp_decide, the whole vocabulary).
+void vp_params(VerifyParams& p, const void* target, const void* draft, const int32_t* tokens, int B,
+               int gamma, int V, float T, float T_d, uint64_t seed, const spec_verify_opts* o) {
+    p.target = target;
+    p.draft = draft;
+    p.tokens = tokens;
+    p.B = B;
+    p.gamma = gamma;
+    p.V = V;
+    p.T = T;
+    p.Td = T_d;
+    p.T_seq = o ? o->T_per_seq : nullptr;
+    p.Td_seq = o ? o->Td_per_seq : nullptr;
+    p.key = philox_key(seed);
+    p.rk = philox_round_keys(p.key);
+    p.seq_base = o ? o->seq_index_base : 0u;
+}
+
+int vp_shape_ok(int B, int gamma, int V, int x_offset, int dtype) {
+    if (B < 0 || gamma < 0 || gamma > kMaxGamma || V < 1 || x_offset < 0 || (x_offset & 7)) return SPEC_EINVAL;
+    if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_EINVAL;
+    if (static_cast<long long>(B) * (gamma + 1) * static_cast<long long>(V) >= (1LL << 40)) return SPEC_EINVAL;
+    return SPEC_OK;
+}
+
+int vp_temps_ok(float T, float T_d, const spec_verify_opts* o) {
+    if (!(o && o->T_per_seq) && !good_temperature(T)) return SPEC_EINVAL;
+    if (!(o && o->Td_per_seq) && !good_temperature(T_d)) return SPEC_EINVAL;
+    return SPEC_OK;
+}
+
+int status_word(const spec_verify_opts* o, int32_t** st) {
+    if (o && o->d_status) {
+        *st = o->d_status;
+        return SPEC_OK;
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState* d = nullptr;
+    const int rc = device_state(&d);
+    if (rc) return rc;
+    *st = d->status;
+    return SPEC_OK;
+}
+
+template <class ET>
+int launch_vp_partials(VerifyParams& p, int sm_count, int x_offset, float2* stats, float2* gathered,
+                       cudaStream_t s) {
+    const int R = 2 * p.gamma + 1;
+    const long long items = static_cast<long long>(p.B) * R * p.npieces;
+    row_stats_kernel<ET, kUnroll><<<grid_for(row_stats_kernel<ET, kUnroll>, sm_count, items), kThreads, 0, s>>>(p);
+    const long long rows = static_cast<long long>(p.B) * R;
+    vp_fold_kernel<<<static_cast<unsigned>(std::min<long long>((rows + kThreads - 1) / kThreads, 4LL * sm_count)),
+                     kThreads, 0, s>>>(p, stats);
+    const long long n = static_cast<long long>(p.B) * p.gamma;
+    if (n > 0)
+        vp_gather_kernel<ET><<<static_cast<unsigned>(std::min<long long>((n + kThreads - 1) / kThreads, 4LL * sm_count)),
+                               kThreads, 0, s>>>(p, x_offset, gathered);
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t spec_vp_state_bytes(int B) { return B > 0 ? static_cast<size_t>(B) * sizeof(VpState) : 0; }
+
+int spec_vp_partials(const void* target_shard, const void* draft_shard, const int32_t* draft_tokens,
+                     int B, int gamma, int V_shard, int x_offset, float T, float T_d, float* out_stats,
+                     float* out_gathered, const spec_verify_opts* opts, void* stream) {
+    const int dtype = opts ? opts->dtype : SPEC_BF16;
+    int rc = vp_shape_ok(B, gamma, V_shard, x_offset, dtype);
+    if (rc || B == 0) return rc;
+    if (!target_shard || !aligned16(target_shard) || !out_stats) return SPEC_EINVAL;
+    if (gamma > 0 && (!draft_shard || !aligned16(draft_shard) || !draft_tokens || !out_gathered))
+        return SPEC_EINVAL;
+    if ((rc = vp_temps_ok(T, T_d, opts))) return rc;
+    VerifyParams p{};
+    vp_params(p, target_shard, draft_shard, draft_tokens, B, gamma, V_shard, T, T_d, 0, opts);
+    DeviceState* d = nullptr;
+    rc = prepare(B, gamma, V_shard, dtype, opts, p, &d);
+    if (rc) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    float2* st = reinterpret_cast<float2*>(out_stats);
+    float2* ga = reinterpret_cast<float2*>(out_gathered);
+    return dtype == SPEC_F32 ? launch_vp_partials<F32Elem>(p, d->sm_count, x_offset, st, ga, s)
+                             : launch_vp_partials<Bf16Elem>(p, d->sm_count, x_offset, st, ga, s);
+}
+
+int spec_vp_decide(const float* stats_all, int world, const float* gathered, const int32_t* draft_tokens,
+                   int B, int gamma, int V, float T, float T_d, uint64_t seed, int32_t* out_tokens,
+                   int32_t* out_n_accepted, void* state, const spec_verify_opts* opts, void* stream) {
+    const int dtype = opts ? opts->dtype : SPEC_BF16;
+    int rc = vp_shape_ok(B, gamma, V, 0, dtype);
+    if (rc || B == 0) return rc;
+    if (world < 1 || !stats_all || !out_tokens || !out_n_accepted || !state) return SPEC_EINVAL;
+    if (gamma > 0 && (!gathered || !draft_tokens)) return SPEC_EINVAL;
+    if ((rc = vp_temps_ok(T, T_d, opts))) return rc;
+    VerifyParams p{};
+    vp_params(p, nullptr, nullptr, draft_tokens, B, gamma, V, T, T_d, seed, opts);
+    p.out_tokens = out_tokens;
+    p.out_n = out_n_accepted;
+    if ((rc = status_word(opts, &p.status))) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    vp_decide_kernel<<<static_cast<unsigned>((static_cast<long long>(B) * 32 + kThreads - 1) / kThreads), kThreads, 0,
+                       s>>>(p, reinterpret_cast<const float2*>(stats_all), world,
+                            reinterpret_cast<const float2*>(gathered), static_cast<VpState*>(state));
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
+}
+
+int spec_vp_race(const void* target_shard, const void* draft_shard, int B, int gamma, int V_shard,
+                 int x_offset, uint64_t seed, const void* state, int64_t* out_keys,
+                 const spec_verify_opts* opts, void* stream) {
+    const int dtype = opts ? opts->dtype : SPEC_BF16;
+    int rc = vp_shape_ok(B, gamma, V_shard, x_offset, dtype);
+    if (rc || B == 0) return rc;
+    if (!target_shard || !aligned16(target_shard) || !state || !out_keys) return SPEC_EINVAL;
+    if (gamma > 0 && (!draft_shard || !aligned16(draft_shard))) return SPEC_EINVAL;
+    VerifyParams p{};
+    vp_params(p, target_shard, draft_shard, nullptr, B, gamma, V_shard, 1.0f, 1.0f, seed, opts);
+    if ((rc = status_word(opts, &p.status))) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    auto* keys = reinterpret_cast<long long*>(out_keys);
+    const auto* vs = static_cast<const VpState*>(state);
+    if (dtype == SPEC_F32)
+        vp_race_kernel<F32Elem><<<static_cast<unsigned>(B), kThreads, 0, s>>>(p, x_offset, vs, keys);
+    else
+        vp_race_kernel<Bf16Elem><<<static_cast<unsigned>(B), kThreads, 0, s>>>(p, x_offset, vs, keys);
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
+}
+
+int spec_vp_finish(const int64_t* keys, const void* state, int B, int gamma, int32_t* out_tokens,
+                   void* stream) {
+    if (B < 0 || gamma < 0 || gamma > kMaxGamma) return SPEC_EINVAL;
+    if (B == 0) return SPEC_OK;
+    if (!keys || !state || !out_tokens) return SPEC_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    vp_finish_kernel<<<static_cast<unsigned>((B + kThreads - 1) / kThreads), kThreads, 0, s>>>(
+        B, gamma, static_cast<const VpState*>(state), reinterpret_cast<const long long*>(keys), out_tokens);
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
 }
 
 }  // extern "C"

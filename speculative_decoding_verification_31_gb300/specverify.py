@@ -26,7 +26,8 @@ EXPORTED = ("spec_verify", "spec_verify_greedy", "spec_verify_ex", "spec_verify_
             "spec_verify_workspace_bytes", "spec_verify_check", "spec_verify_strerror",
             "spec_verify_opts_init", "spec_verify_noalloc", "spec_row_entropy",
             "spec_adaptive_k", "spec_verify_tree", "spec_verify_host", "spec_lmhead_logits",
-            "spec_lmhead_row_stats", "spec_verify_lmhead")
+            "spec_lmhead_row_stats", "spec_verify_lmhead", "spec_vp_state_bytes",
+            "spec_vp_partials", "spec_vp_decide", "spec_vp_race", "spec_vp_finish")
 
 
 class SpecVerifyError(RuntimeError):
@@ -106,6 +107,14 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     D = ctypes.c_double
     lib.spec_adaptive_k.argtypes = [P, I, I, P, P, I, D, D, P, P, P]
     lib.spec_adaptive_k.restype = ctypes.c_int
+    lib.spec_vp_state_bytes.argtypes = [I]
+    lib.spec_vp_state_bytes.restype = ctypes.c_size_t
+    lib.spec_vp_partials.argtypes = [P, P, P, I, I, I, I, F, F, P, P, OP, P]
+    lib.spec_vp_decide.argtypes = [P, I, P, P, I, I, I, F, F, U64, P, P, P, OP, P]
+    lib.spec_vp_race.argtypes = [P, P, I, I, I, I, U64, P, P, OP, P]
+    lib.spec_vp_finish.argtypes = [P, P, I, I, P, P]
+    for f in ("spec_vp_partials", "spec_vp_decide", "spec_vp_race", "spec_vp_finish"):
+        getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
 

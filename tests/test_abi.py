@@ -35,7 +35,8 @@ def test_header_declares_the_boundary():
               "spec_verify_workspace_bytes", "spec_verify_check", "spec_verify_strerror",
               "spec_verify_opts_init", "spec_verify_noalloc", "spec_row_entropy", "spec_adaptive_k",
               "spec_verify_tree", "spec_verify_host", "spec_lmhead_logits",
-              "spec_lmhead_row_stats", "spec_verify_lmhead"):
+              "spec_lmhead_row_stats", "spec_verify_lmhead", "spec_vp_state_bytes",
+              "spec_vp_partials", "spec_vp_decide", "spec_vp_race", "spec_vp_finish"):
         assert f in names
 
 
@@ -116,6 +117,45 @@ def test_host_validation_rejects_bad_sizes_without_a_device(lib):
     opts.dtype = 5
     assert lib.spec_verify_ex(fake, fake, fake, 1, 3, 10, 1.0, 1.0, 0, fake, fake,
                               ctypes.byref(opts), None) == EINVAL
+
+
+def test_vocab_parallel_validation_without_a_device(lib):
+    """The vocabulary-parallel steps reject bad sizes, offsets and pointers on the host."""
+    import speculative_decoding_verification_31_gb300 as sv
+    P = ctypes.c_void_p
+    fake = P(256)
+    EINVAL = sv.SPEC_EINVAL
+    # x_offset must be a multiple of 8; B, gamma, V in range; pointers present and aligned
+    assert lib.spec_vp_partials(fake, fake, fake, 2, 3, 100, 4, 1.0, 1.0, fake, fake, None, None) == EINVAL
+    assert lib.spec_vp_partials(fake, fake, fake, 2, 3, 0, 0, 1.0, 1.0, fake, fake, None, None) == EINVAL
+    assert lib.spec_vp_partials(P(258), fake, fake, 2, 3, 100, 0, 1.0, 1.0, fake, fake, None, None) == EINVAL
+    assert lib.spec_vp_partials(fake, fake, fake, 2, 3, 100, 8, 0.0, 1.0, fake, fake, None, None) == EINVAL
+    assert lib.spec_vp_partials(fake, None, fake, 2, 3, 100, 8, 1.0, 1.0, fake, fake, None, None) == EINVAL
+    assert lib.spec_vp_decide(fake, 0, fake, fake, 2, 3, 100, 1.0, 1.0, 0, fake, fake, fake, None, None) == EINVAL
+    assert lib.spec_vp_decide(fake, 2, fake, fake, 2, 3, 100, 1.0, 1.0, 0, fake, fake, None, None, None) == EINVAL
+    assert lib.spec_vp_race(fake, fake, 2, 3, 100, 12, 0, fake, fake, None, None) == EINVAL
+    assert lib.spec_vp_race(fake, fake, 2, 3, 100, 8, 0, None, fake, None, None) == EINVAL
+    assert lib.spec_vp_finish(None, fake, 2, 3, fake, None) == EINVAL
+    # empty batch: nothing to do
+    assert lib.spec_vp_partials(None, None, None, 0, 3, 100, 0, 1.0, 1.0, None, None, None, None) == 0
+    assert lib.spec_vp_finish(None, None, 0, 3, None, None) == 0
+    assert lib.spec_vp_state_bytes(0) == 0 and lib.spec_vp_state_bytes(5) == 5 * 32
+
+
+def test_vocab_range_partitions():
+    from speculative_decoding_verification_31_gb300.vocab_parallel import vocab_range
+    for V in (8, 17, 1001, 128256, 152064):
+        for world in (1, 2, 3, 8):
+            if -(-V // 8) < world:
+                with pytest.raises(ValueError):
+                    vocab_range(V, world, 0)
+                continue
+            ranges = [vocab_range(V, world, r) for r in range(world)]
+            assert ranges[0][0] == 0 and ranges[-1][1] == V
+            for (a, b), (c, d) in zip(ranges, ranges[1:]):
+                assert b == c and a % 8 == 0 and c % 8 == 0 and b > a
+            blocks = [-(-(b - a) // 8) for a, b in ranges]
+            assert max(blocks) - min(blocks) <= 1
 
 
 def test_product_path_does_not_import_the_oracle():
