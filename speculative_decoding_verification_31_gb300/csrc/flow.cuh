@@ -11,11 +11,11 @@
 // the first sequences start while the last row items are still being read.
 //
 // Work:
-//   row items   (b, r, piece) in sequence-major order, claimed from one cursor by every warp
-//               (the next claim in flight while the current item streams): the streaming
-//               pass's item (partial softmax statistics of one row piece, one packed 64-bit
-//               word), then one relaxed increment of the sequence's item count.  Row items
-//               never wait.
+//   row items   (b, r, piece) in sequence-major order, dealt round-robin to every warp (a
+//               shared claim counter would throttle the stream: measured, its atomics cost
+//               more than half the bandwidth): the streaming pass's item (partial softmax
+//               statistics of one row piece, one packed 64-bit word), then one relaxed
+//               increment of the sequence's item count.  Row items never wait.
 //   race units  (b, u): tokens [u K, (u+1) K) of sequence b's raced row, claimed from a second
 //               cursor once a warp finds no row item left, in spans of consecutive units that
 //               shrink as the units run out (guided self-scheduling).  A span starting at unit
@@ -414,18 +414,15 @@ __global__ void __launch_bounds__(256, SPECVERIFY_FLOW_MINBLOCKS) verify_flow_ke
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the flow region has been zeroed
     const long long RP = static_cast<long long>(2 * p.gamma + 1) * p.npieces;
     const long long total = static_cast<long long>(p.B) * RP;
-    {  // every warp streams row items until they run out, then races
-        long long g = 0;
-        if (lane == 0) g = static_cast<long long>(atomicAdd(p.flow.cursors, 1ull));
-        g = __shfl_sync(0xffffffffu, g, 0);
-        while (g < total) {
-            long long gn = 0;  // the next claim, in flight while this item streams
-            if (lane == 0) gn = static_cast<long long>(atomicAdd(p.flow.cursors, 1ull));
+    {  // every warp streams its row items (round-robin over the warps, in sequence-major
+       // order: one shared claim counter throttles the stream), then races
+        const long long nw = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+        for (long long g = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; g < total;
+             g += nw) {
             const int b = static_cast<int>(g / RP);
             const int within = static_cast<int>(g % RP);
             row_stats_item<ET, UNR, kFlowLoads>(p, b, within / p.npieces, within % p.npieces, lane);
             if (lane == 0) red_add_relaxed(p.flow.items + b, 1);
-            g = __shfl_sync(0xffffffffu, gn, 0);
         }
     }
     // race units, claimed in spans that shrink as the units run out (guided self-scheduling:
