@@ -122,6 +122,11 @@ struct VerifyParams {
     struct TreeRace* tree_race; // [B] the node each sequence races
 };
 
+// Race partial slots per sequence: at most one per block racing it.  A block of the
+// scan-race grid takes at least one step of chunks, so a sequence meets at most
+// ceil(V / kRaceBlockTokens) + 1 blocks; the tree and LM-head races use at most rpieces.
+__host__ __device__ __forceinline__ int race_slots(int rpieces) { return rpieces + 1; }
+
 // Row pieces of the streaming passes: between kMinPieceBytes and kMaxPieceBytes of logits
 // (the early-exit path: kEarlyPieceBytes).
 #ifndef SPECVERIFY_PIECE_BYTES
@@ -279,7 +284,7 @@ __global__ void __launch_bounds__(256, SPECVERIFY_STATS_MINBLOCKS) row_stats_ker
     const int lane = threadIdx.x & 31;
     const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
     const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    for (long long k = tid; k < static_cast<long long>(p.B) * p.rpieces; k += nthreads)
+    for (long long k = tid; k < static_cast<long long>(p.B) * race_slots(p.rpieces); k += nthreads)
         reinterpret_cast<uint4*>(p.race_parts)[k] = make_uint4(0u, 0u, 0u, 0u);
     for (long long k = tid; k < p.B; k += nthreads) p.tickets[k] = 0;
     const long long nwarps = nthreads >> 5;
@@ -458,7 +463,7 @@ __global__ void __launch_bounds__(256, SPECVERIFY_PAIR_MINBLOCKS) pair_stats_ker
     const int lane = threadIdx.x & 31;
     const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
     const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    for (long long k = tid; k < static_cast<long long>(p.B) * p.rpieces; k += nthreads)
+    for (long long k = tid; k < static_cast<long long>(p.B) * race_slots(p.rpieces); k += nthreads)
         reinterpret_cast<uint4*>(p.race_parts)[k] = make_uint4(0u, 0u, 0u, 0u);
     for (long long k = tid; k < p.B; k += nthreads) p.tickets[k] = 0;
     const long long nwarps = nthreads >> 5;
@@ -942,6 +947,7 @@ __device__ __forceinline__ RaceState race_piece(const typename ET::storage* rt,
 
 constexpr int kRaceWarpTokens = 1024;
 constexpr int kRaceBlockTokens = 8 * kRaceWarpTokens;
+constexpr int kRaceBlockChunks = kRaceBlockTokens / kRaceWarpTokens;  // one chunk per warp
 #ifndef SPECVERIFY_RACE_CHAINS
 #define SPECVERIFY_RACE_CHAINS 8
 #endif
@@ -1003,15 +1009,17 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64g(const void* p) {
 
 // The race of sequence b by one of the `nslots` blocks that share it, over target row rt
 // (and, for a residual, draft row rd; statistics in si) with random-number row `pos`: race
-// pieces pc_begin, pc_begin + pc_step, ... (< pc_end), publish the block's winner in
+// the chunks cb + w (warp w) for cb = cb_begin, cb_begin + cb_step, ... (< cb_end), chunks
+// from ch_limit on excluded, publish the block's winner in
 // partial slot `slot`, and if this is the sequence's last block to finish, merge the
 // blocks' winners and write the token to *out.
 template <class ET>
 __device__ __forceinline__ void race_rows_block(const VerifyParams& p, int b,
                                                const typename ET::storage* rt,
                                                const typename ET::storage* rd, bool residual,
-                                               uint32_t pos, int32_t* out, int pc_begin,
-                                               int pc_end, int pc_step, int slot, int nslots,
+                                               uint32_t pos, int32_t* out, int cb_begin,
+                                               int cb_end, int cb_step, int ch_limit, int slot,
+                                               int nslots,
                                                const SeqInfo& si, float* s_thr,
                                                RaceState* s_best, int& s_last) {
     using S = typename ET::storage;
@@ -1029,10 +1037,15 @@ __device__ __forceinline__ void race_rows_block(const VerifyParams& p, int b,
         const float sc = race_exact_score(xt, xd, si, residual, w);
         if (sc > -INFINITY) race_offer(st, sc, x);
     };
-    // This block races pieces g, g + G, ... of the row (warp w: tokens [w, w+1) x 1024 of a
-    // piece).  Vectors of the next piece are loaded before the current one is computed.
-    auto load_piece = [&](int pc, uint4 (&dst)[VPL]) {
-        const int x0 = pc * kRaceBlockTokens + wib * kRaceWarpTokens;
+    // Step k races chunks cb + w (warp w) of kRaceWarpTokens tokens, cb = cb_begin + k cb_step
+    // < cb_end, chunks from ch_limit on excluded.  Vectors of the next step are loaded before
+    // the current one is computed.
+    auto chunk_x0 = [&](int cb) {
+        const int ch = cb + wib;
+        return ch < ch_limit ? ch * kRaceWarpTokens : p.V;
+    };
+    auto load_piece = [&](int cb, uint4 (&dst)[VPL]) {
+        const int x0 = chunk_x0(cb);
         const int x1 = min(p.V, x0 + kRaceWarpTokens);
         const bool ok = x0 < x1 && (reinterpret_cast<uintptr_t>(rt + x0) & 15u) == 0;
         const int nv = ok ? (x1 - x0) / ET::kVec : 0;
@@ -1045,15 +1058,15 @@ __device__ __forceinline__ void race_rows_block(const VerifyParams& p, int b,
         }
     };
     uint4 raw[VPL], raw_next[VPL];
-    load_piece(pc_begin, raw);
+    load_piece(cb_begin, raw);
     float thr = -INFINITY;
     bool first = true;
-    for (int pc = pc_begin; pc < pc_end; pc += pc_step) {
-        const int x0 = pc * kRaceBlockTokens + wib * kRaceWarpTokens;
+    for (int cb = cb_begin; cb < cb_end; cb += cb_step) {
+        const int x0 = chunk_x0(cb);
         const int x1 = min(p.V, x0 + kRaceWarpTokens);
         const bool vec_ok = x0 < x1 && (reinterpret_cast<uintptr_t>(rt + x0) & 15u) == 0;
         const int nvec = vec_ok ? (x1 - x0) / ET::kVec : 0;
-        if (pc + pc_step < pc_end) load_piece(pc + pc_step, raw_next);
+        if (cb + cb_step < cb_end) load_piece(cb + cb_step, raw_next);
         if (first) {
             // seed: each lane's largest logit, scored by a fast lower bound
             float seed = -INFINITY;
@@ -1136,7 +1149,7 @@ __device__ __forceinline__ void race_rows_block(const VerifyParams& p, int b,
         } else {
             for (int x = x0 + lane; x < x1; x += 32) offer_exact(ET::load1(rt + x), x, word_at(x));
         }
-        if (pc + pc_step < pc_end) {
+        if (cb + cb_step < cb_end) {
             // every warp's best so far bounds the sequence's best from below: share them
             // through shared memory without a barrier (whatever value a slot holds, old or
             // new, is such a bound)
@@ -1151,7 +1164,7 @@ __device__ __forceinline__ void race_rows_block(const VerifyParams& p, int b,
     st = warp_race_merge(st);
     if (lane == 0) s_best[wib] = st;
     __syncthreads();
-    RacePart* parts = p.race_parts + static_cast<long long>(b) * p.rpieces;
+    RacePart* parts = p.race_parts + static_cast<long long>(b) * race_slots(p.rpieces);
     if (threadIdx.x == 0) {
         RaceState m = s_best[0];
         for (int k = 1; k < 8; ++k) m = race_merge(m, s_best[k]);
@@ -1195,9 +1208,9 @@ __device__ __forceinline__ void race_rows_block(const VerifyParams& p, int b,
 
 // The chain's race: row j = si.j (the residual of position j < gamma, or the bonus row).
 template <class ET>
-__device__ __forceinline__ void race_sequence_block(const VerifyParams& p, int b, int pc_begin,
-                                                   int pc_end, int pc_step, int slot, int nslots,
-                                                   const SeqInfo& si, float* s_thr,
+__device__ __forceinline__ void race_sequence_block(const VerifyParams& p, int b, int cb_begin,
+                                                   int cb_end, int cb_step, int ch_limit, int slot,
+                                                   int nslots, const SeqInfo& si, float* s_thr,
                                                    RaceState* s_best, int& s_last) {
     using S = typename ET::storage;
     const int j = si.j;
@@ -1206,8 +1219,8 @@ __device__ __forceinline__ void race_sequence_block(const VerifyParams& p, int b
     const S* rd = residual ? static_cast<const S*>(p.draft) + (static_cast<long long>(b) * p.gamma + j) * p.V
                            : nullptr;
     race_rows_block<ET>(p, b, rt, rd, residual, static_cast<uint32_t>(j),
-                        p.out_tokens + static_cast<long long>(b) * (p.gamma + 1) + j, pc_begin,
-                        pc_end, pc_step, slot, nslots, si, s_thr, s_best, s_last);
+                        p.out_tokens + static_cast<long long>(b) * (p.gamma + 1) + j, cb_begin,
+                        cb_end, cb_step, ch_limit, slot, nslots, si, s_thr, s_best, s_last);
 }
 
 // Poll a packed word until it is nonzero; after kWaitLimitNs give up, record SPEC_ETIMEOUT
@@ -1274,22 +1287,24 @@ __global__ void __launch_bounds__(256, SPECVERIFY_RACE_MINBLOCKS) scan_race_kern
     const int R = 2 * p.gamma + 1;
     float* sm_m = smem;
     float* sm_l = smem + R;
-    // this block's race pieces: [k T / n, (k + 1) T / n) of the T = B * rpieces pieces in
-    // sequence-major order (the same count, within one, for every block); a block whose range
-    // crosses a sequence boundary scans and races both sequences
-    const long long T = static_cast<long long>(p.B) * p.rpieces;
+    // this block's race chunks (kRaceWarpTokens tokens each): [k T / n, (k + 1) T / n) of the
+    // T = B * CH chunks in sequence-major order (the same count, within one, for every block;
+    // the launch gives each block at least one chunk per warp); a block whose range crosses a
+    // sequence boundary scans and races both sequences
+    const int CH = (p.V + kRaceWarpTokens - 1) / kRaceWarpTokens;
+    const long long T = static_cast<long long>(p.B) * CH;
     const long long nblk = gridDim.x;
     const long long q0 = static_cast<long long>(blockIdx.x) * T / nblk;
     const long long q1 = (static_cast<long long>(blockIdx.x) + 1) * T / nblk;
-    auto block_of = [&](long long x) { return ((x + 1) * nblk - 1) / T; };  // block racing piece x
+    auto block_of = [&](long long x) { return ((x + 1) * nblk - 1) / T; };  // block racing chunk x
     bool first = true;
     for (long long q = q0; q < q1;) {
-        const int b = static_cast<int>(q / p.rpieces);
-        const int pc0 = static_cast<int>(q % p.rpieces);
-        const int pc1 = static_cast<int>(min(static_cast<long long>(p.rpieces), pc0 + (q1 - q)));
-        q += pc1 - pc0;
-        const long long k_lo = block_of(static_cast<long long>(b) * p.rpieces);
-        const long long k_hi = block_of(static_cast<long long>(b + 1) * p.rpieces - 1);
+        const int b = static_cast<int>(q / CH);
+        const int ch0 = static_cast<int>(q % CH);
+        const int ch1 = static_cast<int>(min(static_cast<long long>(CH), ch0 + (q1 - q)));
+        q += ch1 - ch0;
+        const long long k_lo = block_of(static_cast<long long>(b) * CH);
+        const long long k_hi = block_of(static_cast<long long>(b + 1) * CH - 1);
         const int slot = static_cast<int>(blockIdx.x - k_lo), nslots = static_cast<int>(k_hi - k_lo + 1);
         const bool writer = (slot == 0);  // writes the sequence's outputs
         const float cp = scale_of(seq_T(p, b)), cq = scale_of(seq_Td(p, b));
@@ -1398,7 +1413,8 @@ __global__ void __launch_bounds__(256, SPECVERIFY_RACE_MINBLOCKS) scan_race_kern
             si.mq = residual ? sm_m[p.gamma + 1 + j] : 0.0f;
             si.l2sq = residual ? sm_l[p.gamma + 1 + j] : 0.0f;
             si.pad = 0;
-            race_sequence_block<ET>(p, b, pc0, pc1, 1, slot, nslots, si, s_thr, s_best, s_last);
+            race_sequence_block<ET>(p, b, ch0, ch1, kRaceBlockChunks, ch1, slot, nslots, si, s_thr,
+                                    s_best, s_last);
         }
         __syncthreads();  // before the next sequence reuses shared memory
     }
@@ -1444,7 +1460,7 @@ __global__ void __launch_bounds__(256, SPECVERIFY_STATS_MINBLOCKS) tree_stats_ke
     const int lane = threadIdx.x & 31;
     const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
     const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    for (long long k = tid; k < static_cast<long long>(p.B) * p.rpieces; k += nthreads)
+    for (long long k = tid; k < static_cast<long long>(p.B) * race_slots(p.rpieces); k += nthreads)
         reinterpret_cast<uint4*>(p.race_parts)[k] = make_uint4(0u, 0u, 0u, 0u);
     for (long long k = tid; k < p.B; k += nthreads) p.tickets[k] = 0;
     const long long nwarps = nthreads >> 5;
@@ -1661,8 +1677,9 @@ __global__ void __launch_bounds__(256, SPECVERIFY_RACE_MINBLOCKS) tree_race_kern
     const S* rd = tr.residual ? static_cast<const S*>(p.draft) + (static_cast<long long>(b) * M + tr.drow) * p.V
                               : nullptr;
     race_rows_block<ET>(p, b, rt, rd, tr.residual != 0, static_cast<uint32_t>(tr.node),
-                        p.out_tokens + static_cast<long long>(b) * (D + 1) + tr.k, g, p.rpieces,
-                        G, g, G, si, s_thr, s_best, s_last);
+                        p.out_tokens + static_cast<long long>(b) * (D + 1) + tr.k, g * kRaceBlockChunks,
+                        p.rpieces * kRaceBlockChunks, G * kRaceBlockChunks, INT_MAX, g, G, si, s_thr,
+                        s_best, s_last);
 }
 
 __device__ __forceinline__ int ld_acquire(const int* p) {

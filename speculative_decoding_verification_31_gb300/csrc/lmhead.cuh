@@ -526,8 +526,9 @@ __global__ void __launch_bounds__(256, SPECVERIFY_RACE_MINBLOCKS) lmhead_race_ke
     race_rows_block<F32Elem>(p, b, lt + static_cast<long long>(b) * p.V,
                              residual ? ld + static_cast<long long>(b) * p.V : nullptr, residual,
                              static_cast<uint32_t>(si.j),
-                             p.out_tokens + static_cast<long long>(b) * (p.gamma + 1) + si.j, g,
-                             p.rpieces, G, g, G, si, s_thr, s_best, s_last);
+                             p.out_tokens + static_cast<long long>(b) * (p.gamma + 1) + si.j,
+                             g * kRaceBlockChunks, p.rpieces * kRaceBlockChunks, G * kRaceBlockChunks,
+                             INT_MAX, g, G, si, s_thr, s_best, s_last);
 }
 
 }  // namespace specverify

@@ -74,7 +74,7 @@ Layout layout_of(int B, int gamma, int V, int dtype, long long stream_warps = 0)
     L.seq_off = off;
     off = align_up(off + static_cast<size_t>(B) * sizeof(SeqInfo), 256);
     L.race_off = off;
-    off = align_up(off + static_cast<size_t>(B) * L.rpieces * sizeof(RacePart), 256);
+    off = align_up(off + static_cast<size_t>(B) * race_slots(L.rpieces) * sizeof(RacePart), 256);
     L.ticket_off = off;
     off = align_up(off + static_cast<size_t>(B) * sizeof(int), 256);
     // flow control region: the two cursors on their own 128-byte lines, then per-sequence
@@ -365,8 +365,9 @@ int launch_sampling(VerifyParams& p, int sm_count, const spec_verify_opts* o, cu
                                         kThreads, 0, s>>>(p);
     }
     record(o, 1, s);
-    // scan-race grid: one resident wave of blocks sharing the B * rpieces race pieces evenly
-    // (one block per sequence when the sequences alone fill the wave)
+    // scan-race grid: one resident wave of blocks sharing the race's B * CH chunks evenly, at
+    // least one chunk per warp each (one block per sequence when the sequences alone fill the
+    // wave)
     long long grid;
     {
         int per_sm = 0;
@@ -375,8 +376,9 @@ int launch_sampling(VerifyParams& p, int sm_count, const spec_verify_opts* o, cu
             per_sm < 1)
             per_sm = 1;
         const long long wave = static_cast<long long>(sm_count) * per_sm;
-        const long long pieces = static_cast<long long>(p.B) * p.rpieces;
-        grid = p.B >= wave ? p.B : (pieces < wave ? pieces : wave);
+        const long long steps = static_cast<long long>(p.B) * ((p.V + kRaceWarpTokens - 1) / kRaceWarpTokens) /
+                                kRaceBlockChunks;
+        grid = p.B >= wave ? p.B : std::max<long long>(p.B, std::min(wave, steps));
     }
     // (no PDL when an event is recorded between the kernels, so that each one is timed alone)
     if (launch_pdl(scan_race_kernel<ET>, static_cast<int>(grid), 2 * R * sizeof(float), s,
@@ -998,7 +1000,7 @@ int spec_verify_lmhead(const void* h_target, const void* w_target, const void* h
         o_lt = take(static_cast<size_t>(B) * V * sizeof(float));
         o_ld = take(static_cast<size_t>(B) * V * sizeof(float));  // (unused when gamma = 0)
         o_seq = take(static_cast<size_t>(B) * sizeof(SeqInfo));
-        o_race = take(static_cast<size_t>(B) * rpieces * sizeof(RacePart));
+        o_race = take(static_cast<size_t>(B) * race_slots(rpieces) * sizeof(RacePart));
         o_tick = take(static_cast<size_t>(B) * sizeof(int));
         rc = ensure_workspace(*dev, off);
         if (rc) return rc;
@@ -1036,7 +1038,7 @@ int spec_verify_lmhead(const void* h_target, const void* w_target, const void* h
             q, reinterpret_cast<float*>(ws + o_Tt), reinterpret_cast<int32_t*>(ws + o_tokt),
             reinterpret_cast<float*>(ws + o_Td), reinterpret_cast<int32_t*>(ws + o_tokd));
     }
-    if (cudaMemsetAsync(ws + o_race, 0, static_cast<size_t>(B) * rpieces * sizeof(RacePart), s) != cudaSuccess ||
+    if (cudaMemsetAsync(ws + o_race, 0, static_cast<size_t>(B) * race_slots(rpieces) * sizeof(RacePart), s) != cudaSuccess ||
         cudaMemsetAsync(ws + o_tick, 0, static_cast<size_t>(B) * sizeof(int), s) != cudaSuccess)
         return SPEC_ECUDA;
     // row statistics of the target rows (T_b) and the draft rows (Td_b), with the draft
