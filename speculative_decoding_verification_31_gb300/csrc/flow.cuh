@@ -168,16 +168,7 @@ __device__ __forceinline__ RaceState race_warp_span(const VerifyParams& p,
                     float ft[ET::kVec];
                     ET::widen(raw[k0 + kk], ft);
                     const int xv = x0 + v * ET::kVec;
-                    uint32_t cand = 0;
-#pragma unroll
-                    for (int gg = 0; gg < BPV; ++gg) {
-                        const uint4 bk = blk[kk * BPV + gg];
-                        const uint32_t w4[4] = {bk.x, bk.y, bk.z, bk.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            cand |= (lg2_fast(static_cast<float>(w4[e])) <= fmaf(ft[4 * gg + e], si.cp, C))
-                                        ? (1u << (4 * gg + e)) : 0u;
-                    }
+                    uint32_t cand = vector_candidates<ET>(ft, blk + kk * BPV, si.cp, C);
                     while (cand) {  // rare: exact scores in increasing token order
                         const int e = __ffs(cand) - 1;
                         cand &= cand - 1;

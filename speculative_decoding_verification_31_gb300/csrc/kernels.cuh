@@ -822,6 +822,36 @@ __device__ __noinline__ float race_exact_score(float xt, float xd, SeqInfo si, b
 // The margin (in log2 units) is far above the fp32 error of the exact score.
 constexpr float kRaceBoundMargin2 = 1e-3f;
 
+// Candidate bits of one 16-byte vector of logits ft (ET::kVec tokens) with their Philox
+// words in blk[0 .. kVec/4): token e passes iff lg2(w_e) <= ft[e] cp + C.  The vector is
+// first tested as a whole -- its smallest word against its largest logit, a necessary
+// condition for any of its tokens up to kVectorTestMargin (which covers lg2.approx not being
+// exactly monotone) -- and the tokens one by one only when that passes, which is rare.
+constexpr float kVectorTestMargin = 1e-3f;
+
+template <class ET>
+__device__ __forceinline__ uint32_t vector_candidates(const float (&ft)[ET::kVec], const uint4* blk,
+                                                      float cp, float C) {
+    constexpr int BPV = ET::kVec / 4;
+    uint32_t wmin = 0xffffffffu;
+    float xmax = ft[0];
+#pragma unroll
+    for (int gg = 0; gg < BPV; ++gg)
+        wmin = min(wmin, min(min(blk[gg].x, blk[gg].y), min(blk[gg].z, blk[gg].w)));
+#pragma unroll
+    for (int e = 1; e < ET::kVec; ++e) xmax = fmaxf(xmax, ft[e]);
+    if (!(lg2_fast(static_cast<float>(wmin)) - kVectorTestMargin <= fmaf(xmax, cp, C))) return 0u;
+    uint32_t cand = 0;
+#pragma unroll
+    for (int gg = 0; gg < BPV; ++gg) {
+        const uint32_t w4[4] = {blk[gg].x, blk[gg].y, blk[gg].z, blk[gg].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            cand |= (lg2_fast(static_cast<float>(w4[e])) <= fmaf(ft[4 * gg + e], cp, C)) ? (1u << (4 * gg + e)) : 0u;
+    }
+    return cand;
+}
+
 // Race over tokens [x0, x1) of the raced row; every lane offers its tokens in increasing x.
 // The residual's draft row is read only at candidate tokens.
 template <class ET>
@@ -1125,16 +1155,7 @@ __device__ __forceinline__ void race_rows_block(const VerifyParams& p, int b,
                     float ft[ET::kVec];
                     ET::widen(raw[k0 + kk], ft);
                     const int xv = x0 + v * ET::kVec;
-                    uint32_t cand = 0;
-#pragma unroll
-                    for (int gg = 0; gg < BPV; ++gg) {
-                        const uint4 bk = blk[kk * BPV + gg];
-                        const uint32_t w4[4] = {bk.x, bk.y, bk.z, bk.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            cand |= (lg2_fast(static_cast<float>(w4[e])) <= fmaf(ft[4 * gg + e], si.cp, C))
-                                        ? (1u << (4 * gg + e)) : 0u;
-                    }
+                    uint32_t cand = vector_candidates<ET>(ft, blk + kk * BPV, si.cp, C);
                     while (cand) {  // rare: exact scores in increasing token order
                         const int e = __ffs(cand) - 1;
                         cand &= cand - 1;
