@@ -1308,25 +1308,43 @@ __global__ void __launch_bounds__(256, SPECVERIFY_RACE_MINBLOCKS) scan_race_kern
     const int R = 2 * p.gamma + 1;
     float* sm_m = smem;
     float* sm_l = smem + R;
-    // this block's race chunks (kRaceWarpTokens tokens each): [k T / n, (k + 1) T / n) of the
-    // T = B * CH chunks in sequence-major order (the same count, within one, for every block;
-    // the launch gives each block at least one chunk per warp); a block whose range crosses a
-    // sequence boundary scans and races both sequences
+    // This block's race chunks (kRaceWarpTokens tokens each), in one of two layouts:
+    //   G = p.rgroups > 0: G blocks per sequence, block g racing steps g, g + G, ... of its
+    //     sequence's row (a step: one chunk per warp); every block scans one sequence;
+    //   G = 0: the T = B * CH chunks in sequence-major order split evenly, block k taking
+    //     [k T / n, (k + 1) T / n) (at least one step each); a block whose range crosses a
+    //     sequence boundary scans and races both sequences.
     const int CH = (p.V + kRaceWarpTokens - 1) / kRaceWarpTokens;
+    const int G = p.rgroups;
     const long long T = static_cast<long long>(p.B) * CH;
     const long long nblk = gridDim.x;
-    const long long q0 = static_cast<long long>(blockIdx.x) * T / nblk;
-    const long long q1 = (static_cast<long long>(blockIdx.x) + 1) * T / nblk;
+    const long long q0 = G > 0 ? 0 : static_cast<long long>(blockIdx.x) * T / nblk;
+    const long long q1 = G > 0 ? 1 : (static_cast<long long>(blockIdx.x) + 1) * T / nblk;
     auto block_of = [&](long long x) { return ((x + 1) * nblk - 1) / T; };  // block racing chunk x
     bool first = true;
     for (long long q = q0; q < q1;) {
-        const int b = static_cast<int>(q / CH);
-        const int ch0 = static_cast<int>(q % CH);
-        const int ch1 = static_cast<int>(min(static_cast<long long>(CH), ch0 + (q1 - q)));
-        q += ch1 - ch0;
-        const long long k_lo = block_of(static_cast<long long>(b) * CH);
-        const long long k_hi = block_of(static_cast<long long>(b + 1) * CH - 1);
-        const int slot = static_cast<int>(blockIdx.x - k_lo), nslots = static_cast<int>(k_hi - k_lo + 1);
+        int b, cb_begin, cb_end, cb_step, ch_limit, slot, nslots;
+        if (G > 0) {
+            b = static_cast<int>(blockIdx.x / G);
+            slot = static_cast<int>(blockIdx.x % G);
+            nslots = G;
+            cb_begin = slot * kRaceBlockChunks;
+            cb_step = G * kRaceBlockChunks;
+            cb_end = ch_limit = CH;
+            q = q1;
+        } else {
+            b = static_cast<int>(q / CH);
+            const int ch0 = static_cast<int>(q % CH);
+            const int ch1 = static_cast<int>(min(static_cast<long long>(CH), ch0 + (q1 - q)));
+            q += ch1 - ch0;
+            const long long k_lo = block_of(static_cast<long long>(b) * CH);
+            const long long k_hi = block_of(static_cast<long long>(b + 1) * CH - 1);
+            slot = static_cast<int>(blockIdx.x - k_lo);
+            nslots = static_cast<int>(k_hi - k_lo + 1);
+            cb_begin = ch0;
+            cb_end = ch_limit = ch1;
+            cb_step = kRaceBlockChunks;
+        }
         const bool writer = (slot == 0);  // writes the sequence's outputs
         const float cp = scale_of(seq_T(p, b)), cq = scale_of(seq_Td(p, b));
         const uint32_t bg = p.seq_base + static_cast<uint32_t>(b);
@@ -1434,10 +1452,10 @@ __global__ void __launch_bounds__(256, SPECVERIFY_RACE_MINBLOCKS) scan_race_kern
             si.mq = residual ? sm_m[p.gamma + 1 + j] : 0.0f;
             si.l2sq = residual ? sm_l[p.gamma + 1 + j] : 0.0f;
             si.pad = 0;
-            race_sequence_block<ET>(p, b, ch0, ch1, kRaceBlockChunks, ch1, slot, nslots, si, s_thr,
+            race_sequence_block<ET>(p, b, cb_begin, cb_end, cb_step, ch_limit, slot, nslots, si, s_thr,
                                     s_best, s_last);
         }
-        __syncthreads();  // before the next sequence reuses shared memory
+        if (q < q1) __syncthreads();  // before the next sequence reuses shared memory
     }
 }
 

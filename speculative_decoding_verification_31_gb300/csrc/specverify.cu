@@ -365,9 +365,10 @@ int launch_sampling(VerifyParams& p, int sm_count, const spec_verify_opts* o, cu
                                         kThreads, 0, s>>>(p);
     }
     record(o, 1, s);
-    // scan-race grid: one resident wave of blocks sharing the race's B * CH chunks evenly, at
-    // least one chunk per warp each (one block per sequence when the sequences alone fill the
-    // wave)
+    // scan-race grid, one resident wave: G = wave / B blocks per sequence when that is at
+    // least 2 (every block scans one sequence); else the race's B * CH chunks shared evenly
+    // over the wave, at least one chunk per warp each (one block per sequence when the
+    // sequences alone fill the wave)
     long long grid;
     {
         int per_sm = 0;
@@ -378,7 +379,15 @@ int launch_sampling(VerifyParams& p, int sm_count, const spec_verify_opts* o, cu
         const long long wave = static_cast<long long>(sm_count) * per_sm;
         const long long steps = static_cast<long long>(p.B) * ((p.V + kRaceWarpTokens - 1) / kRaceWarpTokens) /
                                 kRaceBlockChunks;
-        grid = p.B >= wave ? p.B : std::max<long long>(p.B, std::min(wave, steps));
+        long long G = wave / p.B;
+        if (G > p.rpieces) G = p.rpieces;
+        if (G >= 2) {
+            p.rgroups = static_cast<int>(G);
+            grid = p.B * G;
+        } else {
+            p.rgroups = 0;
+            grid = p.B >= wave ? p.B : std::max<long long>(p.B, std::min(wave, steps));
+        }
     }
     // (no PDL when an event is recorded between the kernels, so that each one is timed alone)
     if (launch_pdl(scan_race_kernel<ET>, static_cast<int>(grid), 2 * R * sizeof(float), s,
