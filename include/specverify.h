@@ -225,8 +225,12 @@ int spec_verify_noalloc(const void *target_logits, const void *draft_logits,
  * is refused with SPEC_EINVAL.  Reading logits over the host link is the bottleneck, so
  * this entry point verifies with SPEC_FLAG_EARLY_EXIT (only the rows up to each sequence's
  * first rejection cross the link) unless opts->flags has SPEC_FLAG_FULL_READ or a
- * diagnostic output is requested.  Outputs land in host memory when the stream's work
- * completes: synchronise the stream before reading them.  Otherwise as spec_verify_ex.
+ * diagnostic output is requested.  With early exit the rows it streams are also copied
+ * into a library-owned device buffer the size of the logits (allocated on first use, grown
+ * as needed), from which each sequence's race then reads its raced rows instead of crossing
+ * the link a second time; if that allocation fails the race reads host memory.  Outputs land
+ * in host memory when the stream's work completes: synchronise the stream before reading
+ * them.  Otherwise as spec_verify_ex.
  */
 int spec_verify_host(const void *target_logits, const void *draft_logits,
                      const int32_t *draft_tokens, int B, int gamma, int V, float T, float T_d,

@@ -101,6 +101,8 @@ struct VerifyParams {
     int* race_tail;             // slots of race_task reserved so far
     unsigned long long* race_unit_cursor;  // race units claimed so far
     unsigned long long* early_race;  // [B][npieces] packed (score, index + 1) race winners
+    void* mirror_target;        // early exit over host memory: device copies of the rows streamed,
+    void* mirror_draft;         // laid out like the inputs (the race reads them there); or nullptr
     // outputs
     int32_t* out_tokens;        // [B, gamma+1]
     int32_t* out_n;             // [B]
@@ -197,14 +199,22 @@ __device__ __forceinline__ void stat_push1(SoftmaxStat& st, float x, float c) {
 // Partial statistics of row[x0, x1) by one warp: 16-byte vectors L per lane in flight, taken
 // U at a time (one running-max update per U vectors per lane).  The arithmetic depends on U
 // only: any L (a multiple of U) gives the same bits; an all-padding batch changes nothing.
-template <class ET, int U, int L = U>
+template <class ET, int U, int L = U, bool kMirror = false>
 __device__ __forceinline__ SoftmaxStat stats_piece(const typename ET::storage* row, int x0, int x1,
-                                                   float c, int lane) {
+                                                   float c, int lane,
+                                                   typename ET::storage* mirror = nullptr) {
     static_assert(L % U == 0, "loads in flight must be whole batches");
     SoftmaxStat st{-FLT_MAX, 0.0f};
     const RowSpan<ET> sp(row, x0, x1);
-    if (lane < sp.head) stat_push1(st, ET::load1(sp.base + lane), c);
+    // kMirror: every element read is also written to the same place of the row `mirror`
+    // (a device row with the same alignment as `row`)
+    typename ET::storage* mb = kMirror ? mirror + x0 : nullptr;
+    if (lane < sp.head) {
+        if (kMirror) mb[lane] = sp.base[lane];
+        stat_push1(st, ET::load1(sp.base + lane), c);
+    }
     const uint4* vp = sp.vec();
+    uint4* mv = kMirror ? reinterpret_cast<uint4*>(mb + sp.head) : nullptr;
     for (int v0 = 0; v0 < sp.nvec; v0 += 32 * L) {
         uint4 raw[L];
 #pragma unroll
@@ -213,6 +223,13 @@ __device__ __forceinline__ SoftmaxStat stats_piece(const typename ET::storage* r
             raw[k] = v < sp.nvec ? ld_stream16(vp + v)
                                  : make_uint4(ET::kNegInfWord, ET::kNegInfWord, ET::kNegInfWord,
                                               ET::kNegInfWord);
+        }
+        if (kMirror) {
+#pragma unroll
+            for (int k = 0; k < L; ++k) {
+                const int v = v0 + lane + 32 * k;
+                if (v < sp.nvec) mv[v] = raw[k];
+            }
         }
 #pragma unroll
         for (int h = 0; h < L / U; ++h) {
@@ -246,7 +263,10 @@ __device__ __forceinline__ SoftmaxStat stats_piece(const typename ET::storage* r
         }
     }
     const int t0 = sp.head + sp.nvec * ET::kVec;
-    if (lane < sp.tail) stat_push1(st, ET::load1(sp.base + t0 + lane), c);
+    if (lane < sp.tail) {
+        if (kMirror) mb[t0 + lane] = sp.base[t0 + lane];
+        stat_push1(st, ET::load1(sp.base + t0 + lane), c);
+    }
     return warp_merge_stat(st);
 }
 
@@ -1898,6 +1918,19 @@ __device__ __forceinline__ void early_finish(const VerifyParams& p, int b, int j
     }
 }
 
+// Count one event of an early-exit task (a row piece arrived, a row merged, a position
+// accepted).  Over host memory with a mirror, the count also hands the mirror's contents to
+// whoever acts on it: a fence before the increment (the writer's release) and one after (the
+// reader's acquire), so the rows a sequence's race reads from the mirror were written before
+// its race task was published.
+__device__ __forceinline__ int early_event(const VerifyParams& p, int* addr) {
+    if (!p.mirror_target) return atomicAdd(addr, 1);
+    __threadfence();
+    const int t = atomicAdd(addr, 1);
+    __threadfence();
+    return t;
+}
+
 #ifndef SPECVERIFY_EARLY_GROWTH
 #define SPECVERIFY_EARLY_GROWTH 0
 #endif
@@ -1959,7 +1992,7 @@ __device__ __forceinline__ void early_decide_from(const VerifyParams& p, int b, 
             const int fill = (p.early_fill + undecided - 1) / undecided;
             const int grow = ((i + 1) * kEarlyGrowth) >> 2;
             early_enqueue_upto(p, b, min(p.gamma, i + max(1, max(fill, 1 + grow))));
-            t = atomicAdd(p.pos_done + static_cast<long long>(b) * (p.gamma + 1) + i + 1, 1);
+            t = early_event(p, p.pos_done + static_cast<long long>(b) * (p.gamma + 1) + i + 1);
         }
         t = __shfl_sync(0xffffffffu, t, 0);
         ++i;
@@ -1983,7 +2016,7 @@ __device__ __forceinline__ void early_row_done(const VerifyParams& p, int b, int
     int t = 0;
     if (lane == 0) {
         store_stat(p.row_stat + static_cast<long long>(b) * R + r, st.m, log2f(st.s));
-        t = atomicAdd(p.pos_done + static_cast<long long>(b) * (p.gamma + 1) + i, 1);
+        t = early_event(p, p.pos_done + static_cast<long long>(b) * (p.gamma + 1) + i);
     }
     t = __shfl_sync(0xffffffffu, t, 0);
     if (t == early_events_of(p, i) - 1) early_decide_from<ET>(p, b, i, lane);
@@ -2008,9 +2041,12 @@ __device__ __forceinline__ void early_race_unit(const VerifyParams& p, int b, in
     }
     const int j = si.j;
     const bool residual = j < p.gamma;
-    const S* rt = static_cast<const S*>(p.target) + (static_cast<long long>(b) * (p.gamma + 1) + j) * p.V;
-    const S* rd = residual ? static_cast<const S*>(p.draft) + (static_cast<long long>(b) * p.gamma + j) * p.V
-                           : nullptr;
+    // the raced rows were streamed (and, over host memory, mirrored on the device) before
+    // the sequence was decided
+    const S* tb = static_cast<const S*>(p.mirror_target ? p.mirror_target : p.target);
+    const S* db = static_cast<const S*>(p.mirror_target ? p.mirror_draft : p.draft);
+    const S* rt = tb + (static_cast<long long>(b) * (p.gamma + 1) + j) * p.V;
+    const S* rd = residual ? db + (static_cast<long long>(b) * p.gamma + j) * p.V : nullptr;
     const uint32_t bg = p.seq_base + static_cast<uint32_t>(b);
     const int x0 = piece * p.piece_len;
     const int x1 = min(p.V, x0 + p.piece_len);
@@ -2102,11 +2138,19 @@ __global__ void __launch_bounds__(256, SPECVERIFY_EARLY_MINBLOCKS) verify_early_
                 cs = scale_of(seq_Td(p, b));
             }
             const int x0 = piece * p.piece_len;
-            const SoftmaxStat st = stats_piece<ET, U>(row, x0, min(p.V, x0 + p.piece_len), cs, lane);
+            SoftmaxStat st;
+            if (p.mirror_target) {  // keep a device copy of the row for the race
+                S* mrow = r <= p.gamma
+                    ? static_cast<S*>(p.mirror_target) + (static_cast<long long>(b) * (p.gamma + 1) + r) * p.V
+                    : static_cast<S*>(p.mirror_draft) + (static_cast<long long>(b) * p.gamma + (r - p.gamma - 1)) * p.V;
+                st = stats_piece<ET, U, U, true>(row, x0, min(p.V, x0 + p.piece_len), cs, lane, mrow);
+            } else {
+                st = stats_piece<ET, U>(row, x0, min(p.V, x0 + p.piece_len), cs, lane);
+            }
             int t = 0;
             if (lane == 0) {
                 store_stat(p.stat_parts + static_cast<long long>(d) * np + piece, st.m, st.s);
-                t = atomicAdd(p.row_arrivals + d, 1);
+                t = early_event(p, p.row_arrivals + d);
             }
             t = __shfl_sync(0xffffffffu, t, 0);
             if (t == np - 1) early_row_done<ET>(p, b, r, lane);

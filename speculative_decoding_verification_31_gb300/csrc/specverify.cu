@@ -147,6 +147,8 @@ struct DeviceState {
     long long stream_warps[2] = {0, 0};  // warps of a full streaming grid, per dtype
     void* ws = nullptr;
     size_t ws_bytes = 0;
+    void* mirror = nullptr;     // spec_verify_host: device copies of the rows it streams
+    size_t mirror_bytes = 0;
     int32_t* status = nullptr;  // library status word (its own allocation)
 };
 
@@ -191,6 +193,25 @@ int ensure_workspace(DeviceState& d, size_t bytes) {
     if (cudaMemset(d.ws, 0, bytes) != cudaSuccess) return SPEC_ECUDA;
     d.ws_bytes = bytes;
     return SPEC_OK;
+}
+
+// Grow the host path's row mirror to `bytes`; false (and no mirror) if that fails.  Caller
+// holds g_mu.
+bool ensure_mirror(DeviceState& d, size_t bytes) {
+    if (d.mirror_bytes >= bytes) return true;
+    if (d.mirror) {
+        cudaDeviceSynchronize();
+        cudaFree(d.mirror);
+        d.mirror = nullptr;
+        d.mirror_bytes = 0;
+    }
+    if (cudaMalloc(&d.mirror, bytes) != cudaSuccess) {
+        (void)cudaGetLastError();
+        d.mirror = nullptr;
+        return false;
+    }
+    d.mirror_bytes = bytes;
+    return true;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -537,9 +558,15 @@ size_t spec_verify_workspace_bytes(int B, int gamma, int V, int dtype) {
     return layout_of(B, gamma, V, dtype).total;
 }
 
-int spec_verify_ex(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
+}  // extern "C"
+
+namespace {
+
+// spec_verify_ex, and spec_verify_host's call of it (host_rows: the logits are in host memory;
+// the early-exit kernel then mirrors the rows it streams on the device for the race).
+int verify_ex_impl(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
                    int B, int gamma, int V, float T, float T_d, uint64_t seed, int32_t* out_tokens,
-                   int32_t* out_n_accepted, const spec_verify_opts* opts, void* stream) {
+                   int32_t* out_n_accepted, const spec_verify_opts* opts, void* stream, bool host_rows) {
     const int dtype = opts ? opts->dtype : SPEC_BF16;
     int rc = check_common(target_logits, out_tokens, out_n_accepted, B, gamma, V, dtype);
     if (rc || B == 0) return rc;
@@ -585,9 +612,20 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, const in
     const bool diagnostics = p.out_logp || p.out_logq || p.out_logZp || p.out_logZq || p.out_u ||
                              p.out_race || wants_position_stats(p);
     const Layout L = layout_of(B, gamma, V, dtype, d->stream_warps[dtype == SPEC_F32 ? 0 : 1]);
-    if (d->coop && opts && (opts->flags & SPEC_FLAG_EARLY_EXIT) && !diagnostics)
+    if (d->coop && opts && (opts->flags & SPEC_FLAG_EARLY_EXIT) && !diagnostics) {
+        if (host_rows) {  // a device copy of every row the kernel streams, for the race
+            const size_t es = static_cast<size_t>(elem_bytes(dtype));
+            const size_t tb = align_up(static_cast<size_t>(B) * (gamma + 1) * V * es, 256);
+            const size_t db = static_cast<size_t>(B) * gamma * V * es;
+            std::lock_guard<std::mutex> lock(g_mu);
+            if (ensure_mirror(*d, tb + db)) {
+                p.mirror_target = d->mirror;
+                p.mirror_draft = static_cast<char*>(d->mirror) + tb;
+            }
+        }
         return dtype == SPEC_F32 ? launch_early<F32Elem>(p, d->sm_count, opts, s, L, ws)
                                  : launch_early<Bf16Elem>(p, d->sm_count, opts, s, L, ws);
+    }
     const bool fused = d->coop && opts && (opts->flags & SPEC_FLAG_FUSED) && !wants_position_stats(p);
     if (fused) {
         return dtype == SPEC_F32 ? launch_flow<F32Elem>(p, d->sm_count, opts, s, L, ws)
@@ -595,6 +633,17 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, const in
     }
     return dtype == SPEC_F32 ? launch_sampling<F32Elem>(p, d->sm_count, opts, s)
                              : launch_sampling<Bf16Elem>(p, d->sm_count, opts, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+int spec_verify_ex(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
+                   int B, int gamma, int V, float T, float T_d, uint64_t seed, int32_t* out_tokens,
+                   int32_t* out_n_accepted, const spec_verify_opts* opts, void* stream) {
+    return verify_ex_impl(target_logits, draft_logits, draft_tokens, B, gamma, V, T, T_d, seed,
+                          out_tokens, out_n_accepted, opts, stream, false);
 }
 
 int spec_verify(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
@@ -696,7 +745,7 @@ int spec_verify_host(const void* target_logits, const void* draft_logits, const 
     if (device_alias(o.T_per_seq, &o.T_per_seq) || device_alias(o.Td_per_seq, &o.Td_per_seq))
         return SPEC_EINVAL;
     if (!(o.flags & SPEC_FLAG_FULL_READ)) o.flags |= SPEC_FLAG_EARLY_EXIT;
-    return spec_verify_ex(t, d, tok, B, gamma, V, T, T_d, seed, ot, on, &o, stream);
+    return verify_ex_impl(t, d, tok, B, gamma, V, T, T_d, seed, ot, on, &o, stream, true);
 }
 
 int spec_verify_tree(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
