@@ -45,6 +45,15 @@ struct Bf16Elem {
             f[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
         }
     }
+    // The largest of the vector's eight values (exact: a maximum of bf16 values is one of
+    // them), on packed pairs before widening.
+    __device__ __forceinline__ static float vmax(const uint4& v) {
+        uint32_t a, b;
+        asm("max.bf16x2 %0, %1, %2;" : "=r"(a) : "r"(v.x), "r"(v.y));
+        asm("max.bf16x2 %0, %1, %2;" : "=r"(b) : "r"(v.z), "r"(v.w));
+        asm("max.bf16x2 %0, %1, %2;" : "=r"(a) : "r"(a), "r"(b));
+        return fmaxf(__uint_as_float(a << 16), __uint_as_float(a & 0xFFFF0000u));
+    }
 };
 
 struct F32Elem {
@@ -57,6 +66,10 @@ struct F32Elem {
         f[1] = __uint_as_float(v.y);
         f[2] = __uint_as_float(v.z);
         f[3] = __uint_as_float(v.w);
+    }
+    __device__ __forceinline__ static float vmax(const uint4& v) {
+        return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
+                     fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
     }
 };
 

@@ -449,14 +449,8 @@ __device__ __forceinline__ PairStat pair_piece(const typename ET::storage* rp,
         float bp = -INFINITY, bq = -INFINITY;
 #pragma unroll
         for (int k = 0; k < U; ++k) {
-            float f[ET::kVec], g[ET::kVec];
-            ET::widen(rawp[k], f);
-            ET::widen(rawq[k], g);
-#pragma unroll
-            for (int e = 0; e < ET::kVec; ++e) {
-                bp = fmaxf(bp, f[e]);
-                bq = fmaxf(bq, g[e]);
-            }
+            bp = fmaxf(bp, ET::vmax(rawp[k]));
+            bq = fmaxf(bq, ET::vmax(rawq[k]));
         }
         raise(fmaxf(st.mp, fmaxf(bp * cp, -FLT_MAX)), fmaxf(st.mq, fmaxf(bq * cq, -FLT_MAX)));
 #pragma unroll

@@ -362,7 +362,7 @@ cudaError_t launch_pdl(K kernel, int grid, size_t smem, cudaStream_t s, bool pdl
 // Two-kernel sampling verify: the streaming pass, then the scan-race kernel as its
 // programmatic dependent (its blocks start while the streaming pass drains).
 #ifndef SPECVERIFY_PAIR_UNROLL
-#define SPECVERIFY_PAIR_UNROLL 3
+#define SPECVERIFY_PAIR_UNROLL 4
 #endif
 constexpr int kPairUnroll = SPECVERIFY_PAIR_UNROLL;  // 16-byte loads per row in flight per lane
 
@@ -377,6 +377,15 @@ int launch_sampling(VerifyParams& p, int sm_count, const spec_verify_opts* o, cu
     const bool extra = wants_position_stats(p);
     record(o, 0, s);
     if (extra) {  // the same read of every logit, paired by position, with the extra terms
+        // pieces chosen for this pass's items (position pairs, not rows) and grid
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pair_stats_kernel<ET, kPairUnroll>, kThreads,
+                                                          0) != cudaSuccess || per_sm < 1)
+            per_sm = 1;
+        p.piece_len = pick_piece_len(static_cast<long long>(p.B) * (p.gamma + 1), p.V,
+                                     static_cast<int>(sizeof(typename ET::storage)),
+                                     static_cast<long long>(sm_count) * per_sm * (kThreads / 32));
+        p.npieces = (p.V + p.piece_len - 1) / p.piece_len;
         const long long items = static_cast<long long>(p.B) * (p.gamma + 1) * p.npieces;
         pair_stats_kernel<ET, kPairUnroll><<<grid_for(pair_stats_kernel<ET, kPairUnroll>, sm_count, items),
                                              kThreads, 0, s>>>(p);
