@@ -39,17 +39,21 @@ UNIT = "rows/s"
 
 # DRAM traffic of one row-statistics launch on the throughput workload, from the ncu capture
 # summarised in profiles/ (dram__bytes_read.sum + dram__bytes_write.sum), with the hash of
-# the kernel sources it was taken on; reported as null when the sources have changed since.
-NCU_TRAFFIC = {"bytes": 1953473432, "sources_sha1": "663b6dd375d05984d4f859c74db6ebf4a8927733"}
-KERNEL_SOURCES = ["kernels.cuh", "device_common.cuh", "philox.cuh", "specverify.cu"]  # (row_stats lives here)
+# the code it was taken on (the element types and the row-statistics kernel with the piece
+# choice and the helpers it calls); reported as null once that code has changed.
+NCU_TRAFFIC = {"bytes": 1953473432, "sources_sha1": "e6256d96a1579cff4cf24af00334f2c57fdf566a"}
+ROW_STATS_SPAN = ("inline int pick_piece_len(", "// Per-position entropies and KL divergence")
 
 
 def kernel_sources_sha1() -> str:
     h = hashlib.sha1()
-    for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "speculative_decoding_verification_31_gb300", "csrc", f),
-                  "rb") as fh:
-            h.update(fh.read())
+    csrc = os.path.join(ROOT, "speculative_decoding_verification_31_gb300", "csrc")
+    with open(os.path.join(csrc, "device_common.cuh"), "rb") as fh:
+        h.update(fh.read())
+    with open(os.path.join(csrc, "kernels.cuh"), "r") as fh:
+        text = fh.read()
+    a = text.index(ROW_STATS_SPAN[0])
+    h.update(text[a:text.index(ROW_STATS_SPAN[1], a)].encode())
     return h.hexdigest()
 
 

@@ -66,7 +66,7 @@ struct VerifyParams {
     const int32_t* tokens;      // [B, gamma]
     int B, gamma, V;
     int piece_len, npieces;     // elements per row piece, pieces per row (streaming pass)
-    int rpiece_len, rpieces;    // the same for the race pass (finer: the race is compute-bound)
+    int rpieces;                // race pieces of kRaceBlockTokens per row (partial-slot sizing)
     int rgroups;                // scan-race blocks per sequence (each races rpieces / rgroups pieces)
     float T, Td;                // scalar temperatures
     const float* T_seq;         // [B] or nullptr

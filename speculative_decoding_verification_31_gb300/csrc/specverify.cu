@@ -35,7 +35,7 @@ int elem_bytes(int dtype) { return dtype == SPEC_F32 ? 4 : 2; }
 
 struct Layout {
     int piece_len, npieces;
-    int rpiece_len, rpieces;
+    int rpieces;
     size_t stat_off, ext_off, seq_off, race_off, ticket_off;
     size_t flow_off, flow_bytes;        // flow path (verify_flow_kernel), zeroed before each call
     size_t f_cursor_off, f_items_off, f_ready_off, f_tickets_off, f_race_off, f_second_off,
@@ -62,7 +62,6 @@ Layout layout_of(int B, int gamma, int V, int dtype, long long stream_warps = 0)
     // the workspace always holds the most pieces any choice can give
     const int max_np = (V + kMinPieceBytes / elem_bytes(dtype) - 1) / (kMinPieceBytes / elem_bytes(dtype));
     // race pieces: one block of kRaceBlockTokens tokens each
-    L.rpiece_len = kRaceBlockTokens;
     L.rpieces = (V + kRaceBlockTokens - 1) / kRaceBlockTokens;
     const size_t R = 2 * static_cast<size_t>(gamma) + 1;
     size_t off = 0;
@@ -247,7 +246,6 @@ void record(const spec_verify_opts* o, int k, cudaStream_t s) {
 void bind_workspace(VerifyParams& p, const Layout& L, char* ws) {
     p.piece_len = L.piece_len;
     p.npieces = L.npieces;
-    p.rpiece_len = L.rpiece_len;
     p.rpieces = L.rpieces;
     p.stat_parts = reinterpret_cast<float2*>(ws + L.stat_off);
     p.ext_parts = reinterpret_cast<float2*>(ws + L.ext_off);
@@ -1148,7 +1146,6 @@ int spec_verify_lmhead(const void* h_target, const void* w_target, const void* h
     p.rk = philox_round_keys(q.key);
     p.seq_base = q.seq_base;
     p.seq = q.seq;
-    p.rpiece_len = kRaceBlockTokens;
     p.rpieces = rpieces;
     p.race_parts = reinterpret_cast<RacePart*>(ws + o_race);
     p.tickets = reinterpret_cast<int*>(ws + o_tick);
