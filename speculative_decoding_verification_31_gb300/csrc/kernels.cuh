@@ -136,26 +136,32 @@ __host__ __device__ __forceinline__ int race_slots(int rpieces) { return rpieces
 #endif
 constexpr int kPieceBytes = SPECVERIFY_PIECE_BYTES;  // default (no grid given)
 constexpr int kMinPieceBytes = 8192;
-constexpr int kMaxPieceBytes = 32768;
+constexpr int kMaxPieceBytes = 20480;  // larger pieces measured slower on the throughput workload
 #ifndef SPECVERIFY_EARLY_PIECE_BYTES
 #define SPECVERIFY_EARLY_PIECE_BYTES 8192
 #endif
 constexpr int kEarlyPieceBytes = SPECVERIFY_EARLY_PIECE_BYTES;
 static_assert(kEarlyPieceBytes >= kMinPieceBytes, "the workspace holds rows of kMinPieceBytes pieces");
 
-// Elements per piece for `rows` rows of V elements of es bytes streamed by `warps` warps:
-// the largest piece whose items fill the grid's rounds clearly better than any larger one
-// (the last, partly idle round costs a whole item's time).  warps = 0: the default size.
+// Elements per piece for `rows` rows of V elements of es bytes streamed by `warps` warps.
+// Items are dealt round-robin, so the pass takes about ceil(items / warps) item times, an
+// item costing its piece plus a fixed overhead (the warp's reduction and partial store and
+// the next item's first loads, about kItemOverheadBytes of streaming); the piece with the
+// most useful bytes per unit of that time wins, the larger one on near-equal scores.
+// warps = 0: the default size.
+constexpr float kItemOverheadBytes = 2048.0f;
+
 inline int pick_piece_len(long long rows, int V, int es, long long warps) {
     int best_len = kPieceBytes / es;
     if (warps > 0) {
         const float fw = static_cast<float>(warps);
+        const float work = static_cast<float>(rows) * static_cast<float>(V) * static_cast<float>(es);
         float best_eff = -1.0f;
         for (int bytes = kMaxPieceBytes; bytes >= kMinPieceBytes; bytes -= 1024) {
             const int l = bytes / es;
             const float items = static_cast<float>(rows) * static_cast<float>((V + l - 1) / l);
-            const float eff = items / (ceilf(items / fw) * fw);
-            if (eff > best_eff + 0.02f) {  // prefer bigger pieces unless clearly better filled
+            const float eff = work / (ceilf(items / fw) * fw * (static_cast<float>(bytes) + kItemOverheadBytes));
+            if (eff > best_eff + 0.005f) {
                 best_eff = eff;
                 best_len = l;
             }
