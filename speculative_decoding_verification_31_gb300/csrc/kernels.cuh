@@ -144,11 +144,11 @@ constexpr int kEarlyPieceBytes = SPECVERIFY_EARLY_PIECE_BYTES;
 static_assert(kEarlyPieceBytes >= kMinPieceBytes, "the workspace holds rows of kMinPieceBytes pieces");
 
 // Elements per piece for `rows` rows of V elements of es bytes streamed by `warps` warps.
-// Items are dealt round-robin, so the pass takes about ceil(items / warps) item times, an
-// item costing its piece plus a fixed overhead (the warp's reduction and partial store and
-// the next item's first loads, about kItemOverheadBytes of streaming); the piece with the
-// most useful bytes per unit of that time wins, the larger one on near-equal scores.
-// warps = 0: the default size.
+// The pass takes about ceil(items / warps) item times (every warp takes about the same
+// number of items), an item costing its piece plus a fixed overhead (the warp's reduction
+// and partial store and the next item's first loads, about kItemOverheadBytes of
+// streaming); the piece with the most useful bytes per unit of that time wins, the larger
+// one on near-equal scores.  warps = 0: the default size.
 constexpr float kItemOverheadBytes = 2048.0f;
 
 inline int pick_piece_len(long long rows, int V, int es, long long warps) {
@@ -300,27 +300,63 @@ __device__ __forceinline__ void row_stats_item(const VerifyParams& p, int b, int
         store_stat(p.stat_parts + (static_cast<long long>(b) * R + r) * p.npieces + piece, st.m, st.s);
 }
 
+// The streaming passes (row_stats, pair_stats, row_argmax, tree_stats) run one block of
+// kStreamThreads per SM.  Their items (one row piece per warp) are split into contiguous
+// equal ranges, one per block, and the warps of a block claim the block's items one at a time
+// from a shared counter, so the warps of an SM finish together.  (Dealt round-robin to the
+// warps of three 256-thread blocks per SM, the same items ended over a 33 us window on the
+// throughput workload: the blocks of one SM were not served alike, the last-placed block
+// ending 16 us after the first.)
+#ifndef SPECVERIFY_STREAM_THREADS
+#define SPECVERIFY_STREAM_THREADS 768
+#endif
+#ifndef SPECVERIFY_STATS_MINBLOCKS
+#define SPECVERIFY_STATS_MINBLOCKS 1
+#endif
+constexpr int kStreamThreads = SPECVERIFY_STREAM_THREADS;
+
+// Items [0, total) of a streaming pass, one item per warp at a time: with kClaim, this block's
+// range, claimed by its warps from a shared counter (every thread of the block must call
+// it); without, the item whose index is the global warp index (the launch shape of small
+// calls, a warp for every item).
+template <bool kClaim, class F>
+__device__ __forceinline__ void for_block_items(long long total, F&& f) {
+    if (!kClaim) {
+        const long long item = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+        if (item < total) f(item);
+        return;
+    }
+    __shared__ int s_next;
+    if (threadIdx.x == 0) s_next = 0;
+    __syncthreads();
+    const long long i0 = static_cast<long long>(blockIdx.x) * total / gridDim.x;
+    const long long i1 = (static_cast<long long>(blockIdx.x) + 1) * total / gridDim.x;
+    const int lane = threadIdx.x & 31;
+    for (;;) {
+        int k = 0;
+        if (lane == 0) k = atomicAdd(&s_next, 1);
+        const long long item = i0 + __shfl_sync(0xffffffffu, k, 0);
+        if (item >= i1) break;
+        f(item);
+    }
+}
+
 // Also empties the race partials and arrival counters the scan-race kernel uses, and lets
 // that kernel (launched as a programmatic dependent) start as soon as blocks retire.
-#ifndef SPECVERIFY_STATS_MINBLOCKS
-#define SPECVERIFY_STATS_MINBLOCKS 3
-#endif
-template <class ET, int U>
-__global__ void __launch_bounds__(256, SPECVERIFY_STATS_MINBLOCKS) row_stats_kernel(VerifyParams p) {
+template <class ET, int U, bool kClaim>
+__global__ void __launch_bounds__(kStreamThreads, SPECVERIFY_STATS_MINBLOCKS) row_stats_kernel(VerifyParams p) {
     const int lane = threadIdx.x & 31;
     const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
     const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     for (long long k = tid; k < static_cast<long long>(p.B) * race_slots(p.rpieces); k += nthreads)
         reinterpret_cast<uint4*>(p.race_parts)[k] = make_uint4(0u, 0u, 0u, 0u);
     for (long long k = tid; k < p.B; k += nthreads) p.tickets[k] = 0;
-    const long long nwarps = nthreads >> 5;
     const int R = 2 * p.gamma + 1;
-    const long long total = static_cast<long long>(p.B) * R * p.npieces;
-    for (long long item = tid >> 5; item < total; item += nwarps) {
+    for_block_items<kClaim>(static_cast<long long>(p.B) * R * p.npieces, [&](long long item) {
         const int piece = static_cast<int>(item % p.npieces);
         const long long br = item / p.npieces;
         row_stats_item<ET, U>(p, static_cast<int>(br / R), static_cast<int>(br % R), piece, lane);
-    }
+    });
     asm volatile("griddepcontrol.launch_dependents;");
 }
 
@@ -475,10 +511,10 @@ __device__ __forceinline__ PairStat pair_piece(const typename ET::storage* rp,
 
 // pair_stats: row_stats with the extra terms (see above).  Item (b, i, piece), i <= gamma.
 #ifndef SPECVERIFY_PAIR_MINBLOCKS
-#define SPECVERIFY_PAIR_MINBLOCKS 3
+#define SPECVERIFY_PAIR_MINBLOCKS 1
 #endif
-template <class ET, int U>
-__global__ void __launch_bounds__(256, SPECVERIFY_PAIR_MINBLOCKS) pair_stats_kernel(VerifyParams p) {
+template <class ET, int U, bool kClaim>
+__global__ void __launch_bounds__(kStreamThreads, SPECVERIFY_PAIR_MINBLOCKS) pair_stats_kernel(VerifyParams p) {
     using S = typename ET::storage;
     const int lane = threadIdx.x & 31;
     const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
@@ -486,10 +522,8 @@ __global__ void __launch_bounds__(256, SPECVERIFY_PAIR_MINBLOCKS) pair_stats_ker
     for (long long k = tid; k < static_cast<long long>(p.B) * race_slots(p.rpieces); k += nthreads)
         reinterpret_cast<uint4*>(p.race_parts)[k] = make_uint4(0u, 0u, 0u, 0u);
     for (long long k = tid; k < p.B; k += nthreads) p.tickets[k] = 0;
-    const long long nwarps = nthreads >> 5;
     const int R = 2 * p.gamma + 1;
-    const long long total = static_cast<long long>(p.B) * (p.gamma + 1) * p.npieces;
-    for (long long item = tid >> 5; item < total; item += nwarps) {
+    for_block_items<kClaim>(static_cast<long long>(p.B) * (p.gamma + 1) * p.npieces, [&](long long item) {
         const int piece = static_cast<int>(item % p.npieces);
         const long long bi = item / p.npieces;
         const int b = static_cast<int>(bi / (p.gamma + 1)), i = static_cast<int>(bi % (p.gamma + 1));
@@ -510,7 +544,7 @@ __global__ void __launch_bounds__(256, SPECVERIFY_PAIR_MINBLOCKS) pair_stats_ker
                 p.ext_parts[kq] = make_float2(st.aq, 0.0f);
             }
         }
-    }
+    });
     asm volatile("griddepcontrol.launch_dependents;");
 }
 
@@ -675,15 +709,12 @@ __device__ __forceinline__ ArgMax argmax_piece(const typename ET::storage* row, 
     return warp_argmax(best);
 }
 
-template <class ET, int U>
-__global__ void __launch_bounds__(256) row_argmax_kernel(VerifyParams p) {
+template <class ET, int U, bool kClaim>
+__global__ void __launch_bounds__(kStreamThreads, 1) row_argmax_kernel(VerifyParams p) {
     using S = typename ET::storage;
     const int lane = threadIdx.x & 31;
-    const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
     const int R = p.gamma + 1;
-    const long long total = static_cast<long long>(p.B) * R * p.npieces;
-    for (long long item = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-         item < total; item += nwarps) {
+    for_block_items<kClaim>(static_cast<long long>(p.B) * R * p.npieces, [&](long long item) {
         const int piece = static_cast<int>(item % p.npieces);
         const long long row_index = item / p.npieces;  // = b * (gamma+1) + i
         const S* row = static_cast<const S*>(p.target) + row_index * p.V;
@@ -691,7 +722,7 @@ __global__ void __launch_bounds__(256) row_argmax_kernel(VerifyParams p) {
         const int x1 = min(p.V, x0 + p.piece_len);
         const ArgMax a = argmax_piece<ET, U>(row, x0, x1, lane);
         if (lane == 0) p.stat_parts[item] = make_float2(a.v, __int_as_float(a.i));
-    }
+    });
 }
 
 // ----------------------------------------------------------------------------------------
@@ -1513,8 +1544,8 @@ struct TreeRace {
     int node, k, residual, drow;  // node raced (-1: none), output slot, residual?, its draft row
 };
 
-template <class ET, int U>
-__global__ void __launch_bounds__(256, SPECVERIFY_STATS_MINBLOCKS) tree_stats_kernel(VerifyParams p, int N, int M) {
+template <class ET, int U, bool kClaim>
+__global__ void __launch_bounds__(kStreamThreads, SPECVERIFY_STATS_MINBLOCKS) tree_stats_kernel(VerifyParams p, int N, int M) {
     using S = typename ET::storage;
     const int lane = threadIdx.x & 31;
     const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
@@ -1522,10 +1553,8 @@ __global__ void __launch_bounds__(256, SPECVERIFY_STATS_MINBLOCKS) tree_stats_ke
     for (long long k = tid; k < static_cast<long long>(p.B) * race_slots(p.rpieces); k += nthreads)
         reinterpret_cast<uint4*>(p.race_parts)[k] = make_uint4(0u, 0u, 0u, 0u);
     for (long long k = tid; k < p.B; k += nthreads) p.tickets[k] = 0;
-    const long long nwarps = nthreads >> 5;
     const int R = N + M;
-    const long long total = static_cast<long long>(p.B) * R * p.npieces;
-    for (long long item = tid >> 5; item < total; item += nwarps) {
+    for_block_items<kClaim>(static_cast<long long>(p.B) * R * p.npieces, [&](long long item) {
         const int piece = static_cast<int>(item % p.npieces);
         const long long br = item / p.npieces;
         const int b = static_cast<int>(br / R), r = static_cast<int>(br % R);
@@ -1541,7 +1570,7 @@ __global__ void __launch_bounds__(256, SPECVERIFY_STATS_MINBLOCKS) tree_stats_ke
         const int x0 = piece * p.piece_len;
         const SoftmaxStat st = stats_piece<ET, U>(row, x0, min(p.V, x0 + p.piece_len), c, lane);
         if (lane == 0) store_stat(p.stat_parts + br * p.npieces + piece, st.m, st.s);
-    }
+    });
     asm volatile("griddepcontrol.launch_dependents;");
 }
 

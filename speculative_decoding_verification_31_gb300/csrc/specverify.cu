@@ -217,26 +217,33 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 bool good_temperature(float t) { return std::isfinite(t) && t > 0.0f; }
 
-template <class K>
-int grid_for(K kernel, int sm_count, long long warp_items) {
+// Launch of a streaming kernel: one block of kStreamThreads per SM (the claiming variant kc,
+// whose warps share the block's items) when the items outnumber the warps of that grid;
+// otherwise blocks of kThreads of the plain variant kp, one item per warp, so that a small
+// call starts few threads and spreads its items over as many SMs as it can.
+template <class KC, class KP, class... A>
+void launch_stream(KC kc, KP kp, int sm_count, long long items, cudaStream_t s, A... args) {
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kc, kStreamThreads, 0) != cudaSuccess ||
         per_sm < 1)
         per_sm = 1;
-    const long long want = (warp_items + (kThreads / 32) - 1) / (kThreads / 32);
-    long long g = static_cast<long long>(sm_count) * per_sm;
-    if (want < g) g = want;
-    return static_cast<int>(g < 1 ? 1 : g);
+    const long long full = static_cast<long long>(sm_count) * per_sm;
+    if (items >= full * (kStreamThreads / 32)) {
+        kc<<<static_cast<unsigned>(full), kStreamThreads, 0, s>>>(args...);
+    } else {
+        const long long g = (items + (kThreads / 32) - 1) / (kThreads / 32);
+        kp<<<static_cast<unsigned>(g < 1 ? 1 : g), kThreads, 0, s>>>(args...);
+    }
 }
 
-// Warps of the streaming kernel's full grid (the grid_for cap).
+// Warps of the streaming kernel's full grid.
 long long stream_warps_of(int sm_count, int dtype) {
     int per_sm = 0;
     cudaError_t e = dtype == SPEC_F32
-        ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, row_stats_kernel<F32Elem, kUnroll>, kThreads, 0)
-        : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, row_stats_kernel<Bf16Elem, kUnroll>, kThreads, 0);
+        ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, row_stats_kernel<F32Elem, kUnroll, true>, kStreamThreads, 0)
+        : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, row_stats_kernel<Bf16Elem, kUnroll, true>, kStreamThreads, 0);
     if (e != cudaSuccess || per_sm < 1) per_sm = 1;
-    return static_cast<long long>(sm_count) * per_sm * (kThreads / 32);
+    return static_cast<long long>(sm_count) * per_sm * (kStreamThreads / 32);
 }
 
 void record(const spec_verify_opts* o, int k, cudaStream_t s) {
@@ -377,20 +384,20 @@ int launch_sampling(VerifyParams& p, int sm_count, const spec_verify_opts* o, cu
     if (extra) {  // the same read of every logit, paired by position, with the extra terms
         // pieces chosen for this pass's items (position pairs, not rows) and grid
         int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pair_stats_kernel<ET, kPairUnroll>, kThreads,
-                                                          0) != cudaSuccess || per_sm < 1)
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pair_stats_kernel<ET, kPairUnroll, true>,
+                                                          kStreamThreads, 0) != cudaSuccess || per_sm < 1)
             per_sm = 1;
         p.piece_len = pick_piece_len(static_cast<long long>(p.B) * (p.gamma + 1), p.V,
                                      static_cast<int>(sizeof(typename ET::storage)),
-                                     static_cast<long long>(sm_count) * per_sm * (kThreads / 32));
+                                     static_cast<long long>(sm_count) * per_sm * (kStreamThreads / 32));
         p.npieces = (p.V + p.piece_len - 1) / p.piece_len;
         const long long items = static_cast<long long>(p.B) * (p.gamma + 1) * p.npieces;
-        pair_stats_kernel<ET, kPairUnroll><<<grid_for(pair_stats_kernel<ET, kPairUnroll>, sm_count, items),
-                                             kThreads, 0, s>>>(p);
+        launch_stream(pair_stats_kernel<ET, kPairUnroll, true>, pair_stats_kernel<ET, kPairUnroll, false>,
+                      sm_count, items, s, p);
     } else {
         const long long stat_items = static_cast<long long>(p.B) * R * p.npieces;
-        row_stats_kernel<ET, kUnroll><<<grid_for(row_stats_kernel<ET, kUnroll>, sm_count, stat_items),
-                                        kThreads, 0, s>>>(p);
+        launch_stream(row_stats_kernel<ET, kUnroll, true>, row_stats_kernel<ET, kUnroll, false>, sm_count,
+                      stat_items, s, p);
     }
     record(o, 1, s);
     // scan-race grid, one resident wave: G = wave / B blocks per sequence when that is at
@@ -495,8 +502,8 @@ int launch_tree(VerifyParams& p, const TreeShape& t, int sm_count, const spec_ve
     const bool pdl = !(o && o->prof_events[1]);
     record(o, 0, s);
     const long long items = static_cast<long long>(p.B) * (t.N + t.M) * p.npieces;
-    auto stats = tree_stats_kernel<ET, kUnroll>;
-    stats<<<grid_for(stats, sm_count, items), kThreads, 0, s>>>(p, t.N, t.M);
+    launch_stream(tree_stats_kernel<ET, kUnroll, true>, tree_stats_kernel<ET, kUnroll, false>, sm_count, items,
+                  s, p, t.N, t.M);
     record(o, 1, s);
     {
         cudaLaunchConfig_t cfg = {};
@@ -541,8 +548,8 @@ int launch_greedy(VerifyParams& p, int sm_count, const spec_verify_opts* o, cuda
     const int R = p.gamma + 1;
     record(o, 0, s);
     const long long items = static_cast<long long>(p.B) * R * p.npieces;
-    row_argmax_kernel<ET, kUnroll><<<grid_for(row_argmax_kernel<ET, kUnroll>, sm_count, items),
-                                     kThreads, 0, s>>>(p);
+    launch_stream(row_argmax_kernel<ET, kUnroll, true>, row_argmax_kernel<ET, kUnroll, false>, sm_count,
+                  items, s, p);
     record(o, 1, s);
     scan_greedy_kernel<ET><<<p.B, kThreads, R * sizeof(int), s>>>(p);
     record(o, 2, s);
@@ -1212,11 +1219,11 @@ int spec_row_entropy(const void* logits, int rows, int V, float T, int dtype, fl
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const long long items = static_cast<long long>(rows) * p.npieces;
     if (dtype == SPEC_F32)
-        pair_stats_kernel<F32Elem, kPairUnroll><<<grid_for(pair_stats_kernel<F32Elem, kPairUnroll>, d->sm_count, items),
-                                                  kThreads, 0, s>>>(p);
+        launch_stream(pair_stats_kernel<F32Elem, kPairUnroll, true>, pair_stats_kernel<F32Elem, kPairUnroll, false>,
+                      d->sm_count, items, s, p);
     else
-        pair_stats_kernel<Bf16Elem, kPairUnroll><<<grid_for(pair_stats_kernel<Bf16Elem, kPairUnroll>, d->sm_count, items),
-                                                   kThreads, 0, s>>>(p);
+        launch_stream(pair_stats_kernel<Bf16Elem, kPairUnroll, true>, pair_stats_kernel<Bf16Elem, kPairUnroll, false>,
+                      d->sm_count, items, s, p);
     position_stats_kernel<<<rows, kThreads, 0, s>>>(p);
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
 }
@@ -1294,7 +1301,8 @@ int launch_vp_partials(VerifyParams& p, int sm_count, int x_offset, float2* stat
                        cudaStream_t s) {
     const int R = 2 * p.gamma + 1;
     const long long items = static_cast<long long>(p.B) * R * p.npieces;
-    row_stats_kernel<ET, kUnroll><<<grid_for(row_stats_kernel<ET, kUnroll>, sm_count, items), kThreads, 0, s>>>(p);
+    launch_stream(row_stats_kernel<ET, kUnroll, true>, row_stats_kernel<ET, kUnroll, false>, sm_count, items, s,
+                  p);
     const long long rows = static_cast<long long>(p.B) * R;
     vp_fold_kernel<<<static_cast<unsigned>(std::min<long long>((rows + kThreads - 1) / kThreads, 4LL * sm_count)),
                      kThreads, 0, s>>>(p, stats);
