@@ -319,6 +319,10 @@ constexpr int kStreamThreads = SPECVERIFY_STREAM_THREADS;
 // range, claimed by its warps from a shared counter (every thread of the block must call
 // it); without, the item whose index is the global warp index (the launch shape of small
 // calls, a warp for every item).
+// The streaming kernels are launched as programmatic dependents of whatever kernel precedes
+// them on the stream: wait for it (and its memory) before the first access.
+__device__ __forceinline__ void stream_pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 template <bool kClaim, class F>
 __device__ __forceinline__ void for_block_items(long long total, F&& f) {
     if (!kClaim) {
@@ -345,6 +349,7 @@ __device__ __forceinline__ void for_block_items(long long total, F&& f) {
 // that kernel (launched as a programmatic dependent) start as soon as blocks retire.
 template <class ET, int U, bool kClaim>
 __global__ void __launch_bounds__(kStreamThreads, SPECVERIFY_STATS_MINBLOCKS) row_stats_kernel(VerifyParams p) {
+    stream_pdl_wait();
     const int lane = threadIdx.x & 31;
     const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
     const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -515,6 +520,7 @@ __device__ __forceinline__ PairStat pair_piece(const typename ET::storage* rp,
 #endif
 template <class ET, int U, bool kClaim>
 __global__ void __launch_bounds__(kStreamThreads, SPECVERIFY_PAIR_MINBLOCKS) pair_stats_kernel(VerifyParams p) {
+    stream_pdl_wait();
     using S = typename ET::storage;
     const int lane = threadIdx.x & 31;
     const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
@@ -555,6 +561,7 @@ __global__ void __launch_bounds__(kStreamThreads, SPECVERIFY_PAIR_MINBLOCKS) pai
 // operation rounded on its own).  Runs after the scan, whose accepted counts it reads.
 __global__ void __launch_bounds__(256) position_stats_kernel(VerifyParams p) {
     extern __shared__ float s_hq[];  // [gamma]
+    asm volatile("griddepcontrol.launch_dependents;");  // (see scan_greedy_kernel)
     const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
     const int b = blockIdx.x;
     const int R = 2 * p.gamma + 1;
@@ -711,6 +718,7 @@ __device__ __forceinline__ ArgMax argmax_piece(const typename ET::storage* row, 
 
 template <class ET, int U, bool kClaim>
 __global__ void __launch_bounds__(kStreamThreads, 1) row_argmax_kernel(VerifyParams p) {
+    stream_pdl_wait();
     using S = typename ET::storage;
     const int lane = threadIdx.x & 31;
     const int R = p.gamma + 1;
@@ -751,6 +759,8 @@ __global__ void __launch_bounds__(256) scan_greedy_kernel(VerifyParams p) {
     const int R = p.gamma + 1;
     const int b = blockIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    // a following verify's streaming pass may be set up now: it waits for this grid
+    asm volatile("griddepcontrol.launch_dependents;");
     if (threadIdx.x == 0) {
         s_j = p.gamma;
         s_bad = 0;
@@ -1420,7 +1430,11 @@ __global__ void __launch_bounds__(256, SPECVERIFY_RACE_MINBLOCKS) scan_race_kern
             s_j = p.gamma;
             s_bad = 0;
         }
-        if (first) asm volatile("griddepcontrol.wait;" ::: "memory");
+        if (first) {
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            // a following verify's streaming pass may be set up now: it waits for this grid
+            asm volatile("griddepcontrol.launch_dependents;");
+        }
         first = false;
         __syncthreads();  // s_j and s_bad are set before any thread reports a bad token
         // any draft token outside [0, V) marks the whole sequence
@@ -1546,6 +1560,7 @@ struct TreeRace {
 
 template <class ET, int U, bool kClaim>
 __global__ void __launch_bounds__(kStreamThreads, SPECVERIFY_STATS_MINBLOCKS) tree_stats_kernel(VerifyParams p, int N, int M) {
+    stream_pdl_wait();
     using S = typename ET::storage;
     const int lane = threadIdx.x & 31;
     const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
@@ -1758,6 +1773,7 @@ __global__ void __launch_bounds__(256, SPECVERIFY_RACE_MINBLOCKS) tree_race_kern
     const int G = p.rgroups;
     const int b = blockIdx.x / G, g = blockIdx.x % G;
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");  // (see scan_greedy_kernel)
     const TreeRace tr = p.tree_race[b];
     if (tr.node < 0) return;
     const SeqInfo si = p.seq[b];

@@ -220,20 +220,35 @@ bool good_temperature(float t) { return std::isfinite(t) && t > 0.0f; }
 // Launch of a streaming kernel: one block of kStreamThreads per SM (the claiming variant kc,
 // whose warps share the block's items) when the items outnumber the warps of that grid;
 // otherwise blocks of kThreads of the plain variant kp, one item per warp, so that a small
-// call starts few threads and spreads its items over as many SMs as it can.
+// call starts few threads and spreads its items over as many SMs as it can.  The launch is a
+// programmatic dependent of the kernel before it on the stream (the kernel waits for that one
+// to finish before touching memory), so its blocks are set up while the previous verify's
+// last kernel drains.
 template <class KC, class KP, class... A>
-void launch_stream(KC kc, KP kp, int sm_count, long long items, cudaStream_t s, A... args) {
+cudaError_t launch_stream(KC kc, KP kp, int sm_count, long long items, cudaStream_t s, A... args) {
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kc, kStreamThreads, 0) != cudaSuccess ||
         per_sm < 1)
         per_sm = 1;
     const long long full = static_cast<long long>(sm_count) * per_sm;
-    if (items >= full * (kStreamThreads / 32)) {
-        kc<<<static_cast<unsigned>(full), kStreamThreads, 0, s>>>(args...);
-    } else {
-        const long long g = (items + (kThreads / 32) - 1) / (kThreads / 32);
-        kp<<<static_cast<unsigned>(g < 1 ? 1 : g), kThreads, 0, s>>>(args...);
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const bool claim = items >= full * (kStreamThreads / 32);
+    const long long g = claim ? full : (items + (kThreads / 32) - 1) / (kThreads / 32);
+    cfg.gridDim = dim3(static_cast<unsigned>(g < 1 ? 1 : g));
+    cfg.blockDim = dim3(claim ? kStreamThreads : kThreads);
+    cudaError_t e = claim ? cudaLaunchKernelEx(&cfg, kc, args...) : cudaLaunchKernelEx(&cfg, kp, args...);
+    if (e != cudaSuccess) {  // a device without programmatic launches: a plain one
+        cudaGetLastError();
+        cfg.numAttrs = 0;
+        e = claim ? cudaLaunchKernelEx(&cfg, kc, args...) : cudaLaunchKernelEx(&cfg, kp, args...);
     }
+    return e;
 }
 
 // Warps of the streaming kernel's full grid.
