@@ -97,6 +97,7 @@ __device__ __forceinline__ RaceState race_warp_span(const VerifyParams& p,
     };
     auto load_chunk = [&](int x0, uint4 (&dst)[VPL]) {
         const int x1 = min(xb, x0 + kRaceWarpTokens);
+        if (residual) prefetch_l2(rd, x0, x1, lane);
         const bool ok = x0 < x1 && (reinterpret_cast<uintptr_t>(rt + x0) & 15u) == 0;
         const int nv = ok ? (x1 - x0) / ET::kVec : 0;
         const uint4* vt = reinterpret_cast<const uint4*>(rt + (ok ? x0 : 0));

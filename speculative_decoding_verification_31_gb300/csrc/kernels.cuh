@@ -913,6 +913,18 @@ __device__ __forceinline__ uint32_t vector_candidates(const float (&ft)[ET::kVec
     return cand;
 }
 
+// Bring row[x0, x1) into L2, one prefetch per 128-byte line spread over the warp's lanes.
+// The chunked races read the residual's draft row only at candidate tokens, one dependent
+// load each; prefetched with the target vectors, those loads hit L2 (batched serving 59.4 ->
+// 57.7 us; the early-exit path's 8 KB race units, which seed from a first pass over the
+// piece, measured 1% slower with it and go without).
+template <class S>
+__device__ __forceinline__ void prefetch_l2(const S* row, int x0, int x1, int lane) {
+    constexpr int kLine = 128 / static_cast<int>(sizeof(S));
+    for (int x = x0 + lane * kLine; x < x1; x += 32 * kLine)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(row + x));
+}
+
 // Race over tokens [x0, x1) of the raced row; every lane offers its tokens in increasing x.
 // The residual's draft row is read only at candidate tokens.
 template <class ET>
@@ -1138,6 +1150,7 @@ __device__ __forceinline__ void race_rows_block(const VerifyParams& p, int b,
     auto load_piece = [&](int cb, uint4 (&dst)[VPL]) {
         const int x0 = chunk_x0(cb);
         const int x1 = min(p.V, x0 + kRaceWarpTokens);
+        if (residual) prefetch_l2(rd, x0, x1, lane);
         const bool ok = x0 < x1 && (reinterpret_cast<uintptr_t>(rt + x0) & 15u) == 0;
         const int nv = ok ? (x1 - x0) / ET::kVec : 0;
         const uint4* vt = reinterpret_cast<const uint4*>(rt + (ok ? x0 : 0));
