@@ -16,8 +16,9 @@
 // per-position entropies and KL), and the token-tree kernels.
 // Greedy mode runs row_argmax (first argmax per (row, piece)) and scan_greedy.
 //
-// Streaming work is split into warp-sized items (one row piece each) taken round-robin by
-// every warp of a grid sized to the GPU, so that no item ever waits for another.
+// Streaming work is split into warp-sized items (one row piece each); each SM's block takes a
+// contiguous share and its warps claim the items one at a time (for_block_items), so that no
+// item ever waits for another and the warps of an SM finish together.
 #pragma once
 
 #include <cfloat>
@@ -2159,10 +2160,29 @@ constexpr int kEarlyUnroll = SPECVERIFY_EARLY_UNROLL;
 #endif
 constexpr int kEarlyRaceWarps = SPECVERIFY_EARLY_RACE_WARPS;  // of the 8 warps of a block
 
+// Fill a[0, na) with fa and b[0, nb) with fb (8-byte words) before a launch that depends on
+// them.  Launched as a programmatic dependent of the kernel before it, it waits for that one,
+// then lets its own dependent be set up while it fills.
+__global__ void __launch_bounds__(256) prep_fill_kernel(unsigned long long* a, long long na,
+                                                        unsigned long long fa, unsigned long long* b,
+                                                        long long nb, unsigned long long fb) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < na + nb; i += stride) {
+        if (i < na)
+            a[i] = fa;
+        else
+            b[i - na] = fb;
+    }
+}
+
 template <class ET, int U>
 __global__ void __launch_bounds__(256, SPECVERIFY_EARLY_MINBLOCKS) verify_early_kernel(VerifyParams p) {
     using S = typename ET::storage;
     const int lane = threadIdx.x & 31;
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the workspace fill (prep_fill_kernel)
+    asm volatile("griddepcontrol.launch_dependents;");   // (see scan_greedy_kernel)
     const int R = 2 * p.gamma + 1;
     const int np = p.npieces;
     if ((threadIdx.x >> 5) < 8 - kEarlyRaceWarps) {

@@ -494,17 +494,43 @@ int launch_early(VerifyParams& p, int sm_count, const spec_verify_opts* o, cudaS
     const long long want = (static_cast<long long>(p.n_init) * p.npieces + (kThreads / 32) - 1) /
                            (kThreads / 32);
     if (want < grid) grid = want;
-    if (cudaMemsetAsync(ws + L.e_rowstat_off, 0xFF,
-                        (L.e_stat_off - L.e_rowstat_off) + rows * p.npieces * sizeof(float2), s) != cudaSuccess ||
-        cudaMemsetAsync(ws + L.e_zero_off, 0,
-                        (L.e_race_off - L.e_zero_off) +
-                            static_cast<size_t>(p.B) * p.npieces * sizeof(unsigned long long), s) != cudaSuccess)
-        return SPEC_ECUDA;
+    // the row statistics and their partials start empty (every bit set), the counters, events
+    // and race winners zero: one small kernel, the early-exit kernel its programmatic
+    // dependent (it waits for the fill with griddepcontrol.wait)
+    const size_t fill_bytes = (L.e_stat_off - L.e_rowstat_off) + rows * p.npieces * sizeof(float2);
+    const size_t zero_bytes = (L.e_race_off - L.e_zero_off) +
+                              static_cast<size_t>(p.B) * p.npieces * sizeof(unsigned long long);
+    const long long n_fill = static_cast<long long>(fill_bytes / 8), n_zero = static_cast<long long>(zero_bytes / 8);
+    long long prep_grid = (n_fill + n_zero + kThreads - 1) / kThreads;
+    if (prep_grid > 2LL * sm_count) prep_grid = 2LL * sm_count;
     record(o, 0, s);
-    void* args[] = {&p};
-    if (cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kernel), dim3(static_cast<unsigned>(grid)),
-                                    dim3(kThreads), args, 0, s) != cudaSuccess)
-        return SPEC_ECUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.gridDim = dim3(static_cast<unsigned>(prep_grid < 1 ? 1 : prep_grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.numAttrs = 1;
+    unsigned long long* fill = reinterpret_cast<unsigned long long*>(ws + L.e_rowstat_off);
+    unsigned long long* zero = reinterpret_cast<unsigned long long*>(ws + L.e_zero_off);
+    if (cudaLaunchKernelEx(&cfg, prep_fill_kernel, fill, n_fill, ~0ull, zero, n_zero, 0ull) != cudaSuccess) {
+        (void)cudaGetLastError();  // no programmatic launches: a plain one
+        cfg.numAttrs = 0;
+        if (cudaLaunchKernelEx(&cfg, prep_fill_kernel, fill, n_fill, ~0ull, zero, n_zero, 0ull) != cudaSuccess)
+            return SPEC_ECUDA;
+    }
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.numAttrs = 2;
+    if (cudaLaunchKernelEx(&cfg, kernel, p) != cudaSuccess) {
+        (void)cudaGetLastError();  // not accepted together: a plain cooperative launch
+        cfg.attrs = attr + 1;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, kernel, p) != cudaSuccess) return SPEC_ECUDA;
+    }
     record(o, 1, s);
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
 }
