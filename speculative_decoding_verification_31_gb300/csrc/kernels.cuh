@@ -562,6 +562,8 @@ __global__ void __launch_bounds__(kStreamThreads, SPECVERIFY_PAIR_MINBLOCKS) pai
 // operation rounded on its own).  Runs after the scan, whose accepted counts it reads.
 __global__ void __launch_bounds__(256) position_stats_kernel(VerifyParams p) {
     extern __shared__ float s_hq[];  // [gamma]
+    // a programmatic dependent of the scan-race kernel (or of pair_stats): wait for it
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");  // (see scan_greedy_kernel)
     const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
     const int b = blockIdx.x;
@@ -732,6 +734,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) row_argmax_kernel(VerifyPar
         const ArgMax a = argmax_piece<ET, U>(row, x0, x1, lane);
         if (lane == 0) p.stat_parts[item] = make_float2(a.v, __int_as_float(a.i));
     });
+    asm volatile("griddepcontrol.launch_dependents;");
 }
 
 // ----------------------------------------------------------------------------------------
@@ -760,7 +763,9 @@ __global__ void __launch_bounds__(256) scan_greedy_kernel(VerifyParams p) {
     const int R = p.gamma + 1;
     const int b = blockIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    // a following verify's streaming pass may be set up now: it waits for this grid
+    // launched as a programmatic dependent of row_argmax: wait for its partials; a following
+    // verify's streaming pass may be set up now (it waits for this grid)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
     if (threadIdx.x == 0) {
         s_j = p.gamma;

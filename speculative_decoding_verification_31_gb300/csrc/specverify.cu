@@ -445,7 +445,9 @@ int launch_sampling(VerifyParams& p, int sm_count, const spec_verify_opts* o, cu
         return SPEC_ECUDA;
     record(o, 2, s);
     if (extra) {
-        position_stats_kernel<<<p.B, kThreads, static_cast<size_t>(p.gamma) * sizeof(float), s>>>(p);
+        if (launch_pdl(position_stats_kernel, p.B, static_cast<size_t>(p.gamma) * sizeof(float), s,
+                       !(o && o->prof_events[2]), p) != cudaSuccess)
+            return SPEC_ECUDA;
         record(o, 3, s);
     }
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
@@ -592,7 +594,8 @@ int launch_greedy(VerifyParams& p, int sm_count, const spec_verify_opts* o, cuda
     launch_stream(row_argmax_kernel<ET, kUnroll, true>, row_argmax_kernel<ET, kUnroll, false>, sm_count,
                   items, s, p);
     record(o, 1, s);
-    scan_greedy_kernel<ET><<<p.B, kThreads, R * sizeof(int), s>>>(p);
+    if (launch_pdl(scan_greedy_kernel<ET>, p.B, R * sizeof(int), s, !(o && o->prof_events[1]), p) != cudaSuccess)
+        return SPEC_ECUDA;
     record(o, 2, s);
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
 }
