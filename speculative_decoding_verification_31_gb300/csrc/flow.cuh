@@ -35,7 +35,7 @@
 // race unit cannot share its threshold the way a block does.
 //
 // The flow path's workspace (cursors, counts, flags, tickets, packed winners and the row
-// partials in use, all meaning "nothing yet" when zero) is zeroed by flow_prep_kernel just
+// partials in use, all meaning "nothing yet" when zero) is zeroed by prep_fill_kernel just
 // before the flow kernel, which is its programmatic dependent where the device allows it.
 #pragma once
 
@@ -445,18 +445,6 @@ __global__ void __launch_bounds__(256, SPECVERIFY_FLOW_MINBLOCKS) verify_flow_ke
         }
         flow_span<ET>(p, static_cast<int>(c / U), static_cast<int>(c % U), static_cast<int>(first_end - c), lane);
     }
-}
-
-// Zero the flow control region (n_ctl 16-byte words) and the row partials in use (n_stat
-// words) before the flow kernel, which may start as soon as every block of this kernel has
-// begun.
-__global__ void __launch_bounds__(256) flow_prep_kernel(uint4* ctl, long long n_ctl, uint4* stat,
-                                                        long long n_stat) {
-    asm volatile("griddepcontrol.launch_dependents;");
-    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_ctl + n_stat;
-         i += stride)
-        (i < n_ctl ? ctl[i] : stat[i - n_ctl]) = make_uint4(0u, 0u, 0u, 0u);
 }
 
 }  // namespace specverify

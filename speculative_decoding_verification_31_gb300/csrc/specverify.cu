@@ -337,11 +337,29 @@ int launch_flow(VerifyParams& p, int sm_count, const spec_verify_opts* o, cudaSt
     const long long n_ctl = static_cast<long long>(L.flow_bytes / 16);
     const long long n_stat = static_cast<long long>(
         (static_cast<size_t>(p.B) * (2 * p.gamma + 1) * p.npieces * sizeof(unsigned long long) + 15) / 16);
-    long long prep_grid = (n_ctl + n_stat + kThreads - 1) / kThreads;
+    long long prep_grid = (2 * (n_ctl + n_stat) + kThreads - 1) / kThreads;
     if (prep_grid > 2LL * sm_count) prep_grid = 2LL * sm_count;
     record(o, 0, s);
-    flow_prep_kernel<<<static_cast<unsigned>(prep_grid < 1 ? 1 : prep_grid), kThreads, 0, s>>>(
-        reinterpret_cast<uint4*>(ws + L.flow_off), n_ctl, reinterpret_cast<uint4*>(ws + L.f_stat_off), n_stat);
+    {
+        cudaLaunchConfig_t pc = {};
+        pc.gridDim = dim3(static_cast<unsigned>(prep_grid < 1 ? 1 : prep_grid));
+        pc.blockDim = dim3(kThreads);
+        pc.stream = s;
+        cudaLaunchAttribute pa[1];
+        pa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        pa[0].val.programmaticStreamSerializationAllowed = 1;
+        pc.attrs = pa;
+        pc.numAttrs = 1;
+        unsigned long long* ctl = reinterpret_cast<unsigned long long*>(ws + L.flow_off);
+        unsigned long long* stat = reinterpret_cast<unsigned long long*>(ws + L.f_stat_off);
+        if (cudaLaunchKernelEx(&pc, prep_fill_kernel, ctl, 2 * n_ctl, 0ull, stat, 2 * n_stat, 0ull) != cudaSuccess) {
+            (void)cudaGetLastError();  // no programmatic launches: a plain one
+            pc.numAttrs = 0;
+            if (cudaLaunchKernelEx(&pc, prep_fill_kernel, ctl, 2 * n_ctl, 0ull, stat, 2 * n_stat, 0ull) !=
+                cudaSuccess)
+                return SPEC_ECUDA;
+        }
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(sm_count * per_sm));
     cfg.blockDim = dim3(kThreads);
