@@ -131,7 +131,7 @@ struct VerifyParams {
 __host__ __device__ __forceinline__ int race_slots(int rpieces) { return rpieces + 1; }
 
 // Row pieces of the streaming passes: between kMinPieceBytes and kMaxPieceBytes of logits
-// (the early-exit path: kEarlyPieceBytes).
+// (the early-exit path: kEarlyPieceBytes up to twice that, by the call's size).
 #ifndef SPECVERIFY_PIECE_BYTES
 #define SPECVERIFY_PIECE_BYTES 16384
 #endif

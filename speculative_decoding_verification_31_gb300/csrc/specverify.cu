@@ -483,8 +483,19 @@ int launch_early(VerifyParams& p, int sm_count, const spec_verify_opts* o, cudaS
         per_sm < 1)
         return SPEC_ECUDA;
     const int R = 2 * p.gamma + 1;
-    p.piece_len = kEarlyPieceBytes / static_cast<int>(sizeof(typename ET::storage));
-    p.npieces = (p.V + p.piece_len - 1) / p.piece_len;
+    const long long row_warps = static_cast<long long>(sm_count) * per_sm * (8 - kEarlyRaceWarps);
+    // pieces: the largest of kEarlyPieceBytes x {2, 1.5, 1} that still gives every row warp
+    // two units among the rows all sequences start with (larger units cost less per byte; a
+    // few sequences need small ones to spread each row over many warps).  Measured per call:
+    // throughput workload 167.5 / 155.0 / 152.1 us with 8 / 12 / 16 KB; single sequence
+    // 32.6 / 37.0 / 40.2 us.
+    const long long rows0 = static_cast<long long>(p.B) * (p.gamma > 0 ? 2 : 1);
+    const int es = static_cast<int>(sizeof(typename ET::storage));
+    for (int k = 4; k >= 2; --k) {
+        p.piece_len = (kEarlyPieceBytes * k / 2) / es;
+        p.npieces = (p.V + p.piece_len - 1) / p.piece_len;
+        if (rows0 * p.npieces >= 2 * row_warps) break;
+    }
     p.stat_parts = reinterpret_cast<float2*>(ws + L.e_stat_off);
     p.row_stat = reinterpret_cast<float2*>(ws + L.e_rowstat_off);
     p.task = reinterpret_cast<int*>(ws + L.e_task_off);
@@ -492,7 +503,6 @@ int launch_early(VerifyParams& p, int sm_count, const spec_verify_opts* o, cudaS
     p.enq_pos = reinterpret_cast<int*>(ws + L.e_enq_off);
     // positions in flight that keep the row warps busy, and the positions every sequence
     // starts with (more than position 0 only when there are too few sequences for that)
-    const long long row_warps = static_cast<long long>(sm_count) * per_sm * (8 - kEarlyRaceWarps);
     p.early_fill = static_cast<int>(std::max(1LL, row_warps / (2LL * p.npieces)));
     p.early_L0 = std::min(p.gamma, std::max(0, (p.early_fill + p.B - 1) / p.B - 1));
     const int per_seq = p.early_L0 < p.gamma ? 2 * (p.early_L0 + 1) : 2 * p.gamma + 1;
