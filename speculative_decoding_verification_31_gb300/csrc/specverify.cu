@@ -476,7 +476,7 @@ int launch_sampling(VerifyParams& p, int sm_count, const spec_verify_opts* o, cu
 // work that warps which never wait will publish).
 template <class ET>
 int launch_early(VerifyParams& p, int sm_count, const spec_verify_opts* o, cudaStream_t s,
-                 const Layout& L, char* ws) {
+                 const Layout& L, char* ws, bool host_rows) {
     auto kernel = verify_early_kernel<ET, kEarlyUnroll>;
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) != cudaSuccess ||
@@ -488,10 +488,11 @@ int launch_early(VerifyParams& p, int sm_count, const spec_verify_opts* o, cudaS
     // two units among the rows all sequences start with (larger units cost less per byte; a
     // few sequences need small ones to spread each row over many warps).  Measured per call:
     // throughput workload 167.5 / 155.0 / 152.1 us with 8 / 12 / 16 KB; single sequence
-    // 32.6 / 37.0 / 40.2 us.
+    // 32.6 / 37.0 / 40.2 us.  Rows in host memory keep kEarlyPieceBytes (over the host link
+    // the throughput workload measured 1.80e6 rows/s with 8 KB, 1.72e6 with 16 KB).
     const long long rows0 = static_cast<long long>(p.B) * (p.gamma > 0 ? 2 : 1);
     const int es = static_cast<int>(sizeof(typename ET::storage));
-    for (int k = 4; k >= 2; --k) {
+    for (int k = host_rows ? 2 : 4; k >= 2; --k) {
         p.piece_len = (kEarlyPieceBytes * k / 2) / es;
         p.npieces = (p.V + p.piece_len - 1) / p.piece_len;
         if (rows0 * p.npieces >= 2 * row_warps) break;
@@ -709,8 +710,8 @@ int verify_ex_impl(const void* target_logits, const void* draft_logits, const in
                 p.mirror_draft = static_cast<char*>(d->mirror) + tb;
             }
         }
-        return dtype == SPEC_F32 ? launch_early<F32Elem>(p, d->sm_count, opts, s, L, ws)
-                                 : launch_early<Bf16Elem>(p, d->sm_count, opts, s, L, ws);
+        return dtype == SPEC_F32 ? launch_early<F32Elem>(p, d->sm_count, opts, s, L, ws, host_rows)
+                                 : launch_early<Bf16Elem>(p, d->sm_count, opts, s, L, ws, host_rows);
     }
     const bool fused = d->coop && opts && (opts->flags & SPEC_FLAG_FUSED) && !wants_position_stats(p);
     if (fused) {
