@@ -43,6 +43,14 @@
  *   - The plain entry points use a workspace the library allocates per device on first use
  *     (and grows when a larger problem arrives); calls that use it must not run
  *     concurrently on one device.  The _ex entry points can take a caller workspace.
+ *   - Kernels and stream order: each call's first kernel is launched with programmatic
+ *     stream serialization and waits (griddepcontrol.wait) for the kernel before it on the
+ *     stream before touching memory, so inputs written by that kernel are read; each call's
+ *     last kernel lets a following kernel that was itself launched with programmatic stream
+ *     serialization be scheduled early.  Such a kernel must wait for its prerequisite grid
+ *     (griddepcontrol.wait / cudaGridDependencySynchronize) before it reads this call's
+ *     outputs, as programmatic launches require; ordinary launches, copies and events see
+ *     the call complete as usual.
  */
 #ifndef SPECVERIFY_H
 #define SPECVERIFY_H
