@@ -95,6 +95,7 @@ struct VerifyParams {
     int* enq_pos;               // [B] last position whose rows are queued, minus early_L0
     int early_L0;               // positions 0..early_L0 of every sequence are queued at the start
     int early_fill;             // positions in flight that keep the row warps busy
+    int early_growth;           // extra positions queued ahead after an accepted position i: (i+1)*g/4
     int* race_done;             // [B] race units finished
     int* seq_decided;           // sequences whose first rejection (or bonus) is known
     int* seq_finished;          // sequences finished (token written)
@@ -1997,7 +1998,9 @@ __device__ __forceinline__ int early_event(const VerifyParams& p, int* addr) {
 
 // On acceptance at position i, queue (i+1)*g/4 extra positions ahead.  Throughput workload
 // (16 KB units), us per call with g = 0 / 1 / 2 / 3 / 4: 152.4 / 152.4 / 145.7 / 149.0 / 162.3;
-// the smaller workloads within 1 us of each other.
+// the smaller workloads within 1 us of each other.  Rows in host memory read none ahead
+// (g = 0): over the host link the rows read past a rejection cost as much as the others
+// (1.80e6 rows/s end to end with g = 0, 1.53e6 with g = 2).
 #ifndef SPECVERIFY_EARLY_GROWTH
 #define SPECVERIFY_EARLY_GROWTH 2
 #endif
@@ -2057,7 +2060,7 @@ __device__ __forceinline__ void early_decide_from(const VerifyParams& p, int b, 
         if (lane == 0) {
             const int undecided = max(1, p.B - ld_relaxed(p.seq_decided));
             const int fill = (p.early_fill + undecided - 1) / undecided;
-            const int grow = ((i + 1) * kEarlyGrowth) >> 2;
+            const int grow = ((i + 1) * p.early_growth) >> 2;
             early_enqueue_upto(p, b, min(p.gamma, i + max(1, max(fill, 1 + grow))));
             t = early_event(p, p.pos_done + static_cast<long long>(b) * (p.gamma + 1) + i + 1);
         }

@@ -505,6 +505,7 @@ int launch_early(VerifyParams& p, int sm_count, const spec_verify_opts* o, cudaS
     // positions in flight that keep the row warps busy, and the positions every sequence
     // starts with (more than position 0 only when there are too few sequences for that)
     p.early_fill = static_cast<int>(std::max(1LL, row_warps / (2LL * p.npieces)));
+    p.early_growth = host_rows ? 0 : kEarlyGrowth;
     p.early_L0 = std::min(p.gamma, std::max(0, (p.early_fill + p.B - 1) / p.B - 1));
     const int per_seq = p.early_L0 < p.gamma ? 2 * (p.early_L0 + 1) : 2 * p.gamma + 1;
     p.n_init = p.B * per_seq;
