@@ -425,12 +425,14 @@ int launch_sampling(VerifyParams& p, int sm_count, const spec_verify_opts* o, cu
                                      static_cast<long long>(sm_count) * per_sm * (kStreamThreads / 32));
         p.npieces = (p.V + p.piece_len - 1) / p.piece_len;
         const long long items = static_cast<long long>(p.B) * (p.gamma + 1) * p.npieces;
-        launch_stream(pair_stats_kernel<ET, kPairUnroll, true>, pair_stats_kernel<ET, kPairUnroll, false>,
-                      sm_count, items, s, p);
+        if (launch_stream(pair_stats_kernel<ET, kPairUnroll, true>, pair_stats_kernel<ET, kPairUnroll, false>,
+                      sm_count, items, s, p) != cudaSuccess)
+            return SPEC_ECUDA;
     } else {
         const long long stat_items = static_cast<long long>(p.B) * R * p.npieces;
-        launch_stream(row_stats_kernel<ET, kUnroll, true>, row_stats_kernel<ET, kUnroll, false>, sm_count,
-                      stat_items, s, p);
+        if (launch_stream(row_stats_kernel<ET, kUnroll, true>, row_stats_kernel<ET, kUnroll, false>, sm_count,
+                      stat_items, s, p) != cudaSuccess)
+            return SPEC_ECUDA;
     }
     record(o, 1, s);
     // scan-race grid, one resident wave: G = wave / B blocks per sequence when that is at
@@ -575,8 +577,9 @@ int launch_tree(VerifyParams& p, const TreeShape& t, int sm_count, const spec_ve
     const bool pdl = !(o && o->prof_events[1]);
     record(o, 0, s);
     const long long items = static_cast<long long>(p.B) * (t.N + t.M) * p.npieces;
-    launch_stream(tree_stats_kernel<ET, kUnroll, true>, tree_stats_kernel<ET, kUnroll, false>, sm_count, items,
-                  s, p, t.N, t.M);
+    if (launch_stream(tree_stats_kernel<ET, kUnroll, true>, tree_stats_kernel<ET, kUnroll, false>, sm_count, items,
+                  s, p, t.N, t.M) != cudaSuccess)
+        return SPEC_ECUDA;
     record(o, 1, s);
     {
         cudaLaunchConfig_t cfg = {};
@@ -621,8 +624,9 @@ int launch_greedy(VerifyParams& p, int sm_count, const spec_verify_opts* o, cuda
     const int R = p.gamma + 1;
     record(o, 0, s);
     const long long items = static_cast<long long>(p.B) * R * p.npieces;
-    launch_stream(row_argmax_kernel<ET, kUnroll, true>, row_argmax_kernel<ET, kUnroll, false>, sm_count,
-                  items, s, p);
+    if (launch_stream(row_argmax_kernel<ET, kUnroll, true>, row_argmax_kernel<ET, kUnroll, false>, sm_count,
+                  items, s, p) != cudaSuccess)
+        return SPEC_ECUDA;
     record(o, 1, s);
     if (launch_pdl(scan_greedy_kernel<ET>, p.B, R * sizeof(int), s, !(o && o->prof_events[1]), p) != cudaSuccess)
         return SPEC_ECUDA;
@@ -1292,12 +1296,12 @@ int spec_row_entropy(const void* logits, int rows, int V, float T, int dtype, fl
     if (rc) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const long long items = static_cast<long long>(rows) * p.npieces;
-    if (dtype == SPEC_F32)
-        launch_stream(pair_stats_kernel<F32Elem, kPairUnroll, true>, pair_stats_kernel<F32Elem, kPairUnroll, false>,
-                      d->sm_count, items, s, p);
-    else
-        launch_stream(pair_stats_kernel<Bf16Elem, kPairUnroll, true>, pair_stats_kernel<Bf16Elem, kPairUnroll, false>,
-                      d->sm_count, items, s, p);
+    const cudaError_t e = dtype == SPEC_F32
+        ? launch_stream(pair_stats_kernel<F32Elem, kPairUnroll, true>, pair_stats_kernel<F32Elem, kPairUnroll, false>,
+                        d->sm_count, items, s, p)
+        : launch_stream(pair_stats_kernel<Bf16Elem, kPairUnroll, true>, pair_stats_kernel<Bf16Elem, kPairUnroll, false>,
+                        d->sm_count, items, s, p);
+    if (e != cudaSuccess) return SPEC_ECUDA;
     position_stats_kernel<<<rows, kThreads, 0, s>>>(p);
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
 }
@@ -1375,8 +1379,9 @@ int launch_vp_partials(VerifyParams& p, int sm_count, int x_offset, float2* stat
                        cudaStream_t s) {
     const int R = 2 * p.gamma + 1;
     const long long items = static_cast<long long>(p.B) * R * p.npieces;
-    launch_stream(row_stats_kernel<ET, kUnroll, true>, row_stats_kernel<ET, kUnroll, false>, sm_count, items, s,
-                  p);
+    if (launch_stream(row_stats_kernel<ET, kUnroll, true>, row_stats_kernel<ET, kUnroll, false>, sm_count, items, s,
+                  p) != cudaSuccess)
+        return SPEC_ECUDA;
     const long long rows = static_cast<long long>(p.B) * R;
     vp_fold_kernel<<<static_cast<unsigned>(std::min<long long>((rows + kThreads - 1) / kThreads, 4LL * sm_count)),
                      kThreads, 0, s>>>(p, stats);
