@@ -317,14 +317,14 @@ __device__ __forceinline__ void row_stats_item(const VerifyParams& p, int b, int
 #endif
 constexpr int kStreamThreads = SPECVERIFY_STREAM_THREADS;
 
-// Items [0, total) of a streaming pass, one item per warp at a time: with kClaim, this block's
-// range, claimed by its warps from a shared counter (every thread of the block must call
-// it); without, the item whose index is the global warp index (the launch shape of small
-// calls, a warp for every item).
 // The streaming kernels are launched as programmatic dependents of whatever kernel precedes
 // them on the stream: wait for it (and its memory) before the first access.
 __device__ __forceinline__ void stream_pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Items [0, total) of a streaming pass, one item per warp at a time: with kClaim, this block's
+// range, claimed by its warps from a shared counter (every thread of the block must call
+// it); without, the item whose index is the global warp index (the launch shape of small
+// calls, a warp for every item).
 template <bool kClaim, class F>
 __device__ __forceinline__ void for_block_items(long long total, F&& f) {
     if (!kClaim) {
