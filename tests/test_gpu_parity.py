@@ -160,6 +160,24 @@ def test_throughput_workload_full_size_sampled(sv, orc):
         assert np.all((g["n"] >= 0) & (g["n"] <= w.gamma))
 
 
+@pytest.mark.parametrize("B,gamma,V,dtype", [(24, 8, 128257, "bf16"), (20, 8, 65537, "f32")])
+def test_streaming_claim_launch_unaligned_rows(sv, orc, B, gamma, V, dtype):
+    """Calls with more row pieces than the streaming grid has warps take the claiming launch
+    (one block per SM, pieces claimed from a shared counter); here with rows that start off
+    16-byte boundaries (odd V), against the oracle, in sampling and greedy mode."""
+    w = workloads.generic(B=B, gamma=gamma, V=V, dtype=dtype, seed=B + V, sigma=0.8, T=0.9, Td=0.45)
+    dw = DeviceWorkload(w)
+    for seed in (0, 3):
+        g = run_gpu(sv, dw, seed, diagnostics=(seed == 0))
+        compare_sampling(w, g, orc.verify(w.target, w.draft, w.tokens, w.T, w.Td, seed),
+                         check_values=(seed == 0))
+    out_t, out_n = sv.spec_verify_greedy_ex(dw.target, dw.tokens)
+    torch.cuda.synchronize()
+    rt, rn, _ = orc.verify_greedy(w.target, w.tokens)
+    compare_greedy(out_t.cpu().numpy(), out_n.cpu().numpy(), rt, rn)
+    assert sv.spec_verify_check() == sv.SPEC_OK
+
+
 def test_seq_index_base_splits_a_batch(sv, orc):
     """Two half-batch calls with seq_index_base give exactly the one-call result."""
     w = workloads.generic(B=8, gamma=5, V=6000, dtype="bf16", seed=9, T=0.8, Td=0.4)
