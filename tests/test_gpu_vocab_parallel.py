@@ -54,7 +54,9 @@ def emulate(sv, w, world, seed, tokens=None, per_seq=False):
 
 
 CASES = [(5, 4, 3001, "bf16", 2), (4, 6, 2000, "f32", 3), (3, 0, 1500, "bf16", 2),
-         (3, 40, 20000, "bf16", 4), (6, 3, 40001, "f32", 2), (2, 5, 152064, "bf16", 8)]
+         (3, 40, 20000, "bf16", 4), (6, 3, 40001, "f32", 2), (2, 5, 152064, "bf16", 8),
+         # each shard with more row pieces than the streaming grid has warps (its claiming launch)
+         (32, 8, 128256, "bf16", 2)]
 
 
 @pytest.mark.parametrize("B,gamma,V,dtype,world", CASES)
