@@ -16,8 +16,13 @@ steps).  Rank 0 prints one JSON line:
   cpu_baseline the CPU oracle on a bounded sample of the same workload, on 1 host core
 
 ``--impl reference`` times the CPU oracle as the reference arm (there is no reference code to
-install: the pages describe the method only).  Under torchrun with N > 1 every rank verifies
-its own batch (global sequence indices offset by rank) with no collective on the data path.
+install: the pages describe the method only).  With ``--gpus N`` (N > 1) the script starts N
+ranks itself, one process per GPU, unless a launcher such as torchrun already set WORLD_SIZE;
+every rank verifies its own batch (global sequence indices offset by rank) with no collective
+on the data path, and the line reports the slowest rank's time.  The line also carries a
+sustained leg (the step for over a second, clocks sampled inside it) and ``per_config``: the
+other four workloads (and the greedy modes) with rotating input copies where one copy fits in
+L2, each with its kernel split, roofline fraction and the oracle's one-core rate.
 """
 from __future__ import annotations
 
@@ -185,6 +190,118 @@ def early_exit_rows_read(n: np.ndarray, gamma: int) -> tuple[int, int]:
     return streamed, raced
 
 
+def device_copies(w, dev, l2: int, greedy: bool):
+    """The workload's logits on the device, as `copies` back-to-back copies whose total
+    exceeds twice L2 when one copy alone would not (calls rotate over them, so every call
+    reads HBM, not a warm L2); one copy otherwise.  Returns (targets, drafts, copies)."""
+    import torch
+    nbytes = w.bytes_greedy() if greedy else w.bytes_sampling()
+    copies = 1 if nbytes > 2 * l2 else int(-(-2 * l2 // nbytes)) + 1
+    t = to_torch(w.target, w.dtype).to(dev)
+    d = to_torch(w.draft, w.dtype).to(dev)
+    tb = t.unsqueeze(0).expand(copies, *t.shape).contiguous()
+    db = d.unsqueeze(0).expand(copies, *d.shape).contiguous()
+    return tb, db, copies
+
+
+def time_calls(call, n: int, stream) -> float:
+    """Mean ms per call over n calls (call(k) issues call k), CUDA events on `stream`, after
+    warm-up calls."""
+    import torch
+    for k in range(5):
+        call(k)
+    torch.cuda.synchronize()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for k in range(n):
+        call(k)
+    s1.record(stream)
+    torch.cuda.synchronize()
+    return s0.elapsed_time(s1) / n
+
+
+def kernel_split_ms(call_events, n: int, nkern: int, stream) -> list:
+    """Mean CUDA-event time of each of a call's nkern kernels over n calls (events recorded
+    between the kernels, which also turns their programmatic launch off)."""
+    import torch
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nkern + 1)] for _ in range(n)]
+    for e in evs:
+        for ev in e:
+            ev.record(stream)
+    torch.cuda.synchronize()
+    for k in range(n):
+        call_events(k, evs[k])
+    torch.cuda.synchronize()
+    return [float(np.mean([e[i].elapsed_time(e[i + 1]) for e in evs])) for i in range(nkern)]
+
+
+def measure_config(sv, cfg: int, dev, stream, seed: int, seq_base: int, l2: int, peak: float,
+                   cpu_seconds: float):
+    """One named workload on this GPU: the default sampling call, the early-exit call and
+    (where the workload has one) the greedy call, each as us/call, rows/s, GB/s of one read
+    of the logits and its fraction of the measured HBM bandwidth, with the split between the
+    call's kernels; and the CPU oracle on one core over a bounded sample."""
+    import torch
+    import workloads
+    out = {"workload": workloads.CONFIG_NAMES[cfg]}
+    modes = ["sampling", "early_exit"] + (["greedy"] if cfg in (1, 3, 4) else [])
+    if cfg == 4:
+        modes = ["greedy"]  # the sampling paths of this workload are the line's headline
+    w_s = None
+    for mode in modes:
+        greedy = mode == "greedy"
+        w = workloads.config(cfg, greedy=greedy)
+        if not greedy:
+            w_s = w
+        tb, db, copies = device_copies(w, dev, l2, greedy)
+        tok = torch.from_numpy(w.tokens).to(dev)
+        Tq, Tdq = torch.from_numpy(w.T).to(dev), torch.from_numpy(w.Td).to(dev)
+        kw = dict(T_per_seq=Tq, Td_per_seq=Tdq) if cfg == 3 else {}
+        out_t = torch.empty((w.B, w.gamma + 1), dtype=torch.int32, device=dev)
+        out_n = torch.empty((w.B,), dtype=torch.int32, device=dev)
+        flags = sv.SPEC_FLAG_EARLY_EXIT if mode == "early_exit" else 0
+
+        def call(k, events=None):
+            c = k % copies
+            if greedy:
+                sv.spec_verify_greedy_ex(tb[c], tok, out_t, out_n, prof_events=events)
+            else:
+                sv.spec_verify_ex(tb[c], db[c], tok, float(w.T[0]), float(w.Td[0]), seed, out_t,
+                                  out_n, seq_index_base=seq_base, flags=flags,
+                                  prof_events=events, **kw)
+
+        est = time_calls(call, 20, stream)
+        n = int(max(200, min(20000, 250.0 / max(est, 1e-3))))
+        ms = time_calls(call, n, stream)
+        status = sv.spec_verify_check()
+        nbytes = w.bytes_greedy() if greedy else w.bytes_sampling()
+        entry = {"us_per_call": ms * 1e3, "rows_per_s": w.rows / (ms / 1e3), "calls": n,
+                 "GBps_one_read": nbytes / (ms / 1e3) / 1e9,
+                 "frac_of_measured_hbm": nbytes / (ms / 1e3) / 1e9 / peak,
+                 "inputs": (f"{copies} rotating copies ({copies * nbytes / 1e6:.0f} MB > 2x L2)"
+                            if copies > 1 else "one copy, larger than 2x L2"),
+                 "status": status}
+        if mode == "early_exit":
+            streamed, raced = early_exit_rows_read(out_n.cpu().numpy(), w.gamma)
+            es_ = 2 if w.dtype == "bf16" else 4
+            entry["logit_bytes_read_per_call"] = (streamed + raced) * w.V * es_
+            entry["note"] = ("same outputs; reads rows only up to each sequence's first "
+                             "rejection: GBps_one_read is the full read's bytes over this time")
+        else:
+            names = ["row_argmax", "scan_greedy"] if greedy else ["row_stats", "scan_race"]
+            kms = kernel_split_ms(lambda k, ev: call(k, ev), min(n, 500), 2, stream)
+            entry["kernel_us"] = {nm: v * 1e3 for nm, v in zip(names, kms)}
+            entry["dominant"] = names[0]
+            entry["dominant_frac_of_measured_hbm"] = nbytes / (kms[0] / 1e3) / 1e9 / peak
+        out[mode] = entry
+        del tb, db
+    if w_s is not None and cpu_seconds > 0:
+        rate, nseq, secs = cpu_oracle_rate(w_s, seed, cpu_seconds, max_seqs=w_s.B)
+        out["cpu_oracle"] = {"rows_per_s": rate, "cores": 1,
+                             "sample": f"{nseq} of {w_s.B} sequences, {secs:.2f} s, single-threaded C"}
+    return out
+
+
 def run_ours(args):
     import torch
     import workloads
@@ -248,6 +365,32 @@ def run_ours(args):
     if sampler:
         clocks = ClockSampler.summarise(sampler.stop(), h0, h1)
     ms = start.elapsed_time(end)
+    # Sustained leg: the same step for at least a second (however few steps the timed region
+    # above has), with the clocks sampled inside it.
+    sustained = None
+    if not args.no_sustained:
+        Ks = int(np.ceil(args.sustained_seconds * 1e3 / max(ms / K, 1e-3)))
+        sampler2 = ClockSampler(local) if rank == 0 else None
+        time.sleep(0.15 if sampler2 else 0)
+        if ws_ > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        g0 = time.time()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(Ks):
+            step()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        g1 = time.time()
+        sms = s0.elapsed_time(s1)
+        if ws_ > 1:
+            mt = torch.tensor([sms], device=dev, dtype=torch.float64)
+            torch.distributed.all_reduce(mt, op=torch.distributed.ReduceOp.MAX)
+            sms = float(mt.item())
+        sustained = {"value": ws_ * w.rows * Ks / (sms / 1e3), "unit": UNIT, "steps": Ks,
+                     "seconds": sms / 1e3, "ms_per_step": sms / Ks,
+                     "clocks": ClockSampler.summarise(sampler2.stop(), g0, g1) if sampler2 else None}
     # Roofline pass: the same steps again with events around each kernel (an event between
     # the two kernels turns off the programmatic dependent launch, so these steps are not
     # the timed ones).
@@ -422,6 +565,15 @@ def run_ours(args):
                "sample": f"{nseq} of {w.B} sequences of the same workload "
                          f"({nseq * (w.gamma + 1)} rows, {secs:.1f} s, single-threaded C, fp64)"}
 
+    per_config = None
+    if not args.no_per_config:
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        per_config = {}
+        for c in range(5):
+            per_config[f"cfg{c}"] = measure_config(
+                sv, c, dev, stream, args.seed, seq_base, l2, peaks["hbm_gbs"],
+                args.cpu_seconds_per_config if rank == 0 and not args.no_cpu_baseline else 0.0)
+
     if ws_ > 1:
         torch.distributed.destroy_process_group()
     if rank != 0:
@@ -449,6 +601,8 @@ def run_ours(args):
         "e2e_copy": e2e_copy,
         "early_exit": early,
         "with_position_stats": stats,
+        "sustained": sustained,
+        "per_config": per_config,
         "gpu_launches": nkern * K,
         "clocks": clocks,
     }
@@ -574,7 +728,7 @@ def run_table(args):
             stats_out = {"Hp": torch.empty((w.B, w.gamma + 1), dtype=torch.float32, device=dev),
                          "Hq": torch.empty((w.B, w.gamma), dtype=torch.float32, device=dev),
                          "KL": torch.empty((w.B, w.gamma), dtype=torch.float32, device=dev)}
-            modes = [("greedy", None)] if greedy else [("two-kernel", 0), ("fused", sv.SPEC_FLAG_FUSED),
+            modes = [("greedy", None)] if greedy else [("two-kernel", 0),
                                                         ("early-exit", sv.SPEC_FLAG_EARLY_EXIT),
                                                         ("with H, KL", "stats")]
             for label, dbg in modes:
@@ -655,6 +809,67 @@ def run_table(args):
               file=sys.stderr)
 
 
+def launch_ranks(n: int, argv) -> int:
+    """Run this script as n ranks, one process per GPU (LOCAL_RANK = RANK = 0..n-1, WORLD_SIZE =
+    n, rendezvous on 127.0.0.1), as torchrun would; rank 0 prints the JSON line.  If a rank
+    fails the others are stopped.  Returns the first non-zero exit status, else 0."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    procs = []
+    for r in range(n):
+        env = dict(os.environ, RANK=str(r), LOCAL_RANK=str(r), WORLD_SIZE=str(n),
+                   LOCAL_WORLD_SIZE=str(n), MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+        procs.append(subprocess.Popen([sys.executable, os.path.abspath(__file__), *argv], env=env))
+    rc = 0
+    while procs:
+        for p in list(procs):
+            code = p.poll()
+            if code is None:
+                continue
+            procs.remove(p)
+            if code != 0 and rc == 0:
+                rc = code
+                for q in procs:  # the ranks this launcher started, by their own handles
+                    q.terminate()
+        time.sleep(0.05)
+    return rc
+
+
+def run_dry(args):
+    """CPU only: every rank joins a gloo group, 'times' K steps that sleep (rank + 1) * 10 ms
+    each, and rank 0 prints the line with the maximum over ranks, as the GPU run does."""
+    import torch
+    import torch.distributed as dist
+    import workloads
+    ws_, rank, _ = dist_env()
+    if ws_ > 1:
+        dist.init_process_group("gloo")
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        time.sleep((rank + 1) * 0.01)
+    ms = (time.perf_counter() - t0) * 1e3
+    ranks = [rank]
+    if ws_ > 1:
+        mt = torch.tensor([ms], dtype=torch.float64)
+        dist.all_reduce(mt, op=dist.ReduceOp.MAX)
+        ms = float(mt.item())
+        got = [torch.zeros(1, dtype=torch.int64) for _ in range(ws_)]
+        dist.all_gather(got, torch.tensor([rank], dtype=torch.int64))
+        ranks = sorted(int(g.item()) for g in got)
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+    B, gamma, V, _ = workloads.CONFIG_SHAPES[args.config]
+    rows = B * (gamma + 1)
+    print(json.dumps({"metric": METRIC, "value": ws_ * rows * args.steps / (ms / 1e3), "unit": UNIT,
+                      "n_gpus": ws_, "steps": args.steps, "warmup": args.warmup,
+                      "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+                      "dry_run": True, "ranks": ranks}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -673,10 +888,22 @@ def main():
     ap.add_argument("--lm-steps", type=int, default=10)
     ap.add_argument("--all", action="store_true",
                     help="print a per-workload table (both sampling paths, greedy) to stderr")
+    ap.add_argument("--no-sustained", action="store_true")
+    ap.add_argument("--sustained-seconds", type=float, default=1.2)
+    ap.add_argument("--no-per-config", action="store_true")
+    ap.add_argument("--cpu-seconds-per-config", type=float, default=2.0)
+    ap.add_argument("--dry-run", action="store_true",
+                    help="CPU only: exercise the rank launcher and the max-over-ranks timing on\n"
+                         "gloo without touching a GPU (prints a line marked dry_run)")
     ap.add_argument("--ref-seqs", type=int, default=1,
                     help="sequences per reference step (one throughput-workload sequence is\n"
                          "about 0.04 s of oracle work)")
     args = ap.parse_args()
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(launch_ranks(args.gpus, sys.argv[1:]))
+    if args.dry_run:
+        run_dry(args)
+        return
     if args.lmhead:
         import torch
         import speculative_decoding_verification_31_gb300 as sv

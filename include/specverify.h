@@ -88,7 +88,9 @@ typedef struct {
                                    no initial contents are needed.  Calls sharing one
                                    workspace must not overlap on the device. */
     size_t workspace_bytes;
-    int32_t *d_status;          /* device int32 status word (NULL: the library's own) */
+    int32_t *d_status;          /* device int32 status word (NULL: the library's own, which
+                                   spec_verify_check(stream, NULL) reads on the current
+                                   device) */
     /* Diagnostic outputs (device, NULL = not written), all fp32: */
     float *out_logp_draft;      /* [B, gamma]   ln p_i(d_i) */
     float *out_logq_draft;      /* [B, gamma]   ln q_i(d_i) */
@@ -99,9 +101,10 @@ typedef struct {
                                                 runner-up score (approximate) */
     void *prof_events[4];       /* optional cudaEvent_t: recorded before the first kernel and
                                    after each kernel of the call (sampling: two kernels, three
-                                   with per-position statistics, one with SPEC_FLAG_FUSED or
-                                   SPEC_FLAG_EARLY_EXIT; greedy: two) */
-    uint32_t flags;             /* SPEC_FLAG_* / SPEC_DEBUG_* bits; 0 in normal use */
+                                   with per-position statistics, one with SPEC_FLAG_EARLY_EXIT;
+                                   greedy: two) */
+    uint32_t flags;             /* SPEC_FLAG_* / SPEC_DEBUG_* bits; 0 in normal use; any other
+                                   bit is SPEC_EINVAL */
     /* Per-position statistics ("投机解码的第二本账" (SparseSpec-L), section 3.3: every draft
      * token's entropy feeds two class centres, accepted and rejected, kept as moving
      * averages; "SubSpec: the target model's own low-bit shadow as the draft model" quotes
@@ -121,14 +124,13 @@ typedef struct {
                                    when ctrl_centres is set) */
 } spec_verify_opts;
 
-/* flags bits. */
-#define SPEC_FLAG_FUSED 1u        /* sampling: one persistent cooperative kernel (after a small
-                                     kernel that zeroes its control words) instead of the
-                                     default two kernels; same outputs, bit for bit, but
-                                     slower on GB300 at every size measured */
-#define SPEC_DEBUG_NEVER_READY 2u /* tests only, with SPEC_FLAG_FUSED: the race waits on a flag
-                                     that is never set, give up after their bounded wait and
-                                     report SPEC_ETIMEOUT (outputs are then invalid) */
+/* flags bits (bit 0 is unused). */
+#define SPEC_DEBUG_NEVER_READY 2u /* tests only, with SPEC_FLAG_EARLY_EXIT: no race unit
+                                     publishes its winner, so each sequence's last race unit
+                                     waits for them until its bounded wait (0.5 s) gives up,
+                                     records SPEC_ETIMEOUT and draws from p_j instead (the
+                                     outputs are then invalid).  Exercises the bounded waits
+                                     without faulting or hanging the device. */
 #define SPEC_FLAG_EARLY_EXIT 4u   /* sampling, spec_verify_ex only: read each sequence's rows one
                                      position at a time and stop after its first rejection (the
                                      rows the method discards); one persistent cooperative
@@ -189,6 +191,19 @@ size_t spec_verify_workspace_bytes(int B, int gamma, int V, int dtype);
  * of the current device), reset it to SPEC_OK and return what it held (or SPEC_ECUDA). */
 int spec_verify_check(void *stream, int32_t *d_status);
 
+/*
+ * Diagnostic: Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as
+ * 1, 2, 3", SC'11, section 4) exactly as the verify kernels evaluate it, for testing the
+ * device generator word for word.  counters [n, 4] and out [n, 4] uint32 (16-byte aligned),
+ * keys [n, 2] uint32 (8-byte aligned), all device memory: out[i] = Philox4x32-10 of counter
+ * i under key (keys[i][0], keys[i][1]).  form 0: the plain ten rounds (the acceptance
+ * uniforms' path); form 1: the race's evaluation, which takes counter word 3 as 1 and
+ * precomputes the per-row parts of rounds 1 and 2.  Asynchronous on `stream`; SPEC_EINVAL
+ * for n < 0, another form, NULL or misaligned pointers.
+ */
+int spec_philox4x32_10(const uint32_t *counters, const uint32_t *keys, int64_t n, int form,
+                       uint32_t *out, void *stream);
+
 /* Static English text of a status code. */
 const char *spec_verify_strerror(int status);
 
@@ -210,11 +225,14 @@ const char *spec_verify_strerror(int status);
  * that overlap on the GPU (other streams, other threads) race and give wrong results, so
  * serialise them.  Nothing in the array needs to start at zero: every call writes what it
  * reads.  Device-side errors go to opts->d_status when given; otherwise to a word inside the
- * array that this call clears first and that spec_verify_check cannot read (a bad draft
- * token still shows as n_accepted = -1).  No cudaMalloc, cudaFree or allocating library
- * routine is called.
- * SPEC_FLAG_EARLY_EXIT and the per-position statistics (out_H_p, out_H_q, out_KL,
- * ctrl_centres) are ignored here.
+ * array that this call clears first and that spec_verify_check cannot read: a caller who
+ * needs to see SPEC_EBADTOKEN must pass opts->d_status (a bad draft token also shows as
+ * n_accepted = -1).  This entry point runs the default two-kernel schedule only, whose one
+ * wait (the last race block of a sequence polling the others' winners, bounded) follows
+ * blocks that have already counted their arrival.  No cudaMalloc, cudaFree or allocating
+ * library routine is called.
+ * SPEC_FLAG_EARLY_EXIT, SPEC_DEBUG_NEVER_READY and the per-position statistics (out_H_p,
+ * out_H_q, out_KL, ctrl_centres) are ignored here; other flag bits are SPEC_EINVAL.
  * Returns SPEC_ESCRATCH, without launching anything, when spec_verify_workspace_bytes() of
  * the problem exceeds SPEC_NOALLOC_SCRATCH_BYTES - 256; otherwise as spec_verify_ex.
  */

@@ -15,7 +15,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libspecverify.so")
 SOURCES = ["specverify.cu"]
-DEPS = ["specverify.cu", "kernels.cuh", "flow.cuh", "vocab.cuh", "device_common.cuh", "philox.cuh", "lmhead.cuh"]
+DEPS = ["specverify.cu", "kernels.cuh", "vocab.cuh", "device_common.cuh", "philox.cuh", "lmhead.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -10,10 +10,9 @@
 //               for the residual max(0, p_j - q_j), or target row gamma for the bonus token
 //               -- as an exponential race; the last block of a sequence merges the winners
 //               and writes the token.
-// Other schedules of the same computation: the flow kernel (flow.cuh: one persistent launch
-// whose races overlap the streaming of later sequences), the early-exit kernel (below: reads
-// rows only up to each sequence's first rejection), pair_stats (the streaming pass with
-// per-position entropies and KL), and the token-tree kernels.
+// Other schedules of the same computation: the early-exit kernel (below: reads rows only up
+// to each sequence's first rejection), pair_stats (the streaming pass with per-position
+// entropies and KL), and the token-tree kernels.
 // Greedy mode runs row_argmax (first argmax per (row, piece)) and scan_greedy.
 //
 // Streaming work is split into warp-sized items (one row piece each); each SM's block takes a
@@ -48,19 +47,6 @@ struct RacePart {
     int pad;
 };
 
-// The flow path's workspace region (verify_flow_kernel): every word means "nothing yet" when
-// zero, and the region is zeroed before each call.
-struct FlowRegion {
-    unsigned long long* cursors;  // [0]: row items claimed, [16]: race units claimed (own lines)
-    int* items;                   // [B] row items of sequence b streamed
-    int* ready;                   // [B] 1 once sequence b's scan is published
-    int* tickets;                 // [B] race units of sequence b finished
-    unsigned long long* race;     // [B][units] packed unit winners (score bits | index + 1)
-    float* second;                // [B][units] runner-up scores of the units (diagnostic)
-    SeqInfo* seq;                 // [B] published scans
-    int units;                    // race units per sequence
-};
-
 struct VerifyParams {
     const void* target;         // [B, gamma+1, V]
     const void* draft;          // [B, gamma, V]
@@ -82,7 +68,6 @@ struct VerifyParams {
     int* tickets;               // [B] race arrival counters, zeroed by the scan
     int32_t* status;
     float2* row_stat;           // [B][2*gamma+1] merged (scaled max, log2 sum) per row (early exit)
-    FlowRegion flow;            // the flow path's region (verify_flow_kernel)
     uint32_t debug_flags;       // kDebug* test switches
     // early-exit path (verify_early_kernel): task queue and its counters
     int* task;                  // [task_cap] appended task descriptors (pre-filled kTaskEmpty)
@@ -174,8 +159,8 @@ inline int pick_piece_len(long long rows, int V, int es, long long warps) {
 
 // (m, s) pairs travel as one naturally aligned 64-bit word, so a reader that polls the word
 // sees both halves or neither and the writer needs no memory fence.  The early-exit path
-// pre-fills them with kStatEmpty (two NaN halves); the flow path with zero (a real pair has
-// s >= 1, or m = -FLT_MAX when every logit of the piece is -inf).
+// pre-fills them with kStatEmpty (two NaN halves; a real pair has s >= 1, or m = -FLT_MAX
+// when every logit of the piece is -inf).
 constexpr unsigned long long kStatEmpty = 0xFFFFFFFFFFFFFFFFull;
 
 __device__ __forceinline__ void store_stat(float2* dst, float m, float s) {
@@ -743,7 +728,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) row_argmax_kernel(VerifyPar
 // draft token is not the target row's argmax.
 // ----------------------------------------------------------------------------------------
 
-constexpr uint32_t kDebugNeverReady = 1u;         // published scans never set their flag (tests)
+constexpr uint32_t kDebugNeverReady = 1u;  // early-exit race units never publish their winners (tests)
 constexpr unsigned long long kWaitLimitNs = 500000000ull;  // give up a wait after 0.5 s
 
 __device__ __forceinline__ unsigned long long global_time_ns() {
@@ -806,6 +791,28 @@ __global__ void __launch_bounds__(256) scan_greedy_kernel(VerifyParams p) {
             else if (t == j) v = sm_g[j];
         }
         out[t] = v;
+    }
+}
+
+// ----------------------------------------------------------------------------------------
+// The generator as the verify kernels evaluate it, exposed for testing: form 0 runs the plain
+// ten rounds (the acceptance uniforms' path), form 1 the race's evaluation of counter
+// (c0, c1, c2, 1) with the per-row parts of rounds 1 and 2 precomputed (race_row_rng and
+// race_block_fast, as every race calls them).
+// ----------------------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(256) philox_probe_kernel(const uint4* ctr, const uint2* key, long long n,
+                                                           int form, uint4* out) {
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+        const uint4 c = ctr[i];
+        const PhiloxKey k{key[i].x, key[i].y};
+        if (form == 0) {
+            out[i] = philox4x32_10(c, k);
+        } else {
+            const PhiloxRoundKeys rk = philox_round_keys(k);
+            out[i] = race_block_fast(race_row_rng(rk, c.z, c.y), rk, c.x);
+        }
     }
 }
 
@@ -1325,43 +1332,20 @@ __device__ __forceinline__ void race_sequence_block(const VerifyParams& p, int b
                         cb_end, cb_step, ch_limit, slot, nslots, si, s_thr, s_best, s_last);
 }
 
-// Poll a packed word until it is nonzero; after kWaitLimitNs give up, record SPEC_ETIMEOUT
-// and return 0.
-__device__ __forceinline__ unsigned long long poll_nonzero_u64(const VerifyParams& p,
-                                                               const unsigned long long* w) {
-    unsigned long long v = ld_relaxed_u64g(w);
-    if (v != 0ull) return v;
-    const unsigned long long t0 = global_time_ns();
-    unsigned ns = 32;
-    while ((v = ld_relaxed_u64g(w)) == 0ull) {
-        if (global_time_ns() - t0 > kWaitLimitNs) {
-            set_status(p.status, 4 /* SPEC_ETIMEOUT */);
-            return 0ull;
-        }
-        __nanosleep(ns);
-        if (ns < 256) ns <<= 1;
-    }
-    return v;
-}
-
-// The merged statistics of one row from its P partials (packed (m, s) words), by one thread
-// in a fixed order: eight partials at a time merged as a balanced tree (pairs, pairs of
-// pairs, root), the eight-partial results folded in piece order.  Every schedule merges rows
-// this way, so they all get the same bits.  kPoll: partials are polled until written (the
-// flow path, where they carry no fence); otherwise they are complete (a kernel boundary).
-template <bool kPoll>
-__device__ __forceinline__ SoftmaxStat fold_row_stats(const VerifyParams& p,
-                                                      const unsigned long long* parts, int P) {
+// The merged statistics of one row from its P partials (packed (m, s) words, complete: they
+// were written by an earlier kernel), by one thread in a fixed order: eight partials at a
+// time merged as a balanced tree (pairs, pairs of pairs, root), the eight-partial results
+// folded in piece order, so that every call merges a row's pieces into the same bits.
+__device__ __forceinline__ SoftmaxStat fold_row_stats(const unsigned long long* parts, int P) {
     SoftmaxStat acc{-FLT_MAX, 0.0f};
     for (int k0 = 0; k0 < P; k0 += 8) {
         unsigned long long v[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q)
-            v[q] = (k0 + q < P) ? (kPoll ? ld_relaxed_u64g(parts + k0 + q) : __ldcg(parts + k0 + q)) : 0ull;
+            v[q] = (k0 + q < P) ? __ldcg(parts + k0 + q) : 0ull;
         SoftmaxStat t[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-            if (kPoll && k0 + q < P && v[q] == 0ull) v[q] = poll_nonzero_u64(p, parts + k0 + q);
             t[q] = (k0 + q < P) ? SoftmaxStat{__uint_as_float(static_cast<uint32_t>(v[q])),
                                               __uint_as_float(static_cast<uint32_t>(v[q] >> 32))}
                                 : SoftmaxStat{-FLT_MAX, 0.0f};
@@ -1489,7 +1473,7 @@ __global__ void __launch_bounds__(256, SPECVERIFY_RACE_MINBLOCKS) scan_race_kern
         const unsigned long long* parts =
             reinterpret_cast<const unsigned long long*>(p.stat_parts) + static_cast<long long>(b) * R * p.npieces;
         for (int r = threadIdx.x; r < R; r += blockDim.x) {
-            const SoftmaxStat st = fold_row_stats<false>(p, parts + static_cast<long long>(r) * p.npieces, p.npieces);
+            const SoftmaxStat st = fold_row_stats(parts + static_cast<long long>(r) * p.npieces, p.npieces);
             const float l2s = log2f(st.s);
             sm_m[r] = st.m;
             sm_l[r] = l2s;
@@ -2125,7 +2109,9 @@ __device__ __forceinline__ void early_race_unit(const VerifyParams& p, int b, in
     unsigned long long* parts = p.early_race + static_cast<long long>(b) * p.npieces;
     int t = 0;
     if (lane == 0) {
-        parts[piece] = pack_race(st.best, st.idx);  // never zero: the index field is idx + 1
+        // never zero: the index field is idx + 1.  (kDebugNeverReady, tests only: no unit
+        // publishes its winner, so the last unit's bounded wait below runs out.)
+        if (!(p.debug_flags & kDebugNeverReady)) parts[piece] = pack_race(st.best, st.idx);
         t = atomicAdd(p.race_done + b, 1);
     }
     t = __shfl_sync(0xffffffffu, t, 0);

@@ -12,7 +12,6 @@
 #include <mutex>
 
 #include "kernels.cuh"
-#include "flow.cuh"
 #include "vocab.cuh"
 #include "lmhead.cuh"
 #include "specverify.h"
@@ -37,10 +36,7 @@ struct Layout {
     int piece_len, npieces;
     int rpieces;
     size_t stat_off, ext_off, seq_off, race_off, ticket_off;
-    size_t flow_off, flow_bytes;        // flow path (verify_flow_kernel), zeroed before each call
-    size_t f_cursor_off, f_items_off, f_ready_off, f_tickets_off, f_race_off, f_second_off,
-        f_seq_off, f_stat_off;
-    int f_units;                        // flow race units per sequence
+    size_t tree_off;                    // token-tree verify: the node each sequence races
     int e_n_init, e_task_cap;           // early-exit path (verify_early_kernel)
     size_t e_rowstat_off, e_task_off, e_stat_off, e_zero_off, e_cursor_off, e_tail_off,
         e_finished_off, e_rowarr_off, e_pos_off, e_racedone_off, e_race_off, e_racetask_off,
@@ -68,7 +64,6 @@ Layout layout_of(int B, int gamma, int V, int dtype, long long stream_warps = 0)
     L.stat_off = off;
     off = align_up(off + static_cast<size_t>(B) * R * max_np * sizeof(float2), 256);
     L.ext_off = off;  // per-position statistics: entropy and cross terms per row piece
-    L.f_stat_off = off;  // the flow path's row partials (that path computes no such terms)
     off = align_up(off + static_cast<size_t>(B) * R * max_np * sizeof(float2) + 16, 256);
     L.seq_off = off;
     off = align_up(off + static_cast<size_t>(B) * sizeof(SeqInfo), 256);
@@ -76,26 +71,8 @@ Layout layout_of(int B, int gamma, int V, int dtype, long long stream_warps = 0)
     off = align_up(off + static_cast<size_t>(B) * race_slots(L.rpieces) * sizeof(RacePart), 256);
     L.ticket_off = off;
     off = align_up(off + static_cast<size_t>(B) * sizeof(int), 256);
-    // flow control region: the two cursors on their own 128-byte lines, then per-sequence
-    // counts, flags and tickets, the units' packed winners and runner-up scores, the scans
-    L.flow_off = off;
-    L.f_cursor_off = off;
-    off += 2 * 128;
-    L.f_items_off = off;
-    off += static_cast<size_t>(B) * sizeof(int);
-    L.f_ready_off = off;
-    off += static_cast<size_t>(B) * sizeof(int);
-    L.f_tickets_off = off;
-    off = align_up(off + static_cast<size_t>(B) * sizeof(int), 16);
-    L.f_units = (V + kFlowUnitTokens - 1) / kFlowUnitTokens;
-    L.f_race_off = off;
-    off += static_cast<size_t>(B) * L.f_units * sizeof(unsigned long long);
-    L.f_second_off = off;
-    off = align_up(off + static_cast<size_t>(B) * L.f_units * sizeof(float), 16);
-    L.f_seq_off = off;
-    off = align_up(off + static_cast<size_t>(B) * sizeof(SeqInfo), 256);
-    L.flow_bytes = off - L.flow_off;
-    off = align_up(off, 256);
+    L.tree_off = off;
+    off = align_up(off + static_cast<size_t>(B) * sizeof(TreeRace), 256);
     // early-exit region: a block filled with 0xFF before each call (merged rows, task queue,
     // then the row partials, last so that only the pieces in use need filling), then a
     // zeroed block (counters, then the race winners)
@@ -215,6 +192,8 @@ bool ensure_mirror(DeviceState& d, size_t bytes) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+constexpr uint32_t kKnownFlags = SPEC_DEBUG_NEVER_READY | SPEC_FLAG_EARLY_EXIT | SPEC_FLAG_FULL_READ;
+
 bool good_temperature(float t) { return std::isfinite(t) && t > 0.0f; }
 
 // Launch of a streaming kernel: one block of kStreamThreads per SM (the claiming variant kc,
@@ -274,14 +253,7 @@ void bind_workspace(VerifyParams& p, const Layout& L, char* ws) {
     p.seq = reinterpret_cast<SeqInfo*>(ws + L.seq_off);
     p.race_parts = reinterpret_cast<RacePart*>(ws + L.race_off);
     p.tickets = reinterpret_cast<int*>(ws + L.ticket_off);
-    p.flow.cursors = reinterpret_cast<unsigned long long*>(ws + L.f_cursor_off);
-    p.flow.items = reinterpret_cast<int*>(ws + L.f_items_off);
-    p.flow.ready = reinterpret_cast<int*>(ws + L.f_ready_off);
-    p.flow.tickets = reinterpret_cast<int*>(ws + L.f_tickets_off);
-    p.flow.race = reinterpret_cast<unsigned long long*>(ws + L.f_race_off);
-    p.flow.second = reinterpret_cast<float*>(ws + L.f_second_off);
-    p.flow.seq = reinterpret_cast<SeqInfo*>(ws + L.f_seq_off);
-    p.flow.units = L.f_units;
+    p.tree_race = reinterpret_cast<TreeRace*>(ws + L.tree_off);
 }
 
 // Validated common set-up of a call: fills `p` with the workspace pointers.
@@ -319,65 +291,6 @@ int check_common(const void* target, const int32_t* out_tokens, const int32_t* o
     if (!target || !out_tokens || !out_n) return SPEC_EINVAL;
     if (!aligned16(target)) return SPEC_EINVAL;
     return SPEC_OK;
-}
-
-// Flow sampling verify (SPEC_FLAG_FUSED): flow_prep zeroes the flow region, then the flow
-// kernel runs as one cooperative launch (every block resident: its waits rely on it), started
-// as the prep kernel's programmatic dependent where the device accepts both attributes.
-template <class ET>
-int launch_flow(VerifyParams& p, int sm_count, const spec_verify_opts* o, cudaStream_t s,
-                const Layout& L, char* ws) {
-    auto kernel = verify_flow_kernel<ET, kUnroll>;
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) != cudaSuccess ||
-        per_sm < 1)
-        return SPEC_ECUDA;
-    p.stat_parts = reinterpret_cast<float2*>(ws + L.f_stat_off);
-    // both zeroed ranges are whole 16-byte words inside their regions (256-byte aligned ends)
-    const long long n_ctl = static_cast<long long>(L.flow_bytes / 16);
-    const long long n_stat = static_cast<long long>(
-        (static_cast<size_t>(p.B) * (2 * p.gamma + 1) * p.npieces * sizeof(unsigned long long) + 15) / 16);
-    long long prep_grid = (2 * (n_ctl + n_stat) + kThreads - 1) / kThreads;
-    if (prep_grid > 2LL * sm_count) prep_grid = 2LL * sm_count;
-    record(o, 0, s);
-    {
-        cudaLaunchConfig_t pc = {};
-        pc.gridDim = dim3(static_cast<unsigned>(prep_grid < 1 ? 1 : prep_grid));
-        pc.blockDim = dim3(kThreads);
-        pc.stream = s;
-        cudaLaunchAttribute pa[1];
-        pa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        pa[0].val.programmaticStreamSerializationAllowed = 1;
-        pc.attrs = pa;
-        pc.numAttrs = 1;
-        unsigned long long* ctl = reinterpret_cast<unsigned long long*>(ws + L.flow_off);
-        unsigned long long* stat = reinterpret_cast<unsigned long long*>(ws + L.f_stat_off);
-        if (cudaLaunchKernelEx(&pc, prep_fill_kernel, ctl, 2 * n_ctl, 0ull, stat, 2 * n_stat, 0ull) != cudaSuccess) {
-            (void)cudaGetLastError();  // no programmatic launches: a plain one
-            pc.numAttrs = 0;
-            if (cudaLaunchKernelEx(&pc, prep_fill_kernel, ctl, 2 * n_ctl, 0ull, stat, 2 * n_stat, 0ull) !=
-                cudaSuccess)
-                return SPEC_ECUDA;
-        }
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(sm_count * per_sm));
-    cfg.blockDim = dim3(kThreads);
-    cfg.stream = s;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    if (cudaLaunchKernelEx(&cfg, kernel, p) != cudaSuccess) {
-        (void)cudaGetLastError();  // not accepted together: a plain cooperative launch
-        cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, kernel, p) != cudaSuccess) return SPEC_ECUDA;
-    }
-    record(o, 1, s);
-    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
 }
 
 // Launch with programmatic stream serialization when `pdl`: the kernel may start before the
@@ -695,6 +608,7 @@ int verify_ex_impl(const void* target_logits, const void* draft_logits, const in
         p.ctrl_beta = opts->ctrl_beta;
         if (p.ctrl_centres && !(p.ctrl_beta > 0.0 && p.ctrl_beta <= 1.0)) return SPEC_EINVAL;
     }
+    if (opts && (opts->flags & ~kKnownFlags)) return SPEC_EINVAL;
     p.debug_flags = (opts && (opts->flags & SPEC_DEBUG_NEVER_READY)) ? kDebugNeverReady : 0u;
     DeviceState* d = nullptr;
     char* ws = nullptr;
@@ -717,11 +631,6 @@ int verify_ex_impl(const void* target_logits, const void* draft_logits, const in
         }
         return dtype == SPEC_F32 ? launch_early<F32Elem>(p, d->sm_count, opts, s, L, ws, host_rows)
                                  : launch_early<Bf16Elem>(p, d->sm_count, opts, s, L, ws, host_rows);
-    }
-    const bool fused = d->coop && opts && (opts->flags & SPEC_FLAG_FUSED) && !wants_position_stats(p);
-    if (fused) {
-        return dtype == SPEC_F32 ? launch_flow<F32Elem>(p, d->sm_count, opts, s, L, ws)
-                                 : launch_flow<Bf16Elem>(p, d->sm_count, opts, s, L, ws);
     }
     return dtype == SPEC_F32 ? launch_sampling<F32Elem>(p, d->sm_count, opts, s)
                              : launch_sampling<Bf16Elem>(p, d->sm_count, opts, s);
@@ -772,6 +681,21 @@ int spec_verify_greedy(const void* target_logits, const int32_t* draft_tokens, i
                        int V, int32_t* out_tokens, int32_t* out_n_accepted, void* stream) {
     return spec_verify_greedy_ex(target_logits, draft_tokens, B, gamma, V, out_tokens,
                                  out_n_accepted, nullptr, stream);
+}
+
+int spec_philox4x32_10(const uint32_t* counters, const uint32_t* keys, int64_t n, int form,
+                       uint32_t* out, void* stream) {
+    if (n < 0 || (form != 0 && form != 1)) return SPEC_EINVAL;
+    if (n == 0) return SPEC_OK;
+    if (!counters || !keys || !out || !aligned16(counters) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(keys) & 7u) != 0)
+        return SPEC_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const long long blocks = std::min<long long>((n + kThreads - 1) / kThreads, 1LL << 20);
+    philox_probe_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(
+        reinterpret_cast<const uint4*>(counters), reinterpret_cast<const uint2*>(keys), n, form,
+        reinterpret_cast<uint4*>(out));
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
 }
 
 int spec_verify_check(void* stream, int32_t* d_status) {
@@ -897,10 +821,6 @@ int spec_verify_tree(const void* target_logits, const void* draft_logits, const 
     DeviceState* d = nullptr;
     rc = prepare(B, gamma_eq, V, dtype, opts, p, &d);
     if (rc) return rc;
-    // the per-sequence race records live in the flow path's scan area (B SeqInfo of 32 bytes
-    // >= B TreeRace of 16), which the tree path does not otherwise use
-    static_assert(sizeof(TreeRace) <= sizeof(SeqInfo), "the scan area holds the race records");
-    p.tree_race = reinterpret_cast<TreeRace*>(p.flow.seq);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return dtype == SPEC_F32 ? launch_tree<F32Elem>(p, t, d->sm_count, opts, s)
                              : launch_tree<Bf16Elem>(p, t, d->sm_count, opts, s);
@@ -1533,6 +1453,7 @@ extern "C" int spec_verify_noalloc(const void* target_logits, const void* draft_
     int rc = check_common(target_logits, out_tokens, out_n_accepted, B, gamma, V, dtype);
     if (rc || B == 0) return rc;
     if (opts && opts->workspace) return SPEC_EINVAL;
+    if (opts && (opts->flags & ~kKnownFlags)) return SPEC_EINVAL;
     if (gamma > 0 && (!draft_logits || !draft_tokens || !aligned16(draft_logits))) return SPEC_EINVAL;
     if (!(opts && opts->T_per_seq) && !good_temperature(T)) return SPEC_EINVAL;
     if (!(opts && opts->Td_per_seq) && !good_temperature(T_d)) return SPEC_EINVAL;
@@ -1569,16 +1490,12 @@ extern "C" int spec_verify_noalloc(const void* target_logits, const void* draft_
     }
     char* ws = nd->scratch;
     bind_workspace(p, L, ws);
-    p.debug_flags = (opts && (opts->flags & SPEC_DEBUG_NEVER_READY)) ? kDebugNeverReady : 0u;
     if (opts && opts->d_status) {
         p.status = opts->d_status;
     } else {
         p.status = reinterpret_cast<int32_t*>(ws + kNoallocStatusOff);
         if (cudaMemsetAsync(p.status, 0, sizeof(int32_t), s) != cudaSuccess) return SPEC_ECUDA;
     }
-    if (nd->coop && opts && (opts->flags & SPEC_FLAG_FUSED))
-        return dtype == SPEC_F32 ? launch_flow<F32Elem>(p, nd->sm_count, opts, s, L, ws)
-                                 : launch_flow<Bf16Elem>(p, nd->sm_count, opts, s, L, ws);
     return dtype == SPEC_F32 ? launch_sampling<F32Elem>(p, nd->sm_count, opts, s)
                              : launch_sampling<Bf16Elem>(p, nd->sm_count, opts, s);
 }

@@ -20,9 +20,133 @@
 // one-GPU verify except where the two merge orders round a near-tie differently.
 #pragma once
 
-#include "flow.cuh"
+#include "kernels.cuh"
 
 namespace specverify {
+
+// Exponential race over tokens [xa, xb) of one raced row by one warp.  The span is read in
+// chunks of kRaceWarpTokens (the next chunk's vectors are loaded while the current one is
+// scored); Philox blocks are computed kRaceChains at a time per lane; the threshold is seeded
+// from each lane's largest logit (a fast lower bound of its score) and raised to the warp's
+// best exact score after every group, and a token is scored exactly only if it passes the
+// bound test (see kRaceBoundMargin2).  Each lane offers its tokens in increasing x, so the
+// result is the same winner, bit for bit, as any other split of the row.  rt and rd hold
+// tokens xoff, xoff + 1, ... of the row (a vocabulary shard; xoff a multiple of 8): random
+// numbers and the winner's index are those of token x + xoff.
+template <class ET>
+__device__ __forceinline__ RaceState race_warp_span(const VerifyParams& p,
+                                                   const typename ET::storage* rt,
+                                                   const typename ET::storage* rd, bool residual,
+                                                   uint32_t bg, uint32_t pos, int xa, int xb,
+                                                   const SeqInfo& si, int lane, int xoff = 0) {
+    constexpr int VPL = kRaceWarpTokens / (32 * ET::kVec);
+    const RaceRowRng q = race_row_rng(p.rk, bg, pos);
+    RaceState st{-INFINITY, INT_MAX, -INFINITY};
+    auto word_at = [&](int x) {
+        const uint4 blk = race_block_fast(q, p.rk, static_cast<uint32_t>(x + xoff) >> 2);
+        return word_of(blk, static_cast<uint32_t>(x + xoff) & 3u);
+    };
+    auto offer_exact = [&](float xt, int x, uint32_t w) {
+        const float xd = residual ? ET::load1(rd + x) : 0.0f;
+        const float sc = race_exact_score(xt, xd, si, residual, w);
+        if (sc > -INFINITY) race_offer(st, sc, x + xoff);
+    };
+    auto load_chunk = [&](int x0, uint4 (&dst)[VPL]) {
+        const int x1 = min(xb, x0 + kRaceWarpTokens);
+        if (residual) prefetch_l2(rd, x0, x1, lane);
+        const bool ok = x0 < x1 && (reinterpret_cast<uintptr_t>(rt + x0) & 15u) == 0;
+        const int nv = ok ? (x1 - x0) / ET::kVec : 0;
+        const uint4* vt = reinterpret_cast<const uint4*>(rt + (ok ? x0 : 0));
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) {
+            const int v = lane + 32 * k;
+            dst[k] = v < nv ? __ldg(vt + v) : make_uint4(ET::kNegInfWord, ET::kNegInfWord,
+                                                         ET::kNegInfWord, ET::kNegInfWord);
+        }
+    };
+    uint4 raw[VPL], raw_next[VPL];
+    load_chunk(xa, raw);
+    float thr = -INFINITY;
+    bool first = true;
+    for (int x0 = xa; x0 < xb; x0 += kRaceWarpTokens) {
+        const int x1 = min(xb, x0 + kRaceWarpTokens);
+        const bool vec_ok = (reinterpret_cast<uintptr_t>(rt + x0) & 15u) == 0;
+        const int nvec = vec_ok ? (x1 - x0) / ET::kVec : 0;
+        const bool more = x0 + kRaceWarpTokens < xb;
+        if (more) load_chunk(x0 + kRaceWarpTokens, raw_next);
+        if (first) {
+            float seed = -INFINITY;
+            if (vec_ok) {
+                float vmax = -INFINITY;
+                int xs = -1;
+#pragma unroll
+                for (int k = 0; k < VPL; ++k) {
+                    float ft[ET::kVec];
+                    ET::widen(raw[k], ft);
+                    float m = ft[0];
+#pragma unroll
+                    for (int e = 1; e < ET::kVec; ++e) m = fmaxf(m, ft[e]);
+                    if (m > vmax) {
+                        vmax = m;
+#pragma unroll
+                        for (int e = ET::kVec - 1; e >= 0; --e)
+                            if (ft[e] == m) xs = x0 + (lane + 32 * k) * ET::kVec + e;
+                    }
+                }
+                if (xs >= 0) {
+                    const float xd = residual ? ET::load1(rd + xs) : 0.0f;
+                    seed = race_score_lower_bound(vmax, xd, si, residual, word_at(xs));
+                }
+            }
+            thr = float_unorder(__reduce_max_sync(0xffffffffu, float_order(seed)));
+            first = false;
+        }
+        if (vec_ok) {
+            const float mpl = si.mp + si.l2sp;
+            constexpr int BPV = ET::kVec / 4;  // Philox blocks per 16-byte vector
+            constexpr int VG = kRaceChains / BPV;
+            static_assert(VPL % VG == 0, "race vectors per lane must fill whole groups");
+#pragma unroll
+            for (int k0 = 0; k0 < VPL; k0 += VG) {
+                const float C = (thr > -INFINITY) ? 32.0f + kRaceBoundMargin2 - thr * kLog2e - mpl
+                                                  : INFINITY;
+                uint4 blk[VG * BPV];
+#pragma unroll
+                for (int kk = 0; kk < VG; ++kk)
+#pragma unroll
+                    for (int gg = 0; gg < BPV; ++gg)
+                        blk[kk * BPV + gg] = race_block_fast(
+                            q, p.rk,
+                            static_cast<uint32_t>(xoff + x0 + (lane + 32 * (k0 + kk)) * ET::kVec + 4 * gg) >> 2);
+#pragma unroll
+                for (int kk = 0; kk < VG; ++kk) {
+                    const int v = lane + 32 * (k0 + kk);
+                    if (v >= nvec) continue;
+                    float ft[ET::kVec];
+                    ET::widen(raw[k0 + kk], ft);
+                    const int xv = x0 + v * ET::kVec;
+                    uint32_t cand = vector_candidates<ET>(ft, blk + kk * BPV, si.cp, C);
+                    while (cand) {  // rare: exact scores in increasing token order
+                        const int e = __ffs(cand) - 1;
+                        cand &= cand - 1;
+                        offer_exact(ET::load1(rt + xv + e), xv + e, word_at(xv + e));
+                    }
+                }
+                thr = fmaxf(thr, float_unorder(__reduce_max_sync(0xffffffffu, float_order(st.best))));
+            }
+            const int t0 = nvec * ET::kVec;
+            if (lane < (x1 - x0) - t0)
+                offer_exact(ET::load1(rt + x0 + t0 + lane), x0 + t0 + lane, word_at(x0 + t0 + lane));
+        } else {
+            for (int x = x0 + lane; x < x1; x += 32) offer_exact(ET::load1(rt + x), x, word_at(x));
+        }
+        if (more) {
+#pragma unroll
+            for (int k = 0; k < VPL; ++k) raw[k] = raw_next[k];
+        }
+    }
+    return warp_race_merge(st);
+}
 
 // Per-sequence state between vp_decide and vp_race / vp_finish (opaque to callers).
 struct VpState {
@@ -51,8 +175,8 @@ __global__ void __launch_bounds__(256) vp_fold_kernel(VerifyParams p, float2* ou
     const long long rows = static_cast<long long>(p.B) * R;
     for (long long r = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; r < rows;
          r += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const SoftmaxStat st = fold_row_stats<false>(
-            p, reinterpret_cast<const unsigned long long*>(p.stat_parts) + r * p.npieces, p.npieces);
+        const SoftmaxStat st = fold_row_stats(
+            reinterpret_cast<const unsigned long long*>(p.stat_parts) + r * p.npieces, p.npieces);
         out[r] = make_float2(st.m, st.s);
     }
 }

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libspecverify.so")
 SPEC_OK, SPEC_EINVAL, SPEC_ECUDA, SPEC_EBADTOKEN, SPEC_ETIMEOUT, SPEC_ENOMEM = range(6)
 SPEC_ESCRATCH = 6
 SPEC_NOALLOC_SCRATCH_BYTES = 8 << 20
-SPEC_FLAG_FUSED, SPEC_DEBUG_NEVER_READY, SPEC_FLAG_EARLY_EXIT, SPEC_FLAG_FULL_READ = 1, 2, 4, 8
+SPEC_DEBUG_NEVER_READY, SPEC_FLAG_EARLY_EXIT, SPEC_FLAG_FULL_READ = 2, 4, 8
 SPEC_F32, SPEC_BF16 = 0, 1
 
 EXPORTED = ("spec_verify", "spec_verify_greedy", "spec_verify_ex", "spec_verify_greedy_ex",
@@ -27,7 +27,8 @@ EXPORTED = ("spec_verify", "spec_verify_greedy", "spec_verify_ex", "spec_verify_
             "spec_verify_opts_init", "spec_verify_noalloc", "spec_row_entropy",
             "spec_adaptive_k", "spec_verify_tree", "spec_verify_host", "spec_lmhead_logits",
             "spec_lmhead_row_stats", "spec_verify_lmhead", "spec_vp_state_bytes",
-            "spec_vp_partials", "spec_vp_decide", "spec_vp_race", "spec_vp_finish")
+            "spec_vp_partials", "spec_vp_decide", "spec_vp_race", "spec_vp_finish",
+            "spec_philox4x32_10")
 
 
 class SpecVerifyError(RuntimeError):
@@ -115,8 +116,19 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.spec_vp_finish.argtypes = [P, P, I, I, P, P]
     for f in ("spec_vp_partials", "spec_vp_decide", "spec_vp_race", "spec_vp_finish"):
         getattr(lib, f).restype = ctypes.c_int
+    lib.spec_philox4x32_10.argtypes = [P, P, ctypes.c_int64, I, P, P]
+    lib.spec_philox4x32_10.restype = ctypes.c_int
     _lib = lib
     return lib
+
+
+def _call(device, name: str, *args) -> int:
+    """Call entry point `name` with `device` current: the library finds its per-device state
+    (workspace, status word, SM count) through the current device, which must be the device
+    of the tensors and of the stream the call is given."""
+    lib = load_library()
+    with torch.cuda.device(device):
+        return getattr(lib, name)(*args)
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -173,7 +185,7 @@ def spec_verify(target_logits, draft_logits, draft_tokens, T: float, T_d: float,
     if target_logits.dtype != torch.bfloat16:
         raise TypeError("spec_verify takes bf16 logits; use spec_verify_ex for float32")
     out_tokens, out_n_accepted = _outputs(target_logits, B, g, out_tokens, out_n_accepted)
-    rc = load_library().spec_verify(
+    rc = _call(target_logits.device, "spec_verify",
         _ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), B, g, V, T, T_d,
         int(seed) & (2**64 - 1), _ptr(out_tokens), _ptr(out_n_accepted),
         _stream_handle(stream, target_logits.device))
@@ -189,7 +201,7 @@ def spec_verify_greedy(target_logits, draft_tokens, out_tokens=None, out_n_accep
     if target_logits.dtype != torch.bfloat16:
         raise TypeError("spec_verify_greedy takes bf16 logits; use spec_verify_greedy_ex")
     out_tokens, out_n_accepted = _outputs(target_logits, B, g, out_tokens, out_n_accepted)
-    rc = load_library().spec_verify_greedy(
+    rc = _call(target_logits.device, "spec_verify_greedy",
         _ptr(target_logits), _ptr(draft_tokens), B, g, V, _ptr(out_tokens),
         _ptr(out_n_accepted), _stream_handle(stream, target_logits.device))
     if rc != SPEC_OK:
@@ -283,7 +295,7 @@ def spec_verify_ex(target_logits, draft_logits, draft_tokens, T: float, T_d: flo
             raise ValueError(f"ctrl_centres must be a contiguous float64 [B, 2] tensor on {dev}")
         o.ctrl_centres = ctrl_centres.data_ptr()
         o.ctrl_beta = float(ctrl_beta)
-    rc = load_library().spec_verify_ex(
+    rc = _call(dev, "spec_verify_ex",
         _ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), B, g, V, float(T),
         float(T_d), int(seed) & (2**64 - 1), _ptr(out_tokens), _ptr(out_n_accepted),
         ctypes.byref(o), _stream_handle(stream, dev))
@@ -299,7 +311,7 @@ def spec_verify_greedy_ex(target_logits, draft_tokens, out_tokens=None, out_n_ac
     out_tokens, out_n_accepted = _outputs(target_logits, B, g, out_tokens, out_n_accepted)
     o = _make_opts(_dtype_code(target_logits), None, None, 0, workspace, d_status, None,
                    prof_events)
-    rc = load_library().spec_verify_greedy_ex(
+    rc = _call(dev, "spec_verify_greedy_ex",
         _ptr(target_logits), _ptr(draft_tokens), B, g, V, _ptr(out_tokens), _ptr(out_n_accepted),
         ctypes.byref(o), _stream_handle(stream, dev))
     if rc != SPEC_OK:
@@ -323,7 +335,7 @@ def spec_verify_noalloc(target_logits, draft_logits, draft_tokens, T: float, T_d
     Td_per_seq = _check_temps(Td_per_seq, B, dev, "Td_per_seq")
     o = _make_opts(_dtype_code(target_logits), T_per_seq, Td_per_seq, seq_index_base, None,
                    d_status, diag, None, flags)
-    rc = load_library().spec_verify_noalloc(
+    rc = _call(dev, "spec_verify_noalloc",
         _ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), B, g, V, float(T),
         float(T_d), int(seed) & (2**64 - 1), _ptr(out_tokens), _ptr(out_n_accepted),
         ctypes.byref(o), _stream_handle(stream, dev))
@@ -353,7 +365,7 @@ def spec_verify_host(target_logits, draft_logits, draft_tokens, T: float, T_d: f
                    None, None, None, SPEC_FLAG_FULL_READ if full_read else 0)
     if g == 0:  # nothing to read: no draft rows or tokens
         draft_logits = draft_tokens = None
-    rc = load_library().spec_verify_host(
+    rc = _call(dev, "spec_verify_host",
         _ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), B, g, V, float(T),
         float(T_d), int(seed) & (2**64 - 1), _ptr(out_tokens), _ptr(out_n_accepted),
         ctypes.byref(o), _stream_handle(stream, dev))
@@ -376,7 +388,7 @@ def spec_lmhead_logits(hidden, weight, out_logits=None, stream=None):
     rows, V, d = _check_lmhead(hidden, weight)
     if out_logits is None:
         out_logits = torch.empty((rows, V), dtype=torch.float32, device=hidden.device)
-    rc = load_library().spec_lmhead_logits(_ptr(hidden), _ptr(weight), rows, V, d, _ptr(out_logits),
+    rc = _call(hidden.device, "spec_lmhead_logits", _ptr(hidden), _ptr(weight), rows, V, d, _ptr(out_logits),
                                            _stream_handle(stream, hidden.device))
     if rc != SPEC_OK:
         raise SpecVerifyError(rc, "spec_lmhead_logits")
@@ -390,7 +402,7 @@ def spec_lmhead_row_stats(hidden, weight, T_row, token_row=None, stream=None):
     dev = hidden.device
     logz = torch.empty((rows,), dtype=torch.float32, device=dev)
     logp = torch.empty((rows,), dtype=torch.float32, device=dev) if token_row is not None else None
-    rc = load_library().spec_lmhead_row_stats(_ptr(hidden), _ptr(weight), rows, V, d, _ptr(T_row),
+    rc = _call(dev, "spec_lmhead_row_stats", _ptr(hidden), _ptr(weight), rows, V, d, _ptr(T_row),
                                               _ptr(token_row), _ptr(logz), _ptr(logp),
                                               _stream_handle(stream, dev))
     if rc != SPEC_OK:
@@ -419,7 +431,7 @@ def spec_verify_lmhead(h_target, w_target, h_draft, w_draft, draft_tokens, T: fl
     T_per_seq = _check_temps(T_per_seq, B, dev, "T_per_seq")
     Td_per_seq = _check_temps(Td_per_seq, B, dev, "Td_per_seq")
     o = _make_opts(SPEC_BF16, T_per_seq, Td_per_seq, seq_index_base, None, None, None, prof_events)
-    rc = load_library().spec_verify_lmhead(
+    rc = _call(dev, "spec_verify_lmhead",
         _ptr(h_target), _ptr(w_target), _ptr(h_draft) if g else None, _ptr(w_draft) if g else None,
         _ptr(draft_tokens) if g else None, B, g, V, d, float(T), float(T_d), int(seed) & (2**64 - 1),
         _ptr(out_tokens), _ptr(out_n_accepted), ctypes.byref(o), _stream_handle(stream, dev))
@@ -478,7 +490,7 @@ def spec_verify_tree(target_logits, draft_logits, draft_tokens, tree, T: float, 
     Td_per_seq = _check_temps(Td_per_seq, B, dev, "Td_per_seq")
     o = _make_opts(_dtype_code(target_logits), T_per_seq, Td_per_seq, seq_index_base, workspace,
                    d_status, None, prof_events)
-    rc = load_library().spec_verify_tree(
+    rc = _call(dev, "spec_verify_tree",
         _ptr(target_logits), _ptr(draft_logits) if (M or not tree.valid) else None,
         _ptr(draft_tokens), tree.c_parent, B, N, V, float(T), float(T_d), int(seed) & (2**64 - 1),
         _ptr(out_tokens), _ptr(out_nodes), _ptr(out_n_accepted), ctypes.byref(o),
@@ -496,7 +508,7 @@ def spec_row_entropy(logits, T: float, out_H=None, stream=None):
     rows, V = logits.shape
     if out_H is None:
         out_H = torch.empty((rows,), dtype=torch.float32, device=logits.device)
-    rc = load_library().spec_row_entropy(_ptr(logits), rows, V, float(T), _dtype_code(logits),
+    rc = _call(logits.device, "spec_row_entropy", _ptr(logits), rows, V, float(T), _dtype_code(logits),
                                          _ptr(out_H), _stream_handle(stream, logits.device))
     if rc != SPEC_OK:
         raise SpecVerifyError(rc, "spec_row_entropy")
@@ -519,12 +531,30 @@ def spec_adaptive_k(H_next, centres, candidates: Sequence[int], C_d: float, C_v:
         out_k = torch.empty((B,), dtype=torch.int32, device=dev)
     if out_eff is None:
         out_eff = torch.empty((B,), dtype=torch.float64, device=dev)
-    rc = load_library().spec_adaptive_k(_ptr(H_next), B, K, _ptr(centres), cand, len(candidates),
+    rc = _call(dev, "spec_adaptive_k", _ptr(H_next), B, K, _ptr(centres), cand, len(candidates),
                                         float(C_d), float(C_v), _ptr(out_k), _ptr(out_eff),
                                         _stream_handle(stream, dev))
     if rc != SPEC_OK:
         raise SpecVerifyError(rc, "spec_adaptive_k")
     return out_k, out_eff
+
+
+def spec_philox4x32_10(counters, keys, form: int = 0, out=None, stream=None):
+    """Diagnostic: the device Philox4x32-10 of counters [n, 4] under keys [n, 2] (int32 CUDA
+    tensors holding the uint32 bits), as the verify kernels evaluate it (form 0: plain; form
+    1: the race's evaluation, counter word 3 taken as 1).  Returns out [n, 4] (int32 bits)."""
+    n = counters.shape[0]
+    for name, t, cols in (("counters", counters, 4), ("keys", keys, 2)):
+        if tuple(t.shape) != (n, cols) or t.dtype != torch.int32 or not t.is_cuda \
+                or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous int32 CUDA tensor [n, {cols}]")
+    if out is None:
+        out = torch.empty((n, 4), dtype=torch.int32, device=counters.device)
+    rc = _call(counters.device, "spec_philox4x32_10", _ptr(counters), _ptr(keys), n, int(form), _ptr(out),
+                                           _stream_handle(stream, counters.device))
+    if rc != SPEC_OK:
+        raise SpecVerifyError(rc, "spec_philox4x32_10")
+    return out
 
 
 def spec_verify_workspace_bytes(B: int, gamma: int, V: int, dtype: int = SPEC_BF16) -> int:
@@ -533,7 +563,11 @@ def spec_verify_workspace_bytes(B: int, gamma: int, V: int, dtype: int = SPEC_BF
 
 def spec_verify_check(stream=None, d_status=None, device=None) -> int:
     """Synchronise the stream and return (and clear) the device status word."""
-    return int(load_library().spec_verify_check(_stream_handle(stream, device), _ptr(d_status)))
+    if device is None and d_status is not None:
+        device = d_status.device
+    if device is None:
+        return int(load_library().spec_verify_check(_stream_handle(stream, device), _ptr(d_status)))
+    return int(_call(device, "spec_verify_check", _stream_handle(stream, device), _ptr(d_status)))
 
 
 def spec_verify_strerror(code: int) -> str:

@@ -22,7 +22,7 @@ import ctypes
 import torch
 import torch.distributed as dist
 
-from .specverify import (SpecVerifyError, SPEC_OK, _check_temps, _dtype_code, _make_opts, _ptr,
+from .specverify import (SpecVerifyError, SPEC_OK, _call, _check_temps, _dtype_code, _make_opts, _ptr,
                          _stream_handle, load_library)
 
 
@@ -68,7 +68,7 @@ def spec_vp_partials(target_shard, draft_shard, draft_tokens, x_offset: int, T: 
     Td_per_seq = _check_temps(Td_per_seq, B, dev, "Td_per_seq")
     o = _make_opts(_dtype_code(target_shard), T_per_seq, Td_per_seq, seq_index_base, workspace,
                    d_status, None, None)
-    rc = load_library().spec_vp_partials(
+    rc = _call(dev, "spec_vp_partials",
         _ptr(target_shard), _ptr(draft_shard) if g else None, _ptr(draft_tokens) if g else None,
         B, g, Vs, int(x_offset), float(T), float(T_d), _ptr(stats), _ptr(gathered) if g else None,
         ctypes.byref(o), _stream_handle(stream, dev))
@@ -94,7 +94,7 @@ def spec_vp_decide(stats_all, gathered, draft_tokens, V: int, T: float, T_d: flo
     T_per_seq = _check_temps(T_per_seq, B, dev, "T_per_seq")
     Td_per_seq = _check_temps(Td_per_seq, B, dev, "Td_per_seq")
     o = _make_opts(dtype_code, T_per_seq, Td_per_seq, seq_index_base, None, d_status, None, None)
-    rc = lib.spec_vp_decide(_ptr(stats_all), W, _ptr(gathered) if g else None,
+    rc = _call(dev, "spec_vp_decide", _ptr(stats_all), W, _ptr(gathered) if g else None,
                             _ptr(draft_tokens) if g else None, B, g, int(V), float(T), float(T_d),
                             int(seed) & (2**64 - 1), _ptr(out_t), _ptr(out_n), _ptr(state),
                             ctypes.byref(o), _stream_handle(stream, dev))
@@ -110,7 +110,7 @@ def spec_vp_race(target_shard, draft_shard, x_offset: int, seed: int, state, *,
     dev = target_shard.device
     keys = torch.empty((B, 2), dtype=torch.int64, device=dev)
     o = _make_opts(_dtype_code(target_shard), None, None, seq_index_base, None, d_status, None, None)
-    rc = load_library().spec_vp_race(_ptr(target_shard), _ptr(draft_shard) if g else None, B, g, Vs,
+    rc = _call(dev, "spec_vp_race", _ptr(target_shard), _ptr(draft_shard) if g else None, B, g, Vs,
                                      int(x_offset), int(seed) & (2**64 - 1), _ptr(state), _ptr(keys),
                                      ctypes.byref(o), _stream_handle(stream, dev))
     if rc != SPEC_OK:
@@ -121,7 +121,7 @@ def spec_vp_race(target_shard, draft_shard, x_offset: int, seed: int, state, *,
 def spec_vp_finish(keys, state, out_tokens, stream=None):
     """Write the drawn tokens (from the max-reduced keys) into out_tokens [B, gamma+1]."""
     B, g1 = out_tokens.shape
-    rc = load_library().spec_vp_finish(_ptr(keys), _ptr(state), B, g1 - 1, _ptr(out_tokens),
+    rc = _call(out_tokens.device, "spec_vp_finish", _ptr(keys), _ptr(state), B, g1 - 1, _ptr(out_tokens),
                                        _stream_handle(stream, out_tokens.device))
     if rc != SPEC_OK:
         raise SpecVerifyError(rc, "spec_vp_finish")
@@ -162,6 +162,29 @@ class VocabShard:
         self.seq_index_base = int(seq_index_base)
 
 
+def _host_staged(group) -> bool:
+    """Whether the group's collectives take host tensors (gloo): the exchanged statistics
+    and keys (O(B gamma) bytes) then travel through host memory."""
+    return dist.get_backend(group) == "gloo"
+
+
+def _all_gather(t, world, group, staged):
+    src = t.cpu() if staged else t.contiguous()
+    parts = [torch.empty_like(src) for _ in range(world)]
+    dist.all_gather(parts, src, group=group)
+    return torch.stack(parts).to(t.device)
+
+
+def _all_reduce_max(t, group, staged):
+    if not staged:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+        return t
+    h = t.cpu()
+    dist.all_reduce(h, op=dist.ReduceOp.MAX, group=group)
+    t.copy_(h)
+    return t
+
+
 def verify_vocab_parallel(shard: VocabShard, seed: int, group=None, backend=None):
     """One sampling verify with the vocabulary split over the ranks of `group` (every rank
     calls this with its own shard; without an initialised process group, one rank holding the
@@ -171,17 +194,16 @@ def verify_vocab_parallel(shard: VocabShard, seed: int, group=None, backend=None
     distributed = dist.is_available() and dist.is_initialized()
     world = dist.get_world_size(group) if distributed else 1
     stats, gathered = backend.partials(shard)
+    staged = world > 1 and stats.is_cuda and _host_staged(group)
     if world > 1:
-        parts = [torch.empty_like(stats) for _ in range(world)]
-        dist.all_gather(parts, stats.contiguous(), group=group)
-        stats_all = torch.stack(parts)
+        stats_all = _all_gather(stats, world, group, staged)
         if gathered.numel():
-            dist.all_reduce(gathered, op=dist.ReduceOp.MAX, group=group)
+            _all_reduce_max(gathered, group, staged)
     else:
         stats_all = stats.unsqueeze(0)
     tokens, n, state = backend.decide(stats_all.contiguous(), gathered, shard, seed)
     keys = backend.race(shard, state, seed)
     if world > 1:
-        dist.all_reduce(keys, op=dist.ReduceOp.MAX, group=group)
+        _all_reduce_max(keys, group, staged)
     backend.finish(keys, state, tokens)
     return tokens, n

@@ -6,7 +6,8 @@ random-number contract):
   * greedy mode: tokens and accepted counts bit-exact;
   * sampling mode: tokens and accepted counts bit-exact, except sequences the oracle flags
     as near-ties (|u - p/q| < 1e-5 at a tested position, or top-two race scores within
-    1e-6 relative); flagged decisions must stay under 1e-4 of all decisions;
+    1e-6); flagged decisions (positions and races) must stay under 1e-4 of all decisions
+    compared in the session (tests/test_zy_near_tie_budget.py);
   * p(d_i) and q(d_i) within 1e-5 relative; u_i bit-exact; ln Z within 1e-6 relative.
 """
 from __future__ import annotations
@@ -19,8 +20,34 @@ import workloads
 
 NEAR_TIE = oracle.FLAG_ACCEPT_NEAR_TIE | oracle.FLAG_RACE_NEAR_TIE | oracle.FLAG_RESIDUAL_EMPTY
 
-# running totals over the session: decisions compared and decisions flagged
+# The accept-test band: a tested position whose |u - p/q| is below this is a near-tie.
+ACCEPT_BAND = 1e-5
+
+# Running totals over the session (every module that compares sampling results with the
+# oracle adds to them): decisions compared (each tested position and each race), decisions
+# flagged as near-ties, sequences, and flagged sequences whose outputs differed.
 TOTALS = {"decisions": 0, "flagged": 0, "sequences": 0, "mismatch_flagged": 0}
+
+
+def decision_counts(r: "oracle.OracleResult", gamma: int):
+    """(decisions, flagged decisions) of oracle results `r`: the tested positions of each
+    sequence (0..min(j, gamma - 1) for first rejection j) and its race; a tested position is
+    flagged when |u - p/q| < ACCEPT_BAND, a race when the oracle flags its top two scores as
+    within 1e-6 (or its residual as empty).  Sequences with a bad draft token decide
+    nothing."""
+    bad = (r.flags & oracle.FLAG_BAD_TOKEN) != 0
+    n = np.where(bad, -1, r.n_accepted)
+    tested = np.minimum(n + 1, gamma)                      # positions whose test ran
+    decisions = int(np.sum(np.where(bad, 0, tested + 1)))
+    flagged = 0
+    if gamma:
+        pos = np.arange(gamma)[None, :]
+        mask = (pos < tested[:, None]) & ~bad[:, None]
+        near = np.abs(r.u - r.a) < ACCEPT_BAND
+        flagged += int(np.sum(mask & near))
+    race_flag = (r.flags & (oracle.FLAG_RACE_NEAR_TIE | oracle.FLAG_RESIDUAL_EMPTY)) != 0
+    flagged += int(np.sum(race_flag & ~bad))
+    return decisions, flagged
 
 
 def to_device(a: np.ndarray, dtype: str, dev) -> torch.Tensor:
@@ -57,18 +84,20 @@ def run_gpu(sv, dw: DeviceWorkload, seed: int, per_seq_temps: bool = True, seq_i
 
 
 def compare_sampling(w: workloads.Workload, g: dict, r: "oracle.OracleResult",
-                     check_values: bool = True, idx=None):
+                     check_values: bool = True, idx=None, count: bool = True):
     """Assert parity of GPU results `g` with oracle results `r` (same sequences).
-    `idx` selects GPU rows when the oracle ran on a subset."""
+    `idx` selects GPU rows when the oracle ran on a subset.  `count` adds the comparison's
+    decisions to TOTALS (False when the same oracle result is compared a second time)."""
     if idx is not None:
         g = {k: v[idx] for k, v in g.items()}
     B, gamma = w.B if idx is None else len(idx), w.gamma
     flagged = (r.flags & NEAR_TIE) != 0
     bad = (r.flags & oracle.FLAG_BAD_TOKEN) != 0
-    decisions = int(np.sum(np.where(bad, 0, np.minimum(r.n_accepted + 1, gamma) + 1)))
-    TOTALS["decisions"] += decisions
-    TOTALS["flagged"] += int(flagged.sum())
-    TOTALS["sequences"] += B
+    if count:
+        decisions, flagged_decisions = decision_counts(r, gamma)
+        TOTALS["decisions"] += decisions
+        TOTALS["flagged"] += flagged_decisions
+        TOTALS["sequences"] += B
     for b in range(B):
         if flagged[b]:
             TOTALS["mismatch_flagged"] += int(g["n"][b] != r.n_accepted[b] or

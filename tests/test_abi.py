@@ -36,7 +36,8 @@ def test_header_declares_the_boundary():
               "spec_verify_opts_init", "spec_verify_noalloc", "spec_row_entropy", "spec_adaptive_k",
               "spec_verify_tree", "spec_verify_host", "spec_lmhead_logits",
               "spec_lmhead_row_stats", "spec_verify_lmhead", "spec_vp_state_bytes",
-              "spec_vp_partials", "spec_vp_decide", "spec_vp_race", "spec_vp_finish"):
+              "spec_vp_partials", "spec_vp_decide", "spec_vp_race", "spec_vp_finish",
+              "spec_philox4x32_10"):
         assert f in names
 
 
@@ -117,6 +118,21 @@ def test_host_validation_rejects_bad_sizes_without_a_device(lib):
     opts.dtype = 5
     assert lib.spec_verify_ex(fake, fake, fake, 1, 3, 10, 1.0, 1.0, 0, fake, fake,
                               ctypes.byref(opts), None) == EINVAL
+    # unknown flag bits (bit 0, once a schedule that was removed, included)
+    for bad in (1, 16, 1 << 31):
+        opts.dtype = sv.SPEC_BF16
+        opts.flags = bad
+        assert lib.spec_verify_ex(fake, fake, fake, 1, 3, 10, 1.0, 1.0, 0, fake, fake,
+                                  ctypes.byref(opts), None) == EINVAL
+        assert lib.spec_verify_noalloc(fake, fake, fake, 1, 3, 10, 1.0, 1.0, 0, fake, fake,
+                                       ctypes.byref(opts), None) == EINVAL
+    # the Philox diagnostic: sizes, forms and alignment are checked on the host
+    assert lib.spec_philox4x32_10(fake, fake, -1, 0, fake, None) == EINVAL
+    assert lib.spec_philox4x32_10(fake, fake, 4, 2, fake, None) == EINVAL
+    assert lib.spec_philox4x32_10(P(264), fake, 4, 0, fake, None) == EINVAL
+    assert lib.spec_philox4x32_10(fake, P(260), 4, 1, fake, None) == EINVAL
+    assert lib.spec_philox4x32_10(fake, fake, 4, 0, None, None) == EINVAL
+    assert lib.spec_philox4x32_10(None, None, 0, 0, None, None) == 0
 
 
 def test_vocab_parallel_validation_without_a_device(lib):

@@ -53,13 +53,8 @@ def _calls(sv, dws):
             t, n = sv.spec_verify_greedy_ex(dw.target, dw.tokens)
             return [t, n]
 
-        def flow(dw=dw, w=w, kw=kw, k=k):
-            t, n, _ = sv.spec_verify_ex(dw.target, dw.draft, dw.tokens, float(w.T[0]), float(w.Td[0]),
-                                        17 + k, flags=sv.SPEC_FLAG_FUSED, **kw)
-            return [t, n]
-
         out += [(f"default{k}", default), (f"early{k}", early), (f"stats{k}", stats),
-                (f"greedy{k}", greedy), (f"flow{k}", flow)]
+                (f"greedy{k}", greedy)]
     return out
 
 

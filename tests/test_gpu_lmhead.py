@@ -99,33 +99,114 @@ def lmhead_workload(B, gamma, V, d, seed, sigma=0.3, scale=1.0):
     return ht, wt, hd, wd
 
 
+def host_logits(h_bits, w_bits):
+    """Logits H W^T from the bf16 inputs, products and sums in fp64, and the per-logit bound
+    on how far the tensor cores' fp32 accumulation may lie from them (the bound
+    test_lmhead_logits_match_fp64 checks: 2e-5 sum_k |h_k w_k| + 1e-5), widened by the
+    fp32 rounding of the exact value that the oracle is given."""
+    hf = workloads.bf16_bits_to_f32(h_bits).astype(np.float64)
+    wf = workloads.bf16_bits_to_f32(w_bits).astype(np.float64)
+    exact = hf @ wf.T
+    bound = 2e-5 * (np.abs(hf) @ np.abs(wf).T) + 1e-5 + 2.0 ** -24 * np.abs(exact)
+    return exact.astype(np.float32), bound
+
+
+def gemm_sensitive(orc, lt, et, ld, ed, tok, T, Td, seed, r):
+    """Sequences whose oracle decisions a logit error within the bounds (et, ed) could
+    change: a tested position whose accept ratio a = p(d)/q(d) may move across u (or lies
+    within the usual 1e-5 band), or a race whose winner's score interval meets another
+    token's (widened by the usual 1e-6).  ln Z moves by at most the row's largest logit
+    error / T; each token's score ln w - ln E moves within the interval its weight takes
+    over the perturbed p and q."""
+    B, G1, V = lt.shape
+    g = G1 - 1
+    flagged = np.zeros(B, dtype=bool)
+    for b in range(B):
+        j = int(r.n_accepted[b])
+        emax_t = et[b].max(axis=1) / T
+        emax_d = ed[b].max(axis=1) / Td if g else None
+        for i in range(min(j + 1, g)):
+            x = int(tok[b, i])
+            dp = et[b, i, x] / T + emax_t[i]
+            dq = ed[b, i, x] / Td + emax_d[i]
+            la = np.log(r.a[b, i]) if r.a[b, i] > 0 else -np.inf
+            lo, hi = np.exp(la - dp - dq), np.exp(la + dp + dq)
+            if lo - 1e-5 <= r.u[b, i] <= hi + 1e-5:
+                flagged[b] = True
+        if r.flags[b] & oracle.FLAG_RESIDUAL_EMPTY:  # the race fell back to p_j
+            flagged[b] = True
+            continue
+        row = j
+        lp = lt[b, row].astype(np.float64) / T - r.logZp[b, row]
+        dp = et[b, row] / T + emax_t[row]
+        lnE = np.log(orc.race_exponentials(seed, b, row, V))
+        p_lo, p_hi = np.exp(lp - dp), np.exp(lp + dp)
+        if j < g:
+            lq = ld[b, row].astype(np.float64) / Td - r.logZq[b, row]
+            dq = ed[b, row] / Td + emax_d[row]
+            w_lo = np.maximum(0.0, p_lo - np.exp(lq + dq))
+            w_hi = np.maximum(0.0, p_hi - np.exp(lq - dq))
+        else:
+            w_lo, w_hi = p_lo, p_hi
+        with np.errstate(divide="ignore"):
+            s_lo, s_hi = np.log(w_lo) - lnE, np.log(w_hi) - lnE
+        y = int(r.tokens[b, j])
+        others = np.delete(s_hi, y)
+        if others.size and others.max() >= s_lo[y] - 1e-6:
+            flagged[b] = True
+    return flagged
+
+
 @pytest.mark.parametrize("B,gamma,V,d,T,Td", [(4, 3, 4096, 128, 1.0, 0.5), (8, 5, 10000, 256, 0.8, 0.4),
                                                (3, 0, 2048, 64, 1.0, 1.0), (64, 8, 32000, 256, 1.0, 0.5)])
 def test_verify_from_hidden_states_matches_oracle(sv, B, gamma, V, d, T, Td):
-    """The fused verify equals the oracle run on the logits the tensor cores compute (the
-    same GEMM: spec_lmhead_logits) under the usual parity rules, and the logits path on
-    those logits."""
-    from _parity import compare_sampling
+    """The verify from hidden states against the oracle run on logits computed on the host
+    (fp64 products of the same bf16 inputs, rounded to fp32), independent of the library's
+    GEMM.  Tokens and counts must match except in sequences where the GEMM's error bound
+    could move a decision (those must still be valid cycles); and, on the logits the tensor
+    cores compute, the fused path must give exactly the logits path's tokens."""
     ht, wt, hd, wd = lmhead_workload(B, gamma, V, d, seed=B * 100 + V)
     dev = torch.device("cuda")
     Ht, Wt, Hd, Wd = (to_dev(a) for a in (ht, wt, hd, wd))
-    lt = sv.spec_lmhead_logits(Ht.reshape(B * (gamma + 1), d), Wt).reshape(B, gamma + 1, V)
-    ld = (sv.spec_lmhead_logits(Hd.reshape(B * gamma, d), Wd).reshape(B, gamma, V) if gamma
-          else torch.empty((B, 0, V), dtype=torch.float32, device=dev))
-    torch.cuda.synchronize()
-    lt_np, ld_np = lt.cpu().numpy(), ld.cpu().numpy()
+    lt, et = host_logits(ht.reshape(B * (gamma + 1), d), wt)
+    lt, et = lt.reshape(B, gamma + 1, V), et.reshape(B, gamma + 1, V)
+    if gamma:
+        ld, ed = host_logits(hd.reshape(B * gamma, d), wd)
+        ld, ed = ld.reshape(B, gamma, V), ed.reshape(B, gamma, V)
+    else:
+        ld, ed = np.zeros((B, 0, V), np.float32), np.zeros((B, 0, V))
     rng = np.random.default_rng(7)
     tok = np.zeros((B, gamma), np.int32)
     for b in range(B):
         if gamma:
-            tok[b] = workloads.draw_drafts(rng, ld_np[b], Td)
+            tok[b] = workloads.draw_drafts(rng, ld[b], Td)
     dtok = torch.from_numpy(tok).to(dev)
-    w = workloads.Workload("lmhead", B, gamma, V, "f32", lt_np, ld_np, tok,
-                           np.full(B, T, np.float32), np.full(B, Td, np.float32))
+    Tv, Tdv = np.full(B, T, np.float32), np.full(B, Td, np.float32)
     orc = oracle.get()
+    # the logits path on the tensor cores' own logits (consistency of the fused path)
+    lt_gpu = sv.spec_lmhead_logits(Ht.reshape(B * (gamma + 1), d), Wt).reshape(B, gamma + 1, V)
+    ld_gpu = (sv.spec_lmhead_logits(Hd.reshape(B * gamma, d), Wd).reshape(B, gamma, V) if gamma
+              else torch.empty((B, 0, V), dtype=torch.float32, device=dev))
+    n_flagged = n_seq = 0
     for seed in range(3):
         t, n = sv.spec_verify_lmhead(Ht, Wt, Hd if gamma else None, Wd if gamma else None, dtok, T, Td, seed)
         torch.cuda.synchronize()
         assert sv.spec_verify_check() == sv.SPEC_OK
-        g = {"tokens": t.cpu().numpy(), "n": n.cpu().numpy()}
-        compare_sampling(w, g, orc.verify(lt_np, ld_np, tok, w.T, w.Td, seed))
+        gt, gn = t.cpu().numpy(), n.cpu().numpy()
+        r = orc.verify(lt, ld, tok, Tv, Tdv, seed)
+        flagged = gemm_sensitive(orc, lt, et, ld, ed, tok, T, Td, seed, r)
+        n_flagged += int(flagged.sum())
+        n_seq += B
+        for b in range(B):
+            j = int(gn[b])
+            assert 0 <= j <= gamma and 0 <= gt[b, j] < V and np.all(gt[b, j + 1:] == -1)
+            if flagged[b]:
+                continue
+            assert j == r.n_accepted[b], (seed, b, j, r.n_accepted[b])
+            np.testing.assert_array_equal(gt[b], r.tokens[b], err_msg=f"seed {seed} sequence {b}")
+        tl, nl, _ = sv.spec_verify_ex(lt_gpu, ld_gpu, dtok, T, Td, seed)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(nl.cpu().numpy(), gn)
+        np.testing.assert_array_equal(tl.cpu().numpy(), gt)
+    # the bound is loose (worst-case accumulation error): most decisions still compare
+    assert n_flagged <= max(2, 0.1 * n_seq), (n_flagged, n_seq)

@@ -12,7 +12,7 @@ import torch
 
 import oracle
 import workloads
-from _parity import TOTALS, DeviceWorkload, compare_greedy, compare_sampling, run_gpu
+from _parity import DeviceWorkload, compare_greedy, compare_sampling, run_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -139,25 +139,43 @@ def test_batched_serving_workload_full(sv, orc):
     compare_greedy(out_t.cpu().numpy(), out_n.cpu().numpy(), rt, rn)
 
 
-def test_throughput_workload_full_size_sampled(sv, orc):
-    """B=256, gamma=12, V=152064 bf16 (1.95 GB): one full-size call in the benchmark's
-    launch configuration, 32 sampled sequences recomputed by the oracle one by one."""
+def _oracle_pool_verify(cfg, seeds):
+    """The oracle's verify of every sequence of named workload `cfg` for each seed, the seeds
+    spread over processes (spawned: the parent holds a CUDA context; each regenerates the
+    workload from its seeded recipe).  Returns {seed: OracleResult}."""
+    import concurrent.futures as cf
+    import multiprocessing as mp
+    import os
+    workers = max(1, min(len(seeds), (os.cpu_count() or 1)))
+    with cf.ProcessPoolExecutor(max_workers=workers, mp_context=mp.get_context("spawn")) as ex:
+        futs = {s: ex.submit(_oracle_verify_config, cfg, s) for s in seeds}
+        return {s: f.result() for s, f in futs.items()}
+
+
+def _oracle_verify_config(cfg, seed):
+    # runs in a spawned worker
+    import oracle as orc_mod
+    import workloads as wl
+    w = wl.config(cfg)
+    return orc_mod.get().verify(w.target, w.draft, w.tokens, w.T, w.Td, seed)
+
+
+def test_throughput_workload_full_size_every_sequence(sv, orc):
+    """B=256, gamma=12, V=152064 bf16 (1.95 GB) in the benchmark's launch configuration:
+    every one of the 256 sequences against the oracle for four seeds, on the full read and
+    on the early-exit path (the oracle's result is the same for both)."""
+    seeds = (0, 1, 2, 3)
+    refs = _oracle_pool_verify(4, seeds)
     w = workloads.config(4)
     dw = DeviceWorkload(w)
-    rng = np.random.default_rng(0)
-    idx = np.sort(rng.choice(w.B, size=32, replace=False))
-    for seed in (0, 1):
-        g = run_gpu(sv, dw, seed, per_seq_temps=False, diagnostics=True)
-        sub = w.subset(idx)
-        # the oracle takes the global sequence index from b_base: one call per sequence
-        parts = [orc.verify(sub.target[k:k + 1], sub.draft[k:k + 1], sub.tokens[k:k + 1],
-                            sub.T[k:k + 1], sub.Td[k:k + 1], seed, b_base=int(b))
-                 for k, b in enumerate(idx)]
-        r = oracle.OracleResult(**{f: np.concatenate([getattr(p, f) for p in parts])
-                                   for f in oracle.OracleResult.__dataclass_fields__})
-        compare_sampling(sub, g, r, idx=idx)
-        # every sequence emits a valid cycle
+    for seed in seeds:
+        r = refs[seed]
+        g = run_gpu(sv, dw, seed, per_seq_temps=False, diagnostics=(seed < 2))
+        compare_sampling(w, g, r, check_values=(seed < 2))
         assert np.all((g["n"] >= 0) & (g["n"] <= w.gamma))
+        ge = run_gpu(sv, dw, seed, per_seq_temps=False, diagnostics=False,
+                     flags=sv.SPEC_FLAG_EARLY_EXIT)
+        compare_sampling(w, ge, r, check_values=False, count=False)
 
 
 @pytest.mark.parametrize("B,gamma,V,dtype", [(24, 8, 128257, "bf16"), (20, 8, 65537, "f32")])
@@ -272,51 +290,29 @@ def test_empty_batch_and_invalid_arguments(sv):
     assert ex.value.code == sv.SPEC_EINVAL
 
 
-@pytest.mark.parametrize("B,gamma,V,dtype", [(3, 4, 5003, "bf16"), (2, 7, 9000, "f32"),
-                                              (4, 0, 777, "bf16"), (6, 3, 40000, "bf16")])
-def test_fused_path_matches_default_and_oracle(sv, orc, B, gamma, V, dtype):
-    """The fused single-kernel path (SPEC_FLAG_FUSED) and the default two-kernel path give
-    identical outputs, and both match the oracle."""
-    w = workloads.generic(B=B, gamma=gamma, V=V, dtype=dtype, seed=B * 31 + V, sigma=0.9,
-                          T=0.8, Td=0.35)
-    dw = DeviceWorkload(w)
-    for seed in range(3):
-        base = run_gpu(sv, dw, seed, per_seq_temps=False)
-        t, n, d = sv.spec_verify_ex(dw.target, dw.draft, dw.tokens, float(w.T[0]),
-                                    float(w.Td[0]), seed, diagnostics=True,
-                                    flags=sv.SPEC_FLAG_FUSED)
-        torch.cuda.synchronize()
-        np.testing.assert_array_equal(t.cpu().numpy(), base["tokens"])
-        np.testing.assert_array_equal(n.cpu().numpy(), base["n"])
-        fused = {k: v.cpu().numpy() for k, v in d.items()}
-        fused.update(tokens=t.cpu().numpy(), n=n.cpu().numpy())
-        for k in ("logp", "logq", "logZp", "logZq", "u"):
-            np.testing.assert_allclose(fused[k], base[k], rtol=2e-6, atol=2e-6,
-                                       equal_nan=True, err_msg=k)
-        r = orc.verify(w.target, w.draft, w.tokens, w.T, w.Td, seed)
-        compare_sampling(w, base, r)
-        compare_sampling(w, fused, r)
-
-
 def test_bounded_wait_times_out_and_context_survives(sv, orc):
-    """The fused kernel's waits are bounded: with the test flag that makes every race wait
-    on a flag nothing sets, the call ends (after about half a second per wait) with
-    SPEC_ETIMEOUT in the status word, and the next normal call is correct."""
+    """The early-exit kernel's waits are bounded: with the test flag under which no race unit
+    publishes its winner, each sequence's last race unit waits for them until the wait
+    gives up (about half a second), records SPEC_ETIMEOUT and finishes; the context stays
+    usable and the next normal call is correct."""
     import time
     w = workloads.generic(B=2, gamma=3, V=3000, dtype="bf16", seed=77)
     dw = DeviceWorkload(w)
     t0 = time.time()
     sv.spec_verify_ex(dw.target, dw.draft, dw.tokens, 1.0, 1.0, 0,
-                      flags=sv.SPEC_FLAG_FUSED | sv.SPEC_DEBUG_NEVER_READY)
+                      flags=sv.SPEC_FLAG_EARLY_EXIT | sv.SPEC_DEBUG_NEVER_READY)
     assert sv.spec_verify_check() == sv.SPEC_ETIMEOUT
     assert time.time() - t0 < 30
-    g = run_gpu(sv, dw, 0, per_seq_temps=False)
-    assert sv.spec_verify_check() == sv.SPEC_OK
-    compare_sampling(w, g, orc.verify(w.target, w.draft, w.tokens, w.T, w.Td, 0))
+    for flags in (0, sv.SPEC_FLAG_EARLY_EXIT):
+        g = run_gpu(sv, dw, 0, per_seq_temps=False, diagnostics=False, flags=flags)
+        assert sv.spec_verify_check() == sv.SPEC_OK
+        compare_sampling(w, g, orc.verify(w.target, w.draft, w.tokens, w.T, w.Td, 0))
 
 
-def test_zz_near_tie_budget():
-    """Flagged near-tie decisions stay under 1e-4 of all decisions compared in this module."""
-    if TOTALS["decisions"] == 0:
-        pytest.skip("no sampling comparisons ran")
-    assert TOTALS["flagged"] <= max(1, 1e-4 * TOTALS["decisions"]), TOTALS
+def test_unknown_flag_bits_are_refused(sv):
+    w = workloads.generic(B=2, gamma=3, V=300, dtype="bf16", seed=1)
+    dw = DeviceWorkload(w)
+    for bad in (1, 16, 1 << 31):
+        with pytest.raises(sv.SpecVerifyError) as e:
+            sv.spec_verify_ex(dw.target, dw.draft, dw.tokens, 1.0, 1.0, 0, flags=bad)
+        assert e.value.code == sv.SPEC_EINVAL

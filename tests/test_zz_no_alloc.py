@@ -5,6 +5,7 @@ nearly all device memory, or a caller that may not block on the device synchroni
 allocation can imply.  spec_verify_noalloc keeps its scratch in a static device array
 instead.  These tests call it through the C ABI and check that two calls in a row give the
 same tokens, accepted counts and diagnostic values as the workspace-using spec_verify_ex,
+that, in a fresh process, calls after the first change nothing in the device's free memory,
 and that a problem too large for the static array is refused before anything runs.  The
 file is named to be collected last; it also passes alone in a fresh process.
 """
@@ -71,6 +72,56 @@ def test_noalloc_matches_the_workspace_entry_point(sv, name, make, per_seq):
             np.testing.assert_allclose(diag[k].cpu().numpy(), ref_d[k].cpu().numpy(),
                                        rtol=1e-6, atol=1e-6, equal_nan=True, err_msg=k)
         assert int(status.item()) == sv.SPEC_OK
+
+
+_ALLOC_PROBE = r"""
+import sys
+import numpy as np
+import torch
+sys.path.insert(0, "tests")
+import workloads
+from _parity import DeviceWorkload
+import speculative_decoding_verification_31_gb300 as sv
+w = workloads.config(3, B=12)
+dw = DeviceWorkload(w)
+B, g = w.B, w.gamma
+out_t = torch.empty((B, g + 1), dtype=torch.int32, device="cuda")
+out_n = torch.empty((B,), dtype=torch.int32, device="cuda")
+status = torch.zeros(1, dtype=torch.int32, device="cuda")
+toks = []
+def call():
+    sv.spec_verify_noalloc(dw.target, dw.draft, dw.tokens, 1.0, 0.5, 7, out_t, out_n,
+                           T_per_seq=dw.T, Td_per_seq=dw.Td, d_status=status)
+    torch.cuda.synchronize()
+    toks.append(out_t.cpu().numpy().copy())
+call()  # the first call loads the library's kernels and looks up the static array
+free0 = torch.cuda.mem_get_info()[0]
+for _ in range(3):
+    call()
+free1 = torch.cuda.mem_get_info()[0]
+assert all(np.array_equal(t, toks[0]) for t in toks), "calls disagree"
+assert int(status.item()) == 0, int(status.item())
+print("FREE", free0, free1)
+"""
+
+
+def test_noalloc_allocates_nothing():
+    """In a fresh process where spec_verify_noalloc is the library's only entry point called,
+    calls after the first (which loads the kernels and the static array's module) leave the
+    device's free memory unchanged: the library allocates nothing on this path, not even its
+    own status word (any cudaMalloc shows at the allocator's granularity)."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    r = subprocess.run([sys.executable, "-c", _ALLOC_PROBE], cwd=root, capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0, r.stdout + r.stderr
+    line = [ln for ln in r.stdout.splitlines() if ln.startswith("FREE")][-1]
+    _, free0, free1 = line.split()
+    assert int(free0) == int(free1), line
 
 
 def test_noalloc_refuses_oversized_problems(sv):
