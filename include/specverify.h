@@ -70,9 +70,19 @@ typedef enum {
     SPEC_EBADTOKEN = 3,  /* (device) a draft token outside [0, V) */
     SPEC_ETIMEOUT = 4,   /* (device) a bounded wait gave up */
     SPEC_ENOMEM = 5,     /* workspace allocation failed or caller workspace too small */
-    SPEC_ESCRATCH = 6    /* problem needs more scratch than spec_verify_noalloc's static
+    SPEC_ESCRATCH = 6,   /* problem needs more scratch than spec_verify_noalloc's static
                             buffer (SPEC_NOALLOC_SCRATCH_BYTES) holds */
+    SPEC_EINDEX = 7      /* (device, index-checked build only) a computed index fell outside
+                            its buffer; the access was skipped and the outputs are invalid */
 } spec_status;
+
+/* The index-checked build.  libspecverify_checked.so is the same library compiled with
+ * SPECVERIFY_CHECKED: in the sampling (default and early-exit) and greedy kernels every
+ * computed index into the logits, the draft tokens, the outputs, the workspace's partial
+ * statistics, race partials and queues is tested against its buffer's size before the
+ * access; an index outside it records SPEC_EINDEX in the status word and skips the access
+ * (no trap and no assert: waits that then go unanswered end after their bounded time).  It
+ * stands in for a memory checker on this GPU; it is slower and meant for tests. */
 
 /* Element type of the logits. */
 typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;

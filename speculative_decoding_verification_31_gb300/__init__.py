@@ -4,7 +4,7 @@ The hot path lives in ``libspecverify.so`` (hand-written CUDA, C ABI in
 ``include/specverify.h``); this package only builds it and binds it.
 """
 from .specverify import (  # noqa: F401
-    EXPORTED, SPEC_BF16, SPEC_DEBUG_NEVER_READY, SPEC_FLAG_EARLY_EXIT, SPEC_EBADTOKEN, SPEC_ECUDA, SPEC_EINVAL, SPEC_ENOMEM, SPEC_ESCRATCH,
+    EXPORTED, SPEC_BF16, SPEC_DEBUG_NEVER_READY, SPEC_FLAG_EARLY_EXIT, SPEC_EBADTOKEN, SPEC_ECUDA, SPEC_EINVAL, SPEC_ENOMEM, SPEC_ESCRATCH, SPEC_EINDEX,
     SPEC_ETIMEOUT, SPEC_F32, SPEC_NOALLOC_SCRATCH_BYTES, SPEC_OK, SpecVerifyError,
     SpecVerifyOpts, load_library, spec_verify, spec_verify_check, spec_verify_ex,
     spec_verify_greedy, spec_verify_greedy_ex, spec_verify_noalloc, spec_verify_strerror,

@@ -14,6 +14,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libspecverify.so")
+CHECKED_LIB = os.path.join(PKG, "libspecverify_checked.so")  # SPECVERIFY_CHECKED: index checks
 SOURCES = ["specverify.cu"]
 DEPS = ["specverify.cu", "kernels.cuh", "vocab.cuh", "device_common.cuh", "philox.cuh", "lmhead.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -45,13 +46,22 @@ def up_to_date(out: str = LIB) -> bool:
     return all(os.path.getmtime(d) <= t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra=()) -> str:
-    if not force and up_to_date():
-        return LIB
-    cmd = nvcc_command(extra=list(extra))
-    if verbose:
-        print(" ".join(cmd))
-    subprocess.run(cmd, check=True)
+def build(force: bool = False, verbose: bool = False, extra=(), checked: bool = True) -> str:
+    """Compile libspecverify.so and (unless checked=False) its index-checked variant
+    libspecverify_checked.so, the two nvcc runs side by side.  Returns the library's path."""
+    jobs = []
+    if force or not up_to_date(LIB):
+        jobs.append(nvcc_command(out=LIB, extra=list(extra)))
+    if checked and (force or not up_to_date(CHECKED_LIB)):
+        jobs.append(nvcc_command(out=CHECKED_LIB, extra=["-DSPECVERIFY_CHECKED", *extra]))
+    procs = []
+    for cmd in jobs:
+        if verbose:
+            print(" ".join(cmd))
+        procs.append((cmd, subprocess.Popen(cmd)))
+    failed = [cmd for cmd, pr in procs if pr.wait() != 0]
+    if failed:
+        raise subprocess.CalledProcessError(1, failed[0])
     return LIB
 
 

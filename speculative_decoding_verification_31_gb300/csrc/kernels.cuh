@@ -47,6 +47,15 @@ struct RacePart {
     int pad;
 };
 
+// Element counts of the buffers a call's kernels index, for the index-checked build
+// (SPECVERIFY_CHECKED): the caller's tensors and the workspace regions.
+struct BufferCaps {
+    long long target, draft, tokens, out_tokens;  // caller tensors
+    long long stat;                               // stat_parts (float2)
+    long long race;                               // race_parts (RacePart)
+    long long row_stat, pos, rowarr, task, race_task, early_race;  // early-exit regions
+};
+
 struct VerifyParams {
     const void* target;         // [B, gamma+1, V]
     const void* draft;          // [B, gamma, V]
@@ -109,7 +118,30 @@ struct VerifyParams {
     // token-tree verify
     int32_t* out_nodes;         // [B, depth] accepted nodes, or nullptr
     struct TreeRace* tree_race; // [B] the node each sequence races
+    BufferCaps caps;            // buffer sizes (checked by the index-checked build only)
 };
+
+// The index-checked build (compiled with SPECVERIFY_CHECKED): before an access through a
+// computed index, sv_in_range(p, i, n) tests 0 <= i < n for the buffer's n elements; on
+// failure it records SPEC_EINDEX (7) in the status word (the first error recorded stays) and
+// the caller skips the access -- no trap, no assert, so the context stays usable.  In the
+// normal build the test is the constant true and compiles away.
+__device__ __forceinline__ bool sv_in_range(const VerifyParams& p, long long i, long long n) {
+#ifdef SPECVERIFY_CHECKED
+    if (i >= 0 && i < n) return true;
+    atomicCAS(reinterpret_cast<int*>(p.status), 0, 7 /* SPEC_EINDEX */);
+    return false;
+#else
+    (void)p; (void)i; (void)n;
+    return true;
+#endif
+}
+
+// Whether the elements [first, first + count) lie in a buffer of n elements (count >= 0).
+__device__ __forceinline__ bool sv_span_in_range(const VerifyParams& p, long long first, long long count,
+                                                 long long n) {
+    return count <= 0 || (sv_in_range(p, first, n) && sv_in_range(p, first + count - 1, n));
+}
 
 // Race partial slots per sequence: at most one per block racing it.  A block of the
 // scan-race grid takes at least one step of chunks, so a sequence meets at most
@@ -281,8 +313,18 @@ __device__ __forceinline__ void row_stats_item(const VerifyParams& p, int b, int
     }
     const int x0 = piece * p.piece_len;
     const int x1 = min(p.V, x0 + p.piece_len);
-    const SoftmaxStat st = stats_piece<ET, U, L>(row, x0, x1, c, lane);
     const int R = 2 * p.gamma + 1;
+#ifdef SPECVERIFY_CHECKED
+    {
+        const bool tgt = r <= p.gamma;
+        const long long off = tgt ? (static_cast<long long>(b) * (p.gamma + 1) + r) * p.V
+                                  : (static_cast<long long>(b) * p.gamma + (r - p.gamma - 1)) * p.V;
+        if (!(sv_span_in_range(p, off + x0, x1 - x0, tgt ? p.caps.target : p.caps.draft) &&
+              sv_in_range(p, (static_cast<long long>(b) * R + r) * p.npieces + piece, p.caps.stat)))
+            return;
+    }
+#endif
+    const SoftmaxStat st = stats_piece<ET, U, L>(row, x0, x1, c, lane);
     if (lane == 0)  // one aligned 64-bit store: readers see both halves or neither
         store_stat(p.stat_parts + (static_cast<long long>(b) * R + r) * p.npieces + piece, st.m, st.s);
 }
@@ -717,6 +759,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1) row_argmax_kernel(VerifyPar
         const S* row = static_cast<const S*>(p.target) + row_index * p.V;
         const int x0 = piece * p.piece_len;
         const int x1 = min(p.V, x0 + p.piece_len);
+#ifdef SPECVERIFY_CHECKED
+        if (!(sv_span_in_range(p, row_index * p.V + x0, x1 - x0, p.caps.target) &&
+              sv_in_range(p, item, p.caps.stat)))
+            return;
+#endif
         const ArgMax a = argmax_piece<ET, U>(row, x0, x1, lane);
         if (lane == 0) p.stat_parts[item] = make_float2(a.v, __int_as_float(a.i));
     });
@@ -759,7 +806,9 @@ __global__ void __launch_bounds__(256) scan_greedy_kernel(VerifyParams p) {
     }
     for (int r = warp; r < R; r += nw) {
         ArgMax a{-INFINITY, INT_MAX};
-        const float2* parts = p.stat_parts + (static_cast<long long>(b) * R + r) * p.npieces;
+        const long long pbase = (static_cast<long long>(b) * R + r) * p.npieces;
+        const float2* parts = p.stat_parts + pbase;
+        if (!sv_span_in_range(p, pbase, p.npieces, p.caps.stat)) continue;
         for (int k = lane; k < p.npieces; k += 32) {
             const float2 q = parts[k];
             const ArgMax o{q.x, __float_as_int(q.y)};
@@ -784,6 +833,7 @@ __global__ void __launch_bounds__(256) scan_greedy_kernel(VerifyParams p) {
         if (j < 0) set_status(p.status, 3 /* SPEC_EBADTOKEN */);
     }
     int32_t* out = p.out_tokens + static_cast<long long>(b) * (p.gamma + 1);
+    if (!sv_span_in_range(p, static_cast<long long>(b) * (p.gamma + 1), p.gamma + 1, p.caps.out_tokens)) return;
     for (int t = threadIdx.x; t <= p.gamma; t += blockDim.x) {
         int v = -1;
         if (j >= 0) {
@@ -1277,8 +1327,11 @@ __device__ __forceinline__ void race_rows_block(const VerifyParams& p, int b,
     if (threadIdx.x == 0) {
         RaceState m = s_best[0];
         for (int k = 1; k < 8; ++k) m = race_merge(m, s_best[k]);
-        parts[slot].second = m.second;  // diagnostic only
-        *reinterpret_cast<unsigned long long*>(parts + slot) = pack_race(m.best, m.idx);
+        const long long ps = static_cast<long long>(b) * race_slots(p.rpieces) + slot;
+        if (slot < race_slots(p.rpieces) && sv_in_range(p, ps, p.caps.race)) {
+            parts[slot].second = m.second;  // diagnostic only
+            *reinterpret_cast<unsigned long long*>(parts + slot) = pack_race(m.best, m.idx);
+        }
         s_last = (atomicAdd(p.tickets + b, 1) == nslots - 1);
     }
     __syncthreads();
@@ -1327,6 +1380,11 @@ __device__ __forceinline__ void race_sequence_block(const VerifyParams& p, int b
     const S* rt = static_cast<const S*>(p.target) + (static_cast<long long>(b) * (p.gamma + 1) + j) * p.V;
     const S* rd = residual ? static_cast<const S*>(p.draft) + (static_cast<long long>(b) * p.gamma + j) * p.V
                            : nullptr;
+    // (every block of the sequence takes the same branch: none arrives, none waits)
+    if (!(sv_span_in_range(p, (static_cast<long long>(b) * (p.gamma + 1) + j) * p.V, p.V, p.caps.target) &&
+          (!residual || sv_span_in_range(p, (static_cast<long long>(b) * p.gamma + j) * p.V, p.V, p.caps.draft)) &&
+          sv_in_range(p, static_cast<long long>(b) * (p.gamma + 1) + j, p.caps.out_tokens)))
+        return;
     race_rows_block<ET>(p, b, rt, rd, residual, static_cast<uint32_t>(j),
                         p.out_tokens + static_cast<long long>(b) * (p.gamma + 1) + j, cb_begin,
                         cb_end, cb_step, ch_limit, slot, nslots, si, s_thr, s_best, s_last);
@@ -1421,11 +1479,11 @@ __global__ void __launch_bounds__(256, SPECVERIFY_RACE_MINBLOCKS) scan_race_kern
             s_d[i0] = d;
             s_u[i0] = accept_uniform(p.key, bg, static_cast<uint32_t>(i0));
             float xt = 0.0f, xd = 0.0f;
-            if (d >= 0 && d < p.V) {
-                xt = ET::load1(static_cast<const S*>(p.target) +
-                               (static_cast<long long>(b) * (p.gamma + 1) + i0) * p.V + d);
-                xd = ET::load1(static_cast<const S*>(p.draft) +
-                               (static_cast<long long>(b) * p.gamma + i0) * p.V + d);
+            const long long kt = (static_cast<long long>(b) * (p.gamma + 1) + i0) * p.V + d;
+            const long long kd = (static_cast<long long>(b) * p.gamma + i0) * p.V + d;
+            if (d >= 0 && d < p.V && sv_in_range(p, kt, p.caps.target) && sv_in_range(p, kd, p.caps.draft)) {
+                xt = ET::load1(static_cast<const S*>(p.target) + kt);
+                xd = ET::load1(static_cast<const S*>(p.draft) + kd);
             }
             s_xt[i0] = xt;
             s_xd[i0] = xd;
@@ -1454,10 +1512,10 @@ __global__ void __launch_bounds__(256, SPECVERIFY_RACE_MINBLOCKS) scan_race_kern
             } else {
                 d = p.tokens[static_cast<long long>(b) * p.gamma + i];
                 u = accept_uniform(p.key, bg, static_cast<uint32_t>(i));
-                xt = ET::load1(static_cast<const S*>(p.target) +
-                               (static_cast<long long>(b) * (p.gamma + 1) + i) * p.V + d);
-                xd = ET::load1(static_cast<const S*>(p.draft) +
-                               (static_cast<long long>(b) * p.gamma + i) * p.V + d);
+                const long long kt = (static_cast<long long>(b) * (p.gamma + 1) + i) * p.V + d;
+                const long long kd = (static_cast<long long>(b) * p.gamma + i) * p.V + d;
+                xt = sv_in_range(p, kt, p.caps.target) ? ET::load1(static_cast<const S*>(p.target) + kt) : 0.0f;
+                xd = sv_in_range(p, kd, p.caps.draft) ? ET::load1(static_cast<const S*>(p.draft) + kd) : 0.0f;
             }
             const long long k = static_cast<long long>(b) * p.gamma + i;
             if (writer && p.out_u) p.out_u[k] = u;
@@ -1473,7 +1531,10 @@ __global__ void __launch_bounds__(256, SPECVERIFY_RACE_MINBLOCKS) scan_race_kern
         const unsigned long long* parts =
             reinterpret_cast<const unsigned long long*>(p.stat_parts) + static_cast<long long>(b) * R * p.npieces;
         for (int r = threadIdx.x; r < R; r += blockDim.x) {
-            const SoftmaxStat st = fold_row_stats(parts + static_cast<long long>(r) * p.npieces, p.npieces);
+            const long long pbase = (static_cast<long long>(b) * R + r) * p.npieces;
+            const SoftmaxStat st = sv_span_in_range(p, pbase, p.npieces, p.caps.stat)
+                ? fold_row_stats(parts + static_cast<long long>(r) * p.npieces, p.npieces)
+                : SoftmaxStat{-FLT_MAX, 1.0f};
             const float l2s = log2f(st.s);
             sm_m[r] = st.m;
             sm_l[r] = l2s;
@@ -1507,8 +1568,9 @@ __global__ void __launch_bounds__(256, SPECVERIFY_RACE_MINBLOCKS) scan_race_kern
                 if (j < 0) set_status(p.status, 3 /* SPEC_EBADTOKEN */);
             }
             int32_t* out = p.out_tokens + static_cast<long long>(b) * (p.gamma + 1);
-            for (int t = threadIdx.x; t <= p.gamma; t += blockDim.x)
-                if (t != j) out[t] = (j >= 0 && t < j) ? p.tokens[static_cast<long long>(b) * p.gamma + t] : -1;
+            if (sv_span_in_range(p, static_cast<long long>(b) * (p.gamma + 1), p.gamma + 1, p.caps.out_tokens))
+                for (int t = threadIdx.x; t <= p.gamma; t += blockDim.x)
+                    if (t != j) out[t] = (j >= 0 && t < j) ? p.tokens[static_cast<long long>(b) * p.gamma + t] : -1;
         }
         if (j >= 0) {
             SeqInfo si;
@@ -1925,8 +1987,12 @@ __device__ __forceinline__ void early_enqueue_upto(const VerifyParams& p, int b,
     const int n = early_rows_upto(p, hi) - early_rows_upto(p, old);
     int q = atomicAdd(p.task_tail, n);
     for (int k = old + 1; k <= hi; ++k) {
-        st_relaxed(p.task + q++, b * R + k);
-        if (k < p.gamma) st_relaxed(p.task + q++, b * R + p.gamma + 1 + k);
+        if (sv_in_range(p, q, p.caps.task)) st_relaxed(p.task + q, b * R + k);
+        ++q;
+        if (k < p.gamma) {
+            if (sv_in_range(p, q, p.caps.task)) st_relaxed(p.task + q, b * R + p.gamma + 1 + k);
+            ++q;
+        }
     }
 }
 
@@ -1962,7 +2028,8 @@ __device__ __forceinline__ void early_finish(const VerifyParams& p, int b, int j
         p.seq[b] = si;
         p.out_n[b] = j;
         // the race reads seq[b] after acquiring this slot
-        st_release(p.race_task + atomicAdd(p.race_tail, 1), b);
+        const int rs = atomicAdd(p.race_tail, 1);
+        if (sv_in_range(p, rs, p.caps.race_task)) st_release(p.race_task + rs, b);
         atomicAdd(p.seq_decided, 1);
     }
 }
@@ -2021,10 +2088,10 @@ __device__ __forceinline__ void early_decide_from(const VerifyParams& p, int b, 
                 const int d = tok[i];
                 const uint32_t bg = p.seq_base + static_cast<uint32_t>(b);
                 const float u = accept_uniform(p.key, bg, static_cast<uint32_t>(i));
-                const float xt = ET::load1(static_cast<const S*>(p.target) +
-                                           (static_cast<long long>(b) * (p.gamma + 1) + i) * p.V + d);
-                const float xd = ET::load1(static_cast<const S*>(p.draft) +
-                                           (static_cast<long long>(b) * p.gamma + i) * p.V + d);
+                const long long kt = (static_cast<long long>(b) * (p.gamma + 1) + i) * p.V + d;
+                const long long kd = (static_cast<long long>(b) * p.gamma + i) * p.V + d;
+                const float xt = sv_in_range(p, kt, p.caps.target) ? ET::load1(static_cast<const S*>(p.target) + kt) : 0.0f;
+                const float xd = sv_in_range(p, kd, p.caps.draft) ? ET::load1(static_cast<const S*>(p.draft) + kd) : 0.0f;
                 const float l2p = fmaf(xt, scale_of(seq_T(p, b)), -sp.x) - sp.y;
                 const float l2q = fmaf(xd, scale_of(seq_Td(p, b)), -sq.x) - sq.y;
                 // accept iff u < min(1, p/q); p(d) = 0 rejects, q(d) = 0 < p(d) accepts
@@ -2060,7 +2127,12 @@ template <class ET>
 __device__ __forceinline__ void early_row_done(const VerifyParams& p, int b, int r, int lane) {
     const int R = 2 * p.gamma + 1;
     SoftmaxStat st{-FLT_MAX, 0.0f};
-    const float2* parts = p.stat_parts + (static_cast<long long>(b) * R + r) * p.npieces;
+    const long long pbase = (static_cast<long long>(b) * R + r) * p.npieces;
+    const float2* parts = p.stat_parts + pbase;
+    if (!(sv_span_in_range(p, pbase, p.npieces, p.caps.stat) &&
+          sv_span_in_range(p, static_cast<long long>(b) * R, R, p.caps.row_stat) &&
+          sv_span_in_range(p, static_cast<long long>(b) * (p.gamma + 1), p.gamma + 1, p.caps.pos)))
+        return;
     for (int k = lane; k < p.npieces; k += 32) {
         const float2 q = wait_stat(p, parts + k);
         st = merge_stat(st, SoftmaxStat{q.x, q.y});
@@ -2104,6 +2176,11 @@ __device__ __forceinline__ void early_race_unit(const VerifyParams& p, int b, in
     const uint32_t bg = p.seq_base + static_cast<uint32_t>(b);
     const int x0 = piece * p.piece_len;
     const int x1 = min(p.V, x0 + p.piece_len);
+    if (!(sv_span_in_range(p, (static_cast<long long>(b) * (p.gamma + 1) + j) * p.V, p.V, p.caps.target) &&
+          (!residual || sv_span_in_range(p, (static_cast<long long>(b) * p.gamma + j) * p.V, p.V, p.caps.draft)) &&
+          sv_span_in_range(p, static_cast<long long>(b) * p.npieces, p.npieces, p.caps.early_race) &&
+          sv_in_range(p, static_cast<long long>(b) * (p.gamma + 1) + j, p.caps.out_tokens)))
+        return;
     const RaceState st = race_piece<ET>(rt, rd, x0, x1, si, residual, p.rk, bg,
                                         static_cast<uint32_t>(j), lane);
     unsigned long long* parts = p.early_race + static_cast<long long>(b) * p.npieces;
@@ -2197,11 +2274,22 @@ __global__ void __launch_bounds__(256, SPECVERIFY_EARLY_MINBLOCKS) verify_early_
                 d = early_initial_task(p, q);
             } else {
                 d = 0;
+                if (!sv_in_range(p, q - p.n_init, p.caps.task)) break;
                 if (lane == 0) d = early_wait_slot(p, p.task + (q - p.n_init), p.seq_decided);
                 d = __shfl_sync(0xffffffffu, d, 0);
                 if (d == kTaskEmpty) break;
             }
             const int b = d / R, r = d % R;
+#ifdef SPECVERIFY_CHECKED
+            if (!(sv_in_range(p, static_cast<long long>(d) * np + piece, p.caps.stat) &&
+                  sv_in_range(p, d, p.caps.rowarr) &&
+                  sv_span_in_range(p, (r <= p.gamma ? static_cast<long long>(b) * (p.gamma + 1) + r
+                                                     : static_cast<long long>(b) * p.gamma + (r - p.gamma - 1)) * p.V +
+                                          static_cast<long long>(piece) * p.piece_len,
+                                   min(p.V - piece * p.piece_len, p.piece_len),
+                                   r <= p.gamma ? p.caps.target : p.caps.draft)))
+                continue;
+#endif
             const S* row;
             float cs;
             if (r <= p.gamma) {
@@ -2239,6 +2327,7 @@ __global__ void __launch_bounds__(256, SPECVERIFY_EARLY_MINBLOCKS) verify_early_
         c = __shfl_sync(0xffffffffu, c, 0);
         if (c >= race_cap) break;
         int b = 0;
+        if (!sv_in_range(p, c / np, p.caps.race_task)) break;
         if (lane == 0) b = early_wait_slot(p, p.race_task + c / np, p.seq_finished);
         b = __shfl_sync(0xffffffffu, b, 0);
         __syncwarp();  // the other lanes' reads of seq[b] follow lane 0's acquire

@@ -244,6 +244,25 @@ void record(const spec_verify_opts* o, int k, cudaStream_t s) {
     if (o && o->prof_events[k]) cudaEventRecord(static_cast<cudaEvent_t>(o->prof_events[k]), s);
 }
 
+// Element counts of the buffers the call's kernels index (checked by the index-checked
+// build): the caller's tensors from the problem's sizes, the workspace regions from the
+// layout.
+void set_caps(VerifyParams& p, const Layout& L, int B, int gamma, int V) {
+    const long long R = 2LL * gamma + 1;
+    p.caps.target = static_cast<long long>(B) * (gamma + 1) * V;
+    p.caps.draft = static_cast<long long>(B) * gamma * V;
+    p.caps.tokens = static_cast<long long>(B) * gamma;
+    p.caps.out_tokens = static_cast<long long>(B) * (gamma + 1);
+    p.caps.stat = static_cast<long long>((L.ext_off - L.stat_off) / sizeof(float2));
+    p.caps.race = static_cast<long long>((L.ticket_off - L.race_off) / sizeof(RacePart));
+    p.caps.row_stat = B * R;
+    p.caps.pos = static_cast<long long>(B) * (gamma + 1);
+    p.caps.rowarr = B * R;
+    p.caps.task = L.e_task_cap;
+    p.caps.race_task = B;
+    p.caps.early_race = static_cast<long long>((L.total - L.e_race_off) / sizeof(unsigned long long));
+}
+
 void bind_workspace(VerifyParams& p, const Layout& L, char* ws) {
     p.piece_len = L.piece_len;
     p.npieces = L.npieces;
@@ -276,6 +295,7 @@ int prepare(int B, int gamma, int V, int dtype, const spec_verify_opts* o, Verif
         ws = static_cast<char*>((*dstate)->ws);
     }
     bind_workspace(p, L, ws);
+    set_caps(p, L, B, gamma, V);
     p.status = (o && o->d_status) ? o->d_status : (*dstate)->status;
     if (ws_out) *ws_out = ws;
     return SPEC_OK;
@@ -1235,6 +1255,7 @@ const char* spec_verify_strerror(int status) {
         case SPEC_ETIMEOUT: return "bounded device wait timed out";
         case SPEC_ENOMEM: return "workspace allocation failed or caller workspace too small";
         case SPEC_ESCRATCH: return "problem needs more scratch than the static no-alloc buffer";
+        case SPEC_EINDEX: return "index outside its buffer (index-checked build): access skipped";
         default: return "unknown status";
     }
 }
@@ -1490,6 +1511,7 @@ extern "C" int spec_verify_noalloc(const void* target_logits, const void* draft_
     }
     char* ws = nd->scratch;
     bind_workspace(p, L, ws);
+    set_caps(p, L, B, gamma, V);
     if (opts && opts->d_status) {
         p.status = opts->d_status;
     } else {

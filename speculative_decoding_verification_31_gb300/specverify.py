@@ -15,9 +15,11 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libspecverify.so")
+CHECKED_LIB_PATH = os.path.join(_HERE, "libspecverify_checked.so")  # index-checked build (tests)
 
 SPEC_OK, SPEC_EINVAL, SPEC_ECUDA, SPEC_EBADTOKEN, SPEC_ETIMEOUT, SPEC_ENOMEM = range(6)
 SPEC_ESCRATCH = 6
+SPEC_EINDEX = 7
 SPEC_NOALLOC_SCRATCH_BYTES = 8 << 20
 SPEC_DEBUG_NEVER_READY, SPEC_FLAG_EARLY_EXIT, SPEC_FLAG_FULL_READ = 2, 4, 8
 SPEC_F32, SPEC_BF16 = 0, 1
@@ -64,6 +66,14 @@ class SpecVerifyOpts(ctypes.Structure):
 
 
 _lib = None
+
+
+def use_library(path: str) -> ctypes.CDLL:
+    """Make every entry point of this module call the library at `path` from now on (the
+    index-checked build, for tests); returns it."""
+    global _lib
+    _lib = None
+    return load_library(path)
 
 
 def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
@@ -125,10 +135,14 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
 def _call(device, name: str, *args) -> int:
     """Call entry point `name` with `device` current: the library finds its per-device state
     (workspace, status word, SM count) through the current device, which must be the device
-    of the tensors and of the stream the call is given."""
-    lib = load_library()
+    of the tensors and of the stream the call is given.  The device is switched (and
+    switched back) only when it is not current already."""
+    fn = getattr(load_library(), name)
+    idx = device.index if isinstance(device, torch.device) else device
+    if idx is None or idx == torch.cuda.current_device():
+        return fn(*args)
     with torch.cuda.device(device):
-        return getattr(lib, name)(*args)
+        return fn(*args)
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -211,8 +225,7 @@ def spec_verify_greedy(target_logits, draft_tokens, out_tokens=None, out_n_accep
 
 def _make_opts(dtype, T_per_seq, Td_per_seq, seq_index_base, workspace, d_status, diag,
                prof_events: Optional[Sequence], flags: int = 0):
-    o = SpecVerifyOpts()
-    load_library().spec_verify_opts_init(ctypes.byref(o))
+    o = SpecVerifyOpts()  # zero-initialised, as spec_verify_opts_init leaves it
     o.dtype = dtype
     o.flags = int(flags)
     o.seq_index_base = int(seq_index_base)

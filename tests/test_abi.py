@@ -55,6 +55,19 @@ def test_every_declared_symbol_is_exported(lib):
         assert set(names) <= exported
 
 
+def test_checked_library_exports_the_same_entry_points(lib):
+    """The index-checked variant is the same ABI (built beside the library)."""
+    import speculative_decoding_verification_31_gb300 as sv
+    path = sv.specverify.CHECKED_LIB_PATH
+    assert os.path.exists(path)
+    checked = ctypes.CDLL(path)
+    for f in declared_functions():
+        assert hasattr(checked, f), f
+    assert checked.spec_verify_strerror  # loads and resolves
+    checked.spec_verify_strerror.restype = ctypes.c_char_p
+    assert b"index" in checked.spec_verify_strerror(7)
+
+
 def test_opts_struct_layout_matches_c(lib, tmp_path):
     from speculative_decoding_verification_31_gb300.specverify import SpecVerifyOpts
     src = tmp_path / "layout.c"
@@ -81,7 +94,7 @@ def test_opts_struct_layout_matches_c(lib, tmp_path):
 
 def test_strerror_and_workspace_size(lib):
     import speculative_decoding_verification_31_gb300 as sv
-    for code in range(6):
+    for code in range(8):
         assert sv.spec_verify_strerror(code) != "unknown status"
     assert sv.spec_verify_strerror(99) == "unknown status"
     small = sv.spec_verify_workspace_bytes(1, 5, 1024, sv.SPEC_F32)

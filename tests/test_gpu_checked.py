@@ -1,0 +1,80 @@
+"""The index-checked build, libspecverify_checked.so (marked gpu).
+
+It is the library compiled with SPECVERIFY_CHECKED: the sampling (default and early-exit)
+and greedy kernels test every computed index into the logits, tokens, outputs and workspace
+regions before the access, and record SPEC_EINDEX instead of making it.  Here the small
+ragged shapes of the parity and early-exit suites run through it: every call must finish
+with the status word clear (no index left its buffer) and give the oracle's results.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from _parity import DeviceWorkload, compare_greedy, compare_sampling, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [
+    # B, gamma, V, dtype, draft noise
+    (1, 5, 1024, "f32", 0.5),
+    (3, 4, 5003, "bf16", 0.3),
+    (2, 7, 9000, "f32", 0.2),
+    (4, 0, 777, "bf16", 1.0),
+    (2, 3, 1, "f32", 1.0),
+    (5, 2, 7, "bf16", 0.5),
+    (2, 6, 20000, "bf16", 0.7),
+    (1, 1, 4100, "f32", 0.7),
+    (8, 8, 20000, "bf16", 0.1),
+    (3, 48, 2500, "bf16", 0.01),
+    (33, 6, 12000, "bf16", 1.2),
+    (24, 8, 128257, "bf16", 0.8),
+]
+
+
+@pytest.fixture(scope="module")
+def sv():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import speculative_decoding_verification_31_gb300 as m
+    m.specverify.use_library(m.specverify.CHECKED_LIB_PATH)
+    yield m
+    m.specverify.use_library(m.specverify.LIB_PATH)
+
+
+@pytest.mark.parametrize("B,gamma,V,dtype,sigma", SHAPES)
+def test_checked_build_sampling_early_exit_and_greedy(sv, B, gamma, V, dtype, sigma):
+    orc = oracle.get()
+    w = workloads.generic(B=B, gamma=gamma, V=V, dtype=dtype, seed=B * 13 + V + gamma,
+                          sigma=sigma, T=0.9, Td=0.45)
+    dw = DeviceWorkload(w)
+    for seed in range(2):
+        r = orc.verify(w.target, w.draft, w.tokens, w.T, w.Td, seed)
+        for flags in (0, sv.SPEC_FLAG_EARLY_EXIT):
+            g = run_gpu(sv, dw, seed, per_seq_temps=(seed == 1), diagnostics=(flags == 0),
+                        flags=flags)
+            assert sv.spec_verify_check() == sv.SPEC_OK, (seed, flags)
+            compare_sampling(w, g, r, check_values=(flags == 0), count=False)
+    wg = workloads.generic(B=B, gamma=gamma, V=V, dtype=dtype, seed=B + V, greedy=True)
+    dg = DeviceWorkload(wg)
+    t, n = sv.spec_verify_greedy_ex(dg.target, dg.tokens)
+    assert sv.spec_verify_check() == sv.SPEC_OK
+    rt, rn, _ = orc.verify_greedy(wg.target, wg.tokens)
+    compare_greedy(t.cpu().numpy(), n.cpu().numpy(), rt, rn)
+
+
+def test_checked_build_bad_tokens_still_reported(sv):
+    """A draft token outside [0, V) is the input error it always was (SPEC_EBADTOKEN), found
+    before any gather at that index is made."""
+    w = workloads.generic(B=4, gamma=3, V=500, dtype="bf16", seed=6)
+    tok = w.tokens.copy()
+    tok[1, 1] = 500
+    tok[3, 0] = -1
+    dw = DeviceWorkload(w)
+    dtok = torch.from_numpy(tok).cuda()
+    for flags in (0, sv.SPEC_FLAG_EARLY_EXIT):
+        t, n, _ = sv.spec_verify_ex(dw.target, dw.draft, dtok, 1.0, 1.0, 3, flags=flags)
+        assert sv.spec_verify_check() == sv.SPEC_EBADTOKEN
+        got = n.cpu().numpy()
+        assert got[1] == -1 and got[3] == -1
