@@ -108,7 +108,9 @@ typedef struct {
     float *out_logZ_q;          /* [B, gamma]   ln sum_x exp(L_d[b,i,x] / Td_b) */
     float *out_u;               /* [B, gamma]   acceptance uniforms */
     float *out_race;            /* [B, 2]       winning race score ln(w(y)/E_y), and the
-                                                runner-up score (approximate) */
+                                                runner-up score (approximate: the best of
+                                                the tokens scored exactly, which can vary
+                                                from call to call) */
     void *prof_events[4];       /* optional cudaEvent_t: recorded before the first kernel and
                                    after each kernel of the call (sampling: two kernels, three
                                    with per-position statistics, one with SPEC_FLAG_EARLY_EXIT;

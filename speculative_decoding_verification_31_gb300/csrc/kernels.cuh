@@ -1174,13 +1174,14 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64g(const void* p) {
     return v;
 }
 
-// The race of sequence b by one of the `nslots` blocks that share it, over target row rt
-// (and, for a residual, draft row rd; statistics in si) with random-number row `pos`: race
-// the chunks cb + w (warp w) for cb = cb_begin, cb_begin + cb_step, ... (< cb_end), chunks
-// from ch_limit on excluded, publish the block's winner in
-// partial slot `slot`, and if this is the sequence's last block to finish, merge the
-// blocks' winners and write the token to *out.
-template <class ET>
+// The race of sequence b by one of the `nslots` groups of NW warps that share it (a block,
+// or the racing warps of one), over target row rt (and, for a residual, draft row rd;
+// statistics in si) with random-number row `pos`: race the chunks cb + w (warp w of the
+// group, wib) for cb = cb_begin, cb_begin + cb_step, ... (< cb_end), chunks from ch_limit on
+// excluded, publish the group's winner in partial slot `slot`, and if this is the sequence's
+// last group to finish, merge the groups' winners and write the token to *out.  sync() is
+// the group's barrier; CHAINS Philox blocks are computed at a time per lane.
+template <class ET, int NW, class Sync, int CHAINS = kRaceChains>
 __device__ __forceinline__ void race_rows_block(const VerifyParams& p, int b,
                                                const typename ET::storage* rt,
                                                const typename ET::storage* rd, bool residual,
@@ -1188,10 +1189,10 @@ __device__ __forceinline__ void race_rows_block(const VerifyParams& p, int b,
                                                int cb_end, int cb_step, int ch_limit, int slot,
                                                int nslots,
                                                const SeqInfo& si, float* s_thr,
-                                               RaceState* s_best, int& s_last) {
+                                               RaceState* s_best, int& s_last, int wib, Sync sync) {
     using S = typename ET::storage;
     constexpr int VPL = kRaceWarpTokens / (32 * ET::kVec);
-    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
     const uint32_t bg = p.seq_base + static_cast<uint32_t>(b);
     const RaceRowRng q = race_row_rng(p.rk, bg, pos);
     RaceState st{-INFINITY, INT_MAX, -INFINITY};
@@ -1262,18 +1263,18 @@ __device__ __forceinline__ void race_rows_block(const VerifyParams& p, int b,
             }
             seed = float_unorder(__reduce_max_sync(0xffffffffu, float_order(seed)));
             if (lane == 0) s_thr[wib] = seed;
-            __syncthreads();
+            sync();
             thr = s_thr[0];
 #pragma unroll
-            for (int k = 1; k < 8; ++k) thr = fmaxf(thr, s_thr[k]);
+            for (int k = 1; k < NW; ++k) thr = fmaxf(thr, s_thr[k]);
             first = false;
         }
         if (vec_ok) {
             const float mpl = si.mp + si.l2sp;
-            // Philox blocks are computed kRaceChains at a time (independent dependency chains,
-            // so the rounds of one hide the latency of another), then tested
+            // Philox blocks are computed CHAINS at a time (independent dependency chains, so
+            // the rounds of one hide the latency of another), then tested
             constexpr int BPV = ET::kVec / 4;  // Philox blocks per 16-byte vector
-            constexpr int VG = kRaceChains / BPV;
+            constexpr int VG = CHAINS / BPV;
             static_assert(VPL % VG == 0, "race vectors per lane must fill whole groups");
 #pragma unroll
             for (int k0 = 0; k0 < VPL; k0 += VG) {
@@ -1314,7 +1315,7 @@ __device__ __forceinline__ void race_rows_block(const VerifyParams& p, int b,
             // new, is such a bound)
             volatile float* vt = s_thr;
             if (lane == 0) vt[wib] = thr;
-            const float t = lane < 8 ? vt[lane] : -INFINITY;
+            const float t = lane < NW ? vt[lane] : -INFINITY;
             thr = fmaxf(thr, float_unorder(__reduce_max_sync(0xffffffffu, float_order(t))));
 #pragma unroll
             for (int k = 0; k < VPL; ++k) raw[k] = raw_next[k];
@@ -1322,11 +1323,11 @@ __device__ __forceinline__ void race_rows_block(const VerifyParams& p, int b,
     }
     st = warp_race_merge(st);
     if (lane == 0) s_best[wib] = st;
-    __syncthreads();
+    sync();
     RacePart* parts = p.race_parts + static_cast<long long>(b) * race_slots(p.rpieces);
-    if (threadIdx.x == 0) {
+    if (wib == 0 && lane == 0) {
         RaceState m = s_best[0];
-        for (int k = 1; k < 8; ++k) m = race_merge(m, s_best[k]);
+        for (int k = 1; k < NW; ++k) m = race_merge(m, s_best[k]);
         const long long ps = static_cast<long long>(b) * race_slots(p.rpieces) + slot;
         if (slot < race_slots(p.rpieces) && sv_in_range(p, ps, p.caps.race)) {
             parts[slot].second = m.second;  // diagnostic only
@@ -1334,7 +1335,7 @@ __device__ __forceinline__ void race_rows_block(const VerifyParams& p, int b,
         }
         s_last = (atomicAdd(p.tickets + b, 1) == nslots - 1);
     }
-    __syncthreads();
+    sync();
     if (!s_last || wib != 0) return;
     // last block of this sequence: merge every block's winner, waiting (bounded) for each
     RaceState m{-INFINITY, INT_MAX, -INFINITY};
@@ -1368,12 +1369,13 @@ __device__ __forceinline__ void race_rows_block(const VerifyParams& p, int b,
     }
 }
 
-// The chain's race: row j = si.j (the residual of position j < gamma, or the bonus row).
-template <class ET>
+// The chain's race: row j = si.j (the residual of position j < gamma, or the bonus row), by
+// a group of NW warps (see race_rows_block).
+template <class ET, int NW, class Sync, int CHAINS = kRaceChains>
 __device__ __forceinline__ void race_sequence_block(const VerifyParams& p, int b, int cb_begin,
                                                    int cb_end, int cb_step, int ch_limit, int slot,
                                                    int nslots, const SeqInfo& si, float* s_thr,
-                                                   RaceState* s_best, int& s_last) {
+                                                   RaceState* s_best, int& s_last, int wib, Sync sync) {
     using S = typename ET::storage;
     const int j = si.j;
     const bool residual = j < p.gamma;
@@ -1385,9 +1387,10 @@ __device__ __forceinline__ void race_sequence_block(const VerifyParams& p, int b
           (!residual || sv_span_in_range(p, (static_cast<long long>(b) * p.gamma + j) * p.V, p.V, p.caps.draft)) &&
           sv_in_range(p, static_cast<long long>(b) * (p.gamma + 1) + j, p.caps.out_tokens)))
         return;
-    race_rows_block<ET>(p, b, rt, rd, residual, static_cast<uint32_t>(j),
-                        p.out_tokens + static_cast<long long>(b) * (p.gamma + 1) + j, cb_begin,
-                        cb_end, cb_step, ch_limit, slot, nslots, si, s_thr, s_best, s_last);
+    race_rows_block<ET, NW, Sync, CHAINS>(p, b, rt, rd, residual, static_cast<uint32_t>(j),
+                            p.out_tokens + static_cast<long long>(b) * (p.gamma + 1) + j, cb_begin,
+                            cb_end, cb_step, ch_limit, slot, nslots, si, s_thr, s_best, s_last, wib,
+                            sync);
 }
 
 // The merged statistics of one row from its P partials (packed (m, s) words, complete: they
@@ -1419,18 +1422,160 @@ __device__ __forceinline__ SoftmaxStat fold_row_stats(const unsigned long long* 
     return acc;
 }
 
+// One sequence's scan by a group of nt threads (thread tid of them): the draft tokens and
+// their logits, the acceptance uniforms, every row's merged statistics, the accept tests and
+// the first rejection.  Split in two so that the inputs-only part can run before the
+// statistics are complete: scan_prologue (positions i = tid < min(nt, kScanFast) gathered
+// into shared memory), then, after the group's barrier, scan_sequence.
+constexpr int kScanFast = 256;  // positions gathered ahead by the prologue, at most
+
+struct ScanShared {
+    int j, bad;
+    int d[kScanFast];
+    float xt[kScanFast], xd[kScanFast], u[kScanFast];
+};
+
+template <class ET>
+__device__ __forceinline__ void scan_prologue(const VerifyParams& p, int b, int tid, ScanShared& sh) {
+    using S = typename ET::storage;
+    const uint32_t bg = p.seq_base + static_cast<uint32_t>(b);
+    const int i0 = tid;
+    if (i0 < p.gamma && i0 < kScanFast) {
+        const int d = p.tokens[static_cast<long long>(b) * p.gamma + i0];
+        sh.d[i0] = d;
+        sh.u[i0] = accept_uniform(p.key, bg, static_cast<uint32_t>(i0));
+        float xt = 0.0f, xd = 0.0f;
+        const long long kt = (static_cast<long long>(b) * (p.gamma + 1) + i0) * p.V + d;
+        const long long kd = (static_cast<long long>(b) * p.gamma + i0) * p.V + d;
+        if (d >= 0 && d < p.V && sv_in_range(p, kt, p.caps.target) && sv_in_range(p, kd, p.caps.draft)) {
+            xt = ET::load1(static_cast<const S*>(p.target) + kt);
+            xd = ET::load1(static_cast<const S*>(p.draft) + kd);
+        }
+        sh.xt[i0] = xt;
+        sh.xd[i0] = xd;
+    }
+    if (tid == 0) {
+        sh.j = p.gamma;
+        sh.bad = 0;
+    }
+}
+
+// The rest of the scan, after the prologue and a barrier: returns the first rejection j
+// (gamma: all accepted; -1: a draft token outside [0, V)), with every row's scaled max and
+// log2 sum in sm_m / sm_l.  The writer group also writes the sequence's outputs (n_accepted,
+// the accepted prefix and the -1 padding; the drawn token is the race's) and diagnostics.
+template <class ET, class Sync>
+__device__ __forceinline__ int scan_sequence(const VerifyParams& p, int b, bool writer, int tid, int nt,
+                                             ScanShared& sh, float* sm_m, float* sm_l, Sync sync) {
+    using S = typename ET::storage;
+    const int R = 2 * p.gamma + 1;
+    const int nfast = min(nt, kScanFast);
+    const float cp = scale_of(seq_T(p, b)), cq = scale_of(seq_Td(p, b));
+    const uint32_t bg = p.seq_base + static_cast<uint32_t>(b);
+    // any draft token outside [0, V) marks the whole sequence
+    for (int i = tid; i < p.gamma; i += nt) {
+        const int d = (i < nfast) ? sh.d[i] : p.tokens[static_cast<long long>(b) * p.gamma + i];
+        if (d < 0 || d >= p.V) sh.bad = 1;
+    }
+    auto decide = [&](int i) {  // one thread: the accept test at position i
+        int d;
+        float xt, xd, u;
+        if (i < nfast) {
+            d = sh.d[i]; xt = sh.xt[i]; xd = sh.xd[i]; u = sh.u[i];
+        } else {
+            d = p.tokens[static_cast<long long>(b) * p.gamma + i];
+            u = accept_uniform(p.key, bg, static_cast<uint32_t>(i));
+            const long long kt = (static_cast<long long>(b) * (p.gamma + 1) + i) * p.V + d;
+            const long long kd = (static_cast<long long>(b) * p.gamma + i) * p.V + d;
+            xt = sv_in_range(p, kt, p.caps.target) ? ET::load1(static_cast<const S*>(p.target) + kt) : 0.0f;
+            xd = sv_in_range(p, kd, p.caps.draft) ? ET::load1(static_cast<const S*>(p.draft) + kd) : 0.0f;
+        }
+        const long long k = static_cast<long long>(b) * p.gamma + i;
+        if (writer && p.out_u) p.out_u[k] = u;
+        const float l2p = fmaf(xt, cp, -sm_m[i]) - sm_l[i];
+        const float l2q = fmaf(xd, cq, -sm_m[p.gamma + 1 + i]) - sm_l[p.gamma + 1 + i];
+        if (writer && p.out_logp) p.out_logp[k] = l2p * kLn2;
+        if (writer && p.out_logq) p.out_logq[k] = l2q * kLn2;
+        // accept iff u < min(1, p/q); p(d) = 0 rejects, q(d) = 0 < p(d) accepts
+        if (!((l2p > -INFINITY) && (u < exp2f(l2p - l2q)))) atomicMin(&sh.j, i);
+    };
+    // every row's statistics, one thread per row (fold_row_stats: the order every schedule
+    // uses); rows past the first rejection decide nothing but cost one L2 read per partial
+    const unsigned long long* parts =
+        reinterpret_cast<const unsigned long long*>(p.stat_parts) + static_cast<long long>(b) * R * p.npieces;
+    for (int r = tid; r < R; r += nt) {
+        const long long pbase = (static_cast<long long>(b) * R + r) * p.npieces;
+        const SoftmaxStat st = sv_span_in_range(p, pbase, p.npieces, p.caps.stat)
+            ? fold_row_stats(parts + static_cast<long long>(r) * p.npieces, p.npieces)
+            : SoftmaxStat{-FLT_MAX, 1.0f};
+        const float l2s = log2f(st.s);
+        sm_m[r] = st.m;
+        sm_l[r] = l2s;
+        if (writer) {
+            const float lz = (st.m + l2s) * kLn2;
+            if (r <= p.gamma) {
+                if (p.out_logZp) p.out_logZp[static_cast<long long>(b) * (p.gamma + 1) + r] = lz;
+            } else if (p.out_logZq) {
+                p.out_logZq[static_cast<long long>(b) * p.gamma + (r - p.gamma - 1)] = lz;
+            }
+        }
+    }
+    sync();
+    if (sh.bad) {
+        if (writer) {
+            for (int i = tid; i < p.gamma; i += nt) {
+                const long long k = static_cast<long long>(b) * p.gamma + i;
+                if (p.out_u) p.out_u[k] = accept_uniform(p.key, bg, static_cast<uint32_t>(i));
+                if (p.out_logp) p.out_logp[k] = NAN;
+                if (p.out_logq) p.out_logq[k] = NAN;
+            }
+        }
+    } else {
+        for (int i = tid; i < p.gamma; i += nt) decide(i);
+    }
+    sync();
+    const int j = sh.bad ? -1 : sh.j;
+    if (writer) {
+        if (tid == 0) {
+            p.out_n[b] = j;
+            if (j < 0) set_status(p.status, 3 /* SPEC_EBADTOKEN */);
+        }
+        int32_t* out = p.out_tokens + static_cast<long long>(b) * (p.gamma + 1);
+        if (sv_span_in_range(p, static_cast<long long>(b) * (p.gamma + 1), p.gamma + 1, p.caps.out_tokens))
+            for (int t = tid; t <= p.gamma; t += nt)
+                if (t != j) out[t] = (j >= 0 && t < j) ? p.tokens[static_cast<long long>(b) * p.gamma + t] : -1;
+    }
+    return j;
+}
+
+// The statistics of sequence b's raced row j (target row j and, for a residual, draft row
+// j) from the scan's shared row statistics.
+__device__ __forceinline__ SeqInfo raced_row_info(const VerifyParams& p, int b, int j, const float* sm_m,
+                                                  const float* sm_l) {
+    SeqInfo si;
+    si.j = j;
+    si.cp = scale_of(seq_T(p, b));
+    si.cq = scale_of(seq_Td(p, b));
+    si.mp = sm_m[j];
+    si.l2sp = sm_l[j];
+    const bool residual = j < p.gamma;
+    si.mq = residual ? sm_m[p.gamma + 1 + j] : 0.0f;
+    si.l2sq = residual ? sm_l[p.gamma + 1 + j] : 0.0f;
+    si.pad = 0;
+    return si;
+}
+
 template <class ET>
 __global__ void __launch_bounds__(256, SPECVERIFY_RACE_MINBLOCKS) scan_race_kernel(VerifyParams p) {
-    using S = typename ET::storage;
     extern __shared__ float smem[];  // [2R]: scaled max and log2 sum of every row
-    __shared__ int s_j, s_bad, s_last;
+    __shared__ int s_last;
     __shared__ float s_thr[8];
     __shared__ RaceState s_best[8];
-    __shared__ int s_d[256];
-    __shared__ float s_xt[256], s_xd[256], s_u[256];
+    __shared__ ScanShared sh;
     const int R = 2 * p.gamma + 1;
     float* sm_m = smem;
     float* sm_l = smem + R;
+    auto sync = [] { __syncthreads(); };
     // This block's race chunks (kRaceWarpTokens tokens each), in one of two layouts:
     //   G = p.rgroups > 0: G blocks per sequence, block g racing steps g, g + G, ... of its
     //     sequence's row (a step: one chunk per warp); every block scans one sequence;
@@ -1468,124 +1613,20 @@ __global__ void __launch_bounds__(256, SPECVERIFY_RACE_MINBLOCKS) scan_race_kern
             cb_end = ch_limit = ch1;
             cb_step = kRaceBlockChunks;
         }
-        const bool writer = (slot == 0);  // writes the sequence's outputs
-        const float cp = scale_of(seq_T(p, b)), cq = scale_of(seq_Td(p, b));
-        const uint32_t bg = p.seq_base + static_cast<uint32_t>(b);
-        // inputs-only prologue (position i = threadIdx.x): the first sequence's overlaps the
-        // streaming pass's tail
-        const int i0 = threadIdx.x;
-        if (i0 < p.gamma) {
-            const int d = p.tokens[static_cast<long long>(b) * p.gamma + i0];
-            s_d[i0] = d;
-            s_u[i0] = accept_uniform(p.key, bg, static_cast<uint32_t>(i0));
-            float xt = 0.0f, xd = 0.0f;
-            const long long kt = (static_cast<long long>(b) * (p.gamma + 1) + i0) * p.V + d;
-            const long long kd = (static_cast<long long>(b) * p.gamma + i0) * p.V + d;
-            if (d >= 0 && d < p.V && sv_in_range(p, kt, p.caps.target) && sv_in_range(p, kd, p.caps.draft)) {
-                xt = ET::load1(static_cast<const S*>(p.target) + kt);
-                xd = ET::load1(static_cast<const S*>(p.draft) + kd);
-            }
-            s_xt[i0] = xt;
-            s_xd[i0] = xd;
-        }
-        if (threadIdx.x == 0) {
-            s_j = p.gamma;
-            s_bad = 0;
-        }
+        // inputs-only prologue: the first sequence's overlaps the streaming pass's tail
+        scan_prologue<ET>(p, b, threadIdx.x, sh);
         if (first) {
             asm volatile("griddepcontrol.wait;" ::: "memory");
             // a following verify's streaming pass may be set up now: it waits for this grid
             asm volatile("griddepcontrol.launch_dependents;");
         }
         first = false;
-        __syncthreads();  // s_j and s_bad are set before any thread reports a bad token
-        // any draft token outside [0, V) marks the whole sequence
-        for (int i = threadIdx.x; i < p.gamma; i += blockDim.x) {
-            const int d = (i < 256) ? s_d[i] : p.tokens[static_cast<long long>(b) * p.gamma + i];
-            if (d < 0 || d >= p.V) s_bad = 1;
-        }
-        auto decide = [&](int i) {  // one thread: the accept test at position i
-            int d;
-            float xt, xd, u;
-            if (i < 256) {
-                d = s_d[i]; xt = s_xt[i]; xd = s_xd[i]; u = s_u[i];
-            } else {
-                d = p.tokens[static_cast<long long>(b) * p.gamma + i];
-                u = accept_uniform(p.key, bg, static_cast<uint32_t>(i));
-                const long long kt = (static_cast<long long>(b) * (p.gamma + 1) + i) * p.V + d;
-                const long long kd = (static_cast<long long>(b) * p.gamma + i) * p.V + d;
-                xt = sv_in_range(p, kt, p.caps.target) ? ET::load1(static_cast<const S*>(p.target) + kt) : 0.0f;
-                xd = sv_in_range(p, kd, p.caps.draft) ? ET::load1(static_cast<const S*>(p.draft) + kd) : 0.0f;
-            }
-            const long long k = static_cast<long long>(b) * p.gamma + i;
-            if (writer && p.out_u) p.out_u[k] = u;
-            const float l2p = fmaf(xt, cp, -sm_m[i]) - sm_l[i];
-            const float l2q = fmaf(xd, cq, -sm_m[p.gamma + 1 + i]) - sm_l[p.gamma + 1 + i];
-            if (writer && p.out_logp) p.out_logp[k] = l2p * kLn2;
-            if (writer && p.out_logq) p.out_logq[k] = l2q * kLn2;
-            // accept iff u < min(1, p/q); p(d) = 0 rejects, q(d) = 0 < p(d) accepts
-            if (!((l2p > -INFINITY) && (u < exp2f(l2p - l2q)))) atomicMin(&s_j, i);
-        };
-        // every row's statistics, one thread per row (fold_row_stats: the order every schedule
-        // uses); rows past the first rejection decide nothing but cost one L2 read per partial
-        const unsigned long long* parts =
-            reinterpret_cast<const unsigned long long*>(p.stat_parts) + static_cast<long long>(b) * R * p.npieces;
-        for (int r = threadIdx.x; r < R; r += blockDim.x) {
-            const long long pbase = (static_cast<long long>(b) * R + r) * p.npieces;
-            const SoftmaxStat st = sv_span_in_range(p, pbase, p.npieces, p.caps.stat)
-                ? fold_row_stats(parts + static_cast<long long>(r) * p.npieces, p.npieces)
-                : SoftmaxStat{-FLT_MAX, 1.0f};
-            const float l2s = log2f(st.s);
-            sm_m[r] = st.m;
-            sm_l[r] = l2s;
-            if (writer) {
-                const float lz = (st.m + l2s) * kLn2;
-                if (r <= p.gamma) {
-                    if (p.out_logZp) p.out_logZp[static_cast<long long>(b) * (p.gamma + 1) + r] = lz;
-                } else if (p.out_logZq) {
-                    p.out_logZq[static_cast<long long>(b) * p.gamma + (r - p.gamma - 1)] = lz;
-                }
-            }
-        }
-        __syncthreads();
-        if (s_bad) {
-            if (writer) {
-                for (int i = threadIdx.x; i < p.gamma; i += blockDim.x) {
-                    const long long k = static_cast<long long>(b) * p.gamma + i;
-                    if (p.out_u) p.out_u[k] = accept_uniform(p.key, bg, static_cast<uint32_t>(i));
-                    if (p.out_logp) p.out_logp[k] = NAN;
-                    if (p.out_logq) p.out_logq[k] = NAN;
-                }
-            }
-        } else {
-            for (int i = threadIdx.x; i < p.gamma; i += blockDim.x) decide(i);
-        }
-        __syncthreads();
-        const int j = s_bad ? -1 : s_j;
-        if (writer) {
-            if (threadIdx.x == 0) {
-                p.out_n[b] = j;
-                if (j < 0) set_status(p.status, 3 /* SPEC_EBADTOKEN */);
-            }
-            int32_t* out = p.out_tokens + static_cast<long long>(b) * (p.gamma + 1);
-            if (sv_span_in_range(p, static_cast<long long>(b) * (p.gamma + 1), p.gamma + 1, p.caps.out_tokens))
-                for (int t = threadIdx.x; t <= p.gamma; t += blockDim.x)
-                    if (t != j) out[t] = (j >= 0 && t < j) ? p.tokens[static_cast<long long>(b) * p.gamma + t] : -1;
-        }
-        if (j >= 0) {
-            SeqInfo si;
-            si.j = j;
-            si.cp = cp;
-            si.cq = cq;
-            si.mp = sm_m[j];
-            si.l2sp = sm_l[j];
-            const bool residual = j < p.gamma;
-            si.mq = residual ? sm_m[p.gamma + 1 + j] : 0.0f;
-            si.l2sq = residual ? sm_l[p.gamma + 1 + j] : 0.0f;
-            si.pad = 0;
-            race_sequence_block<ET>(p, b, cb_begin, cb_end, cb_step, ch_limit, slot, nslots, si, s_thr,
-                                    s_best, s_last);
-        }
+        __syncthreads();  // sh.j and sh.bad are set before any thread reports a bad token
+        const int j = scan_sequence<ET>(p, b, slot == 0, threadIdx.x, blockDim.x, sh, sm_m, sm_l, sync);
+        if (j >= 0)
+            race_sequence_block<ET, 8>(p, b, cb_begin, cb_end, cb_step, ch_limit, slot, nslots,
+                                       raced_row_info(p, b, j, sm_m, sm_l), s_thr, s_best, s_last,
+                                       static_cast<int>(threadIdx.x >> 5), sync);
         if (q < q1) __syncthreads();  // before the next sequence reuses shared memory
     }
 }
@@ -1846,10 +1887,10 @@ __global__ void __launch_bounds__(256, SPECVERIFY_RACE_MINBLOCKS) tree_race_kern
     const S* rt = static_cast<const S*>(p.target) + (static_cast<long long>(b) * N + tr.node) * p.V;
     const S* rd = tr.residual ? static_cast<const S*>(p.draft) + (static_cast<long long>(b) * M + tr.drow) * p.V
                               : nullptr;
-    race_rows_block<ET>(p, b, rt, rd, tr.residual != 0, static_cast<uint32_t>(tr.node),
-                        p.out_tokens + static_cast<long long>(b) * (D + 1) + tr.k, g * kRaceBlockChunks,
-                        p.rpieces * kRaceBlockChunks, G * kRaceBlockChunks, INT_MAX, g, G, si, s_thr,
-                        s_best, s_last);
+    race_rows_block<ET, 8>(p, b, rt, rd, tr.residual != 0, static_cast<uint32_t>(tr.node),
+                           p.out_tokens + static_cast<long long>(b) * (D + 1) + tr.k, g * kRaceBlockChunks,
+                           p.rpieces * kRaceBlockChunks, G * kRaceBlockChunks, INT_MAX, g, G, si, s_thr,
+                           s_best, s_last, static_cast<int>(threadIdx.x >> 5), [] { __syncthreads(); });
 }
 
 __device__ __forceinline__ int ld_acquire(const int* p) {

@@ -46,10 +46,6 @@ constexpr uint32_t kGemmIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
                                 (static_cast<uint32_t>(kGemmBN >> 3) << 17) |
                                 (static_cast<uint32_t>(kGemmBM >> 4) << 24);
 
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
 // Shared-memory matrix descriptor of a K-major tile stored as TMA writes it with the
 // 128-byte swizzle: rows of 128 bytes, 8-row (1024-byte) swizzle atoms.  Start address
 // >> 4 in bits 0-13, leading-byte offset (unused by this layout) 1 in bits 16-29, stride
@@ -59,31 +55,6 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
     return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1) << 16) |
            (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
            (static_cast<uint64_t>(2) << 61);
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
 }
 
 // Bounded wait for the phase of the given parity to complete; false after kWaitLimitNs or
@@ -523,12 +494,13 @@ __global__ void __launch_bounds__(256, SPECVERIFY_RACE_MINBLOCKS) lmhead_race_ke
     const SeqInfo si = p.seq[b];
     if (si.j < 0) return;
     const bool residual = si.j < p.gamma;
-    race_rows_block<F32Elem>(p, b, lt + static_cast<long long>(b) * p.V,
-                             residual ? ld + static_cast<long long>(b) * p.V : nullptr, residual,
-                             static_cast<uint32_t>(si.j),
-                             p.out_tokens + static_cast<long long>(b) * (p.gamma + 1) + si.j,
-                             g * kRaceBlockChunks, p.rpieces * kRaceBlockChunks, G * kRaceBlockChunks,
-                             INT_MAX, g, G, si, s_thr, s_best, s_last);
+    race_rows_block<F32Elem, 8>(p, b, lt + static_cast<long long>(b) * p.V,
+                                residual ? ld + static_cast<long long>(b) * p.V : nullptr, residual,
+                                static_cast<uint32_t>(si.j),
+                                p.out_tokens + static_cast<long long>(b) * (p.gamma + 1) + si.j,
+                                g * kRaceBlockChunks, p.rpieces * kRaceBlockChunks, G * kRaceBlockChunks,
+                                INT_MAX, g, G, si, s_thr, s_best, s_last, static_cast<int>(threadIdx.x >> 5),
+                                [] { __syncthreads(); });
 }
 
 }  // namespace specverify

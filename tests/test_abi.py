@@ -132,7 +132,7 @@ def test_host_validation_rejects_bad_sizes_without_a_device(lib):
     assert lib.spec_verify_ex(fake, fake, fake, 1, 3, 10, 1.0, 1.0, 0, fake, fake,
                               ctypes.byref(opts), None) == EINVAL
     # unknown flag bits (bit 0, once a schedule that was removed, included)
-    for bad in (1, 16, 1 << 31):
+    for bad in (1, 32, 1 << 31):
         opts.dtype = sv.SPEC_BF16
         opts.flags = bad
         assert lib.spec_verify_ex(fake, fake, fake, 1, 3, 10, 1.0, 1.0, 0, fake, fake,
