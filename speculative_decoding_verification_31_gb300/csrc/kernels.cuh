@@ -947,25 +947,32 @@ __device__ __noinline__ float race_exact_score(float xt, float xd, SeqInfo si, b
 // The margin (in log2 units) is far above the fp32 error of the exact score.
 constexpr float kRaceBoundMargin2 = 1e-3f;
 
-// Candidate bits of one 16-byte vector of logits ft (ET::kVec tokens) with their Philox
-// words in blk[0 .. kVec/4): token e passes iff lg2(w_e) <= ft[e] cp + C.  The vector is
-// first tested as a whole -- its smallest word against its largest logit, a necessary
-// condition for any of its tokens up to kVectorTestMargin (which covers lg2.approx not being
-// exactly monotone) -- and the tokens one by one only when that passes, which is rare.
+// A vector of tokens is first tested as a whole (vector_may_win), and its tokens one by one
+// (token_candidates) only when that passes, which is rare.
 constexpr float kVectorTestMargin = 1e-3f;
 
+// The coarse test of one 16-byte vector `raw` (ET::kVec logits) whose Philox words are
+// blk[0 .. kVec/4): false when no token of the vector can pass the bound, i.e. when its
+// smallest word fails against its largest logit (a necessary condition, up to
+// kVectorTestMargin, which covers lg2.approx not being exactly monotone).  Straight-line
+// code, so that the tests of a group of vectors overlap; it fails for all but a few vectors
+// in a thousand.
 template <class ET>
-__device__ __forceinline__ uint32_t vector_candidates(const float (&ft)[ET::kVec], const uint4* blk,
-                                                      float cp, float C) {
+__device__ __forceinline__ bool vector_may_win(const uint4& raw, const uint4* blk, float cp, float C) {
     constexpr int BPV = ET::kVec / 4;
     uint32_t wmin = 0xffffffffu;
-    float xmax = ft[0];
 #pragma unroll
     for (int gg = 0; gg < BPV; ++gg)
         wmin = min(wmin, min(min(blk[gg].x, blk[gg].y), min(blk[gg].z, blk[gg].w)));
-#pragma unroll
-    for (int e = 1; e < ET::kVec; ++e) xmax = fmaxf(xmax, ft[e]);
-    if (!(lg2_fast(static_cast<float>(wmin)) - kVectorTestMargin <= fmaf(xmax, cp, C))) return 0u;
+    return lg2_fast(static_cast<float>(wmin)) - kVectorTestMargin <= fmaf(ET::vmax(raw), cp, C);
+}
+
+// The tokens of one vector (logits ft, Philox words blk) that pass the bound, as bits:
+// token e passes iff lg2(w_e) <= ft[e] cp + C.
+template <class ET>
+__device__ __forceinline__ uint32_t token_candidates(const float (&ft)[ET::kVec], const uint4* blk, float cp,
+                                                     float C) {
+    constexpr int BPV = ET::kVec / 4;
     uint32_t cand = 0;
 #pragma unroll
     for (int gg = 0; gg < BPV; ++gg) {
@@ -1075,29 +1082,29 @@ __device__ __forceinline__ RaceState race_piece(const typename ET::storage* rt,
             for (int g = 0; g < ET::kVec / 4; ++g)
                 blk[k][g] = race_block_fast(
                     q, rk, static_cast<uint32_t>(xb + (v0 + lane + 32 * k) * ET::kVec + 4 * g) >> 2);
-        // candidate bits: token e of vector k passes the bound
-        uint32_t cand = 0;
+        // each vector's coarse test, then (rarely) its tokens, scored exactly in increasing
+        // token order
+        bool coarse[kRaceBatch];
+        bool any = false;
 #pragma unroll
         for (int k = 0; k < kRaceBatch; ++k) {
-            const int v = v0 + lane + 32 * k;
-            float ft[ET::kVec];
-            ET::widen(raw[k], ft);
+            coarse[k] = v0 + lane + 32 * k < sp.nvec && vector_may_win<ET>(raw[k], blk[k], si.cp, C);
+            any |= coarse[k];
+        }
+        if (any) {
 #pragma unroll
-            for (int g = 0; g < ET::kVec / 4; ++g) {
-                const uint32_t w4[4] = {blk[k][g].x, blk[k][g].y, blk[k][g].z, blk[k][g].w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const bool pass = lg2_fast(static_cast<float>(w4[e])) <= fmaf(ft[4 * g + e], si.cp, C);
-                    cand |= (pass && v < sp.nvec) ? (1u << (k * ET::kVec + 4 * g + e)) : 0u;
+            for (int k = 0; k < kRaceBatch; ++k) {
+                if (!coarse[k]) continue;
+                float ft[ET::kVec];
+                ET::widen(raw[k], ft);
+                uint32_t cand = token_candidates<ET>(ft, blk[k], si.cp, C);
+                while (cand) {
+                    const int e = __ffs(cand) - 1;
+                    cand &= cand - 1;
+                    const int x = xb + (v0 + lane + 32 * k) * ET::kVec + e;
+                    offer_exact(ET::load1(rt + x), x, word_at(x));  // recomputed: no indexed registers
                 }
             }
-        }
-        while (cand) {  // rare: score the candidates exactly, in increasing token order
-            const int bit = __ffs(cand) - 1;
-            cand &= cand - 1;
-            const int k = bit / ET::kVec, e = bit % ET::kVec;
-            const int x = xb + (v0 + lane + 32 * k) * ET::kVec + e;
-            offer_exact(ET::load1(rt + x), x, word_at(x));  // recomputed: no indexed registers
         }
         thr = fmaxf(thr, float_unorder(__reduce_max_sync(0xffffffffu, float_order(st.best))));
     }
@@ -1287,18 +1294,29 @@ __device__ __forceinline__ void race_rows_block(const VerifyParams& p, int b,
                     for (int gg = 0; gg < BPV; ++gg)
                         blk[kk * BPV + gg] = race_block_fast(
                             q, p.rk, static_cast<uint32_t>(x0 + (lane + 32 * (k0 + kk)) * ET::kVec + 4 * gg) >> 2);
+                // every vector's coarse test first, then (rarely) its tokens, scored exactly in
+                // increasing token order
+                bool coarse[VG];
+                bool any = false;
 #pragma unroll
                 for (int kk = 0; kk < VG; ++kk) {
-                    const int v = lane + 32 * (k0 + kk);
-                    if (v >= nvec) continue;
-                    float ft[ET::kVec];
-                    ET::widen(raw[k0 + kk], ft);
-                    const int xv = x0 + v * ET::kVec;
-                    uint32_t cand = vector_candidates<ET>(ft, blk + kk * BPV, si.cp, C);
-                    while (cand) {  // rare: exact scores in increasing token order
-                        const int e = __ffs(cand) - 1;
-                        cand &= cand - 1;
-                        offer_exact(ET::load1(rt + xv + e), xv + e, word_at(xv + e));
+                    coarse[kk] = lane + 32 * (k0 + kk) < nvec &&
+                                 vector_may_win<ET>(raw[k0 + kk], blk + kk * BPV, si.cp, C);
+                    any |= coarse[kk];
+                }
+                if (any) {
+#pragma unroll
+                    for (int kk = 0; kk < VG; ++kk) {
+                        if (!coarse[kk]) continue;
+                        float ft[ET::kVec];
+                        ET::widen(raw[k0 + kk], ft);
+                        const int xv = x0 + (lane + 32 * (k0 + kk)) * ET::kVec;
+                        uint32_t cand = token_candidates<ET>(ft, blk + kk * BPV, si.cp, C);
+                        while (cand) {
+                            const int e = __ffs(cand) - 1;
+                            cand &= cand - 1;
+                            offer_exact(ET::load1(rt + xv + e), xv + e, word_at(xv + e));
+                        }
                     }
                 }
                 thr = fmaxf(thr, float_unorder(__reduce_max_sync(0xffffffffu, float_order(st.best))));

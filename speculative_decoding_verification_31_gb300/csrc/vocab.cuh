@@ -118,18 +118,29 @@ __device__ __forceinline__ RaceState race_warp_span(const VerifyParams& p,
                         blk[kk * BPV + gg] = race_block_fast(
                             q, p.rk,
                             static_cast<uint32_t>(xoff + x0 + (lane + 32 * (k0 + kk)) * ET::kVec + 4 * gg) >> 2);
+                // every vector's coarse test first, then (rarely) its tokens, scored exactly in
+                // increasing token order
+                bool coarse[VG];
+                bool any = false;
 #pragma unroll
                 for (int kk = 0; kk < VG; ++kk) {
-                    const int v = lane + 32 * (k0 + kk);
-                    if (v >= nvec) continue;
-                    float ft[ET::kVec];
-                    ET::widen(raw[k0 + kk], ft);
-                    const int xv = x0 + v * ET::kVec;
-                    uint32_t cand = vector_candidates<ET>(ft, blk + kk * BPV, si.cp, C);
-                    while (cand) {  // rare: exact scores in increasing token order
-                        const int e = __ffs(cand) - 1;
-                        cand &= cand - 1;
-                        offer_exact(ET::load1(rt + xv + e), xv + e, word_at(xv + e));
+                    coarse[kk] = lane + 32 * (k0 + kk) < nvec &&
+                                 vector_may_win<ET>(raw[k0 + kk], blk + kk * BPV, si.cp, C);
+                    any |= coarse[kk];
+                }
+                if (any) {
+#pragma unroll
+                    for (int kk = 0; kk < VG; ++kk) {
+                        if (!coarse[kk]) continue;
+                        float ft[ET::kVec];
+                        ET::widen(raw[k0 + kk], ft);
+                        const int xv = x0 + (lane + 32 * (k0 + kk)) * ET::kVec;
+                        uint32_t cand = token_candidates<ET>(ft, blk + kk * BPV, si.cp, C);
+                        while (cand) {
+                            const int e = __ffs(cand) - 1;
+                            cand &= cand - 1;
+                            offer_exact(ET::load1(rt + xv + e), xv + e, word_at(xv + e));
+                        }
                     }
                 }
                 thr = fmaxf(thr, float_unorder(__reduce_max_sync(0xffffffffu, float_order(st.best))));
