@@ -46,7 +46,7 @@ UNIT = "rows/s"
 # summarised in profiles/ (dram__bytes_read.sum + dram__bytes_write.sum), with the hash of
 # the code it was taken on (the element types and the row-statistics kernel with the piece
 # choice and the helpers it calls); reported as null once that code has changed.
-NCU_TRAFFIC = {"bytes": 1949598976, "sources_sha1": "04b60e7b82fb1981ff16a549dda3ed505cf1ad53"}
+NCU_TRAFFIC = {"bytes": 1949289984, "sources_sha1": "69e434eed7294eb40b8644960bd4653e31430da5"}
 ROW_STATS_SPAN = ("inline int pick_piece_len(", "// Per-position entropies and KL divergence")
 
 
@@ -750,9 +750,11 @@ def run_lmhead(sv, dev, B, gamma, V, d, steps=10):
 
 
 def run_table(args):
-    """Every named workload, both sampling paths (fused single kernel, three kernels) and the
-    greedy mode, as a table on stderr.  Workloads smaller than twice L2 are timed twice: on
-    one resident copy (warm L2) and rotating over enough copies to exceed twice L2 (cold)."""
+    """Every named workload -- the default sampling call, the early-exit call, the call with
+    per-position statistics, and the greedy mode -- then the token trees and the verify from
+    hidden states, as a table on stderr (calls issued from Python, CUDA events).  Workloads
+    smaller than twice L2 are timed twice: on one resident copy (warm L2) and rotating over
+    enough copies to exceed twice L2 (cold)."""
     import torch
     import workloads
     import speculative_decoding_verification_31_gb300 as sv
@@ -935,7 +937,7 @@ def main():
                     help="time the verify from hidden states (fused LM head) only, to stderr")
     ap.add_argument("--lm-steps", type=int, default=10)
     ap.add_argument("--all", action="store_true",
-                    help="print a per-workload table (both sampling paths, greedy) to stderr")
+                    help="print a per-workload table (every path, trees, LM head) to stderr")
     ap.add_argument("--no-sustained", action="store_true")
     ap.add_argument("--sustained-seconds", type=float, default=1.2)
     ap.add_argument("--no-per-config", action="store_true")

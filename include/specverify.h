@@ -249,7 +249,7 @@ const char *spec_verify_strerror(int status);
  * the problem exceeds SPEC_NOALLOC_SCRATCH_BYTES - 256; otherwise as spec_verify_ex.
  */
 #define SPEC_NOALLOC_SCRATCH_BYTES (8u << 20) /* 8 MiB: B=256, gamma=12, V=152064 bf16 needs
-                                                 6.6 MB */
+                                                 6.1 MB */
 int spec_verify_noalloc(const void *target_logits, const void *draft_logits,
                         const int32_t *draft_tokens, int B, int gamma, int V, float T, float T_d,
                         uint64_t seed, int32_t *out_tokens, int32_t *out_n_accepted,
