@@ -196,6 +196,37 @@ constexpr uint32_t kKnownFlags = SPEC_DEBUG_NEVER_READY | SPEC_FLAG_EARLY_EXIT |
 
 bool good_temperature(float t) { return std::isfinite(t) && t > 0.0f; }
 
+// Resident blocks per SM of `kernel` at `threads` threads and `smem` bytes of dynamic shared
+// memory on the current device, or 0 if the query fails.  The answer cannot change within a
+// process, and the query costs host microseconds on every call, so each (device, kernel,
+// threads, smem) is queried once and kept.
+struct OccupancyEntry {
+    int dev, threads, value;
+    const void* fn;
+    size_t smem;
+};
+std::mutex g_occ_mu;
+OccupancyEntry g_occ[64];
+int g_occ_n = 0;
+
+template <class K>
+int blocks_per_sm(K kernel, int threads, size_t smem) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const void* fn = reinterpret_cast<const void*>(kernel);
+    std::lock_guard<std::mutex> lock(g_occ_mu);
+    for (int i = 0; i < g_occ_n; ++i)
+        if (g_occ[i].fn == fn && g_occ[i].dev == dev && g_occ[i].threads == threads && g_occ[i].smem == smem)
+            return g_occ[i].value;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    if (g_occ_n < 64) g_occ[g_occ_n++] = OccupancyEntry{dev, threads, per_sm, fn, smem};
+    return per_sm;
+}
+
 // Launch of a streaming kernel: one block of kStreamThreads per SM (the claiming variant kc,
 // whose warps share the block's items) when the items outnumber the warps of that grid;
 // otherwise blocks of kThreads of the plain variant kp, one item per warp, so that a small
@@ -205,10 +236,8 @@ bool good_temperature(float t) { return std::isfinite(t) && t > 0.0f; }
 // last kernel drains.
 template <class KC, class KP, class... A>
 cudaError_t launch_stream(KC kc, KP kp, int sm_count, long long items, cudaStream_t s, A... args) {
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kc, kStreamThreads, 0) != cudaSuccess ||
-        per_sm < 1)
-        per_sm = 1;
+    int per_sm = blocks_per_sm(kc, kStreamThreads, 0);
+    if (per_sm < 1) per_sm = 1;
     const long long full = static_cast<long long>(sm_count) * per_sm;
     cudaLaunchConfig_t cfg = {};
     cfg.stream = s;
@@ -232,11 +261,9 @@ cudaError_t launch_stream(KC kc, KP kp, int sm_count, long long items, cudaStrea
 
 // Warps of the streaming kernel's full grid.
 long long stream_warps_of(int sm_count, int dtype) {
-    int per_sm = 0;
-    cudaError_t e = dtype == SPEC_F32
-        ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, row_stats_kernel<F32Elem, kUnroll, true>, kStreamThreads, 0)
-        : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, row_stats_kernel<Bf16Elem, kUnroll, true>, kStreamThreads, 0);
-    if (e != cudaSuccess || per_sm < 1) per_sm = 1;
+    int per_sm = dtype == SPEC_F32 ? blocks_per_sm(row_stats_kernel<F32Elem, kUnroll, true>, kStreamThreads, 0)
+                                   : blocks_per_sm(row_stats_kernel<Bf16Elem, kUnroll, true>, kStreamThreads, 0);
+    if (per_sm < 1) per_sm = 1;
     return static_cast<long long>(sm_count) * per_sm * (kStreamThreads / 32);
 }
 
@@ -349,10 +376,8 @@ int launch_sampling(VerifyParams& p, int sm_count, const spec_verify_opts* o, cu
     record(o, 0, s);
     if (extra) {  // the same read of every logit, paired by position, with the extra terms
         // pieces chosen for this pass's items (position pairs, not rows) and grid
-        int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pair_stats_kernel<ET, kPairUnroll, true>,
-                                                          kStreamThreads, 0) != cudaSuccess || per_sm < 1)
-            per_sm = 1;
+        int per_sm = blocks_per_sm(pair_stats_kernel<ET, kPairUnroll, true>, kStreamThreads, 0);
+        if (per_sm < 1) per_sm = 1;
         p.piece_len = pick_piece_len(static_cast<long long>(p.B) * (p.gamma + 1), p.V,
                                      static_cast<int>(sizeof(typename ET::storage)),
                                      static_cast<long long>(sm_count) * per_sm * (kStreamThreads / 32));
@@ -374,11 +399,8 @@ int launch_sampling(VerifyParams& p, int sm_count, const spec_verify_opts* o, cu
     // sequences alone fill the wave)
     long long grid;
     {
-        int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, scan_race_kernel<ET>, kThreads,
-                                                          2 * R * sizeof(float)) != cudaSuccess ||
-            per_sm < 1)
-            per_sm = 1;
+        int per_sm = blocks_per_sm(scan_race_kernel<ET>, kThreads, 2 * R * sizeof(float));
+        if (per_sm < 1) per_sm = 1;
         const long long wave = static_cast<long long>(sm_count) * per_sm;
         const long long steps = static_cast<long long>(p.B) * ((p.V + kRaceWarpTokens - 1) / kRaceWarpTokens) /
                                 kRaceBlockChunks;
@@ -413,10 +435,8 @@ template <class ET>
 int launch_early(VerifyParams& p, int sm_count, const spec_verify_opts* o, cudaStream_t s,
                  const Layout& L, char* ws, bool host_rows) {
     auto kernel = verify_early_kernel<ET, kEarlyUnroll>;
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) != cudaSuccess ||
-        per_sm < 1)
-        return SPEC_ECUDA;
+    const int per_sm = blocks_per_sm(kernel, kThreads, 0);
+    if (per_sm < 1) return SPEC_ECUDA;
     const int R = 2 * p.gamma + 1;
     const long long row_warps = static_cast<long long>(sm_count) * per_sm * (8 - kEarlyRaceWarps);
     // pieces: the largest of kEarlyPieceBytes x {2, 1.5, 1} that still gives every row warp
@@ -527,10 +547,8 @@ int launch_tree(VerifyParams& p, const TreeShape& t, int sm_count, const spec_ve
         if (cudaLaunchKernelEx(&cfg, tree_walk_kernel<ET>, p, t) != cudaSuccess) return SPEC_ECUDA;
     }
     record(o, 2, s);
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tree_race_kernel<ET>, kThreads, 0) != cudaSuccess ||
-        per_sm < 1)
-        per_sm = 1;
+    int per_sm = blocks_per_sm(tree_race_kernel<ET>, kThreads, 0);
+    if (per_sm < 1) per_sm = 1;
     long long G = static_cast<long long>(sm_count) * per_sm / p.B;
     if (G > p.rpieces) G = p.rpieces;
     if (G < 1) G = 1;
@@ -1177,10 +1195,8 @@ int spec_verify_lmhead(const void* h_target, const void* w_target, const void* h
     p.status = q.status;
     p.out_tokens = out_tokens;
     p.out_n = out_n_accepted;
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, lmhead_race_kernel, kThreads, 0) != cudaSuccess ||
-        per_sm < 1)
-        per_sm = 1;
+    int per_sm = blocks_per_sm(lmhead_race_kernel, kThreads, 0);
+    if (per_sm < 1) per_sm = 1;
     long long G = static_cast<long long>(dev->sm_count) * per_sm / B;
     if (G > rpieces) G = rpieces;
     if (G < 1) G = 1;

@@ -178,6 +178,26 @@ def test_throughput_workload_full_size_every_sequence(sv, orc):
         compare_sampling(w, ge, r, check_values=False, count=False)
 
 
+@pytest.mark.parametrize("sigma,T,Td", [(0.0, 1.0, 1.0), (0.1, 1.0, 1.0), (0.1, 0.7, 0.7), (0.3, 1.0, 0.8)])
+def test_long_accepted_prefixes(sv, orc, sigma, T, Td):
+    """Drafts close to the target (draft = target at sigma = 0): long accepted prefixes, bonus
+    races, and residual races where q is close to p, so that many tokens pass the race
+    filter and are scored exactly.  Every sequence against the oracle, on the full read and
+    on the early-exit path."""
+    w = workloads.generic(B=16, gamma=8, V=128256, dtype="bf16", seed=77, scale=3.0,
+                          sigma=sigma, T=T, Td=Td, kind="zipf")
+    dw = DeviceWorkload(w)
+    for seed in (0, 1):
+        r = orc.verify(w.target, w.draft, w.tokens, w.T, w.Td, seed)
+        g = run_gpu(sv, dw, seed, diagnostics=(seed == 0))
+        compare_sampling(w, g, r, check_values=(seed == 0))
+        ge = run_gpu(sv, dw, seed, diagnostics=False, flags=sv.SPEC_FLAG_EARLY_EXIT)
+        compare_sampling(w, ge, r, check_values=False, count=False)
+    if sigma == 0.0 and T == Td:
+        assert np.all(r.n_accepted == w.gamma)  # p / q = 1 accepts every draft token
+    assert sv.spec_verify_check() == sv.SPEC_OK
+
+
 @pytest.mark.parametrize("B,gamma,V,dtype", [(24, 8, 128257, "bf16"), (20, 8, 65537, "f32")])
 def test_streaming_claim_launch_unaligned_rows(sv, orc, B, gamma, V, dtype):
     """Calls with more row pieces than the streaming grid has warps take the claiming launch
