@@ -1683,6 +1683,49 @@ struct TreeRace {
     int node, k, residual, drow;  // node raced (-1: none), output slot, residual?, its draft row
 };
 
+// ----------------------------------------------------------------------------------------
+// verify_small: the whole sampling verify of one sequence in one block, for calls whose
+// sequences are so small that a second launch costs more than their work (every row's
+// pieces read by the block's warps, and the raced row one race step long).  Warp w takes
+// the sequence's row pieces w, w + 8, ... with the same pieces and arithmetic as row_stats,
+// so the partials are the same bits; the block then scans and races the sequence exactly as
+// scan_race does with one block per sequence.  The block empties its sequence's race slot
+// and arrival count itself (row_stats does that on the two-kernel path).
+// ----------------------------------------------------------------------------------------
+constexpr int kSmallSeqBytes = 64 * 1024;  // largest (2 gamma + 1) V s taken by verify_small
+
+template <class ET, int U>
+__global__ void __launch_bounds__(256, SPECVERIFY_RACE_MINBLOCKS) verify_small_kernel(VerifyParams p) {
+    extern __shared__ float smem[];  // [2R]: scaled max and log2 sum of every row
+    __shared__ int s_last;
+    __shared__ float s_thr[8];
+    __shared__ RaceState s_best[8];
+    __shared__ ScanShared sh;
+    const int R = 2 * p.gamma + 1;
+    float* sm_m = smem;
+    float* sm_l = smem + R;
+    auto sync = [] { __syncthreads(); };
+    const int lane = threadIdx.x & 31;
+    const int warp = static_cast<int>(threadIdx.x >> 5);
+    const int b = blockIdx.x;
+    scan_prologue<ET>(p, b, threadIdx.x, sh);  // inputs only: overlaps the previous kernel
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int ns = race_slots(p.rpieces);
+    for (int k = threadIdx.x; k < ns; k += blockDim.x)
+        if (sv_in_range(p, static_cast<long long>(b) * ns + k, p.caps.race))
+            reinterpret_cast<uint4*>(p.race_parts + static_cast<long long>(b) * ns)[k] = make_uint4(0u, 0u, 0u, 0u);
+    if (threadIdx.x == 0) p.tickets[b] = 0;
+    for (int item = warp; item < R * p.npieces; item += static_cast<int>(blockDim.x >> 5))
+        row_stats_item<ET, U>(p, b, item / p.npieces, item % p.npieces, lane);
+    __syncthreads();  // the partials (and sh, the emptied slots) are visible to the block
+    const int j = scan_sequence<ET>(p, b, true, threadIdx.x, blockDim.x, sh, sm_m, sm_l, sync);
+    const int CH = (p.V + kRaceWarpTokens - 1) / kRaceWarpTokens;
+    if (j >= 0)
+        race_sequence_block<ET, 8>(p, b, 0, CH, kRaceBlockChunks, CH, 0, 1,
+                                   raced_row_info(p, b, j, sm_m, sm_l), s_thr, s_best, s_last, warp, sync);
+}
+
 template <class ET, int U, bool kClaim>
 __global__ void __launch_bounds__(kStreamThreads, SPECVERIFY_STATS_MINBLOCKS) tree_stats_kernel(VerifyParams p, int N, int M) {
     stream_pdl_wait();

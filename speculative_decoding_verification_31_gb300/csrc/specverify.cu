@@ -374,6 +374,15 @@ int launch_sampling(VerifyParams& p, int sm_count, const spec_verify_opts* o, cu
     const int R = 2 * p.gamma + 1;
     const bool extra = wants_position_stats(p);
     record(o, 0, s);
+    const long long seq_bytes = static_cast<long long>(R) * p.V * static_cast<long long>(sizeof(typename ET::storage));
+    if (!extra && seq_bytes <= kSmallSeqBytes && p.V <= kRaceBlockTokens) {
+        // small sequences: one block each does the whole verify (one launch instead of two)
+        if (launch_pdl(verify_small_kernel<ET, kUnroll>, p.B, 2 * R * sizeof(float), s, true, p) != cudaSuccess)
+            return SPEC_ECUDA;
+        record(o, 1, s);
+        record(o, 2, s);
+        return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
+    }
     if (extra) {  // the same read of every logit, paired by position, with the extra terms
         // pieces chosen for this pass's items (position pairs, not rows) and grid
         int per_sm = blocks_per_sm(pair_stats_kernel<ET, kPairUnroll, true>, kStreamThreads, 0);
