@@ -198,6 +198,44 @@ def test_long_accepted_prefixes(sv, orc, sigma, T, Td):
     assert sv.spec_verify_check() == sv.SPEC_OK
 
 
+@pytest.mark.parametrize("B,gamma,V,dtype,sigma", [(2, 2048, 40, "f32", 0.0), (3, 2048, 33, "bf16", 0.01),
+                                                   (4, 300, 257, "bf16", 0.01)])
+def test_longest_drafts(sv, orc, B, gamma, V, dtype, sigma):
+    """Draft lengths past the positions the scan gathers ahead (256) up to the largest gamma
+    the library takes (2048), with drafts so close to the target that the first rejection
+    falls deep in the draft (sigma = 0: never), on the full read, the early-exit path and in
+    greedy mode, against the oracle; gamma = 2049 is refused."""
+    w = workloads.generic(B=B, gamma=gamma, V=V, dtype=dtype, seed=gamma + V, scale=2.0,
+                          sigma=sigma, T=1.0, Td=1.0)
+    dw = DeviceWorkload(w)
+    accepted = []
+    for seed in (0, 1):
+        r = orc.verify(w.target, w.draft, w.tokens, w.T, w.Td, seed)
+        g = run_gpu(sv, dw, seed, diagnostics=(seed == 0))
+        compare_sampling(w, g, r, check_values=(seed == 0))
+        ge = run_gpu(sv, dw, seed, diagnostics=False, flags=sv.SPEC_FLAG_EARLY_EXIT)
+        compare_sampling(w, ge, r, check_values=False, count=False)
+        accepted.append(r.n_accepted)
+    accepted = np.concatenate(accepted)
+    if sigma == 0.0:
+        assert np.all(accepted == gamma)
+    else:
+        assert np.any(accepted > 256)  # some rejection past the gathered-ahead positions
+    wg = workloads.generic(B=B, gamma=gamma, V=V, dtype=dtype, seed=gamma + V + 1, scale=2.0,
+                           sigma=sigma, greedy=True)
+    dg = DeviceWorkload(wg)
+    out_t, out_n = sv.spec_verify_greedy_ex(dg.target, dg.tokens)
+    torch.cuda.synchronize()
+    rt, rn, _ = orc.verify_greedy(wg.target, wg.tokens)
+    compare_greedy(out_t.cpu().numpy(), out_n.cpu().numpy(), rt, rn)
+    assert sv.spec_verify_check() == sv.SPEC_OK
+    with pytest.raises(sv.SpecVerifyError) as e:
+        sv.spec_verify_ex(torch.zeros((1, 2050, 8), dtype=torch.float32, device="cuda"),
+                          torch.zeros((1, 2049, 8), dtype=torch.float32, device="cuda"),
+                          torch.zeros((1, 2049), dtype=torch.int32, device="cuda"), 1.0, 1.0, 0)
+    assert e.value.code == sv.SPEC_EINVAL
+
+
 @pytest.mark.parametrize("B,gamma,V,dtype", [(24, 8, 128257, "bf16"), (20, 8, 65537, "f32")])
 def test_streaming_claim_launch_unaligned_rows(sv, orc, B, gamma, V, dtype):
     """Calls with more row pieces than the streaming grid has warps take the claiming launch
