@@ -45,6 +45,27 @@ struct Bf16Elem {
             f[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
         }
     }
+    // Eight values from an address that is only 2-byte aligned, packed as a 16-byte load of
+    // them packs them (the lower address in the lower half of each word), with the widest
+    // loads the address allows.  (Rows of an odd vocabulary start off 16-byte boundaries.)
+    __device__ __forceinline__ static uint4 load_vec_unaligned(const storage* p) {
+        const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+        if ((a & 7u) == 0) {
+            const uint2* q = reinterpret_cast<const uint2*>(p);
+            const uint2 lo = __ldg(q), hi = __ldg(q + 1);
+            return make_uint4(lo.x, lo.y, hi.x, hi.y);
+        }
+        if ((a & 3u) == 0) {
+            const unsigned int* q = reinterpret_cast<const unsigned int*>(p);
+            return make_uint4(__ldg(q), __ldg(q + 1), __ldg(q + 2), __ldg(q + 3));
+        }
+        const unsigned short* q = reinterpret_cast<const unsigned short*>(p);
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            w[k] = static_cast<uint32_t>(__ldg(q + 2 * k)) | (static_cast<uint32_t>(__ldg(q + 2 * k + 1)) << 16);
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
     // The largest of the vector's eight values (exact: a maximum of bf16 values is one of
     // them), on packed pairs before widening.
     __device__ __forceinline__ static float vmax(const uint4& v) {
@@ -70,6 +91,16 @@ struct F32Elem {
     __device__ __forceinline__ static float vmax(const uint4& v) {
         return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
                      fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
+    }
+    // Four values from an address that is only 4-byte aligned (see Bf16Elem).
+    __device__ __forceinline__ static uint4 load_vec_unaligned(const storage* p) {
+        if ((reinterpret_cast<uintptr_t>(p) & 7u) == 0) {
+            const uint2* q = reinterpret_cast<const uint2*>(p);
+            const uint2 lo = __ldg(q), hi = __ldg(q + 1);
+            return make_uint4(lo.x, lo.y, hi.x, hi.y);
+        }
+        const unsigned int* q = reinterpret_cast<const unsigned int*>(p);
+        return make_uint4(__ldg(q), __ldg(q + 1), __ldg(q + 2), __ldg(q + 3));
     }
 };
 

@@ -997,15 +997,16 @@ __device__ __forceinline__ void prefetch_l2(const S* row, int x0, int x1, int la
 }
 
 // Race over tokens [x0, x1) of the raced row; every lane offers its tokens in increasing x.
-// The residual's draft row is read only at candidate tokens.
-template <class ET>
-__device__ __forceinline__ RaceState race_piece(const typename ET::storage* rt,
-                                                const typename ET::storage* rd, int x0, int x1,
-                                                const SeqInfo& si, bool residual,
-                                                const PhiloxRoundKeys& rk, uint32_t bg,
-                                                uint32_t pos, int lane) {
+// The residual's draft row is read only at candidate tokens.  kAligned: the vectors are the
+// row span's 16-byte-aligned ones (sp as built); otherwise they start at x0 (sp.head = 0) and
+// are read with narrower loads.
+template <class ET, bool kAligned>
+__device__ __forceinline__ RaceState race_piece_body(const typename ET::storage* rt,
+                                                     const typename ET::storage* rd, int x0, int x1,
+                                                     const RowSpan<ET>& sp, const SeqInfo& si,
+                                                     bool residual, const PhiloxRoundKeys& rk,
+                                                     uint32_t bg, uint32_t pos, int lane) {
     RaceState st{-INFINITY, INT_MAX, -INFINITY};
-    const RowSpan<ET> sp(rt, x0, x1);
     const RaceRowRng q = race_row_rng(rk, bg, pos);
     auto word_at = [&](int x) {
         const uint4 blk = race_block_fast(q, rk, static_cast<uint32_t>(x) >> 2);
@@ -1016,14 +1017,13 @@ __device__ __forceinline__ RaceState race_piece(const typename ET::storage* rt,
         const float s = race_exact_score(xt, xd, si, residual, w);
         if (s > -INFINITY) race_offer(st, s, x);
     };
-    // Vector path: Philox blocks of four tokens must start on a vector boundary.
-    if (((x0 + sp.head) & 3) != 0) {
-        for (int x = x0 + lane; x < x1; x += 32) offer_exact(ET::load1(rt + x), x, word_at(x));
-        return warp_race_merge(st);
-    }
     if (lane < sp.head) offer_exact(ET::load1(sp.base + lane), x0 + lane, word_at(x0 + lane));
     const int xb = x0 + sp.head;
-    const uint4* vt = sp.vec();
+    const uint4* vt = reinterpret_cast<const uint4*>(sp.base + sp.head);
+    auto vload = [&](int v) {
+        if constexpr (kAligned) return __ldg(vt + v);
+        else return ET::load_vec_unaligned(sp.base + v * ET::kVec);
+    };
     // Seed the threshold: each lane finds its largest target logit (a cheap pass, no random
     // numbers) and scores that token exactly.  Any token's score is at most the final best,
     // and a lane's most likely token is usually close to it, so few tokens pass the filter.
@@ -1039,7 +1039,7 @@ __device__ __forceinline__ RaceState race_piece(const typename ET::storage* rt,
 #pragma unroll
             for (int k = 0; k < kSeedBatch; ++k) {
                 const int v = v0 + lane + 32 * k;
-                raw[k] = v < sp.nvec ? __ldg(vt + v)
+                raw[k] = v < sp.nvec ? vload(v)
                                      : make_uint4(ET::kNegInfWord, ET::kNegInfWord,
                                                   ET::kNegInfWord, ET::kNegInfWord);
             }
@@ -1073,7 +1073,7 @@ __device__ __forceinline__ RaceState race_piece(const typename ET::storage* rt,
 #pragma unroll
         for (int k = 0; k < kRaceBatch; ++k) {
             const int v = v0 + lane + 32 * k;
-            raw[k] = v < sp.nvec ? __ldg(vt + v) : make_uint4(0u, 0u, 0u, 0u);
+            raw[k] = v < sp.nvec ? vload(v) : make_uint4(0u, 0u, 0u, 0u);
         }
         uint4 blk[kRaceBatch][ET::kVec / 4];
 #pragma unroll
@@ -1111,6 +1111,46 @@ __device__ __forceinline__ RaceState race_piece(const typename ET::storage* rt,
     const int t0 = sp.head + sp.nvec * ET::kVec;
     if (lane < sp.tail) offer_exact(ET::load1(sp.base + t0 + lane), x0 + t0 + lane, word_at(x0 + t0 + lane));
     return warp_race_merge(st);
+}
+
+template <class ET>
+__device__ __noinline__ RaceState race_piece_unaligned(const typename ET::storage* rt,
+                                                      const typename ET::storage* rd, int x0, int x1,
+                                                      RowSpan<ET> sp, SeqInfo si, bool residual,
+                                                      PhiloxRoundKeys rk, uint32_t bg, uint32_t pos,
+                                                      int lane) {
+    return race_piece_body<ET, false>(rt, rd, x0, x1, sp, si, residual, rk, bg, pos, lane);
+}
+
+// The race over [x0, x1): vectors of whole Philox blocks.  Where the row span's first 16-byte
+// boundary does not fall on a multiple of four tokens (a row of an odd vocabulary), the
+// vectors start at x0 instead (x0 is one) and are read with narrower loads.  kAligned: the
+// caller knows rt + x0 is on a 16-byte boundary.
+template <class ET, bool kAligned = false>
+__device__ __forceinline__ RaceState race_piece(const typename ET::storage* rt,
+                                                const typename ET::storage* rd, int x0, int x1,
+                                                const SeqInfo& si, bool residual,
+                                                const PhiloxRoundKeys& rk, uint32_t bg,
+                                                uint32_t pos, int lane) {
+    RowSpan<ET> sp(rt, x0, x1);
+    if (kAligned || ((x0 + sp.head) & 3) == 0)
+        return race_piece_body<ET, true>(rt, rd, x0, x1, sp, si, residual, rk, bg, pos, lane);
+    if constexpr (kAligned) return RaceState{};  // (not reached)
+    if ((x0 & 3) != 0) {  // (no caller starts a piece off a Philox block)
+        const RaceRowRng q = race_row_rng(rk, bg, pos);
+        RaceState st{-INFINITY, INT_MAX, -INFINITY};
+        for (int x = x0 + lane; x < x1; x += 32) {
+            const uint4 blk = race_block_fast(q, rk, static_cast<uint32_t>(x) >> 2);
+            const float xd = residual ? ET::load1(rd + x) : 0.0f;
+            const float sc = race_exact_score(ET::load1(rt + x), xd, si, residual, word_of(blk, static_cast<uint32_t>(x) & 3u));
+            if (sc > -INFINITY) race_offer(st, sc, x);
+        }
+        return warp_race_merge(st);
+    }
+    sp.head = 0;
+    sp.nvec = (x1 - x0) / ET::kVec;
+    sp.tail = (x1 - x0) - sp.nvec * ET::kVec;
+    return race_piece_unaligned<ET>(rt, rd, x0, x1, sp, si, residual, rk, bg, pos, lane);
 }
 
 // ----------------------------------------------------------------------------------------
@@ -1181,22 +1221,19 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64g(const void* p) {
     return v;
 }
 
-// The race of sequence b by one of the `nslots` groups of NW warps that share it (a block,
-// or the racing warps of one), over target row rt (and, for a residual, draft row rd;
-// statistics in si) with random-number row `pos`: race the chunks cb + w (warp w of the
-// group, wib) for cb = cb_begin, cb_begin + cb_step, ... (< cb_end), chunks from ch_limit on
-// excluded, publish the group's winner in partial slot `slot`, and if this is the sequence's
-// last group to finish, merge the groups' winners and write the token to *out.  sync() is
-// the group's barrier; CHAINS Philox blocks are computed at a time per lane.
-template <class ET, int NW, class Sync, int CHAINS = kRaceChains>
-__device__ __forceinline__ void race_rows_block(const VerifyParams& p, int b,
-                                               const typename ET::storage* rt,
-                                               const typename ET::storage* rd, bool residual,
-                                               uint32_t pos, int32_t* out, int cb_begin,
-                                               int cb_end, int cb_step, int ch_limit, int slot,
-                                               int nslots,
-                                               const SeqInfo& si, float* s_thr,
-                                               RaceState* s_best, int& s_last, int wib, Sync sync) {
+// race_rows_block (below) for a raced row that starts on a 16-byte boundary (kAligned; so
+// does every chunk, chunks being 1024 tokens) or not (a row of an odd vocabulary: the
+// chunks' vectors are read with narrower loads -- still whole Philox blocks, chunks starting
+// on multiples of four tokens).
+template <class ET, int NW, class Sync, int CHAINS, bool kAligned>
+__device__ __forceinline__ void race_rows_block_impl(const VerifyParams& p, int b,
+                                                    const typename ET::storage* rt,
+                                                    const typename ET::storage* rd, bool residual,
+                                                    uint32_t pos, int32_t* out, int cb_begin,
+                                                    int cb_end, int cb_step, int ch_limit, int slot,
+                                                    int nslots,
+                                                    const SeqInfo& si, float* s_thr,
+                                                    RaceState* s_best, int& s_last, int wib, Sync sync) {
     using S = typename ET::storage;
     constexpr int VPL = kRaceWarpTokens / (32 * ET::kVec);
     const int lane = threadIdx.x & 31;
@@ -1223,14 +1260,17 @@ __device__ __forceinline__ void race_rows_block(const VerifyParams& p, int b,
         const int x0 = chunk_x0(cb);
         const int x1 = min(p.V, x0 + kRaceWarpTokens);
         if (residual) prefetch_l2(rd, x0, x1, lane);
-        const bool ok = x0 < x1 && (reinterpret_cast<uintptr_t>(rt + x0) & 15u) == 0;
-        const int nv = ok ? (x1 - x0) / ET::kVec : 0;
-        const uint4* vt = reinterpret_cast<const uint4*>(rt + (ok ? x0 : 0));
+        const int nv = x0 < x1 ? (x1 - x0) / ET::kVec : 0;
+        const S* base = rt + (x0 < x1 ? x0 : 0);
 #pragma unroll
         for (int k = 0; k < VPL; ++k) {
             const int v = lane + 32 * k;
-            dst[k] = v < nv ? __ldg(vt + v) : make_uint4(ET::kNegInfWord, ET::kNegInfWord,
-                                                         ET::kNegInfWord, ET::kNegInfWord);
+            if constexpr (kAligned)
+                dst[k] = v < nv ? __ldg(reinterpret_cast<const uint4*>(base) + v)
+                                : make_uint4(ET::kNegInfWord, ET::kNegInfWord, ET::kNegInfWord, ET::kNegInfWord);
+            else
+                dst[k] = v < nv ? ET::load_vec_unaligned(base + v * ET::kVec)
+                                : make_uint4(ET::kNegInfWord, ET::kNegInfWord, ET::kNegInfWord, ET::kNegInfWord);
         }
     };
     uint4 raw[VPL], raw_next[VPL];
@@ -1240,7 +1280,7 @@ __device__ __forceinline__ void race_rows_block(const VerifyParams& p, int b,
     for (int cb = cb_begin; cb < cb_end; cb += cb_step) {
         const int x0 = chunk_x0(cb);
         const int x1 = min(p.V, x0 + kRaceWarpTokens);
-        const bool vec_ok = x0 < x1 && (reinterpret_cast<uintptr_t>(rt + x0) & 15u) == 0;
+        const bool vec_ok = x0 < x1 && (!kAligned || (reinterpret_cast<uintptr_t>(rt + x0) & 15u) == 0);
         const int nvec = vec_ok ? (x1 - x0) / ET::kVec : 0;
         if (cb + cb_step < cb_end) load_piece(cb + cb_step, raw_next);
         if (first) {
@@ -1376,7 +1416,7 @@ __device__ __forceinline__ void race_rows_block(const VerifyParams& p, int b,
     m = warp_race_merge(m);
     if (m.idx == INT_MAX) {
         // Every residual weight was zero (p <= q everywhere in fp32): draw from p_j.
-        m = race_piece<ET>(rt, nullptr, 0, p.V, si, false, p.rk, bg, pos, lane);
+        m = race_piece<ET, kAligned>(rt, nullptr, 0, p.V, si, false, p.rk, bg, pos, lane);
     }
     if (lane == 0) {
         *out = m.idx;
@@ -1387,9 +1427,52 @@ __device__ __forceinline__ void race_rows_block(const VerifyParams& p, int b,
     }
 }
 
+// The rare unaligned case kept out of line, so that the aligned race is compiled as if it
+// were the only one.
+template <class ET, int NW, class Sync, int CHAINS>
+__device__ __noinline__ void race_rows_block_unaligned(const VerifyParams& p, int b,
+                                                       const typename ET::storage* rt,
+                                                       const typename ET::storage* rd, bool residual,
+                                                       uint32_t pos, int32_t* out, int cb_begin,
+                                                       int cb_end, int cb_step, int ch_limit, int slot,
+                                                       int nslots, SeqInfo si, float* s_thr,
+                                                       RaceState* s_best, int* s_last, int wib, Sync sync) {
+    race_rows_block_impl<ET, NW, Sync, CHAINS, false>(p, b, rt, rd, residual, pos, out, cb_begin, cb_end,
+                                                      cb_step, ch_limit, slot, nslots, si, s_thr, s_best,
+                                                      *s_last, wib, sync);
+}
+
+// The race of sequence b by one of the `nslots` groups of NW warps that share it (a block,
+// or the racing warps of one), over target row rt (and, for a residual, draft row rd;
+// statistics in si) with random-number row `pos`: race the chunks cb + w (warp w of the
+// group, wib) for cb = cb_begin, cb_begin + cb_step, ... (< cb_end), chunks from ch_limit on
+// excluded, publish the group's winner in partial slot `slot`, and if this is the sequence's
+// last group to finish, merge the groups' winners and write the token to *out.  sync() is
+// the group's barrier; CHAINS Philox blocks are computed at a time per lane.
+// kRowsAligned: the caller knows every row starts on a 16-byte boundary (no out-of-line
+// path compiled in).
+template <class ET, int NW, class Sync, int CHAINS = kRaceChains, bool kRowsAligned = false>
+__device__ __forceinline__ void race_rows_block(const VerifyParams& p, int b,
+                                               const typename ET::storage* rt,
+                                               const typename ET::storage* rd, bool residual,
+                                               uint32_t pos, int32_t* out, int cb_begin,
+                                               int cb_end, int cb_step, int ch_limit, int slot,
+                                               int nslots,
+                                               const SeqInfo& si, float* s_thr,
+                                               RaceState* s_best, int& s_last, int wib, Sync sync) {
+    if (kRowsAligned || (reinterpret_cast<uintptr_t>(rt) & 15u) == 0)
+        race_rows_block_impl<ET, NW, Sync, CHAINS, true>(p, b, rt, rd, residual, pos, out, cb_begin, cb_end,
+                                                         cb_step, ch_limit, slot, nslots, si, s_thr, s_best,
+                                                         s_last, wib, sync);
+    else if constexpr (!kRowsAligned)
+        race_rows_block_unaligned<ET, NW, Sync, CHAINS>(p, b, rt, rd, residual, pos, out, cb_begin, cb_end,
+                                                        cb_step, ch_limit, slot, nslots, si, s_thr, s_best,
+                                                        &s_last, wib, sync);
+}
+
 // The chain's race: row j = si.j (the residual of position j < gamma, or the bonus row), by
 // a group of NW warps (see race_rows_block).
-template <class ET, int NW, class Sync, int CHAINS = kRaceChains>
+template <class ET, int NW, class Sync, int CHAINS = kRaceChains, bool kRowsAligned = false>
 __device__ __forceinline__ void race_sequence_block(const VerifyParams& p, int b, int cb_begin,
                                                    int cb_end, int cb_step, int ch_limit, int slot,
                                                    int nslots, const SeqInfo& si, float* s_thr,
@@ -1405,7 +1488,7 @@ __device__ __forceinline__ void race_sequence_block(const VerifyParams& p, int b
           (!residual || sv_span_in_range(p, (static_cast<long long>(b) * p.gamma + j) * p.V, p.V, p.caps.draft)) &&
           sv_in_range(p, static_cast<long long>(b) * (p.gamma + 1) + j, p.caps.out_tokens)))
         return;
-    race_rows_block<ET, NW, Sync, CHAINS>(p, b, rt, rd, residual, static_cast<uint32_t>(j),
+    race_rows_block<ET, NW, Sync, CHAINS, kRowsAligned>(p, b, rt, rd, residual, static_cast<uint32_t>(j),
                             p.out_tokens + static_cast<long long>(b) * (p.gamma + 1) + j, cb_begin,
                             cb_end, cb_step, ch_limit, slot, nslots, si, s_thr, s_best, s_last, wib,
                             sync);
@@ -1690,7 +1773,8 @@ struct TreeRace {
 // the sequence's row pieces w, w + 8, ... with the same pieces and arithmetic as row_stats,
 // so the partials are the same bits; the block then scans and races the sequence exactly as
 // scan_race does with one block per sequence.  The block empties its sequence's race slot
-// and arrival count itself (row_stats does that on the two-kernel path).
+// and arrival count itself (row_stats does that on the two-kernel path).  Taken only when
+// every row starts on a 16-byte boundary (V s a multiple of 16).
 // ----------------------------------------------------------------------------------------
 constexpr int kSmallSeqBytes = 64 * 1024;  // largest (2 gamma + 1) V s taken by verify_small
 
@@ -1722,7 +1806,7 @@ __global__ void __launch_bounds__(256, SPECVERIFY_RACE_MINBLOCKS) verify_small_k
     const int j = scan_sequence<ET>(p, b, true, threadIdx.x, blockDim.x, sh, sm_m, sm_l, sync);
     const int CH = (p.V + kRaceWarpTokens - 1) / kRaceWarpTokens;
     if (j >= 0)
-        race_sequence_block<ET, 8>(p, b, 0, CH, kRaceBlockChunks, CH, 0, 1,
+        race_sequence_block<ET, 8, decltype(sync), kRaceChains, true>(p, b, 0, CH, kRaceBlockChunks, CH, 0, 1,
                                    raced_row_info(p, b, j, sm_m, sm_l), s_thr, s_best, s_last, warp, sync);
 }
 

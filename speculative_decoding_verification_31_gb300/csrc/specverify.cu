@@ -375,7 +375,8 @@ int launch_sampling(VerifyParams& p, int sm_count, const spec_verify_opts* o, cu
     const bool extra = wants_position_stats(p);
     record(o, 0, s);
     const long long seq_bytes = static_cast<long long>(R) * p.V * static_cast<long long>(sizeof(typename ET::storage));
-    if (!extra && seq_bytes <= kSmallSeqBytes && p.V <= kRaceBlockTokens) {
+    const bool rows_aligned = (static_cast<long long>(p.V) * static_cast<long long>(sizeof(typename ET::storage))) % 16 == 0;
+    if (!extra && seq_bytes <= kSmallSeqBytes && p.V <= kRaceBlockTokens && rows_aligned) {
         // small sequences: one block each does the whole verify (one launch instead of two)
         if (launch_pdl(verify_small_kernel<ET, kUnroll>, p.B, 2 * R * sizeof(float), s, true, p) != cudaSuccess)
             return SPEC_ECUDA;

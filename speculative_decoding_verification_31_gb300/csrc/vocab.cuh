@@ -51,17 +51,20 @@ __device__ __forceinline__ RaceState race_warp_span(const VerifyParams& p,
         const float sc = race_exact_score(xt, xd, si, residual, w);
         if (sc > -INFINITY) race_offer(st, sc, x + xoff);
     };
+    // (chunks start on multiples of four tokens; one off a 16-byte boundary is read with
+    // narrower loads)
     auto load_chunk = [&](int x0, uint4 (&dst)[VPL]) {
         const int x1 = min(xb, x0 + kRaceWarpTokens);
         if (residual) prefetch_l2(rd, x0, x1, lane);
-        const bool ok = x0 < x1 && (reinterpret_cast<uintptr_t>(rt + x0) & 15u) == 0;
-        const int nv = ok ? (x1 - x0) / ET::kVec : 0;
-        const uint4* vt = reinterpret_cast<const uint4*>(rt + (ok ? x0 : 0));
+        const int nv = x0 < x1 ? (x1 - x0) / ET::kVec : 0;
+        const typename ET::storage* base = rt + (x0 < x1 ? x0 : 0);
+        const bool al = (reinterpret_cast<uintptr_t>(base) & 15u) == 0;
 #pragma unroll
         for (int k = 0; k < VPL; ++k) {
             const int v = lane + 32 * k;
-            dst[k] = v < nv ? __ldg(vt + v) : make_uint4(ET::kNegInfWord, ET::kNegInfWord,
-                                                         ET::kNegInfWord, ET::kNegInfWord);
+            dst[k] = v >= nv ? make_uint4(ET::kNegInfWord, ET::kNegInfWord, ET::kNegInfWord, ET::kNegInfWord)
+                   : al ? __ldg(reinterpret_cast<const uint4*>(base) + v)
+                        : ET::load_vec_unaligned(base + v * ET::kVec);
         }
     };
     uint4 raw[VPL], raw_next[VPL];
@@ -70,7 +73,7 @@ __device__ __forceinline__ RaceState race_warp_span(const VerifyParams& p,
     bool first = true;
     for (int x0 = xa; x0 < xb; x0 += kRaceWarpTokens) {
         const int x1 = min(xb, x0 + kRaceWarpTokens);
-        const bool vec_ok = (reinterpret_cast<uintptr_t>(rt + x0) & 15u) == 0;
+        const bool vec_ok = ((x0 + xoff) & 3) == 0;  // a vector's Philox blocks are whole
         const int nvec = vec_ok ? (x1 - x0) / ET::kVec : 0;
         const bool more = x0 + kRaceWarpTokens < xb;
         if (more) load_chunk(x0 + kRaceWarpTokens, raw_next);

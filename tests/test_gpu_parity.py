@@ -236,6 +236,36 @@ def test_longest_drafts(sv, orc, B, gamma, V, dtype, sigma):
     assert e.value.code == sv.SPEC_EINVAL
 
 
+@pytest.mark.parametrize("B", [180, 240, 400])
+def test_batch_sizes_around_the_race_wave(sv, orc, B):
+    """The race's three grid layouts by batch size against one resident wave of race blocks
+    (304 on a 152-SM GPU): chunks shared evenly with blocks straddling two sequences (180),
+    one block per sequence when the batch fills three quarters of the wave (240), and more
+    sequences than the wave holds (400) -- every sequence against the oracle."""
+    w = workloads.generic(B=B, gamma=3, V=3001, dtype="bf16", seed=B, sigma=0.8, T=0.9, Td=0.6)
+    dw = DeviceWorkload(w)
+    for seed in (0, 1):
+        r = orc.verify(w.target, w.draft, w.tokens, w.T, w.Td, seed)
+        g = run_gpu(sv, dw, seed, diagnostics=(seed == 0))
+        compare_sampling(w, g, r, check_values=(seed == 0))
+    assert sv.spec_verify_check() == sv.SPEC_OK
+
+
+def test_a_million_token_vocabulary(sv, orc):
+    """V = 2^20 + 3 (1024 race chunks and a ragged tail per raced row) against the oracle, on
+    the full read and the early-exit path."""
+    w = workloads.generic(B=2, gamma=2, V=(1 << 20) + 3, dtype="bf16", seed=11, sigma=0.9,
+                          T=1.0, Td=0.7)
+    dw = DeviceWorkload(w)
+    for seed in (0, 1, 2):
+        r = orc.verify(w.target, w.draft, w.tokens, w.T, w.Td, seed)
+        g = run_gpu(sv, dw, seed, diagnostics=(seed == 0))
+        compare_sampling(w, g, r, check_values=(seed == 0))
+        ge = run_gpu(sv, dw, seed, diagnostics=False, flags=sv.SPEC_FLAG_EARLY_EXIT)
+        compare_sampling(w, ge, r, check_values=False, count=False)
+    assert sv.spec_verify_check() == sv.SPEC_OK
+
+
 @pytest.mark.parametrize("B,gamma,V,dtype", [(24, 8, 128257, "bf16"), (20, 8, 65537, "f32")])
 def test_streaming_claim_launch_unaligned_rows(sv, orc, B, gamma, V, dtype):
     """Calls with more row pieces than the streaming grid has warps take the claiming launch
