@@ -358,6 +358,42 @@ def test_degenerate_distributions(sv, orc):
         assert gres["n"][1] == g
 
 
+@pytest.mark.parametrize("dtype,T,Td", [("bf16", 1.0, 0.5), ("f32", 0.05, 0.05), ("bf16", 20.0, 8.0)])
+def test_masked_vocabulary_and_extreme_temperatures(sv, orc, dtype, T, Td):
+    """Logits masked to -inf (a third of the vocabulary, the same tokens in target and
+    draft, as a constrained or padded vocabulary gives), one sequence whose target rows keep
+    a single token (p one-hot), one whose draft tokens are masked in the target (p(d) = 0:
+    rejected at position 0), at sharp and flat temperatures -- against the oracle, on the
+    full read and the early-exit path."""
+    B, g, V = 6, 5, 20011
+    w = workloads.generic(B=B, gamma=g, V=V, dtype="f32", seed=int(T * 100) + V, sigma=0.4,
+                          T=T, Td=Td)
+    rng = np.random.default_rng(5)
+    mask = rng.random(V) < 1.0 / 3.0
+    tgt, drf, tok = w.target.copy(), w.draft.copy(), w.tokens.copy()
+    tgt[:, :, mask] = -np.inf
+    drf[:, :, mask] = -np.inf
+    live = np.flatnonzero(~mask)
+    for b in range(B):  # draft tokens drawn from the masked draft rows
+        tok[b] = workloads.draw_drafts(rng, drf[b], float(Td))
+    keep = live[7]
+    tgt[1] = -np.inf
+    tgt[1, :, keep] = 0.5                              # p one-hot on `keep`
+    tgt[2, 0, tok[2, 0]] = -np.inf                     # p(d_0) = 0 for sequence 2
+    enc = (lambda a: workloads.to_bf16_bits(a)) if dtype == "bf16" else (lambda a: a.astype(np.float32))
+    w2 = workloads.Workload("masked", B, g, V, dtype, enc(tgt), enc(drf), tok, w.T, w.Td)
+    dw = DeviceWorkload(w2)
+    for seed in range(4):
+        r = orc.verify(w2.target, w2.draft, w2.tokens, w2.T, w2.Td, seed)
+        gres = run_gpu(sv, dw, seed, diagnostics=(seed == 0))
+        compare_sampling(w2, gres, r, check_values=(seed == 0))
+        ge = run_gpu(sv, dw, seed, diagnostics=False, flags=sv.SPEC_FLAG_EARLY_EXIT)
+        compare_sampling(w2, ge, r, check_values=False, count=False)
+        assert r.n_accepted[2] == 0
+        assert not mask[gres["tokens"][np.arange(B), gres["n"]]].any()  # no masked token drawn
+    assert sv.spec_verify_check() == sv.SPEC_OK
+
+
 def test_empty_batch_and_invalid_arguments(sv):
     e = torch.empty((0, 4, 100), dtype=torch.bfloat16, device="cuda")
     d = torch.empty((0, 3, 100), dtype=torch.bfloat16, device="cuda")
