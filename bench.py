@@ -27,6 +27,7 @@ L2, each with its kernel split, roofline fraction and the oracle's one-core rate
 from __future__ import annotations
 
 import argparse
+import contextlib
 import hashlib
 import json
 import os
@@ -48,6 +49,24 @@ UNIT = "rows/s"
 # choice and the helpers it calls); reported as null once that code has changed.
 NCU_TRAFFIC = {"bytes": 1949927680, "sources_sha1": "26041dca03e6079a385837ca77d81ca2ff8828bc"}
 ROW_STATS_SPAN = ("inline int pick_piece_len(", "// Per-position entropies and KL divergence")
+
+
+@contextlib.contextmanager
+def nvtx(name: str):
+    """An NVTX range around a phase of the run (host markers only, outside the timed kernel
+    work), so that a profiler can select it (`ncu --nvtx --nvtx-include name/`); nothing if
+    torch has no NVTX."""
+    import torch
+    try:
+        torch.cuda.nvtx.range_push(name)
+        pushed = True
+    except Exception:
+        pushed = False
+    try:
+        yield
+    finally:
+        if pushed:
+            torch.cuda.nvtx.range_pop()
 
 
 def kernel_sources_sha1() -> str:
@@ -311,10 +330,11 @@ def measure_config(sv, cfg: int, dev, stream, seed: int, seq_base: int, l2: int,
                                   out_n, seq_index_base=seq_base, flags=flags,
                                   prof_events=events, **kw)
 
-        est = time_calls(call, 20, stream)
-        n = int(max(200, min(20000, 250.0 / max(est, 1e-3))))
-        ms_api = time_calls(call, n, stream)
-        ms, ng = time_graph_calls(call, copies, stream)
+        with nvtx(f"workload {cfg} {mode}"):
+            est = time_calls(call, 20, stream)
+            n = int(max(200, min(20000, 250.0 / max(est, 1e-3))))
+            ms_api = time_calls(call, n, stream)
+            ms, ng = time_graph_calls(call, copies, stream)
         status = sv.spec_verify_check()
         nbytes = w.bytes_greedy() if greedy else w.bytes_sampling()
         timing = "CUDA graph replay of the calls (device time, no host work between calls)"
@@ -400,13 +420,14 @@ def run_ours(args):
     if ws_ > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    h0 = time.time()
-    start.record(stream)
-    for k in range(K):
-        step()
-    end.record(stream)
-    torch.cuda.synchronize()
-    h1 = time.time()
+    with nvtx("timed steps"):
+        h0 = time.time()
+        start.record(stream)
+        for k in range(K):
+            step()
+        end.record(stream)
+        torch.cuda.synchronize()
+        h1 = time.time()
     if ws_ > 1:
         torch.distributed.barrier()
     clocks = None
@@ -425,11 +446,12 @@ def run_ours(args):
         torch.cuda.synchronize()
         g0 = time.time()
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s0.record(stream)
-        for _ in range(Ks):
-            step()
-        s1.record(stream)
-        torch.cuda.synchronize()
+        with nvtx("sustained steps"):
+            s0.record(stream)
+            for _ in range(Ks):
+                step()
+            s1.record(stream)
+            torch.cuda.synchronize()
         g1 = time.time()
         sms = s0.elapsed_time(s1)
         if ws_ > 1:
@@ -448,9 +470,10 @@ def run_ours(args):
         for ev in e:
             ev.record(stream)
     torch.cuda.synchronize()
-    for k in range(Kr):
-        step(evs[k])
-    torch.cuda.synchronize()
+    with nvtx("roofline pass"):
+        for k in range(Kr):
+            step(evs[k])
+        torch.cuda.synchronize()
     kern_ms = [float(np.mean([e[i].elapsed_time(e[i + 1]) for e in evs])) for i in range(nkern)]
     if ws_ > 1:
         mt = torch.tensor([ms], device=dev, dtype=torch.float64)

@@ -40,6 +40,8 @@ SMALL_SHAPES = [
     (2, 3, 1, "f32"),        # V = 1
     (5, 2, 7, "bf16"),       # V < one vector
     (2, 6, 20000, "bf16"),   # several pieces, aligned rows
+    (3, 1, 8, "bf16"),       # V = one bf16 vector, gamma = 1
+    (2, 1, 9, "f32"),        # V = two f32 vectors and one, rows off 16-byte boundaries
     (1, 1, 4100, "f32"),     # piece boundary + 4
 ]
 
