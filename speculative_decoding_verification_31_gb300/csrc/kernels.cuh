@@ -1494,31 +1494,37 @@ __device__ __forceinline__ void race_sequence_block(const VerifyParams& p, int b
                             sync);
 }
 
+// Eight partials (packed (m, s) words; past P: empty) merged as a balanced tree.
+__device__ __forceinline__ SoftmaxStat fold8(const unsigned long long* v, int n) {
+    SoftmaxStat t[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        t[q] = q < n ? SoftmaxStat{__uint_as_float(static_cast<uint32_t>(v[q])),
+                                   __uint_as_float(static_cast<uint32_t>(v[q] >> 32))}
+                     : SoftmaxStat{-FLT_MAX, 0.0f};
+    t[0] = merge_stat(t[0], t[1]);
+    t[2] = merge_stat(t[2], t[3]);
+    t[4] = merge_stat(t[4], t[5]);
+    t[6] = merge_stat(t[6], t[7]);
+    t[0] = merge_stat(t[0], t[2]);
+    t[4] = merge_stat(t[4], t[6]);
+    return merge_stat(t[0], t[4]);
+}
+
 // The merged statistics of one row from its P partials (packed (m, s) words, complete: they
 // were written by an earlier kernel), by one thread in a fixed order: eight partials at a
 // time merged as a balanced tree (pairs, pairs of pairs, root), the eight-partial results
 // folded in piece order, so that every call merges a row's pieces into the same bits.
 __device__ __forceinline__ SoftmaxStat fold_row_stats(const unsigned long long* parts, int P) {
     SoftmaxStat acc{-FLT_MAX, 0.0f};
-    for (int k0 = 0; k0 < P; k0 += 8) {
-        unsigned long long v[8];
+    // sixteen loads in flight (two eight-partial groups), folded in the same order
+    for (int k0 = 0; k0 < P; k0 += 16) {
+        unsigned long long v[16];
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
+        for (int q = 0; q < 16; ++q)
             v[q] = (k0 + q < P) ? __ldcg(parts + k0 + q) : 0ull;
-        SoftmaxStat t[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            t[q] = (k0 + q < P) ? SoftmaxStat{__uint_as_float(static_cast<uint32_t>(v[q])),
-                                              __uint_as_float(static_cast<uint32_t>(v[q] >> 32))}
-                                : SoftmaxStat{-FLT_MAX, 0.0f};
-        }
-        t[0] = merge_stat(t[0], t[1]);
-        t[2] = merge_stat(t[2], t[3]);
-        t[4] = merge_stat(t[4], t[5]);
-        t[6] = merge_stat(t[6], t[7]);
-        t[0] = merge_stat(t[0], t[2]);
-        t[4] = merge_stat(t[4], t[6]);
-        acc = merge_stat(acc, merge_stat(t[0], t[4]));
+        acc = merge_stat(acc, fold8(v, P - k0));
+        if (k0 + 8 < P) acc = merge_stat(acc, fold8(v + 8, P - k0 - 8));
     }
     return acc;
 }
