@@ -300,6 +300,21 @@ def test_seq_index_base_splits_a_batch(sv, orc):
     np.testing.assert_array_equal(full["n"], np.concatenate([h["n"] for h in halves]))
 
 
+def test_seq_index_base_wraps_like_the_oracle(sv, orc):
+    """Global sequence indices are 32-bit counter words: a base of 2^32 - 3 wraps to 0 within
+    the batch, on the device exactly as in the oracle (full read and early exit)."""
+    w = workloads.generic(B=6, gamma=4, V=7001, dtype="bf16", seed=12, sigma=0.6, T=0.9, Td=0.5)
+    dw = DeviceWorkload(w)
+    base = (1 << 32) - 3
+    for seed in (0, 1):
+        r = orc.verify(w.target, w.draft, w.tokens, w.T, w.Td, seed, b_base=base)
+        g = run_gpu(sv, dw, seed, seq_index_base=base, diagnostics=(seed == 0))
+        compare_sampling(w, g, r, check_values=(seed == 0))
+        ge = run_gpu(sv, dw, seed, seq_index_base=base, diagnostics=False,
+                     flags=sv.SPEC_FLAG_EARLY_EXIT)
+        compare_sampling(w, ge, r, check_values=False, count=False)
+
+
 def test_repeatable_and_caller_workspace(sv, orc):
     w = workloads.generic(B=5, gamma=6, V=33000, dtype="bf16", seed=4, T=1.0, Td=0.3)
     dw = DeviceWorkload(w)
