@@ -46,6 +46,44 @@ SMALL_SHAPES = [
 ]
 
 
+TINY_SHAPES = [
+    # B, gamma, V, dtype: rows of at most 4 KB (the one-launch small-sequence path)
+    (4, 7, 2048, "bf16"),
+    (3, 0, 1024, "f32"),
+    (8, 3, 512, "bf16"),
+    (2, 6, 64, "f32"),
+    (5, 2, 8, "bf16"),
+]
+
+
+@pytest.mark.parametrize("B,gamma,V,dtype", TINY_SHAPES)
+def test_tiny_sequences(sv, orc, B, gamma, V, dtype):
+    """Tiny sequences (the one-launch small-sequence path) with per-sequence temperatures,
+    diagnostics, a bad draft token and a sequence whose draft equals its target, against
+    the oracle."""
+    w = workloads.generic(B=B, gamma=gamma, V=V, dtype=dtype, seed=B * 100 + V + gamma, sigma=0.7,
+                          T=0.8, Td=0.5)
+    T = np.linspace(0.4, 1.6, B).astype(np.float32)
+    Td = (T * np.linspace(0.3, 1.0, B)).astype(np.float32)
+    draft, tok = w.draft.copy(), w.tokens.copy()
+    if gamma and B > 2:
+        draft[1] = w.target[1, :gamma]
+        Td[1] = T[1]
+        tok[2, gamma - 1] = V  # out of range: sequence 2 is marked
+    w2 = workloads.Workload("tiny", B, gamma, V, dtype, w.target, draft, tok, T, Td)
+    dw = DeviceWorkload(w2)
+    for seed in range(3):
+        r = orc.verify(w2.target, w2.draft, w2.tokens, w2.T, w2.Td, seed)
+        g = run_gpu(sv, dw, seed, diagnostics=(seed == 0))
+        compare_sampling(w2, g, r, check_values=(seed == 0))
+        if gamma and B > 2:
+            assert g["n"][2] == -1 and np.all(g["tokens"][2] == -1)
+            assert g["n"][1] == gamma  # p = q: every draft token accepted
+    if gamma and B > 2:
+        assert sv.spec_verify_check() == sv.SPEC_EBADTOKEN
+    assert sv.spec_verify_check() == sv.SPEC_OK
+
+
 @pytest.mark.parametrize("B,gamma,V,dtype", SMALL_SHAPES)
 def test_greedy_small(sv, orc, B, gamma, V, dtype):
     w = workloads.generic(B=B, gamma=gamma, V=V, dtype=dtype, seed=B * 1000 + V, greedy=True)
