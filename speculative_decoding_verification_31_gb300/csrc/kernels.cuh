@@ -1113,6 +1113,8 @@ __device__ __forceinline__ RaceState race_piece_body(const typename ET::storage*
     return warp_race_merge(st);
 }
 
+// The unaligned race over a piece, kept out of line so that the aligned one is compiled as
+// if it were the only one.
 template <class ET>
 __device__ __noinline__ RaceState race_piece_unaligned(const typename ET::storage* rt,
                                                       const typename ET::storage* rd, int x0, int x1,
