@@ -78,3 +78,32 @@ def test_checked_build_bad_tokens_still_reported(sv):
         assert sv.spec_verify_check() == sv.SPEC_EBADTOKEN
         got = n.cpu().numpy()
         assert got[1] == -1 and got[3] == -1
+
+
+@pytest.mark.parametrize("cfg", [3, 4])
+def test_checked_build_named_batched_workloads_full_size(sv, cfg):
+    """The batched-serving and throughput workloads at full size through the checked build:
+    no index leaves its buffer, and the tokens are the normal build's, on the full read,
+    the early-exit path and in greedy mode."""
+    w = workloads.config(cfg)
+    dw = DeviceWorkload(w)
+    results = {}
+    for lib in (sv.specverify.CHECKED_LIB_PATH, sv.specverify.LIB_PATH):
+        sv.specverify.use_library(lib)
+        for flags in (0, sv.SPEC_FLAG_EARLY_EXIT):
+            g = run_gpu(sv, dw, 7, per_seq_temps=(cfg == 3), diagnostics=False, flags=flags)
+            assert sv.spec_verify_check() == sv.SPEC_OK, (lib, flags)
+            results[(lib, flags)] = g
+    sv.specverify.use_library(sv.specverify.CHECKED_LIB_PATH)
+    for flags in (0, sv.SPEC_FLAG_EARLY_EXIT):
+        a = results[(sv.specverify.CHECKED_LIB_PATH, flags)]
+        b = results[(sv.specverify.LIB_PATH, flags)]
+        np.testing.assert_array_equal(a["tokens"], b["tokens"])
+        np.testing.assert_array_equal(a["n"], b["n"])
+    wg = workloads.config(cfg, greedy=True)
+    dg = DeviceWorkload(wg)
+    t, n = sv.spec_verify_greedy_ex(dg.target, dg.tokens)
+    assert sv.spec_verify_check() == sv.SPEC_OK
+    rt, rn, _ = oracle.get().verify_greedy(wg.target, wg.tokens)
+    compare_greedy(t.cpu().numpy(), n.cpu().numpy(), rt, rn)
+
