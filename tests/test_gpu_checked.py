@@ -107,3 +107,30 @@ def test_checked_build_named_batched_workloads_full_size(sv, cfg):
     rt, rn, _ = oracle.get().verify_greedy(wg.target, wg.tokens)
     compare_greedy(t.cpu().numpy(), n.cpu().numpy(), rt, rn)
 
+
+def test_checked_build_token_trees(sv):
+    """Token-tree verifies (random trees with ragged rows, and SubSpec's depth-48 tree at
+    V = 152064) through the checked build: status clear, and the normal build's tokens."""
+    from _parity import to_device
+    rng = np.random.default_rng(4)
+    cases = [workloads.tree(workloads.random_tree(rng, 20, 4), B=5, V=4099, dtype="bf16", seed=8,
+                            scale=3.0, sigma=0.6, T=0.9, Td=0.45),
+             workloads.tree(workloads.deep_narrow_tree(48, 6), B=2, V=152064, dtype="bf16",
+                            seed=1005, scale=5.0, sigma=workloads.DEEP_CHAIN_SIGMA, T=0.6, Td=0.2)]
+    dev = torch.device("cuda")
+    for w in cases:
+        t = to_device(w.target, w.dtype, dev)
+        d = to_device(w.draft, w.dtype, dev)
+        tok = torch.from_numpy(np.ascontiguousarray(w.tokens)).to(dev)
+        outs = []
+        for lib in (sv.specverify.CHECKED_LIB_PATH, sv.specverify.LIB_PATH):
+            sv.specverify.use_library(lib)
+            for seed in range(2):
+                o = sv.spec_verify_tree(t, d, tok, w.parent, float(w.T[0]), float(w.Td[0]), seed)
+                assert sv.spec_verify_check() == sv.SPEC_OK
+                outs.append([x.cpu().numpy() for x in o])
+        sv.specverify.use_library(sv.specverify.CHECKED_LIB_PATH)
+        for a, b in zip(outs[:2], outs[2:]):
+            for x, y in zip(a, b):
+                np.testing.assert_array_equal(x, y)
+
