@@ -119,18 +119,30 @@ def compare_sampling(w: workloads.Workload, g: dict, r: "oracle.OracleResult",
             want = ref[ok]
             fin = np.isfinite(want)
             assert np.array_equal(np.isfinite(got), fin), name
-            # p and q within 1e-5 relative  <=>  |ln p_gpu - ln p_oracle| < ~1e-5
+            # p and q within 1e-5 relative  <=>  |ln p_gpu - ln p_oracle| < ~1e-5; a probability
+            # so small that |ln p| * 2^-24 (fp32's own resolution of the logarithm the kernels
+            # keep) approaches that is allowed four such units more
             err = np.abs(np.expm1(got[fin] - want[fin]))
-            assert err.size == 0 or err.max() < 1e-5, (name, float(err.max()))
+            allow = 1e-5 + 4.0 * 2.0 ** -24 * np.abs(want[fin])
+            assert err.size == 0 or np.all(err < allow), (name, float(err.max()))
         zq = g["logZq"].astype(np.float64)
         np.testing.assert_allclose(zq, r.logZq, rtol=1e-6, atol=1e-6)
     zp = g["logZp"].astype(np.float64)
     np.testing.assert_allclose(zp, r.logZp, rtol=1e-6, atol=1e-6)
-    # the winning race score ln w(y) - ln E_y (a check of the device Philox and E mapping)
+    # the winning race score ln w(y) - ln E_y (a check of the device Philox and E mapping).
+    # For a residual, ln(p - q) at the winner inherits the errors of ln p and ln q (fp32, a few
+    # 1e-6) amplified by (q/p) / (1 - q/p): the allowance grows with that factor.
     sel = ok & ~flagged
-    if sel.any():
-        np.testing.assert_allclose(g["race"][sel, 0].astype(np.float64), r.race[sel, 0],
-                                   rtol=1e-5, atol=2e-5)
+    for b in np.flatnonzero(sel):
+        j, y = int(r.n_accepted[b]), int(r.tokens[b, r.n_accepted[b]])
+        cond = 0.0
+        if j < gamma:
+            lp = float(workloads.as_f32(w.target[b, j, y:y + 1], w.dtype)[0]) / float(w.T[b]) - r.logZp[b, j]
+            lq = float(workloads.as_f32(w.draft[b, j, y:y + 1], w.dtype)[0]) / float(w.Td[b]) - r.logZq[b, j]
+            ratio = np.exp(min(0.0, lq - lp))
+            cond = ratio / max(1.0 - ratio, 1e-12)
+        tol = 2e-5 + 1e-5 * abs(r.race[b, 0]) + 1e-5 * cond
+        assert abs(float(g["race"][b, 0]) - r.race[b, 0]) <= tol, (b, float(g["race"][b, 0]), r.race[b, 0], cond)
 
 
 def gpu_near_ties(g: dict, gamma: int) -> np.ndarray:
