@@ -75,3 +75,66 @@ def test_random_shapes(sv, case):
     rt, rn, _ = orc.verify_greedy(w.target, w.tokens)
     compare_greedy(t.cpu().numpy(), n.cpu().numpy(), rt, rn)
     assert sv.spec_verify_check() == sv.SPEC_OK, c
+
+
+N_SPLIT = int(os.environ.get("SPECVERIFY_FUZZ_SPLIT_CASES", "16"))
+N_TREE = int(os.environ.get("SPECVERIFY_FUZZ_TREE_CASES", "16"))
+
+
+@pytest.mark.parametrize("case", range(N_SPLIT))
+def test_random_vocab_splits(sv, case):
+    """The vocabulary-parallel steps on random shapes and rank counts (ranks emulated one
+    after another on this GPU), against the oracle except at its flagged near-ties."""
+    from _parity import NEAR_TIE
+    from test_gpu_vocab_parallel import emulate
+    rng = np.random.default_rng(7_000_000 + case)
+    world = int(rng.integers(2, 9))
+    dtype = "bf16" if rng.random() < 0.6 else "f32"
+    V = int(rng.integers(8 * world + 1, 200_000))
+    gamma = int(rng.choice([0, 1, 3, 6, 12]))
+    B = int(rng.integers(1, max(2, min(16, 3_000_000 // ((2 * gamma + 1) * V)) + 1)))
+    T = float(rng.uniform(0.3, 1.8))
+    sigma = float(rng.choice([0.1, 0.6, 1.2]))
+    per_seq = bool(rng.random() < 0.5)
+    kind = str(rng.choice(["normal", "zipf", "heavy"]))
+    target_fn = {"normal": lambda r_, n, v: workloads.normal_rows(r_, n, v, 3.0),
+                 "zipf": lambda r_, n, v: workloads.zipf_shaped_rows(r_, n, v, 3.0),
+                 "heavy": workloads.heavy_tailed_rows}[kind]
+
+    def params(r_):
+        t = r_.uniform(0.3, 1.8)
+        return t, t * r_.uniform(0.3, 1.0), sigma
+
+    w = workloads.make_workload(f"split{case}", B, gamma, V, dtype, case, target_fn, sigma, T,
+                                Td=T * float(rng.uniform(0.3, 1.0)),
+                                per_seq_params=params if per_seq else None)
+    orc = oracle.get()
+    seed = int(rng.integers(0, 1 << 31))
+    vt, vn = emulate(sv, w, world, seed, per_seq=per_seq)
+    r = orc.verify(w.target, w.draft, w.tokens, w.T, w.Td, seed)
+    ok = (r.flags & NEAR_TIE) == 0
+    np.testing.assert_array_equal(vn[ok], r.n_accepted[ok])
+    np.testing.assert_array_equal(vt[ok], r.tokens[ok])
+    assert sv.spec_verify_check() == sv.SPEC_OK
+
+
+@pytest.mark.parametrize("case", range(N_TREE))
+def test_random_token_trees(sv, case):
+    """Token-tree verifies of random trees, shapes and temperatures against the oracle."""
+    from test_gpu_tree import compare_tree, run_tree
+    rng = np.random.default_rng(9_000_000 + case)
+    N = int(rng.integers(1, 80))
+    parent = workloads.random_tree(rng, N, int(rng.integers(1, 6)))
+    dtype = "bf16" if rng.random() < 0.6 else "f32"
+    V = int(rng.integers(2, 60_000))
+    if rng.random() < 0.5:
+        V += (-V) % 8
+    B = int(rng.integers(1, 6))
+    T = float(rng.uniform(0.3, 1.8))
+    w = workloads.tree(parent, B=B, V=V, dtype=dtype, seed=case, scale=3.0,
+                       sigma=float(rng.choice([0.1, 0.6, 1.2])), T=T, Td=T * float(rng.uniform(0.3, 1.0)))
+    orc = oracle.get()
+    for seed in range(2):
+        compare_tree(w, run_tree(sv, w, seed),
+                     orc.verify_tree(w.target, w.draft, w.tokens, w.parent, w.T, w.Td, seed))
+    assert sv.spec_verify_check() == sv.SPEC_OK
