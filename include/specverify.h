@@ -331,17 +331,22 @@ int spec_lmhead_row_stats(const void *hidden, const void *weight, int rows, int 
                           float *out_logp_token, void *stream);
 
 /*
- * The sampling verify step from the models' last hidden states: h_target [B, gamma+1, d]
+ * The sampling verify step from the models' last hidden states ("How speculative decoding
+ * makes LLMs go brrr", module 2: the gamma+1 target distributions of one forward pass, here
+ * from the hidden states through the LM head): h_target [B, gamma+1, d]
  * with the target LM head w_target [V, d], and h_draft [B, gamma, d] with the draft LM head
- * w_draft [V, d] (may be w_target), all bf16 row-major device memory, d a multiple of 64.
- * The target and draft row statistics come from spec_lmhead_row_stats' kernel (the B (2
- * gamma + 1) x V logits are never written); only the raced row of each sequence (target
- * row j, and draft row j for a residual) is computed as logits, on the tensor cores, and
- * raced.  Outputs, decisions and random numbers are those of spec_verify_ex run on the
- * logits H W^T.  opts: per-sequence temperatures, seq_index_base, d_status and prof_events
- * (before the first kernel, after the statistics, after the raced rows' logits, after the
- * race) are honoured; the library's own workspace is used (about 8 B V bytes for the raced
- * rows' fp32 logits).  SPEC_EINVAL for bad sizes, NULL or misaligned pointers.
+ * w_draft [V, d] (may be w_target), all bf16 row-major device memory, d a multiple of 64 and
+ * at most 32768.  The target and draft row statistics come from spec_lmhead_row_stats'
+ * kernel (one pass over each head on the tensor cores; the B (2 gamma + 1) x V logits are
+ * never written), which also keeps the largest logit of every 8-token block of the target
+ * rows; each sequence's race then draws every token's random number, drops the tokens whose
+ * block maximum cannot reach the best score found so far, and computes the logits h . w_x
+ * of the rest (a few dozen per sequence) by dot products in fp32.  Outputs, decisions and
+ * random numbers are those of spec_verify_ex run on the logits H W^T.  opts: per-sequence
+ * temperatures, seq_index_base, d_status and prof_events (before the first kernel, after
+ * the statistics, after the scan, after the race) are honoured; the library's own
+ * workspace is used (B (gamma + 1) ceil(V / 8) bf16 block maxima plus a few words
+ * per row).  SPEC_EINVAL for bad sizes, NULL or misaligned pointers.
  */
 int spec_verify_lmhead(const void *h_target, const void *w_target, const void *h_draft,
                        const void *w_draft, const int32_t *draft_tokens, int B, int gamma, int V,

@@ -1074,6 +1074,7 @@ int spec_verify_lmhead(const void* h_target, const void* w_target, const void* h
                        int d, float T, float T_d, uint64_t seed, int32_t* out_tokens,
                        int32_t* out_n_accepted, const spec_verify_opts* opts, void* stream) {
     if (B < 0 || gamma < 0 || gamma > kMaxGamma) return SPEC_EINVAL;
+    if (d > kLmMaxD) return SPEC_EINVAL;
     int rc = lmhead_check(h_target, w_target, B * (gamma + 1), V, d);
     if (rc) return rc;
     if (B == 0) return SPEC_OK;
@@ -1098,8 +1099,9 @@ int spec_verify_lmhead(const void* h_target, const void* w_target, const void* h
     size_t off = 0;
     auto take = [&](size_t bytes) { const size_t o = off; off = align_up(off + bytes, 256); return o; };
     char* ws = nullptr;
-    size_t o_Tt, o_tokt, o_partt, o_xt, o_Zt, o_pt, o_Td, o_tokd, o_partd, o_xd, o_Zd, o_qd, o_ht, o_hd,
-        o_lt, o_ld, o_seq, o_race, o_tick;
+    size_t o_Tt, o_tokt, o_partt, o_xt, o_Zt, o_pt, o_Td, o_tokd, o_partd, o_xd, o_Zd, o_qd, o_bm, o_seq,
+        o_race, o_tick;
+    const int nbm = lm_block_stride(V);
     {
         std::lock_guard<std::mutex> lock(g_mu);
         rc = device_state(&dev);
@@ -1117,10 +1119,7 @@ int spec_verify_lmhead(const void* h_target, const void* w_target, const void* h
         o_xd = take(rows_d * sizeof(float) + 4);
         o_Zd = take(rows_d * sizeof(float) + 4);
         o_qd = take(rows_d * sizeof(float) + 4);
-        o_ht = take(static_cast<size_t>(B) * d * 2);
-        o_hd = take(static_cast<size_t>(B) * d * 2);
-        o_lt = take(static_cast<size_t>(B) * V * sizeof(float));
-        o_ld = take(static_cast<size_t>(B) * V * sizeof(float));  // (unused when gamma = 0)
+        o_bm = take(static_cast<size_t>(rows_t) * nbm * sizeof(uint16_t));  // target rows' block maxima
         o_seq = take(static_cast<size_t>(B) * sizeof(SeqInfo));
         o_race = take(static_cast<size_t>(B) * race_slots(rpieces) * sizeof(RacePart));
         o_tick = take(static_cast<size_t>(B) * sizeof(int));
@@ -1141,8 +1140,6 @@ int spec_verify_lmhead(const void* h_target, const void* w_target, const void* h
     q.logp_t = reinterpret_cast<float*>(ws + o_pt);
     q.logZ_d = reinterpret_cast<float*>(ws + o_Zd);
     q.logq_d = reinterpret_cast<float*>(ws + o_qd);
-    q.h_race_t = reinterpret_cast<uint16_t*>(ws + o_ht);
-    q.h_race_d = reinterpret_cast<uint16_t*>(ws + o_hd);
     q.seq = reinterpret_cast<SeqInfo*>(ws + o_seq);
     q.T = T;
     q.Td = T_d;
@@ -1164,7 +1161,8 @@ int spec_verify_lmhead(const void* h_target, const void* w_target, const void* h
         cudaMemsetAsync(ws + o_tick, 0, static_cast<size_t>(B) * sizeof(int), s) != cudaSuccess)
         return SPEC_ECUDA;
     // row statistics of the target rows (T_b) and the draft rows (Td_b), with the draft
-    // tokens, in one launch
+    // tokens and the target rows' block maxima, in one launch
+    ps.part[0].block_max = reinterpret_cast<uint16_t*>(ws + o_bm);
     ps.part[0].T_row = reinterpret_cast<float*>(ws + o_Tt);
     ps.part[0].token_row = reinterpret_cast<int32_t*>(ws + o_tokt);
     ps.part[0].stat_parts = reinterpret_cast<float2*>(ws + o_partt);
@@ -1183,17 +1181,6 @@ int spec_verify_lmhead(const void* h_target, const void* w_target, const void* h
                                                                      reinterpret_cast<float*>(ws + o_qd));
     record(opts, 1, s);
     lmhead_scan_kernel<<<(B * 32 + 255) / 256, 256, 0, s>>>(q);
-    // logits of the raced rows only (target row j; draft row j of the residuals), one launch
-    LmHeadParams pr{};
-    pr.V = V;
-    pr.d = d;
-    pr.part[0].rows = B;
-    pr.part[0].logits = reinterpret_cast<float*>(ws + o_lt);
-    pr.part[1].rows = gamma > 0 ? B : 0;
-    pr.part[1].logits = reinterpret_cast<float*>(ws + o_ld);
-    pr.status = q.status;
-    rc = launch_lmhead<true>(q.h_race_t, w_target, q.h_race_d, w_draft, pr, dev->sm_count, s);
-    if (rc) return rc;
     record(opts, 2, s);
     VerifyParams p{};
     p.B = B;
@@ -1209,14 +1196,30 @@ int spec_verify_lmhead(const void* h_target, const void* w_target, const void* h
     p.status = q.status;
     p.out_tokens = out_tokens;
     p.out_n = out_n_accepted;
-    int per_sm = blocks_per_sm(lmhead_race_kernel, kThreads, 0);
+    p.caps.out_tokens = static_cast<long long>(B) * (gamma + 1);
+    p.caps.race = static_cast<long long>(B) * race_slots(rpieces);
+    LmRaceParams lq{};
+    lq.h_target = static_cast<const uint16_t*>(h_target);
+    lq.h_draft = static_cast<const uint16_t*>(h_draft);
+    lq.w_target = static_cast<const uint16_t*>(w_target);
+    lq.w_draft = static_cast<const uint16_t*>(gamma > 0 ? w_draft : w_target);
+    lq.block_max = reinterpret_cast<const uint16_t*>(ws + o_bm);
+    lq.logp_t = q.logp_t;
+    lq.logq_d = q.logq_d;
+    lq.d = d;
+    lq.nbm = nbm;
+    const size_t race_smem = static_cast<size_t>(d) * 4;  // the two raced hidden states, bf16
+    if (race_smem > 48 * 1024 &&
+        cudaFuncSetAttribute(lmhead_race_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(race_smem)) != cudaSuccess)
+        return SPEC_ECUDA;
+    int per_sm = blocks_per_sm(lmhead_race_kernel, kThreads, race_smem);
     if (per_sm < 1) per_sm = 1;
     long long G = static_cast<long long>(dev->sm_count) * per_sm / B;
     if (G > rpieces) G = rpieces;
     if (G < 1) G = 1;
     p.rgroups = static_cast<int>(G);
-    lmhead_race_kernel<<<static_cast<unsigned>(B * G), kThreads, 0, s>>>(
-        p, reinterpret_cast<float*>(ws + o_lt), reinterpret_cast<float*>(ws + o_ld));
+    lmhead_race_kernel<<<static_cast<unsigned>(B * G), kThreads, race_smem, s>>>(p, lq);
     record(opts, 3, s);
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
 }

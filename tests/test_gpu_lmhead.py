@@ -158,13 +158,16 @@ def gemm_sensitive(orc, lt, et, ld, ed, tok, T, Td, seed, r):
 
 
 @pytest.mark.parametrize("B,gamma,V,d,T,Td", [(4, 3, 4096, 128, 1.0, 0.5), (8, 5, 10000, 256, 0.8, 0.4),
-                                               (3, 0, 2048, 64, 1.0, 1.0), (64, 8, 32000, 256, 1.0, 0.5)])
+                                               (3, 0, 2048, 64, 1.0, 1.0), (64, 8, 32000, 256, 1.0, 0.5),
+                                               (8, 4, 50257, 1024, 1.0, 0.6)])
 def test_verify_from_hidden_states_matches_oracle(sv, B, gamma, V, d, T, Td):
     """The verify from hidden states against the oracle run on logits computed on the host
     (fp64 products of the same bf16 inputs, rounded to fp32), independent of the library's
     GEMM.  Tokens and counts must match except in sequences where the GEMM's error bound
-    could move a decision (those must still be valid cycles); and, on the logits the tensor
-    cores compute, the fused path must give exactly the logits path's tokens."""
+    could move a decision (those must still be valid cycles); and the logits path run on the
+    tensor cores' logits must give the fused path's tokens outside those sequences (the fused
+    race scores its candidates with logits recomputed by dot products, equal to the GEMM's
+    within the same error bound)."""
     ht, wt, hd, wd = lmhead_workload(B, gamma, V, d, seed=B * 100 + V)
     dev = torch.device("cuda")
     Ht, Wt, Hd, Wd = (to_dev(a) for a in (ht, wt, hd, wd))
@@ -206,7 +209,8 @@ def test_verify_from_hidden_states_matches_oracle(sv, B, gamma, V, d, T, Td):
             np.testing.assert_array_equal(gt[b], r.tokens[b], err_msg=f"seed {seed} sequence {b}")
         tl, nl, _ = sv.spec_verify_ex(lt_gpu, ld_gpu, dtok, T, Td, seed)
         torch.cuda.synchronize()
-        np.testing.assert_array_equal(nl.cpu().numpy(), gn)
-        np.testing.assert_array_equal(tl.cpu().numpy(), gt)
+        ok = ~flagged
+        np.testing.assert_array_equal(nl.cpu().numpy()[ok], gn[ok])
+        np.testing.assert_array_equal(tl.cpu().numpy()[ok], gt[ok])
     # the bound is loose (worst-case accumulation error): most decisions still compare
     assert n_flagged <= max(2, 0.1 * n_seq), (n_flagged, n_seq)
