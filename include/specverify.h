@@ -155,6 +155,9 @@ typedef struct {
 
 #define SPEC_FLAG_FULL_READ 8u    /* spec_verify_host only: read every row (the default there
                                      is SPEC_FLAG_EARLY_EXIT) */
+#define SPEC_DEBUG_RACE_AGAIN 16u /* tests only, spec_verify_lmhead: the race starts from a score
+                                     above any winner, so every sequence is raced a second time
+                                     from nothing; the outputs must not change. */
 
 /* Zero every field and set dtype = SPEC_BF16. */
 void spec_verify_opts_init(spec_verify_opts *opts);
@@ -346,7 +349,8 @@ int spec_lmhead_row_stats(const void *hidden, const void *weight, int rows, int 
  * temperatures, seq_index_base, d_status and prof_events (before the first kernel, after
  * the statistics, after the scan, after the race) are honoured; the library's own
  * workspace is used (B (gamma + 1) ceil(V / 8) bf16 block maxima plus a few words
- * per row).  SPEC_EINVAL for bad sizes, NULL or misaligned pointers.
+ * per row).  Of opts->flags only SPEC_DEBUG_RACE_AGAIN is read.  SPEC_EINVAL for bad sizes,
+ * NULL or misaligned pointers.
  */
 int spec_verify_lmhead(const void *h_target, const void *w_target, const void *h_draft,
                        const void *w_draft, const int32_t *draft_tokens, int B, int gamma, int V,

@@ -9,7 +9,7 @@ from .specverify import (  # noqa: F401
     SpecVerifyOpts, load_library, spec_verify, spec_verify_check, spec_verify_ex,
     spec_verify_greedy, spec_verify_greedy_ex, spec_verify_noalloc, spec_verify_strerror,
     spec_verify_workspace_bytes, spec_row_entropy, spec_adaptive_k, spec_verify_tree, Tree,
-    spec_verify_host, SPEC_FLAG_FULL_READ, spec_lmhead_logits, spec_lmhead_row_stats,
+    spec_verify_host, SPEC_FLAG_FULL_READ, SPEC_DEBUG_RACE_AGAIN, spec_lmhead_logits, spec_lmhead_row_stats,
     spec_verify_lmhead, spec_philox4x32_10)
 from .vocab_parallel import (  # noqa: F401
     LibraryBackend, VocabShard, spec_vp_decide, spec_vp_finish, spec_vp_partials, spec_vp_race,

@@ -776,6 +776,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) row_argmax_kernel(VerifyPar
 // ----------------------------------------------------------------------------------------
 
 constexpr uint32_t kDebugNeverReady = 1u;  // early-exit race units never publish their winners (tests)
+constexpr uint32_t kDebugRaceAgain = 2u;   // the LM-head race starts above any winner (tests)
 constexpr unsigned long long kWaitLimitNs = 500000000ull;  // give up a wait after 0.5 s
 
 __device__ __forceinline__ unsigned long long global_time_ns() {

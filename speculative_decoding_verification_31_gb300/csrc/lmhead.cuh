@@ -754,7 +754,7 @@ __global__ void __launch_bounds__(256, SPECVERIFY_RACE_MINBLOCKS) lmhead_race_ke
     __syncthreads();
     const uint32_t bg = p.seq_base + static_cast<uint32_t>(b);
     const uint16_t* bm_row = q.block_max + (static_cast<long long>(b) * (p.gamma + 1) + si.j) * q.nbm;
-    const float guess = lm_race_guess(q, p, b, si.j);
+    const float guess = (p.debug_flags & kDebugRaceAgain) ? INFINITY : lm_race_guess(q, p, b, si.j);
     float best = -INFINITY, thr = guess;
     int best_idx = INT_MAX;
     lm_race_chunks(p, q, si, residual, bg, bm_row, hs_t, hs_d, q.w_target, q.w_draft, g * NW, G * NW, wib, lane,

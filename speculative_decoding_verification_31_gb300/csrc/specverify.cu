@@ -1198,6 +1198,7 @@ int spec_verify_lmhead(const void* h_target, const void* w_target, const void* h
     p.out_n = out_n_accepted;
     p.caps.out_tokens = static_cast<long long>(B) * (gamma + 1);
     p.caps.race = static_cast<long long>(B) * race_slots(rpieces);
+    p.debug_flags = (opts && (opts->flags & SPEC_DEBUG_RACE_AGAIN)) ? kDebugRaceAgain : 0u;
     LmRaceParams lq{};
     lq.h_target = static_cast<const uint16_t*>(h_target);
     lq.h_draft = static_cast<const uint16_t*>(h_draft);

@@ -21,7 +21,7 @@ SPEC_OK, SPEC_EINVAL, SPEC_ECUDA, SPEC_EBADTOKEN, SPEC_ETIMEOUT, SPEC_ENOMEM = r
 SPEC_ESCRATCH = 6
 SPEC_EINDEX = 7
 SPEC_NOALLOC_SCRATCH_BYTES = 8 << 20
-SPEC_DEBUG_NEVER_READY, SPEC_FLAG_EARLY_EXIT, SPEC_FLAG_FULL_READ = 2, 4, 8
+SPEC_DEBUG_NEVER_READY, SPEC_FLAG_EARLY_EXIT, SPEC_FLAG_FULL_READ, SPEC_DEBUG_RACE_AGAIN = 2, 4, 8, 16
 SPEC_F32, SPEC_BF16 = 0, 1
 
 EXPORTED = ("spec_verify", "spec_verify_greedy", "spec_verify_ex", "spec_verify_greedy_ex",
@@ -435,7 +435,8 @@ def spec_lmhead_row_stats(hidden, weight, T_row, token_row=None, stream=None):
 
 def spec_verify_lmhead(h_target, w_target, h_draft, w_draft, draft_tokens, T: float, T_d: float,
                        seed: int, out_tokens=None, out_n_accepted=None, *, T_per_seq=None,
-                       Td_per_seq=None, seq_index_base: int = 0, prof_events=None, stream=None):
+                       Td_per_seq=None, seq_index_base: int = 0, prof_events=None, flags: int = 0,
+                       stream=None):
     """Sampling verify from hidden states (see ``spec_verify_lmhead`` in the C header):
     h_target bf16 [B, gamma+1, d], w_target [V, d], h_draft [B, gamma, d], w_draft [V, d]."""
     if h_target.dim() != 3 or h_target.dtype != torch.bfloat16 or not h_target.is_contiguous():
@@ -453,7 +454,7 @@ def spec_verify_lmhead(h_target, w_target, h_draft, w_draft, draft_tokens, T: fl
     out_tokens, out_n_accepted = _outputs(h_target, B, g, out_tokens, out_n_accepted)
     T_per_seq = _check_temps(T_per_seq, B, dev, "T_per_seq")
     Td_per_seq = _check_temps(Td_per_seq, B, dev, "Td_per_seq")
-    o = _make_opts(SPEC_BF16, T_per_seq, Td_per_seq, seq_index_base, None, None, None, prof_events)
+    o = _make_opts(SPEC_BF16, T_per_seq, Td_per_seq, seq_index_base, None, None, None, prof_events, flags)
     rc = _call(dev, "spec_verify_lmhead",
         _ptr(h_target), _ptr(w_target), _ptr(h_draft) if g else None, _ptr(w_draft) if g else None,
         _ptr(draft_tokens) if g else None, B, g, V, d, float(T), float(T_d), int(seed) & (2**64 - 1),

@@ -7,6 +7,8 @@ so a logit carries an absolute error of a few times 2^-24 * sum |h_k w_k| (the t
 2e-5 * that sum + 1e-5); ln Z and ln p inherit the logits' error divided by T, plus the fp32
 softmax sum's own (allowed: 1e-4 absolute at these sizes).
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -214,3 +216,69 @@ def test_verify_from_hidden_states_matches_oracle(sv, B, gamma, V, d, T, Td):
         np.testing.assert_array_equal(tl.cpu().numpy()[ok], gt[ok])
     # the bound is loose (worst-case accumulation error): most decisions still compare
     assert n_flagged <= max(2, 0.1 * n_seq), (n_flagged, n_seq)
+
+
+@pytest.mark.parametrize("B,gamma,V,d,T,Td", [(64, 8, 32000, 256, 1.0, 0.5), (8, 4, 50257, 1024, 1.0, 0.6)])
+def test_race_again_gives_the_same_tokens(sv, B, gamma, V, d, T, Td):
+    """The race's starting score is a guess the winner almost always beats; when it does
+    not, the sequence is raced again from the best score found.  With the guess forced above
+    every winner, every sequence takes that path: the tokens must not change."""
+    ht, wt, hd, wd = lmhead_workload(B, gamma, V, d, seed=B * 100 + V + 1)
+    Ht, Wt, Hd, Wd = (to_dev(a) for a in (ht, wt, hd, wd))
+    ld = host_logits(hd.reshape(B * gamma, d), wd)[0].reshape(B, gamma, V)
+    rng = np.random.default_rng(11)
+    tok = torch.from_numpy(np.stack([workloads.draw_drafts(rng, ld[b], Td) for b in range(B)])
+                           .astype(np.int32)).to(Ht.device)
+    for seed in range(3):
+        t0, n0 = sv.spec_verify_lmhead(Ht, Wt, Hd, Wd, tok, T, Td, seed)
+        t1, n1 = sv.spec_verify_lmhead(Ht, Wt, Hd, Wd, tok, T, Td, seed, flags=sv.SPEC_DEBUG_RACE_AGAIN)
+        torch.cuda.synchronize()
+        assert sv.spec_verify_check() == sv.SPEC_OK
+        np.testing.assert_array_equal(n1.cpu().numpy(), n0.cpu().numpy())
+        np.testing.assert_array_equal(t1.cpu().numpy(), t0.cpu().numpy())
+
+
+N_LM_CASES = int(os.environ.get("SPECVERIFY_LM_FUZZ_CASES", "6"))
+
+
+@pytest.mark.parametrize("case", range(N_LM_CASES))
+def test_random_lmhead_shapes(sv, case):
+    """Seeded random shapes of the verify from hidden states (batch, draft length, odd and
+    even vocabularies, hidden sizes, temperatures) against the oracle on host fp64 logits,
+    outside the sequences the GEMM's error bound could move."""
+    rng = np.random.default_rng(31_000 + case)
+    B = int(rng.integers(1, 13))
+    gamma = int(rng.choice([0, 1, 3, 6]))
+    V = int(rng.integers(64, 40_000))
+    d = int(rng.choice([64, 128, 256, 512]))
+    T = float(rng.uniform(0.6, 1.5))
+    Td = float(T * rng.uniform(0.5, 1.0))
+    ht, wt, hd, wd = lmhead_workload(B, gamma, V, d, seed=case)
+    Ht, Wt, Hd, Wd = (to_dev(a) for a in (ht, wt, hd, wd))
+    lt, et = host_logits(ht.reshape(B * (gamma + 1), d), wt)
+    lt, et = lt.reshape(B, gamma + 1, V), et.reshape(B, gamma + 1, V)
+    if gamma:
+        ld, ed = host_logits(hd.reshape(B * gamma, d), wd)
+        ld, ed = ld.reshape(B, gamma, V), ed.reshape(B, gamma, V)
+    else:
+        ld, ed = np.zeros((B, 0, V), np.float32), np.zeros((B, 0, V))
+    tok = np.zeros((B, gamma), np.int32)
+    for b in range(B):
+        if gamma:
+            tok[b] = workloads.draw_drafts(rng, ld[b], Td)
+    orc = oracle.get()
+    seed = int(rng.integers(0, 1 << 31))
+    t, n = sv.spec_verify_lmhead(Ht, Wt, Hd if gamma else None, Wd if gamma else None,
+                                 torch.from_numpy(tok).to(Ht.device), T, Td, seed)
+    torch.cuda.synchronize()
+    assert sv.spec_verify_check() == sv.SPEC_OK
+    gt, gn = t.cpu().numpy(), n.cpu().numpy()
+    r = orc.verify(lt, ld, tok, np.full(B, T, np.float32), np.full(B, Td, np.float32), seed)
+    flagged = gemm_sensitive(orc, lt, et, ld, ed, tok, T, Td, seed, r)
+    for b in range(B):
+        j = int(gn[b])
+        assert 0 <= j <= gamma and 0 <= gt[b, j] < V and np.all(gt[b, j + 1:] == -1)
+        if flagged[b]:
+            continue
+        assert j == r.n_accepted[b], (case, b, j, r.n_accepted[b])
+        np.testing.assert_array_equal(gt[b], r.tokens[b], err_msg=f"case {case} sequence {b}")
