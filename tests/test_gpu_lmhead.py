@@ -161,7 +161,9 @@ def gemm_sensitive(orc, lt, et, ld, ed, tok, T, Td, seed, r):
 
 @pytest.mark.parametrize("B,gamma,V,d,T,Td", [(4, 3, 4096, 128, 1.0, 0.5), (8, 5, 10000, 256, 0.8, 0.4),
                                                (3, 0, 2048, 64, 1.0, 1.0), (64, 8, 32000, 256, 1.0, 0.5),
-                                               (8, 4, 50257, 1024, 1.0, 0.6)])
+                                               (8, 4, 50257, 1024, 1.0, 0.6),
+                                               # the race's hidden states need 64 KB of shared memory
+                                               (4, 2, 3001, 16384, 1.0, 0.8)])
 def test_verify_from_hidden_states_matches_oracle(sv, B, gamma, V, d, T, Td):
     """The verify from hidden states against the oracle run on logits computed on the host
     (fp64 products of the same bf16 inputs, rounded to fp32), independent of the library's
