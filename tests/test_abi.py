@@ -131,8 +131,9 @@ def test_host_validation_rejects_bad_sizes_without_a_device(lib):
     opts.dtype = 5
     assert lib.spec_verify_ex(fake, fake, fake, 1, 3, 10, 1.0, 1.0, 0, fake, fake,
                               ctypes.byref(opts), None) == EINVAL
-    # unknown flag bits (bit 0, once a schedule that was removed, included)
-    for bad in (1, 32, 1 << 31):
+    # unknown flag bits (bit 0, once a schedule that was removed, included; SPEC_DEBUG_RACE_AGAIN
+    # belongs to spec_verify_lmhead alone)
+    for bad in (1, sv.SPEC_DEBUG_RACE_AGAIN, 32, 1 << 31):
         opts.dtype = sv.SPEC_BF16
         opts.flags = bad
         assert lib.spec_verify_ex(fake, fake, fake, 1, 3, 10, 1.0, 1.0, 0, fake, fake,
