@@ -134,3 +134,29 @@ def test_checked_build_token_trees(sv):
             for x, y in zip(a, b):
                 np.testing.assert_array_equal(x, y)
 
+
+
+def test_checked_build_verify_from_hidden_states(sv):
+    """The verify from hidden states through the index-checked build (its race publishes
+    each block's winner through the checked slot index): the status word stays clear and
+    the tokens equal the normal build's, including the forced second race."""
+    from test_gpu_lmhead import host_logits, lmhead_workload, to_dev
+    B, gamma, V, d = 6, 4, 10001, 256
+    ht, wt, hd, wd = lmhead_workload(B, gamma, V, d, seed=5)
+    Ht, Wt, Hd, Wd = (to_dev(a) for a in (ht, wt, hd, wd))
+    ld = host_logits(hd.reshape(B * gamma, d), wd)[0].reshape(B, gamma, V)
+    rng = np.random.default_rng(3)
+    tok = torch.from_numpy(np.stack([workloads.draw_drafts(rng, ld[b], 0.6) for b in range(B)])
+                           .astype(np.int32)).to(Ht.device)
+    got = []
+    for path in (sv.specverify.CHECKED_LIB_PATH, sv.specverify.LIB_PATH):
+        sv.specverify.use_library(path)
+        for flags in (0, sv.SPEC_DEBUG_RACE_AGAIN):
+            t, n = sv.spec_verify_lmhead(Ht, Wt, Hd, Wd, tok, 0.9, 0.6, 17, flags=flags)
+            torch.cuda.synchronize()
+            assert sv.spec_verify_check() == sv.SPEC_OK, (path, flags)
+            got.append((t.cpu().numpy(), n.cpu().numpy()))
+    sv.specverify.use_library(sv.specverify.CHECKED_LIB_PATH)
+    for t, n in got[1:]:
+        np.testing.assert_array_equal(n, got[0][1])
+        np.testing.assert_array_equal(t, got[0][0])
