@@ -2,11 +2,8 @@
 // row statistics as its epilogue.
 //
 // Logits are L = H W^T: hidden states H [rows, d] and head weights W [V, d], both bf16 and
-// row-major (so both operands are K-major), accumulated in fp32.  The output tiles (128 rows
-// x 256 vocabulary entries) are dealt to a persistent grid of one CTA per SM in vocabulary-
-// major order, tile u to CTA u mod grid, so that at any moment the CTAs work on a few
-// neighbouring head tiles (each read from HBM once, then served from L2 to every row tile)
-// and every SM gets the same number of tiles to within one.  Per tile a CTA streams K in
+// row-major (so both operands are K-major), accumulated in fp32.  A CTA owns one tile of
+// 128 rows and a contiguous run of 256-wide vocabulary tiles; per tile it streams K in
 // 64-element slices:
 //   warp 0     one elected thread issues TMA loads (cp.async.bulk.tensor, 128-byte swizzle)
 //              of the A and B slices into a 4-stage shared-memory ring;
@@ -136,18 +133,17 @@ struct LmHeadPart {
                                   // each 8-token block, rounded up (statistics epilogue), or nullptr
     const float* T_row;           // [rows] temperature of each row (statistics epilogue)
     const int32_t* token_row;     // [rows] token whose logit to keep (-1: none), or nullptr
-    float2* stat_parts;           // [rows][n_tiles] (scaled max, sum) in base 2 per vocabulary tile
+    float2* stat_parts;           // [rows][nchunks] (scaled max, sum) in base 2
     float* token_logit;           // [rows] logit at token_row (raw, before 1/T)
 };
 
 // A launch computes up to two products with the same V and d (the target rows against the
-// target head and the draft rows against the draft head): row tiles [0, m_tiles0) are part
-// 0's, the rest part 1's, so both share one persistent grid.  Output tile u is vocabulary
-// tile u / m_tiles of row tile u % m_tiles.
+// target head and the draft rows against the draft head): grid rows [0, m_tiles0) are
+// part 0's row tiles, the rest part 1's, so both share one wave of CTAs.
 struct LmHeadParams {
     int V, d;
-    int n_tiles;                  // vocabulary tiles: ceil(V / kGemmBN)
-    int m_tiles;                  // row tiles of both parts
+    int tiles_per_cta;            // vocabulary tiles of one CTA (its chunk)
+    int nchunks;                  // chunks per row: ceil(V / (kGemmBN * tiles_per_cta))
     int m_tiles0;                 // row tiles of part 0
     LmHeadPart part[2];
     int32_t* status;
@@ -208,19 +204,16 @@ lmhead_kernel(const __grid_constant__ CUtensorMap map_h0, const __grid_constant_
     float* stage_out = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 256);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // this CTA's output tiles: u = blockIdx.x + t gridDim.x for t < ntiles
-    const int units = p.n_tiles * p.m_tiles;
-    const int ntiles = static_cast<int>(blockIdx.x) < units
-                           ? (units - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
-                           : 0;
-    // tile t: part (0 or 1), its row tile within the part, its first vocabulary entry
-    auto tile_of = [&](int t, int& pidx, int& m_tile, int& n_tile) {
-        const int u = static_cast<int>(blockIdx.x) + t * static_cast<int>(gridDim.x);
-        n_tile = u / p.m_tiles;
-        const int mt = u - n_tile * p.m_tiles;
-        pidx = mt >= p.m_tiles0 ? 1 : 0;
-        m_tile = pidx ? mt - p.m_tiles0 : mt;
-    };
+    const bool second = static_cast<int>(blockIdx.y) >= p.m_tiles0;
+    const LmHeadPart& part = p.part[second ? 1 : 0];
+    const CUtensorMap* map_h = second ? &map_h1 : &map_h0;
+    const CUtensorMap* map_w = second ? &map_w1 : &map_w0;
+    const int m_tile = second ? static_cast<int>(blockIdx.y) - p.m_tiles0 : static_cast<int>(blockIdx.y);
+    const int chunk = blockIdx.x;
+    const int n_tiles_total = (p.V + kGemmBN - 1) / kGemmBN;
+    const int t_begin = chunk * p.tiles_per_cta;
+    const int t_end = min(n_tiles_total, t_begin + p.tiles_per_cta);
+    const int ntiles = max(0, t_end - t_begin);
     const int kb_count = p.d / kGemmBK;
 
     if (threadIdx.x == 0) {
@@ -255,11 +248,7 @@ lmhead_kernel(const __grid_constant__ CUtensorMap map_h0, const __grid_constant_
             uint32_t phase = 0;
             int issued = 0;
             for (int t = 0; t < ntiles && !*abort; ++t) {
-                int pidx, m_tile, n_tile;
-                tile_of(t, pidx, m_tile, n_tile);
-                const CUtensorMap* map_h = pidx ? &map_h1 : &map_h0;
-                const CUtensorMap* map_w = pidx ? &map_w1 : &map_w0;
-                const int n0 = n_tile * kGemmBN;
+                const int n0 = (t_begin + t) * kGemmBN;
                 for (int kb = 0; kb < kb_count; ++kb) {
                     if (!mbar_wait(empty + stage, phase ^ 1u, abort)) {
                         *abort = 1;
@@ -332,29 +321,27 @@ lmhead_kernel(const __grid_constant__ CUtensorMap map_h0, const __grid_constant_
     } else {
         // ---- epilogue: warps 2..5, TMEM lane slice (warp % 4) * 32 ----
         const int slice = warp & 3;
+        const int row = m_tile * kGemmBM + slice * 32 + lane;
+        const bool row_ok = row < part.rows;
+        float c = 1.0f;
+        int tok = -1;
+        if (!kLogits && row_ok) {
+            c = kLog2e / part.T_row[row];
+            if (part.token_row) tok = part.token_row[row];
+        }
+        // logits output (logits epilogue): staged and written row by row where the rows are
+        // 16-byte aligned
+        float* const lout = kLogits ? part.logits : nullptr;
+        const bool staged = lout && p.V % 4 == 0 && (reinterpret_cast<uintptr_t>(lout) & 15u) == 0;
         float* const stg = stage_out + slice * 32 * kStageStride;
+        const int row0 = m_tile * kGemmBM + slice * 32;
+        uint16_t* const bmrow = (!kLogits && row_ok && part.block_max)
+                                    ? part.block_max + static_cast<long long>(row) * lm_block_stride(p.V)
+                                    : nullptr;
+        float m = -FLT_MAX, s = 0.0f, xtok = 0.0f;
         for (int t = 0; t < ntiles; ++t) {
             const int acc = t & 1;
             const uint32_t acc_phase = (t >> 1) & 1u;
-            int pidx, m_tile, n_tile;
-            tile_of(t, pidx, m_tile, n_tile);
-            const LmHeadPart& pt = p.part[pidx];
-            const int row0 = m_tile * kGemmBM + slice * 32;
-            const int row = row0 + lane;
-            const bool row_ok = row < pt.rows;
-            float c = 1.0f;
-            int tok = -1;
-            if (!kLogits && row_ok) {
-                c = kLog2e / pt.T_row[row];
-                if (pt.token_row) tok = pt.token_row[row];
-            }
-            // logits output (logits epilogue): staged and written row by row where the rows
-            // are 16-byte aligned
-            float* const lout = kLogits ? pt.logits : nullptr;
-            const bool staged = lout && p.V % 4 == 0 && (reinterpret_cast<uintptr_t>(lout) & 15u) == 0;
-            uint16_t* const bmrow = (!kLogits && row_ok && pt.block_max)
-                                        ? pt.block_max + static_cast<long long>(row) * lm_block_stride(p.V)
-                                        : nullptr;
             // lane 0 waits (bounded) and the warp follows it, so that the warp stays converged
             // for the .sync.aligned TMEM loads; then every lane observes the completed phase
             int ok = 0;
@@ -368,8 +355,7 @@ lmhead_kernel(const __grid_constant__ CUtensorMap map_h0, const __grid_constant_
             mbar_wait(tfull + acc, acc_phase, &never);  // completed: returns at once
             __syncwarp();
             tmem_fence_after();
-            const int n0 = n_tile * kGemmBN;
-            float m = -FLT_MAX, s = 0.0f, xtok = 0.0f;
+            const int n0 = (t_begin + t) * kGemmBN;
 #pragma unroll 1
             for (int c32 = 0; c32 < kGemmBN / 32; ++c32) {
                 float v[32];
@@ -388,7 +374,7 @@ lmhead_kernel(const __grid_constant__ CUtensorMap map_h0, const __grid_constant_
 #pragma unroll
                         for (int r0 = 0; r0 < 32; r0 += 4) {
                             const int r = r0 + (lane >> 3);
-                            if (row0 + r < pt.rows)  // streaming stores: keep the heads' tiles in L2
+                            if (row0 + r < part.rows)  // streaming stores: keep the heads' tiles in L2
                                 __stcs(reinterpret_cast<float4*>(lout + static_cast<long long>(row0 + r) * p.V + col0 + cq),
                                        *reinterpret_cast<const float4*>(stg + r * kStageStride + cq));
                         }
@@ -415,11 +401,11 @@ lmhead_kernel(const __grid_constant__ CUtensorMap map_h0, const __grid_constant_
                         *reinterpret_cast<uint2*>(bmrow + (col0 >> 3)) = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
                     }
                     const float mn = fmaxf(m, fmaxf(bmax * c, -FLT_MAX));
-                    float sum = 0.0f;
+                    float part = 0.0f;
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
-                        if (col0 + i < p.V) sum += ex2_fast(fmaf(v[i], c, -mn));
-                    s = fmaf(s, ex2_fast(m - mn), sum);
+                        if (col0 + i < p.V) part += ex2_fast(fmaf(v[i], c, -mn));
+                    s = fmaf(s, ex2_fast(m - mn), part);
                     m = mn;
                     if (tok >= col0 && tok < col0 + 32) {
 #pragma unroll
@@ -431,10 +417,11 @@ lmhead_kernel(const __grid_constant__ CUtensorMap map_h0, const __grid_constant_
             tmem_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty + acc);
-            if (!kLogits && row_ok) {  // this tile's partial, and the token's logit if it is here
-                store_stat(pt.stat_parts + static_cast<long long>(row) * p.n_tiles + n_tile, m, s);
-                if (tok >= n0 && tok < n0 + kGemmBN && tok < p.V && pt.token_logit) pt.token_logit[row] = xtok;
-            }
+        }
+        if (!kLogits && row_ok && !*abort) {
+            store_stat(part.stat_parts + static_cast<long long>(row) * p.nchunks + chunk, m, s);
+            if (tok >= t_begin * kGemmBN && tok < t_end * kGemmBN && tok < p.V && part.token_logit)
+                part.token_logit[row] = xtok;
         }
         if (*abort && lane == 0) set_status(p.status, 4 /* SPEC_ETIMEOUT */);
     }

@@ -920,16 +920,20 @@ int lmhead_check(const void* H, const void* W, int rows, int V, int d) {
     return SPEC_OK;
 }
 
-// Grid of the LM-head kernel: one CTA per SM (each holds 512 TMEM columns and 211 KB of
-// shared memory), or one per output tile when there are fewer tiles; the kernel deals the
-// tiles to them in vocabulary-major order.
+// Grid of the LM-head kernel: one grid row per row tile (of both parts), the vocabulary
+// tiles split into chunks so that the CTAs fill the GPU about once (one CTA per SM: each
+// holds 512 TMEM columns and 193 KB of shared memory).  The CTAs of one chunk sweep the same
+// head tiles in step, so each head is read from HBM about once.
 void lmhead_grid(int rows0, int rows1, int V, int sm_count, LmHeadParams& lp, dim3& grid) {
     const int m0 = (rows0 + kGemmBM - 1) / kGemmBM, m1 = (rows1 + kGemmBM - 1) / kGemmBM;
-    lp.n_tiles = (V + kGemmBN - 1) / kGemmBN;
-    lp.m_tiles = m0 + m1;
+    const int n_tiles = (V + kGemmBN - 1) / kGemmBN;
+    long long want = sm_count / std::max(1, m0 + m1);  // chunks per row tile
+    if (want < 1) want = 1;
+    if (want > n_tiles) want = n_tiles;
+    lp.tiles_per_cta = static_cast<int>((n_tiles + want - 1) / want);
+    lp.nchunks = (n_tiles + lp.tiles_per_cta - 1) / lp.tiles_per_cta;
     lp.m_tiles0 = m0;
-    const long long units = static_cast<long long>(lp.n_tiles) * lp.m_tiles;
-    grid = dim3(static_cast<unsigned>(std::max(1LL, std::min<long long>(sm_count, units))));
+    grid = dim3(static_cast<unsigned>(lp.nchunks), static_cast<unsigned>(m0 + m1));
 }
 
 // Launch part 0 = (H0, W0) and, if lp.part[1].rows > 0, part 1 = (H1, W1) in one grid.
@@ -999,7 +1003,7 @@ int spec_lmhead_logits(const void* hidden, const void* weight, int rows, int V, 
 
 namespace {
 
-// Merge each row's per-tile partials: ln Z = (m + log2 s) ln 2 and, when a token is given,
+// Merge each row's chunk partials: ln Z = (m + log2 s) ln 2 and, when a token is given,
 // ln p(token) = x_token / T - ln Z.  One warp per row.
 __global__ void __launch_bounds__(256) lmhead_merge_kernel(LmHeadParams p, float* out_logZ,
                                                            float* out_logp_token) {
@@ -1007,8 +1011,8 @@ __global__ void __launch_bounds__(256) lmhead_merge_kernel(LmHeadParams p, float
     const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (row >= p.rows) return;
     SoftmaxStat st{-FLT_MAX, 0.0f};
-    for (int k = lane; k < p.n_tiles; k += 32) {
-        const float2 q = p.stat_parts[static_cast<long long>(row) * p.n_tiles + k];
+    for (int k = lane; k < p.nchunks; k += 32) {
+        const float2 q = p.stat_parts[static_cast<long long>(row) * p.nchunks + k];
         st = merge_stat(st, SoftmaxStat{q.x, q.y});
     }
     st = warp_merge_stat(st);
@@ -1045,8 +1049,8 @@ int spec_lmhead_row_stats(const void* hidden, const void* weight, int rows, int 
         rc = device_state(&dev);
         if (rc) return rc;
         lmhead_grid(rows, 0, V, dev->sm_count, lp, grid);
-        // workspace: [rows][n_tiles] partials, then [rows] token logits
-        const size_t need = align_up(static_cast<size_t>(rows) * lp.n_tiles * sizeof(float2), 256) +
+        // workspace: [rows][nchunks] partials, then [rows] token logits
+        const size_t need = align_up(static_cast<size_t>(rows) * lp.nchunks * sizeof(float2), 256) +
                             align_up(static_cast<size_t>(rows) * sizeof(float), 256);
         rc = ensure_workspace(*dev, need);
         if (rc) return rc;
@@ -1056,7 +1060,7 @@ int spec_lmhead_row_stats(const void* hidden, const void* weight, int rows, int 
     lp.part[0].token_row = token_row;
     lp.part[0].stat_parts = reinterpret_cast<float2*>(ws);
     lp.part[0].token_logit = reinterpret_cast<float*>(
-        ws + align_up(static_cast<size_t>(rows) * lp.n_tiles * sizeof(float2), 256));
+        ws + align_up(static_cast<size_t>(rows) * lp.nchunks * sizeof(float2), 256));
     lp.status = dev->status;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     rc = launch_lmhead<false>(hidden, weight, nullptr, nullptr, lp, dev->sm_count, s);
@@ -1105,13 +1109,13 @@ int spec_verify_lmhead(const void* h_target, const void* w_target, const void* h
         lmhead_grid(rows_t, rows_d, V, dev->sm_count, ps, grid_s);
         o_Tt = take(rows_t * sizeof(float));
         o_tokt = take(rows_t * sizeof(int32_t));
-        o_partt = take(static_cast<size_t>(rows_t) * ps.n_tiles * sizeof(float2));
+        o_partt = take(static_cast<size_t>(rows_t) * ps.nchunks * sizeof(float2));
         o_xt = take(rows_t * sizeof(float));
         o_Zt = take(rows_t * sizeof(float));
         o_pt = take(rows_t * sizeof(float));
         o_Td = take(rows_d * sizeof(float) + 4);
         o_tokd = take(rows_d * sizeof(int32_t) + 4);
-        o_partd = take(static_cast<size_t>(rows_d) * ps.n_tiles * sizeof(float2) + 8);
+        o_partd = take(static_cast<size_t>(rows_d) * ps.nchunks * sizeof(float2) + 8);
         o_xd = take(rows_d * sizeof(float) + 4);
         o_Zd = take(rows_d * sizeof(float) + 4);
         o_qd = take(rows_d * sizeof(float) + 4);
