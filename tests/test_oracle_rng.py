@@ -4,6 +4,7 @@
   (``triton.language.philox_impl``), run by Triton's CPU interpreter in a child process.
 * Uniformity of the acceptance uniforms (chi-square over 2^16 buckets) and their 24-bit
   grid; the race exponentials against Exp(1) (Kolmogorov-Smirnov) and their mean.
+* The race's winning score minus the log of the total weight against the standard Gumbel law.
 """
 import json
 import os
@@ -139,3 +140,28 @@ def test_race_exponential_word_layout():
     for i in [0, 1, 47]:
         w = orc.philox(np.array([0, i, b, 0], np.uint32), key)[0]
         assert orc.accept_uniform(seed, b, i) == (int(w) >> 8) / 2**24
+
+
+def test_race_winner_score_is_gumbel_shifted_by_the_log_total_weight():
+    """The verify from hidden states starts each race from ln N - 2 (N the total weight) and
+    races again when the winner falls below it; that start is cheap only if the winning
+    score max_x ln w(x) - ln E_x is ln N plus a standard Gumbel variable, as the race's
+    exponentials make it.  Over many independent races of one weight vector: the winning
+    scores minus ln N follow the standard Gumbel law (Kolmogorov-Smirnov), and the share
+    below -2 is exp(-e^2) < 7e-4 within binomial error."""
+    orc = oracle.get()
+    rng = np.random.default_rng(0)
+    V = 512
+    w = rng.gamma(0.3, size=V)
+    w[rng.random(V) < 0.2] = 0.0  # zero weights take no part
+    lnN = np.log(w.sum())
+    with np.errstate(divide="ignore"):
+        lw = np.log(w)
+    n = 20_000
+    g = np.empty(n)
+    for k in range(n):  # race k: sequence k of seed 11, row 3
+        g[k] = np.max(lw - np.log(orc.race_exponentials(11, k, 3, V))) - lnN
+    assert stats.kstest(g, stats.gumbel_r.cdf).pvalue > 1e-3
+    p = np.exp(-np.exp(2.0))
+    low = int((g < -2.0).sum())
+    assert abs(low - n * p) < 5 * np.sqrt(n * p * (1 - p)) + 1, (low, n * p)
